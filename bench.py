@@ -1,0 +1,454 @@
+"""SGEMM benchmark: TFLOP/s (2MNK / time) and fraction of the per-shape roofline.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--algo auto|ffma|tf32x3] [--shapes-out FILE]
+
+One step is one C = alpha*A*B + beta*C call on the workload (default
+square5120: M=N=K=5120, alpha=1, beta=0.5, the size of the overview table of
+"NVIDIA_SGEMM_PRACTICE"), inputs resident in HBM.  Inputs (315 MB) exceed the
+129 MB L2, so no flush is needed between steps.  Rank 0 prints one JSON line.
+
+  value     device time of K back-to-back steps, CUDA events on the launch
+            stream, max over ranks; whole-job TFLOP/s = N * 2MNK * K / time
+  e2e       the same metric through sgemm_host() (host buffers, pinned): per
+            step host->device copies of A, B, C, the GEMM, device->host C
+  roofline  the GEMM kernel's 2MNK per launch / mean launch time (CUDA events
+            around each launch in the timed region) against the path's peak
+  cpu_baseline  the float64 oracle on a bounded row sample, host cores
+--impl reference times the oracle alone (the pages publish no GPU code to
+run here), same workload and metric.
+Multi-GPU (torchrun): independent replicas, one per GPU ("scaling": "weak").
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import signal
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "SGEMM TFLOP/s (2MNK/time) and % of per-shape roofline, 1×GB300"
+UNIT = "TFLOP/s"
+# The pages' own number for this metric and size: "NVIDIA_SGEMM_PRACTICE"
+# overview table, kernel_7 (double-buffered prefetch), 5120^3, RTX 3090.
+PAGES_5120_TFLOPS = 13.63498
+# nominal dense tensor rates (per GPU): tf32 1.1 PFLOP/s, bf16 2.25 PFLOP/s
+TF32_OVER_BF16 = 1.1 / 2.25
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                  "sm_max_mhz": 2070.0}
+KERNEL_SOURCES = ["dense_fp32_matrix_05_gb300/csrc/tf32x3_gemm.cuh",
+                  "dense_fp32_matrix_05_gb300/csrc/ffma_gemm.cuh",
+                  "dense_fp32_matrix_05_gb300/csrc/common.cuh",
+                  "dense_fp32_matrix_05_gb300/csrc/ptx.cuh"]
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str, path_name: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel sources (the summary records their hash)."""
+    fn = os.path.join(ROOT, "profiles", f"{path_name}_{workload}.md")
+    if not os.path.exists(fn):
+        return None
+    text = open(fn).read()
+    m_hash = re.search(r"kernel_source_hash:\s*([0-9a-f]+)", text)
+    m_bytes = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not m_hash or not m_bytes or m_hash.group(1) != kernel_source_hash():
+        return None
+    return float(m_bytes.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            import tempfile
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL, start_new_session=True)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            try:
+                os.killpg(self.proc.pid, signal.SIGTERM)
+            except Exception:
+                self.proc.terminate()
+            self.proc.wait(timeout=10)
+
+    def summary(self):
+        if not self.path or not os.path.exists(self.path):
+            return None
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, flags in rows for i, v in enumerate(flags)
+                          if v.lower() == "active"})
+        return {"sm_mhz": float(np.median([r[0] for r in rows])), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+def roofline_peak(path: int, peaks: dict, source: str, sms: int):
+    """(bound, peak TFLOP/s, basis text) for a path."""
+    import dense_fp32_matrix_05_gb300 as pkg
+    if path == pkg.SGEMM_ALGO_TF32X3:
+        tf32 = peaks["bf16_tflops"] * TF32_OVER_BF16
+        return ("tensor", tf32 / 3.0,
+                f"3xTF32 fp32-accurate tensor peak = {source} bf16 burst {peaks['bf16_tflops']} TF/s "
+                f"x (tf32 1.1 / bf16 2.25 nominal) / 3 MMAs per fp32 product "
+                f"(raw tf32 peak {tf32:.1f} TF/s)")
+    mhz = peaks.get("sm_max_mhz", 2070.0)
+    peak = sms * 128 * 2 * mhz * 1e6 / 1e12
+    return ("alu", peak, f"FFMA peak = {sms} SMs x 128 fp32 lanes x 2 flop x {mhz} MHz ({source} max clock)")
+
+
+def run_ours(args, rank: int, world: int, local_rank: int):
+    import torch
+
+    import dense_fp32_matrix_05_gb300 as pkg
+    from dense_fp32_matrix_05_gb300.workloads import WORKLOADS, make_problem
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    from dense_fp32_matrix_05_gb300 import _build_ext
+    _build_ext.build()
+    pkg.library()
+    w = WORKLOADS[args.workload]
+    algo = {"auto": 0, "ffma": 1, "tf32x3": 2}[args.algo]
+    p = make_problem(w, pad_value=0.0)
+    A = torch.from_numpy(p.A).to(dev)
+    B = torch.from_numpy(p.B).to(dev)
+    C = torch.from_numpy(p.C).to(dev)
+    stream = torch.cuda.current_stream(dev)
+    props = torch.cuda.get_device_properties(dev)
+    plan = pkg.sgemm_plan_info(p.M, p.N, p.K, A.data_ptr(), p.lda, B.data_ptr(), p.ldb,
+                               C.data_ptr(), p.ldc, algo=algo, num_sms=props.multi_processor_count)
+    flops = 2.0 * p.M * p.N * p.K
+
+    def step():
+        rc = pkg.sgemm_ex(p.M, p.N, p.K, p.alpha, A, p.lda, B, p.ldb, p.beta, C, p.ldc, stream, algo, 0, 0)
+        if rc != 0:
+            raise pkg.SgemmError("sgemm_ex", rc)
+
+    for _ in range(args.warmup):
+        step()
+    st = pkg.sgemm_check_status(stream)
+    if st != 0:
+        raise pkg.SgemmError("warmup", st)
+
+    dist = world > 1
+    if dist:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank) as clk:
+        t0.record(stream)
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        t1.record(stream)
+        torch.cuda.synchronize()
+    if dist:
+        torch.distributed.barrier()
+    total_ms = t0.elapsed_time(t1)
+    launch_ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
+    st = pkg.sgemm_check_status(stream)
+    if st != 0:
+        raise pkg.SgemmError("timed region", st)
+    if dist:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    clocks = clk.summary()
+
+    # ---------------------------------------------------------- e2e
+    e2e_steps = max(1, min(args.steps, args.e2e_steps))
+    hA = torch.from_numpy(p.A).pin_memory()
+    hB = torch.from_numpy(p.B).pin_memory()
+    hC = torch.from_numpy(p.C.copy()).pin_memory()
+
+    def host_step():
+        rc = pkg.sgemm_host(p.M, p.N, p.K, p.alpha, hA.data_ptr(), p.lda, hB.data_ptr(), p.ldb,
+                            p.beta, hC.data_ptr(), p.ldc, algo)
+        if rc != 0:
+            raise pkg.SgemmError("sgemm_host", rc)
+
+    for _ in range(min(3, args.warmup)):
+        host_step()
+    torch.cuda.synchronize()
+    if dist:
+        torch.distributed.barrier()
+    h0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        host_step()
+    e2e_s = time.perf_counter() - h0
+    if dist:
+        t = torch.tensor([e2e_s], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    h2d = 4 * (p.A.size + p.B.size + (p.C.size if p.beta != 0 else 0))
+    d2h = 4 * p.C.size
+
+    # ---------------------------------------------------------- context: cuBLAS SGEMM
+    cublas = None
+    if args.cublas and rank == 0:
+        torch.backends.cuda.matmul.allow_tf32 = False
+        a2 = A[:, :p.K]
+        b2 = B[:, :p.N]
+        out = torch.empty((p.M, p.N), device=dev)
+        for _ in range(3):
+            torch.matmul(a2, b2, out=out)
+        torch.cuda.synchronize()
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n = max(3, min(args.steps, 50))
+        c0.record()
+        for _ in range(n):
+            torch.matmul(a2, b2, out=out)
+        c1.record()
+        torch.cuda.synchronize()
+        cublas = flops * n / (c0.elapsed_time(c1) * 1e-3) / 1e12
+
+    peaks, peak_src = load_peaks()
+    bound, peak, basis = roofline_peak(plan["path"], peaks, peak_src, props.multi_processor_count)
+    achieved = flops / (launch_ms * 1e-3) / 1e12
+    path_name = {1: "ffma", 2: "tf32x3"}[plan["path"]]
+    traffic = recorded_traffic(args.workload, path_name)
+    value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
+
+    result = {
+        "metric": METRIC,
+        "value": round(value, 3),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(total_ms / args.steps, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": round(value / PAGES_5120_TFLOPS, 3) if args.workload == "square5120" else None,
+        "vs_baseline_ref": "NVIDIA_SGEMM_PRACTICE overview table, kernel_7, 5120^3, RTX 3090, 13634.98 GFLOPS",
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {
+            "workload": f"{w.name}: M={p.M} N={p.N} K={p.K} fp32 row-major, {w.note}",
+            "algo": f"{args.algo} -> {path_name}",
+            "tile": f"{plan['tile_m']}x{plan['tile_n']}", "splits": plan["splits"],
+            "grid": plan["grid"], "stages": plan["stages"],
+            "l2": f"no flush: inputs larger than L2 ({w.compulsory_bytes / 1e6:.0f} MB vs 129 MB)"
+                  if w.compulsory_bytes > 130e6 else "L2-resident inputs (small workload)",
+            "parallelism": f"replicas x{world}",
+        },
+        "roofline": {"bound": bound, "achieved": round(achieved, 3), "peak": round(peak, 3),
+                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "peak_basis": basis, "kernel": f"{path_name}_gemm_kernel",
+                     "launch_ms": round(launch_ms, 5),
+                     "compulsory_bytes": w.compulsory_bytes,
+                     "hbm_frac_of_measured": round(w.compulsory_bytes / (launch_ms * 1e-3) /
+                                                   (peaks["hbm_gbs"] * 1e9), 4)},
+        "e2e": {"value": round(world * flops * e2e_steps / e2e_s / 1e12, 3), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                "api": "sgemm_host (pinned host buffers)"},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    if cublas is not None:
+        result["context_cublas_sgemm_tflops"] = round(cublas, 3)
+    return result, p
+
+
+def oracle_sample_rate(p, target_s: float, threads: int = 0):
+    """Time the oracle on a bounded row sample; returns (TFLOP/s, rows, seconds)."""
+    import oracle
+    oracle.build()
+    rows = 1
+    while True:
+        sel = np.linspace(0, p.M - 1, rows).astype(np.int64).tolist()
+        t = time.perf_counter()
+        oracle.sgemm_ref(p.M, p.N, p.K, p.alpha, p.A, p.lda, p.B, p.ldb, p.beta,
+                         p.C if p.beta != 0 else None, p.ldc, rows=sel, threads=threads)
+        dt = time.perf_counter() - t
+        if dt >= target_s or rows >= p.M:
+            return 2.0 * rows * p.N * p.K / dt / 1e12, rows, dt
+        rows = min(p.M, max(rows + 1, int(rows * min(8.0, 1.3 * target_s / max(dt, 1e-3)))))
+
+
+def cpu_baseline(p, target_s: float):
+    import oracle
+    v, rows, dt = oracle_sample_rate(p, target_s)
+    return {"value": v, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": f"{rows} of {p.M} output rows x all {p.N} columns, K={p.K}, float64 "
+                      f"(oracle as committed), {dt:.1f} s"}
+
+
+def run_reference(args, world: int):
+    """The reference arm: the float64 oracle on the host cores."""
+    import oracle
+
+    from dense_fp32_matrix_05_gb300.workloads import WORKLOADS, make_problem
+    w = WORKLOADS[args.workload]
+    p = make_problem(w, pad_value=0.0)
+    oracle.build()
+    # size one step so that warmup + steps fit the time budget
+    per_step = max(0.02, args.reference_budget_s / max(1, args.warmup + args.steps))
+    _, rows, _ = oracle_sample_rate(p, per_step)
+    sel = np.linspace(0, p.M - 1, rows).astype(np.int64).tolist()
+
+    def step():
+        oracle.sgemm_ref(p.M, p.N, p.K, p.alpha, p.A, p.lda, p.B, p.ldb, p.beta,
+                         p.C if p.beta != 0 else None, p.ldc, rows=sel)
+
+    for _ in range(args.warmup):
+        step()
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t
+    flops_step = 2.0 * rows * p.N * p.K
+    value = flops_step * args.steps / dt / 1e12
+    sample = f"{rows} of {p.M} output rows x all {p.N} columns per step, K={p.K}, float64"
+    return {
+        "impl": "reference",
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{w.name}: M={p.M} N={p.N} K={p.K} fp32 row-major, {w.note}",
+                   "algo": "float64 CPU oracle (the pages publish no GPU code to run here)"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.max_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="square5120")
+    ap.add_argument("--algo", choices=["auto", "ffma", "tf32x3"], default="auto")
+    ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--cpu-baseline-s", type=float, default=10.0)
+    ap.add_argument("--reference-budget-s", type=float, default=90.0)
+    ap.add_argument("--no-cublas", dest="cublas", action="store_false")
+    ap.add_argument("--shapes-out", default=None,
+                    help="also measure every benchmark workload and write JSON lines here")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", str(args.gpus)))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if "WORLD_SIZE" not in os.environ:
+        world = 1
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        print(json.dumps(run_reference(args, world)), flush=True)
+        return 0
+
+    if world > 1:
+        import torch
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    result, p = run_ours(args, rank, world, local_rank)
+    if rank == 0 and world == 1:
+        result["cpu_baseline"] = cpu_baseline(p, args.cpu_baseline_s)
+    elif rank == 0:
+        result["cpu_baseline"] = None
+    if rank == 0 and args.shapes_out:
+        measure_all(args, local_rank)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def measure_all(args, local_rank):
+    """Every benchmark workload on both paths, one JSON line each (to a file)."""
+    from dense_fp32_matrix_05_gb300.workloads import WORKLOADS
+    out = open(args.shapes_out, "w")
+    names = ["square256", "square1024", "ragged1023x1021x1025", "square5120"] + \
+        [n for n in WORKLOADS if n.startswith("skinny")] + [n for n in WORKLOADS if n.startswith("sweep")]
+    for name in names:
+        for algo in ("auto", "ffma"):
+            a = argparse.Namespace(**vars(args))
+            a.workload, a.algo = name, algo
+            w = WORKLOADS[name]
+            a.steps = max(5, min(200, int(2e12 / max(w.flops, 1.0))))
+            a.warmup = 3
+            a.e2e_steps = 3
+            a.cublas = True
+            try:
+                r, _ = run_ours(a, 0, 1, local_rank)
+            except Exception as e:  # keep measuring the rest
+                r = {"workload": name, "algo": algo, "error": str(e)}
+            out.write(json.dumps(r) + "\n")
+            out.flush()
+            log(f"{name} {algo}: {r.get('value')} TFLOP/s, roofline {r.get('roofline', {}).get('frac')}")
+    out.close()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

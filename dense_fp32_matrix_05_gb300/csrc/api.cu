@@ -1,0 +1,500 @@
+// C ABI of the library (declared in include/sgemm_gb300.h): argument
+// checks, quick returns, the planner, library-owned device memory and the
+// launches.  The problem statement is mysgemm(M,N,K,alpha,A,B,beta,C) of
+// "NVIDIA_SGEMM_PRACTICE" (section "kernel 1") with leading dimensions; the
+// pages' error handling (print and exit, "matmul_opt.cu" CHECK_CUDA_ERROR)
+// is replaced by status codes: nothing here exits the process.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <map>
+#include <mutex>
+
+#include "../../include/sgemm_gb300.h"
+#include "launch.h"
+
+namespace {
+
+using sg::DeviceCtl;
+using sg::GemmArgs;
+using sg::Schedule;
+
+constexpr int kVersion = 100;              // 0.1.0
+constexpr int kMaxDevices = 64;
+constexpr long long kWaitBudget = 20000000000LL;  // ~10 s of SM clock: only a broken pipeline waits that long
+constexpr long long kDebugWaitBudget = 2000000LL;  // ~1 ms, test-only withheld-arrive mode
+
+struct Workspace {
+    float *ws = nullptr;
+    size_t ws_bytes = 0;
+    int *counters = nullptr;
+    size_t n_counters = 0;
+};
+
+struct HostBuffers {
+    float *A = nullptr, *B = nullptr, *C = nullptr;
+    size_t a_bytes = 0, b_bytes = 0, c_bytes = 0;
+    cudaStream_t stream = nullptr;
+};
+
+struct DevState {
+    bool ready = false;
+    int sms = 0;
+    int major = 0, minor = 0;
+    int *status = nullptr;
+    std::map<cudaStream_t, Workspace> ws;
+    HostBuffers host;
+};
+
+std::mutex g_mu;  // guards g_dev (setup, workspace growth, host buffers)
+DevState g_dev[kMaxDevices];
+
+int from_cuda(cudaError_t e) { return e == cudaSuccess ? 0 : static_cast<int>(e); }
+
+// Initialise per-device state; caller holds g_mu.
+int device_state(DevState **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e == cudaErrorNoDevice || e == cudaErrorInsufficientDriver
+                                     ? SGEMM_ERR_NO_DEVICE : from_cuda(e);
+    if (dev < 0 || dev >= kMaxDevices) return SGEMM_ERR_NO_DEVICE;
+    DevState &d = g_dev[dev];
+    if (!d.ready) {
+        cudaDeviceProp prop;
+        e = cudaGetDeviceProperties(&prop, dev);
+        if (e != cudaSuccess) return from_cuda(e);
+        d.major = prop.major;
+        d.minor = prop.minor;
+        d.sms = prop.multiProcessorCount;
+        if (!(d.major == 10 && d.minor == 3)) return SGEMM_ERR_UNSUPPORTED_DEVICE;
+        e = cudaMalloc(reinterpret_cast<void **>(&d.status), sizeof(int));
+        if (e != cudaSuccess) return from_cuda(e);
+        e = cudaMemset(d.status, 0, sizeof(int));
+        if (e != cudaSuccess) return from_cuda(e);
+        d.ready = true;
+    }
+    *out = &d;
+    return 0;
+}
+
+// ------------------------------------------------------------------ planner
+
+struct Plan {
+    int path = 0;
+    int tile_m = 0, tile_n = 0;
+    Schedule sch{};
+    int grid = 0;
+    int stages = 0;
+    int vec_a = 0, vec_b = 0, vec_c = 0;
+    size_t ws_bytes = 0;
+};
+
+int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
+
+bool aligned16(const void *p, long long ld) {
+    return (reinterpret_cast<uintptr_t>(p) % 16u) == 0 && (ld % 4) == 0;
+}
+
+// K slices for a grid of `tiles` tiles on `slots` resident CTAs, keeping at
+// least `min_kt` K tiles per slice.
+int choose_splits(int tiles, int k_tiles, int slots, int splits_req, int min_kt) {
+    if (splits_req > 0) return std::max(1, std::min(splits_req, k_tiles));
+    if (tiles >= slots) return 1;
+    int s = std::min(slots / std::max(tiles, 1), k_tiles / std::max(min_kt, 1));
+    s = std::min(s, 16);
+    return std::max(s, 1);
+}
+
+// C rows per tile of the 3xTF32 kernel (MMA N).
+int choose_tm(int M, int N, int K, int sms) {
+    int tm;
+    if (M <= 16) tm = 16;
+    else if (M <= 32) tm = 32;
+    else if (M <= 64) tm = 64;
+    else if (M <= 128) tm = 128;
+    else if (M <= 192) tm = 192;
+    else if (M <= 256) tm = 256;
+    else {
+        const long long p256 = static_cast<long long>(ceil_div(M, 256)) * 256;
+        const long long p192 = static_cast<long long>(ceil_div(M, 192)) * 192;
+        tm = (p192 < p256) ? 192 : 256;
+    }
+    // small problems: trade tile efficiency for parallelism when even the
+    // largest useful split count leaves most SMs idle
+    const int n_tiles = ceil_div(N, sg::kTf32x3TileN);
+    const int k_tiles = ceil_div(std::max(K, 1), sg::kTf32x3BK);
+    while (tm > 64) {
+        const long long units = static_cast<long long>(ceil_div(M, tm)) * n_tiles *
+                                std::max(1, std::min(16, k_tiles / 4));
+        if (units >= sms) break;
+        tm = (tm == 192) ? 128 : tm / 2;
+    }
+    return tm;
+}
+
+void plan_tf32x3(int M, int N, int K, int sms, int splits_req, Plan &p) {
+    p.path = SGEMM_ALGO_TF32X3;
+    const int tm = choose_tm(M, N, K, sms);
+    p.tile_m = tm;
+    p.tile_n = sg::kTf32x3TileN;
+    Schedule &s = p.sch;
+    s.m_tiles = ceil_div(M, tm);
+    s.n_tiles = ceil_div(N, p.tile_n);
+    s.k_tiles = ceil_div(K, sg::kTf32x3BK);
+    const int tiles = s.m_tiles * s.n_tiles;
+    s.splits = choose_splits(tiles, s.k_tiles, sms, splits_req, 4);
+    s.units = tiles * s.splits;
+    s.group_m = std::min(8, s.m_tiles);
+    p.grid = std::min(s.units, sms);
+    p.stages = sg::tf32x3_stages(tm);
+    p.ws_bytes = s.splits > 1 ? static_cast<size_t>(s.units) * p.tile_n * tm * sizeof(float) : 0;
+}
+
+void plan_ffma(int M, int N, int K, int sms, int splits_req, Plan &p) {
+    p.path = SGEMM_ALGO_FFMA;
+    if (M <= 32) { p.tile_m = 32; p.tile_n = 512; }
+    else if (M <= 64) { p.tile_m = 64; p.tile_n = 256; }
+    else { p.tile_m = 128; p.tile_n = 128; }
+    Schedule &s = p.sch;
+    s.m_tiles = ceil_div(M, p.tile_m);
+    s.n_tiles = ceil_div(N, p.tile_n);
+    s.k_tiles = ceil_div(K, sg::kFfmaBK);
+    const int tiles = s.m_tiles * s.n_tiles;
+    s.splits = choose_splits(tiles, s.k_tiles, 2 * sms, splits_req, 4);
+    s.units = tiles * s.splits;
+    s.group_m = std::min(8, s.m_tiles);
+    p.grid = s.units;
+    p.stages = sg::ffma_stages(p.tile_m, p.tile_n);
+    p.ws_bytes = s.splits > 1
+                     ? static_cast<size_t>(s.units) * p.tile_m * p.tile_n * sizeof(float) : 0;
+}
+
+int make_plan(int M, int N, int K, const void *A, int lda, const void *B, int ldb, const void *C, int ldc,
+              int algo, int splits, int sms, Plan &p) {
+    const int path = (algo == SGEMM_ALGO_AUTO) ? SGEMM_ALGO_TF32X3 : algo;
+    if (path == SGEMM_ALGO_TF32X3) plan_tf32x3(M, N, K, sms, splits, p);
+    else plan_ffma(M, N, K, sms, splits, p);
+    p.vec_a = aligned16(A, lda);
+    p.vec_b = aligned16(B, ldb);
+    p.vec_c = aligned16(C, ldc);
+    if (p.sch.units <= 0 || p.grid <= 0) return SGEMM_ERR_INTERNAL;
+    return 0;
+}
+
+// --------------------------------------------------------- argument checks
+
+bool overlaps(const void *a, size_t a_bytes, const void *b, size_t b_bytes) {
+    if (!a || !b || a_bytes == 0 || b_bytes == 0) return false;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + b_bytes && b0 < a0 + a_bytes;
+}
+
+size_t span_bytes(int rows, int cols, long long ld) {
+    if (rows <= 0 || cols <= 0) return 0;
+    return static_cast<size_t>((static_cast<long long>(rows) - 1) * ld + cols) * sizeof(float);
+}
+
+int check_args(int M, int N, int K, float alpha, const float *A, int lda, const float *B, int ldb, float beta,
+               float *C, int ldc, int algo, int splits, int flags) {
+    (void)beta;
+    if (M < 0) return -1;
+    if (N < 0) return -2;
+    if (K < 0) return -3;
+    if (lda < std::max(1, K)) return -6;
+    if (ldb < std::max(1, N)) return -8;
+    if (ldc < std::max(1, N)) return -11;
+    if (algo < SGEMM_ALGO_AUTO || algo > SGEMM_ALGO_TF32X3) return -13;
+    if (splits < 0) return -14;
+    if (flags & ~SGEMM_FLAG_DEBUG_WITHHOLD_ARRIVE) return -15;
+    if (M == 0 || N == 0) return 0;
+    const bool use_ab = alpha != 0.f && K > 0;
+    if (use_ab && A == nullptr) return -5;
+    if (use_ab && B == nullptr) return -7;
+    if (C == nullptr) return -10;
+    const size_t c_bytes = span_bytes(M, N, ldc);
+    if (use_ab && (overlaps(C, c_bytes, A, span_bytes(M, K, lda)) ||
+                   overlaps(C, c_bytes, B, span_bytes(K, N, ldb))))
+        return -10;
+    return 0;
+}
+
+// Grow the split-K workspace of (device, stream); caller holds g_mu.
+int get_workspace(DevState &d, cudaStream_t stream, size_t bytes, size_t counters, Workspace **out) {
+    Workspace &w = d.ws[stream];
+    if (w.ws_bytes < bytes) {
+        if (w.ws) {
+            cudaError_t e = cudaStreamSynchronize(stream);
+            if (e != cudaSuccess) return from_cuda(e);
+            cudaFree(w.ws);
+            w.ws = nullptr;
+            w.ws_bytes = 0;
+        }
+        if (cudaMalloc(reinterpret_cast<void **>(&w.ws), bytes) != cudaSuccess) {
+            cudaGetLastError();
+            return SGEMM_ERR_WORKSPACE;
+        }
+        w.ws_bytes = bytes;
+    }
+    if (w.n_counters < counters) {
+        const size_t n = std::max<size_t>(counters, 1024);
+        if (w.counters) {
+            cudaError_t e = cudaStreamSynchronize(stream);
+            if (e != cudaSuccess) return from_cuda(e);
+            cudaFree(w.counters);
+            w.counters = nullptr;
+            w.n_counters = 0;
+        }
+        if (cudaMalloc(reinterpret_cast<void **>(&w.counters), n * sizeof(int)) != cudaSuccess) {
+            cudaGetLastError();
+            return SGEMM_ERR_WORKSPACE;
+        }
+        cudaError_t e = cudaMemsetAsync(w.counters, 0, n * sizeof(int), stream);
+        if (e != cudaSuccess) return from_cuda(e);
+        w.n_counters = n;
+    }
+    *out = &w;
+    return 0;
+}
+
+int run(int M, int N, int K, float alpha, const float *A, int lda, const float *B, int ldb, float beta,
+        float *C, int ldc, cudaStream_t stream, int algo, int splits, int flags) {
+    int rc = check_args(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, algo, splits, flags);
+    if (rc != 0) return rc;
+    if (M == 0 || N == 0) return 0;
+
+    DevState *d = nullptr;
+    DeviceCtl ctl{};
+    Plan p;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        rc = device_state(&d);
+        if (rc != 0) return rc;
+        if (alpha == 0.f || K == 0) {
+            if (beta == 1.f) return 0;
+            return from_cuda(sg::scale_c_launch(C, ldc, M, N, beta, d->sms, stream));
+        }
+        rc = make_plan(M, N, K, A, lda, B, ldb, C, ldc, algo, splits, d->sms, p);
+        if (rc != 0) return rc;
+        ctl.status = d->status;
+        ctl.wait_budget = (flags & SGEMM_FLAG_DEBUG_WITHHOLD_ARRIVE) ? kDebugWaitBudget : kWaitBudget;
+        ctl.debug_flags = (flags & SGEMM_FLAG_DEBUG_WITHHOLD_ARRIVE) ? sg::kDebugWithholdArrive : 0;
+        if (p.sch.splits > 1) {
+            Workspace *w = nullptr;
+            rc = get_workspace(*d, stream, p.ws_bytes,
+                               static_cast<size_t>(p.sch.m_tiles) * p.sch.n_tiles, &w);
+            if (rc != 0) return rc;
+            ctl.ws = w->ws;
+            ctl.counters = w->counters;
+        }
+    }
+    GemmArgs g{M, N, K, alpha, beta, A, lda, B, ldb, C, ldc};
+    cudaError_t e;
+    if (p.path == SGEMM_ALGO_TF32X3)
+        e = sg::tf32x3_launch(p.tile_m, g, p.sch, ctl, p.vec_a, p.grid, stream);
+    else
+        e = sg::ffma_launch(p.tile_m, p.tile_n, g, p.sch, ctl, p.vec_a, p.vec_b, p.vec_c, stream);
+    return from_cuda(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+int sgemm(int M, int N, int K, float alpha, const float *A, int lda, const float *B, int ldb, float beta,
+          float *C, int ldc, sgemm_stream_t stream) {
+    return run(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, reinterpret_cast<cudaStream_t>(stream),
+               SGEMM_ALGO_AUTO, 0, 0);
+}
+
+int sgemm_ex(int M, int N, int K, float alpha, const float *A, int lda, const float *B, int ldb, float beta,
+             float *C, int ldc, sgemm_stream_t stream, int algo, int splits, int flags) {
+    return run(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, reinterpret_cast<cudaStream_t>(stream), algo,
+               splits, flags);
+}
+
+int sgemm_host(int M, int N, int K, float alpha, const float *A, int lda, const float *B, int ldb, float beta,
+               float *C, int ldc, int algo) {
+    int rc = check_args(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, algo, 0, 0);
+    if (rc != 0) return rc;
+    if (M == 0 || N == 0) return 0;
+    std::unique_lock<std::mutex> lk(g_mu);
+    DevState *d = nullptr;
+    rc = device_state(&d);
+    if (rc != 0) return rc;
+    HostBuffers &h = d->host;
+    cudaError_t e;
+    if (!h.stream) {
+        e = cudaStreamCreateWithFlags(&h.stream, cudaStreamNonBlocking);
+        if (e != cudaSuccess) return from_cuda(e);
+    }
+    const bool use_ab = alpha != 0.f && K > 0;
+    const size_t a_bytes = use_ab ? span_bytes(M, K, lda) : 0;
+    const size_t b_bytes = use_ab ? span_bytes(K, N, ldb) : 0;
+    const size_t c_bytes = span_bytes(M, N, ldc);
+    auto grow = [&](float *&buf, size_t &cap, size_t need) -> int {
+        if (cap >= need) return 0;
+        if (buf) {
+            cudaStreamSynchronize(h.stream);
+            cudaFree(buf);
+            buf = nullptr;
+            cap = 0;
+        }
+        if (cudaMalloc(reinterpret_cast<void **>(&buf), need) != cudaSuccess) {
+            cudaGetLastError();
+            return SGEMM_ERR_WORKSPACE;
+        }
+        cap = need;
+        return 0;
+    };
+    if ((rc = grow(h.A, h.a_bytes, std::max<size_t>(a_bytes, 16))) != 0) return rc;
+    if ((rc = grow(h.B, h.b_bytes, std::max<size_t>(b_bytes, 16))) != 0) return rc;
+    if ((rc = grow(h.C, h.c_bytes, c_bytes)) != 0) return rc;
+    if (a_bytes && (e = cudaMemcpyAsync(h.A, A, a_bytes, cudaMemcpyHostToDevice, h.stream)) != cudaSuccess)
+        return from_cuda(e);
+    if (b_bytes && (e = cudaMemcpyAsync(h.B, B, b_bytes, cudaMemcpyHostToDevice, h.stream)) != cudaSuccess)
+        return from_cuda(e);
+    if (beta != 0.f &&
+        (e = cudaMemcpyAsync(h.C, C, c_bytes, cudaMemcpyHostToDevice, h.stream)) != cudaSuccess)
+        return from_cuda(e);
+    float *dA = h.A, *dB = h.B, *dC = h.C;
+    cudaStream_t st = h.stream;
+    lk.unlock();
+    rc = run(M, N, K, alpha, use_ab ? dA : nullptr, lda, use_ab ? dB : nullptr, ldb, beta, dC, ldc, st, algo,
+             0, 0);
+    if (rc != 0) return rc;
+    if ((e = cudaMemcpyAsync(C, dC, c_bytes, cudaMemcpyDeviceToHost, st)) != cudaSuccess) return from_cuda(e);
+    return from_cuda(cudaStreamSynchronize(st));
+}
+
+int sgemm_plan_info(int M, int N, int K, const void *A, int lda, const void *B, int ldb, const void *C, int ldc,
+                    int algo, int splits, float alpha, float beta, int num_sms, int *info, int ninfo) {
+    if (M < 0) return -1;
+    if (N < 0) return -2;
+    if (K < 0) return -3;
+    if (lda < std::max(1, K)) return -5;
+    if (ldb < std::max(1, N)) return -7;
+    if (ldc < std::max(1, N)) return -9;
+    if (algo < SGEMM_ALGO_AUTO || algo > SGEMM_ALGO_TF32X3) return -10;
+    if (splits < 0) return -11;
+    if (num_sms < 0) return -14;
+    if (info == nullptr && ninfo > 0) return -15;
+    if (ninfo < 0) return -16;
+    (void)alpha;
+    (void)beta;
+    int sms = num_sms;
+    if (sms == 0) {
+        std::lock_guard<std::mutex> lk(g_mu);
+        DevState *d = nullptr;
+        int rc = device_state(&d);
+        if (rc != 0) return rc;
+        sms = d->sms;
+    }
+    int vals[10] = {0};
+    if (M > 0 && N > 0 && K > 0) {
+        Plan p;
+        int rc = make_plan(M, N, K, A, lda, B, ldb, C, ldc, algo, splits, sms, p);
+        if (rc != 0) return rc;
+        vals[0] = p.path;
+        vals[1] = p.tile_m;
+        vals[2] = p.tile_n;
+        vals[3] = p.sch.splits;
+        vals[4] = p.sch.units;
+        vals[5] = p.grid;
+        vals[6] = p.stages;
+        vals[7] = p.vec_a;
+        vals[8] = p.vec_b;
+        vals[9] = static_cast<int>(std::min<size_t>(p.ws_bytes, 0x7fffffff));
+    }
+    for (int i = 0; i < ninfo && i < 10; ++i) info[i] = vals[i];
+    return 0;
+}
+
+int sgemm_check_status(sgemm_stream_t stream) {
+    cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return from_cuda(e);
+    std::lock_guard<std::mutex> lk(g_mu);
+    DevState *d = nullptr;
+    int rc = device_state(&d);
+    if (rc != 0) return rc;
+    int word = 0;
+    e = cudaMemcpy(&word, d->status, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return from_cuda(e);
+    if (word != 0) {
+        // a kernel that gave up may have left split-K arrival counters
+        // non-zero: wait for the device and clear them all
+        e = cudaDeviceSynchronize();
+        if (e != cudaSuccess) return from_cuda(e);
+        for (auto &kv : d->ws)
+            if (kv.second.counters) cudaMemset(kv.second.counters, 0, kv.second.n_counters * sizeof(int));
+        e = cudaMemset(d->status, 0, sizeof(int));
+        if (e != cudaSuccess) return from_cuda(e);
+        return SGEMM_ERR_DEVICE_TIMEOUT;
+    }
+    return 0;
+}
+
+const char *sgemm_status_string(int status) {
+    if (status == 0) return "success";
+    if (status < 0) {
+        switch (-status) {
+            case 1: return "invalid argument 1 (M < 0)";
+            case 2: return "invalid argument 2 (N < 0)";
+            case 3: return "invalid argument 3 (K < 0)";
+            case 5: return "invalid argument 5 (A is NULL)";
+            case 6: return "invalid argument 6 (lda < max(1, K))";
+            case 7: return "invalid argument 7 (B is NULL)";
+            case 8: return "invalid argument 8 (ldb < max(1, N))";
+            case 10: return "invalid argument 10 (C is NULL or overlaps A or B)";
+            case 11: return "invalid argument 11 (ldc < max(1, N))";
+            case 13: return "invalid argument 13 (unknown algo)";
+            case 14: return "invalid argument 14 (splits < 0)";
+            case 15: return "invalid argument 15 (unknown flags)";
+            default: return "invalid argument";
+        }
+    }
+    switch (status) {
+        case SGEMM_ERR_DEVICE_TIMEOUT: return "a bounded on-device wait gave up (result unspecified)";
+        case SGEMM_ERR_NO_DEVICE: return "no usable CUDA device";
+        case SGEMM_ERR_UNSUPPORTED_DEVICE: return "device is not compute capability 10.3 (sm_103a)";
+        case SGEMM_ERR_WORKSPACE: return "could not allocate library-owned device memory";
+        case SGEMM_ERR_INTERNAL: return "internal planner error";
+        default: break;
+    }
+    if (status > 0 && status < 10000) return cudaGetErrorString(static_cast<cudaError_t>(status));
+    return "unknown status";
+}
+
+int sgemm_release(void) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    int cur = 0;
+    if (cudaGetDevice(&cur) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    int rc = 0;
+    for (int dev = 0; dev < kMaxDevices; ++dev) {
+        DevState &d = g_dev[dev];
+        if (!d.ready) continue;
+        cudaSetDevice(dev);
+        cudaError_t e = cudaDeviceSynchronize();
+        if (e != cudaSuccess && rc == 0) rc = from_cuda(e);
+        for (auto &kv : d.ws) {
+            cudaFree(kv.second.ws);
+            cudaFree(kv.second.counters);
+        }
+        d.ws.clear();
+        cudaFree(d.host.A);
+        cudaFree(d.host.B);
+        cudaFree(d.host.C);
+        d.host.A = d.host.B = d.host.C = nullptr;
+        d.host.a_bytes = d.host.b_bytes = d.host.c_bytes = 0;
+    }
+    cudaSetDevice(cur);
+    return rc;
+}
+
+int sgemm_version(void) { return kVersion; }
+
+}  // extern "C"

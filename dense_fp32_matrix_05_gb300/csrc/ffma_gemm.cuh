@@ -1,0 +1,257 @@
+// SGEMM on the CUDA cores (fp32 FFMA): exact fp32 products and sums.
+//
+// Structure (re-done for sm_103a from the ideas of "NVIDIA_SGEMM_PRACTICE",
+// sections "kernel 2" shared-memory tiles, "kernel 4" 2-D thread tiles,
+// "kernel 5" fragment registers, "kernel 6" 128-bit loads, "kernel 7"
+// prefetching, and the zero-filled edge tiles of "matmul_opt.cu"):
+//   - CTA tile BM x BN x 16, 256 threads, each thread an 8 x 8 block of C
+//     (two 4-row x two 4-column sub-blocks, so fragment reads are 128-bit);
+//     warp tile 32 x 64;
+//   - an STAGES-deep cp.async ring: 16-byte copies when a matrix's rows are
+//     16-byte aligned, 4-byte copies otherwise; edges are zero-filled by the
+//     copy itself (src-size < copy size);
+//   - A is kept K-major in shared memory (as stored in global memory) with
+//     its 16-byte chunks XOR-swizzled by (row / 4) % 4, so the four distinct
+//     rows a warp reads per instruction fall in four different bank groups;
+//     B is kept N-major, read as 8 consecutive 16-byte chunks per warp;
+//   - per 4-k step a thread loads its 8 rows x 4 k of A and, per k, 8 values
+//     of B (16 LDS.128 per 256 FFMA) and updates 64 accumulators;
+//   - epilogue alpha*acc + beta*C (C not read when beta == 0), 128-bit
+//     accesses when C rows are aligned, predicated edges; split-K partials
+//     go to a workspace and the last slice to arrive sums them in order.
+#pragma once
+#include <cstdint>
+
+#include "common.cuh"
+
+namespace sg {
+namespace ffma {
+
+constexpr int kThreads = 256;
+constexpr int kBK = 16;
+
+template <int BM, int BN, int STAGES>
+struct Cfg {
+    static constexpr int kWarpsN = BN / 64;
+    static constexpr int kWarpsM = BM / 32;
+    static_assert(kWarpsM * kWarpsN == 8, "8 warps of 32 x 64");
+    static constexpr int kAFloats = BM * kBK;
+    static constexpr int kBFloats = kBK * BN;
+    static constexpr int kStageFloats = kAFloats + kBFloats;
+    static constexpr int kSmemBytes = STAGES * kStageFloats * 4 + 16;
+};
+
+template <int BM, int BN>
+__device__ __forceinline__ void load_stage(const GemmArgs &g, bool vec_a, bool vec_b, int m0, int n0,
+                                           int k0, uint32_t sA, uint32_t sB, int tid) {
+    // A tile: BM rows x 16 k, K-major, chunk c of row r stored at c ^ ((r >> 2) & 3)
+    if (vec_a) {
+#pragma unroll
+        for (int j = tid; j < BM * 4; j += kThreads) {
+            const int r = j >> 2, kc = j & 3;
+            const int m = m0 + r, k = k0 + kc * 4;
+            const float *src = g.A;
+            uint32_t bytes = 0;
+            if (m < g.M && k < g.K) {
+                src = g.A + static_cast<long long>(m) * g.lda + k;
+                bytes = static_cast<uint32_t>(min(4, g.K - k) * 4);
+            }
+            cp_async16(sA + static_cast<uint32_t>((r * kBK + ((kc ^ ((r >> 2) & 3)) << 2)) * 4), src, bytes);
+        }
+    } else {
+#pragma unroll 4
+        for (int j = tid; j < BM * kBK; j += kThreads) {
+            const int r = j >> 4, kk = j & 15;
+            const int m = m0 + r, k = k0 + kk;
+            const bool ok = m < g.M && k < g.K;
+            const float *src = ok ? g.A + static_cast<long long>(m) * g.lda + k : g.A;
+            const int col = (((kk >> 2) ^ ((r >> 2) & 3)) << 2) | (kk & 3);
+            cp_async4(sA + static_cast<uint32_t>((r * kBK + col) * 4), src, ok ? 4u : 0u);
+        }
+    }
+    // B tile: 16 k x BN, N-major
+    if (vec_b) {
+#pragma unroll
+        for (int j = tid; j < kBK * BN / 4; j += kThreads) {
+            const int r = j / (BN / 4), nc = j % (BN / 4);
+            const int k = k0 + r, n = n0 + nc * 4;
+            const float *src = g.B;
+            uint32_t bytes = 0;
+            if (k < g.K && n < g.N) {
+                src = g.B + static_cast<long long>(k) * g.ldb + n;
+                bytes = static_cast<uint32_t>(min(4, g.N - n) * 4);
+            }
+            cp_async16(sB + static_cast<uint32_t>((r * BN + nc * 4) * 4), src, bytes);
+        }
+    } else {
+#pragma unroll 4
+        for (int j = tid; j < kBK * BN; j += kThreads) {
+            const int r = j / BN, c = j % BN;
+            const int k = k0 + r, n = n0 + c;
+            const bool ok = k < g.K && n < g.N;
+            const float *src = ok ? g.B + static_cast<long long>(k) * g.ldb + n : g.B;
+            cp_async4(sB + static_cast<uint32_t>((r * BN + c) * 4), src, ok ? 4u : 0u);
+        }
+    }
+}
+
+template <int BM, int BN, int STAGES>
+__global__ void __launch_bounds__(kThreads, 2)
+    ffma_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ Schedule sch,
+                     const __grid_constant__ DeviceCtl ctl, int vec_a, int vec_b, int vec_c) {
+    using Cf = Cfg<BM, BN, STAGES>;
+    extern __shared__ __align__(16) float smem_f[];
+    __shared__ int s_last;
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int wm = warp / Cf::kWarpsN, wn = warp % Cf::kWarpsN;
+    const int lm = lane >> 3, ln = lane & 7;
+    const int row_base = wm * 32 + lm * 4;  // rows row_base+i and row_base+16+i, i < 4
+    const int col_base = wn * 64 + ln * 4;  // cols col_base+j and col_base+32+j, j < 4
+
+    const UnitCoord c = decode_unit(sch, blockIdx.x);
+    const int m0 = c.mt * BM, n0 = c.nt * BN;
+    const int KT = c.ke - c.kb;
+    const uint32_t s0 = smem_u32(smem_f);
+
+    float acc[8][8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+
+#pragma unroll
+    for (int s = 0; s < STAGES - 1; ++s) {
+        if (s < KT) {
+            const uint32_t st = s0 + static_cast<uint32_t>(s * Cf::kStageFloats * 4);
+            load_stage<BM, BN>(g, vec_a, vec_b, m0, n0, (c.kb + s) * kBK, st, st + Cf::kAFloats * 4, tid);
+        }
+        cp_async_commit();
+    }
+
+#pragma unroll 1
+    for (int t = 0; t < KT; ++t) {
+        cp_async_wait<STAGES - 2>();
+        __syncthreads();
+        {
+            const int nt = t + STAGES - 1;
+            if (nt < KT) {
+                const uint32_t st = s0 + static_cast<uint32_t>((nt % STAGES) * Cf::kStageFloats * 4);
+                load_stage<BM, BN>(g, vec_a, vec_b, m0, n0, (c.kb + nt) * kBK, st, st + Cf::kAFloats * 4, tid);
+            }
+            cp_async_commit();
+        }
+        const uint32_t sA = s0 + static_cast<uint32_t>((t % STAGES) * Cf::kStageFloats * 4);
+        const uint32_t sB = sA + Cf::kAFloats * 4;
+#pragma unroll
+        for (int kq = 0; kq < 4; ++kq) {
+            float a[8][4];
+            const uint32_t chunk = static_cast<uint32_t>((kq ^ lm) << 2);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float4 v0 = lds128(sA + ((row_base + i) * kBK + chunk) * 4);
+                const float4 v1 = lds128(sA + ((row_base + 16 + i) * kBK + chunk) * 4);
+                a[i][0] = v0.x; a[i][1] = v0.y; a[i][2] = v0.z; a[i][3] = v0.w;
+                a[4 + i][0] = v1.x; a[4 + i][1] = v1.y; a[4 + i][2] = v1.z; a[4 + i][3] = v1.w;
+            }
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                const int k = kq * 4 + kk;
+                const float4 b0 = lds128(sB + (k * BN + col_base) * 4);
+                const float4 b1 = lds128(sB + (k * BN + col_base + 32) * 4);
+                const float b[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i][kk], b[j], acc[i][j]);
+            }
+        }
+    }
+    cp_async_wait<0>();
+
+    if (sch.splits > 1) {
+        constexpr int kTileElems = BM * BN;
+        float *wt = ctl.ws + (static_cast<long long>(c.tile) * sch.splits + c.split) * kTileElems + tid * 64;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            __stcg(reinterpret_cast<float4 *>(wt + i * 8), make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]));
+            __stcg(reinterpret_cast<float4 *>(wt + i * 8 + 4), make_float4(acc[i][4], acc[i][5], acc[i][6], acc[i][7]));
+        }
+        __threadfence();
+        __syncthreads();
+        if (tid == 0) {
+            const int prev = atomicAdd(ctl.counters + c.tile, 1);
+            s_last = (prev == sch.splits - 1) ? 1 : 0;
+        }
+        __syncthreads();
+        if (!s_last) return;
+        __threadfence();
+        const float *wb = ctl.ws + static_cast<long long>(c.tile) * sch.splits * kTileElems + tid * 64;
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+#pragma unroll 1
+        for (int sp = 0; sp < sch.splits; ++sp) {
+            const float *p = wb + static_cast<long long>(sp) * kTileElems;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float4 x0 = __ldcg(reinterpret_cast<const float4 *>(p + i * 8));
+                const float4 x1 = __ldcg(reinterpret_cast<const float4 *>(p + i * 8 + 4));
+                acc[i][0] += x0.x; acc[i][1] += x0.y; acc[i][2] += x0.z; acc[i][3] += x0.w;
+                acc[i][4] += x1.x; acc[i][5] += x1.y; acc[i][6] += x1.z; acc[i][7] += x1.w;
+            }
+        }
+        if (tid == 0) ctl.counters[c.tile] = 0;
+    }
+
+    // epilogue: C = alpha * acc + beta * C
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int m = m0 + row_base + (i < 4 ? i : 12 + i);
+        if (m >= g.M) continue;
+        float *crow = g.C + static_cast<long long>(m) * g.ldc;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int n = n0 + col_base + h * 32;
+            float r[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) r[e] = g.alpha * acc[i][h * 4 + e];
+            if (vec_c && n + 3 < g.N) {
+                float4 *p = reinterpret_cast<float4 *>(crow + n);
+                if (g.beta != 0.f) {
+                    const float4 o = *p;
+                    r[0] = fmaf(g.beta, o.x, r[0]);
+                    r[1] = fmaf(g.beta, o.y, r[1]);
+                    r[2] = fmaf(g.beta, o.z, r[2]);
+                    r[3] = fmaf(g.beta, o.w, r[3]);
+                }
+                *p = make_float4(r[0], r[1], r[2], r[3]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    if (n + e < g.N) {
+                        float *p = crow + n + e;
+                        *p = (g.beta == 0.f) ? r[e] : fmaf(g.beta, *p, r[e]);
+                    }
+                }
+            }
+        }
+    }
+}
+
+// C = beta * C (C := 0 when beta == 0, without reading C): the alpha == 0 /
+// K == 0 case of the problem statement.
+__global__ void scale_c_kernel(float *C, long long ldc, int M, int N, float beta) {
+    const long long total = static_cast<long long>(M) * N;
+    for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
+         idx += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const long long m = idx / N, n = idx - m * N;
+        float *p = C + m * ldc + n;
+        *p = (beta == 0.f) ? 0.f : beta * *p;
+    }
+}
+
+}  // namespace ffma
+}  // namespace sg

@@ -1,0 +1,469 @@
+// SGEMM on the tcgen05 tensor cores with the 3xTF32 split.
+//
+// Each fp32 operand x is split into hi = x with the low 13 mantissa bits
+// cleared (an exact tf32 value) and lo = tf32(x - hi); the product a*b is
+// then accumulated as hi_a*hi_b + hi_a*lo_b + lo_a*hi_b (lo_a*lo_b, below
+// 2^-20 |a*b|, is dropped) into one fp32 accumulator in tensor memory.
+//
+// The kernel computes each C tile transposed: the MMA's M dimension (128
+// tensor-memory lanes) runs over C columns n and its N dimension over C rows
+// m, so D[n][m] = sum_k B[k][n] * A[m][k].  The epilogue then reads one C
+// column per thread and, for each row, a warp stores 32 consecutive floats:
+// coalesced for any ldc, including odd row lengths such as N = 14161.
+//
+// Roles (one persistent CTA per SM, work units strided over the grid):
+//   warps 0-3   epilogue: tensor memory -> alpha/beta -> C (or split-K
+//               partials); warp w owns tensor-memory lanes 32w..32w+31
+//   warps 4-11  producers: global loads (any alignment, zero-filled edges)
+//               -> hi/lo split in registers -> K-major 64-byte-swizzled
+//               shared-memory stages; the next stage's loads are in flight
+//               while the current one is split and stored
+//   warp 12     tensor-memory allocation and the single MMA-issuing thread
+// Pipelines: STAGES-deep shared-memory ring (full/empty mbarriers; the
+// tensor core frees a stage through tcgen05.commit) and two accumulators in
+// tensor memory (acc_full/acc_empty) so that a tile's epilogue overlaps the
+// next tile's main loop.  Every wait is bounded (see mbar_wait_bounded).
+//
+// Operand staging follows the shared-memory tiling and vector-load ideas of
+// "NVIDIA_SGEMM_PRACTICE" (sections "kernel 2", "kernel 6", "kernel 7") and
+// the zero-filled edge tiles of "matmul_opt.cu" (matrixMulOptimized),
+// re-done for the tensor core: the split has to touch every element, so
+// operands go global -> registers -> shared memory once, already split and
+// swizzled, instead of through an extra raw staging copy.
+#pragma once
+#include <cstdint>
+
+#include "common.cuh"
+
+namespace sg {
+namespace tf32x3 {
+
+constexpr int kTileN = 128;  // C columns per tile (MMA M, tensor-memory lanes)
+constexpr int kBK = 16;      // K per stage: one 64-byte swizzled row per operand row
+constexpr int kEpiWarps = 4;
+constexpr int kProdWarps = 8;
+constexpr int kProdThreads = kProdWarps * 32;
+constexpr int kMmaWarp = kEpiWarps + kProdWarps;
+constexpr int kThreads = (kEpiWarps + kProdWarps + 1) * 32;
+constexpr int kEpiBarrierId = 1;
+
+__host__ __device__ constexpr int stages_for(int tm) {
+    return tm >= 256 ? 4 : tm >= 192 ? 5 : tm >= 128 ? 6 : 8;
+}
+__host__ __device__ constexpr uint32_t tmem_cols_for(int tm) {
+    return (2 * tm) <= 32 ? 32u : (2 * tm) <= 64 ? 64u : (2 * tm) <= 128 ? 128u
+         : (2 * tm) <= 256 ? 256u : 512u;
+}
+
+// TM = C rows per tile (MMA N).
+template <int TM>
+struct Cfg {
+    static_assert(TM % 16 == 0 && TM >= 16 && TM <= 256, "MMA N for M=128 must be 16..256, step 16");
+    static constexpr int kStages = stages_for(TM);
+    static constexpr int kBtBytes = kTileN * kBK * 4;  // B^T tile (MMA A operand)
+    static constexpr int kABytes = TM * kBK * 4;       // A tile (MMA B operand)
+    static constexpr int kOffBtHi = 0;
+    static constexpr int kOffBtLo = kBtBytes;
+    static constexpr int kOffAHi = 2 * kBtBytes;
+    static constexpr int kOffALo = 2 * kBtBytes + kABytes;
+    static constexpr int kStageBytes = 2 * kBtBytes + 2 * kABytes;
+    static_assert(kStageBytes % 1024 == 0, "stages must keep 1 KB alignment");
+    static constexpr int kAJobs = (TM * 4 + kProdThreads - 1) / kProdThreads;
+    static constexpr int kChunk = TM < 32 ? 16 : 32;
+    static constexpr uint32_t kTmemCols = tmem_cols_for(TM);
+    static constexpr uint32_t kIdesc = umma_idesc_tf32(kTileN, TM);
+    // barriers: full[S], empty[S], acc_full[2], acc_empty[2], drain; then
+    // tensor-memory address, abort flag, split-K "last arrival" flag
+    static constexpr int kBarBytes = 8 * (2 * kStages + 5) + 16;
+    static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes;
+};
+
+// Byte offset of the 16-byte chunk `chunk` (k / 4) of row `row` inside a
+// K-major tile with 64-byte rows and the 64-byte swizzle.
+__device__ __forceinline__ uint32_t sw64_off(int row, int chunk) {
+    return static_cast<uint32_t>(row * 64 + (((chunk ^ (row >> 1)) & 3) << 4));
+}
+
+// hi/lo split of one fp32 value (bit patterns of two exact tf32 values).
+// Non-finite x: hi keeps x (a NaN keeps a high mantissa bit, so the tensor
+// core still sees a NaN), lo = 0 (so Inf - Inf cannot create a NaN).
+__device__ __forceinline__ void split_tf32(float x, uint32_t &hi, uint32_t &lo) {
+    const uint32_t u = __float_as_uint(x);
+    const uint32_t hu = u & 0xFFFFE000u;
+    const float rest = x - __uint_as_float(hu);  // exact
+    const uint32_t lu = (__float_as_uint(rest) + 0x1000u) & 0xFFFFE000u;  // round |rest| to tf32
+    const bool nonfinite = (u & 0x7F800000u) == 0x7F800000u;
+    hi = nonfinite ? (u | ((u & 0x007FFFFFu) ? 0x00400000u : 0u)) : hu;
+    lo = nonfinite ? 0u : lu;
+}
+
+template <int AJ>
+struct Raw {
+    float b[2][4];   // B^T chunks: 4 consecutive k of one column n
+    float a[AJ][4];  // A chunks: 4 consecutive k of one row m
+};
+
+// Producer: load one k-tile (K-range [k0, k0+16)) of B^T (128 columns) and A
+// (TM rows) into registers; out-of-range elements read as 0.
+template <int TM, int AJ>
+__device__ __forceinline__ void load_raw(const GemmArgs &g, bool vec_a, int m0, int n0, int k0,
+                                         int ptid, Raw<AJ> &raw) {
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+        const int j = ptid + r * kProdThreads;
+        const int n = n0 + (j & (kTileN - 1));
+        const int kb = k0 + (j >> 7) * 4;
+        const bool n_ok = n < g.N;
+        const float *src = g.B + static_cast<long long>(kb) * g.ldb + n;
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            raw.b[r][e] = (n_ok && kb + e < g.K) ? __ldg(src + e * g.ldb) : 0.f;
+    }
+#pragma unroll
+    for (int r = 0; r < AJ; ++r) {
+        const int j = ptid + r * kProdThreads;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (j < TM * 4) {
+            const int m = m0 + (j >> 2);
+            const int k = k0 + (j & 3) * 4;
+            if (m < g.M) {
+                const float *src = g.A + static_cast<long long>(m) * g.lda + k;
+                if (vec_a && k + 3 < g.K) {
+                    v = __ldg(reinterpret_cast<const float4 *>(src));
+                } else {
+                    v.x = (k + 0 < g.K) ? __ldg(src + 0) : 0.f;
+                    v.y = (k + 1 < g.K) ? __ldg(src + 1) : 0.f;
+                    v.z = (k + 2 < g.K) ? __ldg(src + 2) : 0.f;
+                    v.w = (k + 3 < g.K) ? __ldg(src + 3) : 0.f;
+                }
+            }
+        }
+        raw.a[r][0] = v.x;
+        raw.a[r][1] = v.y;
+        raw.a[r][2] = v.z;
+        raw.a[r][3] = v.w;
+    }
+}
+
+__device__ __forceinline__ void split_store4(uint32_t hi_addr, uint32_t lo_addr, const float (&x)[4]) {
+    uint32_t h0, h1, h2, h3, l0, l1, l2, l3;
+    split_tf32(x[0], h0, l0);
+    split_tf32(x[1], h1, l1);
+    split_tf32(x[2], h2, l2);
+    split_tf32(x[3], h3, l3);
+    sts128(hi_addr, h0, h1, h2, h3);
+    sts128(lo_addr, l0, l1, l2, l3);
+}
+
+// Producer: split the registers of one k-tile into stage `stage`.
+template <int TM, int AJ>
+__device__ __forceinline__ void store_split(uint32_t stage, int ptid, const Raw<AJ> &raw) {
+    using C = Cfg<TM>;
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+        const int j = ptid + r * kProdThreads;
+        const uint32_t off = sw64_off(j & (kTileN - 1), j >> 7);
+        split_store4(stage + C::kOffBtHi + off, stage + C::kOffBtLo + off, raw.b[r]);
+    }
+#pragma unroll
+    for (int r = 0; r < AJ; ++r) {
+        const int j = ptid + r * kProdThreads;
+        if (j < TM * 4) {
+            const uint32_t off = sw64_off(j >> 2, j & 3);
+            split_store4(stage + C::kOffAHi + off, stage + C::kOffALo + off, raw.a[r]);
+        }
+    }
+}
+
+// Exact fp32 dot product of row m of A and column n of B, in k order.  The
+// epilogue calls it only for an accumulator that came out NaN: with the
+// 3xTF32 split an infinite operand meeting a partner whose lo part is zero
+// gives Inf * 0 = NaN where fp32 arithmetic gives +-Inf, so NaN results are
+// recomputed on the CUDA cores.  Stops early once the sum itself is NaN.
+__device__ __noinline__ float recompute_dot(const GemmArgs &g, int m, int n) {
+    const float *a = g.A + static_cast<long long>(m) * g.lda;
+    const float *b = g.B + n;
+    float s = 0.f;
+    for (int k = 0; k < g.K; ++k) {
+        s = fmaf(__ldg(a + k), __ldg(b + static_cast<long long>(k) * g.ldb), s);
+        if (s != s) break;
+    }
+    return s;
+}
+
+// Epilogue-wide vote: all 128 epilogue threads synchronise and agree.
+__device__ __forceinline__ bool epi_all(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(v)), "r"(kEpiBarrierId), "r"(kEpiWarps * 32)
+        : "memory");
+    return r != 0;
+}
+
+template <int TM>
+__device__ __forceinline__ void tmem_load_chunk(uint32_t taddr, float (&v)[Cfg<TM>::kChunk]) {
+    if constexpr (Cfg<TM>::kChunk == 32) {
+        uint32_t r[32];
+        tmem_ld32x32(taddr, r);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+    } else {
+        uint32_t r[16];
+        tmem_ld32x16(taddr, r);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
+    }
+}
+
+template <int TM>
+__global__ void __launch_bounds__(kThreads, 1)
+    tf32x3_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ Schedule sch,
+                       const __grid_constant__ DeviceCtl ctl, int vec_a) {
+    using C = Cfg<TM>;
+    constexpr int S = C::kStages;
+    constexpr int CH = C::kChunk;
+    extern __shared__ uint8_t smem_raw[];
+
+    const uint32_t raw_base = smem_u32(smem_raw);
+    const uint32_t base = (raw_base + 1023u) & ~1023u;
+    uint8_t *base_ptr = smem_raw + (base - raw_base);
+    const uint32_t bars = base + S * C::kStageBytes;
+    const uint32_t acc_full0 = bars + 8u * (2 * S);
+    const uint32_t acc_empty0 = acc_full0 + 16u;
+    const uint32_t drain_bar = acc_empty0 + 16u;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(base_ptr + S * C::kStageBytes + 8 * (2 * S + 5));
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    volatile int *s_last = reinterpret_cast<volatile int *>(tmem_slot + 2);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(bars + 8u * s, kProdThreads);  // full: every producer thread arrives
+            mbar_init(bars + 8u * (S + s), 1);       // empty: one tcgen05.commit
+        }
+        mbar_init(acc_full0, 1);
+        mbar_init(acc_full0 + 8u, 1);
+        mbar_init(acc_empty0, kEpiWarps * 32);
+        mbar_init(acc_empty0 + 8u, kEpiWarps * 32);
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        *s_last = 0;
+        fence_mbar_init();
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp < kEpiWarps) {
+        // ------------------------------------------------------ epilogue
+        const int nl = warp * 32 + lane;  // tensor-memory lane = column within the tile
+        int it = 0;
+        for (int u = blockIdx.x; u < sch.units; u += gridDim.x, ++it) {
+            const UnitCoord c = decode_unit(sch, u);
+            const int acc = it & 1;
+            const uint32_t aph = (it >> 1) & 1;
+            const bool w = mbar_wait_bounded(acc_full0 + 8u * acc, aph, abort_flag, ctl,
+                                             kStatusTimeoutEpilogue);
+            if (!epi_all(w)) break;
+            tc_fence_after();
+            const int n = c.nt * kTileN + nl;
+            const int m0 = c.mt * TM;
+            const uint32_t t0 = tmem_base + (static_cast<uint32_t>(warp * 32) << 16) +
+                                static_cast<uint32_t>(acc * TM);
+            if (sch.splits == 1) {
+#pragma unroll 1
+                for (int ch = 0; ch < TM / CH; ++ch) {
+                    float v[CH];
+                    tmem_load_chunk<TM>(t0 + ch * CH, v);
+                    const int mb = m0 + ch * CH;
+                    if (n < g.N) {
+#pragma unroll
+                        for (int j = 0; j < CH; ++j)
+                            if (v[j] != v[j] && mb + j < g.M) v[j] = recompute_dot(g, mb + j, n);
+                        float *cp = g.C + static_cast<long long>(mb) * g.ldc + n;
+                        if (g.beta == 0.f) {
+#pragma unroll
+                            for (int j = 0; j < CH; ++j)
+                                if (mb + j < g.M) cp[j * g.ldc] = g.alpha * v[j];
+                        } else {
+                            float old[CH];
+#pragma unroll
+                            for (int j = 0; j < CH; ++j)
+                                old[j] = (mb + j < g.M) ? cp[j * g.ldc] : 0.f;
+#pragma unroll
+                            for (int j = 0; j < CH; ++j)
+                                if (mb + j < g.M) cp[j * g.ldc] = fmaf(g.beta, old[j], g.alpha * v[j]);
+                        }
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(acc_empty0 + 8u * acc);
+            } else {
+                // split-K: write this slice's partial tile, then the last
+                // slice to arrive adds all partials in slice order
+                constexpr int kTileElems = kTileN * TM;
+                float *wt = ctl.ws + (static_cast<long long>(c.tile) * sch.splits + c.split) * kTileElems;
+#pragma unroll 1
+                for (int ch = 0; ch < TM / CH; ++ch) {
+                    float v[CH];
+                    tmem_load_chunk<TM>(t0 + ch * CH, v);
+#pragma unroll
+                    for (int j = 0; j < CH; ++j) __stcg(wt + (ch * CH + j) * kTileN + nl, v[j]);
+                }
+                tc_fence_before();
+                mbar_arrive(acc_empty0 + 8u * acc);
+                __threadfence();
+                named_bar_sync(kEpiBarrierId, kEpiWarps * 32);
+                if (threadIdx.x == 0) {
+                    const int prev = atomicAdd(ctl.counters + c.tile, 1);
+                    *s_last = (prev == sch.splits - 1) ? 1 : 0;
+                }
+                named_bar_sync(kEpiBarrierId, kEpiWarps * 32);
+                if (*s_last) {
+                    __threadfence();
+                    const float *wb = ctl.ws + static_cast<long long>(c.tile) * sch.splits * kTileElems;
+                    if (n < g.N) {
+#pragma unroll 1
+                        for (int mb = 0; mb < TM; mb += 8) {
+                            float sum[8];
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) sum[j] = 0.f;
+#pragma unroll 1
+                            for (int sp = 0; sp < sch.splits; ++sp) {
+                                const float *p = wb + static_cast<long long>(sp) * kTileElems + mb * kTileN + nl;
+#pragma unroll
+                                for (int j = 0; j < 8; ++j) sum[j] += __ldcg(p + j * kTileN);
+                            }
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                const int m = m0 + mb + j;
+                                if (m < g.M) {
+                                    if (sum[j] != sum[j]) sum[j] = recompute_dot(g, m, n);
+                                    float *cp = g.C + static_cast<long long>(m) * g.ldc + n;
+                                    const float r = g.alpha * sum[j];
+                                    *cp = (g.beta == 0.f) ? r : fmaf(g.beta, *cp, r);
+                                }
+                            }
+                        }
+                    }
+                    if (threadIdx.x == 0) ctl.counters[c.tile] = 0;
+                }
+            }
+        }
+    } else if (warp < kMmaWarp) {
+        // ------------------------------------------------------ producers
+        const int ptid = threadIdx.x - kEpiWarps * 32;
+        constexpr int AJ = C::kAJobs;
+        int s = 0;
+        uint32_t ph = 0;
+        int u = blockIdx.x;
+        if (u < sch.units) {
+            UnitCoord c = decode_unit(sch, u);
+            int kt = c.kb;
+            Raw<AJ> cur;
+            load_raw<TM, AJ>(g, vec_a != 0, c.mt * TM, c.nt * kTileN, kt * kBK, ptid, cur);
+            bool first = true;
+#pragma unroll 1
+            while (true) {
+                int u2 = u;
+                UnitCoord c2 = c;
+                int kt2 = kt + 1;
+                if (kt2 >= c.ke) {
+                    u2 = u + gridDim.x;
+                    if (u2 < sch.units) {
+                        c2 = decode_unit(sch, u2);
+                        kt2 = c2.kb;
+                    }
+                }
+                const bool have2 = u2 < sch.units;
+                Raw<AJ> nxt;
+                if (have2) load_raw<TM, AJ>(g, vec_a != 0, c2.mt * TM, c2.nt * kTileN, kt2 * kBK, ptid, nxt);
+                if (!mbar_wait_bounded(bars + 8u * (S + s), ph ^ 1u, abort_flag, ctl,
+                                       kStatusTimeoutProducer))
+                    break;
+                store_split<TM, AJ>(base + s * C::kStageBytes, ptid, cur);
+                fence_proxy_async_smem();
+                const bool withhold = first && (ctl.debug_flags & kDebugWithholdArrive) && ptid == 0;
+                if (!withhold) mbar_arrive(bars + 8u * s);
+                first = false;
+                if (++s == S) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+                if (!have2) break;
+                u = u2;
+                c = c2;
+                kt = kt2;
+                cur = nxt;
+            }
+        }
+    } else if (lane == 0) {
+        // ------------------------------------------------------ MMA issuer
+        int s = 0;
+        uint32_t ph = 0;
+        int it = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < sch.units && ok; u += gridDim.x, ++it) {
+            const UnitCoord c = decode_unit(sch, u);
+            const int acc = it & 1;
+            const uint32_t aph = (it >> 1) & 1;
+            if (!mbar_wait_bounded(acc_empty0 + 8u * acc, aph ^ 1u, abort_flag, ctl, kStatusTimeoutMma)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t d = tmem_base + static_cast<uint32_t>(acc * TM);
+            for (int kt = c.kb; kt < c.ke; ++kt) {
+                if (!mbar_wait_bounded(bars + 8u * s, ph, abort_flag, ctl, kStatusTimeoutMma)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t st = base + s * C::kStageBytes;
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const uint64_t a_hi = umma_desc_kmajor_sw64(st + C::kOffBtHi + j * 32);
+                    const uint64_t a_lo = umma_desc_kmajor_sw64(st + C::kOffBtLo + j * 32);
+                    const uint64_t b_hi = umma_desc_kmajor_sw64(st + C::kOffAHi + j * 32);
+                    const uint64_t b_lo = umma_desc_kmajor_sw64(st + C::kOffALo + j * 32);
+                    mma_tf32_ss(d, a_lo, b_hi, C::kIdesc, (kt != c.kb || j != 0) ? 1u : 0u);
+                    mma_tf32_ss(d, a_hi, b_lo, C::kIdesc, 1u);
+                    mma_tf32_ss(d, a_hi, b_hi, C::kIdesc, 1u);
+                }
+                mma_commit(bars + 8u * (S + s));
+                if (++s == S) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+            if (!ok) break;
+            mma_commit(acc_full0 + 8u * acc);
+        }
+        // every MMA this thread issued has finished once the drain arrives
+        mma_commit(drain_bar);
+        volatile int no_abort = 0;
+        mbar_wait_bounded(drain_bar, 0u, &no_abort, ctl, kStatusTimeoutDrain);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, C::kTmemCols);
+    }
+}
+
+}  // namespace tf32x3
+}  // namespace sg

@@ -1,0 +1,166 @@
+/*
+ * sgemm_gb300.h - C ABI of the GB300 (sm_103a) single-precision GEMM library.
+ *
+ * The operation is the problem statement mysgemm(M, N, K, alpha, A, B, beta,
+ * C) of "NVIDIA_SGEMM_PRACTICE" (section "kernel 1", and the launch comment
+ * of section "kernel 2"):
+ *
+ *     C[m][n] = alpha * sum_{k<K} A[m][k] * B[k][n] + beta * C[m][n]
+ *
+ * on row-major float32 matrices: A is M x K, B is K x N, C is M x N.  The
+ * pages use packed matrices; here each matrix has a leading dimension (the
+ * distance in elements between consecutive rows), so the pages' case is
+ * lda = K, ldb = N, ldc = N.
+ *
+ * Conventions shared by every entry point below:
+ *   - A, B, C are device pointers owned by the caller (except sgemm_host).
+ *     The library never frees or retains them beyond the call.
+ *   - Calls are asynchronous on `stream` (NULL = the legacy default stream)
+ *     unless stated otherwise.
+ *   - Return value: 0 on success; -i when the i-th argument (1-based) is
+ *     invalid; a positive cudaError_t value when a CUDA call fails; or one of
+ *     the SGEMM_ERR_* codes (all > 10000).
+ *   - Argument rules: M, N, K >= 0; lda >= max(1, K); ldb >= max(1, N);
+ *     ldc >= max(1, N); A and B must be non-NULL when alpha != 0 and K > 0;
+ *     C must be non-NULL when M > 0 and N > 0; C must not overlap A or B.
+ *   - Quick returns: M == 0 or N == 0 does nothing.  alpha == 0 or K == 0
+ *     computes C = beta * C without reading A or B.  beta == 0 makes C
+ *     write-only: its old contents (NaN included) never reach the result.
+ *   - Results are deterministic: the same call on the same device gives the
+ *     same bits every time (no floating-point atomics).
+ *   - Accuracy: every element lies within
+ *     1e-4 * (|alpha| * sum_k |A[m][k] * B[k][n]| + |beta * C[m][n]|)
+ *     of the exact result, on every path.
+ *   - Calls from several host threads on different streams are safe.
+ */
+#ifndef SGEMM_GB300_H
+#define SGEMM_GB300_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; declared here so that this header does not
+ * need the CUDA headers. */
+struct CUstream_st;
+typedef struct CUstream_st *sgemm_stream_t;
+
+/* Status codes beyond 0 / -i / cudaError_t. */
+#define SGEMM_ERR_DEVICE_TIMEOUT     10001 /* a bounded on-device wait gave up */
+#define SGEMM_ERR_NO_DEVICE          10002 /* no CUDA device is usable        */
+#define SGEMM_ERR_UNSUPPORTED_DEVICE 10003 /* device is not compute 10.3     */
+#define SGEMM_ERR_WORKSPACE          10004 /* split-K workspace unavailable   */
+#define SGEMM_ERR_INTERNAL           10005 /* planner found no kernel         */
+
+/* Algorithm selector for sgemm_ex / sgemm_host. */
+#define SGEMM_ALGO_AUTO   0 /* planner picks the faster path                  */
+#define SGEMM_ALGO_FFMA   1 /* register-blocked fp32 FMA on the CUDA cores    */
+#define SGEMM_ALGO_TF32X3 2 /* tcgen05 tensor cores, fp32 split into hi + lo
+                               tf32 parts, hi*hi + hi*lo + lo*hi accumulated
+                               in fp32 in tensor memory                        */
+
+/* Flags for sgemm_ex. */
+#define SGEMM_FLAG_DEBUG_WITHHOLD_ARRIVE 1 /* test only: one pipeline arrive
+                                              is withheld and the on-device
+                                              wait budget is cut to ~1 ms, so
+                                              the bounded wait runs out; the
+                                              call then reports
+                                              SGEMM_ERR_DEVICE_TIMEOUT through
+                                              sgemm_check_status and C is
+                                              unspecified                      */
+
+/*
+ * sgemm - C = alpha * A * B + beta * C, planner-chosen path.
+ *
+ * Arguments 1-12 in the order of the problem statement, with leading
+ * dimensions after each matrix and the stream last.  Same as
+ * sgemm_ex(..., SGEMM_ALGO_AUTO, 0, 0).
+ */
+int sgemm(int M, int N, int K, float alpha,
+          const float *A, int lda,
+          const float *B, int ldb,
+          float beta, float *C, int ldc,
+          sgemm_stream_t stream);
+
+/*
+ * sgemm_ex - as sgemm, with explicit choices.
+ *
+ *   algo   (13): SGEMM_ALGO_AUTO / _FFMA / _TF32X3.
+ *   splits (14): 0 = planner's choice; s >= 1 forces s slices of K (clamped
+ *                to the number of K tiles).  With s > 1 each slice writes a
+ *                partial tile to a library-owned workspace and the last slice
+ *                to finish adds the partials in slice order, so the result
+ *                does not depend on timing.
+ *   flags  (15): 0, or SGEMM_FLAG_DEBUG_WITHHOLD_ARRIVE (tests only).
+ *
+ * The split-K workspace is owned by the library, kept per device and stream,
+ * grown on demand (a synchronous cudaMalloc, so make the first call of a
+ * given size outside stream capture) and released by sgemm_release().
+ */
+int sgemm_ex(int M, int N, int K, float alpha,
+             const float *A, int lda,
+             const float *B, int ldb,
+             float beta, float *C, int ldc,
+             sgemm_stream_t stream, int algo, int splits, int flags);
+
+/*
+ * sgemm_host - C = alpha * A * B + beta * C on HOST buffers, synchronous.
+ *
+ * A, B, C are host pointers (pinned memory gives full copy bandwidth).  The
+ * call copies A, B (and C when beta != 0) to library-owned device buffers on
+ * the current device, runs the GEMM, copies C back and waits for completion.
+ * Same argument rules and return codes as sgemm_ex; algo as in sgemm_ex.
+ * The device buffers are kept for reuse and freed by sgemm_release().
+ */
+int sgemm_host(int M, int N, int K, float alpha,
+               const float *A, int lda,
+               const float *B, int ldb,
+               float beta, float *C, int ldc, int algo);
+
+/*
+ * sgemm_plan_info - what the planner would launch, without launching.
+ *
+ * Host-only: makes no CUDA call when num_sms > 0 (num_sms = 0 queries the
+ * current device).  Arguments as in sgemm_ex; the pointers are only used for
+ * alignment and may be any values.  Writes up to `ninfo` ints to `info`:
+ *   [0] path (SGEMM_ALGO_FFMA or SGEMM_ALGO_TF32X3)
+ *   [1] tile rows of C      [2] tile columns of C
+ *   [3] K splits            [4] work units (tiles * splits)
+ *   [5] grid size (CTAs)    [6] pipeline stages
+ *   [7] 1 if A is read with 16-byte vector loads
+ *   [8] 1 if B is read with 16-byte vector loads
+ *   [9] workspace bytes needed
+ * Returns 0, or -i for an invalid argument (same numbering as sgemm_ex,
+ * ninfo = 17, info = 16, num_sms = 15).
+ */
+int sgemm_plan_info(int M, int N, int K, const void *A, int lda,
+                    const void *B, int ldb, const void *C, int ldc,
+                    int algo, int splits, float alpha, float beta,
+                    int num_sms, int *info, int ninfo);
+
+/*
+ * sgemm_check_status - wait for `stream`, then read and clear the device
+ * status word of the current device.  Returns 0, SGEMM_ERR_DEVICE_TIMEOUT if
+ * a kernel launched since the last check gave up a bounded wait, or a
+ * positive cudaError_t.
+ */
+int sgemm_check_status(sgemm_stream_t stream);
+
+/* sgemm_status_string - static, human-readable text for any return code. */
+const char *sgemm_status_string(int status);
+
+/*
+ * sgemm_release - free every library-owned device buffer (workspaces, host
+ * call staging buffers) on all devices.  Waits for the device first.  Not
+ * safe while another thread is inside a call of this library.
+ */
+int sgemm_release(void);
+
+/* sgemm_version - library version as 10000*major + 100*minor + patch. */
+int sgemm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SGEMM_GB300_H */

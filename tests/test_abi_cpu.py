@@ -1,0 +1,142 @@
+"""Host-side checks of the C ABI that need no GPU.
+
+The library must load and export every function the header declares;
+invalid arguments are rejected with -i (1-based, LAPACK style) before any
+CUDA call; empty problems return 0 without touching the device; the planner
+(sgemm_plan_info with an explicit SM count) makes the documented choices.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import pytest
+
+import dense_fp32_matrix_05_gb300 as pkg
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+    __graft_entry__.build()
+    return pkg.library()
+
+
+def test_exports_every_declared_symbol(lib):
+    declared = pkg.declared_functions()
+    assert {"sgemm", "sgemm_ex", "sgemm_host", "sgemm_plan_info", "sgemm_check_status",
+            "sgemm_status_string", "sgemm_release", "sgemm_version"} <= set(declared)
+    raw = ctypes.CDLL(pkg.lib_path())
+    for name in declared:
+        assert hasattr(raw, name), f"{name} declared in the header but not exported"
+
+
+def test_version(lib):
+    assert pkg.sgemm_version() >= 100
+
+
+FAKE = 1 << 20  # never dereferenced: every call below returns before any CUDA call
+
+
+@pytest.mark.parametrize("args,code", [
+    ((-1, 4, 4, 1.0, FAKE, 4, FAKE, 4, 0.0, FAKE, 4), -1),
+    ((4, -1, 4, 1.0, FAKE, 4, FAKE, 4, 0.0, FAKE, 4), -2),
+    ((4, 4, -1, 1.0, FAKE, 4, FAKE, 4, 0.0, FAKE, 4), -3),
+    ((4, 4, 4, 1.0, FAKE, 3, FAKE, 4, 0.0, FAKE, 4), -6),
+    ((4, 4, 0, 1.0, FAKE, 0, FAKE, 4, 0.0, FAKE, 4), -6),
+    ((4, 4, 4, 1.0, FAKE, 4, FAKE, 3, 0.0, FAKE, 4), -8),
+    ((4, 4, 4, 1.0, FAKE, 4, FAKE, 4, 0.0, FAKE, 3), -11),
+    ((4, 4, 4, 1.0, None, 4, FAKE, 4, 0.0, FAKE + 4096, 4), -5),
+    ((4, 4, 4, 1.0, FAKE, 4, None, 4, 0.0, FAKE + 4096, 4), -7),
+    ((4, 4, 4, 1.0, FAKE, 4, FAKE + 4096, 4, 0.0, None, 4), -10),
+    # C overlapping A / B
+    ((4, 4, 4, 1.0, FAKE, 4, FAKE + 4096, 4, 0.0, FAKE + 16, 4), -10),
+    ((4, 4, 4, 1.0, FAKE, 4, FAKE + 4096, 4, 0.0, FAKE + 4096 + 60, 4), -10),
+])
+def test_invalid_arguments(lib, args, code):
+    assert pkg.sgemm(*args) == code
+    assert pkg.sgemm_ex(*args, None, 0, 0, 0) == code
+
+
+def test_invalid_extended_arguments(lib):
+    base = (4, 4, 4, 1.0, FAKE, 4, FAKE + 4096, 4, 0.0, FAKE + 8192, 4, None)
+    assert pkg.sgemm_ex(*base, 3, 0, 0) == -13
+    assert pkg.sgemm_ex(*base, -1, 0, 0) == -13
+    assert pkg.sgemm_ex(*base, 0, -1, 0) == -14
+    assert pkg.sgemm_ex(*base, 0, 0, 2) == -15
+
+
+def test_empty_problems_need_no_device(lib):
+    assert pkg.sgemm(0, 5, 5, 1.0, None, 5, None, 5, 0.0, None, 5) == 0
+    assert pkg.sgemm(5, 0, 5, 1.0, None, 5, None, 1, 0.0, None, 1) == 0
+    assert pkg.sgemm_host(0, 5, 5, 1.0, None, 5, None, 5, 0.0, None, 5) == 0
+
+
+def test_no_ab_needed_when_alpha_zero_validation(lib):
+    # alpha == 0: A and B may be NULL; with M == 0 the call is a no-op
+    assert pkg.sgemm(0, 4, 4, 0.0, None, 4, None, 4, 1.0, None, 4) == 0
+
+
+def test_status_strings(lib):
+    assert pkg.sgemm_status_string(0) == "success"
+    assert "argument 6" in pkg.sgemm_status_string(-6)
+    assert "wait" in pkg.sgemm_status_string(pkg.SGEMM_ERR_DEVICE_TIMEOUT)
+    assert pkg.sgemm_status_string(987654) == "unknown status"
+
+
+SMS = 152
+
+
+def plan(M, N, K, **kw):
+    kw.setdefault("num_sms", SMS)
+    return pkg.sgemm_plan_info(M, N, K, A=0x100000, B=0x200000, C=0x300000, **kw)
+
+
+def test_plan_large_square_uses_tensor_path_without_split():
+    p = plan(5120, 5120, 5120)
+    assert p["path"] == pkg.SGEMM_ALGO_TF32X3
+    assert (p["tile_m"], p["tile_n"]) == (256, 128)
+    assert p["splits"] == 1 and p["units"] == 20 * 40 and p["grid"] == SMS
+    assert p["vec_a"] == 1 and p["vec_b"] == 1 and p["ws_bytes"] == 0
+
+
+def test_plan_small_square_splits_k():
+    p = plan(1024, 1024, 1024)
+    assert p["splits"] > 1
+    assert p["units"] <= SMS
+    assert p["ws_bytes"] == p["units"] * p["tile_m"] * p["tile_n"] * 4
+
+
+def test_plan_skinny_shapes_pick_matching_tile_rows():
+    assert plan(32, 1605632, 27)["tile_m"] == 32
+    assert plan(64, 559104, 147)["tile_m"] == 64
+    assert plan(384, 14161, 1152)["tile_m"] == 192
+    assert plan(256, 50176, 1024)["tile_m"] == 256
+
+
+def test_plan_alignment_detection():
+    p = pkg.sgemm_plan_info(64, 64, 27, A=0x100000, lda=27, B=0x200004, C=0x300000,
+                            num_sms=SMS)
+    assert p["vec_a"] == 0 and p["vec_b"] == 0
+    p = pkg.sgemm_plan_info(64, 64, 28, A=0x100000, lda=28, B=0x200000, C=0x300000,
+                            num_sms=SMS)
+    assert p["vec_a"] == 1 and p["vec_b"] == 1
+
+
+def test_plan_forced_splits_are_clamped():
+    p = plan(512, 512, 64, splits=100)
+    assert p["splits"] == 4  # 64 / 16 K tiles
+    p = plan(512, 512, 64, splits=100, algo=pkg.SGEMM_ALGO_FFMA)
+    assert p["splits"] == 4
+
+
+def test_plan_ffma_tiles():
+    assert (plan(32, 4096, 64, algo=1)["tile_m"], plan(32, 4096, 64, algo=1)["tile_n"]) == (32, 512)
+    assert plan(64, 4096, 64, algo=1)["tile_n"] == 256
+    assert plan(4096, 4096, 4096, algo=1)["tile_n"] == 128
+
+
+def test_plan_info_rejects_bad_arguments():
+    with pytest.raises(pkg.SgemmError):
+        pkg.sgemm_plan_info(-1, 4, 4, num_sms=SMS)
+    with pytest.raises(pkg.SgemmError):
+        pkg.sgemm_plan_info(4, 4, 4, algo=7, num_sms=SMS)

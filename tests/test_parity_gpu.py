@@ -1,0 +1,254 @@
+"""GPU parity: every path, through the C ABI, against the float64 oracle.
+
+Acceptance rule (per element, both paths):
+    |gpu - ref| <= 1e-4 * (|alpha| * sum_k |a_mk b_kn| + |beta c_mn|)
+Small cases (ragged, several tiles, alignment and leading-dimension
+variants) are checked on every element; the full-size workloads (square
+5120, the six im2col shapes, the square sweep) on sampled rows, in the same
+launch configuration the benchmark times.  Guard bands around A, B, C and
+the ld padding of C must stay untouched; A and B must not change.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import dense_fp32_matrix_05_gb300 as pkg
+import oracle
+from dense_fp32_matrix_05_gb300.workloads import (SKINNY_SHAPES, SWEEP_SIZES, WORKLOADS,
+                                                  make_problem, random_problem, uniform)
+from gpu_util import check_against_oracle, run_sgemm, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+ALGOS = [pkg.SGEMM_ALGO_TF32X3, pkg.SGEMM_ALGO_FFMA]
+ALGO_IDS = ["tf32x3", "ffma"]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def gpu_ready():
+    import torch
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+    yield
+    torch.cuda.synchronize()
+
+
+def _with_c(p, seed=99):
+    if p.beta != 0:
+        p.C[:, :p.N] = uniform(np.random.default_rng(seed), p.M * p.N).reshape(p.M, p.N)
+    return p
+
+
+SMALL_SHAPES = [(1, 1, 1), (2, 3, 4), (7, 9, 5), (16, 16, 16), (17, 15, 33), (31, 33, 17),
+                (63, 65, 64), (65, 63, 129), (127, 129, 31), (128, 128, 128), (129, 127, 65),
+                (200, 300, 77), (257, 130, 160), (33, 515, 20), (300, 1, 40), (1, 300, 40)]
+
+
+@pytest.mark.parametrize("algo", ALGOS, ids=ALGO_IDS)
+@pytest.mark.parametrize("shape", SMALL_SHAPES, ids=[f"{m}x{n}x{k}" for m, n, k in SMALL_SHAPES])
+def test_small_ragged_shapes(algo, shape):
+    M, N, K = shape
+    p = _with_c(random_problem(M, N, K, alpha=1.5, beta=0.5, seed=M * 10007 + N * 101 + K))
+    C, st = run_sgemm(p, algo)
+    assert st == 0
+    check_against_oracle(p, C, what=f"{shape} algo={algo}")
+
+
+LAYOUTS = {
+    "packed": dict(ld=(0, 0, 0), off=(0, 0, 0)),
+    "odd_ld": dict(ld=(1, 3, 5), off=(0, 0, 0)),
+    "ld_plus4": dict(ld=(4, 4, 4), off=(0, 0, 0)),
+    "misaligned_ptrs": dict(ld=(0, 0, 0), off=(1, 3, 2)),
+    "odd_ld_misaligned": dict(ld=(3, 1, 7), off=(2, 1, 3)),
+}
+
+
+@pytest.mark.parametrize("algo", ALGOS, ids=ALGO_IDS)
+@pytest.mark.parametrize("layout", list(LAYOUTS))
+@pytest.mark.parametrize("shape", [(100, 130, 36), (130, 260, 129), (33, 700, 27)])
+def test_leading_dimensions_and_alignment(algo, layout, shape):
+    M, N, K = shape
+    L = LAYOUTS[layout]
+    p = _with_c(random_problem(M, N, K, alpha=-0.75, beta=1.25, seed=M + N + K,
+                               lda=K + L["ld"][0], ldb=N + L["ld"][1], ldc=N + L["ld"][2]))
+    C, st = run_sgemm(p, algo, offsets=L["off"])
+    assert st == 0
+    check_against_oracle(p, C, what=f"{shape} {layout} algo={algo}")
+
+
+@pytest.mark.parametrize("algo", ALGOS, ids=ALGO_IDS)
+@pytest.mark.parametrize("splits", [1, 2, 3, 7])
+def test_forced_split_k(algo, splits):
+    p = _with_c(random_problem(129, 257, 1000, alpha=1.0, beta=0.5, seed=5))
+    C, st = run_sgemm(p, algo, splits=splits)
+    assert st == 0
+    check_against_oracle(p, C, what=f"splits={splits} algo={algo}")
+
+
+@pytest.mark.parametrize("algo", ALGOS, ids=ALGO_IDS)
+@pytest.mark.parametrize("name", ["square256", "square1024", "ragged1023x1021x1025"])
+def test_small_configs_full(algo, name):
+    p = make_problem(name, pad_value=0.0)
+    C, st = run_sgemm(p, algo)
+    assert st == 0
+    check_against_oracle(p, C, what=f"{name} algo={algo}")
+
+
+@pytest.mark.parametrize("algo", [pkg.SGEMM_ALGO_AUTO, pkg.SGEMM_ALGO_FFMA], ids=["auto", "ffma"])
+def test_square5120_sampled(algo):
+    p = make_problem("square5120", pad_value=0.0)
+    C, st = run_sgemm(p, algo)
+    assert st == 0
+    check_against_oracle(p, C, rows=sample_rows(p.M, 48, seed=1), what=f"square5120 algo={algo}")
+
+
+@pytest.mark.parametrize("algo", [pkg.SGEMM_ALGO_AUTO, pkg.SGEMM_ALGO_FFMA], ids=["auto", "ffma"])
+@pytest.mark.parametrize("shape", SKINNY_SHAPES, ids=[f"{m}x{n}x{k}" for m, n, k in SKINNY_SHAPES])
+def test_skinny_shapes_sampled(algo, shape):
+    M, N, K = shape
+    p = make_problem(f"skinny{M}x{N}x{K}", pad_value=0.0)
+    C, st = run_sgemm(p, algo)
+    assert st == 0
+    check_against_oracle(p, C, rows=sample_rows(M, 24, seed=2), what=f"{shape} algo={algo}")
+
+
+@pytest.mark.parametrize("size", SWEEP_SIZES)
+def test_sweep_sampled(size):
+    p = make_problem(f"sweep{size}", pad_value=0.0)
+    for algo in (pkg.SGEMM_ALGO_AUTO, pkg.SGEMM_ALGO_FFMA):
+        C, st = run_sgemm(p, algo)
+        assert st == 0
+        check_against_oracle(p, C, rows=sample_rows(p.M, 12, seed=3), what=f"sweep{size} algo={algo}")
+
+
+@pytest.mark.parametrize("algo", ALGOS, ids=ALGO_IDS)
+def test_deterministic_bits(algo):
+    p = make_problem("square1024", pad_value=0.0)
+    C1, _ = run_sgemm(p, algo)
+    C2, _ = run_sgemm(p, algo)
+    assert np.array_equal(C1.view(np.uint32), C2.view(np.uint32))
+
+
+@pytest.mark.parametrize("algo", ALGOS, ids=ALGO_IDS)
+@pytest.mark.parametrize("beta", [0.0, 1.0])
+def test_small_integers_exact(algo, beta):
+    rng = np.random.default_rng(31)
+    M, N, K = 130, 260, 300
+    p = random_problem(M, N, K, alpha=1.0, beta=beta, seed=1, pad_value=0.0)
+    Ai = rng.integers(-8, 9, size=(M, K))
+    Bi = rng.integers(-8, 9, size=(K, N))
+    Ci = rng.integers(-8, 9, size=(M, N))
+    p.A[:] = Ai
+    p.B[:] = Bi
+    p.C[:] = Ci
+    C, st = run_sgemm(p, algo)
+    assert st == 0
+    want = Ai @ Bi + (Ci if beta else 0)
+    assert np.array_equal(C, want.astype(np.float32))
+
+
+@pytest.mark.parametrize("algo", ALGOS, ids=ALGO_IDS)
+def test_beta_zero_ignores_nan_c(algo):
+    p = random_problem(150, 140, 50, alpha=2.0, beta=0.0, seed=3, pad_value=0.0)
+    p.C[:] = np.nan
+    C, st = run_sgemm(p, algo)
+    assert st == 0 and np.all(np.isfinite(C))
+    check_against_oracle(p, C, what="beta=0, C=NaN")
+
+
+@pytest.mark.parametrize("alpha,K", [(0.0, 40), (1.0, 0)])
+@pytest.mark.parametrize("beta", [0.0, 1.0, -2.5])
+def test_alpha_or_k_zero(alpha, K, beta):
+    M, N = 70, 90
+    p = random_problem(M, N, max(K, 1), alpha=alpha, beta=beta, seed=4, pad_value=np.nan)
+    p.K = K
+    p.A[:] = np.nan
+    p.B[:] = np.nan
+    p.C[:, :N] = uniform(np.random.default_rng(5), M * N).reshape(M, N)
+    C, st = run_sgemm(p)
+    assert st == 0
+    want = (beta * p.C[:, :N]) if beta != 0 else np.zeros((M, N), np.float32)
+    assert np.array_equal(C[:, :N], want.astype(np.float32))
+
+
+@pytest.mark.parametrize("algo", ALGOS, ids=ALGO_IDS)
+def test_special_values(algo):
+    M, N, K = 40, 48, 37
+    p = random_problem(M, N, K, alpha=1.0, beta=0.5, seed=6, pad_value=0.0)
+    p.C[:, :N] = uniform(np.random.default_rng(7), M * N).reshape(M, N)
+    # partners that are exact tf32 values (their lo part is zero)
+    p.B[3, :] = 0.5
+    p.A[:, 9] = -2.0
+    p.A[0, 3] = np.inf            # row 0: +-Inf wherever B[3, n] != 0
+    p.A[1, 5] = np.nan            # row 1: NaN
+    p.B[9, 7] = -np.inf           # column 7: -Inf * -2 = +Inf except rows 0 (Inf*0.5 + Inf)
+    p.A[2, 0] = np.float32(3.0e37)
+    p.A[4, :] = 0.0
+    p.A[4, 2] = -0.0
+    p.A[5, 1] = np.float32(1e-40)  # subnormal among normal terms
+    p.B[1, 11] = np.float32(1e-39)
+    p.C[6, 13] = np.nan            # beta * NaN = NaN
+    C, st = run_sgemm(p, algo)
+    assert st == 0
+    check_against_oracle(p, C, what=f"special values algo={algo}")
+
+
+def test_timeout_is_reported_and_recoverable():
+    """A withheld pipeline arrive makes the bounded wait run out: the call
+    reports SGEMM_ERR_DEVICE_TIMEOUT and the next call works normally."""
+    p = random_problem(256, 256, 256, alpha=1.0, beta=0.0, seed=8, pad_value=0.0)
+    _, st = run_sgemm(p, pkg.SGEMM_ALGO_TF32X3, flags=pkg.SGEMM_FLAG_DEBUG_WITHHOLD_ARRIVE)
+    assert st == pkg.SGEMM_ERR_DEVICE_TIMEOUT
+    C, st = run_sgemm(p, pkg.SGEMM_ALGO_TF32X3)
+    assert st == 0
+    check_against_oracle(p, C, what="after timeout")
+    C, st = run_sgemm(p, pkg.SGEMM_ALGO_TF32X3, splits=4)
+    assert st == 0
+    check_against_oracle(p, C, what="split-K after timeout")
+
+
+@pytest.mark.parametrize("algo", [pkg.SGEMM_ALGO_AUTO, pkg.SGEMM_ALGO_FFMA], ids=["auto", "ffma"])
+def test_host_entry_point(algo):
+    import torch
+    p = _with_c(random_problem(300, 200, 150, alpha=1.5, beta=0.5, seed=9, pad_value=0.0))
+    A = torch.from_numpy(p.A).pin_memory()
+    B = torch.from_numpy(p.B).pin_memory()
+    C = torch.from_numpy(p.C.copy()).pin_memory()
+    rc = pkg.sgemm_host(p.M, p.N, p.K, p.alpha, A.data_ptr(), p.lda, B.data_ptr(), p.ldb, p.beta,
+                        C.data_ptr(), p.ldc, algo)
+    assert rc == 0
+    check_against_oracle(p, C.numpy(), what=f"sgemm_host algo={algo}")
+    # pageable numpy buffers work too
+    Cn = p.C.copy()
+    assert pkg.sgemm_host(p.M, p.N, p.K, p.alpha, p.A, p.lda, p.B, p.ldb, p.beta, Cn, p.ldc, algo) == 0
+    check_against_oracle(p, Cn, what="sgemm_host pageable")
+
+
+def test_torch_matmul_and_streams():
+    import torch
+    a = torch.rand(513, 257, device="cuda") - 0.5
+    b = torch.rand(257, 1025, device="cuda") - 0.5
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        c = pkg.matmul(a, b)
+    s.synchronize()
+    ref, scale = oracle.sgemm_ref(513, 1025, 257, 1.0, a.cpu().numpy(), 257, b.cpu().numpy(), 1025,
+                                  0.0, None, 1025)
+    assert not oracle.first_failures(c.cpu().numpy(), ref, scale)
+    # column slices (ld > cols) through the tensor API
+    big = torch.rand(300, 700, device="cuda")
+    sub = big[:, 50:350]
+    cs = pkg.matmul(sub, b[:300, :64].contiguous())
+    ref, scale = oracle.sgemm_ref(300, 64, 300, 1.0, big.cpu().numpy()[:, 50:350].copy(), 300,
+                                  b[:300, :64].cpu().numpy().copy(), 64, 0.0, None, 64)
+    assert not oracle.first_failures(cs.cpu().numpy(), ref, scale)
+
+
+def test_plan_info_on_device_matches_sm_count():
+    import torch
+    props = torch.cuda.get_device_properties(0)
+    info = pkg.sgemm_plan_info(5120, 5120, 5120, num_sms=0)
+    assert info["grid"] == min(info["units"], props.multi_processor_count)
