@@ -84,17 +84,17 @@ __device__ __forceinline__ uint32_t sw64_off(int row, int chunk) {
     return static_cast<uint32_t>(row * 64 + (((chunk ^ (row >> 1)) & 3) << 4));
 }
 
-// hi/lo split of one fp32 value (bit patterns of two exact tf32 values).
-// Non-finite x: hi keeps x (a NaN keeps a high mantissa bit, so the tensor
-// core still sees a NaN), lo = 0 (so Inf - Inf cannot create a NaN).
+// hi/lo split of one fp32 value: hi = x with the low 13 mantissa bits
+// cleared (an exact tf32 value, so the tensor core's own rounding of its
+// inputs never matters), lo = x - hi (exact in fp32; |lo| < 2^-10 |x|, the
+// tensor core keeps its top 11 significant bits, an error below 2^-20 |x|).
+// Non-finite x gives lo = NaN; the accumulator then comes out NaN and the
+// epilogue recomputes that element exactly (recompute_dot), so Inf and NaN
+// inputs still produce the IEEE fp32 result.  One logic op and one FADD.
 __device__ __forceinline__ void split_tf32(float x, uint32_t &hi, uint32_t &lo) {
-    const uint32_t u = __float_as_uint(x);
-    const uint32_t hu = u & 0xFFFFE000u;
-    const float rest = x - __uint_as_float(hu);  // exact
-    const uint32_t lu = (__float_as_uint(rest) + 0x1000u) & 0xFFFFE000u;  // round |rest| to tf32
-    const bool nonfinite = (u & 0x7F800000u) == 0x7F800000u;
-    hi = nonfinite ? (u | ((u & 0x007FFFFFu) ? 0x00400000u : 0u)) : hu;
-    lo = nonfinite ? 0u : lu;
+    const uint32_t hu = __float_as_uint(x) & 0xFFFFE000u;
+    hi = hu;
+    lo = __float_as_uint(x - __uint_as_float(hu));
 }
 
 template <int AJ>
@@ -190,6 +190,26 @@ __device__ __noinline__ float recompute_dot(const GemmArgs &g, int m, int n) {
     }
     return s;
 }
+
+// The (work unit, k tile) jobs of one CTA, in the order the producers fill
+// the pipeline: units blockIdx.x, blockIdx.x + gridDim.x, ..., each from its
+// first to its last k tile.
+struct JobIter {
+    int u;
+    UnitCoord c;
+    int kt;
+    __device__ __forceinline__ void start(const Schedule &s, int u0) {
+        u = u0;
+        if (u < s.units) {
+            c = decode_unit(s, u);
+            kt = c.kb;
+        }
+    }
+    __device__ __forceinline__ bool valid(const Schedule &s) const { return u < s.units; }
+    __device__ __forceinline__ void advance(const Schedule &s) {
+        if (++kt >= c.ke) start(s, u + static_cast<int>(gridDim.x));
+    }
+};
 
 // Epilogue-wide vote: all 128 epilogue threads synchronise and agree.
 __device__ __forceinline__ bool epi_all(bool v) {
@@ -364,49 +384,52 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp < kMmaWarp) {
         // ------------------------------------------------------ producers
+        // Jobs are the (unit, k tile) pairs of this CTA in order.  Three
+        // register buffers rotate: while one job is split into shared memory
+        // the loads of the next two are in flight.
         const int ptid = threadIdx.x - kEpiWarps * 32;
         constexpr int AJ = C::kAJobs;
         int s = 0;
         uint32_t ph = 0;
-        int u = blockIdx.x;
-        if (u < sch.units) {
-            UnitCoord c = decode_unit(sch, u);
-            int kt = c.kb;
-            Raw<AJ> cur;
-            load_raw<TM, AJ>(g, vec_a != 0, c.mt * TM, c.nt * kTileN, kt * kBK, ptid, cur);
-            bool first = true;
+        JobIter next;
+        next.start(sch, blockIdx.x);
+        Raw<AJ> buf[3];
+        int loaded = 0, done = 0;
+#pragma unroll
+        for (int i = 0; i < 3; ++i) {
+            if (next.valid(sch)) {
+                load_raw<TM, AJ>(g, vec_a != 0, next.c.mt * TM, next.c.nt * kTileN, next.kt * kBK, ptid, buf[i]);
+                next.advance(sch);
+                ++loaded;
+            }
+        }
+        bool ok = true;
 #pragma unroll 1
-            while (true) {
-                int u2 = u;
-                UnitCoord c2 = c;
-                int kt2 = kt + 1;
-                if (kt2 >= c.ke) {
-                    u2 = u + gridDim.x;
-                    if (u2 < sch.units) {
-                        c2 = decode_unit(sch, u2);
-                        kt2 = c2.kb;
+        while (ok && done < loaded) {
+#pragma unroll
+            for (int i = 0; i < 3; ++i) {
+                if (done < loaded) {
+                    if (!mbar_wait_bounded(bars + 8u * (S + s), ph ^ 1u, abort_flag, ctl,
+                                           kStatusTimeoutProducer)) {
+                        ok = false;
+                        break;
+                    }
+                    store_split<TM, AJ>(base + s * C::kStageBytes, ptid, buf[i]);
+                    fence_proxy_async_smem();
+                    const bool withhold = done == 0 && (ctl.debug_flags & kDebugWithholdArrive) && ptid == 0;
+                    if (!withhold) mbar_arrive(bars + 8u * s);
+                    ++done;
+                    if (++s == S) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                    if (next.valid(sch)) {
+                        load_raw<TM, AJ>(g, vec_a != 0, next.c.mt * TM, next.c.nt * kTileN, next.kt * kBK, ptid,
+                                         buf[i]);
+                        next.advance(sch);
+                        ++loaded;
                     }
                 }
-                const bool have2 = u2 < sch.units;
-                Raw<AJ> nxt;
-                if (have2) load_raw<TM, AJ>(g, vec_a != 0, c2.mt * TM, c2.nt * kTileN, kt2 * kBK, ptid, nxt);
-                if (!mbar_wait_bounded(bars + 8u * (S + s), ph ^ 1u, abort_flag, ctl,
-                                       kStatusTimeoutProducer))
-                    break;
-                store_split<TM, AJ>(base + s * C::kStageBytes, ptid, cur);
-                fence_proxy_async_smem();
-                const bool withhold = first && (ctl.debug_flags & kDebugWithholdArrive) && ptid == 0;
-                if (!withhold) mbar_arrive(bars + 8u * s);
-                first = false;
-                if (++s == S) {
-                    s = 0;
-                    ph ^= 1u;
-                }
-                if (!have2) break;
-                u = u2;
-                c = c2;
-                kt = kt2;
-                cur = nxt;
             }
         }
     } else if (lane == 0) {

@@ -240,10 +240,11 @@ def test_torch_matmul_and_streams():
     assert not oracle.first_failures(c.cpu().numpy(), ref, scale)
     # column slices (ld > cols) through the tensor API
     big = torch.rand(300, 700, device="cuda")
-    sub = big[:, 50:350]
-    cs = pkg.matmul(sub, b[:300, :64].contiguous())
-    ref, scale = oracle.sgemm_ref(300, 64, 300, 1.0, big.cpu().numpy()[:, 50:350].copy(), 300,
-                                  b[:300, :64].cpu().numpy().copy(), 64, 0.0, None, 64)
+    sub = big[:, 50:307]                      # 300 x 257, lda = 700
+    bsub = b[:, 100:164]                      # 257 x 64, ldb = 1025
+    cs = pkg.matmul(sub, bsub)
+    ref, scale = oracle.sgemm_ref(300, 64, 257, 1.0, big.cpu().numpy()[:, 50:307].copy(), 257,
+                                  bsub.cpu().numpy().copy(), 64, 0.0, None, 64)
     assert not oracle.first_failures(cs.cpu().numpy(), ref, scale)
 
 
