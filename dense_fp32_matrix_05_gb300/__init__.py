@@ -18,7 +18,7 @@ from . import _build_ext
 
 __all__ = [
     "SGEMM_ALGO_AUTO", "SGEMM_ALGO_FFMA", "SGEMM_ALGO_TF32X3",
-    "SGEMM_FLAG_DEBUG_WITHHOLD_ARRIVE", "SGEMM_ERR_DEVICE_TIMEOUT",
+    "SGEMM_FLAG_DEBUG_WITHHOLD_ARRIVE", "SGEMM_FLAG_TILE_ROWS", "SGEMM_ERR_DEVICE_TIMEOUT",
     "SgemmError", "library", "lib_path", "declared_functions",
     "sgemm", "sgemm_ex", "sgemm_host", "sgemm_plan_info", "sgemm_check_status",
     "sgemm_status_string", "sgemm_release", "sgemm_version", "matmul",
@@ -28,6 +28,13 @@ SGEMM_ALGO_AUTO = 0
 SGEMM_ALGO_FFMA = 1
 SGEMM_ALGO_TF32X3 = 2
 SGEMM_FLAG_DEBUG_WITHHOLD_ARRIVE = 1
+
+
+def SGEMM_FLAG_TILE_ROWS(r: int) -> int:
+    """Force r C rows per 3xTF32 tile (16, 32, 64, 128, 192 or 256)."""
+    return ((r // 16) & 0xFF) << 8
+
+
 SGEMM_ERR_DEVICE_TIMEOUT = 10001
 SGEMM_ERR_NO_DEVICE = 10002
 SGEMM_ERR_UNSUPPORTED_DEVICE = 10003
@@ -45,7 +52,7 @@ _SIGS = {
     "sgemm": (_i, [_i, _i, _i, _f, _p, _i, _p, _i, _f, _p, _i, _p]),
     "sgemm_ex": (_i, [_i, _i, _i, _f, _p, _i, _p, _i, _f, _p, _i, _p, _i, _i, _i]),
     "sgemm_host": (_i, [_i, _i, _i, _f, _p, _i, _p, _i, _f, _p, _i, _i]),
-    "sgemm_plan_info": (_i, [_i, _i, _i, _p, _i, _p, _i, _p, _i, _i, _i, _f, _f, _i,
+    "sgemm_plan_info": (_i, [_i, _i, _i, _p, _i, _p, _i, _p, _i, _i, _i, _i, _f, _f, _i,
                              ctypes.POINTER(ctypes.c_int), _i]),
     "sgemm_check_status": (_i, [_p]),
     "sgemm_status_string": (ctypes.c_char_p, [_i]),
@@ -135,13 +142,13 @@ _PLAN_KEYS = ["path", "tile_m", "tile_n", "splits", "units", "grid", "stages", "
 
 
 def sgemm_plan_info(M, N, K, A=0, lda=None, B=0, ldb=None, C=0, ldc=None, algo=0, splits=0,
-                    alpha=1.0, beta=0.0, num_sms=0) -> dict:
+                    flags=0, alpha=1.0, beta=0.0, num_sms=0) -> dict:
     lda = max(1, K) if lda is None else lda
     ldb = max(1, N) if ldb is None else ldb
     ldc = max(1, N) if ldc is None else ldc
     buf = (ctypes.c_int * len(_PLAN_KEYS))()
     rc = library().sgemm_plan_info(M, N, K, _ptr(A), lda, _ptr(B), ldb, _ptr(C), ldc, algo, splits,
-                                   alpha, beta, num_sms, buf, len(_PLAN_KEYS))
+                                   flags, alpha, beta, num_sms, buf, len(_PLAN_KEYS))
     if rc != 0:
         raise SgemmError("sgemm_plan_info", rc)
     return dict(zip(_PLAN_KEYS, list(buf)))
@@ -164,6 +171,7 @@ def sgemm_release() -> int:
 
 def sgemm_version() -> int:
     return library().sgemm_version()
+
 
 
 # ------------------------------------------------------- torch convenience

@@ -12,7 +12,7 @@
 #include <map>
 #include <mutex>
 
-#include "../../include/sgemm_gb300.h"
+#include "sgemm_gb300.h"
 #include "launch.h"
 
 namespace {
@@ -108,7 +108,8 @@ int choose_splits(int tiles, int k_tiles, int slots, int splits_req, int min_kt)
 }
 
 // C rows per tile of the 3xTF32 kernel (MMA N).
-int choose_tm(int M, int N, int K, int sms) {
+int choose_tm(int M, int N, int K, int sms, int forced) {
+    if (forced > 0) return forced;
     int tm;
     if (M <= 16) tm = 16;
     else if (M <= 32) tm = 32;
@@ -134,9 +135,11 @@ int choose_tm(int M, int N, int K, int sms) {
     return tm;
 }
 
-void plan_tf32x3(int M, int N, int K, int sms, int splits_req, Plan &p) {
+int forced_tile_rows(int flags) { return ((flags >> 8) & 0xFF) * 16; }
+
+void plan_tf32x3(int M, int N, int K, int sms, int splits_req, int flags, Plan &p) {
     p.path = SGEMM_ALGO_TF32X3;
-    const int tm = choose_tm(M, N, K, sms);
+    const int tm = choose_tm(M, N, K, sms, forced_tile_rows(flags));
     p.tile_m = tm;
     p.tile_n = sg::kTf32x3TileN;
     Schedule &s = p.sch;
@@ -172,9 +175,9 @@ void plan_ffma(int M, int N, int K, int sms, int splits_req, Plan &p) {
 }
 
 int make_plan(int M, int N, int K, const void *A, int lda, const void *B, int ldb, const void *C, int ldc,
-              int algo, int splits, int sms, Plan &p) {
+              int algo, int splits, int flags, int sms, Plan &p) {
     const int path = (algo == SGEMM_ALGO_AUTO) ? SGEMM_ALGO_TF32X3 : algo;
-    if (path == SGEMM_ALGO_TF32X3) plan_tf32x3(M, N, K, sms, splits, p);
+    if (path == SGEMM_ALGO_TF32X3) plan_tf32x3(M, N, K, sms, splits, flags, p);
     else plan_ffma(M, N, K, sms, splits, p);
     p.vec_a = aligned16(A, lda);
     p.vec_b = aligned16(B, ldb);
@@ -196,6 +199,12 @@ size_t span_bytes(int rows, int cols, long long ld) {
     return static_cast<size_t>((static_cast<long long>(rows) - 1) * ld + cols) * sizeof(float);
 }
 
+bool flags_valid(int flags) {
+    if (flags & ~(SGEMM_FLAG_DEBUG_WITHHOLD_ARRIVE | 0xFF00)) return false;
+    const int tm = forced_tile_rows(flags);
+    return tm == 0 || sg::tf32x3_supported_tm(tm);
+}
+
 int check_args(int M, int N, int K, float alpha, const float *A, int lda, const float *B, int ldb, float beta,
                float *C, int ldc, int algo, int splits, int flags) {
     (void)beta;
@@ -207,7 +216,7 @@ int check_args(int M, int N, int K, float alpha, const float *A, int lda, const 
     if (ldc < std::max(1, N)) return -11;
     if (algo < SGEMM_ALGO_AUTO || algo > SGEMM_ALGO_TF32X3) return -13;
     if (splits < 0) return -14;
-    if (flags & ~SGEMM_FLAG_DEBUG_WITHHOLD_ARRIVE) return -15;
+    if (!flags_valid(flags)) return -15;
     if (M == 0 || N == 0) return 0;
     const bool use_ab = alpha != 0.f && K > 0;
     if (use_ab && A == nullptr) return -5;
@@ -275,7 +284,7 @@ int run(int M, int N, int K, float alpha, const float *A, int lda, const float *
             if (beta == 1.f) return 0;
             return from_cuda(sg::scale_c_launch(C, ldc, M, N, beta, d->sms, stream));
         }
-        rc = make_plan(M, N, K, A, lda, B, ldb, C, ldc, algo, splits, d->sms, p);
+        rc = make_plan(M, N, K, A, lda, B, ldb, C, ldc, algo, splits, flags, d->sms, p);
         if (rc != 0) return rc;
         ctl.status = d->status;
         ctl.wait_budget = (flags & SGEMM_FLAG_DEBUG_WITHHOLD_ARRIVE) ? kDebugWaitBudget : kWaitBudget;
@@ -369,7 +378,8 @@ int sgemm_host(int M, int N, int K, float alpha, const float *A, int lda, const 
 }
 
 int sgemm_plan_info(int M, int N, int K, const void *A, int lda, const void *B, int ldb, const void *C, int ldc,
-                    int algo, int splits, float alpha, float beta, int num_sms, int *info, int ninfo) {
+                    int algo, int splits, int flags, float alpha, float beta, int num_sms, int *info,
+                    int ninfo) {
     if (M < 0) return -1;
     if (N < 0) return -2;
     if (K < 0) return -3;
@@ -378,9 +388,10 @@ int sgemm_plan_info(int M, int N, int K, const void *A, int lda, const void *B, 
     if (ldc < std::max(1, N)) return -9;
     if (algo < SGEMM_ALGO_AUTO || algo > SGEMM_ALGO_TF32X3) return -10;
     if (splits < 0) return -11;
-    if (num_sms < 0) return -14;
-    if (info == nullptr && ninfo > 0) return -15;
-    if (ninfo < 0) return -16;
+    if (!flags_valid(flags)) return -12;
+    if (num_sms < 0) return -15;
+    if (info == nullptr && ninfo > 0) return -16;
+    if (ninfo < 0) return -17;
     (void)alpha;
     (void)beta;
     int sms = num_sms;
@@ -394,7 +405,7 @@ int sgemm_plan_info(int M, int N, int K, const void *A, int lda, const void *B, 
     int vals[10] = {0};
     if (M > 0 && N > 0 && K > 0) {
         Plan p;
-        int rc = make_plan(M, N, K, A, lda, B, ldb, C, ldc, algo, splits, sms, p);
+        int rc = make_plan(M, N, K, A, lda, B, ldb, C, ldc, algo, splits, flags, sms, p);
         if (rc != 0) return rc;
         vals[0] = p.path;
         vals[1] = p.tile_m;
@@ -498,3 +509,4 @@ int sgemm_release(void) {
 int sgemm_version(void) { return kVersion; }
 
 }  // extern "C"
+

@@ -15,14 +15,17 @@
 //   warps 0-3   epilogue: tensor memory -> alpha/beta -> C (or split-K
 //               partials); warp w owns tensor-memory lanes 32w..32w+31
 //   warps 4-11  producers: global loads (any alignment, zero-filled edges)
-//               -> hi/lo split in registers -> K-major 64-byte-swizzled
-//               shared-memory stages; the next stage's loads are in flight
-//               while the current one is split and stored
+//               -> hi/lo split in registers -> the B^T tile (MMA A operand)
+//               into a tensor-memory ring with tcgen05.st, the A tile (MMA B
+//               operand) into K-major 64-byte-swizzled shared memory; the
+//               loads of the next two stages are in flight meanwhile
 //   warp 12     tensor-memory allocation and the single MMA-issuing thread
-// Pipelines: STAGES-deep shared-memory ring (full/empty mbarriers; the
-// tensor core frees a stage through tcgen05.commit) and two accumulators in
-// tensor memory (acc_full/acc_empty) so that a tile's epilogue overlaps the
-// next tile's main loop.  Every wait is bounded (see mbar_wait_bounded).
+// Keeping the 128-row operand in tensor memory halves the shared-memory
+// traffic per MMA (the tensor core reads only the A tile from shared memory).
+// Pipelines: a STAGES-deep ring (full/empty mbarriers; the tensor core frees
+// a stage through tcgen05.commit) and one or two accumulators in tensor
+// memory (acc_full/acc_empty; with two, a tile's epilogue overlaps the next
+// tile's main loop).  Every wait is bounded (see mbar_wait_bounded).
 //
 // Operand staging follows the shared-memory tiling and vector-load ideas of
 // "NVIDIA_SGEMM_PRACTICE" (sections "kernel 2", "kernel 6", "kernel 7") and
@@ -41,36 +44,37 @@ namespace tf32x3 {
 constexpr int kTileN = 128;  // C columns per tile (MMA M, tensor-memory lanes)
 constexpr int kBK = 16;      // K per stage: one 64-byte swizzled row per operand row
 constexpr int kEpiWarps = 4;
-constexpr int kProdWarps = 8;
+constexpr int kProdWarps = 16;            // multiple of 4: each lane quadrant gets kProdWarps/4 warps
 constexpr int kProdThreads = kProdWarps * 32;
+constexpr int kBtK = kBK * 4 / kProdWarps;  // k values of one B^T column per producer thread
+constexpr int kPrefetch = 3;              // register buffers per producer (kPrefetch-1 in flight)
 constexpr int kMmaWarp = kEpiWarps + kProdWarps;
 constexpr int kThreads = (kEpiWarps + kProdWarps + 1) * 32;
 constexpr int kEpiBarrierId = 1;
 
-__host__ __device__ constexpr int stages_for(int tm) {
-    return tm >= 256 ? 4 : tm >= 192 ? 5 : tm >= 128 ? 6 : 8;
-}
-__host__ __device__ constexpr uint32_t tmem_cols_for(int tm) {
-    return (2 * tm) <= 32 ? 32u : (2 * tm) <= 64 ? 64u : (2 * tm) <= 128 ? 128u
-         : (2 * tm) <= 256 ? 256u : 512u;
-}
+// Tensor memory (512 columns of 128 lanes x 32 bit): accumulators of TM
+// columns each, then a ring of STAGES B^T stages of 32 columns (16 hi + 16 lo
+// k values per lane = per C column).
+__host__ __device__ constexpr int nacc_for(int tm) { return tm >= 192 ? 1 : 2; }
+__host__ __device__ constexpr int stages_for(int tm) { return tm >= 256 ? 6 : 8; }
+constexpr int kRingColsPerStage = 2 * kBK;
+constexpr uint32_t kTmemCols = 512;
 
 // TM = C rows per tile (MMA N).
 template <int TM>
 struct Cfg {
     static_assert(TM % 16 == 0 && TM >= 16 && TM <= 256, "MMA N for M=128 must be 16..256, step 16");
     static constexpr int kStages = stages_for(TM);
-    static constexpr int kBtBytes = kTileN * kBK * 4;  // B^T tile (MMA A operand)
-    static constexpr int kABytes = TM * kBK * 4;       // A tile (MMA B operand)
-    static constexpr int kOffBtHi = 0;
-    static constexpr int kOffBtLo = kBtBytes;
-    static constexpr int kOffAHi = 2 * kBtBytes;
-    static constexpr int kOffALo = 2 * kBtBytes + kABytes;
-    static constexpr int kStageBytes = 2 * kBtBytes + 2 * kABytes;
+    static constexpr int kNacc = nacc_for(TM);
+    static constexpr int kABytes = TM * kBK * 4;  // A tile (MMA B operand), one of hi / lo
+    static constexpr int kOffAHi = 0;
+    static constexpr int kOffALo = kABytes;
+    static constexpr int kStageBytes = 2 * kABytes;
     static_assert(kStageBytes % 1024 == 0, "stages must keep 1 KB alignment");
+    static constexpr int kRingCol = kNacc * TM;
+    static_assert(kRingCol + kStages * kRingColsPerStage <= static_cast<int>(kTmemCols), "tensor memory");
     static constexpr int kAJobs = (TM * 4 + kProdThreads - 1) / kProdThreads;
     static constexpr int kChunk = TM < 32 ? 16 : 32;
-    static constexpr uint32_t kTmemCols = tmem_cols_for(TM);
     static constexpr uint32_t kIdesc = umma_idesc_tf32(kTileN, TM);
     // barriers: full[S], empty[S], acc_full[2], acc_empty[2], drain; then
     // tensor-memory address, abort flag, split-K "last arrival" flag
@@ -99,25 +103,25 @@ __device__ __forceinline__ void split_tf32(float x, uint32_t &hi, uint32_t &lo) 
 
 template <int AJ>
 struct Raw {
-    float b[2][4];   // B^T chunks: 4 consecutive k of one column n
+    float b[kBtK];   // B^T: kBtK consecutive k of one column n
     float a[AJ][4];  // A chunks: 4 consecutive k of one row m
 };
 
-// Producer: load one k-tile (K-range [k0, k0+16)) of B^T (128 columns) and A
-// (TM rows) into registers; out-of-range elements read as 0.
+// Producer: load one k-tile (K-range [k0, k0+16)) into registers; out-of-range
+// elements read as 0.  Thread ptid holds B[k0+kBtK*h .. +kBtK-1][n0+(ptid&127)]
+// with h = ptid >> 7 (its tensor-memory lane is its column), and A chunks
+// j = ptid + kProdThreads * r: row j >> 2, k chunk j & 3.
 template <int TM, int AJ>
 __device__ __forceinline__ void load_raw(const GemmArgs &g, bool vec_a, int m0, int n0, int k0,
                                          int ptid, Raw<AJ> &raw) {
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-        const int j = ptid + r * kProdThreads;
-        const int n = n0 + (j & (kTileN - 1));
-        const int kb = k0 + (j >> 7) * 4;
+    {
+        const int n = n0 + (ptid & (kTileN - 1));
+        const int kb = k0 + (ptid >> 7) * kBtK;
         const bool n_ok = n < g.N;
         const float *src = g.B + static_cast<long long>(kb) * g.ldb + n;
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-            raw.b[r][e] = (n_ok && kb + e < g.K) ? __ldg(src + e * g.ldb) : 0.f;
+        for (int e = 0; e < kBtK; ++e)
+            raw.b[e] = (n_ok && kb + e < g.K) ? __ldg(src + e * g.ldb) : 0.f;
     }
 #pragma unroll
     for (int r = 0; r < AJ; ++r) {
@@ -155,15 +159,19 @@ __device__ __forceinline__ void split_store4(uint32_t hi_addr, uint32_t lo_addr,
     sts128(lo_addr, l0, l1, l2, l3);
 }
 
-// Producer: split the registers of one k-tile into stage `stage`.
+// Producer: split the registers of one k-tile into pipeline stage `s`: B^T
+// hi/lo into tensor-memory columns [ring + 32 s, +32) of this warp's lanes,
+// A hi/lo into the shared-memory stage at `stage`.
 template <int TM, int AJ>
-__device__ __forceinline__ void store_split(uint32_t stage, int ptid, const Raw<AJ> &raw) {
+__device__ __forceinline__ void store_split(uint32_t stage, uint32_t ring_taddr, int ptid, const Raw<AJ> &raw) {
     using C = Cfg<TM>;
+    {
+        uint32_t hi[kBtK], lo[kBtK];
 #pragma unroll
-    for (int r = 0; r < 2; ++r) {
-        const int j = ptid + r * kProdThreads;
-        const uint32_t off = sw64_off(j & (kTileN - 1), j >> 7);
-        split_store4(stage + C::kOffBtHi + off, stage + C::kOffBtLo + off, raw.b[r]);
+        for (int e = 0; e < kBtK; ++e) split_tf32(raw.b[e], hi[e], lo[e]);
+        const uint32_t t = ring_taddr + static_cast<uint32_t>((ptid >> 7) * kBtK);
+        tmem_st_cols<kBtK>(t, hi);
+        tmem_st_cols<kBtK>(t + kBK, lo);
     }
 #pragma unroll
     for (int r = 0; r < AJ; ++r) {
@@ -278,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_mbar_init();
     }
     if (warp == kMmaWarp) {
-        tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -292,8 +300,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         int it = 0;
         for (int u = blockIdx.x; u < sch.units; u += gridDim.x, ++it) {
             const UnitCoord c = decode_unit(sch, u);
-            const int acc = it & 1;
-            const uint32_t aph = (it >> 1) & 1;
+            const int acc = it % C::kNacc;
+            const uint32_t aph = (it / C::kNacc) & 1;
             const bool w = mbar_wait_bounded(acc_full0 + 8u * acc, aph, abort_flag, ctl,
                                              kStatusTimeoutEpilogue);
             if (!epi_all(w)) break;
@@ -384,38 +392,47 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp < kMmaWarp) {
         // ------------------------------------------------------ producers
-        // Jobs are the (unit, k tile) pairs of this CTA in order.  Three
-        // register buffers rotate: while one job is split into shared memory
-        // the loads of the next two are in flight.
+        // Jobs are the (unit, k tile) pairs of this CTA in order.  kPrefetch
+        // register buffers rotate: while one job is split and stored the
+        // loads of the next kPrefetch-1 are in flight.
         const int ptid = threadIdx.x - kEpiWarps * 32;
         constexpr int AJ = C::kAJobs;
         int s = 0;
         uint32_t ph = 0;
         JobIter next;
         next.start(sch, blockIdx.x);
-        Raw<AJ> buf[3];
+        Raw<AJ> buf[kPrefetch];
         int loaded = 0, done = 0;
 #pragma unroll
-        for (int i = 0; i < 3; ++i) {
+        for (int i = 0; i < kPrefetch; ++i) {
             if (next.valid(sch)) {
                 load_raw<TM, AJ>(g, vec_a != 0, next.c.mt * TM, next.c.nt * kTileN, next.kt * kBK, ptid, buf[i]);
                 next.advance(sch);
                 ++loaded;
             }
         }
+        // this warp's tensor-memory lanes hold the B^T columns of its threads
+        const uint32_t ring_lane = tmem_base + (static_cast<uint32_t>((warp & 3) * 32) << 16) +
+                                   static_cast<uint32_t>(C::kRingCol);
         bool ok = true;
 #pragma unroll 1
         while (ok && done < loaded) {
 #pragma unroll
-            for (int i = 0; i < 3; ++i) {
+            for (int i = 0; i < kPrefetch; ++i) {
                 if (done < loaded) {
-                    if (!mbar_wait_bounded(bars + 8u * (S + s), ph ^ 1u, abort_flag, ctl,
-                                           kStatusTimeoutProducer)) {
+                    // warp-uniform decision: tcgen05.st below is warp-collective
+                    const bool w = mbar_wait_bounded(bars + 8u * (S + s), ph ^ 1u, abort_flag, ctl,
+                                                     kStatusTimeoutProducer);
+                    if (!__all_sync(0xffffffffu, w)) {
                         ok = false;
                         break;
                     }
-                    store_split<TM, AJ>(base + s * C::kStageBytes, ptid, buf[i]);
+                    tc_fence_after();
+                    store_split<TM, AJ>(base + s * C::kStageBytes,
+                                        ring_lane + static_cast<uint32_t>(s * kRingColsPerStage), ptid, buf[i]);
                     fence_proxy_async_smem();
+                    tmem_st_wait();
+                    tc_fence_before();
                     const bool withhold = done == 0 && (ctl.debug_flags & kDebugWithholdArrive) && ptid == 0;
                     if (!withhold) mbar_arrive(bars + 8u * s);
                     ++done;
@@ -440,8 +457,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         for (int u = blockIdx.x; u < sch.units && ok; u += gridDim.x, ++it) {
             const UnitCoord c = decode_unit(sch, u);
-            const int acc = it & 1;
-            const uint32_t aph = (it >> 1) & 1;
+            const int acc = it % C::kNacc;
+            const uint32_t aph = (it / C::kNacc) & 1;
             if (!mbar_wait_bounded(acc_empty0 + 8u * acc, aph ^ 1u, abort_flag, ctl, kStatusTimeoutMma)) {
                 ok = false;
                 break;
@@ -455,15 +472,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after();
                 const uint32_t st = base + s * C::kStageBytes;
+                const uint32_t ring = tmem_base + static_cast<uint32_t>(C::kRingCol + s * kRingColsPerStage);
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {
-                    const uint64_t a_hi = umma_desc_kmajor_sw64(st + C::kOffBtHi + j * 32);
-                    const uint64_t a_lo = umma_desc_kmajor_sw64(st + C::kOffBtLo + j * 32);
+                    const uint32_t a_hi = ring + static_cast<uint32_t>(j * 8);
+                    const uint32_t a_lo = a_hi + static_cast<uint32_t>(kBK);
                     const uint64_t b_hi = umma_desc_kmajor_sw64(st + C::kOffAHi + j * 32);
                     const uint64_t b_lo = umma_desc_kmajor_sw64(st + C::kOffALo + j * 32);
-                    mma_tf32_ss(d, a_lo, b_hi, C::kIdesc, (kt != c.kb || j != 0) ? 1u : 0u);
-                    mma_tf32_ss(d, a_hi, b_lo, C::kIdesc, 1u);
-                    mma_tf32_ss(d, a_hi, b_hi, C::kIdesc, 1u);
+                    mma_tf32_ts(d, a_lo, b_hi, C::kIdesc, (kt != c.kb || j != 0) ? 1u : 0u);
+                    mma_tf32_ts(d, a_hi, b_lo, C::kIdesc, 1u);
+                    mma_tf32_ts(d, a_hi, b_hi, C::kIdesc, 1u);
                 }
                 mma_commit(bars + 8u * (S + s));
                 if (++s == S) {
@@ -484,7 +502,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     if (warp == kMmaWarp) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, C::kTmemCols);
+        tmem_dealloc(tmem_base, kTmemCols);
     }
 }
 

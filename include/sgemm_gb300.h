@@ -60,6 +60,9 @@ typedef struct CUstream_st *sgemm_stream_t;
                                in fp32 in tensor memory                        */
 
 /* Flags for sgemm_ex. */
+/* SGEMM_FLAG_TILE_ROWS(r): 3xTF32 path only, force r C rows per tile
+ * (r in 16, 32, 64, 128, 192, 256); 0 lets the planner choose. */
+#define SGEMM_FLAG_TILE_ROWS(r) ((((r) / 16) & 0xFF) << 8)
 #define SGEMM_FLAG_DEBUG_WITHHOLD_ARRIVE 1 /* test only: one pipeline arrive
                                               is withheld and the on-device
                                               wait budget is cut to ~1 ms, so
@@ -91,7 +94,9 @@ int sgemm(int M, int N, int K, float alpha,
  *                partial tile to a library-owned workspace and the last slice
  *                to finish adds the partials in slice order, so the result
  *                does not depend on timing.
- *   flags  (15): 0, or SGEMM_FLAG_DEBUG_WITHHOLD_ARRIVE (tests only).
+ *   flags  (15): 0, SGEMM_FLAG_TILE_ROWS(r), and/or
+ *                SGEMM_FLAG_DEBUG_WITHHOLD_ARRIVE (tests only).  Any other
+ *                bit, or a tile height that is not supported, is rejected.
  *
  * The split-K workspace is owned by the library, kept per device and stream,
  * grown on demand (a synchronous cudaMalloc, so make the first call of a
@@ -130,12 +135,12 @@ int sgemm_host(int M, int N, int K, float alpha,
  *   [7] 1 if A is read with 16-byte vector loads
  *   [8] 1 if B is read with 16-byte vector loads
  *   [9] workspace bytes needed
- * Returns 0, or -i for an invalid argument (same numbering as sgemm_ex,
- * ninfo = 17, info = 16, num_sms = 15).
+ * Returns 0, or -i for an invalid argument (the i-th argument of this
+ * function, 1-based).
  */
 int sgemm_plan_info(int M, int N, int K, const void *A, int lda,
                     const void *B, int ldb, const void *C, int ldc,
-                    int algo, int splits, float alpha, float beta,
+                    int algo, int splits, int flags, float alpha, float beta,
                     int num_sms, int *info, int ninfo);
 
 /*

@@ -63,6 +63,8 @@ def test_invalid_extended_arguments(lib):
     assert pkg.sgemm_ex(*base, -1, 0, 0) == -13
     assert pkg.sgemm_ex(*base, 0, -1, 0) == -14
     assert pkg.sgemm_ex(*base, 0, 0, 2) == -15
+    assert pkg.sgemm_ex(*base, 0, 0, pkg.SGEMM_FLAG_TILE_ROWS(48)) == -15
+    assert pkg.sgemm_ex(*base, 0, 0, 1 << 20) == -15
 
 
 def test_empty_problems_need_no_device(lib):
@@ -135,8 +137,17 @@ def test_plan_ffma_tiles():
     assert plan(4096, 4096, 4096, algo=1)["tile_n"] == 128
 
 
+@pytest.mark.parametrize("rows", [16, 32, 64, 128, 192, 256])
+def test_plan_forced_tile_rows(rows):
+    p = plan(5120, 5120, 5120, flags=pkg.SGEMM_FLAG_TILE_ROWS(rows))
+    assert p["tile_m"] == rows
+    assert p["units"] == -(-5120 // rows) * 40
+
+
 def test_plan_info_rejects_bad_arguments():
     with pytest.raises(pkg.SgemmError):
         pkg.sgemm_plan_info(-1, 4, 4, num_sms=SMS)
     with pytest.raises(pkg.SgemmError):
         pkg.sgemm_plan_info(4, 4, 4, algo=7, num_sms=SMS)
+    with pytest.raises(pkg.SgemmError):
+        pkg.sgemm_plan_info(4, 4, 4, flags=pkg.SGEMM_FLAG_TILE_ROWS(80), num_sms=SMS)

@@ -79,6 +79,23 @@ def test_leading_dimensions_and_alignment(algo, layout, shape):
     check_against_oracle(p, C, what=f"{shape} {layout} algo={algo}")
 
 
+TILE_ROWS = [16, 32, 64, 128, 192, 256]
+
+
+@pytest.mark.parametrize("rows", TILE_ROWS)
+@pytest.mark.parametrize("shape", [(300, 270, 200), (37, 1000, 45), (513, 129, 1100)],
+                         ids=["300x270x200", "37x1000x45", "513x129x1100"])
+def test_every_tile_height(rows, shape):
+    """Each tensor-core kernel instantiation (C rows per tile) on ragged shapes
+    spanning several tiles and pipeline wraps, with and without split-K."""
+    M, N, K = shape
+    p = _with_c(random_problem(M, N, K, alpha=1.25, beta=-0.5, seed=rows + M))
+    for splits in (1, 3):
+        C, st = run_sgemm(p, pkg.SGEMM_ALGO_TF32X3, splits=splits, flags=pkg.SGEMM_FLAG_TILE_ROWS(rows))
+        assert st == 0
+        check_against_oracle(p, C, what=f"{shape} rows={rows} splits={splits}")
+
+
 @pytest.mark.parametrize("algo", ALGOS, ids=ALGO_IDS)
 @pytest.mark.parametrize("splits", [1, 2, 3, 7])
 def test_forced_split_k(algo, splits):
