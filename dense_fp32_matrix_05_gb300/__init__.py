@@ -21,7 +21,8 @@ __all__ = [
     "SGEMM_FLAG_DEBUG_WITHHOLD_ARRIVE", "SGEMM_FLAG_TILE_ROWS", "SGEMM_ERR_DEVICE_TIMEOUT",
     "SgemmError", "library", "lib_path", "declared_functions",
     "sgemm", "sgemm_ex", "sgemm_host", "sgemm_plan_info", "sgemm_check_status",
-    "sgemm_status_string", "sgemm_release", "sgemm_version", "matmul",
+    "sgemm_status_string", "sgemm_release", "sgemm_version", "sgemm_noalloc", "matmul",
+    "SGEMM_ERR_SCRATCH_LIMIT",
 ]
 
 SGEMM_ALGO_AUTO = 0
@@ -40,6 +41,7 @@ SGEMM_ERR_NO_DEVICE = 10002
 SGEMM_ERR_UNSUPPORTED_DEVICE = 10003
 SGEMM_ERR_WORKSPACE = 10004
 SGEMM_ERR_INTERNAL = 10005
+SGEMM_ERR_SCRATCH_LIMIT = 10006
 
 HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
                       "include", "sgemm_gb300.h")
@@ -58,6 +60,7 @@ _SIGS = {
     "sgemm_status_string": (ctypes.c_char_p, [_i]),
     "sgemm_release": (_i, []),
     "sgemm_version": (_i, []),
+    "sgemm_noalloc": (_i, [_i, _i, _i, _f, _p, _i, _p, _i, _f, _p, _i, _p, _i]),
 }
 
 
@@ -172,6 +175,11 @@ def sgemm_release() -> int:
 def sgemm_version() -> int:
     return library().sgemm_version()
 
+
+def sgemm_noalloc(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None, splits=0) -> int:
+    """Allocation-free 3xTF32 entry point (split-K scratch in a fixed library array)."""
+    return library().sgemm_noalloc(M, N, K, alpha, _ptr(A), lda, _ptr(B), ldb, beta, _ptr(C), ldc,
+                                   _stream(stream), splits)
 
 
 # ------------------------------------------------------- torch convenience

@@ -471,6 +471,9 @@ const char *sgemm_status_string(int status) {
         case SGEMM_ERR_UNSUPPORTED_DEVICE: return "device is not compute capability 10.3 (sm_103a)";
         case SGEMM_ERR_WORKSPACE: return "could not allocate library-owned device memory";
         case SGEMM_ERR_INTERNAL: return "internal planner error";
+        case SGEMM_ERR_SCRATCH_LIMIT:
+            return "the problem needs more split-K scratch than sgemm_noalloc's fixed array "
+                   "(16 MiB of partial tiles, 4096 tiles): use sgemm_ex or fewer splits";
         default: break;
     }
     if (status > 0 && status < 10000) return cudaGetErrorString(static_cast<cudaError_t>(status));
@@ -510,3 +513,30 @@ int sgemm_version(void) { return kVersion; }
 
 }  // extern "C"
 
+// ---------------------------------------------------------------- internal
+// Used by sgemm_noalloc (noalloc.cu): the same checks and planner as
+// sgemm_ex with algo = SGEMM_ALGO_TF32X3 and flags = 0.
+namespace sg {
+
+int check_tensor_call(int M, int N, int K, float alpha, const float *A, int lda, const float *B, int ldb,
+                      float beta, const float *C, int ldc, int splits) {
+    const int rc = check_args(M, N, K, alpha, A, lda, B, ldb, beta, const_cast<float *>(C), ldc,
+                              SGEMM_ALGO_TF32X3, splits, 0);
+    return rc == -15 ? SGEMM_ERR_INTERNAL : rc;  // flags are fixed here
+}
+
+int plan_tensor_call(int M, int N, int K, const float *A, int lda, const float *B, int ldb, const float *C,
+                     int ldc, int splits, int sms, TensorPlan *out) {
+    Plan p;
+    const int rc = make_plan(M, N, K, A, lda, B, ldb, C, ldc, SGEMM_ALGO_TF32X3, splits, 0, sms, p);
+    if (rc != 0) return rc;
+    out->tile_m = p.tile_m;
+    out->sch = p.sch;
+    out->grid = p.grid;
+    out->vec_a = p.vec_a;
+    out->ws_floats = p.ws_bytes / sizeof(float);
+    out->tiles = p.sch.m_tiles * p.sch.n_tiles;
+    return 0;
+}
+
+}  // namespace sg

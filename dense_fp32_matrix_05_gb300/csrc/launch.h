@@ -25,6 +25,21 @@ int ffma_smem_bytes(int bm, int bn);
 cudaError_t ffma_launch(int bm, int bn, const GemmArgs &g, const Schedule &s, const DeviceCtl &ctl,
                         int vec_a, int vec_b, int vec_c, cudaStream_t stream);
 
+// Planner and argument checks of the 3xTF32 path, for entry points defined
+// outside api.cu (noalloc.cu).  check_tensor_call makes no CUDA call.
+struct TensorPlan {
+    int tile_m = 0;
+    Schedule sch{};
+    int grid = 0;
+    int vec_a = 0;
+    size_t ws_floats = 0;  // split-K partial-tile floats needed (0 without split-K)
+    int tiles = 0;         // output tiles (= arrival counters needed)
+};
+int check_tensor_call(int M, int N, int K, float alpha, const float *A, int lda, const float *B, int ldb,
+                      float beta, const float *C, int ldc, int splits);
+int plan_tensor_call(int M, int N, int K, const float *A, int lda, const float *B, int ldb, const float *C,
+                     int ldc, int splits, int sms, TensorPlan *out);
+
 // C = beta * C (alpha == 0 or K == 0).
 cudaError_t scale_c_launch(float *C, long long ldc, int M, int N, float beta, int num_sms,
                            cudaStream_t stream);

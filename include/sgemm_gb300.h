@@ -51,6 +51,9 @@ typedef struct CUstream_st *sgemm_stream_t;
 #define SGEMM_ERR_UNSUPPORTED_DEVICE 10003 /* device is not compute 10.3     */
 #define SGEMM_ERR_WORKSPACE          10004 /* split-K workspace unavailable   */
 #define SGEMM_ERR_INTERNAL           10005 /* planner found no kernel         */
+#define SGEMM_ERR_SCRATCH_LIMIT      10006 /* sgemm_noalloc: problem needs more
+                                              split-K scratch than its fixed
+                                              array holds                      */
 
 /* Algorithm selector for sgemm_ex / sgemm_host. */
 #define SGEMM_ALGO_AUTO   0 /* planner picks the faster path                  */
@@ -160,6 +163,44 @@ const char *sgemm_status_string(int status);
  * safe while another thread is inside a call of this library.
  */
 int sgemm_release(void);
+
+/*
+ * sgemm_noalloc - C = alpha * A * B + beta * C on the 3xTF32 path without
+ * allocating any device memory.  (The pages have no counterpart: this entry
+ * point exists for callers of this library.)
+ *
+ * Who needs it: callers that cannot let a library allocate device memory
+ * behind their back - programs that reserve the whole GPU for their own
+ * memory pool up front, where a hidden cudaMalloc fails or breaks their
+ * accounting, and latency-sensitive loops in which cudaMalloc/cudaFree's
+ * implicit device-wide synchronisation would stall other streams.
+ *
+ * Same arguments, rules and results as
+ * sgemm_ex(..., stream, SGEMM_ALGO_TF32X3, splits, 0); the caller still
+ * passes A, B and C.  The split-K partial tiles and arrival counters live in
+ * fixed arrays compiled into the library: 16 MiB of partials (units x 128 x
+ * tile rows floats) and 4096 counters (one per output tile), held on every
+ * GPU that loads the library until the process exits.  A plan that needs
+ * more returns SGEMM_ERR_SCRATCH_LIMIT before anything runs.  The call never
+ * calls cudaMalloc, cudaFree or any allocating routine.
+ *
+ * Set-up: the first call on a device (with that device current) resolves
+ * the arrays' device addresses with cudaGetSymbolAddress; make that first
+ * call before any stream capture.
+ * Sharing: every call uses the same arrays, which keep the previous call's
+ * contents (the counters are cleared at the start of each call with
+ * cudaMemsetAsync).  Calls whose work overlaps on the GPU - on different
+ * streams, or from several host threads at once - race on the arrays and
+ * give wrong results: serialise them.
+ * Status: a bounded on-device wait that gives up (only a broken GPU does)
+ * leaves C unspecified and is recorded in a status word of this entry point
+ * that sgemm_check_status does not read.
+ */
+int sgemm_noalloc(int M, int N, int K, float alpha,
+                  const float *A, int lda,
+                  const float *B, int ldb,
+                  float beta, float *C, int ldc,
+                  sgemm_stream_t stream, int splits);
 
 /* sgemm_version - library version as 10000*major + 100*minor + patch. */
 int sgemm_version(void);
