@@ -47,6 +47,30 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Arrive once and add `bytes` to the transaction count the current phase
+// waits for (the TMA copy that follows completes them).
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+// ---------------------------------------------------------------- TMA
+
+// 2-D tiled tensor copy global -> shared (this CTA); completion is signalled
+// as transaction bytes on the mbarrier.  x is the innermost coordinate (its
+// byte offset must be a multiple of 16), y the outer one; elements outside
+// the tensor read as zero.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int x, int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const void *tmap) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
+}
+
 // ------------------------------------------------------------ proxy fences
 
 // Order this thread's generic-proxy shared-memory writes before later

@@ -1,4 +1,13 @@
-// Instantiations and launcher of the 3xTF32 tensor-core kernel.
+// Instantiations and launcher of the 3xTF32 tensor-core kernel, including
+// the TMA tensor map for A (built on the host with the driver's
+// cuTensorMapEncodeTiled, reached through the runtime's entry-point query so
+// that the library needs no link-time dependency on the driver).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cstring>
+#include <mutex>
+
 #include "launch.h"
 #include "tf32x3_gemm.cuh"
 
@@ -7,16 +16,61 @@ namespace sg {
 static_assert(kTf32x3TileN == tf32x3::kTileN && kTf32x3BK == tf32x3::kBK, "planner constants");
 
 namespace {
-template <int TM>
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    std::call_once(g_encode_once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        else
+            cudaGetLastError();
+    });
+    return g_encode;
+}
+
+// Tensor map of A for the TMA path: a K x M fp32 tensor (K innermost) with
+// row stride lda * 4 bytes, copied in boxes of 16 (k) x tm (rows) with the
+// 64-byte swizzle, out-of-range elements filled with zeros.  Requires A and
+// lda * 4 to be multiples of 16 bytes.  Returns false when no map can be made.
+bool make_tmap_a(const GemmArgs &g, int tm, CUtensorMap *map) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(g.K), static_cast<cuuint64_t>(g.M)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(g.lda) * sizeof(float)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(tf32x3::kBK), static_cast<cuuint32_t>(tm)};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(g.A), dims, strides,
+                           box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int TM, bool TMA>
 cudaError_t launch_tm(const GemmArgs &g, const Schedule &s, const DeviceCtl &ctl, int vec_a, int grid,
-                      cudaStream_t stream) {
+                      const CUtensorMap &map, cudaStream_t stream) {
     using C = tf32x3::Cfg<TM>;
-    auto kern = tf32x3::tf32x3_gemm_kernel<TM>;
+    auto kern = tf32x3::tf32x3_gemm_kernel<TM, TMA>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    kern<<<grid, tf32x3::kThreads, C::kSmemBytes, stream>>>(g, s, ctl, vec_a);
+    kern<<<grid, tf32x3::kThreads, C::kSmemBytes, stream>>>(g, s, ctl, vec_a, map);
     return cudaGetLastError();
 }
+
+template <int TM>
+cudaError_t launch_rows(const GemmArgs &g, const Schedule &s, const DeviceCtl &ctl, int vec_a, int grid,
+                        cudaStream_t stream) {
+    CUtensorMap map;
+    std::memset(&map, 0, sizeof(map));
+    if (vec_a && make_tmap_a(g, TM, &map)) return launch_tm<TM, true>(g, s, ctl, vec_a, grid, map, stream);
+    return launch_tm<TM, false>(g, s, ctl, vec_a, grid, map, stream);
+}
+
 }  // namespace
 
 bool tf32x3_supported_tm(int tm) {
@@ -40,12 +94,12 @@ int tf32x3_smem_bytes(int tm) {
 cudaError_t tf32x3_launch(int tm, const GemmArgs &g, const Schedule &s, const DeviceCtl &ctl, int vec_a,
                           int grid, cudaStream_t stream) {
     switch (tm) {
-        case 16: return launch_tm<16>(g, s, ctl, vec_a, grid, stream);
-        case 32: return launch_tm<32>(g, s, ctl, vec_a, grid, stream);
-        case 64: return launch_tm<64>(g, s, ctl, vec_a, grid, stream);
-        case 128: return launch_tm<128>(g, s, ctl, vec_a, grid, stream);
-        case 192: return launch_tm<192>(g, s, ctl, vec_a, grid, stream);
-        case 256: return launch_tm<256>(g, s, ctl, vec_a, grid, stream);
+        case 16: return launch_rows<16>(g, s, ctl, vec_a, grid, stream);
+        case 32: return launch_rows<32>(g, s, ctl, vec_a, grid, stream);
+        case 64: return launch_rows<64>(g, s, ctl, vec_a, grid, stream);
+        case 128: return launch_rows<128>(g, s, ctl, vec_a, grid, stream);
+        case 192: return launch_rows<192>(g, s, ctl, vec_a, grid, stream);
+        case 256: return launch_rows<256>(g, s, ctl, vec_a, grid, stream);
         default: return cudaErrorInvalidValue;
     }
 }

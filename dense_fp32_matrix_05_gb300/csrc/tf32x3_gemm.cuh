@@ -14,12 +14,14 @@
 // Roles (one persistent CTA per SM, work units strided over the grid):
 //   warps 0-3   epilogue: tensor memory -> alpha/beta -> C (or split-K
 //               partials); warp w owns tensor-memory lanes 32w..32w+31
-//   warps 4-11  producers: global loads (any alignment, zero-filled edges)
-//               -> hi/lo split in registers -> the B^T tile (MMA A operand)
-//               into a tensor-memory ring with tcgen05.st, the A tile (MMA B
-//               operand) into K-major 64-byte-swizzled shared memory; the
-//               loads of the next two stages are in flight meanwhile
-//   warp 12     tensor-memory allocation and the single MMA-issuing thread
+//   warps 4-19  producers: B^T (MMA A operand) global loads (any alignment,
+//               zero-filled edges, several stages in flight in registers)
+//               -> hi/lo split -> a tensor-memory ring (tcgen05.st); the A
+//               tile (MMA B operand) -> hi/lo in K-major 64-byte-swizzled
+//               shared memory, either from their own global loads or, when A
+//               rows are 16-byte aligned, split in place after a TMA copy
+//   warp 20     tensor-memory allocation and the single MMA-issuing thread
+//   warp 21     the TMA thread: copies raw A tiles into the stage ring
 // Keeping the 128-row operand in tensor memory halves the shared-memory
 // traffic per MMA (the tensor core reads only the A tile from shared memory).
 // Pipelines: a STAGES-deep ring (full/empty mbarriers; the tensor core frees
@@ -27,13 +29,16 @@
 // memory (acc_full/acc_empty; with two, a tile's epilogue overlaps the next
 // tile's main loop).  Every wait is bounded (see mbar_wait_bounded).
 //
-// Operand staging follows the shared-memory tiling and vector-load ideas of
-// "NVIDIA_SGEMM_PRACTICE" (sections "kernel 2", "kernel 6", "kernel 7") and
-// the zero-filled edge tiles of "matmul_opt.cu" (matrixMulOptimized),
-// re-done for the tensor core: the split has to touch every element, so
-// operands go global -> registers -> shared memory once, already split and
-// swizzled, instead of through an extra raw staging copy.
+// Operand staging follows the shared-memory tiling, vector-load and
+// prefetch ideas of "NVIDIA_SGEMM_PRACTICE" (sections "kernel 2", "kernel 6",
+// "kernel 7") and the zero-filled edge tiles of "matmul_opt.cu"
+// (matrixMulOptimized), re-done for the tensor core: every element has to
+// pass a producer thread for the split, so B^T goes global -> registers ->
+// tensor memory, and A either the same way or TMA -> shared memory ->
+// split in place.
 #pragma once
+#include <cuda.h>  // CUtensorMap (type only; the library does not link the driver)
+
 #include <cstdint>
 
 #include "common.cuh"
@@ -44,13 +49,17 @@ namespace tf32x3 {
 constexpr int kTileN = 128;  // C columns per tile (MMA M, tensor-memory lanes)
 constexpr int kBK = 16;      // K per stage: one 64-byte swizzled row per operand row
 constexpr int kEpiWarps = 4;
-constexpr int kProdWarps = 16;            // multiple of 4: each lane quadrant gets kProdWarps/4 warps
+constexpr int kProdWarps = 16;              // multiple of 4: each lane quadrant gets kProdWarps/4 warps
 constexpr int kProdThreads = kProdWarps * 32;
 constexpr int kBtK = kBK * 4 / kProdWarps;  // k values of one B^T column per producer thread
-constexpr int kPrefetch = 3;              // register buffers per producer (kPrefetch-1 in flight)
 constexpr int kMmaWarp = kEpiWarps + kProdWarps;
-constexpr int kThreads = (kEpiWarps + kProdWarps + 1) * 32;
+constexpr int kTmaWarp = kMmaWarp + 1;
+constexpr int kThreads = (kEpiWarps + kProdWarps + 2) * 32;
 constexpr int kEpiBarrierId = 1;
+
+// Register buffers per producer thread (kPrefetch - 1 k-tiles of loads in
+// flight): A through TMA leaves only the B^T values in registers.
+__host__ __device__ constexpr int prefetch_for(bool tma_a) { return tma_a ? 6 : 3; }
 
 // Tensor memory (512 columns of 128 lanes x 32 bit): accumulators of TM
 // columns each, then a ring of STAGES B^T stages of 32 columns (16 hi + 16 lo
@@ -67,7 +76,7 @@ struct Cfg {
     static constexpr int kStages = stages_for(TM);
     static constexpr int kNacc = nacc_for(TM);
     static constexpr int kABytes = TM * kBK * 4;  // A tile (MMA B operand), one of hi / lo
-    static constexpr int kOffAHi = 0;
+    static constexpr int kOffAHi = 0;             // also where TMA lands the raw A tile
     static constexpr int kOffALo = kABytes;
     static constexpr int kStageBytes = 2 * kABytes;
     static_assert(kStageBytes % 1024 == 0, "stages must keep 1 KB alignment");
@@ -76,14 +85,15 @@ struct Cfg {
     static constexpr int kAJobs = (TM * 4 + kProdThreads - 1) / kProdThreads;
     static constexpr int kChunk = TM < 32 ? 16 : 32;
     static constexpr uint32_t kIdesc = umma_idesc_tf32(kTileN, TM);
-    // barriers: full[S], empty[S], acc_full[2], acc_empty[2], drain; then
-    // tensor-memory address, abort flag, split-K "last arrival" flag
-    static constexpr int kBarBytes = 8 * (2 * kStages + 5) + 16;
+    // barriers: full[S], empty[S], a_full[S], acc_full[2], acc_empty[2],
+    // drain; then tensor-memory address, abort flag, split-K "last" flag
+    static constexpr int kBarBytes = 8 * (3 * kStages + 5) + 16;
     static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes;
 };
 
 // Byte offset of the 16-byte chunk `chunk` (k / 4) of row `row` inside a
-// K-major tile with 64-byte rows and the 64-byte swizzle.
+// K-major tile with 64-byte rows and the 64-byte swizzle (the layout both the
+// tensor core and a TMA copy with 64-byte swizzle use).
 __device__ __forceinline__ uint32_t sw64_off(int row, int chunk) {
     return static_cast<uint32_t>(row * 64 + (((chunk ^ (row >> 1)) & 3) << 4));
 }
@@ -101,10 +111,15 @@ __device__ __forceinline__ void split_tf32(float x, uint32_t &hi, uint32_t &lo) 
     lo = __float_as_uint(x - __uint_as_float(hu));
 }
 
+// One k-tile of operands held in a producer thread's registers.
 template <int AJ>
 struct Raw {
     float b[kBtK];   // B^T: kBtK consecutive k of one column n
     float a[AJ][4];  // A chunks: 4 consecutive k of one row m
+};
+template <>
+struct Raw<0> {
+    float b[kBtK];
 };
 
 // Producer: load one k-tile (K-range [k0, k0+16)) into registers; out-of-range
@@ -123,29 +138,31 @@ __device__ __forceinline__ void load_raw(const GemmArgs &g, bool vec_a, int m0, 
         for (int e = 0; e < kBtK; ++e)
             raw.b[e] = (n_ok && kb + e < g.K) ? __ldg(src + e * g.ldb) : 0.f;
     }
+    if constexpr (AJ > 0) {
 #pragma unroll
-    for (int r = 0; r < AJ; ++r) {
-        const int j = ptid + r * kProdThreads;
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (j < TM * 4) {
-            const int m = m0 + (j >> 2);
-            const int k = k0 + (j & 3) * 4;
-            if (m < g.M) {
-                const float *src = g.A + static_cast<long long>(m) * g.lda + k;
-                if (vec_a && k + 3 < g.K) {
-                    v = __ldg(reinterpret_cast<const float4 *>(src));
-                } else {
-                    v.x = (k + 0 < g.K) ? __ldg(src + 0) : 0.f;
-                    v.y = (k + 1 < g.K) ? __ldg(src + 1) : 0.f;
-                    v.z = (k + 2 < g.K) ? __ldg(src + 2) : 0.f;
-                    v.w = (k + 3 < g.K) ? __ldg(src + 3) : 0.f;
+        for (int r = 0; r < AJ; ++r) {
+            const int j = ptid + r * kProdThreads;
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (j < TM * 4) {
+                const int m = m0 + (j >> 2);
+                const int k = k0 + (j & 3) * 4;
+                if (m < g.M) {
+                    const float *src = g.A + static_cast<long long>(m) * g.lda + k;
+                    if (vec_a && k + 3 < g.K) {
+                        v = __ldg(reinterpret_cast<const float4 *>(src));
+                    } else {
+                        v.x = (k + 0 < g.K) ? __ldg(src + 0) : 0.f;
+                        v.y = (k + 1 < g.K) ? __ldg(src + 1) : 0.f;
+                        v.z = (k + 2 < g.K) ? __ldg(src + 2) : 0.f;
+                        v.w = (k + 3 < g.K) ? __ldg(src + 3) : 0.f;
+                    }
                 }
             }
+            raw.a[r][0] = v.x;
+            raw.a[r][1] = v.y;
+            raw.a[r][2] = v.z;
+            raw.a[r][3] = v.w;
         }
-        raw.a[r][0] = v.x;
-        raw.a[r][1] = v.y;
-        raw.a[r][2] = v.z;
-        raw.a[r][3] = v.w;
     }
 }
 
@@ -159,9 +176,11 @@ __device__ __forceinline__ void split_store4(uint32_t hi_addr, uint32_t lo_addr,
     sts128(lo_addr, l0, l1, l2, l3);
 }
 
-// Producer: split the registers of one k-tile into pipeline stage `s`: B^T
-// hi/lo into tensor-memory columns [ring + 32 s, +32) of this warp's lanes,
-// A hi/lo into the shared-memory stage at `stage`.
+// Producer: split one k-tile into pipeline stage `s`: B^T hi/lo from
+// registers into tensor-memory columns [ring + 32 s, +32) of this warp's
+// lanes; A hi/lo into the shared-memory stage at `stage`, from registers
+// (AJ > 0) or, after a TMA copy, from the raw tile in the hi buffer (split in
+// place: each thread reads and rewrites its own chunks).
 template <int TM, int AJ>
 __device__ __forceinline__ void store_split(uint32_t stage, uint32_t ring_taddr, int ptid, const Raw<AJ> &raw) {
     using C = Cfg<TM>;
@@ -173,12 +192,25 @@ __device__ __forceinline__ void store_split(uint32_t stage, uint32_t ring_taddr,
         tmem_st_cols<kBtK>(t, hi);
         tmem_st_cols<kBtK>(t + kBK, lo);
     }
+    if constexpr (AJ > 0) {
 #pragma unroll
-    for (int r = 0; r < AJ; ++r) {
-        const int j = ptid + r * kProdThreads;
-        if (j < TM * 4) {
-            const uint32_t off = sw64_off(j >> 2, j & 3);
-            split_store4(stage + C::kOffAHi + off, stage + C::kOffALo + off, raw.a[r]);
+        for (int r = 0; r < AJ; ++r) {
+            const int j = ptid + r * kProdThreads;
+            if (j < TM * 4) {
+                const uint32_t off = sw64_off(j >> 2, j & 3);
+                split_store4(stage + C::kOffAHi + off, stage + C::kOffALo + off, raw.a[r]);
+            }
+        }
+    } else {
+#pragma unroll
+        for (int r = 0; r < C::kAJobs; ++r) {
+            const int j = ptid + r * kProdThreads;
+            if (j < TM * 4) {
+                const uint32_t off = sw64_off(j >> 2, j & 3);
+                const float4 v = lds128(stage + C::kOffAHi + off);
+                const float x[4] = {v.x, v.y, v.z, v.w};
+                split_store4(stage + C::kOffAHi + off, stage + C::kOffALo + off, x);
+            }
         }
     }
 }
@@ -248,23 +280,28 @@ __device__ __forceinline__ void tmem_load_chunk(uint32_t taddr, float (&v)[Cfg<T
     }
 }
 
-template <int TM>
+// TMA_A: A rows are 16-byte aligned and tmap_a describes A (K x M, 64-byte
+// swizzle, box 16 x TM); otherwise the producers load A themselves.
+template <int TM, bool TMA_A>
 __global__ void __launch_bounds__(kThreads, 1)
     tf32x3_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ Schedule sch,
-                       const __grid_constant__ DeviceCtl ctl, int vec_a) {
+                       const __grid_constant__ DeviceCtl ctl, int vec_a,
+                       const __grid_constant__ CUtensorMap tmap_a) {
     using C = Cfg<TM>;
     constexpr int S = C::kStages;
     constexpr int CH = C::kChunk;
+    constexpr int kPrefetch = prefetch_for(TMA_A);
     extern __shared__ uint8_t smem_raw[];
 
     const uint32_t raw_base = smem_u32(smem_raw);
     const uint32_t base = (raw_base + 1023u) & ~1023u;
     uint8_t *base_ptr = smem_raw + (base - raw_base);
-    const uint32_t bars = base + S * C::kStageBytes;
-    const uint32_t acc_full0 = bars + 8u * (2 * S);
+    const uint32_t bars = base + S * C::kStageBytes;  // full[s] = bars + 8s, empty[s] = bars + 8(S+s)
+    const uint32_t afull0 = bars + 8u * (2 * S);       // a_full[s]: TMA copy of stage s landed
+    const uint32_t acc_full0 = bars + 8u * (3 * S);
     const uint32_t acc_empty0 = acc_full0 + 16u;
     const uint32_t drain_bar = acc_empty0 + 16u;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(base_ptr + S * C::kStageBytes + 8 * (2 * S + 5));
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(base_ptr + S * C::kStageBytes + 8 * (3 * S + 5));
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     volatile int *s_last = reinterpret_cast<volatile int *>(tmem_slot + 2);
 
@@ -275,6 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < S; ++s) {
             mbar_init(bars + 8u * s, kProdThreads);  // full: every producer thread arrives
             mbar_init(bars + 8u * (S + s), 1);       // empty: one tcgen05.commit
+            mbar_init(afull0 + 8u * s, 1);           // a_full: the TMA thread's expect_tx arrive
         }
         mbar_init(acc_full0, 1);
         mbar_init(acc_full0 + 8u, 1);
@@ -396,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // register buffers rotate: while one job is split and stored the
         // loads of the next kPrefetch-1 are in flight.
         const int ptid = threadIdx.x - kEpiWarps * 32;
-        constexpr int AJ = C::kAJobs;
+        constexpr int AJ = TMA_A ? 0 : C::kAJobs;
         int s = 0;
         uint32_t ph = 0;
         JobIter next;
@@ -421,8 +459,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < kPrefetch; ++i) {
                 if (done < loaded) {
                     // warp-uniform decision: tcgen05.st below is warp-collective
-                    const bool w = mbar_wait_bounded(bars + 8u * (S + s), ph ^ 1u, abort_flag, ctl,
-                                                     kStatusTimeoutProducer);
+                    bool w = mbar_wait_bounded(bars + 8u * (S + s), ph ^ 1u, abort_flag, ctl,
+                                               kStatusTimeoutProducer);
+                    if (TMA_A && w)
+                        w = mbar_wait_bounded(afull0 + 8u * s, ph, abort_flag, ctl, kStatusTimeoutProducer);
                     if (!__all_sync(0xffffffffu, w)) {
                         ok = false;
                         break;
@@ -449,7 +489,36 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
-    } else if (lane == 0) {
+    } else if (TMA_A && warp == kTmaWarp) {
+        // ------------------------------------------------------ TMA thread
+        if (lane == 0) {
+            prefetch_tmap(&tmap_a);
+            int s = 0;
+            uint32_t ph = 0;
+            uint32_t used = 0, last_ph = 0;  // per stage: copy issued / its phase parity
+            JobIter it;
+            it.start(sch, blockIdx.x);
+            while (it.valid(sch)) {
+                if (!mbar_wait_bounded(bars + 8u * (S + s), ph ^ 1u, abort_flag, ctl, kStatusTimeoutProducer))
+                    break;
+                mbar_arrive_expect_tx(afull0 + 8u * s, static_cast<uint32_t>(TM * kBK * 4));
+                tma_load_2d(base + s * C::kStageBytes + C::kOffAHi, &tmap_a, it.kt * kBK, it.c.mt * TM,
+                            afull0 + 8u * s);
+                used |= 1u << s;
+                last_ph = (last_ph & ~(1u << s)) | (ph << s);
+                it.advance(sch);
+                if (++s == S) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+            // every copy this thread issued has landed before the CTA can exit
+            volatile int no_abort = 0;
+            for (int t = 0; t < S; ++t)
+                if (used & (1u << t))
+                    mbar_wait_bounded(afull0 + 8u * t, (last_ph >> t) & 1u, &no_abort, ctl, kStatusTimeoutDrain);
+        }
+    } else if (warp == kMmaWarp && lane == 0) {
         // ------------------------------------------------------ MMA issuer
         int s = 0;
         uint32_t ph = 0;
