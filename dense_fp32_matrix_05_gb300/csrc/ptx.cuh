@@ -188,11 +188,23 @@ __device__ __forceinline__ void tmem_st32x4(uint32_t taddr, const uint32_t (&r)[
                  : "memory");
 }
 
-// N (4 or 8) consecutive columns.
+// Same with 16 columns.
+__device__ __forceinline__ void tmem_st32x16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+
+// N (4, 8 or 16) consecutive columns.
 template <int N>
 __device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t (&r)[N]) {
-    static_assert(N == 4 || N == 8, "4 or 8 columns");
-    if constexpr (N == 8) {
+    static_assert(N == 4 || N == 8 || N == 16, "4, 8 or 16 columns");
+    if constexpr (N == 16) {
+        tmem_st32x16(taddr, r);
+    } else if constexpr (N == 8) {
         tmem_st32x8(taddr, r);
     } else {
         tmem_st32x4(taddr, r);

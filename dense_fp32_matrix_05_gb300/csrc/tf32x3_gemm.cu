@@ -58,7 +58,7 @@ cudaError_t launch_tm(const GemmArgs &g, const Schedule &s, const DeviceCtl &ctl
     auto kern = tf32x3::tf32x3_gemm_kernel<TM, TMA>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    kern<<<grid, tf32x3::kThreads, C::kSmemBytes, stream>>>(g, s, ctl, vec_a, map);
+    kern<<<grid, tf32x3::Roles<TM, TMA>::kThreads, C::kSmemBytes, stream>>>(g, s, ctl, vec_a, map);
     return cudaGetLastError();
 }
 

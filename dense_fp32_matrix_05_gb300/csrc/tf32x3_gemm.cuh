@@ -49,17 +49,30 @@ namespace tf32x3 {
 constexpr int kTileN = 128;  // C columns per tile (MMA M, tensor-memory lanes)
 constexpr int kBK = 16;      // K per stage: one 64-byte swizzled row per operand row
 constexpr int kEpiWarps = 4;
-constexpr int kProdWarps = 16;              // multiple of 4: each lane quadrant gets kProdWarps/4 warps
-constexpr int kProdThreads = kProdWarps * 32;
-constexpr int kBtK = kBK * 4 / kProdWarps;  // k values of one B^T column per producer thread
-constexpr int kMmaWarp = kEpiWarps + kProdWarps;
-constexpr int kTmaWarp = kMmaWarp + 1;
-constexpr int kThreads = (kEpiWarps + kProdWarps + 2) * 32;
 constexpr int kEpiBarrierId = 1;
 
-// Register buffers per producer thread (kPrefetch - 1 k-tiles of loads in
-// flight): A through TMA leaves only the B^T values in registers.
-__host__ __device__ constexpr int prefetch_for(bool tma_a) { return tma_a ? 6 : 3; }
+// Warp roles.  The producer warps form kGroups groups; group g fills the
+// k tiles (jobs) g, g + kGroups, g + 2 kGroups, ... of the CTA, so several
+// stages are being split at once.  Each group has a multiple of 4 warps (one
+// or more per tensor-memory lane quadrant); thread t of a group holds B^T
+// column t % 128 and kBtK of the stage's 16 k values.  kPrefetch register
+// buffers per producer thread: the loads of kPrefetch - 1 of its jobs are in
+// flight while it splits one.  With A arriving by TMA the registers only
+// hold B^T; without it they also hold A chunks, so wide tiles use fewer,
+// larger groups to stay within the register budget.
+template <int TM, bool TMA_A>
+struct Roles {
+    static constexpr int kProdWarps = 16;
+    static constexpr int kGroups = (TMA_A || TM <= 64) ? 4 : 2;
+    static constexpr int kWarpsPerGroup = kProdWarps / kGroups;
+    static_assert(kWarpsPerGroup % 4 == 0, "each group covers the four lane quadrants");
+    static constexpr int kGroupThreads = kWarpsPerGroup * 32;
+    static constexpr int kBtK = kBK * 4 / kWarpsPerGroup;
+    static constexpr int kPrefetch = 2;
+    static constexpr int kMmaWarp = kEpiWarps + kProdWarps;
+    static constexpr int kTmaWarp = kMmaWarp + 1;
+    static constexpr int kThreads = (kEpiWarps + kProdWarps + 2) * 32;
+};
 
 // Tensor memory (512 columns of 128 lanes x 32 bit): accumulators of TM
 // columns each, then a ring of STAGES B^T stages of 32 columns (16 hi + 16 lo
@@ -82,7 +95,6 @@ struct Cfg {
     static_assert(kStageBytes % 1024 == 0, "stages must keep 1 KB alignment");
     static constexpr int kRingCol = kNacc * TM;
     static_assert(kRingCol + kStages * kRingColsPerStage <= static_cast<int>(kTmemCols), "tensor memory");
-    static constexpr int kAJobs = (TM * 4 + kProdThreads - 1) / kProdThreads;
     static constexpr int kChunk = TM < 32 ? 16 : 32;
     static constexpr uint32_t kIdesc = umma_idesc_tf32(kTileN, TM);
     // barriers: full[S], empty[S], a_full[S], acc_full[2], acc_empty[2],
@@ -112,36 +124,36 @@ __device__ __forceinline__ void split_tf32(float x, uint32_t &hi, uint32_t &lo) 
 }
 
 // One k-tile of operands held in a producer thread's registers.
-template <int AJ>
+template <int BK_, int AJ>
 struct Raw {
-    float b[kBtK];   // B^T: kBtK consecutive k of one column n
+    float b[BK_];    // B^T: BK_ consecutive k of one column n
     float a[AJ][4];  // A chunks: 4 consecutive k of one row m
 };
-template <>
-struct Raw<0> {
-    float b[kBtK];
+template <int BK_>
+struct Raw<BK_, 0> {
+    float b[BK_];
 };
 
 // Producer: load one k-tile (K-range [k0, k0+16)) into registers; out-of-range
-// elements read as 0.  Thread ptid holds B[k0+kBtK*h .. +kBtK-1][n0+(ptid&127)]
-// with h = ptid >> 7 (its tensor-memory lane is its column), and A chunks
-// j = ptid + kProdThreads * r: row j >> 2, k chunk j & 3.
-template <int TM, int AJ>
+// elements read as 0.  Thread gt of a group holds B[k0+BtK*h .. +BtK-1][n0+(gt&127)]
+// with h = gt >> 7 (its tensor-memory lane is its column), and A chunks
+// j = gt + GT * r: row j >> 2, k chunk j & 3 (GT threads per group).
+template <int TM, int BtK, int GT, int AJ>
 __device__ __forceinline__ void load_raw(const GemmArgs &g, bool vec_a, int m0, int n0, int k0,
-                                         int ptid, Raw<AJ> &raw) {
+                                         int ptid, Raw<BtK, AJ> &raw) {
     {
         const int n = n0 + (ptid & (kTileN - 1));
-        const int kb = k0 + (ptid >> 7) * kBtK;
+        const int kb = k0 + (ptid >> 7) * BtK;
         const bool n_ok = n < g.N;
         const float *src = g.B + static_cast<long long>(kb) * g.ldb + n;
 #pragma unroll
-        for (int e = 0; e < kBtK; ++e)
+        for (int e = 0; e < BtK; ++e)
             raw.b[e] = (n_ok && kb + e < g.K) ? __ldg(src + e * g.ldb) : 0.f;
     }
     if constexpr (AJ > 0) {
 #pragma unroll
         for (int r = 0; r < AJ; ++r) {
-            const int j = ptid + r * kProdThreads;
+            const int j = ptid + r * GT;
             float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
             if (j < TM * 4) {
                 const int m = m0 + (j >> 2);
@@ -181,21 +193,22 @@ __device__ __forceinline__ void split_store4(uint32_t hi_addr, uint32_t lo_addr,
 // lanes; A hi/lo into the shared-memory stage at `stage`, from registers
 // (AJ > 0) or, after a TMA copy, from the raw tile in the hi buffer (split in
 // place: each thread reads and rewrites its own chunks).
-template <int TM, int AJ>
-__device__ __forceinline__ void store_split(uint32_t stage, uint32_t ring_taddr, int ptid, const Raw<AJ> &raw) {
+template <int TM, int BtK, int GT, int AJ, int AJ_TMA>
+__device__ __forceinline__ void store_split(uint32_t stage, uint32_t ring_taddr, int ptid,
+                                            const Raw<BtK, AJ> &raw) {
     using C = Cfg<TM>;
     {
-        uint32_t hi[kBtK], lo[kBtK];
+        uint32_t hi[BtK], lo[BtK];
 #pragma unroll
-        for (int e = 0; e < kBtK; ++e) split_tf32(raw.b[e], hi[e], lo[e]);
-        const uint32_t t = ring_taddr + static_cast<uint32_t>((ptid >> 7) * kBtK);
-        tmem_st_cols<kBtK>(t, hi);
-        tmem_st_cols<kBtK>(t + kBK, lo);
+        for (int e = 0; e < BtK; ++e) split_tf32(raw.b[e], hi[e], lo[e]);
+        const uint32_t t = ring_taddr + static_cast<uint32_t>((ptid >> 7) * BtK);
+        tmem_st_cols<BtK>(t, hi);
+        tmem_st_cols<BtK>(t + kBK, lo);
     }
     if constexpr (AJ > 0) {
 #pragma unroll
         for (int r = 0; r < AJ; ++r) {
-            const int j = ptid + r * kProdThreads;
+            const int j = ptid + r * GT;
             if (j < TM * 4) {
                 const uint32_t off = sw64_off(j >> 2, j & 3);
                 split_store4(stage + C::kOffAHi + off, stage + C::kOffALo + off, raw.a[r]);
@@ -203,8 +216,8 @@ __device__ __forceinline__ void store_split(uint32_t stage, uint32_t ring_taddr,
         }
     } else {
 #pragma unroll
-        for (int r = 0; r < C::kAJobs; ++r) {
-            const int j = ptid + r * kProdThreads;
+        for (int r = 0; r < AJ_TMA; ++r) {
+            const int j = ptid + r * GT;
             if (j < TM * 4) {
                 const uint32_t off = sw64_off(j >> 2, j & 3);
                 const float4 v = lds128(stage + C::kOffAHi + off);
@@ -283,14 +296,15 @@ __device__ __forceinline__ void tmem_load_chunk(uint32_t taddr, float (&v)[Cfg<T
 // TMA_A: A rows are 16-byte aligned and tmap_a describes A (K x M, 64-byte
 // swizzle, box 16 x TM); otherwise the producers load A themselves.
 template <int TM, bool TMA_A>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Roles<TM, TMA_A>::kThreads, 1)
     tf32x3_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ Schedule sch,
                        const __grid_constant__ DeviceCtl ctl, int vec_a,
                        const __grid_constant__ CUtensorMap tmap_a) {
     using C = Cfg<TM>;
+    using R = Roles<TM, TMA_A>;
     constexpr int S = C::kStages;
     constexpr int CH = C::kChunk;
-    constexpr int kPrefetch = prefetch_for(TMA_A);
+    static_assert(R::kGroups <= S, "a group's next stage must not wrap the ring twice");
     extern __shared__ uint8_t smem_raw[];
 
     const uint32_t raw_base = smem_u32(smem_raw);
@@ -310,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            mbar_init(bars + 8u * s, kProdThreads);  // full: every producer thread arrives
+            mbar_init(bars + 8u * s, R::kGroupThreads);  // full: every thread of the filling group
             mbar_init(bars + 8u * (S + s), 1);       // empty: one tcgen05.commit
             mbar_init(afull0 + 8u * s, 1);           // a_full: the TMA thread's expect_tx arrive
         }
@@ -323,7 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         *s_last = 0;
         fence_mbar_init();
     }
-    if (warp == kMmaWarp) {
+    if (warp == R::kMmaWarp) {
         tmem_alloc(smem_u32(tmem_slot), kTmemCols);
         tmem_relinquish();
     }
@@ -428,24 +442,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
-    } else if (warp < kMmaWarp) {
+    } else if (warp < R::kMmaWarp) {
         // ------------------------------------------------------ producers
-        // Jobs are the (unit, k tile) pairs of this CTA in order.  kPrefetch
-        // register buffers rotate: while one job is split and stored the
-        // loads of the next kPrefetch-1 are in flight.
-        const int ptid = threadIdx.x - kEpiWarps * 32;
-        constexpr int AJ = TMA_A ? 0 : C::kAJobs;
-        int s = 0;
+        // Group g fills the jobs (unit, k tile) q = g, g + G, g + 2G, ... of
+        // this CTA (G = kGroups), job q into stage q % S.  kPrefetch register
+        // buffers rotate: while one job is split and stored, the loads of the
+        // group's next kPrefetch-1 jobs are in flight.
+        constexpr int G = R::kGroups;
+        constexpr int GT = R::kGroupThreads;
+        constexpr int BtK = R::kBtK;
+        constexpr int AJ_ALL = (TM * 4 + GT - 1) / GT;
+        constexpr int AJ = TMA_A ? 0 : AJ_ALL;
+        constexpr int NB = R::kPrefetch;
+        const int group = (warp - kEpiWarps) / R::kWarpsPerGroup;
+        const int gt = threadIdx.x - kEpiWarps * 32 - group * GT;  // thread index within the group
+        int s = group;  // stage of the group's current job (q % S, with G <= S)
         uint32_t ph = 0;
         JobIter next;
         next.start(sch, blockIdx.x);
-        Raw<AJ> buf[kPrefetch];
+        for (int i = 0; i < group && next.valid(sch); ++i) next.advance(sch);
+        Raw<BtK, AJ> buf[NB];
         int loaded = 0, done = 0;
 #pragma unroll
-        for (int i = 0; i < kPrefetch; ++i) {
+        for (int i = 0; i < NB; ++i) {
             if (next.valid(sch)) {
-                load_raw<TM, AJ>(g, vec_a != 0, next.c.mt * TM, next.c.nt * kTileN, next.kt * kBK, ptid, buf[i]);
-                next.advance(sch);
+                load_raw<TM, BtK, GT, AJ>(g, vec_a != 0, next.c.mt * TM, next.c.nt * kTileN, next.kt * kBK, gt,
+                                          buf[i]);
+                for (int t = 0; t < G && next.valid(sch); ++t) next.advance(sch);
                 ++loaded;
             }
         }
@@ -456,7 +479,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
         while (ok && done < loaded) {
 #pragma unroll
-            for (int i = 0; i < kPrefetch; ++i) {
+            for (int i = 0; i < NB; ++i) {
                 if (done < loaded) {
                     // warp-uniform decision: tcgen05.st below is warp-collective
                     bool w = mbar_wait_bounded(bars + 8u * (S + s), ph ^ 1u, abort_flag, ctl,
@@ -468,28 +491,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    store_split<TM, AJ>(base + s * C::kStageBytes,
-                                        ring_lane + static_cast<uint32_t>(s * kRingColsPerStage), ptid, buf[i]);
+                    store_split<TM, BtK, GT, AJ, AJ_ALL>(base + s * C::kStageBytes,
+                                                         ring_lane + static_cast<uint32_t>(s * kRingColsPerStage),
+                                                         gt, buf[i]);
                     fence_proxy_async_smem();
                     tmem_st_wait();
                     tc_fence_before();
-                    const bool withhold = done == 0 && (ctl.debug_flags & kDebugWithholdArrive) && ptid == 0;
+                    const bool withhold =
+                        done == 0 && group == 0 && gt == 0 && (ctl.debug_flags & kDebugWithholdArrive);
                     if (!withhold) mbar_arrive(bars + 8u * s);
                     ++done;
-                    if (++s == S) {
-                        s = 0;
+                    s += G;
+                    if (s >= S) {
+                        s -= S;
                         ph ^= 1u;
                     }
                     if (next.valid(sch)) {
-                        load_raw<TM, AJ>(g, vec_a != 0, next.c.mt * TM, next.c.nt * kTileN, next.kt * kBK, ptid,
-                                         buf[i]);
-                        next.advance(sch);
+                        load_raw<TM, BtK, GT, AJ>(g, vec_a != 0, next.c.mt * TM, next.c.nt * kTileN, next.kt * kBK,
+                                                  gt, buf[i]);
+                        for (int t = 0; t < G && next.valid(sch); ++t) next.advance(sch);
                         ++loaded;
                     }
                 }
             }
         }
-    } else if (TMA_A && warp == kTmaWarp) {
+    } else if (TMA_A && warp == R::kTmaWarp) {
         // ------------------------------------------------------ TMA thread
         if (lane == 0) {
             prefetch_tmap(&tmap_a);
@@ -518,7 +544,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (used & (1u << t))
                     mbar_wait_bounded(afull0 + 8u * t, (last_ph >> t) & 1u, &no_abort, ctl, kStatusTimeoutDrain);
         }
-    } else if (warp == kMmaWarp && lane == 0) {
+    } else if (warp == R::kMmaWarp && lane == 0) {
         // ------------------------------------------------------ MMA issuer
         int s = 0;
         uint32_t ph = 0;
@@ -569,7 +595,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     tc_fence_before();
     __syncthreads();
-    if (warp == kMmaWarp) {
+    if (warp == R::kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem_base, kTmemCols);
     }
