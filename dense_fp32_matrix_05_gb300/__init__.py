@@ -18,7 +18,8 @@ from . import _build_ext
 
 __all__ = [
     "SGEMM_ALGO_AUTO", "SGEMM_ALGO_FFMA", "SGEMM_ALGO_TF32X3",
-    "SGEMM_FLAG_DEBUG_WITHHOLD_ARRIVE", "SGEMM_FLAG_TILE_ROWS", "SGEMM_ERR_DEVICE_TIMEOUT",
+    "SGEMM_FLAG_DEBUG_WITHHOLD_ARRIVE", "SGEMM_FLAG_TILE_ROWS", "SGEMM_FLAG_WHOLE_TILES",
+    "SGEMM_ERR_DEVICE_TIMEOUT",
     "SgemmError", "library", "lib_path", "declared_functions",
     "sgemm", "sgemm_ex", "sgemm_host", "sgemm_plan_info", "sgemm_check_status",
     "sgemm_status_string", "sgemm_release", "sgemm_version", "sgemm_noalloc", "matmul",
@@ -29,6 +30,7 @@ SGEMM_ALGO_AUTO = 0
 SGEMM_ALGO_FFMA = 1
 SGEMM_ALGO_TF32X3 = 2
 SGEMM_FLAG_DEBUG_WITHHOLD_ARRIVE = 1
+SGEMM_FLAG_WHOLE_TILES = 2
 
 
 def SGEMM_FLAG_TILE_ROWS(r: int) -> int:
@@ -141,7 +143,7 @@ def sgemm_host(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, algo=0) -> int:
 
 
 _PLAN_KEYS = ["path", "tile_m", "tile_n", "splits", "units", "grid", "stages", "vec_a", "vec_b",
-              "ws_bytes"]
+              "ws_bytes", "tail_tiles"]
 
 
 def sgemm_plan_info(M, N, K, A=0, lda=None, B=0, ldb=None, C=0, ldc=None, algo=0, splits=0,

@@ -153,6 +153,26 @@ void plan_tf32x3(int M, int N, int K, int sms, int splits_req, int flags, Plan &
     p.grid = std::min(s.units, sms);
     p.stages = sg::tf32x3_stages(tm);
     p.ws_bytes = s.splits > 1 ? static_cast<size_t>(s.units) * p.tile_n * tm * sizeof(float) : 0;
+    // Split tail: when whole tiles leave the last wave partly empty, the
+    // whole waves stay as they are and the leftover tiles are cut into K
+    // slices so that the last wave keeps (almost) every SM busy.
+    if (splits_req == 0 && s.splits == 1 && !(flags & SGEMM_FLAG_WHOLE_TILES)) {
+        const int grid = sms;
+        const int waves = tiles / grid, rem = tiles % grid;
+        // with few waves the tail's partial-tile traffic and last-arriver sums
+        // cost more than the idle SMs it saves (measured: a loss at 5 waves,
+        // a gain at 13)
+        if (waves >= 8 && rem != 0) {
+            const int ts = std::min(grid / rem, s.k_tiles / 8);
+            if (ts >= 2) {
+                s.dp_tiles = waves * grid;
+                s.tail_tiles = rem;
+                s.tail_splits = ts;
+                p.grid = grid;
+                p.ws_bytes = static_cast<size_t>(rem) * ts * p.tile_n * tm * sizeof(float);
+            }
+        }
+    }
 }
 
 void plan_ffma(int M, int N, int K, int sms, int splits_req, Plan &p) {
@@ -200,7 +220,7 @@ size_t span_bytes(int rows, int cols, long long ld) {
 }
 
 bool flags_valid(int flags) {
-    if (flags & ~(SGEMM_FLAG_DEBUG_WITHHOLD_ARRIVE | 0xFF00)) return false;
+    if (flags & ~(SGEMM_FLAG_DEBUG_WITHHOLD_ARRIVE | SGEMM_FLAG_WHOLE_TILES | 0xFF00)) return false;
     const int tm = forced_tile_rows(flags);
     return tm == 0 || sg::tf32x3_supported_tm(tm);
 }
@@ -289,7 +309,7 @@ int run(int M, int N, int K, float alpha, const float *A, int lda, const float *
         ctl.status = d->status;
         ctl.wait_budget = (flags & SGEMM_FLAG_DEBUG_WITHHOLD_ARRIVE) ? kDebugWaitBudget : kWaitBudget;
         ctl.debug_flags = (flags & SGEMM_FLAG_DEBUG_WITHHOLD_ARRIVE) ? sg::kDebugWithholdArrive : 0;
-        if (p.sch.splits > 1) {
+        if (p.ws_bytes > 0) {  // split-K or split tail: tiles shared by several units
             Workspace *w = nullptr;
             rc = get_workspace(*d, stream, p.ws_bytes,
                                static_cast<size_t>(p.sch.m_tiles) * p.sch.n_tiles, &w);
@@ -301,7 +321,7 @@ int run(int M, int N, int K, float alpha, const float *A, int lda, const float *
     GemmArgs g{M, N, K, alpha, beta, A, lda, B, ldb, C, ldc};
     cudaError_t e;
     if (p.path == SGEMM_ALGO_TF32X3)
-        e = sg::tf32x3_launch(p.tile_m, g, p.sch, ctl, p.vec_a, p.grid, stream);
+        e = sg::tf32x3_launch(p.tile_m, g, p.sch, ctl, p.vec_a, p.vec_b, p.grid, stream);
     else
         e = sg::ffma_launch(p.tile_m, p.tile_n, g, p.sch, ctl, p.vec_a, p.vec_b, p.vec_c, stream);
     return from_cuda(e);
@@ -402,7 +422,7 @@ int sgemm_plan_info(int M, int N, int K, const void *A, int lda, const void *B, 
         if (rc != 0) return rc;
         sms = d->sms;
     }
-    int vals[10] = {0};
+    int vals[11] = {0};
     if (M > 0 && N > 0 && K > 0) {
         Plan p;
         int rc = make_plan(M, N, K, A, lda, B, ldb, C, ldc, algo, splits, flags, sms, p);
@@ -417,8 +437,9 @@ int sgemm_plan_info(int M, int N, int K, const void *A, int lda, const void *B, 
         vals[7] = p.vec_a;
         vals[8] = p.vec_b;
         vals[9] = static_cast<int>(std::min<size_t>(p.ws_bytes, 0x7fffffff));
+        vals[10] = p.sch.tail_tiles;
     }
-    for (int i = 0; i < ninfo && i < 10; ++i) info[i] = vals[i];
+    for (int i = 0; i < ninfo && i < 11; ++i) info[i] = vals[i];
     return 0;
 }
 
@@ -526,14 +547,22 @@ int check_tensor_call(int M, int N, int K, float alpha, const float *A, int lda,
 }
 
 int plan_tensor_call(int M, int N, int K, const float *A, int lda, const float *B, int ldb, const float *C,
-                     int ldc, int splits, int sms, TensorPlan *out) {
+                     int ldc, int splits, int sms, size_t max_ws_floats, TensorPlan *out) {
     Plan p;
-    const int rc = make_plan(M, N, K, A, lda, B, ldb, C, ldc, SGEMM_ALGO_TF32X3, splits, 0, sms, p);
+    int rc = make_plan(M, N, K, A, lda, B, ldb, C, ldc, SGEMM_ALGO_TF32X3, splits, 0, sms, p);
     if (rc != 0) return rc;
+    if (p.sch.tail_tiles > 0 && p.ws_bytes / sizeof(float) > max_ws_floats) {
+        // the split tail is an optimisation: drop it rather than exceed the scratch
+        p = Plan();
+        rc = make_plan(M, N, K, A, lda, B, ldb, C, ldc, SGEMM_ALGO_TF32X3, splits, SGEMM_FLAG_WHOLE_TILES, sms,
+                       p);
+        if (rc != 0) return rc;
+    }
     out->tile_m = p.tile_m;
     out->sch = p.sch;
     out->grid = p.grid;
     out->vec_a = p.vec_a;
+    out->vec_b = p.vec_b;
     out->ws_floats = p.ws_bytes / sizeof(float);
     out->tiles = p.sch.m_tiles * p.sch.n_tiles;
     return 0;

@@ -14,6 +14,7 @@ enum : int {
     kStatusTimeoutMma = 2,
     kStatusTimeoutEpilogue = 4,
     kStatusTimeoutDrain = 8,
+    kStatusNoWorkspace = 16,  // a shared tile met a missing workspace (a planner bug)
 };
 
 // Test-only flag: withhold the first producer arrive (see the header).
@@ -32,42 +33,116 @@ struct GemmArgs {
     long long ldc;
 };
 
-// Work decomposition shared by both paths.  A work unit is one (tile, K
-// slice) pair; the K tiles of slice s are [s*KT/S, (s+1)*KT/S).
+// Work decomposition.  A work unit is one (tile, K range) pair; a tile whose
+// K range is spread over nseg > 1 units is finished by the last of its units
+// to arrive, which adds the partial tiles in segment order.
+//   Split-K (tail_tiles == 0): unit u = (tile u / S, slice u % S); slice s
+//     covers K tiles [s*KT/S, (s+1)*KT/S); units are strided over the grid.
+//   Whole waves + split tail (tail_tiles > 0): the first dp_tiles tiles (a
+//     whole number of waves over the grid) are whole units, strided over the
+//     grid, so every wave walks K in step and shares A/B slices in L2; the
+//     remaining tail_tiles (< one wave) are cut into tail_splits K slices, one
+//     slice per CTA, so the last wave is not left mostly idle.
 struct Schedule {
     int m_tiles, n_tiles;
-    int k_tiles;   // ceil(K / BK)
-    int splits;    // S >= 1
-    int units;     // m_tiles * n_tiles * S
-    int group_m;   // tile raster: groups of group_m tile rows, row index fastest
+    int k_tiles;      // ceil(K / BK)
+    int splits;       // S >= 1 (split-K)
+    int units;        // split-K: m_tiles * n_tiles * S
+    int group_m;      // tile raster: groups of group_m tile rows, row index fastest
+    int dp_tiles;     // whole-wave tiles
+    int tail_tiles;   // tiles after them, split along K (0 = split-K schedule)
+    int tail_splits;  // K slices per tail tile
 };
 
 struct DeviceCtl {
-    float *ws;           // split-K partial tiles: [tile][split][tile elements]
-    int *counters;       // split-K arrival counters, one per tile, kept at 0
+    float *ws;           // partial tiles, one slot of tile elements per unit of a shared tile
+    int *counters;       // arrival counters, one per tile, kept at 0
     int *status;         // device status word
     long long wait_budget;  // clock64 cycles a bounded wait may spin
     int debug_flags;
 };
 
 struct UnitCoord {
-    int mt, nt, tile, split, kb, ke;
+    int mt, nt, tile;
+    int kb, ke;       // K tiles [kb, ke)
+    int seg, nseg;    // this unit's index among the tile's units, and their count
+    long long slot0;  // workspace slot of segment 0 of this tile
 };
 
-__device__ __forceinline__ UnitCoord decode_unit(const Schedule &s, int u) {
-    UnitCoord c;
-    c.split = u % s.splits;
-    c.tile = u / s.splits;
+__device__ __forceinline__ void tile_coords(const Schedule &s, int tile, UnitCoord &c) {
     const int per_group = s.group_m * s.n_tiles;
-    const int g = c.tile / per_group;
-    const int r = c.tile - g * per_group;
+    const int g = tile / per_group;
+    const int r = tile - g * per_group;
     const int rows_here = min(s.group_m, s.m_tiles - g * s.group_m);
+    c.tile = tile;
     c.mt = g * s.group_m + r % rows_here;
     c.nt = r / rows_here;
-    c.kb = static_cast<int>((static_cast<long long>(c.split) * s.k_tiles) / s.splits);
-    c.ke = static_cast<int>((static_cast<long long>(c.split + 1) * s.k_tiles) / s.splits);
+}
+
+// Unit u of a tile split into `splits` K slices: slice u % splits of tile
+// first_tile + u / splits; its slots start at slot_base + (u / splits) * splits.
+__device__ __forceinline__ UnitCoord slice_unit(const Schedule &s, int first_tile, int u, int splits,
+                                                long long slot_base) {
+    UnitCoord c;
+    const int split = u % splits;
+    const int t = u / splits;
+    tile_coords(s, first_tile + t, c);
+    c.seg = split;
+    c.nseg = splits;
+    c.slot0 = slot_base + static_cast<long long>(t) * splits;
+    c.kb = static_cast<int>((static_cast<long long>(split) * s.k_tiles) / splits);
+    c.ke = static_cast<int>((static_cast<long long>(split + 1) * s.k_tiles) / splits);
     return c;
 }
+
+// Split-K unit u.
+__device__ __forceinline__ UnitCoord decode_unit(const Schedule &s, int u) {
+    return slice_unit(s, 0, u, s.splits, 0);
+}
+
+// The work units of one CTA, in order: next_unit() advances the position
+// (i: index of the next strided unit; tail: the tail slice was handed out)
+// and returns the unit there.  Every role of the CTA walks the same sequence.
+__device__ __forceinline__ bool next_unit(const Schedule &s, int cta, int &i, bool &tail, UnitCoord &c) {
+    if (s.tail_tiles == 0) {
+        const int u = cta + i * static_cast<int>(gridDim.x);
+        ++i;
+        if (u >= s.units) return false;
+        c = decode_unit(s, u);
+        return true;
+    }
+    const int t = cta + i * static_cast<int>(gridDim.x);
+    if (t < s.dp_tiles) {
+        ++i;
+        tile_coords(s, t, c);
+        c.kb = 0;
+        c.ke = s.k_tiles;
+        c.seg = 0;
+        c.nseg = 1;
+        c.slot0 = 0;
+        return true;
+    }
+    if (tail || cta >= s.tail_tiles * s.tail_splits) return false;
+    tail = true;
+    c = slice_unit(s, s.dp_tiles, cta, s.tail_splits, 0);
+    return true;
+}
+
+// Full unit coordinates (epilogue, MMA issuer).
+struct UnitIter {
+    int cta;
+    int i;
+    bool tail;
+    UnitCoord c;  // the current unit (valid while ok)
+    bool ok;
+    __device__ __forceinline__ void start(const Schedule &s, int cta_) {
+        cta = cta_;
+        i = 0;
+        tail = false;
+        next(s);
+    }
+    __device__ __forceinline__ void next(const Schedule &s) { ok = next_unit(s, cta, i, tail, c); }
+};
 
 // Spin on an mbarrier phase with a cycle budget.  Returns false when the
 // budget runs out (the status word and the CTA's abort flag are then set) or

@@ -170,9 +170,14 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     cp_async_wait<0>();
 
-    if (sch.splits > 1) {
+    if (c.nseg > 1 && (ctl.ws == nullptr || ctl.counters == nullptr)) {
+        // a shared tile without a workspace: report, never dereference
+        if (tid == 0) atomicOr(ctl.status, kStatusNoWorkspace);
+        return;
+    }
+    if (c.nseg > 1) {
         constexpr int kTileElems = BM * BN;
-        float *wt = ctl.ws + (static_cast<long long>(c.tile) * sch.splits + c.split) * kTileElems + tid * 64;
+        float *wt = ctl.ws + (c.slot0 + c.seg) * kTileElems + tid * 64;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             __stcg(reinterpret_cast<float4 *>(wt + i * 8), make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]));
@@ -182,18 +187,18 @@ __global__ void __launch_bounds__(kThreads, 2)
         __syncthreads();
         if (tid == 0) {
             const int prev = atomicAdd(ctl.counters + c.tile, 1);
-            s_last = (prev == sch.splits - 1) ? 1 : 0;
+            s_last = (prev == c.nseg - 1) ? 1 : 0;
         }
         __syncthreads();
         if (!s_last) return;
         __threadfence();
-        const float *wb = ctl.ws + static_cast<long long>(c.tile) * sch.splits * kTileElems + tid * 64;
+        const float *wb = ctl.ws + c.slot0 * kTileElems + tid * 64;
 #pragma unroll
         for (int i = 0; i < 8; ++i)
 #pragma unroll
             for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
 #pragma unroll 1
-        for (int sp = 0; sp < sch.splits; ++sp) {
+        for (int sp = 0; sp < c.nseg; ++sp) {
             const float *p = wb + static_cast<long long>(sp) * kTileElems;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {

@@ -16,7 +16,7 @@ bool tf32x3_supported_tm(int tm);
 int tf32x3_stages(int tm);
 int tf32x3_smem_bytes(int tm);
 cudaError_t tf32x3_launch(int tm, const GemmArgs &g, const Schedule &s, const DeviceCtl &ctl,
-                          int vec_a, int grid, cudaStream_t stream);
+                          int vec_a, int vec_b, int grid, cudaStream_t stream);
 
 // FFMA path.  (bm, bn) in {(128,128), (64,256), (32,512)}.
 bool ffma_supported_tile(int bm, int bn);
@@ -32,13 +32,14 @@ struct TensorPlan {
     Schedule sch{};
     int grid = 0;
     int vec_a = 0;
+    int vec_b = 0;
     size_t ws_floats = 0;  // split-K partial-tile floats needed (0 without split-K)
     int tiles = 0;         // output tiles (= arrival counters needed)
 };
 int check_tensor_call(int M, int N, int K, float alpha, const float *A, int lda, const float *B, int ldb,
                       float beta, const float *C, int ldc, int splits);
 int plan_tensor_call(int M, int N, int K, const float *A, int lda, const float *B, int ldb, const float *C,
-                     int ldc, int splits, int sms, TensorPlan *out);
+                     int ldc, int splits, int sms, size_t max_ws_floats, TensorPlan *out);
 
 // C = beta * C (alpha == 0 or K == 0).
 cudaError_t scale_c_launch(float *C, long long ldc, int M, int N, float beta, int num_sms,

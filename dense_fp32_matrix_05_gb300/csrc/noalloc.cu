@@ -90,12 +90,13 @@ extern "C" int sgemm_noalloc(int M, int N, int K, float alpha, const float *A, i
         if (beta == 1.f) return 0;
         return static_cast<int>(sg::scale_c_launch(C, ldc, M, N, beta, d->sms, st));
     }
-    if ((rc = sg::plan_tensor_call(M, N, K, A, lda, B, ldb, C, ldc, splits, d->sms, &plan)) != 0) return rc;
+    if ((rc = sg::plan_tensor_call(M, N, K, A, lda, B, ldb, C, ldc, splits, d->sms, kScratchFloats, &plan)) != 0)
+        return rc;
     sg::DeviceCtl ctl{};
     ctl.status = d->status;
     ctl.wait_budget = kWaitBudget;
     ctl.debug_flags = 0;
-    if (plan.sch.splits > 1) {
+    if (plan.ws_floats > 0) {  // split-K or split tail: tiles shared by several units
         if (plan.ws_floats > kScratchFloats || plan.tiles > kScratchCounters) return SGEMM_ERR_SCRATCH_LIMIT;
         // the array keeps the previous call's contents; the counters must
         // start at zero (a call that gave up a bounded wait can leave some set)
@@ -105,5 +106,6 @@ extern "C" int sgemm_noalloc(int M, int N, int K, float alpha, const float *A, i
         ctl.counters = d->counters;
     }
     sg::GemmArgs g{M, N, K, alpha, beta, A, lda, B, ldb, C, ldc};
-    return static_cast<int>(sg::tf32x3_launch(plan.tile_m, g, plan.sch, ctl, plan.vec_a, plan.grid, st));
+    return static_cast<int>(
+        sg::tf32x3_launch(plan.tile_m, g, plan.sch, ctl, plan.vec_a, plan.vec_b, plan.grid, st));
 }

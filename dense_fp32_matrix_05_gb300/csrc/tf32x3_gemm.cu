@@ -51,24 +51,51 @@ bool make_tmap_a(const GemmArgs &g, int tm, CUtensorMap *map) {
     return r == CUDA_SUCCESS;
 }
 
-template <int TM, bool TMA>
+// Tensor map of B for the TMA path of narrow tiles: a N x K fp32 tensor (N
+// innermost) with row stride ldb * 4 bytes, copied in boxes of 128 (n) x 16
+// (k) without swizzle, out-of-range elements filled with zeros.
+bool make_tmap_b(const GemmArgs &g, CUtensorMap *map) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(g.N), static_cast<cuuint64_t>(g.K)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(g.ldb) * sizeof(float)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(tf32x3::kTileN), static_cast<cuuint32_t>(tf32x3::kBK)};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(g.B), dims, strides,
+                           box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int TM, bool TA, bool TB>
 cudaError_t launch_tm(const GemmArgs &g, const Schedule &s, const DeviceCtl &ctl, int vec_a, int grid,
-                      const CUtensorMap &map, cudaStream_t stream) {
-    using C = tf32x3::Cfg<TM>;
-    auto kern = tf32x3::tf32x3_gemm_kernel<TM, TMA>;
+                      const CUtensorMap &map_a, const CUtensorMap &map_b, cudaStream_t stream) {
+    using C = tf32x3::Cfg<TM, TB>;
+    auto kern = tf32x3::tf32x3_gemm_kernel<TM, TA, TB>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    kern<<<grid, tf32x3::Roles<TM, TMA>::kThreads, C::kSmemBytes, stream>>>(g, s, ctl, vec_a, map);
+    kern<<<grid, tf32x3::Roles<TM, TA, TB>::kThreads, C::kSmemBytes, stream>>>(g, s, ctl, vec_a, map_a, map_b);
     return cudaGetLastError();
 }
 
+// Operands go through TMA whenever their rows are 16-byte aligned: the deep
+// asynchronous ring hides memory latency and the producers then hold almost
+// nothing in registers (the extra shared-memory pass for B^T is cheaper than
+// the register spills and load stalls it removes).
 template <int TM>
-cudaError_t launch_rows(const GemmArgs &g, const Schedule &s, const DeviceCtl &ctl, int vec_a, int grid,
-                        cudaStream_t stream) {
-    CUtensorMap map;
-    std::memset(&map, 0, sizeof(map));
-    if (vec_a && make_tmap_a(g, TM, &map)) return launch_tm<TM, true>(g, s, ctl, vec_a, grid, map, stream);
-    return launch_tm<TM, false>(g, s, ctl, vec_a, grid, map, stream);
+cudaError_t launch_rows(const GemmArgs &g, const Schedule &s, const DeviceCtl &ctl, int vec_a, int vec_b,
+                        int grid, cudaStream_t stream) {
+    CUtensorMap ma, mb;
+    std::memset(&ma, 0, sizeof(ma));
+    std::memset(&mb, 0, sizeof(mb));
+    const bool ta = vec_a && make_tmap_a(g, TM, &ma);
+    const bool tb = vec_b && make_tmap_b(g, &mb);
+    if (tb) {
+        if (ta) return launch_tm<TM, true, true>(g, s, ctl, vec_a, grid, ma, mb, stream);
+        return launch_tm<TM, false, true>(g, s, ctl, vec_a, grid, ma, mb, stream);
+    }
+    if (ta) return launch_tm<TM, true, false>(g, s, ctl, vec_a, grid, ma, mb, stream);
+    return launch_tm<TM, false, false>(g, s, ctl, vec_a, grid, ma, mb, stream);
 }
 
 }  // namespace
@@ -81,25 +108,25 @@ int tf32x3_stages(int tm) { return tf32x3::stages_for(tm); }
 
 int tf32x3_smem_bytes(int tm) {
     switch (tm) {
-        case 16: return tf32x3::Cfg<16>::kSmemBytes;
-        case 32: return tf32x3::Cfg<32>::kSmemBytes;
-        case 64: return tf32x3::Cfg<64>::kSmemBytes;
-        case 128: return tf32x3::Cfg<128>::kSmemBytes;
-        case 192: return tf32x3::Cfg<192>::kSmemBytes;
-        case 256: return tf32x3::Cfg<256>::kSmemBytes;
+        case 16: return tf32x3::Cfg<16, true>::kSmemBytes;
+        case 32: return tf32x3::Cfg<32, true>::kSmemBytes;
+        case 64: return tf32x3::Cfg<64, true>::kSmemBytes;
+        case 128: return tf32x3::Cfg<128, true>::kSmemBytes;
+        case 192: return tf32x3::Cfg<192, true>::kSmemBytes;
+        case 256: return tf32x3::Cfg<256, true>::kSmemBytes;
         default: return -1;
     }
 }
 
 cudaError_t tf32x3_launch(int tm, const GemmArgs &g, const Schedule &s, const DeviceCtl &ctl, int vec_a,
-                          int grid, cudaStream_t stream) {
+                          int vec_b, int grid, cudaStream_t stream) {
     switch (tm) {
-        case 16: return launch_rows<16>(g, s, ctl, vec_a, grid, stream);
-        case 32: return launch_rows<32>(g, s, ctl, vec_a, grid, stream);
-        case 64: return launch_rows<64>(g, s, ctl, vec_a, grid, stream);
-        case 128: return launch_rows<128>(g, s, ctl, vec_a, grid, stream);
-        case 192: return launch_rows<192>(g, s, ctl, vec_a, grid, stream);
-        case 256: return launch_rows<256>(g, s, ctl, vec_a, grid, stream);
+        case 16: return launch_rows<16>(g, s, ctl, vec_a, vec_b, grid, stream);
+        case 32: return launch_rows<32>(g, s, ctl, vec_a, vec_b, grid, stream);
+        case 64: return launch_rows<64>(g, s, ctl, vec_a, vec_b, grid, stream);
+        case 128: return launch_rows<128>(g, s, ctl, vec_a, vec_b, grid, stream);
+        case 192: return launch_rows<192>(g, s, ctl, vec_a, vec_b, grid, stream);
+        case 256: return launch_rows<256>(g, s, ctl, vec_a, vec_b, grid, stream);
         default: return cudaErrorInvalidValue;
     }
 }

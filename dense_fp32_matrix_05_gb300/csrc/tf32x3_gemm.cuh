@@ -60,10 +60,13 @@ constexpr int kEpiBarrierId = 1;
 // flight while it splits one.  With A arriving by TMA the registers only
 // hold B^T; without it they also hold A chunks, so wide tiles use fewer,
 // larger groups to stay within the register budget.
-template <int TM, bool TMA_A>
+template <int TM, bool TMA_A, bool TMA_B>
 struct Roles {
-    static constexpr int kProdWarps = 16;
-    static constexpr int kGroups = (TMA_A || TM <= 64) ? 4 : 2;
+    static constexpr bool kTma = TMA_A || TMA_B;  // the TMA thread fills stages
+    // With A copied by TMA the producers hold few registers: 12 warps in 3
+    // groups leave 96 registers per thread; otherwise 16 warps.
+    static constexpr int kProdWarps = TMA_A ? 12 : 16;
+    static constexpr int kGroups = TMA_A ? 3 : (TM <= 64 ? 4 : 2);
     static constexpr int kWarpsPerGroup = kProdWarps / kGroups;
     static_assert(kWarpsPerGroup % 4 == 0, "each group covers the four lane quadrants");
     static constexpr int kGroupThreads = kWarpsPerGroup * 32;
@@ -82,20 +85,23 @@ __host__ __device__ constexpr int stages_for(int tm) { return tm >= 256 ? 6 : 8;
 constexpr int kRingColsPerStage = 2 * kBK;
 constexpr uint32_t kTmemCols = 512;
 
-// TM = C rows per tile (MMA N).
-template <int TM>
+// TM = C rows per tile (MMA N).  TMA_B: the stage also holds the raw B tile
+// (16 k rows x 128 n, copied by TMA) that the producers read and split.
+template <int TM, bool TMA_B = false>
 struct Cfg {
     static_assert(TM % 16 == 0 && TM >= 16 && TM <= 256, "MMA N for M=128 must be 16..256, step 16");
-    static constexpr int kStages = stages_for(TM);
+    static constexpr int kStages = (TMA_B && TM >= 256) ? 5 : stages_for(TM);
     static constexpr int kNacc = nacc_for(TM);
     static constexpr int kABytes = TM * kBK * 4;  // A tile (MMA B operand), one of hi / lo
     static constexpr int kOffAHi = 0;             // also where TMA lands the raw A tile
     static constexpr int kOffALo = kABytes;
-    static constexpr int kStageBytes = 2 * kABytes;
+    static constexpr int kBRawBytes = TMA_B ? kBK * kTileN * 4 : 0;
+    static constexpr int kOffBRaw = 2 * kABytes;
+    static constexpr int kStageBytes = 2 * kABytes + kBRawBytes;
     static_assert(kStageBytes % 1024 == 0, "stages must keep 1 KB alignment");
     static constexpr int kRingCol = kNacc * TM;
     static_assert(kRingCol + kStages * kRingColsPerStage <= static_cast<int>(kTmemCols), "tensor memory");
-    static constexpr int kChunk = TM < 32 ? 16 : 32;
+    static constexpr int kChunk = 16;  // accumulator columns per tensor-memory load in the epilogue
     static constexpr uint32_t kIdesc = umma_idesc_tf32(kTileN, TM);
     // barriers: full[S], empty[S], a_full[S], acc_full[2], acc_empty[2],
     // drain; then tensor-memory address, abort flag, split-K "last" flag
@@ -133,6 +139,12 @@ template <int BK_>
 struct Raw<BK_, 0> {
     float b[BK_];
 };
+template <int AJ>
+struct Raw<0, AJ> {
+    float a[AJ][4];
+};
+template <>
+struct Raw<0, 0> {};
 
 // Producer: load one k-tile (K-range [k0, k0+16)) into registers; out-of-range
 // elements read as 0.  Thread gt of a group holds B[k0+BtK*h .. +BtK-1][n0+(gt&127)]
@@ -141,7 +153,7 @@ struct Raw<BK_, 0> {
 template <int TM, int BtK, int GT, int AJ>
 __device__ __forceinline__ void load_raw(const GemmArgs &g, bool vec_a, int m0, int n0, int k0,
                                          int ptid, Raw<BtK, AJ> &raw) {
-    {
+    if constexpr (BtK > 0) {
         const int n = n0 + (ptid & (kTileN - 1));
         const int kb = k0 + (ptid >> 7) * BtK;
         const bool n_ok = n < g.N;
@@ -193,17 +205,26 @@ __device__ __forceinline__ void split_store4(uint32_t hi_addr, uint32_t lo_addr,
 // lanes; A hi/lo into the shared-memory stage at `stage`, from registers
 // (AJ > 0) or, after a TMA copy, from the raw tile in the hi buffer (split in
 // place: each thread reads and rewrites its own chunks).
-template <int TM, int BtK, int GT, int AJ, int AJ_TMA>
+template <int TM, bool TMA_B, int KB, int BtK, int GT, int AJ, int AJ_TMA>
 __device__ __forceinline__ void store_split(uint32_t stage, uint32_t ring_taddr, int ptid,
                                             const Raw<BtK, AJ> &raw) {
-    using C = Cfg<TM>;
+    using C = Cfg<TM, TMA_B>;
     {
-        uint32_t hi[BtK], lo[BtK];
+        // KB k values of this thread's B^T column: from registers, or from the
+        // raw B tile (k rows of 128 floats) that TMA copied into the stage
+        uint32_t hi[KB], lo[KB];
+        if constexpr (TMA_B) {
+            const uint32_t col = stage + C::kOffBRaw + static_cast<uint32_t>((ptid & (kTileN - 1)) * 4);
+            const int kb = (ptid >> 7) * KB;
 #pragma unroll
-        for (int e = 0; e < BtK; ++e) split_tf32(raw.b[e], hi[e], lo[e]);
-        const uint32_t t = ring_taddr + static_cast<uint32_t>((ptid >> 7) * BtK);
-        tmem_st_cols<BtK>(t, hi);
-        tmem_st_cols<BtK>(t + kBK, lo);
+            for (int e = 0; e < KB; ++e) split_tf32(lds32f(col + static_cast<uint32_t>((kb + e) * kTileN * 4)), hi[e], lo[e]);
+        } else {
+#pragma unroll
+            for (int e = 0; e < KB; ++e) split_tf32(raw.b[e], hi[e], lo[e]);
+        }
+        const uint32_t t = ring_taddr + static_cast<uint32_t>((ptid >> 7) * KB);
+        tmem_st_cols<KB>(t, hi);
+        tmem_st_cols<KB>(t + kBK, lo);
     }
     if constexpr (AJ > 0) {
 #pragma unroll
@@ -245,22 +266,32 @@ __device__ __noinline__ float recompute_dot(const GemmArgs &g, int m, int n) {
 }
 
 // The (work unit, k tile) jobs of one CTA, in the order the producers fill
-// the pipeline: units blockIdx.x, blockIdx.x + gridDim.x, ..., each from its
-// first to its last k tile.
+// the pipeline: the CTA's units in next_unit order, each from its first to
+// its last k tile.  Keeps only what a producer needs (tile position, k tile,
+// end of the unit) to stay light on registers.
 struct JobIter {
-    int u;
-    UnitCoord c;
-    int kt;
-    __device__ __forceinline__ void start(const Schedule &s, int u0) {
-        u = u0;
-        if (u < s.units) {
-            c = decode_unit(s, u);
+    int cta, i;
+    bool tail, ok;
+    int mt, nt, kt, ke;
+    __device__ __forceinline__ void load(const Schedule &s) {
+        UnitCoord c;
+        ok = next_unit(s, cta, i, tail, c);
+        if (ok) {
+            mt = c.mt;
+            nt = c.nt;
             kt = c.kb;
+            ke = c.ke;
         }
     }
-    __device__ __forceinline__ bool valid(const Schedule &s) const { return u < s.units; }
+    __device__ __forceinline__ void start(const Schedule &s, int cta_) {
+        cta = cta_;
+        i = 0;
+        tail = false;
+        load(s);
+    }
+    __device__ __forceinline__ bool valid(const Schedule &) const { return ok; }
     __device__ __forceinline__ void advance(const Schedule &s) {
-        if (++kt >= c.ke) start(s, u + static_cast<int>(gridDim.x));
+        if (++kt >= ke) load(s);
     }
 };
 
@@ -295,13 +326,15 @@ __device__ __forceinline__ void tmem_load_chunk(uint32_t taddr, float (&v)[Cfg<T
 
 // TMA_A: A rows are 16-byte aligned and tmap_a describes A (K x M, 64-byte
 // swizzle, box 16 x TM); otherwise the producers load A themselves.
-template <int TM, bool TMA_A>
-__global__ void __launch_bounds__(Roles<TM, TMA_A>::kThreads, 1)
+// TMA_B: B rows are 16-byte aligned and tmap_b describes B (N x K, box
+// 128 x 16, no swizzle); otherwise the producers load B^T themselves.
+template <int TM, bool TMA_A, bool TMA_B>
+__global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
     tf32x3_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ Schedule sch,
                        const __grid_constant__ DeviceCtl ctl, int vec_a,
-                       const __grid_constant__ CUtensorMap tmap_a) {
-    using C = Cfg<TM>;
-    using R = Roles<TM, TMA_A>;
+                       const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b) {
+    using C = Cfg<TM, TMA_B>;
+    using R = Roles<TM, TMA_A, TMA_B>;
     constexpr int S = C::kStages;
     constexpr int CH = C::kChunk;
     static_assert(R::kGroups <= S, "a group's next stage must not wrap the ring twice");
@@ -350,8 +383,9 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A>::kThreads, 1)
         // ------------------------------------------------------ epilogue
         const int nl = warp * 32 + lane;  // tensor-memory lane = column within the tile
         int it = 0;
-        for (int u = blockIdx.x; u < sch.units; u += gridDim.x, ++it) {
-            const UnitCoord c = decode_unit(sch, u);
+        UnitIter ui;
+        for (ui.start(sch, blockIdx.x); ui.ok; ui.next(sch), ++it) {
+            const UnitCoord &c = ui.c;
             const int acc = it % C::kNacc;
             const uint32_t aph = (it / C::kNacc) & 1;
             const bool w = mbar_wait_bounded(acc_full0 + 8u * acc, aph, abort_flag, ctl,
@@ -362,7 +396,7 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A>::kThreads, 1)
             const int m0 = c.mt * TM;
             const uint32_t t0 = tmem_base + (static_cast<uint32_t>(warp * 32) << 16) +
                                 static_cast<uint32_t>(acc * TM);
-            if (sch.splits == 1) {
+            if (c.nseg == 1) {
 #pragma unroll 1
                 for (int ch = 0; ch < TM / CH; ++ch) {
                     float v[CH];
@@ -390,11 +424,16 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A>::kThreads, 1)
                 }
                 tc_fence_before();
                 mbar_arrive(acc_empty0 + 8u * acc);
+            } else if (ctl.ws == nullptr || ctl.counters == nullptr) {
+                // a shared tile without a workspace: report, never dereference
+                tc_fence_before();
+                mbar_arrive(acc_empty0 + 8u * acc);
+                if (threadIdx.x == 0) atomicOr(ctl.status, kStatusNoWorkspace);
             } else {
-                // split-K: write this slice's partial tile, then the last
-                // slice to arrive adds all partials in slice order
+                // shared tile: write this unit's partial tile, then the last
+                // unit to arrive adds all partials in segment order
                 constexpr int kTileElems = kTileN * TM;
-                float *wt = ctl.ws + (static_cast<long long>(c.tile) * sch.splits + c.split) * kTileElems;
+                float *wt = ctl.ws + (c.slot0 + c.seg) * kTileElems;
 #pragma unroll 1
                 for (int ch = 0; ch < TM / CH; ++ch) {
                     float v[CH];
@@ -408,23 +447,36 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A>::kThreads, 1)
                 named_bar_sync(kEpiBarrierId, kEpiWarps * 32);
                 if (threadIdx.x == 0) {
                     const int prev = atomicAdd(ctl.counters + c.tile, 1);
-                    *s_last = (prev == sch.splits - 1) ? 1 : 0;
+                    *s_last = (prev == c.nseg - 1) ? 1 : 0;
                 }
                 named_bar_sync(kEpiBarrierId, kEpiWarps * 32);
                 if (*s_last) {
                     __threadfence();
-                    const float *wb = ctl.ws + static_cast<long long>(c.tile) * sch.splits * kTileElems;
+                    const float *wb = ctl.ws + c.slot0 * kTileElems;
                     if (n < g.N) {
 #pragma unroll 1
                         for (int mb = 0; mb < TM; mb += 8) {
                             float sum[8];
 #pragma unroll
                             for (int j = 0; j < 8; ++j) sum[j] = 0.f;
+                            // two segments' loads in flight at once, then added
+                            // in segment order (the order fixes the bits)
 #pragma unroll 1
-                            for (int sp = 0; sp < sch.splits; ++sp) {
-                                const float *p = wb + static_cast<long long>(sp) * kTileElems + mb * kTileN + nl;
+                            for (int sp0 = 0; sp0 < c.nseg; sp0 += 2) {
+                                float v[2][8];
 #pragma unroll
-                                for (int j = 0; j < 8; ++j) sum[j] += __ldcg(p + j * kTileN);
+                                for (int q = 0; q < 2; ++q) {
+                                    const float *p = wb + static_cast<long long>(sp0 + q) * kTileElems +
+                                                     mb * kTileN + nl;
+#pragma unroll
+                                    for (int j = 0; j < 8; ++j)
+                                        v[q][j] = (sp0 + q < c.nseg) ? __ldcg(p + j * kTileN) : 0.f;
+                                }
+#pragma unroll
+                                for (int q = 0; q < 2; ++q)
+                                    if (sp0 + q < c.nseg)
+#pragma unroll
+                                        for (int j = 0; j < 8; ++j) sum[j] += v[q][j];
                             }
 #pragma unroll
                             for (int j = 0; j < 8; ++j) {
@@ -450,7 +502,8 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A>::kThreads, 1)
         // group's next kPrefetch-1 jobs are in flight.
         constexpr int G = R::kGroups;
         constexpr int GT = R::kGroupThreads;
-        constexpr int BtK = R::kBtK;
+        constexpr int KB = R::kBtK;                  // B^T k values per thread and job
+        constexpr int BtK = TMA_B ? 0 : KB;          // ... held in registers
         constexpr int AJ_ALL = (TM * 4 + GT - 1) / GT;
         constexpr int AJ = TMA_A ? 0 : AJ_ALL;
         constexpr int NB = R::kPrefetch;
@@ -466,7 +519,7 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A>::kThreads, 1)
 #pragma unroll
         for (int i = 0; i < NB; ++i) {
             if (next.valid(sch)) {
-                load_raw<TM, BtK, GT, AJ>(g, vec_a != 0, next.c.mt * TM, next.c.nt * kTileN, next.kt * kBK, gt,
+                load_raw<TM, BtK, GT, AJ>(g, vec_a != 0, next.mt * TM, next.nt * kTileN, next.kt * kBK, gt,
                                           buf[i]);
                 for (int t = 0; t < G && next.valid(sch); ++t) next.advance(sch);
                 ++loaded;
@@ -484,14 +537,14 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A>::kThreads, 1)
                     // warp-uniform decision: tcgen05.st below is warp-collective
                     bool w = mbar_wait_bounded(bars + 8u * (S + s), ph ^ 1u, abort_flag, ctl,
                                                kStatusTimeoutProducer);
-                    if (TMA_A && w)
+                    if (R::kTma && w)
                         w = mbar_wait_bounded(afull0 + 8u * s, ph, abort_flag, ctl, kStatusTimeoutProducer);
                     if (!__all_sync(0xffffffffu, w)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    store_split<TM, BtK, GT, AJ, AJ_ALL>(base + s * C::kStageBytes,
+                    store_split<TM, TMA_B, KB, BtK, GT, AJ, AJ_ALL>(base + s * C::kStageBytes,
                                                          ring_lane + static_cast<uint32_t>(s * kRingColsPerStage),
                                                          gt, buf[i]);
                     fence_proxy_async_smem();
@@ -507,7 +560,7 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A>::kThreads, 1)
                         ph ^= 1u;
                     }
                     if (next.valid(sch)) {
-                        load_raw<TM, BtK, GT, AJ>(g, vec_a != 0, next.c.mt * TM, next.c.nt * kTileN, next.kt * kBK,
+                        load_raw<TM, BtK, GT, AJ>(g, vec_a != 0, next.mt * TM, next.nt * kTileN, next.kt * kBK,
                                                   gt, buf[i]);
                         for (int t = 0; t < G && next.valid(sch); ++t) next.advance(sch);
                         ++loaded;
@@ -515,10 +568,12 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A>::kThreads, 1)
                 }
             }
         }
-    } else if (TMA_A && warp == R::kTmaWarp) {
+    } else if (R::kTma && warp == R::kTmaWarp) {
         // ------------------------------------------------------ TMA thread
         if (lane == 0) {
-            prefetch_tmap(&tmap_a);
+            if (TMA_A) prefetch_tmap(&tmap_a);
+            if (TMA_B) prefetch_tmap(&tmap_b);
+            constexpr uint32_t kTx = (TMA_A ? TM * kBK * 4 : 0) + (TMA_B ? kBK * kTileN * 4 : 0);
             int s = 0;
             uint32_t ph = 0;
             uint32_t used = 0, last_ph = 0;  // per stage: copy issued / its phase parity
@@ -527,9 +582,13 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A>::kThreads, 1)
             while (it.valid(sch)) {
                 if (!mbar_wait_bounded(bars + 8u * (S + s), ph ^ 1u, abort_flag, ctl, kStatusTimeoutProducer))
                     break;
-                mbar_arrive_expect_tx(afull0 + 8u * s, static_cast<uint32_t>(TM * kBK * 4));
-                tma_load_2d(base + s * C::kStageBytes + C::kOffAHi, &tmap_a, it.kt * kBK, it.c.mt * TM,
-                            afull0 + 8u * s);
+                mbar_arrive_expect_tx(afull0 + 8u * s, kTx);
+                if (TMA_A)
+                    tma_load_2d(base + s * C::kStageBytes + C::kOffAHi, &tmap_a, it.kt * kBK, it.mt * TM,
+                                afull0 + 8u * s);
+                if (TMA_B)
+                    tma_load_2d(base + s * C::kStageBytes + C::kOffBRaw, &tmap_b, it.nt * kTileN, it.kt * kBK,
+                                afull0 + 8u * s);
                 used |= 1u << s;
                 last_ph = (last_ph & ~(1u << s)) | (ph << s);
                 it.advance(sch);
@@ -550,8 +609,9 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A>::kThreads, 1)
         uint32_t ph = 0;
         int it = 0;
         bool ok = true;
-        for (int u = blockIdx.x; u < sch.units && ok; u += gridDim.x, ++it) {
-            const UnitCoord c = decode_unit(sch, u);
+        UnitIter ui;
+        for (ui.start(sch, blockIdx.x); ui.ok && ok; ui.next(sch), ++it) {
+            const UnitCoord &c = ui.c;
             const int acc = it % C::kNacc;
             const uint32_t aph = (it / C::kNacc) & 1;
             if (!mbar_wait_bounded(acc_empty0 + 8u * acc, aph ^ 1u, abort_flag, ctl, kStatusTimeoutMma)) {

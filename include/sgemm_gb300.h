@@ -66,6 +66,9 @@ typedef struct CUstream_st *sgemm_stream_t;
 /* SGEMM_FLAG_TILE_ROWS(r): 3xTF32 path only, force r C rows per tile
  * (r in 16, 32, 64, 128, 192, 256); 0 lets the planner choose. */
 #define SGEMM_FLAG_TILE_ROWS(r) ((((r) / 16) & 0xFF) << 8)
+/* SGEMM_FLAG_WHOLE_TILES: 3xTF32 path only, keep whole tiles in the last
+ * wave instead of splitting the leftover tiles along K over idle SMs. */
+#define SGEMM_FLAG_WHOLE_TILES 2
 #define SGEMM_FLAG_DEBUG_WITHHOLD_ARRIVE 1 /* test only: one pipeline arrive
                                               is withheld and the on-device
                                               wait budget is cut to ~1 ms, so
@@ -97,9 +100,18 @@ int sgemm(int M, int N, int K, float alpha,
  *                partial tile to a library-owned workspace and the last slice
  *                to finish adds the partials in slice order, so the result
  *                does not depend on timing.
- *   flags  (15): 0, SGEMM_FLAG_TILE_ROWS(r), and/or
- *                SGEMM_FLAG_DEBUG_WITHHOLD_ARRIVE (tests only).  Any other
- *                bit, or a tile height that is not supported, is rejected.
+ *   flags  (15): 0, or any of SGEMM_FLAG_TILE_ROWS(r),
+ *                SGEMM_FLAG_WHOLE_TILES and SGEMM_FLAG_DEBUG_WITHHOLD_ARRIVE
+ *                (tests only).  Any other bit, or a tile height that is not
+ *                supported, is rejected.
+ *
+ * Scheduling (3xTF32 path): persistent CTAs, one per SM.  When the output
+ * tiles are fewer than the SMs, K is split (splits).  When they are more but
+ * the last wave would be partly empty, whole waves keep whole tiles and the
+ * leftover tiles are cut into K slices, one per otherwise idle SM (split
+ * tail).  Tiles shared by several units are finished by the last unit to
+ * arrive, which adds the partial tiles in a fixed order, so the result does
+ * not depend on timing.
  *
  * The split-K workspace is owned by the library, kept per device and stream,
  * grown on demand (a synchronous cudaMalloc, so make the first call of a
@@ -138,6 +150,7 @@ int sgemm_host(int M, int N, int K, float alpha,
  *   [7] 1 if A is read with 16-byte vector loads
  *   [8] 1 if B is read with 16-byte vector loads
  *   [9] workspace bytes needed
+ *   [10] leftover tiles split along K after the whole waves (0 = none)
  * Returns 0, or -i for an invalid argument (the i-th argument of this
  * function, 1-based).
  */

@@ -62,7 +62,7 @@ def test_invalid_extended_arguments(lib):
     assert pkg.sgemm_ex(*base, 3, 0, 0) == -13
     assert pkg.sgemm_ex(*base, -1, 0, 0) == -13
     assert pkg.sgemm_ex(*base, 0, -1, 0) == -14
-    assert pkg.sgemm_ex(*base, 0, 0, 2) == -15
+    assert pkg.sgemm_ex(*base, 0, 0, 4) == -15
     assert pkg.sgemm_ex(*base, 0, 0, pkg.SGEMM_FLAG_TILE_ROWS(48)) == -15
     assert pkg.sgemm_ex(*base, 0, 0, 1 << 20) == -15
 
@@ -98,7 +98,7 @@ def test_plan_large_square_uses_tensor_path_without_split():
     assert p["path"] == pkg.SGEMM_ALGO_TF32X3
     assert (p["tile_m"], p["tile_n"]) == (256, 128)
     assert p["splits"] == 1 and p["units"] == 20 * 40 and p["grid"] == SMS
-    assert p["vec_a"] == 1 and p["vec_b"] == 1 and p["ws_bytes"] == 0
+    assert p["vec_a"] == 1 and p["vec_b"] == 1
 
 
 def test_plan_small_square_splits_k():
@@ -135,6 +135,20 @@ def test_plan_ffma_tiles():
     assert (plan(32, 4096, 64, algo=1)["tile_m"], plan(32, 4096, 64, algo=1)["tile_n"]) == (32, 512)
     assert plan(64, 4096, 64, algo=1)["tile_n"] == 256
     assert plan(4096, 4096, 4096, algo=1)["tile_n"] == 128
+
+
+def test_plan_split_tail():
+    """Tiles beyond many whole waves: the whole waves keep whole tiles, the
+    leftover tiles are cut into K slices over the otherwise idle SMs."""
+    p = plan(8192, 8192, 8192)          # 2048 tiles = 13 waves of 152 + 72
+    assert p["tail_tiles"] == 72 and p["grid"] == SMS
+    assert p["ws_bytes"] == 72 * (SMS // 72) * 256 * 128 * 4
+    q = plan(8192, 8192, 8192, flags=pkg.SGEMM_FLAG_WHOLE_TILES)
+    assert q["tail_tiles"] == 0 and q["ws_bytes"] == 0
+    assert plan(5120, 5120, 5120)["tail_tiles"] == 0    # 5 waves + 40: whole tiles measured faster
+    assert plan(4864, 4096, 4096)["tail_tiles"] == 0    # 19 x 32 = 608 tiles: 4 whole waves
+    assert plan(1024, 1024, 1024)["tail_tiles"] == 0    # fewer tiles than SMs: split-K instead
+    assert plan(8192, 8192, 8192, splits=1)["tail_tiles"] == 0  # explicit split count wins
 
 
 @pytest.mark.parametrize("rows", [16, 32, 64, 128, 192, 256])

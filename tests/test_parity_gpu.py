@@ -96,6 +96,28 @@ def test_every_tile_height(rows, shape):
         check_against_oracle(p, C, what=f"{shape} rows={rows} splits={splits}")
 
 
+TAIL_SHAPES = [(2560, 16384, 640), (8192, 8192, 256), (7000, 4700, 333)]
+
+
+@pytest.mark.parametrize("shape", TAIL_SHAPES, ids=[f"{m}x{n}x{k}" for m, n, k in TAIL_SHAPES])
+def test_split_tail(shape):
+    """Shapes whose leftover tiles after the whole waves are split along K,
+    checked on sampled rows against the oracle and the whole-tile schedule."""
+    M, N, K = shape
+    p = _with_c(random_problem(M, N, K, alpha=1.0, beta=-0.75, seed=M ^ N ^ K, pad_value=0.0))
+    info = pkg.sgemm_plan_info(M, N, K, algo=pkg.SGEMM_ALGO_TF32X3, num_sms=0)
+    assert info["tail_tiles"] > 0
+    rows = sample_rows(M, 40, seed=7)
+    C_sk, st = run_sgemm(p, pkg.SGEMM_ALGO_TF32X3)
+    assert st == 0
+    check_against_oracle(p, C_sk, rows=rows, what=f"{shape} split tail")
+    C_dp, st = run_sgemm(p, pkg.SGEMM_ALGO_TF32X3, flags=pkg.SGEMM_FLAG_WHOLE_TILES)
+    assert st == 0
+    check_against_oracle(p, C_dp, rows=rows, what=f"{shape} whole tiles")
+    C_sk2, _ = run_sgemm(p, pkg.SGEMM_ALGO_TF32X3)
+    assert np.array_equal(C_sk.view(np.uint32), C_sk2.view(np.uint32)), "split tail is not deterministic"
+
+
 @pytest.mark.parametrize("algo", ALGOS, ids=ALGO_IDS)
 @pytest.mark.parametrize("splits", [1, 2, 3, 7])
 def test_forced_split_k(algo, splits):
