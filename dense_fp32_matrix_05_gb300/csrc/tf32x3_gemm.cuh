@@ -83,6 +83,7 @@ struct Roles {
 __host__ __device__ constexpr int nacc_for(int tm) { return tm >= 192 ? 1 : 2; }
 __host__ __device__ constexpr int stages_for(int tm) { return tm >= 256 ? 6 : 8; }
 constexpr int kRingColsPerStage = 2 * kBK;
+constexpr int kSmemLimit = 232448;  // dynamic shared memory one CTA may use on sm_103a
 constexpr uint32_t kTmemCols = 512;
 
 // TM = C rows per tile (MMA N).  TMA_B: the stage also holds the raw B tile
@@ -90,7 +91,6 @@ constexpr uint32_t kTmemCols = 512;
 template <int TM, bool TMA_B = false>
 struct Cfg {
     static_assert(TM % 16 == 0 && TM >= 16 && TM <= 256, "MMA N for M=128 must be 16..256, step 16");
-    static constexpr int kStages = (TMA_B && TM >= 256) ? 5 : stages_for(TM);
     static constexpr int kNacc = nacc_for(TM);
     static constexpr int kABytes = TM * kBK * 4;  // A tile (MMA B operand), one of hi / lo
     static constexpr int kOffAHi = 0;             // also where TMA lands the raw A tile
@@ -98,6 +98,9 @@ struct Cfg {
     static constexpr int kBRawBytes = TMA_B ? kBK * kTileN * 4 : 0;
     static constexpr int kOffBRaw = 2 * kABytes;
     static constexpr int kStageBytes = 2 * kABytes + kBRawBytes;
+    // as many stages as tensor memory and the 227 KB of shared memory allow
+    static constexpr int kStages = stages_for(TM) < (kSmemLimit - 2048) / kStageBytes
+                                       ? stages_for(TM) : (kSmemLimit - 2048) / kStageBytes;
     static_assert(kStageBytes % 1024 == 0, "stages must keep 1 KB alignment");
     static constexpr int kRingCol = kNacc * TM;
     static_assert(kRingCol + kStages * kRingColsPerStage <= static_cast<int>(kTmemCols), "tensor memory");
@@ -107,6 +110,8 @@ struct Cfg {
     // drain; then tensor-memory address, abort flag, split-K "last" flag
     static constexpr int kBarBytes = 8 * (3 * kStages + 5) + 16;
     static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes;
+    static_assert(kSmemBytes <= kSmemLimit, "shared memory per CTA");
+    static_assert(kStages >= 4, "pipeline depth");
 };
 
 // Byte offset of the 16-byte chunk `chunk` (k / 4) of row `row` inside a
