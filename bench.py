@@ -65,10 +65,17 @@ def load_peaks():
 
 
 def kernel_source_hash() -> str:
+    """Hash of the kernel sources' code: comments and blank lines are left
+    out, so editing a comment does not retire a recorded ncu summary."""
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel)) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for line in text.splitlines():
+            code = re.sub(r"//.*", "", line).rstrip()
+            if code:
+                h.update(code.encode() + b"\n")
     return h.hexdigest()[:16]
 
 

@@ -14,14 +14,17 @@
 // Roles (one persistent CTA per SM, work units strided over the grid):
 //   warps 0-3   epilogue: tensor memory -> alpha/beta -> C (or split-K
 //               partials); warp w owns tensor-memory lanes 32w..32w+31
-//   warps 4-19  producers: B^T (MMA A operand) global loads (any alignment,
-//               zero-filled edges, several stages in flight in registers)
-//               -> hi/lo split -> a tensor-memory ring (tcgen05.st); the A
-//               tile (MMA B operand) -> hi/lo in K-major 64-byte-swizzled
-//               shared memory, either from their own global loads or, when A
-//               rows are 16-byte aligned, split in place after a TMA copy
-//   warp 20     tensor-memory allocation and the single MMA-issuing thread
-//   warp 21     the TMA thread: copies raw A tiles into the stage ring
+//   warps 4..    producers (12 warps in 3 groups when A comes by TMA, else
+//               16): the B slab (MMA A operand B^T) -> hi/lo split -> a
+//               tensor-memory ring (tcgen05.st), read either from the raw
+//               slab a TMA copy left in shared memory (B rows 16-byte
+//               aligned) or from their own global loads (any alignment,
+//               zero-filled edges, several stages in flight); the A tile
+//               (MMA B operand) -> hi/lo in K-major 64-byte-swizzled shared
+//               memory, split in place after a TMA copy (A rows 16-byte
+//               aligned) or from their own loads
+//   next warp   tensor-memory allocation and the single MMA-issuing thread
+//   last warp   the TMA thread: copies raw A tiles and B slabs into the ring
 // Keeping the 128-row operand in tensor memory halves the shared-memory
 // traffic per MMA (the tensor core reads only the A tile from shared memory).
 // Pipelines: a STAGES-deep ring (full/empty mbarriers; the tensor core frees
@@ -33,9 +36,8 @@
 // prefetch ideas of "NVIDIA_SGEMM_PRACTICE" (sections "kernel 2", "kernel 6",
 // "kernel 7") and the zero-filled edge tiles of "matmul_opt.cu"
 // (matrixMulOptimized), re-done for the tensor core: every element has to
-// pass a producer thread for the split, so B^T goes global -> registers ->
-// tensor memory, and A either the same way or TMA -> shared memory ->
-// split in place.
+// pass a producer thread for the split, so B^T goes (TMA ->) registers ->
+// tensor memory, and A (TMA ->) shared memory -> split in place.
 #pragma once
 #include <cuda.h>  // CUtensorMap (type only; the library does not link the driver)
 
