@@ -18,7 +18,7 @@ from . import _build_ext
 
 __all__ = [
     "SGEMM_ALGO_AUTO", "SGEMM_ALGO_FFMA", "SGEMM_ALGO_TF32X3",
-    "SGEMM_FLAG_DEBUG_WITHHOLD_ARRIVE", "SGEMM_FLAG_TILE_ROWS", "SGEMM_FLAG_WHOLE_TILES",
+    "SGEMM_FLAG_DEBUG_WITHHOLD_ARRIVE", "SGEMM_FLAG_TILE_ROWS", "SGEMM_FLAG_WHOLE_TILES", "SGEMM_FLAG_SPLIT_TAIL",
     "SGEMM_ERR_DEVICE_TIMEOUT",
     "SgemmError", "library", "lib_path", "declared_functions",
     "sgemm", "sgemm_ex", "sgemm_host", "sgemm_plan_info", "sgemm_check_status",
@@ -31,6 +31,7 @@ SGEMM_ALGO_FFMA = 1
 SGEMM_ALGO_TF32X3 = 2
 SGEMM_FLAG_DEBUG_WITHHOLD_ARRIVE = 1
 SGEMM_FLAG_WHOLE_TILES = 2
+SGEMM_FLAG_SPLIT_TAIL = 4
 
 
 def SGEMM_FLAG_TILE_ROWS(r: int) -> int:

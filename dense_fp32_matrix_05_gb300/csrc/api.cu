@@ -107,39 +107,123 @@ int choose_splits(int tiles, int k_tiles, int slots, int splits_req, int min_kt)
     return std::max(s, 1);
 }
 
-// C rows per tile of the 3xTF32 kernel (MMA N).
-int choose_tm(int M, int N, int K, int sms, int forced) {
-    if (forced > 0) return forced;
-    int tm;
-    if (M <= 16) tm = 16;
-    else if (M <= 32) tm = 32;
-    else if (M <= 64) tm = 64;
-    else if (M <= 128) tm = 128;
-    else if (M <= 192) tm = 192;
-    else if (M <= 256) tm = 256;
-    else {
-        const long long p256 = static_cast<long long>(ceil_div(M, 256)) * 256;
-        const long long p192 = static_cast<long long>(ceil_div(M, 192)) * 192;
-        tm = (p192 < p256) ? 192 : 256;
-    }
-    // small problems: trade tile efficiency for parallelism when even the
-    // largest useful split count leaves most SMs idle
-    const int n_tiles = ceil_div(N, sg::kTf32x3TileN);
-    const int k_tiles = ceil_div(std::max(K, 1), sg::kTf32x3BK);
-    while (tm > 64) {
-        const long long units = static_cast<long long>(ceil_div(M, tm)) * n_tiles *
-                                std::max(1, std::min(16, k_tiles / 4));
-        if (units >= sms) break;
-        tm = (tm == 192) ? 128 : tm / 2;
-    }
-    return tm;
+int forced_tile_rows(int flags) { return ((flags >> 8) & 0xFF) * 16; }
+
+// Run-time model of the 3xTF32 kernel (microseconds), fitted to GB300
+// measurements of square, ragged, K-heavy and wide shapes over every tile
+// height and split count: a launch cost, per unit a fixed cost plus a cost
+// per 16-deep K tile (both growing with the tile height), and for a shared
+// tile a sum whose cost grows with its partial tiles.  Waves count the
+// units of the busiest CTA, and CTA waves when there are more CTAs than SMs.
+struct TileCost {
+    double per_k_tile, per_unit;
+};
+
+TileCost tile_cost(int tm) {
+    if (tm <= 64) return {0.364, 1.27};
+    if (tm <= 128) return {0.384, 3.23};
+    if (tm <= 192) return {0.412, 5.18};
+    return {0.459, 9.27};
 }
 
-int forced_tile_rows(int flags) { return ((flags >> 8) & 0xFF) * 16; }
+constexpr double kLaunchUs = 8.2;
+constexpr double kSumUsPer256Rows = 0.99;  // per partial tile (and C) of a shared tile
+
+struct Tf32x3Choice {
+    int tm = 0, splits = 1, tail_splits = 0;
+    double us = 0;
+};
+
+// Split-K (or whole tiles when s == 1) with tile height tm.
+double model_split_k(int M, int N, int K, int tm, int s, int sms) {
+    const TileCost c = tile_cost(tm);
+    const long long tiles = static_cast<long long>(ceil_div(M, tm)) * ceil_div(N, sg::kTf32x3TileN);
+    const int kt = ceil_div(std::max(K, 1), sg::kTf32x3BK);
+    s = std::max(1, std::min(s, kt));
+    const long long units = tiles * s;
+    long long grid = std::min<long long>(units, sms);
+    if (s > 1) grid = std::max(grid, (units + sg::kTf32x3MaxDefer - 1) / sg::kTf32x3MaxDefer);
+    const long long waves = ((units + grid - 1) / grid) * ((grid + sms - 1) / sms);
+    double us = kLaunchUs + waves * (ceil_div(kt, s) * c.per_k_tile + c.per_unit);
+    if (s > 1) us += kSumUsPer256Rows * waves * (s + 1) * tm / 256.0;
+    return us;
+}
+
+// Whole waves of whole tiles, then the leftover tiles in ts K slices each.
+double model_split_tail(int M, int N, int K, int tm, int ts, int sms) {
+    const TileCost c = tile_cost(tm);
+    const long long tiles = static_cast<long long>(ceil_div(M, tm)) * ceil_div(N, sg::kTf32x3TileN);
+    const int kt = ceil_div(std::max(K, 1), sg::kTf32x3BK);
+    const long long waves = tiles / sms;
+    return kLaunchUs + waves * (kt * c.per_k_tile + c.per_unit) + ceil_div(kt, ts) * c.per_k_tile + c.per_unit +
+           kSumUsPer256Rows * (ts + 1) * tm / 256.0;
+}
+
+// K slices per leftover tile of a split tail (0: no split tail possible).
+int tail_splits_for(long long tiles, int kt, int sms) {
+    const long long rem = tiles % sms;
+    if (tiles < sms || rem == 0) return 0;
+    const int ts = static_cast<int>(std::min<long long>(sms / rem, kt / 8));
+    return ts >= 2 ? ts : 0;
+}
+
+// Tile heights the planner may use for M rows: the smallest supported height
+// that covers M (at most 256) and, for M > 64, the lower ones from 64 up.
+int tm_candidates(int M, int out[6]) {
+    static const int kAll[] = {16, 32, 64, 128, 192, 256};
+    int cover = 256;
+    for (int tm : kAll)
+        if (tm >= M) { cover = tm; break; }
+    int n = 0;
+    if (cover <= 64) {
+        out[n++] = cover;
+    } else {
+        for (int tm : kAll)
+            if (tm >= 64 && tm <= cover) out[n++] = tm;
+    }
+    return n;
+}
+
+Tf32x3Choice choose_tf32x3(int M, int N, int K, int sms, int forced_tm, int splits_req, int flags) {
+    int tms[6];
+    int ntm = forced_tm > 0 ? (tms[0] = forced_tm, 1) : tm_candidates(M, tms);
+    const int kt = ceil_div(std::max(K, 1), sg::kTf32x3BK);
+    Tf32x3Choice best, best_tail;
+    best.us = best_tail.us = 1e300;
+    for (int i = 0; i < ntm; ++i) {
+        const int tm = tms[i];
+        const long long tiles = static_cast<long long>(ceil_div(M, tm)) * ceil_div(N, sg::kTf32x3TileN);
+        if (splits_req > 0) {
+            const int s = std::max(1, std::min(splits_req, kt));
+            const double us = model_split_k(M, N, K, tm, s, sms);
+            if (us < best.us) best = {tm, s, 0, us};
+            continue;
+        }
+        // split-K: at least 4 K tiles per slice, at most 16 slices, and
+        // only while the slices still fit in one wave
+        for (int s = 1; s <= 16; ++s) {
+            if (s > 1 && (kt / s < 4 || tiles * s > sms)) break;
+            const double us = model_split_k(M, N, K, tm, s, sms);
+            if (us < best.us) best = {tm, s, 0, us};
+        }
+        if (!(flags & SGEMM_FLAG_WHOLE_TILES)) {
+            const int ts = tail_splits_for(tiles, kt, sms);
+            if (ts > 0) {
+                const double us = model_split_tail(M, N, K, tm, ts, sms);
+                if (us < best.us) best = {tm, 1, ts, us};
+                if (us < best_tail.us) best_tail = {tm, 1, ts, us};
+            }
+        }
+    }
+    // SPLIT_TAIL: the fastest plan that has a split tail, if any has one
+    if ((flags & SGEMM_FLAG_SPLIT_TAIL) && !(flags & SGEMM_FLAG_WHOLE_TILES) && best_tail.tm > 0) return best_tail;
+    return best;
+}
 
 void plan_tf32x3(int M, int N, int K, int sms, int splits_req, int flags, Plan &p) {
     p.path = SGEMM_ALGO_TF32X3;
-    const int tm = choose_tm(M, N, K, sms, forced_tile_rows(flags));
+    const Tf32x3Choice ch = choose_tf32x3(M, N, K, sms, forced_tile_rows(flags), splits_req, flags);
+    const int tm = ch.tm;
     p.tile_m = tm;
     p.tile_n = sg::kTf32x3TileN;
     Schedule &s = p.sch;
@@ -147,31 +231,24 @@ void plan_tf32x3(int M, int N, int K, int sms, int splits_req, int flags, Plan &
     s.n_tiles = ceil_div(N, p.tile_n);
     s.k_tiles = ceil_div(K, sg::kTf32x3BK);
     const int tiles = s.m_tiles * s.n_tiles;
-    s.splits = choose_splits(tiles, s.k_tiles, sms, splits_req, 4);
+    s.splits = ch.splits;
     s.units = tiles * s.splits;
     s.group_m = std::min(8, s.m_tiles);
     p.grid = std::min(s.units, sms);
+    // a CTA finishes at most kTf32x3MaxDefer shared tiles: with more units
+    // than that per SM (forced split counts), run more CTAs than SMs
+    if (s.splits > 1) p.grid = std::max(p.grid, ceil_div(s.units, sg::kTf32x3MaxDefer));
     p.stages = sg::tf32x3_stages(tm);
     p.ws_bytes = s.splits > 1 ? static_cast<size_t>(s.units) * p.tile_n * tm * sizeof(float) : 0;
-    // Split tail: when whole tiles leave the last wave partly empty, the
-    // whole waves stay as they are and the leftover tiles are cut into K
-    // slices so that the last wave keeps (almost) every SM busy.
-    if (splits_req == 0 && s.splits == 1 && !(flags & SGEMM_FLAG_WHOLE_TILES)) {
-        const int grid = sms;
-        const int waves = tiles / grid, rem = tiles % grid;
-        // with few waves the tail's partial-tile traffic and last-arriver sums
-        // cost more than the idle SMs it saves (measured: a loss at 5 waves,
-        // a gain at 13)
-        if (waves >= 8 && rem != 0) {
-            const int ts = std::min(grid / rem, s.k_tiles / 8);
-            if (ts >= 2) {
-                s.dp_tiles = waves * grid;
-                s.tail_tiles = rem;
-                s.tail_splits = ts;
-                p.grid = grid;
-                p.ws_bytes = static_cast<size_t>(rem) * ts * p.tile_n * tm * sizeof(float);
-            }
-        }
+    if (ch.tail_splits > 0) {
+        // whole waves keep whole tiles; the leftover tiles are cut into K
+        // slices so that the last wave keeps (almost) every SM busy
+        const int rem = tiles % sms;
+        s.dp_tiles = tiles - rem;
+        s.tail_tiles = rem;
+        s.tail_splits = ch.tail_splits;
+        p.grid = sms;
+        p.ws_bytes = static_cast<size_t>(rem) * ch.tail_splits * p.tile_n * tm * sizeof(float);
     }
 }
 
@@ -220,7 +297,8 @@ size_t span_bytes(int rows, int cols, long long ld) {
 }
 
 bool flags_valid(int flags) {
-    if (flags & ~(SGEMM_FLAG_DEBUG_WITHHOLD_ARRIVE | SGEMM_FLAG_WHOLE_TILES | 0xFF00)) return false;
+    if (flags & ~(SGEMM_FLAG_DEBUG_WITHHOLD_ARRIVE | SGEMM_FLAG_WHOLE_TILES | SGEMM_FLAG_SPLIT_TAIL | 0xFF00))
+        return false;
     const int tm = forced_tile_rows(flags);
     return tm == 0 || sg::tf32x3_supported_tm(tm);
 }

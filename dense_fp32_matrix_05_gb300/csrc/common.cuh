@@ -15,6 +15,7 @@ enum : int {
     kStatusTimeoutEpilogue = 4,
     kStatusTimeoutDrain = 8,
     kStatusNoWorkspace = 16,  // a shared tile met a missing workspace (a planner bug)
+    kStatusDeferOverflow = 32,  // a CTA got more shared tiles than it can defer (a planner bug)
 };
 
 // Test-only flag: withhold the first producer arrive (see the header).

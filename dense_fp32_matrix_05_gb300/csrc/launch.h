@@ -9,6 +9,7 @@ namespace sg {
 // Tile constants the planner needs (checked against the kernels' own).
 constexpr int kTf32x3TileN = 128;  // C columns per 3xTF32 tile
 constexpr int kTf32x3BK = 16;      // K per 3xTF32 pipeline stage
+constexpr int kTf32x3MaxDefer = 8;  // shared (split-K) tiles one 3xTF32 CTA may finish
 constexpr int kFfmaBK = 16;        // K per FFMA pipeline stage
 
 // 3xTF32 tensor-core path.  tm = C rows per tile: 16, 32, 64, 128, 192, 256.

@@ -13,7 +13,9 @@
 
 namespace sg {
 
-static_assert(kTf32x3TileN == tf32x3::kTileN && kTf32x3BK == tf32x3::kBK, "planner constants");
+static_assert(kTf32x3TileN == tf32x3::kTileN && kTf32x3BK == tf32x3::kBK &&
+                  kTf32x3MaxDefer == tf32x3::kMaxDefer,
+              "planner constants");
 
 namespace {
 

@@ -85,7 +85,10 @@ struct Roles {
 __host__ __device__ constexpr int nacc_for(int tm) { return tm >= 192 ? 1 : 2; }
 __host__ __device__ constexpr int stages_for(int tm) { return tm >= 256 ? 6 : 8; }
 constexpr int kRingColsPerStage = 2 * kBK;
-constexpr int kSmemLimit = 232448;  // dynamic shared memory one CTA may use on sm_103a
+constexpr int kSmemLimit = 232448;
+// Shared tiles whose sum a CTA defers to its exit (see fixup_tile); the
+// planner gives no CTA more split-K units than this.
+constexpr int kMaxDefer = 8;  // dynamic shared memory one CTA may use on sm_103a
 constexpr uint32_t kTmemCols = 512;
 
 // TM = C rows per tile (MMA N).  TMA_B: the stage also holds the raw B tile
@@ -109,8 +112,10 @@ struct Cfg {
     static constexpr int kChunk = 16;  // accumulator columns per tensor-memory load in the epilogue
     static constexpr uint32_t kIdesc = umma_idesc_tf32(kTileN, TM);
     // barriers: full[S], empty[S], a_full[S], acc_full[2], acc_empty[2],
-    // drain; then tensor-memory address, abort flag, split-K "last" flag
-    static constexpr int kBarBytes = 8 * (3 * kStages + 5) + 16;
+    // drain; then words: tensor-memory address, abort flag, (unused), count
+    // of deferred sums, and kMaxDefer entries (tile row, tile column,
+    // segment count, first workspace slot)
+    static constexpr int kBarBytes = 8 * (3 * kStages + 5) + 4 * (4 + 4 * kMaxDefer);
     static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes;
     static_assert(kSmemBytes <= kSmemLimit, "shared memory per CTA");
     static_assert(kStages >= 4, "pipeline depth");
@@ -331,6 +336,123 @@ __device__ __forceinline__ void tmem_load_chunk(uint32_t taddr, float (&v)[Cfg<T
     }
 }
 
+// Last-arriver sum of a shared tile, by a team of nw warps (wid = this
+// warp's index in the team).  The nseg partial tiles (TM x 128, row-major,
+// contiguous from wb) and the C tile are read row by row with 16-byte loads:
+// a warp covers one 128-column row per load and each thread keeps kFixRows
+// rows x (up to kFixSegs segments + C) loads in flight.  The partials are
+// added in segment order, starting from zero, whatever order the units
+// arrived in, so the bits of C do not depend on timing.
+constexpr int kFixRows = 1;
+constexpr int kFixSegs = 3;
+
+__device__ __forceinline__ float4 ld4cg(const float *p) {
+    return __ldcg(reinterpret_cast<const float4 *>(p));
+}
+
+__device__ __forceinline__ float fix_lane(const float4 &v, int q) {
+    return q == 0 ? v.x : q == 1 ? v.y : q == 2 ? v.z : v.w;
+}
+
+template <int TM>
+__device__ __forceinline__ void fixup_tile(const GemmArgs &g, const float *wb, int nseg, int m0, int n0,
+                                        int wid, int nw, int lane) {
+    constexpr long long kTileElems = static_cast<long long>(kTileN) * TM;
+    const int pass = kFixRows * nw;  // rows per pass
+    const int nc = n0 + 4 * lane;    // first of this thread's 4 columns
+    if (nc >= g.N) return;
+    const bool vec_c = (reinterpret_cast<uintptr_t>(g.C) & 15u) == 0 && (g.ldc & 3) == 0;
+    const bool full4 = vec_c && nc + 3 < g.N;
+    const bool read_c = g.beta != 0.f;
+    const int rows = min(TM, g.M - m0);
+#pragma unroll 1
+    for (int r0 = wid; r0 < rows; r0 += pass) {
+        // rows r0 + nw * j of the tile
+        float4 old[kFixRows];
+#pragma unroll
+        for (int j = 0; j < kFixRows; ++j) {
+            const int r = r0 + nw * j;
+            old[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (read_c && r < rows) {
+                const float *cp = g.C + static_cast<long long>(m0 + r) * g.ldc + nc;
+                if (full4) {
+                    old[j] = *reinterpret_cast<const float4 *>(cp);
+                } else {
+                    old[j].x = cp[0];
+                    if (nc + 1 < g.N) old[j].y = cp[1];
+                    if (nc + 2 < g.N) old[j].z = cp[2];
+                    if (nc + 3 < g.N) old[j].w = cp[3];
+                }
+            }
+        }
+        float4 sum[kFixRows];
+#pragma unroll
+        for (int j = 0; j < kFixRows; ++j) sum[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 1
+        for (int s0 = 0; s0 < nseg; s0 += kFixSegs) {
+            float4 v[kFixSegs][kFixRows];
+#pragma unroll
+            for (int q = 0; q < kFixSegs; ++q)
+#pragma unroll
+                for (int j = 0; j < kFixRows; ++j)
+                    if (s0 + q < nseg && r0 + nw * j < rows)
+                        v[q][j] = ld4cg(wb + (s0 + q) * kTileElems +
+                                        static_cast<long long>(r0 + nw * j) * kTileN + 4 * lane);
+#pragma unroll
+            for (int q = 0; q < kFixSegs; ++q)
+                if (s0 + q < nseg)
+#pragma unroll
+                    for (int j = 0; j < kFixRows; ++j) {
+                        sum[j].x += v[q][j].x;
+                        sum[j].y += v[q][j].y;
+                        sum[j].z += v[q][j].z;
+                        sum[j].w += v[q][j].w;
+                    }
+        }
+#pragma unroll
+        for (int j = 0; j < kFixRows; ++j) {
+            const int r = r0 + nw * j;
+            if (r >= rows) continue;
+            const int m = m0 + r;
+            float res[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                float s = fix_lane(sum[j], q);
+                if (s != s && nc + q < g.N) s = recompute_dot(g, m, nc + q);
+                const float a = g.alpha * s;
+                res[q] = read_c ? fmaf(g.beta, fix_lane(old[j], q), a) : a;
+            }
+            float *cp = g.C + static_cast<long long>(m) * g.ldc + nc;
+            if (full4) {
+                *reinterpret_cast<float4 *>(cp) = make_float4(res[0], res[1], res[2], res[3]);
+            } else {
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    if (nc + q < g.N) cp[q] = res[q];
+            }
+        }
+    }
+}
+
+// Ask L2 for the C tile (rows m0.., columns n0..) that an epilogue will read
+// once the accumulator is ready; thread t of the epilogue takes rows t,
+// t + 128, ...  Only whole 16-byte pieces inside C are requested.
+template <int TM>
+__device__ __forceinline__ void prefetch_c_tile(const GemmArgs &g, int m0, int n0, int t) {
+    const int cols = min(kTileN, g.N - n0);
+    const bool vec = (reinterpret_cast<uintptr_t>(g.C) & 15u) == 0 && (g.ldc & 3) == 0;
+#pragma unroll 1
+    for (int r = t; r < TM && m0 + r < g.M; r += kEpiWarps * 32) {
+        const float *row = g.C + static_cast<long long>(m0 + r) * g.ldc + n0;
+        if (vec) {
+            const uint32_t bytes = static_cast<uint32_t>(cols * 4) & ~15u;
+            if (bytes) prefetch_l2_bulk(row, bytes);
+        } else {
+            for (int q = 0; q < cols; q += 32) prefetch_l2(row + q);
+        }
+    }
+}
+
 // TMA_A: A rows are 16-byte aligned and tmap_a describes A (K x M, 64-byte
 // swizzle, box 16 x TM); otherwise the producers load A themselves.
 // TMA_B: B rows are 16-byte aligned and tmap_b describes B (N x K, box
@@ -357,7 +479,8 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
     const uint32_t drain_bar = acc_empty0 + 16u;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(base_ptr + S * C::kStageBytes + 8 * (3 * S + 5));
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-    volatile int *s_last = reinterpret_cast<volatile int *>(tmem_slot + 2);
+    volatile int *s_ndefer = reinterpret_cast<volatile int *>(tmem_slot + 3);
+    volatile int *s_defer = reinterpret_cast<volatile int *>(tmem_slot + 4);  // [kMaxDefer][mt, nt, nseg, slot0]
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -374,7 +497,7 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
         mbar_init(acc_empty0 + 8u, kEpiWarps * 32);
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
-        *s_last = 0;
+        *s_ndefer = 0;
         fence_mbar_init();
     }
     if (warp == R::kMmaWarp) {
@@ -395,6 +518,7 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
             const UnitCoord &c = ui.c;
             const int acc = it % C::kNacc;
             const uint32_t aph = (it / C::kNacc) & 1;
+            if (c.nseg == 1 && g.beta != 0.f) prefetch_c_tile<TM>(g, c.mt * TM, c.nt * kTileN, threadIdx.x);
             const bool w = mbar_wait_bounded(acc_full0 + 8u * acc, aph, abort_flag, ctl,
                                              kStatusTimeoutEpilogue);
             if (!epi_all(w)) break;
@@ -404,28 +528,49 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
             const uint32_t t0 = tmem_base + (static_cast<uint32_t>(warp * 32) << 16) +
                                 static_cast<uint32_t>(acc * TM);
             if (c.nseg == 1) {
+                // Chunks of CH accumulator columns (C rows): each chunk's C
+                // loads are issued before its tensor-memory load and are in
+                // flight together with it (C was requested into L2 while
+                // the accumulator was being computed).
+                static_assert(CH == 16, "the epilogue loads 16 columns at a time");
+                const bool read_c = g.beta != 0.f;
+                const bool n_ok = n < g.N;
+                float *cbase = g.C + static_cast<long long>(m0) * g.ldc + n;
 #pragma unroll 1
                 for (int ch = 0; ch < TM / CH; ++ch) {
-                    float v[CH];
-                    tmem_load_chunk<TM>(t0 + ch * CH, v);
                     const int mb = m0 + ch * CH;
-                    if (n < g.N) {
+                    float *cp = cbase + static_cast<long long>(ch * CH) * g.ldc;
+                    float old[CH];
+                    if (read_c) {
 #pragma unroll
                         for (int j = 0; j < CH; ++j)
+                            old[j] = (n_ok && mb + j < g.M) ? cp[j * g.ldc] : 0.f;
+                    }
+                    uint32_t r[CH];
+                    tmem_ld32x16_issue(t0 + ch * CH, r);
+                    tmem_ld_wait16(r);
+                    float v[CH];
+                    bool nan = false;
+#pragma unroll
+                    for (int j = 0; j < CH; ++j) {
+                        v[j] = __uint_as_float(r[j]);
+                        nan |= v[j] != v[j];
+                    }
+                    if (nan && n_ok) {
+                        // a non-finite input reached this chunk: exact dot products
+#pragma unroll 1
+                        for (int j = 0; j < CH; ++j)
                             if (v[j] != v[j] && mb + j < g.M) v[j] = recompute_dot(g, mb + j, n);
-                        float *cp = g.C + static_cast<long long>(mb) * g.ldc + n;
-                        if (g.beta == 0.f) {
-#pragma unroll
-                            for (int j = 0; j < CH; ++j)
-                                if (mb + j < g.M) cp[j * g.ldc] = g.alpha * v[j];
-                        } else {
-                            float old[CH];
-#pragma unroll
-                            for (int j = 0; j < CH; ++j)
-                                old[j] = (mb + j < g.M) ? cp[j * g.ldc] : 0.f;
+                    }
+                    if (n_ok) {
+                        if (read_c) {
 #pragma unroll
                             for (int j = 0; j < CH; ++j)
                                 if (mb + j < g.M) cp[j * g.ldc] = fmaf(g.beta, old[j], g.alpha * v[j]);
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < CH; ++j)
+                                if (mb + j < g.M) cp[j * g.ldc] = g.alpha * v[j];
                         }
                     }
                 }
@@ -453,51 +598,22 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
                 __threadfence();
                 named_bar_sync(kEpiBarrierId, kEpiWarps * 32);
                 if (threadIdx.x == 0) {
+                    // the last unit to arrive queues the tile's sum for the
+                    // CTA's exit, where every warp of the CTA is free for it
                     const int prev = atomicAdd(ctl.counters + c.tile, 1);
-                    *s_last = (prev == c.nseg - 1) ? 1 : 0;
-                }
-                named_bar_sync(kEpiBarrierId, kEpiWarps * 32);
-                if (*s_last) {
-                    __threadfence();
-                    const float *wb = ctl.ws + c.slot0 * kTileElems;
-                    if (n < g.N) {
-#pragma unroll 1
-                        for (int mb = 0; mb < TM; mb += 8) {
-                            float sum[8];
-#pragma unroll
-                            for (int j = 0; j < 8; ++j) sum[j] = 0.f;
-                            // two segments' loads in flight at once, then added
-                            // in segment order (the order fixes the bits)
-#pragma unroll 1
-                            for (int sp0 = 0; sp0 < c.nseg; sp0 += 2) {
-                                float v[2][8];
-#pragma unroll
-                                for (int q = 0; q < 2; ++q) {
-                                    const float *p = wb + static_cast<long long>(sp0 + q) * kTileElems +
-                                                     mb * kTileN + nl;
-#pragma unroll
-                                    for (int j = 0; j < 8; ++j)
-                                        v[q][j] = (sp0 + q < c.nseg) ? __ldcg(p + j * kTileN) : 0.f;
-                                }
-#pragma unroll
-                                for (int q = 0; q < 2; ++q)
-                                    if (sp0 + q < c.nseg)
-#pragma unroll
-                                        for (int j = 0; j < 8; ++j) sum[j] += v[q][j];
-                            }
-#pragma unroll
-                            for (int j = 0; j < 8; ++j) {
-                                const int m = m0 + mb + j;
-                                if (m < g.M) {
-                                    if (sum[j] != sum[j]) sum[j] = recompute_dot(g, m, n);
-                                    float *cp = g.C + static_cast<long long>(m) * g.ldc + n;
-                                    const float r = g.alpha * sum[j];
-                                    *cp = (g.beta == 0.f) ? r : fmaf(g.beta, *cp, r);
-                                }
-                            }
+                    if (prev == c.nseg - 1) {
+                        ctl.counters[c.tile] = 0;
+                        const int nd = *s_ndefer;
+                        if (nd < kMaxDefer) {
+                            s_defer[4 * nd + 0] = c.mt;
+                            s_defer[4 * nd + 1] = c.nt;
+                            s_defer[4 * nd + 2] = c.nseg;
+                            s_defer[4 * nd + 3] = static_cast<int>(c.slot0);
+                            *s_ndefer = nd + 1;
+                        } else {
+                            atomicOr(ctl.status, kStatusDeferOverflow);
                         }
                     }
-                    if (threadIdx.x == 0) ctl.counters[c.tile] = 0;
                 }
             }
         }
@@ -665,6 +781,16 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
     if (warp == R::kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem_base, kTmemCols);
+    }
+    // deferred sums of shared tiles, by every warp of the CTA
+    const int nd = *s_ndefer;
+    if (nd > 0 && !*abort_flag) {
+        __threadfence();
+#pragma unroll 1
+        for (int e = 0; e < nd; ++e)
+            fixup_tile<TM>(g, ctl.ws + static_cast<long long>(s_defer[4 * e + 3]) * (kTileN * TM),
+                           s_defer[4 * e + 2], s_defer[4 * e] * TM, s_defer[4 * e + 1] * kTileN, warp,
+                           R::kThreads / 32, lane);
     }
 }
 

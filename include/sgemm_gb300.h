@@ -69,6 +69,11 @@ typedef struct CUstream_st *sgemm_stream_t;
 /* SGEMM_FLAG_WHOLE_TILES: 3xTF32 path only, keep whole tiles in the last
  * wave instead of splitting the leftover tiles along K over idle SMs. */
 #define SGEMM_FLAG_WHOLE_TILES 2
+/* SGEMM_FLAG_SPLIT_TAIL: 3xTF32 path only, split the leftover tiles of a
+ * partly empty last wave along K whenever there are any, even where the
+ * planner's run-time estimate prefers whole tiles (for tuning and tests).
+ * Ignored with an explicit split count; WHOLE_TILES wins over it. */
+#define SGEMM_FLAG_SPLIT_TAIL 4
 #define SGEMM_FLAG_DEBUG_WITHHOLD_ARRIVE 1 /* test only: one pipeline arrive
                                               is withheld and the on-device
                                               wait budget is cut to ~1 ms, so
@@ -101,17 +106,18 @@ int sgemm(int M, int N, int K, float alpha,
  *                to finish adds the partials in slice order, so the result
  *                does not depend on timing.
  *   flags  (15): 0, or any of SGEMM_FLAG_TILE_ROWS(r),
- *                SGEMM_FLAG_WHOLE_TILES and SGEMM_FLAG_DEBUG_WITHHOLD_ARRIVE
- *                (tests only).  Any other bit, or a tile height that is not
+ *                SGEMM_FLAG_WHOLE_TILES, SGEMM_FLAG_SPLIT_TAIL and
+ *                SGEMM_FLAG_DEBUG_WITHHOLD_ARRIVE (tests only).  Any other bit, or a tile height that is not
  *                supported, is rejected.
  *
- * Scheduling (3xTF32 path): persistent CTAs, one per SM.  When the output
- * tiles are fewer than the SMs, K is split (splits).  When they are more but
- * the last wave would be partly empty, whole waves keep whole tiles and the
- * leftover tiles are cut into K slices, one per otherwise idle SM (split
- * tail).  Tiles shared by several units are finished by the last unit to
- * arrive, which adds the partial tiles in a fixed order, so the result does
- * not depend on timing.
+ * Scheduling (3xTF32 path): persistent CTAs, one per SM.  The planner
+ * estimates the run time of each tile height, split count and last-wave
+ * treatment from measured per-tile costs and takes the fastest.  With few
+ * output tiles K is split (splits).  With a partly empty last wave, whole
+ * waves keep whole tiles and the leftover tiles may be cut into K slices,
+ * one per otherwise idle SM (split tail).  Tiles shared by several units are
+ * finished by the last unit to arrive, which adds the partial tiles in a
+ * fixed order, so the result does not depend on timing.
  *
  * The split-K workspace is owned by the library, kept per device and stream,
  * grown on demand (a synchronous cudaMalloc, so make the first call of a
@@ -162,7 +168,8 @@ int sgemm_plan_info(int M, int N, int K, const void *A, int lda,
 /*
  * sgemm_check_status - wait for `stream`, then read and clear the device
  * status word of the current device.  Returns 0, SGEMM_ERR_DEVICE_TIMEOUT if
- * a kernel launched since the last check gave up a bounded wait, or a
+ * a kernel launched since the last check gave up a bounded wait (or met a
+ * work split it cannot finish, which the planner never produces), or a
  * positive cudaError_t.
  */
 int sgemm_check_status(sgemm_stream_t stream);

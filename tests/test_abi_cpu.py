@@ -62,7 +62,7 @@ def test_invalid_extended_arguments(lib):
     assert pkg.sgemm_ex(*base, 3, 0, 0) == -13
     assert pkg.sgemm_ex(*base, -1, 0, 0) == -13
     assert pkg.sgemm_ex(*base, 0, -1, 0) == -14
-    assert pkg.sgemm_ex(*base, 0, 0, 4) == -15
+    assert pkg.sgemm_ex(*base, 0, 0, 8) == -15
     assert pkg.sgemm_ex(*base, 0, 0, pkg.SGEMM_FLAG_TILE_ROWS(48)) == -15
     assert pkg.sgemm_ex(*base, 0, 0, 1 << 20) == -15
 
@@ -131,6 +131,16 @@ def test_plan_forced_splits_are_clamped():
     assert p["splits"] == 4
 
 
+def test_plan_forced_splits_bound_units_per_cta():
+    """A CTA finishes at most 8 shared tiles, so many forced K slices get a
+    grid larger than the SM count."""
+    p = plan(4096, 4096, 4096, splits=16)
+    assert p["units"] == 16 * 32 * 16
+    assert p["grid"] == -(-p["units"] // 8) and p["grid"] > SMS
+    q = plan(1024, 1024, 1024, splits=2)
+    assert q["grid"] == min(q["units"], SMS)
+
+
 def test_plan_ffma_tiles():
     assert (plan(32, 4096, 64, algo=1)["tile_m"], plan(32, 4096, 64, algo=1)["tile_n"]) == (32, 512)
     assert plan(64, 4096, 64, algo=1)["tile_n"] == 256
@@ -145,10 +155,19 @@ def test_plan_split_tail():
     assert p["ws_bytes"] == 72 * (SMS // 72) * 256 * 128 * 4
     q = plan(8192, 8192, 8192, flags=pkg.SGEMM_FLAG_WHOLE_TILES)
     assert q["tail_tiles"] == 0 and q["ws_bytes"] == 0
-    assert plan(5120, 5120, 5120)["tail_tiles"] == 0    # 5 waves + 40: whole tiles measured faster
+    p5 = plan(5120, 5120, 5120)                          # 800 tiles = 5 waves + 40
+    assert p5["tail_tiles"] == 40 and p5["tile_m"] == 256
+    assert p5["ws_bytes"] == 40 * (SMS // 40) * 256 * 128 * 4
     assert plan(4864, 4096, 4096)["tail_tiles"] == 0    # 19 x 32 = 608 tiles: 4 whole waves
     assert plan(1024, 1024, 1024)["tail_tiles"] == 0    # fewer tiles than SMs: split-K instead
     assert plan(8192, 8192, 8192, splits=1)["tail_tiles"] == 0  # explicit split count wins
+    # a forced split tail where the estimate prefers whole tiles
+    r = plan(4096, 24576, 256)
+    assert r["tail_tiles"] == 0
+    f = plan(4096, 24576, 256, flags=pkg.SGEMM_FLAG_SPLIT_TAIL)
+    assert f["tail_tiles"] > 0 and f["grid"] == SMS
+    assert f["tail_tiles"] == (-(-4096 // f["tile_m"]) * 192) % SMS
+    assert plan(3072, 3072, 3072, flags=pkg.SGEMM_FLAG_SPLIT_TAIL)["tail_tiles"] == 0  # none possible
 
 
 @pytest.mark.parametrize("rows", [16, 32, 64, 128, 192, 256])

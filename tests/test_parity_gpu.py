@@ -105,17 +105,36 @@ def test_split_tail(shape):
     checked on sampled rows against the oracle and the whole-tile schedule."""
     M, N, K = shape
     p = _with_c(random_problem(M, N, K, alpha=1.0, beta=-0.75, seed=M ^ N ^ K, pad_value=0.0))
-    info = pkg.sgemm_plan_info(M, N, K, algo=pkg.SGEMM_ALGO_TF32X3, num_sms=0)
+    tail = pkg.SGEMM_FLAG_SPLIT_TAIL
+    info = pkg.sgemm_plan_info(M, N, K, algo=pkg.SGEMM_ALGO_TF32X3, flags=tail, num_sms=0)
     assert info["tail_tiles"] > 0
     rows = sample_rows(M, 40, seed=7)
-    C_sk, st = run_sgemm(p, pkg.SGEMM_ALGO_TF32X3)
+    C_sk, st = run_sgemm(p, pkg.SGEMM_ALGO_TF32X3, flags=tail)
     assert st == 0
     check_against_oracle(p, C_sk, rows=rows, what=f"{shape} split tail")
     C_dp, st = run_sgemm(p, pkg.SGEMM_ALGO_TF32X3, flags=pkg.SGEMM_FLAG_WHOLE_TILES)
     assert st == 0
     check_against_oracle(p, C_dp, rows=rows, what=f"{shape} whole tiles")
-    C_sk2, _ = run_sgemm(p, pkg.SGEMM_ALGO_TF32X3)
+    C_sk2, _ = run_sgemm(p, pkg.SGEMM_ALGO_TF32X3, flags=tail)
     assert np.array_equal(C_sk.view(np.uint32), C_sk2.view(np.uint32)), "split tail is not deterministic"
+
+
+@pytest.mark.parametrize("K", [2048, 2047])
+def test_many_split_units_per_sm(K):
+    """Forced split counts that give more shared tiles than one CTA may
+    finish: the planner then runs more CTAs than SMs, and every tile's
+    partial sums still meet in one deferred sum."""
+    import torch
+
+    M, N = 1000, 2000
+    p = _with_c(random_problem(M, N, K, alpha=0.5, beta=2.0, seed=K, pad_value=0.0))
+    flags = pkg.SGEMM_FLAG_TILE_ROWS(64)
+    info = pkg.sgemm_plan_info(M, N, K, algo=pkg.SGEMM_ALGO_TF32X3, splits=8, flags=flags, num_sms=0)
+    assert info["splits"] == 8 and info["units"] == 16 * 16 * 8
+    assert info["grid"] * 8 >= info["units"] and info["grid"] > torch.cuda.get_device_properties(0).multi_processor_count
+    C, st = run_sgemm(p, pkg.SGEMM_ALGO_TF32X3, splits=8, flags=flags)
+    assert st == 0
+    check_against_oracle(p, C, rows=sample_rows(M, 40, seed=K), what=f"K={K} splits=8 rows=64")
 
 
 @pytest.mark.parametrize("algo", ALGOS, ids=ALGO_IDS)
