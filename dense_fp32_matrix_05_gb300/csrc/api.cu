@@ -116,18 +116,18 @@ int forced_tile_rows(int flags) { return ((flags >> 8) & 0xFF) * 16; }
 // tile a sum whose cost grows with its partial tiles.  Waves count the
 // units of the busiest CTA, and CTA waves when there are more CTAs than SMs.
 struct TileCost {
-    double per_k_tile, per_unit;
+    double per_k_tile, per_unit, per_unit_c;  // per_unit_c: added when C is read (beta != 0)
 };
 
 TileCost tile_cost(int tm) {
-    if (tm <= 64) return {0.364, 1.27};
-    if (tm <= 128) return {0.384, 3.23};
-    if (tm <= 192) return {0.412, 5.18};
-    return {0.459, 9.27};
+    if (tm <= 64) return {0.356, 1.84, 0.0};
+    if (tm <= 128) return {0.367, 2.68, 1.57};
+    if (tm <= 192) return {0.394, 6.17, 0.0};
+    return {0.441, 9.28, 1.03};
 }
 
-constexpr double kLaunchUs = 8.2;
-constexpr double kSumUsPer256Rows = 0.99;  // per partial tile (and C) of a shared tile
+constexpr double kLaunchUs = 7.2;
+constexpr double kSumUsPer256Rows = 0.81;  // per partial tile (and C) of a shared tile
 
 struct Tf32x3Choice {
     int tm = 0, splits = 1, tail_splits = 0;
@@ -135,8 +135,9 @@ struct Tf32x3Choice {
 };
 
 // Split-K (or whole tiles when s == 1) with tile height tm.
-double model_split_k(int M, int N, int K, int tm, int s, int sms) {
+double model_split_k(int M, int N, int K, int tm, int s, int sms, bool read_c) {
     const TileCost c = tile_cost(tm);
+    const double unit = c.per_unit + (read_c ? c.per_unit_c : 0.0);
     const long long tiles = static_cast<long long>(ceil_div(M, tm)) * ceil_div(N, sg::kTf32x3TileN);
     const int kt = ceil_div(std::max(K, 1), sg::kTf32x3BK);
     s = std::max(1, std::min(s, kt));
@@ -144,18 +145,19 @@ double model_split_k(int M, int N, int K, int tm, int s, int sms) {
     long long grid = std::min<long long>(units, sms);
     if (s > 1) grid = std::max(grid, (units + sg::kTf32x3MaxDefer - 1) / sg::kTf32x3MaxDefer);
     const long long waves = ((units + grid - 1) / grid) * ((grid + sms - 1) / sms);
-    double us = kLaunchUs + waves * (ceil_div(kt, s) * c.per_k_tile + c.per_unit);
+    double us = kLaunchUs + waves * (ceil_div(kt, s) * c.per_k_tile + unit);
     if (s > 1) us += kSumUsPer256Rows * waves * (s + 1) * tm / 256.0;
     return us;
 }
 
 // Whole waves of whole tiles, then the leftover tiles in ts K slices each.
-double model_split_tail(int M, int N, int K, int tm, int ts, int sms) {
+double model_split_tail(int M, int N, int K, int tm, int ts, int sms, bool read_c) {
     const TileCost c = tile_cost(tm);
+    const double unit = c.per_unit + (read_c ? c.per_unit_c : 0.0);
     const long long tiles = static_cast<long long>(ceil_div(M, tm)) * ceil_div(N, sg::kTf32x3TileN);
     const int kt = ceil_div(std::max(K, 1), sg::kTf32x3BK);
     const long long waves = tiles / sms;
-    return kLaunchUs + waves * (kt * c.per_k_tile + c.per_unit) + ceil_div(kt, ts) * c.per_k_tile + c.per_unit +
+    return kLaunchUs + waves * (kt * c.per_k_tile + unit) + ceil_div(kt, ts) * c.per_k_tile + unit +
            kSumUsPer256Rows * (ts + 1) * tm / 256.0;
 }
 
@@ -184,7 +186,7 @@ int tm_candidates(int M, int out[6]) {
     return n;
 }
 
-Tf32x3Choice choose_tf32x3(int M, int N, int K, int sms, int forced_tm, int splits_req, int flags) {
+Tf32x3Choice choose_tf32x3(int M, int N, int K, int sms, int forced_tm, int splits_req, int flags, bool read_c) {
     int tms[6];
     int ntm = forced_tm > 0 ? (tms[0] = forced_tm, 1) : tm_candidates(M, tms);
     const int kt = ceil_div(std::max(K, 1), sg::kTf32x3BK);
@@ -195,7 +197,7 @@ Tf32x3Choice choose_tf32x3(int M, int N, int K, int sms, int forced_tm, int spli
         const long long tiles = static_cast<long long>(ceil_div(M, tm)) * ceil_div(N, sg::kTf32x3TileN);
         if (splits_req > 0) {
             const int s = std::max(1, std::min(splits_req, kt));
-            const double us = model_split_k(M, N, K, tm, s, sms);
+            const double us = model_split_k(M, N, K, tm, s, sms, read_c);
             if (us < best.us) best = {tm, s, 0, us};
             continue;
         }
@@ -203,13 +205,13 @@ Tf32x3Choice choose_tf32x3(int M, int N, int K, int sms, int forced_tm, int spli
         // only while the slices still fit in one wave
         for (int s = 1; s <= 16; ++s) {
             if (s > 1 && (kt / s < 4 || tiles * s > sms)) break;
-            const double us = model_split_k(M, N, K, tm, s, sms);
+            const double us = model_split_k(M, N, K, tm, s, sms, read_c);
             if (us < best.us) best = {tm, s, 0, us};
         }
         if (!(flags & SGEMM_FLAG_WHOLE_TILES)) {
             const int ts = tail_splits_for(tiles, kt, sms);
             if (ts > 0) {
-                const double us = model_split_tail(M, N, K, tm, ts, sms);
+                const double us = model_split_tail(M, N, K, tm, ts, sms, read_c);
                 if (us < best.us) best = {tm, 1, ts, us};
                 if (us < best_tail.us) best_tail = {tm, 1, ts, us};
             }
@@ -220,9 +222,9 @@ Tf32x3Choice choose_tf32x3(int M, int N, int K, int sms, int forced_tm, int spli
     return best;
 }
 
-void plan_tf32x3(int M, int N, int K, int sms, int splits_req, int flags, Plan &p) {
+void plan_tf32x3(int M, int N, int K, int sms, int splits_req, int flags, bool read_c, Plan &p) {
     p.path = SGEMM_ALGO_TF32X3;
-    const Tf32x3Choice ch = choose_tf32x3(M, N, K, sms, forced_tile_rows(flags), splits_req, flags);
+    const Tf32x3Choice ch = choose_tf32x3(M, N, K, sms, forced_tile_rows(flags), splits_req, flags, read_c);
     const int tm = ch.tm;
     p.tile_m = tm;
     p.tile_n = sg::kTf32x3TileN;
@@ -272,9 +274,9 @@ void plan_ffma(int M, int N, int K, int sms, int splits_req, Plan &p) {
 }
 
 int make_plan(int M, int N, int K, const void *A, int lda, const void *B, int ldb, const void *C, int ldc,
-              int algo, int splits, int flags, int sms, Plan &p) {
+              int algo, int splits, int flags, int sms, bool read_c, Plan &p) {
     const int path = (algo == SGEMM_ALGO_AUTO) ? SGEMM_ALGO_TF32X3 : algo;
-    if (path == SGEMM_ALGO_TF32X3) plan_tf32x3(M, N, K, sms, splits, flags, p);
+    if (path == SGEMM_ALGO_TF32X3) plan_tf32x3(M, N, K, sms, splits, flags, read_c, p);
     else plan_ffma(M, N, K, sms, splits, p);
     p.vec_a = aligned16(A, lda);
     p.vec_b = aligned16(B, ldb);
@@ -382,7 +384,7 @@ int run(int M, int N, int K, float alpha, const float *A, int lda, const float *
             if (beta == 1.f) return 0;
             return from_cuda(sg::scale_c_launch(C, ldc, M, N, beta, d->sms, stream));
         }
-        rc = make_plan(M, N, K, A, lda, B, ldb, C, ldc, algo, splits, flags, d->sms, p);
+        rc = make_plan(M, N, K, A, lda, B, ldb, C, ldc, algo, splits, flags, d->sms, beta != 0.f, p);
         if (rc != 0) return rc;
         ctl.status = d->status;
         ctl.wait_budget = (flags & SGEMM_FLAG_DEBUG_WITHHOLD_ARRIVE) ? kDebugWaitBudget : kWaitBudget;
@@ -503,7 +505,7 @@ int sgemm_plan_info(int M, int N, int K, const void *A, int lda, const void *B, 
     int vals[11] = {0};
     if (M > 0 && N > 0 && K > 0) {
         Plan p;
-        int rc = make_plan(M, N, K, A, lda, B, ldb, C, ldc, algo, splits, flags, sms, p);
+        int rc = make_plan(M, N, K, A, lda, B, ldb, C, ldc, algo, splits, flags, sms, beta != 0.f, p);
         if (rc != 0) return rc;
         vals[0] = p.path;
         vals[1] = p.tile_m;
@@ -624,16 +626,16 @@ int check_tensor_call(int M, int N, int K, float alpha, const float *A, int lda,
     return rc == -15 ? SGEMM_ERR_INTERNAL : rc;  // flags are fixed here
 }
 
-int plan_tensor_call(int M, int N, int K, const float *A, int lda, const float *B, int ldb, const float *C,
-                     int ldc, int splits, int sms, size_t max_ws_floats, TensorPlan *out) {
+int plan_tensor_call(int M, int N, int K, const float *A, int lda, const float *B, int ldb, float beta,
+                     const float *C, int ldc, int splits, int sms, size_t max_ws_floats, TensorPlan *out) {
     Plan p;
-    int rc = make_plan(M, N, K, A, lda, B, ldb, C, ldc, SGEMM_ALGO_TF32X3, splits, 0, sms, p);
+    int rc = make_plan(M, N, K, A, lda, B, ldb, C, ldc, SGEMM_ALGO_TF32X3, splits, 0, sms, beta != 0.f, p);
     if (rc != 0) return rc;
     if (p.sch.tail_tiles > 0 && p.ws_bytes / sizeof(float) > max_ws_floats) {
         // the split tail is an optimisation: drop it rather than exceed the scratch
         p = Plan();
         rc = make_plan(M, N, K, A, lda, B, ldb, C, ldc, SGEMM_ALGO_TF32X3, splits, SGEMM_FLAG_WHOLE_TILES, sms,
-                       p);
+                       beta != 0.f, p);
         if (rc != 0) return rc;
     }
     out->tile_m = p.tile_m;

@@ -39,8 +39,8 @@ struct TensorPlan {
 };
 int check_tensor_call(int M, int N, int K, float alpha, const float *A, int lda, const float *B, int ldb,
                       float beta, const float *C, int ldc, int splits);
-int plan_tensor_call(int M, int N, int K, const float *A, int lda, const float *B, int ldb, const float *C,
-                     int ldc, int splits, int sms, size_t max_ws_floats, TensorPlan *out);
+int plan_tensor_call(int M, int N, int K, const float *A, int lda, const float *B, int ldb, float beta,
+                     const float *C, int ldc, int splits, int sms, size_t max_ws_floats, TensorPlan *out);
 
 // C = beta * C (alpha == 0 or K == 0).
 cudaError_t scale_c_launch(float *C, long long ldc, int M, int N, float beta, int num_sms,

@@ -90,7 +90,7 @@ extern "C" int sgemm_noalloc(int M, int N, int K, float alpha, const float *A, i
         if (beta == 1.f) return 0;
         return static_cast<int>(sg::scale_c_launch(C, ldc, M, N, beta, d->sms, st));
     }
-    if ((rc = sg::plan_tensor_call(M, N, K, A, lda, B, ldb, C, ldc, splits, d->sms, kScratchFloats, &plan)) != 0)
+    if ((rc = sg::plan_tensor_call(M, N, K, A, lda, B, ldb, beta, C, ldc, splits, d->sms, kScratchFloats, &plan)) != 0)
         return rc;
     sg::DeviceCtl ctl{};
     ctl.status = d->status;

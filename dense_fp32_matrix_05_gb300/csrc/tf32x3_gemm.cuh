@@ -21,8 +21,9 @@
 //               aligned) or from their own global loads (any alignment,
 //               zero-filled edges, several stages in flight); the A tile
 //               (MMA B operand) -> hi/lo in K-major 64-byte-swizzled shared
-//               memory, split in place after a TMA copy (A rows 16-byte
-//               aligned) or from their own loads
+//               memory: after a TMA copy (A rows 16-byte aligned) the raw
+//               tile is the hi operand and only lo is written; otherwise
+//               both come from the producers' own loads
 //   next warp   tensor-memory allocation and the single MMA-issuing thread
 //   last warp   the TMA thread: copies raw A tiles and B slabs into the ring
 // Keeping the 128-row operand in tensor memory halves the shared-memory
@@ -37,7 +38,7 @@
 // "kernel 7") and the zero-filled edge tiles of "matmul_opt.cu"
 // (matrixMulOptimized), re-done for the tensor core: every element has to
 // pass a producer thread for the split, so B^T goes (TMA ->) registers ->
-// tensor memory, and A (TMA ->) shared memory -> split in place.
+// tensor memory, and A (TMA ->) shared memory, with lo written beside it.
 #pragma once
 #include <cuda.h>  // CUtensorMap (type only; the library does not link the driver)
 
@@ -129,9 +130,12 @@ __device__ __forceinline__ uint32_t sw64_off(int row, int chunk) {
 }
 
 // hi/lo split of one fp32 value: hi = x with the low 13 mantissa bits
-// cleared (an exact tf32 value, so the tensor core's own rounding of its
-// inputs never matters), lo = x - hi (exact in fp32; |lo| < 2^-10 |x|, the
-// tensor core keeps its top 11 significant bits, an error below 2^-20 |x|).
+// cleared (an exact tf32 value), lo = x - hi (exact in fp32; |lo| < 2^-10
+// |x|, the tensor core keeps its top 11 significant bits, an error below
+// 2^-20 |x|).  The tensor core reads a tf32 operand as the top 19 bits of
+// its 32-bit word and ignores the rest, so the raw fp32 word of x serves as
+// hi unchanged: operands copied by TMA keep x in place and only lo is
+// written (a GPU test checks that both forms give the same bits).
 // Non-finite x gives lo = NaN; the accumulator then comes out NaN and the
 // epilogue recomputes that element exactly (recompute_dot), so Inf and NaN
 // inputs still produce the IEEE fp32 result.  One logic op and one FADD.
@@ -215,8 +219,8 @@ __device__ __forceinline__ void split_store4(uint32_t hi_addr, uint32_t lo_addr,
 // Producer: split one k-tile into pipeline stage `s`: B^T hi/lo from
 // registers into tensor-memory columns [ring + 32 s, +32) of this warp's
 // lanes; A hi/lo into the shared-memory stage at `stage`, from registers
-// (AJ > 0) or, after a TMA copy, from the raw tile in the hi buffer (split in
-// place: each thread reads and rewrites its own chunks).
+// (AJ > 0) or, after a TMA copy into the hi buffer, lo alone (the raw tile
+// is already a valid hi operand).
 template <int TM, bool TMA_B, int KB, int BtK, int GT, int AJ, int AJ_TMA>
 __device__ __forceinline__ void store_split(uint32_t stage, uint32_t ring_taddr, int ptid,
                                             const Raw<BtK, AJ> &raw) {
@@ -229,7 +233,11 @@ __device__ __forceinline__ void store_split(uint32_t stage, uint32_t ring_taddr,
             const uint32_t col = stage + C::kOffBRaw + static_cast<uint32_t>((ptid & (kTileN - 1)) * 4);
             const int kb = (ptid >> 7) * KB;
 #pragma unroll
-            for (int e = 0; e < KB; ++e) split_tf32(lds32f(col + static_cast<uint32_t>((kb + e) * kTileN * 4)), hi[e], lo[e]);
+            for (int e = 0; e < KB; ++e) {
+                const float x = lds32f(col + static_cast<uint32_t>((kb + e) * kTileN * 4));
+                split_tf32(x, hi[e], lo[e]);
+                hi[e] = __float_as_uint(x);  // raw word: the tensor core drops the low bits
+            }
         } else {
 #pragma unroll
             for (int e = 0; e < KB; ++e) split_tf32(raw.b[e], hi[e], lo[e]);
@@ -253,9 +261,14 @@ __device__ __forceinline__ void store_split(uint32_t stage, uint32_t ring_taddr,
             const int j = ptid + r * GT;
             if (j < TM * 4) {
                 const uint32_t off = sw64_off(j >> 2, j & 3);
+                // the raw tile stays in place as hi; only lo is written
                 const float4 v = lds128(stage + C::kOffAHi + off);
-                const float x[4] = {v.x, v.y, v.z, v.w};
-                split_store4(stage + C::kOffAHi + off, stage + C::kOffALo + off, x);
+                uint32_t h, l0, l1, l2, l3;
+                split_tf32(v.x, h, l0);
+                split_tf32(v.y, h, l1);
+                split_tf32(v.z, h, l2);
+                split_tf32(v.w, h, l3);
+                sts128(stage + C::kOffALo + off, l0, l1, l2, l3);
             }
         }
     }

@@ -79,6 +79,26 @@ def test_leading_dimensions_and_alignment(algo, layout, shape):
     check_against_oracle(p, C, what=f"{shape} {layout} algo={algo}")
 
 
+@pytest.mark.parametrize("rows", [64, 256])
+def test_tma_and_load_paths_agree_bitwise(rows):
+    """Operands copied by TMA keep their raw fp32 words as the hi part (the
+    tensor core reads only the top 19 bits of a tf32 operand); operands the
+    producers load themselves get hi with the low 13 bits cleared.  Both must
+    give the same bits: aligned and misaligned copies of the same problem
+    take the two paths with the same schedule and summation order."""
+    M, N, K = 300, 392, 700  # lda and ldb multiples of 4: offset 0 is 16-byte aligned
+    p = _with_c(random_problem(M, N, K, alpha=1.0, beta=0.5, seed=rows, pad_value=0.0))
+    flags = pkg.SGEMM_FLAG_TILE_ROWS(rows) | pkg.SGEMM_FLAG_WHOLE_TILES
+    outs = {}
+    for off in [(0, 0, 0), (1, 0, 0), (0, 1, 0), (1, 1, 0)]:
+        C, st = run_sgemm(p, pkg.SGEMM_ALGO_TF32X3, offsets=off, flags=flags)
+        assert st == 0
+        outs[off] = C.view(np.uint32)
+    check_against_oracle(p, outs[(0, 0, 0)].view(np.float32), what=f"rows={rows} aligned")
+    for off, c in outs.items():
+        assert np.array_equal(c, outs[(0, 0, 0)]), f"offsets {off} differ from the TMA path"
+
+
 TILE_ROWS = [16, 32, 64, 128, 192, 256]
 
 
