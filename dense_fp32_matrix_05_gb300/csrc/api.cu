@@ -401,7 +401,7 @@ int run(int M, int N, int K, float alpha, const float *A, int lda, const float *
     GemmArgs g{M, N, K, alpha, beta, A, lda, B, ldb, C, ldc};
     cudaError_t e;
     if (p.path == SGEMM_ALGO_TF32X3)
-        e = sg::tf32x3_launch(p.tile_m, g, p.sch, ctl, p.vec_a, p.vec_b, p.grid, stream);
+        e = sg::tf32x3_launch(p.tile_m, g, p.sch, ctl, p.vec_a, p.vec_b, p.vec_c, p.grid, stream);
     else
         e = sg::ffma_launch(p.tile_m, p.tile_n, g, p.sch, ctl, p.vec_a, p.vec_b, p.vec_c, stream);
     return from_cuda(e);
@@ -643,6 +643,7 @@ int plan_tensor_call(int M, int N, int K, const float *A, int lda, const float *
     out->grid = p.grid;
     out->vec_a = p.vec_a;
     out->vec_b = p.vec_b;
+    out->vec_c = p.vec_c;
     out->ws_floats = p.ws_bytes / sizeof(float);
     out->tiles = p.sch.m_tiles * p.sch.n_tiles;
     return 0;

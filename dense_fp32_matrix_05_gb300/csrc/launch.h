@@ -17,7 +17,7 @@ bool tf32x3_supported_tm(int tm);
 int tf32x3_stages(int tm);
 int tf32x3_smem_bytes(int tm);
 cudaError_t tf32x3_launch(int tm, const GemmArgs &g, const Schedule &s, const DeviceCtl &ctl,
-                          int vec_a, int vec_b, int grid, cudaStream_t stream);
+                          int vec_a, int vec_b, int vec_c, int grid, cudaStream_t stream);
 
 // FFMA path.  (bm, bn) in {(128,128), (64,256), (32,512)}.
 bool ffma_supported_tile(int bm, int bn);
@@ -34,6 +34,7 @@ struct TensorPlan {
     int grid = 0;
     int vec_a = 0;
     int vec_b = 0;
+    int vec_c = 0;
     size_t ws_floats = 0;  // split-K partial-tile floats needed (0 without split-K)
     int tiles = 0;         // output tiles (= arrival counters needed)
 };

@@ -107,5 +107,5 @@ extern "C" int sgemm_noalloc(int M, int N, int K, float alpha, const float *A, i
     }
     sg::GemmArgs g{M, N, K, alpha, beta, A, lda, B, ldb, C, ldc};
     return static_cast<int>(
-        sg::tf32x3_launch(plan.tile_m, g, plan.sch, ctl, plan.vec_a, plan.vec_b, plan.grid, st));
+        sg::tf32x3_launch(plan.tile_m, g, plan.sch, ctl, plan.vec_a, plan.vec_b, plan.vec_c, plan.grid, st));
 }

@@ -69,14 +69,33 @@ bool make_tmap_b(const GemmArgs &g, CUtensorMap *map) {
     return r == CUDA_SUCCESS;
 }
 
+// Tensor map of C for the TMA epilogue: a N x M fp32 tensor (N innermost)
+// with row stride ldc * 4 bytes, copied in and out in boxes of 128 (n) x 16
+// (rows) without swizzle; loads fill out-of-range elements with zeros and
+// stores skip them.
+bool make_tmap_c(const GemmArgs &g, CUtensorMap *map) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(g.N), static_cast<cuuint64_t>(g.M)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(g.ldc) * sizeof(float)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(tf32x3::kTileN), static_cast<cuuint32_t>(tf32x3::kEpiRows)};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, g.C, dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 template <int TM, bool TA, bool TB>
-cudaError_t launch_tm(const GemmArgs &g, const Schedule &s, const DeviceCtl &ctl, int vec_a, int grid,
-                      const CUtensorMap &map_a, const CUtensorMap &map_b, cudaStream_t stream) {
+cudaError_t launch_tm(const GemmArgs &g, const Schedule &s, const DeviceCtl &ctl, int vec_a, int tma_c, int grid,
+                      const CUtensorMap &map_a, const CUtensorMap &map_b, const CUtensorMap &map_c,
+                      cudaStream_t stream) {
     using C = tf32x3::Cfg<TM, TB>;
     auto kern = tf32x3::tf32x3_gemm_kernel<TM, TA, TB>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    kern<<<grid, tf32x3::Roles<TM, TA, TB>::kThreads, C::kSmemBytes, stream>>>(g, s, ctl, vec_a, map_a, map_b);
+    kern<<<grid, tf32x3::Roles<TM, TA, TB>::kThreads, C::kSmemBytes, stream>>>(g, s, ctl, vec_a, tma_c, map_a,
+                                                                                 map_b, map_c);
     return cudaGetLastError();
 }
 
@@ -86,18 +105,20 @@ cudaError_t launch_tm(const GemmArgs &g, const Schedule &s, const DeviceCtl &ctl
 // the register spills and load stalls it removes).
 template <int TM>
 cudaError_t launch_rows(const GemmArgs &g, const Schedule &s, const DeviceCtl &ctl, int vec_a, int vec_b,
-                        int grid, cudaStream_t stream) {
-    CUtensorMap ma, mb;
+                        int vec_c, int grid, cudaStream_t stream) {
+    CUtensorMap ma, mb, mc;
     std::memset(&ma, 0, sizeof(ma));
     std::memset(&mb, 0, sizeof(mb));
+    std::memset(&mc, 0, sizeof(mc));
     const bool ta = vec_a && make_tmap_a(g, TM, &ma);
     const bool tb = vec_b && make_tmap_b(g, &mb);
+    const int tc = (vec_c && make_tmap_c(g, &mc)) ? 1 : 0;
     if (tb) {
-        if (ta) return launch_tm<TM, true, true>(g, s, ctl, vec_a, grid, ma, mb, stream);
-        return launch_tm<TM, false, true>(g, s, ctl, vec_a, grid, ma, mb, stream);
+        if (ta) return launch_tm<TM, true, true>(g, s, ctl, vec_a, tc, grid, ma, mb, mc, stream);
+        return launch_tm<TM, false, true>(g, s, ctl, vec_a, tc, grid, ma, mb, mc, stream);
     }
-    if (ta) return launch_tm<TM, true, false>(g, s, ctl, vec_a, grid, ma, mb, stream);
-    return launch_tm<TM, false, false>(g, s, ctl, vec_a, grid, ma, mb, stream);
+    if (ta) return launch_tm<TM, true, false>(g, s, ctl, vec_a, tc, grid, ma, mb, mc, stream);
+    return launch_tm<TM, false, false>(g, s, ctl, vec_a, tc, grid, ma, mb, mc, stream);
 }
 
 }  // namespace
@@ -106,7 +127,17 @@ bool tf32x3_supported_tm(int tm) {
     return tm == 16 || tm == 32 || tm == 64 || tm == 128 || tm == 192 || tm == 256;
 }
 
-int tf32x3_stages(int tm) { return tf32x3::stages_for(tm); }
+int tf32x3_stages(int tm) {
+    switch (tm) {  // with B copied by TMA (the usual case)
+        case 16: return tf32x3::Cfg<16, true>::kStages;
+        case 32: return tf32x3::Cfg<32, true>::kStages;
+        case 64: return tf32x3::Cfg<64, true>::kStages;
+        case 128: return tf32x3::Cfg<128, true>::kStages;
+        case 192: return tf32x3::Cfg<192, true>::kStages;
+        case 256: return tf32x3::Cfg<256, true>::kStages;
+        default: return 0;
+    }
+}
 
 int tf32x3_smem_bytes(int tm) {
     switch (tm) {
@@ -121,14 +152,14 @@ int tf32x3_smem_bytes(int tm) {
 }
 
 cudaError_t tf32x3_launch(int tm, const GemmArgs &g, const Schedule &s, const DeviceCtl &ctl, int vec_a,
-                          int vec_b, int grid, cudaStream_t stream) {
+                          int vec_b, int vec_c, int grid, cudaStream_t stream) {
     switch (tm) {
-        case 16: return launch_rows<16>(g, s, ctl, vec_a, vec_b, grid, stream);
-        case 32: return launch_rows<32>(g, s, ctl, vec_a, vec_b, grid, stream);
-        case 64: return launch_rows<64>(g, s, ctl, vec_a, vec_b, grid, stream);
-        case 128: return launch_rows<128>(g, s, ctl, vec_a, vec_b, grid, stream);
-        case 192: return launch_rows<192>(g, s, ctl, vec_a, vec_b, grid, stream);
-        case 256: return launch_rows<256>(g, s, ctl, vec_a, vec_b, grid, stream);
+        case 16: return launch_rows<16>(g, s, ctl, vec_a, vec_b, vec_c, grid, stream);
+        case 32: return launch_rows<32>(g, s, ctl, vec_a, vec_b, vec_c, grid, stream);
+        case 64: return launch_rows<64>(g, s, ctl, vec_a, vec_b, vec_c, grid, stream);
+        case 128: return launch_rows<128>(g, s, ctl, vec_a, vec_b, vec_c, grid, stream);
+        case 192: return launch_rows<192>(g, s, ctl, vec_a, vec_b, vec_c, grid, stream);
+        case 256: return launch_rows<256>(g, s, ctl, vec_a, vec_b, vec_c, grid, stream);
         default: return cudaErrorInvalidValue;
     }
 }

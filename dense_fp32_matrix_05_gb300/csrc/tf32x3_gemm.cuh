@@ -83,14 +83,26 @@ struct Roles {
 // Tensor memory (512 columns of 128 lanes x 32 bit): accumulators of TM
 // columns each, then a ring of STAGES B^T stages of 32 columns (16 hi + 16 lo
 // k values per lane = per C column).
-__host__ __device__ constexpr int nacc_for(int tm) { return tm >= 192 ? 1 : 2; }
-__host__ __device__ constexpr int stages_for(int tm) { return tm >= 256 ? 6 : 8; }
+constexpr uint32_t kTmemCols = 512;
 constexpr int kRingColsPerStage = 2 * kBK;
-constexpr int kSmemLimit = 232448;
+constexpr int kMaxStages = 12;
+__host__ __device__ constexpr int nacc_for(int tm) { return tm >= 192 ? 1 : 2; }
+// every tensor-memory column the accumulators leave, up to kMaxStages (short
+// tiles stream long B panels and want many copies in flight)
+__host__ __device__ constexpr int stages_for(int tm) {
+    return (static_cast<int>(kTmemCols) - nacc_for(tm) * tm) / kRingColsPerStage < kMaxStages
+               ? (static_cast<int>(kTmemCols) - nacc_for(tm) * tm) / kRingColsPerStage
+               : kMaxStages;
+}
+constexpr int kSmemLimit = 232448;  // dynamic shared memory one CTA may use on sm_103a
+// C chunks the epilogue stages in shared memory for TMA copies (16 rows of
+// the 128 tile columns each); loads run two chunks ahead of the arithmetic.
+constexpr int kEpiBufs = 3;
+constexpr int kEpiRows = 16;
+constexpr int kEpiChunkBytes = kEpiRows * 128 * 4;
 // Shared tiles whose sum a CTA defers to its exit (see fixup_tile); the
 // planner gives no CTA more split-K units than this.
-constexpr int kMaxDefer = 8;  // dynamic shared memory one CTA may use on sm_103a
-constexpr uint32_t kTmemCols = 512;
+constexpr int kMaxDefer = 8;
 
 // TM = C rows per tile (MMA N).  TMA_B: the stage also holds the raw B tile
 // (16 k rows x 128 n, copied by TMA) that the producers read and split.
@@ -104,20 +116,23 @@ struct Cfg {
     static constexpr int kBRawBytes = TMA_B ? kBK * kTileN * 4 : 0;
     static constexpr int kOffBRaw = 2 * kABytes;
     static constexpr int kStageBytes = 2 * kABytes + kBRawBytes;
+    // epilogue staging for TMA copies of C: kEpiBufs chunks of 16 rows x 128
+    static constexpr int kEpiBufBytes = kEpiBufs * kEpiChunkBytes;
     // as many stages as tensor memory and the 227 KB of shared memory allow
-    static constexpr int kStages = stages_for(TM) < (kSmemLimit - 2048) / kStageBytes
-                                       ? stages_for(TM) : (kSmemLimit - 2048) / kStageBytes;
+    static constexpr int kStages = stages_for(TM) < (kSmemLimit - 2048 - kEpiBufBytes) / kStageBytes
+                                       ? stages_for(TM) : (kSmemLimit - 2048 - kEpiBufBytes) / kStageBytes;
+    static constexpr int kOffEpi = kStages * kStageBytes;
     static_assert(kStageBytes % 1024 == 0, "stages must keep 1 KB alignment");
     static constexpr int kRingCol = kNacc * TM;
     static_assert(kRingCol + kStages * kRingColsPerStage <= static_cast<int>(kTmemCols), "tensor memory");
     static constexpr int kChunk = 16;  // accumulator columns per tensor-memory load in the epilogue
     static constexpr uint32_t kIdesc = umma_idesc_tf32(kTileN, TM);
     // barriers: full[S], empty[S], a_full[S], acc_full[2], acc_empty[2],
-    // drain; then words: tensor-memory address, abort flag, (unused), count
-    // of deferred sums, and kMaxDefer entries (tile row, tile column,
-    // segment count, first workspace slot)
-    static constexpr int kBarBytes = 8 * (3 * kStages + 5) + 4 * (4 + 4 * kMaxDefer);
-    static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes;
+    // drain, c_full[kEpiBufs]; then words: tensor-memory address, abort
+    // flag, (unused), count of deferred sums, and kMaxDefer entries (tile row,
+    // tile column, segment count, first workspace slot)
+    static constexpr int kBarBytes = 8 * (3 * kStages + 5 + kEpiBufs) + 4 * (4 + 4 * kMaxDefer);
+    static constexpr int kSmemBytes = 1024 + kOffEpi + kEpiBufBytes + kBarBytes;
     static_assert(kSmemBytes <= kSmemLimit, "shared memory per CTA");
     static_assert(kStages >= 4, "pipeline depth");
 };
@@ -473,8 +488,9 @@ __device__ __forceinline__ void prefetch_c_tile(const GemmArgs &g, int m0, int n
 template <int TM, bool TMA_A, bool TMA_B>
 __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
     tf32x3_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ Schedule sch,
-                       const __grid_constant__ DeviceCtl ctl, int vec_a,
-                       const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b) {
+                       const __grid_constant__ DeviceCtl ctl, int vec_a, int tma_c,
+                       const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                       const __grid_constant__ CUtensorMap tmap_c) {
     using C = Cfg<TM, TMA_B>;
     using R = Roles<TM, TMA_A, TMA_B>;
     constexpr int S = C::kStages;
@@ -485,12 +501,15 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
     const uint32_t raw_base = smem_u32(smem_raw);
     const uint32_t base = (raw_base + 1023u) & ~1023u;
     uint8_t *base_ptr = smem_raw + (base - raw_base);
-    const uint32_t bars = base + S * C::kStageBytes;  // full[s] = bars + 8s, empty[s] = bars + 8(S+s)
+    const uint32_t epi_buf0 = base + C::kOffEpi;                   // C chunk b at epi_buf0 + b * kEpiChunkBytes
+    const uint32_t bars = base + C::kOffEpi + C::kEpiBufBytes;  // full[s] = bars + 8s, empty[s] = bars + 8(S+s)
     const uint32_t afull0 = bars + 8u * (2 * S);       // a_full[s]: TMA copy of stage s landed
     const uint32_t acc_full0 = bars + 8u * (3 * S);
     const uint32_t acc_empty0 = acc_full0 + 16u;
     const uint32_t drain_bar = acc_empty0 + 16u;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(base_ptr + S * C::kStageBytes + 8 * (3 * S + 5));
+    const uint32_t cfull0 = drain_bar + 8u;            // c_full[b]: TMA copy of C chunk buffer b landed
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(base_ptr + C::kOffEpi + C::kEpiBufBytes +
+                                                       8 * (3 * S + 5 + kEpiBufs));
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     volatile int *s_ndefer = reinterpret_cast<volatile int *>(tmem_slot + 3);
     volatile int *s_defer = reinterpret_cast<volatile int *>(tmem_slot + 4);  // [kMaxDefer][mt, nt, nseg, slot0]
@@ -509,6 +528,7 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
         mbar_init(acc_empty0, kEpiWarps * 32);
         mbar_init(acc_empty0 + 8u, kEpiWarps * 32);
         mbar_init(drain_bar, 1);
+        for (int b = 0; b < kEpiBufs; ++b) mbar_init(cfull0 + 8u * b, 1);
         *abort_flag = 0;
         *s_ndefer = 0;
         fence_mbar_init();
@@ -526,12 +546,32 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
         // ------------------------------------------------------ epilogue
         const int nl = warp * 32 + lane;  // tensor-memory lane = column within the tile
         int it = 0;
+        uint32_t cpar = 0;      // per C buffer: parity of its next c_full phase
+        uint32_t inflight = 0;  // per C buffer: a TMA copy into it not yet waited for
         UnitIter ui;
         for (ui.start(sch, blockIdx.x); ui.ok; ui.next(sch), ++it) {
             const UnitCoord &c = ui.c;
             const int acc = it % C::kNacc;
             const uint32_t aph = (it / C::kNacc) & 1;
             if (c.nseg == 1 && g.beta != 0.f) prefetch_c_tile<TM>(g, c.mt * TM, c.nt * kTileN, threadIdx.x);
+            if (c.nseg == 1 && tma_c) {
+                // the previous tile's stores have read their buffers; copy the
+                // first C chunks of this tile while the accumulator is computed
+                if (threadIdx.x == 0) bulk_wait_group_read<0>();
+                if (g.beta != 0.f) {
+                    // chunks that start at or beyond row M are never copied
+                    const int nch = min(TM / CH, (g.M - c.mt * TM + CH - 1) / CH);
+#pragma unroll
+                    for (int ch = 0; ch < kEpiBufs - 1 && ch < nch; ++ch) {
+                        if (threadIdx.x == 0) {
+                            mbar_arrive_expect_tx(cfull0 + 8u * ch, kEpiChunkBytes);
+                            tma_load_2d(epi_buf0 + ch * kEpiChunkBytes, &tmap_c, c.nt * kTileN, c.mt * TM + ch * CH,
+                                        cfull0 + 8u * ch);
+                        }
+                        inflight |= 1u << ch;
+                    }
+                }
+            }
             const bool w = mbar_wait_bounded(acc_full0 + 8u * acc, aph, abort_flag, ctl,
                                              kStatusTimeoutEpilogue);
             if (!epi_all(w)) break;
@@ -540,7 +580,77 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
             const int m0 = c.mt * TM;
             const uint32_t t0 = tmem_base + (static_cast<uint32_t>(warp * 32) << 16) +
                                 static_cast<uint32_t>(acc * TM);
-            if (c.nseg == 1) {
+            if (c.nseg == 1 && tma_c) {
+                // Chunks of CH accumulator columns (C rows) staged in shared
+                // memory: C copied in by TMA (two chunks ahead), alpha/beta
+                // applied in place, the chunk copied out by one TMA store.
+                // Buffer b of chunk ch = ch % kEpiBufs; before a buffer is
+                // written again, the store that last read it has finished.
+                static_assert(CH == kEpiRows, "one C chunk per tensor-memory load");
+                const bool read_c = g.beta != 0.f;
+                const bool n_ok = n < g.N;
+                const int n0 = c.nt * kTileN;
+                const int nch = min(TM / CH, (g.M - m0 + CH - 1) / CH);  // chunks with rows below M
+                bool ok = true;
+#pragma unroll 1
+                for (int ch = 0; ch < nch; ++ch) {
+                    const int b = ch % kEpiBufs;
+                    const uint32_t col = epi_buf0 + b * kEpiChunkBytes + nl * 4;
+                    if (read_c) {
+                        const bool wc = mbar_wait_bounded(cfull0 + 8u * b, (cpar >> b) & 1u, abort_flag, ctl,
+                                                          kStatusTimeoutEpilogue);
+                        if (!epi_all(wc)) {
+                            ok = false;
+                            break;
+                        }
+                        cpar ^= 1u << b;
+                        inflight &= ~(1u << b);
+                    }
+                    uint32_t r[CH];
+                    tmem_ld32x16_issue(t0 + ch * CH, r);
+                    tmem_ld_wait16(r);
+                    const int mb = m0 + ch * CH;
+                    float v[CH];
+                    bool nan = false;
+#pragma unroll
+                    for (int j = 0; j < CH; ++j) {
+                        v[j] = __uint_as_float(r[j]);
+                        nan |= v[j] != v[j];
+                    }
+                    if (nan && n_ok) {
+#pragma unroll 1
+                        for (int j = 0; j < CH; ++j)
+                            if (v[j] != v[j] && mb + j < g.M) v[j] = recompute_dot(g, mb + j, n);
+                    }
+#pragma unroll
+                    for (int j = 0; j < CH; ++j) {
+                        const uint32_t a = col + static_cast<uint32_t>(j * kTileN * 4);
+                        sts32(a, read_c ? fmaf(g.beta, lds32f(a), g.alpha * v[j]) : g.alpha * v[j]);
+                    }
+                    fence_proxy_async_smem();
+                    // the store of chunk ch - 2 has read its buffer (next iteration's)
+                    if (threadIdx.x == 0) bulk_wait_group_read<kEpiBufs - 2>();
+                    named_bar_sync(kEpiBarrierId, kEpiWarps * 32);
+                    if (threadIdx.x == 0) {
+                        tma_store_2d(&tmap_c, epi_buf0 + b * kEpiChunkBytes, n0, mb);
+                        bulk_commit_group();
+                    }
+                    if (read_c && ch + kEpiBufs - 1 < nch) {
+                        // chunk ch + 2 goes where chunk ch - 1 was: wait for its store
+                        const int nb = (ch + kEpiBufs - 1) % kEpiBufs;
+                        if (threadIdx.x == 0) {
+                            bulk_wait_group_read<1>();
+                            mbar_arrive_expect_tx(cfull0 + 8u * nb, kEpiChunkBytes);
+                            tma_load_2d(epi_buf0 + nb * kEpiChunkBytes, &tmap_c, n0, mb + (kEpiBufs - 1) * CH,
+                                        cfull0 + 8u * nb);
+                        }
+                        inflight |= 1u << nb;
+                    }
+                }
+                if (!ok) break;
+                tc_fence_before();
+                mbar_arrive(acc_empty0 + 8u * acc);
+            } else if (c.nseg == 1) {
                 // Chunks of CH accumulator columns (C rows): each chunk's C
                 // loads are issued before its tensor-memory load and are in
                 // flight together with it (C was requested into L2 while
@@ -629,6 +739,15 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
                     }
                 }
             }
+        }
+        if (tma_c && threadIdx.x == 0) {
+            // C stores finished and every C copy into shared memory landed
+            // before the CTA may exit
+            bulk_wait_group<0>();
+            volatile int no_abort = 0;
+            for (int b = 0; b < kEpiBufs; ++b)
+                if (inflight & (1u << b))
+                    mbar_wait_bounded(cfull0 + 8u * b, (cpar >> b) & 1u, &no_abort, ctl, kStatusTimeoutDrain);
         }
     } else if (warp < R::kMmaWarp) {
         // ------------------------------------------------------ producers
