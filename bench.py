@@ -148,6 +148,20 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
+_MMA_RATE = {}
+
+
+def tf32_mma_rate(pkg) -> float:
+    """Raw tf32 TFLOP/s of the kernel's MMA form on this GPU (measured once)."""
+    if "v" not in _MMA_RATE:
+        try:
+            _MMA_RATE["v"] = pkg.sgemm_tf32_mma_rate(256, 20000)
+        except Exception as exc:  # reported, not fatal: the contract's peak stands
+            log(f"tf32 MMA rate probe failed: {exc}")
+            _MMA_RATE["v"] = None
+    return _MMA_RATE["v"]
+
+
 def roofline_peak(path: int, peaks: dict, source: str, sms: int):
     """(bound, peak TFLOP/s, basis text) for a path."""
     import dense_fp32_matrix_05_gb300 as pkg
@@ -328,6 +342,12 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     }
     if cublas is not None:
         result["context_cublas_sgemm_tflops"] = round(cublas, 3)
+    if bound == "tensor":
+        rate = tf32_mma_rate(pkg)
+        if rate:
+            # second denominator: the tf32 rate measured on the kernel's own MMA form
+            result["roofline"]["tf32_mma_rate_tflops"] = round(rate, 1)
+            result["roofline"]["frac_of_mma_rate"] = round(achieved / (rate / 3.0), 4)
     return result, p
 
 

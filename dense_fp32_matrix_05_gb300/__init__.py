@@ -22,7 +22,7 @@ __all__ = [
     "SGEMM_ERR_DEVICE_TIMEOUT",
     "SgemmError", "library", "lib_path", "declared_functions",
     "sgemm", "sgemm_ex", "sgemm_host", "sgemm_plan_info", "sgemm_check_status",
-    "sgemm_status_string", "sgemm_release", "sgemm_version", "sgemm_noalloc", "matmul",
+    "sgemm_status_string", "sgemm_release", "sgemm_version", "sgemm_noalloc", "sgemm_tf32_mma_rate", "matmul",
     "SGEMM_ERR_SCRATCH_LIMIT",
 ]
 
@@ -63,6 +63,7 @@ _SIGS = {
     "sgemm_status_string": (ctypes.c_char_p, [_i]),
     "sgemm_release": (_i, []),
     "sgemm_version": (_i, []),
+    "sgemm_tf32_mma_rate": (_i, [_i, _i, _p, ctypes.POINTER(ctypes.c_double)]),
     "sgemm_noalloc": (_i, [_i, _i, _i, _f, _p, _i, _p, _i, _f, _p, _i, _p, _i]),
 }
 
@@ -169,6 +170,15 @@ def sgemm_status_string(status: int) -> str:
         return library().sgemm_status_string(int(status)).decode()
     except Exception:  # library missing: still describe the code
         return f"status {status}"
+
+
+def sgemm_tf32_mma_rate(n: int = 256, iters: int = 20000, stream=None) -> float:
+    """Raw tf32 TFLOP/s of the tensor cores on the 3xTF32 kernel's MMA form."""
+    out = ctypes.c_double(0.0)
+    rc = library().sgemm_tf32_mma_rate(n, iters, _stream(stream), ctypes.byref(out))
+    if rc != 0:
+        raise SgemmError("sgemm_tf32_mma_rate", rc)
+    return out.value
 
 
 def sgemm_release() -> int:

@@ -225,6 +225,26 @@ int sgemm_noalloc(int M, int N, int K, float alpha,
 /* sgemm_version - library version as 10000*major + 100*minor + patch. */
 int sgemm_version(void);
 
+/*
+ * sgemm_tf32_mma_rate - measure the tensor cores' rate on the MMA form the
+ * 3xTF32 path issues (tcgen05.mma kind::tf32, M = 128, N = n, K = 8, A from
+ * tensor memory, B from shared memory, fp32 accumulator), on the current
+ * device.  This is measurement, not GEMM: the pages time their kernels
+ * against a device peak ("NVIDIA_SGEMM_PRACTICE", overview table), and this
+ * call supplies the tf32 peak the way the kernel uses the tensor cores.
+ *
+ *   n      (1): MMA N, a multiple of 16 in [16, 256].
+ *   iters  (2): MMAs per SM, >= 1 (about 150 cycles each at n = 256).
+ *   stream (3): stream the two launches (warm-up, timed) are ordered on;
+ *               the call waits for them.
+ *   tflops (4): out, raw tf32 TFLOP/s = SMs x iters x 2 x 128 x n x 8 / time.
+ *
+ * Returns 0, -i for a bad argument, a positive cudaError_t,
+ * SGEMM_ERR_UNSUPPORTED_DEVICE, or SGEMM_ERR_DEVICE_TIMEOUT if the bounded
+ * wait for the MMAs gave up.  Allocates nothing on the device.
+ */
+int sgemm_tf32_mma_rate(int n, int iters, sgemm_stream_t stream, double *tflops);
+
 #ifdef __cplusplus
 }
 #endif

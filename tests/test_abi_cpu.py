@@ -182,3 +182,16 @@ def test_plan_info_rejects_bad_arguments():
         pkg.sgemm_plan_info(4, 4, 4, algo=7, num_sms=SMS)
     with pytest.raises(pkg.SgemmError):
         pkg.sgemm_plan_info(4, 4, 4, flags=pkg.SGEMM_FLAG_TILE_ROWS(80), num_sms=SMS)
+
+
+def test_tf32_mma_rate_rejects_bad_arguments(lib):
+    """Argument checks come before any device query, so they run here."""
+    import ctypes
+    out = ctypes.c_double(0.0)
+    f = pkg.library().sgemm_tf32_mma_rate
+    assert f(8, 100, None, ctypes.byref(out)) == -1      # n below 16
+    assert f(264, 100, None, ctypes.byref(out)) == -1    # n above 256
+    assert f(72, 100, None, ctypes.byref(out)) == -1     # not a multiple of 16
+    assert f(256, 0, None, ctypes.byref(out)) == -2
+    assert f(256, 100, None, None) == -4
+

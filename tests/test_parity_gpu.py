@@ -331,3 +331,32 @@ def test_plan_info_on_device_matches_sm_count():
     props = torch.cuda.get_device_properties(0)
     info = pkg.sgemm_plan_info(5120, 5120, 5120, num_sms=0)
     assert info["grid"] == min(info["units"], props.multi_processor_count)
+
+
+def test_tf32_mma_rate_is_plausible():
+    """The tensor-core rate probe finishes with a plausible rate, narrower
+    MMAs are not faster, and the 3xTF32 GEMM (three MMAs per product) at
+    4096^3 does not beat a third of the probed rate by more than noise."""
+    import time
+    import torch
+
+    rate = pkg.sgemm_tf32_mma_rate(256, 4000)
+    assert 200.0 < rate < 5000.0, rate
+    small = pkg.sgemm_tf32_mma_rate(64, 4000)
+    assert 0.0 < small <= rate * 1.05
+    M = N = K = 4096
+    g = torch.Generator(device="cpu").manual_seed(0)
+    A = (torch.rand(M, K, generator=g) * 2 - 1).cuda()
+    B = (torch.rand(K, N, generator=g) * 2 - 1).cuda()
+    C = torch.empty(M, N, device="cuda")
+    st = torch.cuda.current_stream()
+    for _ in range(2):
+        assert pkg.sgemm(M, N, K, 1.0, A, K, B, N, 0.0, C, N, st) == 0
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(5):
+        assert pkg.sgemm(M, N, K, 1.0, A, K, B, N, 0.0, C, N, st) == 0
+    torch.cuda.synchronize()
+    gemm = 2.0 * M * N * K * 5 / (time.perf_counter() - t0) / 1e12
+    assert gemm < rate / 3.0 * 1.1, (gemm, rate)
+
