@@ -15,7 +15,9 @@
 //     rows a warp reads per instruction fall in four different bank groups;
 //     B is kept N-major, read as 8 consecutive 16-byte chunks per warp;
 //   - per 4-k step a thread loads its 8 rows x 4 k of A and, per k, 8 values
-//     of B (16 LDS.128 per 256 FFMA) and updates 64 accumulators;
+//     of B (16 LDS.128 per 256 FMAs) and updates 64 accumulators, held as
+//     32 column pairs so that each k takes 32 packed fma.rn.f32x2 (same
+//     per-element rounding and order as fmaf, half the issue slots);
 //   - epilogue alpha*acc + beta*C (C not read when beta == 0), 128-bit
 //     accesses when C rows are aligned, predicated edges; split-K partials
 //     go to a workspace and the last slice to arrive sums them in order.
@@ -115,11 +117,12 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int KT = c.ke - c.kb;
     const uint32_t s0 = smem_u32(smem_f);
 
-    float acc[8][8];
+    // accumulators in column pairs: acc2[i][q] = (C[i][2q], C[i][2q + 1])
+    uint64_t acc2[8][4];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+        for (int q = 0; q < 4; ++q) acc2[i][q] = 0ull;
 
 #pragma unroll
     for (int s = 0; s < STAGES - 1; ++s) {
@@ -157,18 +160,28 @@ __global__ void __launch_bounds__(kThreads, 2)
             }
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
+                // 8 values of B as 4 column pairs; a[i] broadcast into a pair:
+                // 32 paired FMAs per k instead of 64 single ones
                 const int k = kq * 4 + kk;
-                const float4 b0 = lds128(sB + (k * BN + col_base) * 4);
-                const float4 b1 = lds128(sB + (k * BN + col_base + 32) * 4);
-                const float b[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+                uint64_t b[4];
+                lds_pairs(sB + (k * BN + col_base) * 4, b[0], b[1]);
+                lds_pairs(sB + (k * BN + col_base + 32) * 4, b[2], b[3]);
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
+                for (int i = 0; i < 8; ++i) {
+                    const uint64_t ai = pair_bcast(a[i][kk]);
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i][kk], b[j], acc[i][j]);
+                    for (int q = 0; q < 4; ++q) ffma2(acc2[i][q], ai, b[q]);
+                }
             }
         }
     }
     cp_async_wait<0>();
+
+    float acc[8][8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) pair_split(acc2[i][q], acc[i][2 * q], acc[i][2 * q + 1]);
 
     if (c.nseg > 1 && (ctl.ws == nullptr || ctl.counters == nullptr)) {
         // a shared tile without a workspace: report, never dereference

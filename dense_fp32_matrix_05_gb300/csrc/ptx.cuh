@@ -90,6 +90,29 @@ __device__ __forceinline__ void bulk_wait_group() {
     asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// ------------------------------------------------------------ packed fp32
+// fma.rn.f32x2: two independent fp32 FMAs (each lane of the pair rounds as
+// fma.rn.f32 does) in one instruction, so a stream of FMAs takes half the
+// issue slots.  A pair lives in one 64-bit register: .x low, .y high.
+__device__ __forceinline__ void ffma2(uint64_t &d, uint64_t a, uint64_t b) {
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(d) : "l"(a), "l"(b));
+}
+
+__device__ __forceinline__ uint64_t pair_bcast(float x) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %1};" : "=l"(r) : "f"(x));
+    return r;
+}
+
+__device__ __forceinline__ void pair_split(uint64_t p, float &x, float &y) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(x), "=f"(y) : "l"(p));
+}
+
+// Two 64-bit pairs (four consecutive floats) from shared memory.
+__device__ __forceinline__ void lds_pairs(uint32_t addr, uint64_t &p0, uint64_t &p1) {
+    asm volatile("ld.shared.v2.b64 {%0, %1}, [%2];" : "=l"(p0), "=l"(p1) : "r"(addr));
+}
+
 __device__ __forceinline__ void sts32(uint32_t addr, float v) {
     asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
