@@ -48,7 +48,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 KERNEL_SOURCES = ["dense_fp32_matrix_05_gb300/csrc/tf32x3_gemm.cuh",
                   "dense_fp32_matrix_05_gb300/csrc/ffma_gemm.cuh",
                   "dense_fp32_matrix_05_gb300/csrc/common.cuh",
-                  "dense_fp32_matrix_05_gb300/csrc/ptx.cuh"]
+                  "dense_fp32_matrix_05_gb300/csrc/ptx.cuh",
+                  "dense_fp32_matrix_05_gb300/csrc/ffma_wide.cu"]
 
 
 def log(*a):
@@ -300,6 +301,9 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         unit_r = "TFLOP/s"
         achieved = flops / (launch_ms * 1e-3) / 1e12
     path_name = {1: "ffma", 2: "tf32x3"}[plan["path"]]
+    kernel_name = "ffma_wide_kernel" if plan.get("wide") else f"{path_name}_gemm_kernel"
+    if plan.get("wide"):
+        path_name = "ffma_wide"
     traffic = recorded_traffic(args.workload, path_name)
     value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
 
@@ -329,7 +333,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         },
         "roofline": {"bound": bound, "achieved": round(achieved, 3), "peak": round(peak, 3),
                      "unit": unit_r, "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "peak_basis": basis, "kernel": f"{path_name}_gemm_kernel",
+                     "peak_basis": basis, "kernel": kernel_name,
                      "launch_ms": round(launch_ms, 5),
                      "compulsory_bytes": w.compulsory_bytes,
                      "hbm_frac_of_measured": round(w.compulsory_bytes / (launch_ms * 1e-3) /

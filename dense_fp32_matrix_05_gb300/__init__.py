@@ -145,7 +145,7 @@ def sgemm_host(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, algo=0) -> int:
 
 
 _PLAN_KEYS = ["path", "tile_m", "tile_n", "splits", "units", "grid", "stages", "vec_a", "vec_b",
-              "ws_bytes", "tail_tiles"]
+              "ws_bytes", "tail_tiles", "wide"]
 
 
 def sgemm_plan_info(M, N, K, A=0, lda=None, B=0, ldb=None, C=0, ldc=None, algo=0, splits=0,

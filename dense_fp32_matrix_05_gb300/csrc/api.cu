@@ -89,6 +89,7 @@ struct Plan {
     int stages = 0;
     int vec_a = 0, vec_b = 0, vec_c = 0;
     size_t ws_bytes = 0;
+    bool wide = false;  // FFMA path: the wide-N kernel (A resident, B streamed)
 };
 
 int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
@@ -254,8 +255,33 @@ void plan_tf32x3(int M, int N, int K, int sms, int splits_req, int flags, bool r
     }
 }
 
+// The wide-N kernel takes short, shallow A (M <= 32, K <= 64) on the FFMA
+// path unless a split count is forced.  AUTO sends it the shapes where it
+// beats the tensor path's narrow tiles, measured at M = 32, N = 1.6 M:
+// K = 28 98 vs 189 us, K = 32 107 vs 137, K = 48 149 vs 151, K = 64 191 vs
+// 181; streaming B and C needs only part of the CUDA cores there.
+constexpr int kWideAutoMaxK = 48;
+bool use_wide(int M, int K, int splits_req) { return splits_req <= 1 && sg::ffma_wide_fits(M, K); }
+bool auto_wide(int M, int K, int splits_req) { return use_wide(M, K, splits_req) && K <= kWideAutoMaxK; }
+
 void plan_ffma(int M, int N, int K, int sms, int splits_req, Plan &p) {
     p.path = SGEMM_ALGO_FFMA;
+    if (use_wide(M, K, splits_req)) {
+        p.wide = true;
+        p.tile_m = 32;
+        p.tile_n = 512;
+        Schedule &s = p.sch;
+        s.m_tiles = 1;
+        s.n_tiles = sg::ffma_wide_blocks(N);
+        s.k_tiles = ceil_div(K, sg::kFfmaBK);
+        s.splits = 1;
+        s.units = s.n_tiles;
+        s.group_m = 1;
+        p.grid = std::min(s.units, 2 * sms);
+        p.stages = 3;
+        p.ws_bytes = 0;
+        return;
+    }
     if (M <= 32) { p.tile_m = 32; p.tile_n = 512; }
     else if (M <= 64) { p.tile_m = 64; p.tile_n = 256; }
     else { p.tile_m = 128; p.tile_n = 128; }
@@ -275,7 +301,8 @@ void plan_ffma(int M, int N, int K, int sms, int splits_req, Plan &p) {
 
 int make_plan(int M, int N, int K, const void *A, int lda, const void *B, int ldb, const void *C, int ldc,
               int algo, int splits, int flags, int sms, bool read_c, Plan &p) {
-    const int path = (algo == SGEMM_ALGO_AUTO) ? SGEMM_ALGO_TF32X3 : algo;
+    // AUTO: the tensor path, except for the shapes the wide-N FFMA kernel streams
+    const int path = (algo == SGEMM_ALGO_AUTO) ? (auto_wide(M, K, splits) ? SGEMM_ALGO_FFMA : SGEMM_ALGO_TF32X3) : algo;
     if (path == SGEMM_ALGO_TF32X3) plan_tf32x3(M, N, K, sms, splits, flags, read_c, p);
     else plan_ffma(M, N, K, sms, splits, p);
     p.vec_a = aligned16(A, lda);
@@ -402,6 +429,8 @@ int run(int M, int N, int K, float alpha, const float *A, int lda, const float *
     cudaError_t e;
     if (p.path == SGEMM_ALGO_TF32X3)
         e = sg::tf32x3_launch(p.tile_m, g, p.sch, ctl, p.vec_a, p.vec_b, p.vec_c, p.grid, stream);
+    else if (p.wide)
+        e = sg::ffma_wide_launch(g, p.vec_b, p.grid, stream);
     else
         e = sg::ffma_launch(p.tile_m, p.tile_n, g, p.sch, ctl, p.vec_a, p.vec_b, p.vec_c, stream);
     return from_cuda(e);
@@ -502,7 +531,7 @@ int sgemm_plan_info(int M, int N, int K, const void *A, int lda, const void *B, 
         if (rc != 0) return rc;
         sms = d->sms;
     }
-    int vals[11] = {0};
+    int vals[12] = {0};
     if (M > 0 && N > 0 && K > 0) {
         Plan p;
         int rc = make_plan(M, N, K, A, lda, B, ldb, C, ldc, algo, splits, flags, sms, beta != 0.f, p);
@@ -518,8 +547,9 @@ int sgemm_plan_info(int M, int N, int K, const void *A, int lda, const void *B, 
         vals[8] = p.vec_b;
         vals[9] = static_cast<int>(std::min<size_t>(p.ws_bytes, 0x7fffffff));
         vals[10] = p.sch.tail_tiles;
+        vals[11] = p.wide ? 1 : 0;
     }
-    for (int i = 0; i < ninfo && i < 11; ++i) info[i] = vals[i];
+    for (int i = 0; i < ninfo && i < 12; ++i) info[i] = vals[i];
     return 0;
 }
 

@@ -1,0 +1,187 @@
+// Wide-N SGEMM on the CUDA cores for short, shallow A (M <= 32, K <= 64),
+// the im2col shapes whose time is the stream of B and C through HBM.
+//
+// The tiled kernels re-stage a sliver of A for every C tile and pay a
+// pipeline fill per tile that K = 27 never amortises.  Here A stays resident
+// in shared memory for the whole launch, transposed and zero-padded to
+// 64 k x 32 rows, and persistent CTAs stream B through a cp.async ring in
+// slabs of 16 k rows x 512 columns (16-byte copies when B's rows are
+// 16-byte aligned, 4-byte copies otherwise; edges zero-filled by the copy).
+// Thread t owns columns 2t and 2t + 1 of the current 512-column block and all
+// 32 rows, held as packed row pairs: per k it reads 16 A row pairs (the same
+// address for the whole warp, a broadcast) and its two B values, and issues
+// 32 fma.rn.f32x2.  Each element is an in-order fp32 FMA chain over k, as
+// in the tiled FFMA kernel.  When a block's last slab is done, C is written
+// with 8-byte stores, 256 consecutive bytes per warp and row, then the next
+// block's slabs are already in flight.
+//
+// Work decomposition follows the 2-D thread tiles of "NVIDIA_SGEMM_PRACTICE"
+// (sections "kernel 4" and "kernel 5", here 32 x 2 per thread) and the
+// prefetching of its "kernel 7", reorganised around a resident A.
+#include <cstdint>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace sg {
+namespace wide {
+
+constexpr int kThreads = 256;
+constexpr int kCols = 2 * kThreads;  // C columns per block
+constexpr int kMaxM = 32;
+constexpr int kMaxK = 64;
+constexpr int kKc = 16;              // k rows per slab
+constexpr int kStages = 3;
+constexpr int kStageFloats = kKc * kCols;
+constexpr int kAFloats = kMaxK * kMaxM;  // A^T: row k holds A[0..31][k]
+constexpr int kSmemBytes = (kStages * kStageFloats + kAFloats) * 4;
+
+// Slab q of this CTA: k rows [kc * 16, +16) of column block cb.
+__device__ __forceinline__ void load_slab(const GemmArgs &g, bool vec_b, int cb, int kc, uint32_t dst, int tid) {
+    const int n0 = cb * kCols;
+    if (vec_b) {
+#pragma unroll
+        for (int i = 0; i < kKc * kCols / 4 / kThreads; ++i) {
+            const int c = tid + i * kThreads;
+            const int r = c / (kCols / 4), cc = c % (kCols / 4);
+            const int k = kc * kKc + r, n = n0 + cc * 4;
+            const float *src = g.B;
+            uint32_t bytes = 0;
+            if (k < g.K && n < g.N) {
+                src = g.B + static_cast<long long>(k) * g.ldb + n;
+                bytes = static_cast<uint32_t>(min(4, g.N - n) * 4);
+            }
+            cp_async16(dst + static_cast<uint32_t>((r * kCols + cc * 4) * 4), src, bytes);
+        }
+    } else {
+#pragma unroll 4
+        for (int i = 0; i < kKc * kCols / kThreads; ++i) {
+            const int c = tid + i * kThreads;
+            const int r = c / kCols, cc = c % kCols;
+            const int k = kc * kKc + r, n = n0 + cc;
+            const bool ok = k < g.K && n < g.N;
+            const float *src = ok ? g.B + static_cast<long long>(k) * g.ldb + n : g.B;
+            cp_async4(dst + static_cast<uint32_t>((r * kCols + cc) * 4), src, ok ? 4u : 0u);
+        }
+    }
+}
+
+// C[m][n], C[m][n + 1] for the rows m < M of this thread's two columns.
+__device__ __forceinline__ void store_block(const GemmArgs &g, int n, const uint64_t (&acc0)[16],
+                                            const uint64_t (&acc1)[16]) {
+    if (n >= g.N) return;
+    const bool pair = ((reinterpret_cast<uintptr_t>(g.C) & 7u) == 0) && ((g.ldc & 1) == 0) && n + 1 < g.N;
+    const bool read_c = g.beta != 0.f;
+#pragma unroll
+    for (int mp = 0; mp < kMaxM / 2; ++mp) {
+        float c0[2], c1[2];  // (row 2mp, row 2mp + 1) of column n and of column n + 1
+        pair_split(acc0[mp], c0[0], c0[1]);
+        pair_split(acc1[mp], c1[0], c1[1]);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int m = 2 * mp + h;
+            if (m >= g.M) break;
+            float *p = g.C + static_cast<long long>(m) * g.ldc + n;
+            float r0 = g.alpha * c0[h], r1 = g.alpha * c1[h];
+            if (pair) {
+                if (read_c) {
+                    const float2 o = *reinterpret_cast<const float2 *>(p);
+                    r0 = fmaf(g.beta, o.x, r0);
+                    r1 = fmaf(g.beta, o.y, r1);
+                }
+                *reinterpret_cast<float2 *>(p) = make_float2(r0, r1);
+            } else {
+                p[0] = read_c ? fmaf(g.beta, p[0], r0) : r0;
+                if (n + 1 < g.N) p[1] = read_c ? fmaf(g.beta, p[1], r1) : r1;
+            }
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 2) ffma_wide_kernel(const __grid_constant__ GemmArgs g, int vec_b) {
+    extern __shared__ __align__(16) float smem_w[];
+    const int tid = threadIdx.x;
+    const uint32_t s0 = smem_u32(smem_w);
+    const uint32_t sA = s0 + static_cast<uint32_t>(kStages * kStageFloats * 4);
+    float *a_t = smem_w + kStages * kStageFloats;
+
+    const int KC = (g.K + kKc - 1) / kKc;
+    const int nblk = (g.N + kCols - 1) / kCols;
+    const int mine = nblk > static_cast<int>(blockIdx.x)
+                         ? (nblk - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
+                               static_cast<int>(gridDim.x)
+                         : 0;
+    const int jobs = mine * KC;  // slabs of this CTA, block-major
+    auto issue = [&](int q) {
+        if (q < jobs)
+            load_slab(g, vec_b != 0, static_cast<int>(blockIdx.x) + (q / KC) * static_cast<int>(gridDim.x), q % KC,
+                      s0 + static_cast<uint32_t>((q % kStages) * kStageFloats * 4), tid);
+        cp_async_commit();
+    };
+#pragma unroll
+    for (int q = 0; q < kStages - 1; ++q) issue(q);
+
+    // A^T, zero outside M x K (its loads overlap the first slab copies)
+    for (int i = tid; i < kAFloats; i += kThreads) {
+        const int k = i / kMaxM, m = i % kMaxM;
+        a_t[i] = (m < g.M && k < g.K) ? g.A[static_cast<long long>(m) * g.lda + k] : 0.f;
+    }
+
+    uint64_t acc0[kMaxM / 2], acc1[kMaxM / 2];  // row pairs of columns 2t and 2t + 1
+#pragma unroll
+    for (int mp = 0; mp < kMaxM / 2; ++mp) acc0[mp] = acc1[mp] = 0ull;
+
+    int q = 0;
+#pragma unroll 1
+    for (int bi = 0; bi < mine; ++bi) {
+#pragma unroll 1
+        for (int kc = 0; kc < KC; ++kc, ++q) {
+            cp_async_wait<kStages - 2>();
+            __syncthreads();  // slab q landed for all threads; slab q - 1's stage is free (and A^T is staged)
+            issue(q + kStages - 1);
+            const uint32_t st = s0 + static_cast<uint32_t>((q % kStages) * kStageFloats * 4);
+            const int kn = min(kKc, g.K - kc * kKc);  // rows of this slab inside K
+#pragma unroll 2
+            for (int kk = 0; kk < kn; ++kk) {
+                float bx, by;
+                lds2f(st + static_cast<uint32_t>((kk * kCols + 2 * tid) * 4), bx, by);
+                const uint32_t arow = sA + static_cast<uint32_t>((kc * kKc + kk) * kMaxM * 4);
+                const uint64_t b0 = pair_bcast(bx), b1 = pair_bcast(by);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {  // rows 16h .. 16h + 15: 8 A pairs live at a time
+                    uint64_t a[kMaxM / 4];
+#pragma unroll
+                    for (int p = 0; p < kMaxM / 8; ++p) lds_pairs(arow + h * 64 + p * 16, a[2 * p], a[2 * p + 1]);
+#pragma unroll
+                    for (int i = 0; i < kMaxM / 4; ++i) {
+                        ffma2(acc0[h * 8 + i], a[i], b0);
+                        ffma2(acc1[h * 8 + i], a[i], b1);
+                    }
+                }
+            }
+        }
+        const int cb = static_cast<int>(blockIdx.x) + bi * static_cast<int>(gridDim.x);
+        store_block(g, cb * kCols + 2 * tid, acc0, acc1);
+#pragma unroll
+        for (int mp = 0; mp < kMaxM / 2; ++mp) acc0[mp] = acc1[mp] = 0ull;
+    }
+    cp_async_wait<0>();
+}
+
+}  // namespace wide
+
+bool ffma_wide_fits(int M, int K) { return M >= 1 && M <= wide::kMaxM && K >= 1 && K <= wide::kMaxK; }
+
+int ffma_wide_blocks(int N) { return (N + wide::kCols - 1) / wide::kCols; }
+
+int ffma_wide_smem_bytes() { return wide::kSmemBytes; }
+
+cudaError_t ffma_wide_launch(const GemmArgs &g, int vec_b, int grid, cudaStream_t stream) {
+    cudaError_t e =
+        cudaFuncSetAttribute(wide::ffma_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, wide::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    wide::ffma_wide_kernel<<<grid, wide::kThreads, wide::kSmemBytes, stream>>>(g, vec_b);
+    return cudaGetLastError();
+}
+
+}  // namespace sg

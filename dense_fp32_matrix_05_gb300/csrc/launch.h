@@ -43,6 +43,13 @@ int check_tensor_call(int M, int N, int K, float alpha, const float *A, int lda,
 int plan_tensor_call(int M, int N, int K, const float *A, int lda, const float *B, int ldb, float beta,
                      const float *C, int ldc, int splits, int sms, size_t max_ws_floats, TensorPlan *out);
 
+// Wide-N FFMA kernel for M <= 32, K <= 64 (A resident, B streamed):
+// persistent CTAs over blocks of 512 columns.
+bool ffma_wide_fits(int M, int K);
+int ffma_wide_blocks(int N);
+int ffma_wide_smem_bytes();
+cudaError_t ffma_wide_launch(const GemmArgs &g, int vec_b, int grid, cudaStream_t stream);
+
 // C = beta * C (alpha == 0 or K == 0).
 cudaError_t scale_c_launch(float *C, long long ldc, int M, int N, float beta, int num_sms,
                            cudaStream_t stream);

@@ -108,6 +108,11 @@ __device__ __forceinline__ void pair_split(uint64_t p, float &x, float &y) {
     asm("mov.b64 {%0, %1}, %2;" : "=f"(x), "=f"(y) : "l"(p));
 }
 
+// Two consecutive floats from shared memory (8-byte aligned).
+__device__ __forceinline__ void lds2f(uint32_t addr, float &x, float &y) {
+    asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(x), "=f"(y) : "r"(addr));
+}
+
 // Two 64-bit pairs (four consecutive floats) from shared memory.
 __device__ __forceinline__ void lds_pairs(uint32_t addr, uint64_t &p0, uint64_t &p1) {
     asm volatile("ld.shared.v2.b64 {%0, %1}, [%2];" : "=l"(p0), "=l"(p1) : "r"(addr));

@@ -110,6 +110,11 @@ int sgemm(int M, int N, int K, float alpha,
  *                SGEMM_FLAG_DEBUG_WITHHOLD_ARRIVE (tests only).  Any other bit, or a tile height that is not
  *                supported, is rejected.
  *
+ * AUTO takes the 3xTF32 path, except for short, shallow A (M <= 32,
+ * K <= 48, no forced split count).  That goes to the FFMA path's wide-N
+ * kernel, which streams B and C at HBM speed in exact fp32.  An explicit
+ * SGEMM_ALGO_FFMA uses that kernel up to K = 64.
+ *
  * Scheduling (3xTF32 path): persistent CTAs, one per SM.  The planner
  * estimates the run time of each tile height, split count and last-wave
  * treatment from measured per-tile costs and takes the fastest.  With few
@@ -157,6 +162,8 @@ int sgemm_host(int M, int N, int K, float alpha,
  *   [8] 1 if B is read with 16-byte vector loads
  *   [9] workspace bytes needed
  *   [10] leftover tiles split along K after the whole waves (0 = none)
+ *   [11] 1 for the FFMA path's wide-N kernel (M <= 32, K <= 64: A resident
+ *        in shared memory, B streamed, persistent CTAs), else 0
  * Returns 0, or -i for an invalid argument (the i-th argument of this
  * function, 1-based).
  */

@@ -195,3 +195,19 @@ def test_tf32_mma_rate_rejects_bad_arguments(lib):
     assert f(256, 0, None, ctypes.byref(out)) == -2
     assert f(256, 100, None, None) == -4
 
+
+def test_plan_wide_kernel_for_short_shallow_a():
+    """M <= 32 and K <= 64 go to the FFMA path's wide-N kernel under AUTO."""
+    p = plan(32, 1605632, 27)
+    assert p["path"] == pkg.SGEMM_ALGO_FFMA and p["wide"] == 1
+    assert p["units"] == -(-1605632 // 512) and p["grid"] == min(p["units"], 2 * SMS)
+    assert plan(1, 7, 1)["wide"] == 1
+    assert plan(32, 4096, 48)["wide"] == 1
+    assert plan(32, 4096, 64)["path"] == pkg.SGEMM_ALGO_TF32X3      # AUTO: the tensor path wins at K = 64
+    assert plan(32, 4096, 64, algo=pkg.SGEMM_ALGO_FFMA)["wide"] == 1
+    assert plan(32, 4096, 65, algo=pkg.SGEMM_ALGO_FFMA)["wide"] == 0
+    assert plan(33, 4096, 27)["path"] == pkg.SGEMM_ALGO_TF32X3      # more than 32 rows
+    assert plan(32, 4096, 27, algo=pkg.SGEMM_ALGO_TF32X3)["wide"] == 0
+    forced = plan(32, 4096, 64, algo=pkg.SGEMM_ALGO_FFMA, splits=2)
+    assert forced["wide"] == 0 and forced["splits"] == 2             # a forced split keeps the tiled kernel
+

@@ -360,3 +360,26 @@ def test_tf32_mma_rate_is_plausible():
     gemm = 2.0 * M * N * K * 5 / (time.perf_counter() - t0) / 1e12
     assert gemm < rate / 3.0 * 1.1, (gemm, rate)
 
+
+WIDE_SHAPES = [(1, 1, 1), (3, 513, 1), (32, 1537, 27), (17, 5000, 64), (32, 70001, 16), (7, 130, 33)]
+
+
+@pytest.mark.parametrize("layout", ["packed", "odd_ld", "misaligned_ptrs"])
+@pytest.mark.parametrize("shape", WIDE_SHAPES, ids=[f"{m}x{n}x{k}" for m, n, k in WIDE_SHAPES])
+def test_wide_kernel(shape, layout):
+    """The FFMA path's wide-N kernel (M <= 32, K <= 64): every element against
+    the oracle, with 16-byte and 4-byte B copies, pair and single C stores,
+    and beta 0 over a NaN-filled C as well as beta != 0."""
+    M, N, K = shape
+    L = LAYOUTS[layout]
+    info = pkg.sgemm_plan_info(M, N, K, algo=pkg.SGEMM_ALGO_FFMA, num_sms=0)
+    assert info["wide"] == 1
+    for beta in (0.0, -0.5):
+        p = _with_c(random_problem(M, N, K, alpha=-1.5, beta=beta, seed=M * N + K,
+                                   lda=K + L["ld"][0], ldb=N + L["ld"][1], ldc=N + L["ld"][2]))
+        if beta == 0.0:
+            p.C[...] = np.nan
+        C, st = run_sgemm(p, pkg.SGEMM_ALGO_FFMA, offsets=L["off"])
+        assert st == 0
+        check_against_oracle(p, C, what=f"{shape} {layout} beta={beta}")
+
