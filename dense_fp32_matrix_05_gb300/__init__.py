@@ -22,7 +22,7 @@ __all__ = [
     "SGEMM_ERR_DEVICE_TIMEOUT",
     "SgemmError", "library", "lib_path", "declared_functions",
     "sgemm", "sgemm_ex", "sgemm_host", "sgemm_plan_info", "sgemm_check_status",
-    "sgemm_status_string", "sgemm_release", "sgemm_version", "sgemm_noalloc", "sgemm_tf32_mma_rate", "matmul",
+    "sgemm_status_string", "sgemm_release", "sgemm_version", "sgemm_noalloc", "sgemm_tf32_mma_rate", "sgemm_t", "sgemm_strided_batched", "matmul",
     "SGEMM_ERR_SCRATCH_LIMIT",
 ]
 
@@ -64,6 +64,9 @@ _SIGS = {
     "sgemm_release": (_i, []),
     "sgemm_version": (_i, []),
     "sgemm_tf32_mma_rate": (_i, [_i, _i, _p, ctypes.POINTER(ctypes.c_double)]),
+    "sgemm_t": (_i, [_i, _i, _i, _i, _i, _f, _p, _i, _p, _i, _f, _p, _i, _p, _i]),
+    "sgemm_strided_batched": (_i, [_i, _i, _i, _i, _i, _f, _p, _i, ctypes.c_longlong, _p, _i, ctypes.c_longlong,
+                                   _f, _p, _i, ctypes.c_longlong, _i, _p, _i]),
     "sgemm_noalloc": (_i, [_i, _i, _i, _f, _p, _i, _p, _i, _f, _p, _i, _p, _i]),
 }
 
@@ -131,6 +134,18 @@ def sgemm_ex(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None, algo=0, 
              flags=0) -> int:
     return library().sgemm_ex(M, N, K, alpha, _ptr(A), lda, _ptr(B), ldb, beta, _ptr(C), ldc,
                               _stream(stream), algo, splits, flags)
+
+
+def sgemm_t(transa, transb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None, algo=0) -> int:
+    return library().sgemm_t(int(transa), int(transb), M, N, K, alpha, _ptr(A), lda, _ptr(B), ldb, beta,
+                             _ptr(C), ldc, _stream(stream), algo)
+
+
+def sgemm_strided_batched(transa, transb, M, N, K, alpha, A, lda, strideA, B, ldb, strideB, beta, C, ldc,
+                          strideC, batch, stream=None, algo=0) -> int:
+    return library().sgemm_strided_batched(int(transa), int(transb), M, N, K, alpha, _ptr(A), lda, strideA,
+                                           _ptr(B), ldb, strideB, beta, _ptr(C), ldc, strideC, batch,
+                                           _stream(stream), algo)
 
 
 def sgemm_host(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, algo=0) -> int:

@@ -31,6 +31,8 @@ struct Workspace {
     size_t ws_bytes = 0;
     int *counters = nullptr;
     size_t n_counters = 0;
+    float *tr = nullptr;  // transposed operands of sgemm_t
+    size_t tr_bytes = 0;
 };
 
 struct HostBuffers {
@@ -394,6 +396,28 @@ int get_workspace(DevState &d, cudaStream_t stream, size_t bytes, size_t counter
     return 0;
 }
 
+// Room for transposed copies of the operands, grown like the split-K
+// workspace (after the stream's earlier work is done with the old buffer).
+int get_transpose_ws(DevState &d, cudaStream_t stream, size_t bytes, float **out) {
+    Workspace &w = d.ws[stream];
+    if (w.tr_bytes < bytes) {
+        if (w.tr) {
+            cudaError_t e = cudaStreamSynchronize(stream);
+            if (e != cudaSuccess) return from_cuda(e);
+            cudaFree(w.tr);
+            w.tr = nullptr;
+            w.tr_bytes = 0;
+        }
+        if (cudaMalloc(reinterpret_cast<void **>(&w.tr), bytes) != cudaSuccess) {
+            cudaGetLastError();
+            return SGEMM_ERR_WORKSPACE;
+        }
+        w.tr_bytes = bytes;
+    }
+    *out = w.tr;
+    return 0;
+}
+
 int run(int M, int N, int K, float alpha, const float *A, int lda, const float *B, int ldb, float beta,
         float *C, int ldc, cudaStream_t stream, int algo, int splits, int flags) {
     int rc = check_args(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, algo, splits, flags);
@@ -434,6 +458,88 @@ int run(int M, int N, int K, float alpha, const float *A, int lda, const float *
     else
         e = sg::ffma_launch(p.tile_m, p.tile_n, g, p.sch, ctl, p.vec_a, p.vec_b, p.vec_c, stream);
     return from_cuda(e);
+}
+
+// op(X) = X or X^T (BLAS transa / transb, row-major storage): with transa
+// A is stored K x M (lda >= M), with transb B is stored N x K (ldb >= K).
+// A transposed operand is first copied, transposed, into a workspace of this
+// stream; then the planned GEMM runs on the copies.  Returns 0 or -i, i the
+// position of the offending argument in sgemm_t.
+int check_t(int transa, int transb, int M, int N, int K, float alpha, const float *A, int lda, const float *B,
+            int ldb, const float *C, int ldc, int algo) {
+    if (transa != 0 && transa != 1) return -1;
+    if (transb != 0 && transb != 1) return -2;
+    if (M < 0) return -3;
+    if (N < 0) return -4;
+    if (K < 0) return -5;
+    if (lda < std::max(1, transa ? M : K)) return -8;
+    if (ldb < std::max(1, transb ? K : N)) return -10;
+    if (ldc < std::max(1, N)) return -13;
+    if (algo != SGEMM_ALGO_AUTO && algo != SGEMM_ALGO_FFMA && algo != SGEMM_ALGO_TF32X3) return -15;
+    if (M == 0 || N == 0) return 0;
+    const bool use_ab = alpha != 0.f && K > 0;
+    if (use_ab && A == nullptr) return -7;
+    if (use_ab && B == nullptr) return -9;
+    if (C == nullptr) return -12;
+    const size_t c_bytes = span_bytes(M, N, ldc);
+    if (use_ab && (overlaps(C, c_bytes, A, transa ? span_bytes(K, M, lda) : span_bytes(M, K, lda)) ||
+                   overlaps(C, c_bytes, B, transb ? span_bytes(N, K, ldb) : span_bytes(K, N, ldb))))
+        return -12;
+    return 0;
+}
+
+int run_t(int transa, int transb, int M, int N, int K, float alpha, const float *A, int lda, const float *B,
+          int ldb, float beta, float *C, int ldc, cudaStream_t stream, int algo) {
+    int rc0 = check_t(transa, transb, M, N, K, alpha, A, lda, B, ldb, C, ldc, algo);
+    if (rc0 != 0 || M == 0 || N == 0) return rc0;
+    const bool use_ab = alpha != 0.f && K > 0;
+    if (!use_ab)  // C = beta * C; A and B are not read
+        return run(M, N, K, alpha, nullptr, std::max(1, K), nullptr, std::max(1, N), beta, C, ldc, stream, algo, 0, 0);
+    if (!transa && !transb) return run(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream, algo, 0, 0);
+    // A^T copy at offset 0, B^T copy after it on a 256-byte boundary
+    const size_t a_floats = transa ? static_cast<size_t>(M) * K : 0;
+    const size_t b_off = (a_floats + 63) / 64 * 64;
+    const size_t floats = b_off + (transb ? static_cast<size_t>(K) * N : 0);
+    float *ws = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        DevState *d = nullptr;
+        int rc = device_state(&d);
+        if (rc != 0) return rc;
+        rc = get_transpose_ws(*d, stream, floats * sizeof(float), &ws);
+        if (rc != 0) return rc;
+    }
+    cudaError_t e = cudaSuccess;
+    if (transa) e = sg::transpose_launch(A, lda, K, M, ws, K, stream);  // K x M -> M x K
+    if (e == cudaSuccess && transb) e = sg::transpose_launch(B, ldb, N, K, ws + b_off, N, stream);  // N x K -> K x N
+    if (e != cudaSuccess) return from_cuda(e);
+    return run(M, N, K, alpha, transa ? ws : A, transa ? K : lda, transb ? ws + b_off : B, transb ? N : ldb, beta,
+               C, ldc, stream, algo, 0, 0);
+}
+
+// Strided batch of run_t calls: matrix b of each operand starts stride * b
+// elements after the first.  A zero stride shares one operand across the
+// batch; the C matrices must not overlap.  Returns 0 or -i, i the position
+// in sgemm_strided_batched.
+int run_batched(int transa, int transb, int M, int N, int K, float alpha, const float *A, int lda, long long sA,
+                const float *B, int ldb, long long sB, float beta, float *C, int ldc, long long sC, int batch,
+                cudaStream_t stream, int algo) {
+    static const int kPos[16] = {0, 1, 2, 3, 4, 5, 6, 7, 8, 10, 11, 13, 14, 15, 18, 19};  // sgemm_t -> batched
+    const int rc0 = check_t(transa, transb, M, N, K, alpha, A, lda, B, ldb, C, ldc, algo);
+    if (rc0 < 0) return -kPos[-rc0];
+    if (sA < 0) return -9;
+    if (sB < 0) return -12;
+    if (batch < 0) return -17;
+    if (batch > 1 && M > 0 && N > 0 && (sC < 0 || static_cast<size_t>(sC) * sizeof(float) < span_bytes(M, N, ldc)))
+        return -16;
+    for (int b = 0; b < batch; ++b) {
+        const long long ob = b;
+        const int rc = run_t(transa, transb, M, N, K, alpha, A ? A + ob * sA : A, lda, B ? B + ob * sB : B, ldb,
+                             beta, C + ob * sC, ldc, stream, algo);
+        if (rc < 0) return -kPos[-rc];
+        if (rc > 0) return rc;
+    }
+    return 0;
 }
 
 }  // namespace
@@ -628,6 +734,7 @@ int sgemm_release(void) {
         for (auto &kv : d.ws) {
             cudaFree(kv.second.ws);
             cudaFree(kv.second.counters);
+            cudaFree(kv.second.tr);
         }
         d.ws.clear();
         cudaFree(d.host.A);
@@ -638,6 +745,19 @@ int sgemm_release(void) {
     }
     cudaSetDevice(cur);
     return rc;
+}
+
+int sgemm_t(int transa, int transb, int M, int N, int K, float alpha, const float *A, int lda, const float *B,
+            int ldb, float beta, float *C, int ldc, sgemm_stream_t stream, int algo) {
+    return run_t(transa, transb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, reinterpret_cast<cudaStream_t>(stream),
+                 algo);
+}
+
+int sgemm_strided_batched(int transa, int transb, int M, int N, int K, float alpha, const float *A, int lda,
+                          long long strideA, const float *B, int ldb, long long strideB, float beta, float *C,
+                          int ldc, long long strideC, int batch, sgemm_stream_t stream, int algo) {
+    return run_batched(transa, transb, M, N, K, alpha, A, lda, strideA, B, ldb, strideB, beta, C, ldc, strideC,
+                       batch, reinterpret_cast<cudaStream_t>(stream), algo);
 }
 
 int sgemm_version(void) { return kVersion; }

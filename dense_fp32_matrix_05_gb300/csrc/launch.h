@@ -50,6 +50,11 @@ int ffma_wide_blocks(int N);
 int ffma_wide_smem_bytes();
 cudaError_t ffma_wide_launch(const GemmArgs &g, int vec_b, int grid, cudaStream_t stream);
 
+// dst (cols x rows, leading dimension ldd) = transpose of src (rows x cols,
+// leading dimension lds); row-major fp32.
+cudaError_t transpose_launch(const float *src, long long lds, int rows, int cols, float *dst, long long ldd,
+                             cudaStream_t stream);
+
 // C = beta * C (alpha == 0 or K == 0).
 cudaError_t scale_c_launch(float *C, long long ldc, int M, int N, float beta, int num_sms,
                            cudaStream_t stream);

@@ -229,6 +229,53 @@ int sgemm_noalloc(int M, int N, int K, float alpha,
                   float beta, float *C, int ldc,
                   sgemm_stream_t stream, int splits);
 
+/*
+ * sgemm_t - C = alpha * op(A) * op(B) + beta * C, with op(X) = X or X^T
+ * (BLAS transa / transb in row-major storage).  The pages fix both operands
+ * row-major ("NVIDIA_SGEMM_PRACTICE", section "kernel 1"); this is the
+ * transposed-operand extension a BLAS caller expects.
+ *
+ *   transa (1): 0: A is M x K, lda >= K.  1: A is stored K x M (op(A) = A^T),
+ *               lda >= M.
+ *   transb (2): 0: B is K x N, ldb >= N.  1: B is stored N x K, ldb >= K.
+ *   M, N, K, alpha, A, lda, B, ldb, beta, C, ldc (3-13): as in sgemm, with
+ *               the storage above.  C is M x N row-major, ldc >= N.
+ *   stream (14), algo (15): as in sgemm_ex.
+ *
+ * A transposed operand is first copied, transposed, into a library-owned
+ * buffer of this stream (grown on demand like the split-K workspace,
+ * released by sgemm_release).  The planned GEMM then runs on the copy, so a
+ * transposed operand costs one extra read and write of it.  Calls on the
+ * same stream from several threads race on that buffer.  Returns 0, -i for
+ * the i-th argument, a positive cudaError_t, or SGEMM_ERR_WORKSPACE.
+ */
+int sgemm_t(int transa, int transb, int M, int N, int K, float alpha,
+            const float *A, int lda,
+            const float *B, int ldb,
+            float beta, float *C, int ldc,
+            sgemm_stream_t stream, int algo);
+
+/*
+ * sgemm_strided_batched - for b in [0, batch):
+ *   C_b = alpha * op(A_b) * op(B_b) + beta * C_b,
+ * where X_b = X + b * strideX elements (X in A, B, C), op as in sgemm_t.
+ * The pages' per-image im2col GEMMs are such a batch.
+ *
+ *   strideA (9), strideB (12): >= 0; 0 shares one matrix across the batch.
+ *   strideC (16): the C matrices must not overlap, so for batch > 1 at least
+ *                 (M - 1) * ldc + N.
+ *   batch (17): >= 0.
+ *   The other arguments are as in sgemm_t, renumbered.
+ *
+ * The batch runs as one planned GEMM per matrix, in order on `stream`.
+ * Returns 0, -i for the i-th argument, or the first failing call's status.
+ */
+int sgemm_strided_batched(int transa, int transb, int M, int N, int K, float alpha,
+                          const float *A, int lda, long long strideA,
+                          const float *B, int ldb, long long strideB,
+                          float beta, float *C, int ldc, long long strideC,
+                          int batch, sgemm_stream_t stream, int algo);
+
 /* sgemm_version - library version as 10000*major + 100*minor + patch. */
 int sgemm_version(void);
 

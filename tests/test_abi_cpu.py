@@ -211,3 +211,28 @@ def test_plan_wide_kernel_for_short_shallow_a():
     forced = plan(32, 4096, 64, algo=pkg.SGEMM_ALGO_FFMA, splits=2)
     assert forced["wide"] == 0 and forced["splits"] == 2             # a forced split keeps the tiled kernel
 
+
+def test_transposed_and_batched_argument_checks(lib):
+    """sgemm_t and sgemm_strided_batched reject bad arguments, numbered by
+    position, before touching a device."""
+    A, B, C = FAKE, FAKE + (1 << 20), FAKE + (2 << 20)
+    t = pkg.sgemm_t
+    assert t(2, 0, 4, 4, 4, 1.0, A, 4, B, 4, 0.0, C, 4) == -1
+    assert t(0, -1, 4, 4, 4, 1.0, A, 4, B, 4, 0.0, C, 4) == -2
+    assert t(0, 0, -1, 4, 4, 1.0, A, 4, B, 4, 0.0, C, 4) == -3
+    assert t(1, 0, 8, 4, 4, 1.0, A, 4, B, 4, 0.0, C, 4) == -8     # A stored K x M needs lda >= M
+    assert t(0, 1, 4, 4, 8, 1.0, A, 8, B, 4, 0.0, C, 4) == -10    # B stored N x K needs ldb >= K
+    assert t(0, 0, 4, 4, 4, 1.0, A, 4, B, 4, 0.0, C, 3) == -13
+    assert t(0, 0, 4, 4, 4, 1.0, A, 4, B, 4, 0.0, C, 4, None, 7) == -15
+    assert t(0, 0, 4, 4, 4, 1.0, None, 4, B, 4, 0.0, C, 4) == -7
+    assert t(1, 1, 0, 4, 4, 1.0, A, 1, B, 4, 0.0, C, 4) == 0      # M = 0: nothing to do
+    b = pkg.sgemm_strided_batched
+    base = (0, 0, 4, 4, 4, 1.0, A, 4)
+    assert b(*base, -1, B, 4, 0, 0.0, C, 4, 16, 2) == -9
+    assert b(*base, 0, B, 4, -1, 0.0, C, 4, 16, 2) == -12
+    assert b(*base, 0, B, 4, 0, 0.0, C, 4, 15, 2) == -16         # C matrices would overlap
+    assert b(*base, 0, B, 4, 0, 0.0, C, 4, 16, -1) == -17
+    assert b(*base, 0, B, 4, 0, 0.0, C, 3, 16, 2) == -15          # ldc, renumbered
+    assert b(0, 0, 4, 4, 4, 1.0, A, 4, 0, B, 4, 0, 0.0, C, 4, 16, 2, None, 9) == -19
+    assert b(*base, 0, B, 4, 0, 0.0, C, 4, 16, 0) == 0            # empty batch
+

@@ -383,3 +383,69 @@ def test_wide_kernel(shape, layout):
         assert st == 0
         check_against_oracle(p, C, what=f"{shape} {layout} beta={beta}")
 
+
+def _stored(X, trans, ld_pad):
+    """Row-major storage of X, or of X^T when trans, with ld_pad NaN columns."""
+    S = X.T if trans else X
+    rows, cols = S.shape
+    out = np.full((rows, cols + ld_pad), np.nan, np.float32)
+    out[:, :cols] = S
+    return out, cols + ld_pad
+
+
+TRANS_SHAPES = [(130, 260, 129), (257, 130, 160), (31, 500, 20), (64, 1000, 27)]
+
+
+@pytest.mark.parametrize("algo", [pkg.SGEMM_ALGO_AUTO, pkg.SGEMM_ALGO_FFMA, pkg.SGEMM_ALGO_TF32X3],
+                         ids=["auto", "ffma", "tf32x3"])
+@pytest.mark.parametrize("trans", [(0, 1), (1, 0), (1, 1), (0, 0)], ids=["NT", "TN", "TT", "NN"])
+@pytest.mark.parametrize("shape", TRANS_SHAPES, ids=[f"{m}x{n}x{k}" for m, n, k in TRANS_SHAPES])
+def test_transposed_operands(shape, trans, algo):
+    """sgemm_t: A stored K x M and/or B stored N x K (padded leading
+    dimensions full of NaN), every element against the oracle."""
+    import torch
+
+    M, N, K = shape
+    ta, tb = trans
+    p = _with_c(random_problem(M, N, K, alpha=0.75, beta=-1.25, seed=M + N + K + 2 * ta + tb))
+    As, lda = _stored(p.A[:, :K], ta, 3)
+    Bs, ldb = _stored(p.B[:, :N], tb, 5)
+    dA, dB = torch.from_numpy(As).cuda(), torch.from_numpy(Bs).cuda()
+    dC = torch.from_numpy(p.C.copy()).cuda()
+    st = torch.cuda.current_stream()
+    assert pkg.sgemm_t(ta, tb, M, N, K, p.alpha, dA, lda, dB, ldb, p.beta, dC, p.ldc, st, algo) == 0
+    assert pkg.sgemm_check_status(st) == 0
+    check_against_oracle(p, dC.cpu().numpy(), what=f"{shape} trans={trans} algo={algo}")
+
+
+@pytest.mark.parametrize("tb", [0, 1], ids=["B", "Bt"])
+def test_strided_batched(tb):
+    """A batch of 3 sharing one A (stride 0), with B and C strided past
+    padding; each matrix of the batch against the oracle."""
+    import torch
+
+    M, N, K, batch = 100, 130, 64, 3
+    ps = [_with_c(random_problem(M, N, K, alpha=1.5, beta=0.5, seed=40 + b), seed=70 + b) for b in range(batch)]
+    for p in ps[1:]:
+        p.A = ps[0].A
+    lda = ps[0].lda
+    stored = [_stored(p.B[:, :N], tb, 2) for p in ps]
+    ldb = stored[0][1]
+    sB = stored[0][0].size + 17
+    sC = ps[0].C.size + 9
+    hB = np.full(sB * batch, np.nan, np.float32)
+    hC = np.full(sC * batch, np.nan, np.float32)
+    for b in range(batch):
+        hB[b * sB:b * sB + stored[b][0].size] = stored[b][0].reshape(-1)
+        hC[b * sC:b * sC + ps[b].C.size] = ps[b].C.reshape(-1)
+    dA = torch.from_numpy(np.ascontiguousarray(ps[0].A)).cuda()
+    dB, dC = torch.from_numpy(hB).cuda(), torch.from_numpy(hC).cuda()
+    st = torch.cuda.current_stream()
+    rc = pkg.sgemm_strided_batched(0, tb, M, N, K, ps[0].alpha, dA, lda, 0, dB, ldb, sB, ps[0].beta, dC,
+                                   ps[0].ldc, sC, batch, st)
+    assert rc == 0 and pkg.sgemm_check_status(st) == 0
+    out = dC.cpu().numpy()
+    for b, p in enumerate(ps):
+        C = out[b * sC:b * sC + p.C.size].reshape(p.C.shape)
+        check_against_oracle(p, C, what=f"batch {b} tb={tb}")
+
