@@ -200,10 +200,22 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                                C.data_ptr(), p.ldc, algo=algo, num_sms=props.multi_processor_count)
     flops = 2.0 * p.M * p.N * p.K
 
+    ta, tb = (args.trans[0] == "T"), (args.trans[1] == "T")
+    if ta or tb:
+        # transposed storage: A as K x M, B as N x K (sgemm_t copies them back)
+        At = A[:, :p.K].t().contiguous() if ta else A
+        Bt = B[:, :p.N].t().contiguous() if tb else B
+        lda_t = p.M if ta else p.lda
+        ldb_t = p.K if tb else p.ldb
+
     def step():
-        rc = pkg.sgemm_ex(p.M, p.N, p.K, p.alpha, A, p.lda, B, p.ldb, p.beta, C, p.ldc, stream, algo, 0, 0)
+        if ta or tb:
+            rc = pkg.sgemm_t(int(ta), int(tb), p.M, p.N, p.K, p.alpha, At, lda_t, Bt, ldb_t, p.beta, C, p.ldc,
+                             stream, algo)
+        else:
+            rc = pkg.sgemm_ex(p.M, p.N, p.K, p.alpha, A, p.lda, B, p.ldb, p.beta, C, p.ldc, stream, algo, 0, 0)
         if rc != 0:
-            raise pkg.SgemmError("sgemm_ex", rc)
+            raise pkg.SgemmError("sgemm_t" if (ta or tb) else "sgemm_ex", rc)
 
     for _ in range(args.warmup):
         step()
@@ -330,6 +342,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
             "l2": f"no flush: inputs larger than L2 ({w.compulsory_bytes / 1e6:.0f} MB vs 129 MB)"
                   if w.compulsory_bytes > 130e6 else "L2-resident inputs (small workload)",
             "parallelism": f"replicas x{world}",
+            "trans": args.trans,
         },
         "roofline": {"bound": bound, "achieved": round(achieved, 3), "peak": round(peak, 3),
                      "unit": unit_r, "frac": round(achieved / peak, 4), "traffic": traffic,
@@ -341,7 +354,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         "e2e": {"value": round(world * flops * e2e_steps / e2e_s / 1e12, 3), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                 "api": "sgemm_host (pinned host buffers)"},
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * (1 + int(ta) + int(tb)),
         "clocks": clocks,
     }
     if cublas is not None:
@@ -426,6 +439,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="square5120")
     ap.add_argument("--algo", choices=["auto", "ffma", "tf32x3"], default="auto")
+    ap.add_argument("--trans", choices=["NN", "NT", "TN", "TT"], default="NN",
+                    help="op(A) op(B) storage through sgemm_t (timed with its transposes)")
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--cpu-baseline-s", type=float, default=10.0)
     ap.add_argument("--reference-budget-s", type=float, default=90.0)
