@@ -163,6 +163,24 @@ def tf32_mma_rate(pkg) -> float:
     return _MMA_RATE["v"]
 
 
+def max_over_ranks(local_ms: float, device=None) -> float:
+    """The job's time: the largest of the ranks' timed regions (every rank
+    calls this; device None means a single process).  The tensor lives on
+    `device`: the GPU under NCCL, the CPU under gloo."""
+    if device is None:
+        return local_ms
+    import torch
+    t = torch.tensor([local_ms], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, flops_per_step: float, steps: int, job_ms: float) -> float:
+    """Whole-job TFLOP/s: every rank runs `steps` GEMMs of `flops_per_step`
+    (replicas, weak scaling) within the job's time."""
+    return world * flops_per_step * steps / (job_ms * 1e-3) / 1e12
+
+
 def roofline_peak(path: int, peaks: dict, source: str, sms: int):
     """(bound, peak TFLOP/s, basis text) for a path."""
     import dense_fp32_matrix_05_gb300 as pkg
@@ -246,10 +264,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     st = pkg.sgemm_check_status(stream)
     if st != 0:
         raise pkg.SgemmError("timed region", st)
-    if dist:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, dev if dist else None)
     clocks = clk.summary()
 
     # ---------------------------------------------------------- e2e
@@ -317,7 +332,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     if plan.get("wide"):
         path_name = "ffma_wide"
     traffic = recorded_traffic(args.workload, path_name)
-    value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
+    value = job_throughput(world, flops, args.steps, total_ms)
 
     result = {
         "metric": METRIC,
