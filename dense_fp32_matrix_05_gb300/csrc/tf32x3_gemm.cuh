@@ -87,11 +87,20 @@ constexpr uint32_t kTmemCols = 512;
 constexpr int kRingColsPerStage = 2 * kBK;
 constexpr int kMaxStages = 12;
 __host__ __device__ constexpr int nacc_for(int tm) { return tm >= 192 ? 1 : 2; }
+// Short tiles (TM <= 64) pair the products: a tf32 MMA costs at least ~40 ns
+// whatever its N up to 128, and in a stage the lo half of the A tile follows
+// the hi half with the same row pitch, so [A_hi; A_lo] is one 2TM-row
+// operand.  Per 8-deep k slice: B^T_hi x [A_hi; A_lo] (N = 2TM) gives hi*hi
+// and hi*lo side by side, then B^T_lo x A_hi (N = TM) adds lo*hi to the first
+// half: two MMAs instead of three.  The accumulator is 2TM columns wide and
+// the epilogue adds its halves.
+__host__ __device__ constexpr bool paired_for(int tm) { return tm <= 64; }
+__host__ __device__ constexpr int acc_cols_for(int tm) { return (paired_for(tm) ? 2 : 1) * tm; }
 // every tensor-memory column the accumulators leave, up to kMaxStages (short
 // tiles stream long B panels and want many copies in flight)
 __host__ __device__ constexpr int stages_for(int tm) {
-    return (static_cast<int>(kTmemCols) - nacc_for(tm) * tm) / kRingColsPerStage < kMaxStages
-               ? (static_cast<int>(kTmemCols) - nacc_for(tm) * tm) / kRingColsPerStage
+    return (static_cast<int>(kTmemCols) - nacc_for(tm) * acc_cols_for(tm)) / kRingColsPerStage < kMaxStages
+               ? (static_cast<int>(kTmemCols) - nacc_for(tm) * acc_cols_for(tm)) / kRingColsPerStage
                : kMaxStages;
 }
 constexpr int kSmemLimit = 232448;  // dynamic shared memory one CTA may use on sm_103a
@@ -123,10 +132,14 @@ struct Cfg {
                                        ? stages_for(TM) : (kSmemLimit - 2048 - kEpiBufBytes) / kStageBytes;
     static constexpr int kOffEpi = kStages * kStageBytes;
     static_assert(kStageBytes % 1024 == 0, "stages must keep 1 KB alignment");
-    static constexpr int kRingCol = kNacc * TM;
+    static constexpr bool kPaired = paired_for(TM);
+    static constexpr int kAccCols = acc_cols_for(TM);  // one accumulator (two TM halves when paired)
+    static constexpr int kRingCol = kNacc * kAccCols;
     static_assert(kRingCol + kStages * kRingColsPerStage <= static_cast<int>(kTmemCols), "tensor memory");
     static constexpr int kChunk = 16;  // accumulator columns per tensor-memory load in the epilogue
     static constexpr uint32_t kIdesc = umma_idesc_tf32(kTileN, TM);
+    static constexpr uint32_t kIdescPair = umma_idesc_tf32(kTileN, 2 * TM);  // N = 2TM: [A_hi; A_lo]
+    static_assert(!kPaired || (kABytes % 512 == 0 && 2 * TM <= 256), "[A_hi; A_lo] as one swizzled operand");
     // barriers: full[S], empty[S], a_full[S], acc_full[2], acc_empty[2],
     // drain, c_full[kEpiBufs]; then words: tensor-memory address, abort
     // flag, (unused), count of deferred sums, and kMaxDefer entries (tile row,
@@ -349,16 +362,22 @@ __device__ __forceinline__ bool epi_all(bool v) {
     return r != 0;
 }
 
+// One 16-column chunk of an accumulator: 16 C rows of this thread's column.
+// A paired accumulator holds hi*hi + lo*hi in its first TM columns and hi*lo
+// in the next TM; the chunk is their sum.
 template <int TM>
-__device__ __forceinline__ void tmem_load_chunk(uint32_t taddr, float (&v)[Cfg<TM>::kChunk]) {
-    if constexpr (Cfg<TM>::kChunk == 32) {
-        uint32_t r[32];
-        tmem_ld32x32(taddr, r);
+__device__ __forceinline__ void acc_chunk(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    tmem_ld32x16_issue(taddr, r);
+    if constexpr (paired_for(TM)) {
+        uint32_t q[16];
+        tmem_ld32x16_issue(taddr + static_cast<uint32_t>(TM), q);
+        tmem_ld_wait16(r);
+        tmem_ld_wait16(q);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+        for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]) + __uint_as_float(q[j]);
     } else {
-        uint32_t r[16];
-        tmem_ld32x16(taddr, r);
+        tmem_ld_wait16(r);
 #pragma unroll
         for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
     }
@@ -579,7 +598,7 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
             const int n = c.nt * kTileN + nl;
             const int m0 = c.mt * TM;
             const uint32_t t0 = tmem_base + (static_cast<uint32_t>(warp * 32) << 16) +
-                                static_cast<uint32_t>(acc * TM);
+                                static_cast<uint32_t>(acc * C::kAccCols);
             if (c.nseg == 1 && tma_c) {
                 // Chunks of CH accumulator columns (C rows) staged in shared
                 // memory: C copied in by TMA (two chunks ahead), alpha/beta
@@ -606,17 +625,12 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
                         cpar ^= 1u << b;
                         inflight &= ~(1u << b);
                     }
-                    uint32_t r[CH];
-                    tmem_ld32x16_issue(t0 + ch * CH, r);
-                    tmem_ld_wait16(r);
                     const int mb = m0 + ch * CH;
                     float v[CH];
+                    acc_chunk<TM>(t0 + ch * CH, v);
                     bool nan = false;
 #pragma unroll
-                    for (int j = 0; j < CH; ++j) {
-                        v[j] = __uint_as_float(r[j]);
-                        nan |= v[j] != v[j];
-                    }
+                    for (int j = 0; j < CH; ++j) nan |= v[j] != v[j];
                     if (nan && n_ok) {
 #pragma unroll 1
                         for (int j = 0; j < CH; ++j)
@@ -669,16 +683,11 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
                         for (int j = 0; j < CH; ++j)
                             old[j] = (n_ok && mb + j < g.M) ? cp[j * g.ldc] : 0.f;
                     }
-                    uint32_t r[CH];
-                    tmem_ld32x16_issue(t0 + ch * CH, r);
-                    tmem_ld_wait16(r);
                     float v[CH];
+                    acc_chunk<TM>(t0 + ch * CH, v);
                     bool nan = false;
 #pragma unroll
-                    for (int j = 0; j < CH; ++j) {
-                        v[j] = __uint_as_float(r[j]);
-                        nan |= v[j] != v[j];
-                    }
+                    for (int j = 0; j < CH; ++j) nan |= v[j] != v[j];
                     if (nan && n_ok) {
                         // a non-finite input reached this chunk: exact dot products
 #pragma unroll 1
@@ -712,7 +721,7 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
 #pragma unroll 1
                 for (int ch = 0; ch < TM / CH; ++ch) {
                     float v[CH];
-                    tmem_load_chunk<TM>(t0 + ch * CH, v);
+                    acc_chunk<TM>(t0 + ch * CH, v);
 #pragma unroll
                     for (int j = 0; j < CH; ++j) __stcg(wt + (ch * CH + j) * kTileN + nl, v[j]);
                 }
@@ -874,7 +883,7 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
                 break;
             }
             tc_fence_after();
-            const uint32_t d = tmem_base + static_cast<uint32_t>(acc * TM);
+            const uint32_t d = tmem_base + static_cast<uint32_t>(acc * C::kAccCols);
             for (int kt = c.kb; kt < c.ke; ++kt) {
                 if (!mbar_wait_bounded(bars + 8u * s, ph, abort_flag, ctl, kStatusTimeoutMma)) {
                     ok = false;
@@ -888,10 +897,16 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
                     const uint32_t a_hi = ring + static_cast<uint32_t>(j * 8);
                     const uint32_t a_lo = a_hi + static_cast<uint32_t>(kBK);
                     const uint64_t b_hi = umma_desc_kmajor_sw64(st + C::kOffAHi + j * 32);
-                    const uint64_t b_lo = umma_desc_kmajor_sw64(st + C::kOffALo + j * 32);
-                    mma_tf32_ts(d, a_lo, b_hi, C::kIdesc, (kt != c.kb || j != 0) ? 1u : 0u);
-                    mma_tf32_ts(d, a_hi, b_lo, C::kIdesc, 1u);
-                    mma_tf32_ts(d, a_hi, b_hi, C::kIdesc, 1u);
+                    if constexpr (C::kPaired) {
+                        // b_hi spans A_hi then A_lo: 2TM rows at the same pitch
+                        mma_tf32_ts(d, a_hi, b_hi, C::kIdescPair, (kt != c.kb || j != 0) ? 1u : 0u);
+                        mma_tf32_ts(d, a_lo, b_hi, C::kIdesc, 1u);
+                    } else {
+                        const uint64_t b_lo = umma_desc_kmajor_sw64(st + C::kOffALo + j * 32);
+                        mma_tf32_ts(d, a_lo, b_hi, C::kIdesc, (kt != c.kb || j != 0) ? 1u : 0u);
+                        mma_tf32_ts(d, a_hi, b_lo, C::kIdesc, 1u);
+                        mma_tf32_ts(d, a_hi, b_hi, C::kIdesc, 1u);
+                    }
                 }
                 mma_commit(bars + 8u * (S + s));
                 if (++s == S) {
