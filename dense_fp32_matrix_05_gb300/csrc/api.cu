@@ -123,14 +123,14 @@ struct TileCost {
 };
 
 TileCost tile_cost(int tm) {
-    if (tm <= 64) return {0.356, 1.84, 0.0};
-    if (tm <= 128) return {0.367, 2.68, 1.57};
-    if (tm <= 192) return {0.394, 6.17, 0.0};
-    return {0.441, 9.28, 1.03};
+    if (tm <= 64) return {0.302, 1.69, 0.0};
+    if (tm <= 128) return {0.365, 2.43, 1.43};
+    if (tm <= 192) return {0.391, 6.03, 0.0};
+    return {0.431, 9.95, 0.44};
 }
 
-constexpr double kLaunchUs = 7.2;
-constexpr double kSumUsPer256Rows = 0.81;  // per partial tile (and C) of a shared tile
+constexpr double kLaunchUs = 7.8;
+constexpr double kSumUsPer256Rows = 0.93;  // per partial tile (and C) of a shared tile
 
 struct Tf32x3Choice {
     int tm = 0, splits = 1, tail_splits = 0;

@@ -135,7 +135,7 @@ def test_plan_forced_splits_bound_units_per_cta():
     """A CTA finishes at most 8 shared tiles, so many forced K slices get a
     grid larger than the SM count."""
     p = plan(4096, 4096, 4096, splits=16)
-    assert p["units"] == 16 * 32 * 16
+    assert p["splits"] == 16 and p["units"] == -(-4096 // p["tile_m"]) * 32 * 16
     assert p["grid"] == -(-p["units"] // 8) and p["grid"] > SMS
     q = plan(1024, 1024, 1024, splits=2)
     assert q["grid"] == min(q["units"], SMS)
