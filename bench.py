@@ -163,6 +163,46 @@ def tf32_mma_rate(pkg) -> float:
     return _MMA_RATE["v"]
 
 
+# launch-bound sizes: also timed as back-to-back launches replayed from a CUDA graph
+GRAPH_WORKLOADS = ("square256", "square1024", "ragged1023x1021x1025")
+
+
+def graph_rate(pkg, p, A, B, C, algo: int, flops: float, per_graph: int = 20, replays: int = 10) -> dict:
+    """TFLOP/s of `per_graph` GEMMs captured into one CUDA graph (after the
+    timed region has sized every library buffer), replayed `replays` times
+    between CUDA events."""
+    import torch
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    # one plain call on the capture stream sizes its buffers (no allocation may happen while capturing)
+    rc = pkg.sgemm_ex(p.M, p.N, p.K, p.alpha, A, p.lda, B, p.ldb, p.beta, C, p.ldc, side, algo, 0, 0)
+    if rc != 0:
+        raise pkg.SgemmError("sgemm_ex (graph warm-up)", rc)
+    side.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        for _ in range(per_graph):
+            rc = pkg.sgemm_ex(p.M, p.N, p.K, p.alpha, A, p.lda, B, p.ldb, p.beta, C, p.ldc, side, algo, 0, 0)
+            if rc != 0:
+                raise pkg.SgemmError("sgemm_ex (graph capture)", rc)
+    graph.replay()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(replays):
+        graph.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / (replays * per_graph)
+    st = pkg.sgemm_check_status(side)
+    if st != 0:
+        raise pkg.SgemmError("graph replay", st)
+    return {"value": round(flops / (ms * 1e-3) / 1e12, 3), "unit": UNIT, "ms_per_gemm": round(ms, 5),
+            "gemms_per_graph": per_graph, "replays": replays}
+
+
 def max_over_ranks(local_ms: float, device=None) -> float:
     """The job's time: the largest of the ranks' timed regions (every rank
     calls this; device None means a single process).  The tensor lives on
@@ -374,6 +414,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     }
     if cublas is not None:
         result["context_cublas_sgemm_tflops"] = round(cublas, 3)
+    if w.name in GRAPH_WORKLOADS and not (ta or tb):
+        result["graph"] = graph_rate(pkg, p, A, B, C, algo, flops)
     if bound == "tensor":
         rate = tf32_mma_rate(pkg)
         if rate:

@@ -126,7 +126,9 @@ int sgemm(int M, int N, int K, float alpha,
  *
  * The split-K workspace is owned by the library, kept per device and stream,
  * grown on demand (a synchronous cudaMalloc, so make the first call of a
- * given size outside stream capture) and released by sgemm_release().
+ * given size outside stream capture) and released by sgemm_release().  After
+ * such a first call on a stream, calls on it can be captured into a CUDA
+ * graph: a call then only encodes tensor maps on the host and launches.
  */
 int sgemm_ex(int M, int N, int K, float alpha,
              const float *A, int lda,

@@ -449,3 +449,36 @@ def test_strided_batched(tb):
         C = out[b * sC:b * sC + p.C.size].reshape(p.C.shape)
         check_against_oracle(p, C, what=f"batch {b} tb={tb}")
 
+
+@pytest.mark.parametrize("shape,algo", [((1024, 1024, 1024), pkg.SGEMM_ALGO_AUTO),
+                                        ((300, 5000, 200), pkg.SGEMM_ALGO_TF32X3),
+                                        ((24, 3000, 27), pkg.SGEMM_ALGO_AUTO),
+                                        ((257, 130, 160), pkg.SGEMM_ALGO_FFMA)],
+                         ids=["1024-auto", "300x5000x200-tf32x3", "24x3000x27-wide", "257x130x160-ffma"])
+def test_cuda_graph_capture_and_replay(shape, algo):
+    """After one call has sized the library's buffers, calls can be captured
+    into a CUDA graph on a side stream and replayed (beta = 0, so replays are
+    idempotent); the result matches the oracle."""
+    import torch
+
+    M, N, K = shape
+    p = random_problem(M, N, K, alpha=1.25, beta=0.0, seed=M + K, pad_value=0.0)
+    A = torch.from_numpy(p.A).cuda()
+    B = torch.from_numpy(p.B).cuda()
+    C = torch.full(p.C.shape, float("nan"), device="cuda")
+    side = torch.cuda.Stream()
+    with torch.cuda.stream(side):
+        assert pkg.sgemm_ex(M, N, K, p.alpha, A, p.lda, B, p.ldb, p.beta, C, p.ldc, side, algo, 0, 0) == 0
+    side.synchronize()
+    C.fill_(float("nan"))
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        for _ in range(3):
+            rc = pkg.sgemm_ex(M, N, K, p.alpha, A, p.lda, B, p.ldb, p.beta, C, p.ldc, side, algo, 0, 0)
+            assert rc == 0
+    for _ in range(4):
+        graph.replay()
+    torch.cuda.synchronize()
+    assert pkg.sgemm_check_status(side) == 0
+    check_against_oracle(p, C.cpu().numpy(), what=f"graph {shape} algo={algo}")
+
