@@ -138,10 +138,11 @@ struct Tf32x3Choice {
 };
 
 // Split-K (or whole tiles when s == 1) with tile height tm.
-double model_split_k(int M, int N, int K, int tm, int s, int sms, bool read_c) {
+// A strided batch multiplies the tiles by its matrix count.
+double model_split_k(int M, int N, int K, int tm, int s, int sms, bool read_c, long long batch = 1) {
     const TileCost c = tile_cost(tm);
     const double unit = c.per_unit + (read_c ? c.per_unit_c : 0.0);
-    const long long tiles = static_cast<long long>(ceil_div(M, tm)) * ceil_div(N, sg::kTf32x3TileN);
+    const long long tiles = static_cast<long long>(ceil_div(M, tm)) * ceil_div(N, sg::kTf32x3TileN) * batch;
     const int kt = ceil_div(std::max(K, 1), sg::kTf32x3BK);
     s = std::max(1, std::min(s, kt));
     const long long units = tiles * s;
@@ -154,10 +155,10 @@ double model_split_k(int M, int N, int K, int tm, int s, int sms, bool read_c) {
 }
 
 // Whole waves of whole tiles, then the leftover tiles in ts K slices each.
-double model_split_tail(int M, int N, int K, int tm, int ts, int sms, bool read_c) {
+double model_split_tail(int M, int N, int K, int tm, int ts, int sms, bool read_c, long long batch = 1) {
     const TileCost c = tile_cost(tm);
     const double unit = c.per_unit + (read_c ? c.per_unit_c : 0.0);
-    const long long tiles = static_cast<long long>(ceil_div(M, tm)) * ceil_div(N, sg::kTf32x3TileN);
+    const long long tiles = static_cast<long long>(ceil_div(M, tm)) * ceil_div(N, sg::kTf32x3TileN) * batch;
     const int kt = ceil_div(std::max(K, 1), sg::kTf32x3BK);
     const long long waves = tiles / sms;
     return kLaunchUs + waves * (kt * c.per_k_tile + unit) + ceil_div(kt, ts) * c.per_k_tile + unit +
@@ -189,7 +190,8 @@ int tm_candidates(int M, int out[6]) {
     return n;
 }
 
-Tf32x3Choice choose_tf32x3(int M, int N, int K, int sms, int forced_tm, int splits_req, int flags, bool read_c) {
+Tf32x3Choice choose_tf32x3(int M, int N, int K, int sms, int forced_tm, int splits_req, int flags, bool read_c,
+                           long long batch = 1) {
     int tms[6];
     int ntm = forced_tm > 0 ? (tms[0] = forced_tm, 1) : tm_candidates(M, tms);
     const int kt = ceil_div(std::max(K, 1), sg::kTf32x3BK);
@@ -197,10 +199,10 @@ Tf32x3Choice choose_tf32x3(int M, int N, int K, int sms, int forced_tm, int spli
     best.us = best_tail.us = 1e300;
     for (int i = 0; i < ntm; ++i) {
         const int tm = tms[i];
-        const long long tiles = static_cast<long long>(ceil_div(M, tm)) * ceil_div(N, sg::kTf32x3TileN);
+        const long long tiles = static_cast<long long>(ceil_div(M, tm)) * ceil_div(N, sg::kTf32x3TileN) * batch;
         if (splits_req > 0) {
             const int s = std::max(1, std::min(splits_req, kt));
-            const double us = model_split_k(M, N, K, tm, s, sms, read_c);
+            const double us = model_split_k(M, N, K, tm, s, sms, read_c, batch);
             if (us < best.us) best = {tm, s, 0, us};
             continue;
         }
@@ -208,13 +210,13 @@ Tf32x3Choice choose_tf32x3(int M, int N, int K, int sms, int forced_tm, int spli
         // only while the slices still fit in one wave
         for (int s = 1; s <= 16; ++s) {
             if (s > 1 && (kt / s < 4 || tiles * s > sms)) break;
-            const double us = model_split_k(M, N, K, tm, s, sms, read_c);
+            const double us = model_split_k(M, N, K, tm, s, sms, read_c, batch);
             if (us < best.us) best = {tm, s, 0, us};
         }
         if (!(flags & SGEMM_FLAG_WHOLE_TILES)) {
             const int ts = tail_splits_for(tiles, kt, sms);
             if (ts > 0) {
-                const double us = model_split_tail(M, N, K, tm, ts, sms, read_c);
+                const double us = model_split_tail(M, N, K, tm, ts, sms, read_c, batch);
                 if (us < best.us) best = {tm, 1, ts, us};
                 if (us < best_tail.us) best_tail = {tm, 1, ts, us};
             }
@@ -225,9 +227,10 @@ Tf32x3Choice choose_tf32x3(int M, int N, int K, int sms, int forced_tm, int spli
     return best;
 }
 
-void plan_tf32x3(int M, int N, int K, int sms, int splits_req, int flags, bool read_c, Plan &p) {
+// batch > 1: one launch over the tiles of every matrix (Schedule::tpb).
+void plan_tf32x3(int M, int N, int K, int sms, int splits_req, int flags, bool read_c, Plan &p, int batch = 1) {
     p.path = SGEMM_ALGO_TF32X3;
-    const Tf32x3Choice ch = choose_tf32x3(M, N, K, sms, forced_tile_rows(flags), splits_req, flags, read_c);
+    const Tf32x3Choice ch = choose_tf32x3(M, N, K, sms, forced_tile_rows(flags), splits_req, flags, read_c, batch);
     const int tm = ch.tm;
     p.tile_m = tm;
     p.tile_n = sg::kTf32x3TileN;
@@ -235,7 +238,8 @@ void plan_tf32x3(int M, int N, int K, int sms, int splits_req, int flags, bool r
     s.m_tiles = ceil_div(M, tm);
     s.n_tiles = ceil_div(N, p.tile_n);
     s.k_tiles = ceil_div(K, sg::kTf32x3BK);
-    const int tiles = s.m_tiles * s.n_tiles;
+    s.tpb = batch > 1 ? s.m_tiles * s.n_tiles : 0;
+    const int tiles = s.m_tiles * s.n_tiles * batch;
     s.splits = ch.splits;
     s.units = tiles * s.splits;
     s.group_m = std::min(8, s.m_tiles);
@@ -301,15 +305,24 @@ void plan_ffma(int M, int N, int K, int sms, int splits_req, Plan &p) {
                      ? static_cast<size_t>(s.units) * p.tile_m * p.tile_n * sizeof(float) : 0;
 }
 
+// The path AUTO takes: the tensor path, except for the shapes the wide-N
+// FFMA kernel streams.
+int resolve_path(int M, int K, int algo, int splits) {
+    return (algo == SGEMM_ALGO_AUTO) ? (auto_wide(M, K, splits) ? SGEMM_ALGO_FFMA : SGEMM_ALGO_TF32X3) : algo;
+}
+
+// batch > 1 (3xTF32 path only): matrix b of each operand starts b * stride
+// elements after the first; 16-byte copies need 16-byte strides too.
 int make_plan(int M, int N, int K, const void *A, int lda, const void *B, int ldb, const void *C, int ldc,
-              int algo, int splits, int flags, int sms, bool read_c, Plan &p) {
-    // AUTO: the tensor path, except for the shapes the wide-N FFMA kernel streams
-    const int path = (algo == SGEMM_ALGO_AUTO) ? (auto_wide(M, K, splits) ? SGEMM_ALGO_FFMA : SGEMM_ALGO_TF32X3) : algo;
-    if (path == SGEMM_ALGO_TF32X3) plan_tf32x3(M, N, K, sms, splits, flags, read_c, p);
+              int algo, int splits, int flags, int sms, bool read_c, Plan &p, int batch = 1, long long sA = 0,
+              long long sB = 0, long long sC = 0) {
+    const int path = resolve_path(M, K, algo, splits);
+    if (batch > 1 && path != SGEMM_ALGO_TF32X3) return SGEMM_ERR_INTERNAL;
+    if (path == SGEMM_ALGO_TF32X3) plan_tf32x3(M, N, K, sms, splits, flags, read_c, p, batch);
     else plan_ffma(M, N, K, sms, splits, p);
-    p.vec_a = aligned16(A, lda);
-    p.vec_b = aligned16(B, ldb);
-    p.vec_c = aligned16(C, ldc);
+    p.vec_a = aligned16(A, lda) && sA % 4 == 0;
+    p.vec_b = aligned16(B, ldb) && sB % 4 == 0;
+    p.vec_c = aligned16(C, ldc) && sC % 4 == 0;
     if (p.sch.units <= 0 || p.grid <= 0) return SGEMM_ERR_INTERNAL;
     return 0;
 }
@@ -418,8 +431,11 @@ int get_transpose_ws(DevState &d, cudaStream_t stream, size_t bytes, float **out
     return 0;
 }
 
+// batch > 1: a strided batch in one launch of the 3xTF32 kernel (the caller
+// has checked the strides and that the path is the tensor path).
 int run(int M, int N, int K, float alpha, const float *A, int lda, const float *B, int ldb, float beta,
-        float *C, int ldc, cudaStream_t stream, int algo, int splits, int flags) {
+        float *C, int ldc, cudaStream_t stream, int algo, int splits, int flags, int batch = 1, long long sA = 0,
+        long long sB = 0, long long sC = 0) {
     int rc = check_args(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, algo, splits, flags);
     if (rc != 0) return rc;
     if (M == 0 || N == 0) return 0;
@@ -435,7 +451,8 @@ int run(int M, int N, int K, float alpha, const float *A, int lda, const float *
             if (beta == 1.f) return 0;
             return from_cuda(sg::scale_c_launch(C, ldc, M, N, beta, d->sms, stream));
         }
-        rc = make_plan(M, N, K, A, lda, B, ldb, C, ldc, algo, splits, flags, d->sms, beta != 0.f, p);
+        rc = make_plan(M, N, K, A, lda, B, ldb, C, ldc, algo, splits, flags, d->sms, beta != 0.f, p, batch, sA, sB,
+                       sC);
         if (rc != 0) return rc;
         ctl.status = d->status;
         ctl.wait_budget = (flags & SGEMM_FLAG_DEBUG_WITHHOLD_ARRIVE) ? kDebugWaitBudget : kWaitBudget;
@@ -443,16 +460,16 @@ int run(int M, int N, int K, float alpha, const float *A, int lda, const float *
         if (p.ws_bytes > 0) {  // split-K or split tail: tiles shared by several units
             Workspace *w = nullptr;
             rc = get_workspace(*d, stream, p.ws_bytes,
-                               static_cast<size_t>(p.sch.m_tiles) * p.sch.n_tiles, &w);
+                               static_cast<size_t>(p.sch.m_tiles) * p.sch.n_tiles * std::max(batch, 1), &w);
             if (rc != 0) return rc;
             ctl.ws = w->ws;
             ctl.counters = w->counters;
         }
     }
-    GemmArgs g{M, N, K, alpha, beta, A, lda, B, ldb, C, ldc};
+    GemmArgs g{M, N, K, alpha, beta, A, lda, B, ldb, C, ldc, sA, sB, sC};
     cudaError_t e;
     if (p.path == SGEMM_ALGO_TF32X3)
-        e = sg::tf32x3_launch(p.tile_m, g, p.sch, ctl, p.vec_a, p.vec_b, p.vec_c, p.grid, stream);
+        e = sg::tf32x3_launch(p.tile_m, g, p.sch, ctl, p.vec_a, p.vec_b, p.vec_c, p.grid, stream, batch);
     else if (p.wide)
         e = sg::ffma_wide_launch(g, p.vec_b, p.grid, stream);
     else
@@ -517,6 +534,49 @@ int run_t(int transa, int transb, int M, int N, int K, float alpha, const float 
                C, ldc, stream, algo, 0, 0);
 }
 
+// One launch for a whole strided batch on the 3xTF32 path: transposed
+// operands are first copied, transposed, matrix by matrix into this stream's
+// workspace.  Returns 1 where the batch has to run matrix by matrix: the FFMA
+// path, alpha = 0 or K = 0, more tiles than the schedule's 32-bit unit index
+// holds, or C's matrices overlapping A's or B's (each matrix is then checked
+// on its own); else 0 or -i as run_t.
+int run_batched_one_launch(int transa, int transb, int M, int N, int K, float alpha, const float *A, int lda,
+                           long long sA, const float *B, int ldb, long long sB, float beta, float *C, int ldc,
+                           long long sC, int batch, cudaStream_t stream, int algo) {
+    if (alpha == 0.f || K == 0 || resolve_path(M, K, algo, 0) != SGEMM_ALGO_TF32X3) return 1;
+    // units: at most 16 K slices of tiles 16 rows high
+    if (static_cast<long long>(ceil_div(M, 16)) * ceil_div(N, sg::kTf32x3TileN) * batch * 16 > INT32_MAX) return 1;
+    const long long nA = sA ? batch : 1, nB = sB ? batch : 1;
+    const size_t a_span = (nA - 1) * sA * sizeof(float) + (transa ? span_bytes(K, M, lda) : span_bytes(M, K, lda));
+    const size_t b_span = (nB - 1) * sB * sizeof(float) + (transb ? span_bytes(N, K, ldb) : span_bytes(K, N, ldb));
+    const size_t c_span = (batch - 1) * sC * sizeof(float) + span_bytes(M, N, ldc);
+    if (overlaps(C, c_span, A, a_span) || overlaps(C, c_span, B, b_span)) return 1;
+    if (!transa && !transb)
+        return run(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream, algo, 0, 0, batch, sA, sB, sC);
+    // transposed copies, each matrix on a 256-byte boundary: A^T (M x K) first, then B^T (K x N)
+    const long long a_str = transa ? (static_cast<long long>(M) * K + 63) / 64 * 64 : 0;
+    const long long b_str = transb ? (static_cast<long long>(K) * N + 63) / 64 * 64 : 0;
+    const long long b_off = a_str * (transa ? nA : 0);
+    float *ws = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        DevState *d = nullptr;
+        int rc = device_state(&d);
+        if (rc != 0) return rc;
+        rc = get_transpose_ws(*d, stream, static_cast<size_t>(b_off + b_str * (transb ? nB : 0)) * sizeof(float),
+                              &ws);
+        if (rc != 0) return rc;
+    }
+    cudaError_t e = cudaSuccess;
+    if (transa) e = sg::transpose_launch(A, lda, K, M, ws, K, stream, static_cast<int>(nA), sA, a_str);
+    if (e == cudaSuccess && transb)
+        e = sg::transpose_launch(B, ldb, N, K, ws + b_off, N, stream, static_cast<int>(nB), sB, b_str);
+    if (e != cudaSuccess) return from_cuda(e);
+    return run(M, N, K, alpha, transa ? ws : A, transa ? K : lda, transb ? ws + b_off : B, transb ? N : ldb, beta,
+               C, ldc, stream, algo, 0, 0, batch, transa ? (sA ? a_str : 0) : sA, transb ? (sB ? b_str : 0) : sB,
+               sC);
+}
+
 // Strided batch of run_t calls: matrix b of each operand starts stride * b
 // elements after the first.  A zero stride shares one operand across the
 // batch; the C matrices must not overlap.  Returns 0 or -i, i the position
@@ -532,6 +592,11 @@ int run_batched(int transa, int transb, int M, int N, int K, float alpha, const 
     if (batch < 0) return -17;
     if (batch > 1 && M > 0 && N > 0 && (sC < 0 || static_cast<size_t>(sC) * sizeof(float) < span_bytes(M, N, ldc)))
         return -16;
+    if (batch > 1 && M > 0 && N > 0) {
+        const int rc = run_batched_one_launch(transa, transb, M, N, K, alpha, A, lda, sA, B, ldb, sB, beta, C, ldc,
+                                              sC, batch, stream, algo);
+        if (rc <= 0) return rc < 0 ? -kPos[-rc] : 0;
+    }
     for (int b = 0; b < batch; ++b) {
         const long long ob = b;
         const int rc = run_t(transa, transb, M, N, K, alpha, A ? A + ob * sA : A, lda, B ? B + ob * sB : B, ldb,

@@ -22,7 +22,9 @@ enum : int {
 enum : int { kDebugWithholdArrive = 1 };
 
 // One GEMM call: C = alpha * A * B + beta * C, row-major, leading dimensions
-// in elements.  Offsets are formed in 64-bit arithmetic.
+// in elements.  Offsets are formed in 64-bit arithmetic.  A strided batch
+// (3xTF32 path) adds matrix b's offset b * sA, b * sB, b * sC (elements; a
+// zero stride shares one matrix).
 struct GemmArgs {
     int M, N, K;
     float alpha, beta;
@@ -32,6 +34,7 @@ struct GemmArgs {
     long long ldb;
     float *C;
     long long ldc;
+    long long sA = 0, sB = 0, sC = 0;
 };
 
 // Work decomposition.  A work unit is one (tile, K range) pair; a tile whose
@@ -53,6 +56,7 @@ struct Schedule {
     int dp_tiles;     // whole-wave tiles
     int tail_tiles;   // tiles after them, split along K (0 = split-K schedule)
     int tail_splits;  // K slices per tail tile
+    int tpb;          // tiles per matrix of a batch (0: one matrix); tile t is tile t % tpb of matrix t / tpb
 };
 
 struct DeviceCtl {
@@ -64,6 +68,7 @@ struct DeviceCtl {
 };
 
 struct UnitCoord {
+    int b;            // matrix of the batch
     int mt, nt, tile;
     int kb, ke;       // K tiles [kb, ke)
     int seg, nseg;    // this unit's index among the tile's units, and their count
@@ -71,9 +76,15 @@ struct UnitCoord {
 };
 
 __device__ __forceinline__ void tile_coords(const Schedule &s, int tile, UnitCoord &c) {
+    int t = tile;
+    c.b = 0;
+    if (s.tpb > 0) {
+        c.b = tile / s.tpb;
+        t = tile - c.b * s.tpb;
+    }
     const int per_group = s.group_m * s.n_tiles;
-    const int g = tile / per_group;
-    const int r = tile - g * per_group;
+    const int g = t / per_group;
+    const int r = t - g * per_group;
     const int rows_here = min(s.group_m, s.m_tiles - g * s.group_m);
     c.tile = tile;
     c.mt = g * s.group_m + r % rows_here;

@@ -16,8 +16,9 @@ constexpr int kFfmaBK = 16;        // K per FFMA pipeline stage
 bool tf32x3_supported_tm(int tm);
 int tf32x3_stages(int tm);
 int tf32x3_smem_bytes(int tm);
+// batch: matrices of a strided batch (g.sA / sB / sC; s.tpb tiles each).
 cudaError_t tf32x3_launch(int tm, const GemmArgs &g, const Schedule &s, const DeviceCtl &ctl,
-                          int vec_a, int vec_b, int vec_c, int grid, cudaStream_t stream);
+                          int vec_a, int vec_b, int vec_c, int grid, cudaStream_t stream, int batch = 1);
 
 // FFMA path.  (bm, bn) in {(128,128), (64,256), (32,512)}.
 bool ffma_supported_tile(int bm, int bn);
@@ -51,9 +52,11 @@ int ffma_wide_smem_bytes();
 cudaError_t ffma_wide_launch(const GemmArgs &g, int vec_b, int grid, cudaStream_t stream);
 
 // dst (cols x rows, leading dimension ldd) = transpose of src (rows x cols,
-// leading dimension lds); row-major fp32.
+// leading dimension lds); row-major fp32.  count matrices, src_stride /
+// dst_stride elements apart.
 cudaError_t transpose_launch(const float *src, long long lds, int rows, int cols, float *dst, long long ldd,
-                             cudaStream_t stream);
+                             cudaStream_t stream, int count = 1, long long src_stride = 0,
+                             long long dst_stride = 0);
 
 // C = beta * C (alpha == 0 or K == 0).
 cudaError_t scale_c_launch(float *C, long long ldc, int M, int N, float beta, int num_sms,

@@ -36,18 +36,35 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return g_encode;
 }
 
+// Third (batch) dimension of a tensor map: `batch` matrices `stride`
+// elements apart, or one matrix when the stride is 0 (an operand shared by
+// the batch, or no batch).  The stride must be a multiple of 16 bytes.
+bool batch_dim(long long stride, int batch, long long one_matrix_elems, cuuint64_t &dim, cuuint64_t &bytes) {
+    if (stride == 0 || batch <= 1) {
+        dim = 1;
+        bytes = (static_cast<cuuint64_t>(one_matrix_elems) * sizeof(float) + 15) & ~cuuint64_t(15);
+        return true;
+    }
+    if ((stride * sizeof(float)) % 16 != 0) return false;
+    dim = static_cast<cuuint64_t>(batch);
+    bytes = static_cast<cuuint64_t>(stride) * sizeof(float);
+    return true;
+}
+
 // Tensor map of A for the TMA path: a K x M fp32 tensor (K innermost) with
 // row stride lda * 4 bytes, copied in boxes of 16 (k) x tm (rows) with the
 // 64-byte swizzle, out-of-range elements filled with zeros.  Requires A and
 // lda * 4 to be multiples of 16 bytes.  Returns false when no map can be made.
-bool make_tmap_a(const GemmArgs &g, int tm, CUtensorMap *map) {
+bool make_tmap_a(const GemmArgs &g, int tm, int batch, CUtensorMap *map) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
     if (!enc) return false;
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(g.K), static_cast<cuuint64_t>(g.M)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(g.lda) * sizeof(float)};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(tf32x3::kBK), static_cast<cuuint32_t>(tm)};
-    const cuuint32_t estr[2] = {1, 1};
-    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(g.A), dims, strides,
+    cuuint64_t nb, sb;
+    if (!batch_dim(g.sA, batch, g.lda * g.M, nb, sb)) return false;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(g.K), static_cast<cuuint64_t>(g.M), nb};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(g.lda) * sizeof(float), sb};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(tf32x3::kBK), static_cast<cuuint32_t>(tm), 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(g.A), dims, strides,
                            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
@@ -56,14 +73,16 @@ bool make_tmap_a(const GemmArgs &g, int tm, CUtensorMap *map) {
 // Tensor map of B for the TMA path of narrow tiles: a N x K fp32 tensor (N
 // innermost) with row stride ldb * 4 bytes, copied in boxes of 128 (n) x 16
 // (k) without swizzle, out-of-range elements filled with zeros.
-bool make_tmap_b(const GemmArgs &g, CUtensorMap *map) {
+bool make_tmap_b(const GemmArgs &g, int batch, CUtensorMap *map) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
     if (!enc) return false;
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(g.N), static_cast<cuuint64_t>(g.K)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(g.ldb) * sizeof(float)};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(tf32x3::kTileN), static_cast<cuuint32_t>(tf32x3::kBK)};
-    const cuuint32_t estr[2] = {1, 1};
-    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(g.B), dims, strides,
+    cuuint64_t nb, sb;
+    if (!batch_dim(g.sB, batch, g.ldb * g.K, nb, sb)) return false;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(g.N), static_cast<cuuint64_t>(g.K), nb};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(g.ldb) * sizeof(float), sb};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(tf32x3::kTileN), static_cast<cuuint32_t>(tf32x3::kBK), 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(g.B), dims, strides,
                            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
@@ -73,14 +92,16 @@ bool make_tmap_b(const GemmArgs &g, CUtensorMap *map) {
 // with row stride ldc * 4 bytes, copied in and out in boxes of 128 (n) x 16
 // (rows) without swizzle; loads fill out-of-range elements with zeros and
 // stores skip them.
-bool make_tmap_c(const GemmArgs &g, CUtensorMap *map) {
+bool make_tmap_c(const GemmArgs &g, int batch, CUtensorMap *map) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
     if (!enc) return false;
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(g.N), static_cast<cuuint64_t>(g.M)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(g.ldc) * sizeof(float)};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(tf32x3::kTileN), static_cast<cuuint32_t>(tf32x3::kEpiRows)};
-    const cuuint32_t estr[2] = {1, 1};
-    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, g.C, dims, strides, box, estr,
+    cuuint64_t nb, sb;
+    if (!batch_dim(g.sC, batch, g.ldc * g.M, nb, sb)) return false;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(g.N), static_cast<cuuint64_t>(g.M), nb};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(g.ldc) * sizeof(float), sb};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(tf32x3::kTileN), static_cast<cuuint32_t>(tf32x3::kEpiRows), 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, g.C, dims, strides, box, estr,
                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
@@ -105,14 +126,14 @@ cudaError_t launch_tm(const GemmArgs &g, const Schedule &s, const DeviceCtl &ctl
 // the register spills and load stalls it removes).
 template <int TM>
 cudaError_t launch_rows(const GemmArgs &g, const Schedule &s, const DeviceCtl &ctl, int vec_a, int vec_b,
-                        int vec_c, int grid, cudaStream_t stream) {
+                        int vec_c, int grid, int batch, cudaStream_t stream) {
     CUtensorMap ma, mb, mc;
     std::memset(&ma, 0, sizeof(ma));
     std::memset(&mb, 0, sizeof(mb));
     std::memset(&mc, 0, sizeof(mc));
-    const bool ta = vec_a && make_tmap_a(g, TM, &ma);
-    const bool tb = vec_b && make_tmap_b(g, &mb);
-    const int tc = (vec_c && make_tmap_c(g, &mc)) ? 1 : 0;
+    const bool ta = vec_a && make_tmap_a(g, TM, batch, &ma);
+    const bool tb = vec_b && make_tmap_b(g, batch, &mb);
+    const int tc = (vec_c && make_tmap_c(g, batch, &mc)) ? 1 : 0;
     if (tb) {
         if (ta) return launch_tm<TM, true, true>(g, s, ctl, vec_a, tc, grid, ma, mb, mc, stream);
         return launch_tm<TM, false, true>(g, s, ctl, vec_a, tc, grid, ma, mb, mc, stream);
@@ -152,14 +173,14 @@ int tf32x3_smem_bytes(int tm) {
 }
 
 cudaError_t tf32x3_launch(int tm, const GemmArgs &g, const Schedule &s, const DeviceCtl &ctl, int vec_a,
-                          int vec_b, int vec_c, int grid, cudaStream_t stream) {
+                          int vec_b, int vec_c, int grid, cudaStream_t stream, int batch) {
     switch (tm) {
-        case 16: return launch_rows<16>(g, s, ctl, vec_a, vec_b, vec_c, grid, stream);
-        case 32: return launch_rows<32>(g, s, ctl, vec_a, vec_b, vec_c, grid, stream);
-        case 64: return launch_rows<64>(g, s, ctl, vec_a, vec_b, vec_c, grid, stream);
-        case 128: return launch_rows<128>(g, s, ctl, vec_a, vec_b, vec_c, grid, stream);
-        case 192: return launch_rows<192>(g, s, ctl, vec_a, vec_b, vec_c, grid, stream);
-        case 256: return launch_rows<256>(g, s, ctl, vec_a, vec_b, vec_c, grid, stream);
+        case 16: return launch_rows<16>(g, s, ctl, vec_a, vec_b, vec_c, grid, batch, stream);
+        case 32: return launch_rows<32>(g, s, ctl, vec_a, vec_b, vec_c, grid, batch, stream);
+        case 64: return launch_rows<64>(g, s, ctl, vec_a, vec_b, vec_c, grid, batch, stream);
+        case 128: return launch_rows<128>(g, s, ctl, vec_a, vec_b, vec_c, grid, batch, stream);
+        case 192: return launch_rows<192>(g, s, ctl, vec_a, vec_b, vec_c, grid, batch, stream);
+        case 256: return launch_rows<256>(g, s, ctl, vec_a, vec_b, vec_c, grid, batch, stream);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -144,7 +144,7 @@ struct Cfg {
     // drain, c_full[kEpiBufs]; then words: tensor-memory address, abort
     // flag, (unused), count of deferred sums, and kMaxDefer entries (tile row,
     // tile column, segment count, first workspace slot)
-    static constexpr int kBarBytes = 8 * (3 * kStages + 5 + kEpiBufs) + 4 * (4 + 4 * kMaxDefer);
+    static constexpr int kBarBytes = 8 * (3 * kStages + 5 + kEpiBufs) + 4 * (4 + 5 * kMaxDefer);
     static constexpr int kSmemBytes = 1024 + kOffEpi + kEpiBufBytes + kBarBytes;
     static_assert(kSmemBytes <= kSmemLimit, "shared memory per CTA");
     static_assert(kStages >= 4, "pipeline depth");
@@ -195,13 +195,13 @@ struct Raw<0, 0> {};
 // with h = gt >> 7 (its tensor-memory lane is its column), and A chunks
 // j = gt + GT * r: row j >> 2, k chunk j & 3 (GT threads per group).
 template <int TM, int BtK, int GT, int AJ>
-__device__ __forceinline__ void load_raw(const GemmArgs &g, bool vec_a, int m0, int n0, int k0,
+__device__ __forceinline__ void load_raw(const GemmArgs &g, bool vec_a, int bi, int m0, int n0, int k0,
                                          int ptid, Raw<BtK, AJ> &raw) {
     if constexpr (BtK > 0) {
         const int n = n0 + (ptid & (kTileN - 1));
         const int kb = k0 + (ptid >> 7) * BtK;
         const bool n_ok = n < g.N;
-        const float *src = g.B + static_cast<long long>(kb) * g.ldb + n;
+        const float *src = g.B + bi * g.sB + static_cast<long long>(kb) * g.ldb + n;
 #pragma unroll
         for (int e = 0; e < BtK; ++e)
             raw.b[e] = (n_ok && kb + e < g.K) ? __ldg(src + e * g.ldb) : 0.f;
@@ -215,7 +215,7 @@ __device__ __forceinline__ void load_raw(const GemmArgs &g, bool vec_a, int m0, 
                 const int m = m0 + (j >> 2);
                 const int k = k0 + (j & 3) * 4;
                 if (m < g.M) {
-                    const float *src = g.A + static_cast<long long>(m) * g.lda + k;
+                    const float *src = g.A + bi * g.sA + static_cast<long long>(m) * g.lda + k;
                     if (vec_a && k + 3 < g.K) {
                         v = __ldg(reinterpret_cast<const float4 *>(src));
                     } else {
@@ -307,9 +307,9 @@ __device__ __forceinline__ void store_split(uint32_t stage, uint32_t ring_taddr,
 // 3xTF32 split an infinite operand meeting a partner whose lo part is zero
 // gives Inf * 0 = NaN where fp32 arithmetic gives +-Inf, so NaN results are
 // recomputed on the CUDA cores.  Stops early once the sum itself is NaN.
-__device__ __noinline__ float recompute_dot(const GemmArgs &g, int m, int n) {
-    const float *a = g.A + static_cast<long long>(m) * g.lda;
-    const float *b = g.B + n;
+__device__ __noinline__ float recompute_dot(const GemmArgs &g, int bi, int m, int n) {
+    const float *a = g.A + bi * g.sA + static_cast<long long>(m) * g.lda;
+    const float *b = g.B + bi * g.sB + n;
     float s = 0.f;
     for (int k = 0; k < g.K; ++k) {
         s = fmaf(__ldg(a + k), __ldg(b + static_cast<long long>(k) * g.ldb), s);
@@ -325,11 +325,12 @@ __device__ __noinline__ float recompute_dot(const GemmArgs &g, int m, int n) {
 struct JobIter {
     int cta, i;
     bool tail, ok;
-    int mt, nt, kt, ke;
+    int b, mt, nt, kt, ke;
     __device__ __forceinline__ void load(const Schedule &s) {
         UnitCoord c;
         ok = next_unit(s, cta, i, tail, c);
         if (ok) {
+            b = c.b;
             mt = c.mt;
             nt = c.nt;
             kt = c.kb;
@@ -402,13 +403,14 @@ __device__ __forceinline__ float fix_lane(const float4 &v, int q) {
 }
 
 template <int TM>
-__device__ __forceinline__ void fixup_tile(const GemmArgs &g, const float *wb, int nseg, int m0, int n0,
+__device__ __forceinline__ void fixup_tile(const GemmArgs &g, int bi, const float *wb, int nseg, int m0, int n0,
                                         int wid, int nw, int lane) {
+    float *const cmat = g.C + bi * g.sC;  // matrix bi of a batch
     constexpr long long kTileElems = static_cast<long long>(kTileN) * TM;
     const int pass = kFixRows * nw;  // rows per pass
     const int nc = n0 + 4 * lane;    // first of this thread's 4 columns
     if (nc >= g.N) return;
-    const bool vec_c = (reinterpret_cast<uintptr_t>(g.C) & 15u) == 0 && (g.ldc & 3) == 0;
+    const bool vec_c = (reinterpret_cast<uintptr_t>(cmat) & 15u) == 0 && (g.ldc & 3) == 0;
     const bool full4 = vec_c && nc + 3 < g.N;
     const bool read_c = g.beta != 0.f;
     const int rows = min(TM, g.M - m0);
@@ -421,7 +423,7 @@ __device__ __forceinline__ void fixup_tile(const GemmArgs &g, const float *wb, i
             const int r = r0 + nw * j;
             old[j] = make_float4(0.f, 0.f, 0.f, 0.f);
             if (read_c && r < rows) {
-                const float *cp = g.C + static_cast<long long>(m0 + r) * g.ldc + nc;
+                const float *cp = cmat + static_cast<long long>(m0 + r) * g.ldc + nc;
                 if (full4) {
                     old[j] = *reinterpret_cast<const float4 *>(cp);
                 } else {
@@ -465,11 +467,11 @@ __device__ __forceinline__ void fixup_tile(const GemmArgs &g, const float *wb, i
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 float s = fix_lane(sum[j], q);
-                if (s != s && nc + q < g.N) s = recompute_dot(g, m, nc + q);
+                if (s != s && nc + q < g.N) s = recompute_dot(g, bi, m, nc + q);
                 const float a = g.alpha * s;
                 res[q] = read_c ? fmaf(g.beta, fix_lane(old[j], q), a) : a;
             }
-            float *cp = g.C + static_cast<long long>(m) * g.ldc + nc;
+            float *cp = cmat + static_cast<long long>(m) * g.ldc + nc;
             if (full4) {
                 *reinterpret_cast<float4 *>(cp) = make_float4(res[0], res[1], res[2], res[3]);
             } else {
@@ -485,12 +487,13 @@ __device__ __forceinline__ void fixup_tile(const GemmArgs &g, const float *wb, i
 // once the accumulator is ready; thread t of the epilogue takes rows t,
 // t + 128, ...  Only whole 16-byte pieces inside C are requested.
 template <int TM>
-__device__ __forceinline__ void prefetch_c_tile(const GemmArgs &g, int m0, int n0, int t) {
+__device__ __forceinline__ void prefetch_c_tile(const GemmArgs &g, int bi, int m0, int n0, int t) {
     const int cols = min(kTileN, g.N - n0);
-    const bool vec = (reinterpret_cast<uintptr_t>(g.C) & 15u) == 0 && (g.ldc & 3) == 0;
+    float *const cmat = g.C + bi * g.sC;
+    const bool vec = (reinterpret_cast<uintptr_t>(cmat) & 15u) == 0 && (g.ldc & 3) == 0;
 #pragma unroll 1
     for (int r = t; r < TM && m0 + r < g.M; r += kEpiWarps * 32) {
-        const float *row = g.C + static_cast<long long>(m0 + r) * g.ldc + n0;
+        const float *row = cmat + static_cast<long long>(m0 + r) * g.ldc + n0;
         if (vec) {
             const uint32_t bytes = static_cast<uint32_t>(cols * 4) & ~15u;
             if (bytes) prefetch_l2_bulk(row, bytes);
@@ -531,7 +534,7 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
                                                        8 * (3 * S + 5 + kEpiBufs));
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     volatile int *s_ndefer = reinterpret_cast<volatile int *>(tmem_slot + 3);
-    volatile int *s_defer = reinterpret_cast<volatile int *>(tmem_slot + 4);  // [kMaxDefer][mt, nt, nseg, slot0]
+    volatile int *s_defer = reinterpret_cast<volatile int *>(tmem_slot + 4);  // [kMaxDefer][mt, nt, nseg, slot0, b]
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -572,7 +575,7 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
             const UnitCoord &c = ui.c;
             const int acc = it % C::kNacc;
             const uint32_t aph = (it / C::kNacc) & 1;
-            if (c.nseg == 1 && g.beta != 0.f) prefetch_c_tile<TM>(g, c.mt * TM, c.nt * kTileN, threadIdx.x);
+            if (c.nseg == 1 && g.beta != 0.f) prefetch_c_tile<TM>(g, c.b, c.mt * TM, c.nt * kTileN, threadIdx.x);
             if (c.nseg == 1 && tma_c) {
                 // the previous tile's stores have read their buffers; copy the
                 // first C chunks of this tile while the accumulator is computed
@@ -584,8 +587,8 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
                     for (int ch = 0; ch < kEpiBufs - 1 && ch < nch; ++ch) {
                         if (threadIdx.x == 0) {
                             mbar_arrive_expect_tx(cfull0 + 8u * ch, kEpiChunkBytes);
-                            tma_load_2d(epi_buf0 + ch * kEpiChunkBytes, &tmap_c, c.nt * kTileN, c.mt * TM + ch * CH,
-                                        cfull0 + 8u * ch);
+                            tma_load_3d(epi_buf0 + ch * kEpiChunkBytes, &tmap_c, c.nt * kTileN, c.mt * TM + ch * CH,
+                                        c.b, cfull0 + 8u * ch);
                         }
                         inflight |= 1u << ch;
                     }
@@ -634,7 +637,7 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
                     if (nan && n_ok) {
 #pragma unroll 1
                         for (int j = 0; j < CH; ++j)
-                            if (v[j] != v[j] && mb + j < g.M) v[j] = recompute_dot(g, mb + j, n);
+                            if (v[j] != v[j] && mb + j < g.M) v[j] = recompute_dot(g, c.b, mb + j, n);
                     }
 #pragma unroll
                     for (int j = 0; j < CH; ++j) {
@@ -646,7 +649,7 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
                     if (threadIdx.x == 0) bulk_wait_group_read<kEpiBufs - 2>();
                     named_bar_sync(kEpiBarrierId, kEpiWarps * 32);
                     if (threadIdx.x == 0) {
-                        tma_store_2d(&tmap_c, epi_buf0 + b * kEpiChunkBytes, n0, mb);
+                        tma_store_3d(&tmap_c, epi_buf0 + b * kEpiChunkBytes, n0, mb, c.b);
                         bulk_commit_group();
                     }
                     if (read_c && ch + kEpiBufs - 1 < nch) {
@@ -655,8 +658,8 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
                         if (threadIdx.x == 0) {
                             bulk_wait_group_read<1>();
                             mbar_arrive_expect_tx(cfull0 + 8u * nb, kEpiChunkBytes);
-                            tma_load_2d(epi_buf0 + nb * kEpiChunkBytes, &tmap_c, n0, mb + (kEpiBufs - 1) * CH,
-                                        cfull0 + 8u * nb);
+                            tma_load_3d(epi_buf0 + nb * kEpiChunkBytes, &tmap_c, n0, mb + (kEpiBufs - 1) * CH,
+                                        c.b, cfull0 + 8u * nb);
                         }
                         inflight |= 1u << nb;
                     }
@@ -672,7 +675,7 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
                 static_assert(CH == 16, "the epilogue loads 16 columns at a time");
                 const bool read_c = g.beta != 0.f;
                 const bool n_ok = n < g.N;
-                float *cbase = g.C + static_cast<long long>(m0) * g.ldc + n;
+                float *cbase = g.C + c.b * g.sC + static_cast<long long>(m0) * g.ldc + n;
 #pragma unroll 1
                 for (int ch = 0; ch < TM / CH; ++ch) {
                     const int mb = m0 + ch * CH;
@@ -692,7 +695,7 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
                         // a non-finite input reached this chunk: exact dot products
 #pragma unroll 1
                         for (int j = 0; j < CH; ++j)
-                            if (v[j] != v[j] && mb + j < g.M) v[j] = recompute_dot(g, mb + j, n);
+                            if (v[j] != v[j] && mb + j < g.M) v[j] = recompute_dot(g, c.b, mb + j, n);
                     }
                     if (n_ok) {
                         if (read_c) {
@@ -737,10 +740,11 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
                         ctl.counters[c.tile] = 0;
                         const int nd = *s_ndefer;
                         if (nd < kMaxDefer) {
-                            s_defer[4 * nd + 0] = c.mt;
-                            s_defer[4 * nd + 1] = c.nt;
-                            s_defer[4 * nd + 2] = c.nseg;
-                            s_defer[4 * nd + 3] = static_cast<int>(c.slot0);
+                            s_defer[5 * nd + 0] = c.mt;
+                            s_defer[5 * nd + 1] = c.nt;
+                            s_defer[5 * nd + 2] = c.nseg;
+                            s_defer[5 * nd + 3] = static_cast<int>(c.slot0);
+                            s_defer[5 * nd + 4] = c.b;
                             *s_ndefer = nd + 1;
                         } else {
                             atomicOr(ctl.status, kStatusDeferOverflow);
@@ -783,7 +787,7 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
 #pragma unroll
         for (int i = 0; i < NB; ++i) {
             if (next.valid(sch)) {
-                load_raw<TM, BtK, GT, AJ>(g, vec_a != 0, next.mt * TM, next.nt * kTileN, next.kt * kBK, gt,
+                load_raw<TM, BtK, GT, AJ>(g, vec_a != 0, next.b, next.mt * TM, next.nt * kTileN, next.kt * kBK, gt,
                                           buf[i]);
                 for (int t = 0; t < G && next.valid(sch); ++t) next.advance(sch);
                 ++loaded;
@@ -824,7 +828,7 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
                         ph ^= 1u;
                     }
                     if (next.valid(sch)) {
-                        load_raw<TM, BtK, GT, AJ>(g, vec_a != 0, next.mt * TM, next.nt * kTileN, next.kt * kBK,
+                        load_raw<TM, BtK, GT, AJ>(g, vec_a != 0, next.b, next.mt * TM, next.nt * kTileN, next.kt * kBK,
                                                   gt, buf[i]);
                         for (int t = 0; t < G && next.valid(sch); ++t) next.advance(sch);
                         ++loaded;
@@ -848,10 +852,12 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
                     break;
                 mbar_arrive_expect_tx(afull0 + 8u * s, kTx);
                 if (TMA_A)
-                    tma_load_2d(base + s * C::kStageBytes + C::kOffAHi, &tmap_a, it.kt * kBK, it.mt * TM,
+                    tma_load_3d(base + s * C::kStageBytes + C::kOffAHi, &tmap_a, it.kt * kBK, it.mt * TM,
+                                g.sA != 0 ? it.b : 0,
                                 afull0 + 8u * s);
                 if (TMA_B)
-                    tma_load_2d(base + s * C::kStageBytes + C::kOffBRaw, &tmap_b, it.nt * kTileN, it.kt * kBK,
+                    tma_load_3d(base + s * C::kStageBytes + C::kOffBRaw, &tmap_b, it.nt * kTileN, it.kt * kBK,
+                                g.sB != 0 ? it.b : 0,
                                 afull0 + 8u * s);
                 used |= 1u << s;
                 last_ph = (last_ph & ~(1u << s)) | (ph << s);
@@ -935,8 +941,8 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
         __threadfence();
 #pragma unroll 1
         for (int e = 0; e < nd; ++e)
-            fixup_tile<TM>(g, ctl.ws + static_cast<long long>(s_defer[4 * e + 3]) * (kTileN * TM),
-                           s_defer[4 * e + 2], s_defer[4 * e] * TM, s_defer[4 * e + 1] * kTileN, warp,
+            fixup_tile<TM>(g, s_defer[5 * e + 4], ctl.ws + static_cast<long long>(s_defer[5 * e + 3]) * (kTileN * TM),
+                           s_defer[5 * e + 2], s_defer[5 * e] * TM, s_defer[5 * e + 1] * kTileN, warp,
                            R::kThreads / 32, lane);
     }
 }

@@ -269,7 +269,15 @@ int sgemm_t(int transa, int transb, int M, int N, int K, float alpha,
  *   batch (17): >= 0.
  *   The other arguments are as in sgemm_t, renumbered.
  *
- * The batch runs as one planned GEMM per matrix, in order on `stream`.
+ * On the 3xTF32 path (AUTO, except the wide-N FFMA shapes) the whole batch
+ * is one launch: the schedule's tiles run over every matrix, so a batch of
+ * small GEMMs fills the GPU.  Transposed operands are first copied,
+ * transposed, into this stream's buffer (as in sgemm_t), all matrices at
+ * once.  The batch runs instead as one planned GEMM per matrix, in order on
+ * `stream`, on the FFMA path, when alpha = 0 or K = 0, when the tile count
+ * exceeds 2^31 / 16, or when the C matrices overlap A's or B's memory.
+ * 16-byte strides (multiples of 4 elements) keep the tensor-map copies;
+ * other strides use element loads.
  * Returns 0, -i for the i-th argument, or the first failing call's status.
  */
 int sgemm_strided_batched(int transa, int transb, int M, int N, int K, float alpha,

@@ -450,6 +450,66 @@ def test_strided_batched(tb):
         check_against_oracle(p, C, what=f"batch {b} tb={tb}")
 
 
+# (M, N, K, batch, transa, transb, shared A, stride padding in floats, beta)
+BATCH_CASES = [
+    (200, 300, 96, 5, 0, 0, False, 0, 0.5),     # 16-byte strides: tensor-map copies of every matrix
+    (200, 300, 96, 5, 0, 0, False, 3, 0.5),     # odd strides: element loads
+    (256, 256, 2048, 2, 0, 0, False, 0, 0.0),   # few tiles, deep K: K slices of every matrix
+    (512, 512, 1024, 10, 0, 0, True, 0, 1.0),   # 160 tiles: whole waves, then a split tail
+    (130, 260, 129, 4, 1, 1, False, 1, 0.5),    # both operands transposed
+    (130, 260, 129, 4, 1, 0, True, 0, 0.5),     # one transposed A shared by the batch
+    (24, 3000, 27, 3, 0, 0, False, 0, 0.5),     # FFMA wide-N shape: matrix by matrix
+]
+
+
+@pytest.mark.parametrize("case", BATCH_CASES, ids=[f"{c[0]}x{c[1]}x{c[2]}b{c[3]}t{c[4]}{c[5]}"
+                                                   f"{'s' if c[6] else ''}p{c[7]}" for c in BATCH_CASES])
+def test_strided_batched_one_launch(case):
+    """Strided batches on the paths that run them in one launch; every
+    matrix against the oracle, with the gaps between the C matrices checked
+    untouched."""
+    import torch
+
+    M, N, K, batch, ta, tb, shared_a, pad, beta = case
+    aligned = pad % 4 == 0  # leading dimensions and strides in whole 16-byte words
+
+    def ld_pad(cols, odd):
+        return 4 - cols % 4 if aligned else odd
+
+    ps = [_with_c(random_problem(M, N, K, alpha=0.75, beta=beta, seed=300 + b,
+                                 ldc=N + ld_pad(N, 3)), seed=400 + b) for b in range(batch)]
+    if shared_a:
+        for p in ps[1:]:
+            p.A = ps[0].A
+    sa = [_stored(p.A[:, :K], ta, ld_pad(M if ta else K, 1)) for p in ps]
+    sb = [_stored(p.B[:, :N], tb, ld_pad(K if tb else N, 2)) for p in ps]
+    lda, ldb, ldc = sa[0][1], sb[0][1], ps[0].ldc
+    sA = 0 if shared_a else sa[0][0].size + pad
+    sB = sb[0][0].size + pad
+    sC = ps[0].C.size + pad + 4
+    nA = 1 if shared_a else batch
+    hA = np.full(max(sA, sa[0][0].size) * nA, np.nan, np.float32)
+    hB = np.full(sB * batch, np.nan, np.float32)
+    hC = np.full(sC * batch, np.float32(-7.5), np.float32)
+    for b in range(batch):
+        if b < nA:
+            hA[b * sA:b * sA + sa[b][0].size] = sa[b][0].reshape(-1)
+        hB[b * sB:b * sB + sb[b][0].size] = sb[b][0].reshape(-1)
+        hC[b * sC:b * sC + ps[b].C.size] = ps[b].C.reshape(-1)
+    dA, dB, dC = (torch.from_numpy(x).cuda() for x in (hA, hB, hC))
+    st = torch.cuda.current_stream()
+    rc = pkg.sgemm_strided_batched(ta, tb, M, N, K, ps[0].alpha, dA, lda, sA, dB, ldb, sB, beta, dC, ldc, sC,
+                                   batch, st)
+    assert rc == 0 and pkg.sgemm_check_status(st) == 0
+    out = dC.cpu().numpy()
+    rows = sample_rows(M, 96, seed=M) if M * N * batch > 1 << 20 else None
+    for b, p in enumerate(ps):
+        C = out[b * sC:b * sC + p.C.size].reshape(p.C.shape)
+        check_against_oracle(p, C, rows=rows, what=f"batch {b}")
+        gap = out[b * sC + p.C.size:(b + 1) * sC]
+        assert np.all(gap == np.float32(-7.5)), f"write between C matrices after batch {b}"
+
+
 @pytest.mark.parametrize("shape,algo", [((1024, 1024, 1024), pkg.SGEMM_ALGO_AUTO),
                                         ((300, 5000, 200), pkg.SGEMM_ALGO_TF32X3),
                                         ((24, 3000, 27), pkg.SGEMM_ALGO_AUTO),
