@@ -72,6 +72,11 @@ def _lib(plant: int = 0) -> ctypes.CDLL:
                           ctypes.c_double, ctypes.c_void_p, ctypes.c_longlong,
                           ctypes.c_void_p, ctypes.c_int,
                           ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+            g = lib.oracle_conv2d_nchw
+            g.restype = ctypes.c_int
+            g.argtypes = ([ctypes.c_int] * 13 + [ctypes.c_double, ctypes.c_void_p, ctypes.c_void_p,
+                                                 ctypes.c_double, ctypes.c_void_p,
+                                                 ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int])
             lib.oracle_max_threads.restype = ctypes.c_int
             _libs[plant] = lib
         return _libs[plant]
@@ -122,6 +127,52 @@ def sgemm_ref(M: int, N: int, K: int, alpha: float, A, lda: int, B, ldb: int,
         ref.ctypes.data, scale.ctypes.data, int(threads))
     if rc != 0:
         raise ValueError(f"oracle_sgemm_rows rejected argument {-rc}")
+    return ref, scale
+
+
+def conv2d_out_size(H: int, W: int, KH: int, KW: int, stride=(1, 1), pad=(0, 0), dil=(1, 1)):
+    """Output height and width of a 2-D convolution (floor division)."""
+    oh = (H + 2 * pad[0] - dil[0] * (KH - 1) - 1) // stride[0] + 1
+    ow = (W + 2 * pad[1] - dil[1] * (KW - 1) - 1) // stride[1] + 1
+    return oh, ow
+
+
+def conv2d_ref(alpha: float, X, Wt, beta: float = 0.0, Y=None, stride=(1, 1), pad=(0, 0),
+               dil=(1, 1), threads: int = 0, plant: int = 0):
+    """Direct 2-D convolution (no filter flip) of NCHW ``X`` with OIHW
+    ``Wt``: Y = alpha * conv(X, Wt) + beta * Y, zero padding.
+
+    The pages give only the GEMM shapes that this layer lowers to through
+    im2col (filters x (channels * KH * KW) times (channels * KH * KW) x
+    pixels); ``oracle_conv2d_nchw`` in the C file states the definition.
+    Returns (ref, scale), float64 arrays nb x F x OH x OW, with the same
+    per-element error scale as ``sgemm_ref``.
+    """
+    X = np.ascontiguousarray(X)
+    Wt = np.ascontiguousarray(Wt)
+    if X.dtype != np.float32 or Wt.dtype != np.float32:
+        raise TypeError("oracle inputs must be float32")
+    nb, C, H, W = X.shape
+    F, C2, KH, KW = Wt.shape
+    if C2 != C:
+        raise ValueError("filter channels differ from input channels")
+    OH, OW = conv2d_out_size(H, W, KH, KW, stride, pad, dil)
+    if OH < 1 or OW < 1:
+        raise ValueError("empty output")
+    if beta != 0.0:
+        Y = np.ascontiguousarray(Y)
+        if Y.dtype != np.float32 or Y.shape != (nb, F, OH, OW):
+            raise TypeError("Y must be float32 nb x F x OH x OW")
+    else:
+        Y = None
+    ref = np.empty((nb, F, OH, OW), dtype=np.float64)
+    scale = np.empty_like(ref)
+    rc = _lib(plant).oracle_conv2d_nchw(
+        nb, C, H, W, F, KH, KW, int(stride[0]), int(stride[1]), int(pad[0]), int(pad[1]),
+        int(dil[0]), int(dil[1]), float(alpha), X.ctypes.data, Wt.ctypes.data, float(beta),
+        _ptr(Y), ref.ctypes.data, scale.ctypes.data, int(threads))
+    if rc != 0:
+        raise ValueError(f"oracle_conv2d_nchw rejected argument {-rc}")
     return ref, scale
 
 

@@ -139,6 +139,122 @@ int oracle_sgemm_rows(int M, int N, int K, double alpha,
     return 0;
 }
 
+/* Direct 2-D convolution (the deep-learning "convolution", i.e. a
+ * cross-correlation: the filter is not flipped), the operation whose im2col
+ * lowering gives the skinny GEMM shapes of "UNIVERSAL_SGEMM_CUDA" (its shape
+ * list, e.g. M = 32 filters, K = 27 = 3 channels x 3 x 3, N = 32 images x
+ * 224 x 224 output pixels).  The pages give the GEMM shapes only; this is the
+ * plain definition of the layer they come from:
+ *
+ *   X: NCHW input, nb x C x H x W;  Wt: OIHW filter, F x C x KH x KW;
+ *   Y: NCHW output, nb x F x OH x OW with
+ *      OH = (H + 2 ph - dh (KH - 1) - 1) / sh + 1 (and likewise OW);
+ *   Y[b][f][oh][ow] = alpha * sum_{c, kh, kw} Wt[f][c][kh][kw] *
+ *                     X[b][c][oh sh + kh dh - ph][ow sw + kw dw - pw]
+ *                     + beta * Y[b][f][oh][ow],
+ *   input positions outside the image reading as zero.
+ *
+ * Each output element is summed in float64 over c, then kh, then kw (the
+ * order of the im2col row index k = (c KH + kh) KW + kw), with the same
+ * |product| sum as the GEMM oracle for the error scale.  beta == 0: Y is not
+ * read.  ref / scale: nb x F x OH x OW, float64.  OpenMP over (b, f).
+ *
+ * Returns 0, or a negative argument index (1-based) on invalid input.
+ */
+int oracle_conv2d_nchw(int nb, int C, int H, int W, int F, int KH, int KW,
+                       int sh, int sw, int ph, int pw, int dh, int dw,
+                       double alpha, const float *X, const float *Wt,
+                       double beta, const float *Y,
+                       double *ref, double *scale, int nthreads)
+{
+    if (nb < 0) return -1;
+    if (C < 0) return -2;
+    if (H < 0) return -3;
+    if (W < 0) return -4;
+    if (F < 0) return -5;
+    if (KH < 1) return -6;
+    if (KW < 1) return -7;
+    if (sh < 1) return -8;
+    if (sw < 1) return -9;
+    if (ph < 0) return -10;
+    if (pw < 0) return -11;
+    if (dh < 1) return -12;
+    if (dw < 1) return -13;
+    const long long OHn = (long long)H + 2LL * ph - (long long)dh * (KH - 1) - 1;
+    const long long OWn = (long long)W + 2LL * pw - (long long)dw * (KW - 1) - 1;
+    if (OHn < 0 || OWn < 0) return -3;
+    const int OH = (int)(OHn / sh + 1), OW = (int)(OWn / sw + 1);
+    if (nb == 0 || F == 0) return 0;
+    const int use_ab = (alpha != 0.0 && C > 0);
+    if (use_ab && X == NULL) return -15;
+    if (use_ab && Wt == NULL) return -16;
+    if (beta != 0.0 && Y == NULL) return -18;
+    if (ref == NULL) return -19;
+    if (scale == NULL) return -20;
+#ifdef _OPENMP
+    if (nthreads <= 0) nthreads = omp_get_max_threads();
+#else
+    (void)nthreads;
+#endif
+    const long long plane = (long long)OH * OW;
+
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads)
+#endif
+    for (long long bf = 0; bf < (long long)nb * F; ++bf) {
+        const long long b = bf / F, f = bf % F;
+        double *s = ref + bf * plane;
+        double *t = scale + bf * plane;
+        for (long long i = 0; i < plane; ++i) { s[i] = 0.0; t[i] = 0.0; }
+        if (use_ab) {
+            for (int c = 0; c < C; ++c) {
+                const float *xc = X + (b * C + c) * (long long)H * W;
+                for (int kh = 0; kh < KH; ++kh) {
+                    for (int kw = 0; kw < KW; ++kw) {
+#if ORACLE_PLANT == 5
+                        /* planted: filter flipped (true convolution) */
+                        const double w = (double)Wt[((f * C + c) * KH + (KH - 1 - kh)) * KW + (KW - 1 - kw)];
+#else
+                        const double w = (double)Wt[((f * C + c) * KH + kh) * KW + kw];
+#endif
+                        for (int oh = 0; oh < OH; ++oh) {
+#if ORACLE_PLANT == 6
+                            /* planted: padding applied on one side only */
+                            const long long ih = (long long)oh * sh + (long long)kh * dh;
+#elif ORACLE_PLANT == 7
+                            /* planted: dilation ignored */
+                            const long long ih = (long long)oh * sh + kh - ph;
+#else
+                            const long long ih = (long long)oh * sh + (long long)kh * dh - ph;
+#endif
+                            if (ih < 0 || ih >= H) continue;
+                            for (int ow = 0; ow < OW; ++ow) {
+#if ORACLE_PLANT == 7
+                                const long long iw = (long long)ow * sw + kw - pw;
+#else
+                                const long long iw = (long long)ow * sw + (long long)kw * dw - pw;
+#endif
+                                if (iw < 0 || iw >= W) continue;
+                                const double p = w * (double)xc[ih * W + iw];
+                                s[(long long)oh * OW + ow] += p;
+                                t[(long long)oh * OW + ow] += fabs(p);
+                            }
+                        }
+                    }
+                }
+            }
+        }
+        const float *yo = (beta != 0.0) ? Y + bf * plane : NULL;
+        for (long long i = 0; i < plane; ++i) {
+            const double ab = use_ab ? alpha * s[i] : 0.0;
+            const double bc = yo ? beta * (double)yo[i] : 0.0;
+            s[i] = ab + bc;
+            t[i] = fabs(alpha) * t[i] + fabs(bc);
+        }
+    }
+    return 0;
+}
+
 /* Number of threads OpenMP would use by default (for reporting). */
 int oracle_max_threads(void)
 {
