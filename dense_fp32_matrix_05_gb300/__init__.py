@@ -22,7 +22,7 @@ __all__ = [
     "SGEMM_ERR_DEVICE_TIMEOUT",
     "SgemmError", "library", "lib_path", "declared_functions",
     "sgemm", "sgemm_ex", "sgemm_host", "sgemm_plan_info", "sgemm_check_status",
-    "sgemm_status_string", "sgemm_release", "sgemm_version", "sgemm_noalloc", "sgemm_tf32_mma_rate", "sgemm_t", "sgemm_strided_batched", "matmul",
+    "sgemm_status_string", "sgemm_release", "sgemm_version", "sgemm_noalloc", "sgemm_tf32_mma_rate", "sgemm_t", "sgemm_strided_batched", "sgemm_conv2d", "conv2d_out_size", "matmul",
     "SGEMM_ERR_SCRATCH_LIMIT",
 ]
 
@@ -68,6 +68,7 @@ _SIGS = {
     "sgemm_strided_batched": (_i, [_i, _i, _i, _i, _i, _f, _p, _i, ctypes.c_longlong, _p, _i, ctypes.c_longlong,
                                    _f, _p, _i, ctypes.c_longlong, _i, _p, _i]),
     "sgemm_noalloc": (_i, [_i, _i, _i, _f, _p, _i, _p, _i, _f, _p, _i, _p, _i]),
+    "sgemm_conv2d": (_i, [_i] * 13 + [_f, _p, _p, _f, _p, _p, _i]),
 }
 
 
@@ -146,6 +147,25 @@ def sgemm_strided_batched(transa, transb, M, N, K, alpha, A, lda, strideA, B, ld
     return library().sgemm_strided_batched(int(transa), int(transb), M, N, K, alpha, _ptr(A), lda, strideA,
                                            _ptr(B), ldb, strideB, beta, _ptr(C), ldc, strideC, batch,
                                            _stream(stream), algo)
+
+
+def conv2d_out_size(H, W, KH, KW, stride=(1, 1), pad=(0, 0), dil=(1, 1)):
+    """Output height and width of sgemm_conv2d (floor division)."""
+    return ((H + 2 * pad[0] - dil[0] * (KH - 1) - 1) // stride[0] + 1,
+            (W + 2 * pad[1] - dil[1] * (KW - 1) - 1) // stride[1] + 1)
+
+
+def sgemm_conv2d(X, Wt, Y, alpha=1.0, beta=0.0, stride=(1, 1), pad=(0, 0), dil=(1, 1), stream=None,
+                 algo=0, shape=None) -> int:
+    """Y = alpha * conv2d(X, Wt) + beta * Y; X NCHW, Wt OIHW, Y NCHW, fp32 device tensors
+    (or addresses, with ``shape`` = (nb, C, H, W, F, KH, KW))."""
+    if shape is None:
+        nb, C, H, W = X.shape
+        F, _, KH, KW = Wt.shape
+    else:
+        nb, C, H, W, F, KH, KW = shape
+    return library().sgemm_conv2d(nb, C, H, W, F, KH, KW, stride[0], stride[1], pad[0], pad[1], dil[0], dil[1],
+                                  alpha, _ptr(X), _ptr(Wt), beta, _ptr(Y), _stream(stream), algo)
 
 
 def sgemm_host(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, algo=0) -> int:

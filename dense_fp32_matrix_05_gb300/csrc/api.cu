@@ -607,6 +607,114 @@ int run_batched(int transa, int transb, int M, int N, int K, float alpha, const 
     return 0;
 }
 
+// ------------------------------------------------------------ convolution
+
+// Y = alpha * conv2d(X, Wt) + beta * Y (NCHW input and output, OIHW filter)
+// as one implicit GEMM per image: M = F filters, K = C * KH * KW taps,
+// N = OH * OW output pixels, with the images as the kernel's strided batch.
+// The filter is the A operand; a filter whose rows are not 16-byte aligned
+// is first copied into rows padded to 4 floats (this stream's transpose
+// buffer) so that it keeps its tensor-map copies.  Returns 0, -i for the
+// i-th argument of sgemm_conv2d, or a positive error.
+int run_conv(int nb, int C, int H, int W, int F, int KH, int KW, int sh, int sw, int ph, int pw, int dh, int dw,
+             float alpha, const float *X, const float *Wt, float beta, float *Y, cudaStream_t stream, int algo) {
+    if (nb < 0) return -1;
+    if (C < 0) return -2;
+    if (H < 1) return -3;
+    if (W < 1) return -4;
+    if (F < 0) return -5;
+    if (KH < 1) return -6;
+    if (KW < 1) return -7;
+    if (sh < 1) return -8;
+    if (sw < 1) return -9;
+    if (ph < 0) return -10;
+    if (pw < 0) return -11;
+    if (dh < 1) return -12;
+    if (dw < 1) return -13;
+    if (algo != SGEMM_ALGO_AUTO && algo != SGEMM_ALGO_TF32X3) return -20;
+    const long long span_h = static_cast<long long>(H) + 2LL * ph, span_w = static_cast<long long>(W) + 2LL * pw;
+    const long long reach_h = static_cast<long long>(dh) * (KH - 1) + 1, reach_w = static_cast<long long>(dw) * (KW - 1) + 1;
+    if (span_h < reach_h) return -6;  // the filter is taller than the padded image
+    if (span_w < reach_w) return -7;
+    const long long OH = (span_h - reach_h) / sh + 1, OW = (span_w - reach_w) / sw + 1;
+    const long long Kl = static_cast<long long>(C) * KH * KW, Nl = OH * OW;
+    // 32-bit offsets inside one padded image (the gather) and 32-bit GEMM sizes
+    if ((static_cast<long long>(C) + 1) * (span_h + reach_h) * (span_w + reach_w) >= (1LL << 31) || Kl >= (1LL << 31))
+        return -2;
+    if (Nl >= (1LL << 31)) return -3;
+    if (nb == 0 || F == 0) return 0;
+    const bool use_ab = alpha != 0.f && C > 0;
+    if (use_ab && X == nullptr) return -15;
+    if (use_ab && Wt == nullptr) return -16;
+    if (Y == nullptr) return -18;
+    const int K = static_cast<int>(Kl), N = static_cast<int>(Nl);
+    const long long img_in = static_cast<long long>(C) * H * W, img_out = static_cast<long long>(F) * N;
+    const size_t y_bytes = static_cast<size_t>(nb) * img_out * sizeof(float);
+    if (use_ab && (overlaps(Y, y_bytes, X, static_cast<size_t>(nb) * img_in * sizeof(float)) ||
+                   overlaps(Y, y_bytes, Wt, static_cast<size_t>(F) * K * sizeof(float))))
+        return -18;
+
+    DevState *d = nullptr;
+    float *wpad = nullptr;
+    const int lda = (K + 3) / 4 * 4;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        int rc = device_state(&d);
+        if (rc != 0) return rc;
+        if (use_ab && !aligned16(Wt, K)) {
+            rc = get_transpose_ws(*d, stream, static_cast<size_t>(F) * lda * sizeof(float), &wpad);
+            if (rc != 0) return rc;
+        }
+    }
+    if (!use_ab) {  // Y = beta * Y, image by image (F x N each)
+        if (beta == 1.f) return 0;
+        for (int b = 0; b < nb; ++b) {
+            cudaError_t e = sg::scale_c_launch(Y + b * img_out, N, F, N, beta, d->sms, stream);
+            if (e != cudaSuccess) return from_cuda(e);
+        }
+        return 0;
+    }
+    if (wpad) {
+        cudaError_t e = cudaMemcpy2DAsync(wpad, static_cast<size_t>(lda) * sizeof(float), Wt,
+                                          static_cast<size_t>(K) * sizeof(float), static_cast<size_t>(K) * sizeof(float),
+                                          static_cast<size_t>(F), cudaMemcpyDeviceToDevice, stream);
+        if (e != cudaSuccess) return from_cuda(e);
+    }
+    const float *A = wpad ? wpad : Wt;
+    const int ldA = wpad ? lda : K;
+    // images per launch: the schedule's unit index is 32-bit (at most 16 K
+    // slices of tiles 16 rows high)
+    const long long per_img = static_cast<long long>(ceil_div(F, 16)) * ceil_div(N, sg::kTf32x3TileN) * 16;
+    const int chunk = static_cast<int>(std::max(1LL, std::min<long long>(nb, INT32_MAX / per_img)));
+    for (int b0 = 0; b0 < nb; b0 += chunk) {
+        const int nbc = std::min(chunk, nb - b0);
+        Plan p;
+        DeviceCtl ctl{};
+        {
+            std::lock_guard<std::mutex> lk(g_mu);
+            plan_tf32x3(F, N, K, d->sms, 0, 0, beta != 0.f, p, nbc);
+            if (p.sch.units <= 0 || p.grid <= 0) return SGEMM_ERR_INTERNAL;
+            ctl.status = d->status;
+            ctl.wait_budget = kWaitBudget;
+            if (p.ws_bytes > 0) {
+                Workspace *w = nullptr;
+                const int rc = get_workspace(*d, stream, p.ws_bytes,
+                                             static_cast<size_t>(p.sch.m_tiles) * p.sch.n_tiles * nbc, &w);
+                if (rc != 0) return rc;
+                ctl.ws = w->ws;
+                ctl.counters = w->counters;
+            }
+        }
+        float *Yb = Y + b0 * img_out;
+        const int vec_c = aligned16(Yb, N) && img_out % 4 == 0;
+        GemmArgs g{F, N, K, alpha, beta, A, ldA, X + b0 * img_in, N, Yb, N, 0, img_in, img_out};
+        g.cv = sg::ConvGeom{H, W, static_cast<int>(OW), KH, KW, sh, sw, ph, pw, dh, dw};
+        cudaError_t e = sg::tf32x3_conv_launch(p.tile_m, g, p.sch, ctl, 1, vec_c, p.grid, stream, nbc);
+        if (e != cudaSuccess) return from_cuda(e);
+    }
+    return 0;
+}
+
 }  // namespace
 
 extern "C" {
@@ -823,6 +931,13 @@ int sgemm_strided_batched(int transa, int transb, int M, int N, int K, float alp
                           int ldc, long long strideC, int batch, sgemm_stream_t stream, int algo) {
     return run_batched(transa, transb, M, N, K, alpha, A, lda, strideA, B, ldb, strideB, beta, C, ldc, strideC,
                        batch, reinterpret_cast<cudaStream_t>(stream), algo);
+}
+
+int sgemm_conv2d(int nb, int C, int H, int W, int F, int KH, int KW, int stride_h, int stride_w, int pad_h,
+                 int pad_w, int dil_h, int dil_w, float alpha, const float *X, const float *Wt, float beta, float *Y,
+                 sgemm_stream_t stream, int algo) {
+    return run_conv(nb, C, H, W, F, KH, KW, stride_h, stride_w, pad_h, pad_w, dil_h, dil_w, alpha, X, Wt, beta, Y,
+                    reinterpret_cast<cudaStream_t>(stream), algo);
 }
 
 int sgemm_version(void) { return kVersion; }

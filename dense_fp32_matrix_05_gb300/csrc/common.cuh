@@ -21,6 +21,19 @@ enum : int {
 // Test-only flag: withhold the first producer arrive (see the header).
 enum : int { kDebugWithholdArrive = 1 };
 
+// Implicit-GEMM convolution: B is not stored but read from an NCHW input X
+// (B = X, matrix b of the batch = image b, sB = channels * H * W) as its
+// im2col lowering, B[k][n] = X[c][oh * sh + kh * dh - ph][ow * sw + kw * dw - pw]
+// with k = (c * KH + kh) * KW + kw and n = oh * OW + ow, zero outside the
+// image.  A is the OIHW filter (M filters x K), C the image's NCHW output
+// (ldc = N = OH * OW).
+struct ConvGeom {
+    int H, W;    // input plane
+    int OW;      // output width
+    int KH, KW;  // filter
+    int sh, sw, ph, pw, dh, dw;
+};
+
 // One GEMM call: C = alpha * A * B + beta * C, row-major, leading dimensions
 // in elements.  Offsets are formed in 64-bit arithmetic.  A strided batch
 // (3xTF32 path) adds matrix b's offset b * sA, b * sB, b * sC (elements; a
@@ -35,6 +48,7 @@ struct GemmArgs {
     float *C;
     long long ldc;
     long long sA = 0, sB = 0, sC = 0;
+    ConvGeom cv{};  // implicit-GEMM convolution kernels only
 };
 
 // Work decomposition.  A work unit is one (tile, K range) pair; a tile whose

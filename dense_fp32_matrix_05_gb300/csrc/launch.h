@@ -16,6 +16,10 @@ constexpr int kFfmaBK = 16;        // K per FFMA pipeline stage
 bool tf32x3_supported_tm(int tm);
 int tf32x3_stages(int tm);
 int tf32x3_smem_bytes(int tm);
+// Implicit-GEMM convolution (g.cv; B = the NCHW input, batch = images).
+cudaError_t tf32x3_conv_launch(int tm, const GemmArgs &g, const Schedule &s, const DeviceCtl &ctl, int vec_a,
+                               int vec_c, int grid, cudaStream_t stream, int batch);
+
 // batch: matrices of a strided batch (g.sA / sB / sC; s.tpb tiles each).
 cudaError_t tf32x3_launch(int tm, const GemmArgs &g, const Schedule &s, const DeviceCtl &ctl,
                           int vec_a, int vec_b, int vec_c, int grid, cudaStream_t stream, int batch = 1);

@@ -10,6 +10,7 @@
 
 #include "launch.h"
 #include "tf32x3_gemm.cuh"
+#include "tmap.h"
 
 namespace sg {
 
@@ -36,10 +37,12 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return g_encode;
 }
 
+}  // namespace
+
 // Third (batch) dimension of a tensor map: `batch` matrices `stride`
 // elements apart, or one matrix when the stride is 0 (an operand shared by
 // the batch, or no batch).  The stride must be a multiple of 16 bytes.
-bool batch_dim(long long stride, int batch, long long one_matrix_elems, cuuint64_t &dim, cuuint64_t &bytes) {
+static bool batch_dim(long long stride, int batch, long long one_matrix_elems, cuuint64_t &dim, cuuint64_t &bytes) {
     if (stride == 0 || batch <= 1) {
         dim = 1;
         bytes = (static_cast<cuuint64_t>(one_matrix_elems) * sizeof(float) + 15) & ~cuuint64_t(15);
@@ -106,6 +109,8 @@ bool make_tmap_c(const GemmArgs &g, int batch, CUtensorMap *map) {
                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
+
+namespace {
 
 template <int TM, bool TA, bool TB>
 cudaError_t launch_tm(const GemmArgs &g, const Schedule &s, const DeviceCtl &ctl, int vec_a, int tma_c, int grid,

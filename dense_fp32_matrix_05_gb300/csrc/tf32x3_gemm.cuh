@@ -194,10 +194,46 @@ struct Raw<0, 0> {};
 // elements read as 0.  Thread gt of a group holds B[k0+BtK*h .. +BtK-1][n0+(gt&127)]
 // with h = gt >> 7 (its tensor-memory lane is its column), and A chunks
 // j = gt + GT * r: row j >> 2, k chunk j & 3 (GT threads per group).
-template <int TM, int BtK, int GT, int AJ>
+// CONV: B is gathered from the input image (implicit im2col); a warp's 32
+// columns are 32 neighbouring output pixels, so each k reads one stretch of
+// an input row.  The filter tap (c, kh, kw) of k is the same for the whole
+// warp and advances with k.
+template <int TM, int BtK, int GT, int AJ, bool CONV = false>
 __device__ __forceinline__ void load_raw(const GemmArgs &g, bool vec_a, int bi, int m0, int n0, int k0,
                                          int ptid, Raw<BtK, AJ> &raw) {
-    if constexpr (BtK > 0) {
+    if constexpr (BtK > 0 && CONV) {
+        const ConvGeom &cv = g.cv;
+        const int n = n0 + (ptid & (kTileN - 1));
+        const int kb = k0 + (ptid >> 7) * BtK;
+        const bool n_ok = n < g.N;
+        const int oh = n_ok ? n / cv.OW : 0;
+        // first input pixel of this column's window (may lie in the padding)
+        const int ih0 = oh * cv.sh - cv.ph;
+        const int iw0 = (n_ok ? n - oh * cv.OW : 0) * cv.sw - cv.pw;
+        const int pix0 = ih0 * cv.W + iw0;
+        // tap of k: (row offset, column offset, offset in the image), the same
+        // for the whole warp
+        const int khw = cv.KH * cv.KW;
+        const int c = kb / khw;
+        int kh = (kb - c * khw) / cv.KW;
+        int kw = kb - c * khw - kh * cv.KW;
+        int coff = c * cv.H * cv.W;
+        const float *xb = g.B + bi * g.sB;
+#pragma unroll
+        for (int e = 0; e < BtK; ++e) {
+            const int dy = kh * cv.dh, dx = kw * cv.dw;
+            const bool ok = n_ok && kb + e < g.K && static_cast<unsigned>(ih0 + dy) < static_cast<unsigned>(cv.H) &&
+                            static_cast<unsigned>(iw0 + dx) < static_cast<unsigned>(cv.W);
+            raw.b[e] = ok ? __ldg(xb + (coff + dy * cv.W + dx + pix0)) : 0.f;
+            if (++kw == cv.KW) {
+                kw = 0;
+                if (++kh == cv.KH) {
+                    kh = 0;
+                    coff += cv.H * cv.W;
+                }
+            }
+        }
+    } else if constexpr (BtK > 0) {
         const int n = n0 + (ptid & (kTileN - 1));
         const int kb = k0 + (ptid >> 7) * BtK;
         const bool n_ok = n < g.N;
@@ -307,13 +343,34 @@ __device__ __forceinline__ void store_split(uint32_t stage, uint32_t ring_taddr,
 // 3xTF32 split an infinite operand meeting a partner whose lo part is zero
 // gives Inf * 0 = NaN where fp32 arithmetic gives +-Inf, so NaN results are
 // recomputed on the CUDA cores.  Stops early once the sum itself is NaN.
+template <bool CONV>
 __device__ __noinline__ float recompute_dot(const GemmArgs &g, int bi, int m, int n) {
     const float *a = g.A + bi * g.sA + static_cast<long long>(m) * g.lda;
-    const float *b = g.B + bi * g.sB + n;
     float s = 0.f;
-    for (int k = 0; k < g.K; ++k) {
-        s = fmaf(__ldg(a + k), __ldg(b + static_cast<long long>(k) * g.ldb), s);
-        if (s != s) break;
+    if constexpr (CONV) {  // k walks the filter taps (c, kh, kw) in order
+        const ConvGeom &cv = g.cv;
+        const int oh = n / cv.OW;
+        const int ih0 = oh * cv.sh - cv.ph, iw0 = (n - oh * cv.OW) * cv.sw - cv.pw;
+        const float *x = g.B + bi * g.sB;
+        int k = 0;
+        for (; k < g.K; x += static_cast<long long>(cv.H) * cv.W) {
+            for (int kh = 0; kh < cv.KH; ++kh) {
+                const int ih = ih0 + kh * cv.dh;
+                for (int kw = 0; kw < cv.KW; ++kw, ++k) {
+                    const int iw = iw0 + kw * cv.dw;
+                    const bool in = static_cast<unsigned>(ih) < static_cast<unsigned>(cv.H) &&
+                                    static_cast<unsigned>(iw) < static_cast<unsigned>(cv.W);
+                    s = fmaf(__ldg(a + k), in ? __ldg(x + static_cast<long long>(ih) * cv.W + iw) : 0.f, s);
+                }
+            }
+            if (s != s) break;
+        }
+    } else {
+        const float *b = g.B + bi * g.sB + n;
+        for (int k = 0; k < g.K; ++k) {
+            s = fmaf(__ldg(a + k), __ldg(b + static_cast<long long>(k) * g.ldb), s);
+            if (s != s) break;
+        }
     }
     return s;
 }
@@ -402,7 +459,7 @@ __device__ __forceinline__ float fix_lane(const float4 &v, int q) {
     return q == 0 ? v.x : q == 1 ? v.y : q == 2 ? v.z : v.w;
 }
 
-template <int TM>
+template <int TM, bool CONV>
 __device__ __forceinline__ void fixup_tile(const GemmArgs &g, int bi, const float *wb, int nseg, int m0, int n0,
                                         int wid, int nw, int lane) {
     float *const cmat = g.C + bi * g.sC;  // matrix bi of a batch
@@ -467,7 +524,7 @@ __device__ __forceinline__ void fixup_tile(const GemmArgs &g, int bi, const floa
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 float s = fix_lane(sum[j], q);
-                if (s != s && nc + q < g.N) s = recompute_dot(g, bi, m, nc + q);
+                if (s != s && nc + q < g.N) s = recompute_dot<CONV>(g, bi, m, nc + q);
                 const float a = g.alpha * s;
                 res[q] = read_c ? fmaf(g.beta, fix_lane(old[j], q), a) : a;
             }
@@ -507,7 +564,9 @@ __device__ __forceinline__ void prefetch_c_tile(const GemmArgs &g, int bi, int m
 // swizzle, box 16 x TM); otherwise the producers load A themselves.
 // TMA_B: B rows are 16-byte aligned and tmap_b describes B (N x K, box
 // 128 x 16, no swizzle); otherwise the producers load B^T themselves.
-template <int TM, bool TMA_A, bool TMA_B>
+// CONV: implicit-GEMM convolution (B gathered from the input image by the
+// producers; TMA_B is false).
+template <int TM, bool TMA_A, bool TMA_B, bool CONV = false>
 __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
     tf32x3_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ Schedule sch,
                        const __grid_constant__ DeviceCtl ctl, int vec_a, int tma_c,
@@ -515,6 +574,7 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
                        const __grid_constant__ CUtensorMap tmap_c) {
     using C = Cfg<TM, TMA_B>;
     using R = Roles<TM, TMA_A, TMA_B>;
+    static_assert(!(CONV && TMA_B), "a convolution gathers B in the producers");
     constexpr int S = C::kStages;
     constexpr int CH = C::kChunk;
     static_assert(R::kGroups <= S, "a group's next stage must not wrap the ring twice");
@@ -637,7 +697,7 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
                     if (nan && n_ok) {
 #pragma unroll 1
                         for (int j = 0; j < CH; ++j)
-                            if (v[j] != v[j] && mb + j < g.M) v[j] = recompute_dot(g, c.b, mb + j, n);
+                            if (v[j] != v[j] && mb + j < g.M) v[j] = recompute_dot<CONV>(g, c.b, mb + j, n);
                     }
 #pragma unroll
                     for (int j = 0; j < CH; ++j) {
@@ -695,7 +755,7 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
                         // a non-finite input reached this chunk: exact dot products
 #pragma unroll 1
                         for (int j = 0; j < CH; ++j)
-                            if (v[j] != v[j] && mb + j < g.M) v[j] = recompute_dot(g, c.b, mb + j, n);
+                            if (v[j] != v[j] && mb + j < g.M) v[j] = recompute_dot<CONV>(g, c.b, mb + j, n);
                     }
                     if (n_ok) {
                         if (read_c) {
@@ -787,7 +847,7 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
 #pragma unroll
         for (int i = 0; i < NB; ++i) {
             if (next.valid(sch)) {
-                load_raw<TM, BtK, GT, AJ>(g, vec_a != 0, next.b, next.mt * TM, next.nt * kTileN, next.kt * kBK, gt,
+                load_raw<TM, BtK, GT, AJ, CONV>(g, vec_a != 0, next.b, next.mt * TM, next.nt * kTileN, next.kt * kBK, gt,
                                           buf[i]);
                 for (int t = 0; t < G && next.valid(sch); ++t) next.advance(sch);
                 ++loaded;
@@ -828,7 +888,7 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
                         ph ^= 1u;
                     }
                     if (next.valid(sch)) {
-                        load_raw<TM, BtK, GT, AJ>(g, vec_a != 0, next.b, next.mt * TM, next.nt * kTileN, next.kt * kBK,
+                        load_raw<TM, BtK, GT, AJ, CONV>(g, vec_a != 0, next.b, next.mt * TM, next.nt * kTileN, next.kt * kBK,
                                                   gt, buf[i]);
                         for (int t = 0; t < G && next.valid(sch); ++t) next.advance(sch);
                         ++loaded;
@@ -941,7 +1001,7 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
         __threadfence();
 #pragma unroll 1
         for (int e = 0; e < nd; ++e)
-            fixup_tile<TM>(g, s_defer[5 * e + 4], ctl.ws + static_cast<long long>(s_defer[5 * e + 3]) * (kTileN * TM),
+            fixup_tile<TM, CONV>(g, s_defer[5 * e + 4], ctl.ws + static_cast<long long>(s_defer[5 * e + 3]) * (kTileN * TM),
                            s_defer[5 * e + 2], s_defer[5 * e] * TM, s_defer[5 * e + 1] * kTileN, warp,
                            R::kThreads / 32, lane);
     }

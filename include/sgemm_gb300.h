@@ -286,6 +286,49 @@ int sgemm_strided_batched(int transa, int transb, int M, int N, int K, float alp
                           float beta, float *C, int ldc, long long strideC,
                           int batch, sgemm_stream_t stream, int algo);
 
+/*
+ * sgemm_conv2d - Y = alpha * conv2d(X, Wt) + beta * Y in fp32, as an
+ * implicit GEMM: the im2col lowering that gives the skinny GEMM shapes of
+ * "UNIVERSAL_SGEMM_CUDA" (its shape list: filters x (channels * KH * KW)
+ * times (channels * KH * KW) x output pixels) is never stored; the kernel's
+ * producers read each B element straight from the input image.  The pages
+ * give only the lowered shapes; the layer is the usual one: a
+ * cross-correlation (the filter is not flipped) with zero padding,
+ *   Y[b][f][oh][ow] = alpha * sum_{c,kh,kw} Wt[f][c][kh][kw] *
+ *                     X[b][c][oh*stride_h + kh*dil_h - pad_h][ow*stride_w + kw*dil_w - pad_w]
+ *                     + beta * Y[b][f][oh][ow],
+ * input positions outside the image reading as 0.
+ *
+ *   nb (1), C (2), H (3), W (4): X is nb x C x H x W, packed NCHW; nb, C >= 0,
+ *                 H, W >= 1.
+ *   F (5), KH (6), KW (7): Wt is F x C x KH x KW, packed OIHW; F >= 0,
+ *                 KH, KW >= 1, and the dilated filter fits in the padded
+ *                 image (else -6 / -7).
+ *   stride_h, stride_w (8, 9) >= 1; pad_h, pad_w (10, 11) >= 0;
+ *   dil_h, dil_w (12, 13) >= 1.
+ *   alpha (14), X (15), Wt (16), beta (17): device pointers for X and Wt,
+ *                 read only; not read when alpha == 0 or C == 0.
+ *   Y (18):       device pointer, nb x F x OH x OW packed NCHW with
+ *                 OH = (H + 2 pad_h - dil_h (KH - 1) - 1) / stride_h + 1 and
+ *                 OW likewise; must not overlap X or Wt.  beta == 0: Y is
+ *                 not read.
+ *   stream (19):  as in sgemm.
+ *   algo (20):    SGEMM_ALGO_AUTO or SGEMM_ALGO_TF32X3 (3xTF32 tensor path;
+ *                 the FFMA path has no convolution form: -20).
+ * Limits: a padded image with its filter reach, times C + 1, below 2^31
+ * elements (32-bit offsets in the gather; else -2), OH * OW < 2^31 (else -3).
+ * The filter's rows (C * KH * KW floats) are first copied to 16-byte aligned
+ * rows in a library buffer of this stream (as in sgemm_t) when they are not
+ * aligned.  Accuracy and status reporting are those of sgemm_ex with the
+ * TF32X3 path: the same bound per output element, with the sum over the
+ * filter taps that fall inside the image.  Returns 0, -i for the i-th
+ * argument, a positive cudaError_t, or SGEMM_ERR_WORKSPACE.
+ */
+int sgemm_conv2d(int nb, int C, int H, int W, int F, int KH, int KW,
+                 int stride_h, int stride_w, int pad_h, int pad_w, int dil_h, int dil_w,
+                 float alpha, const float *X, const float *Wt, float beta, float *Y,
+                 sgemm_stream_t stream, int algo);
+
 /* sgemm_version - library version as 10000*major + 100*minor + patch. */
 int sgemm_version(void);
 

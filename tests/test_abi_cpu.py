@@ -236,3 +236,40 @@ def test_transposed_and_batched_argument_checks(lib):
     assert b(0, 0, 4, 4, 4, 1.0, A, 4, 0, B, 4, 0, 0.0, C, 4, 16, 2, None, 9) == -19
     assert b(*base, 0, B, 4, 0, 0.0, C, 4, 16, 0) == 0            # empty batch
 
+
+
+def test_conv2d_argument_checks(lib):
+    """sgemm_conv2d rejects bad geometry, numbered by position, before
+    touching a device; an empty batch or no filters is a no-op."""
+    X, W, Y = FAKE, FAKE + (1 << 24), FAKE + (2 << 24)
+
+    def conv(nb=2, C=3, H=8, W_=8, F=4, KH=3, KW=3, sh=1, sw=1, ph=1, pw=1, dh=1, dw=1,
+             x=X, w=W, y=Y, algo=0, alpha=1.0):
+        return pkg.sgemm_conv2d(x, w, y, alpha=alpha, stride=(sh, sw), pad=(ph, pw), dil=(dh, dw), algo=algo,
+                                shape=(nb, C, H, W_, F, KH, KW))
+
+    assert conv(nb=-1) == -1
+    assert conv(C=-1) == -2
+    assert conv(H=0) == -3
+    assert conv(W_=0) == -4
+    assert conv(F=-1) == -5
+    assert conv(KH=0) == -6
+    assert conv(KW=0) == -7
+    assert conv(sh=0) == -8
+    assert conv(sw=0) == -9
+    assert conv(ph=-1) == -10
+    assert conv(pw=-1) == -11
+    assert conv(dh=0) == -12
+    assert conv(dw=0) == -13
+    assert conv(KH=11, ph=1) == -6                     # dilated filter taller than the padded image
+    assert conv(KW=3, dw=5, pw=0) == -7
+    assert conv(algo=pkg.SGEMM_ALGO_FFMA) == -20
+    assert conv(algo=7) == -20
+    assert conv(x=None) == -15
+    assert conv(w=None) == -16
+    assert conv(y=None) == -18
+    assert conv(y=X + 64) == -18                       # Y overlaps X
+    assert conv(C=70000, H=200, W_=200) == -2         # 32-bit offsets inside one image
+    assert conv(nb=0) == 0 and conv(F=0) == 0
+    assert pkg.conv2d_out_size(224, 224, 7, 7, (2, 2), (3, 3)) == (112, 112)
+    assert pkg.conv2d_out_size(10, 9, 3, 2, (1, 2), (0, 1), (2, 3)) == (6, 4)
