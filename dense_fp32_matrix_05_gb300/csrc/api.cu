@@ -612,10 +612,14 @@ int run_batched(int transa, int transb, int M, int N, int K, float alpha, const 
 // Y = alpha * conv2d(X, Wt) + beta * Y (NCHW input and output, OIHW filter)
 // as one implicit GEMM per image: M = F filters, K = C * KH * KW taps,
 // N = OH * OW output pixels, with the images as the kernel's strided batch.
-// The filter is the A operand; a filter whose rows are not 16-byte aligned
-// is first copied into rows padded to 4 floats (this stream's transpose
-// buffer) so that it keeps its tensor-map copies.  Returns 0, -i for the
-// i-th argument of sgemm_conv2d, or a positive error.
+// The filter is the A operand, always read through its tensor map:
+//  - C % 16 == 0: k runs over the channels at each tap (kConvChannels), so
+//    the filter is first reordered to OHWI rows in this stream's transpose
+//    buffer;
+//  - otherwise k runs over the taps of each channel (kConvTaps, the OIHW
+//    order); a filter whose rows are not 16-byte aligned is copied into rows
+//    padded to 4 floats there.
+// Returns 0, -i for the i-th argument of sgemm_conv2d, or a positive error.
 int run_conv(int nb, int C, int H, int W, int F, int KH, int KW, int sh, int sw, int ph, int pw, int dh, int dw,
              float alpha, const float *X, const float *Wt, float beta, float *Y, cudaStream_t stream, int algo) {
     if (nb < 0) return -1;
@@ -657,11 +661,12 @@ int run_conv(int nb, int C, int H, int W, int F, int KH, int KW, int sh, int sw,
     DevState *d = nullptr;
     float *wpad = nullptr;
     const int lda = (K + 3) / 4 * 4;
+    const int order = C % 16 == 0 ? sg::kConvChannels : sg::kConvTaps;
     {
         std::lock_guard<std::mutex> lk(g_mu);
         int rc = device_state(&d);
         if (rc != 0) return rc;
-        if (use_ab && !aligned16(Wt, K)) {
+        if (use_ab && (order == sg::kConvChannels || !aligned16(Wt, K))) {
             rc = get_transpose_ws(*d, stream, static_cast<size_t>(F) * lda * sizeof(float), &wpad);
             if (rc != 0) return rc;
         }
@@ -674,7 +679,10 @@ int run_conv(int nb, int C, int H, int W, int F, int KH, int KW, int sh, int sw,
         }
         return 0;
     }
-    if (wpad) {
+    if (wpad && order == sg::kConvChannels) {
+        cudaError_t e = sg::filter_ohwi_launch(Wt, F, C, KH, KW, wpad, lda, stream);
+        if (e != cudaSuccess) return from_cuda(e);
+    } else if (wpad) {
         cudaError_t e = cudaMemcpy2DAsync(wpad, static_cast<size_t>(lda) * sizeof(float), Wt,
                                           static_cast<size_t>(K) * sizeof(float), static_cast<size_t>(K) * sizeof(float),
                                           static_cast<size_t>(F), cudaMemcpyDeviceToDevice, stream);
@@ -708,8 +716,8 @@ int run_conv(int nb, int C, int H, int W, int F, int KH, int KW, int sh, int sw,
         float *Yb = Y + b0 * img_out;
         const int vec_c = aligned16(Yb, N) && img_out % 4 == 0;
         GemmArgs g{F, N, K, alpha, beta, A, ldA, X + b0 * img_in, N, Yb, N, 0, img_in, img_out};
-        g.cv = sg::ConvGeom{H, W, static_cast<int>(OW), KH, KW, sh, sw, ph, pw, dh, dw};
-        cudaError_t e = sg::tf32x3_conv_launch(p.tile_m, g, p.sch, ctl, 1, vec_c, p.grid, stream, nbc);
+        g.cv = sg::ConvGeom{C, H, W, static_cast<int>(OW), KH, KW, sh, sw, ph, pw, dh, dw};
+        cudaError_t e = sg::tf32x3_conv_launch(p.tile_m, g, p.sch, ctl, order, vec_c, p.grid, stream, nbc);
         if (e != cudaSuccess) return from_cuda(e);
     }
     return 0;

@@ -24,10 +24,19 @@ enum : int { kDebugWithholdArrive = 1 };
 // Implicit-GEMM convolution: B is not stored but read from an NCHW input X
 // (B = X, matrix b of the batch = image b, sB = channels * H * W) as its
 // im2col lowering, B[k][n] = X[c][oh * sh + kh * dh - ph][ow * sw + kw * dw - pw]
-// with k = (c * KH + kh) * KW + kw and n = oh * OW + ow, zero outside the
-// image.  A is the OIHW filter (M filters x K), C the image's NCHW output
-// (ldc = N = OH * OW).
+// with n = oh * OW + ow, zero outside the image, and k a numbering of the
+// taps (c, kh, kw) (kConvTaps / kConvChannels below).  A is the filter,
+// M filters x K in the same k order, C the image's NCHW output (ldc = N =
+// OH * OW).
+// Order of the K index of an implicit-GEMM convolution.
+enum : int {
+    kConvNone = 0,      // a plain GEMM
+    kConvTaps = 1,      // k = (c * KH + kh) * KW + kw (OIHW filter rows)
+    kConvChannels = 2,  // k = (kh * KW + kw) * C + c (OHWI filter rows, C % 16 == 0)
+};
+
 struct ConvGeom {
+    int C;       // input channels
     int H, W;    // input plane
     int OW;      // output width
     int KH, KW;  // filter

@@ -1,8 +1,10 @@
 // Instantiations and launcher of the implicit-GEMM convolution form of the
 // 3xTF32 kernel: the producers gather B, the im2col matrix of each image,
 // straight from the NCHW input (ConvGeom), so it never exists in memory.
-// The filter (A) and the output (C) keep their tensor-map copies when
-// aligned; the images of a batch are the kernel's strided batch.
+// The filter (A) is staged by the host into 16-byte aligned rows in the
+// kernel's k order and always goes through its tensor map; the output (C)
+// keeps its tensor-map copies when aligned; the images of a batch are the
+// kernel's strided batch.
 #include <cuda.h>
 
 #include <cstring>
@@ -14,42 +16,68 @@
 namespace sg {
 namespace {
 
-template <int TM, bool TA>
-cudaError_t launch_conv_tm(const GemmArgs &g, const Schedule &s, const DeviceCtl &ctl, int vec_a, int tma_c,
-                           int grid, const CUtensorMap &map_a, const CUtensorMap &map_c, cudaStream_t stream) {
+template <int TM, int ORDER>
+cudaError_t launch_conv_tm(const GemmArgs &g, const Schedule &s, const DeviceCtl &ctl, int tma_c, int grid,
+                           const CUtensorMap &map_a, const CUtensorMap &map_c, cudaStream_t stream) {
     using C = tf32x3::Cfg<TM, false>;
-    auto kern = tf32x3::tf32x3_gemm_kernel<TM, TA, false, true>;
+    auto kern = tf32x3::tf32x3_gemm_kernel<TM, true, false, ORDER>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     // no B map: the kernel does not read it when TMA_B is false
-    kern<<<grid, tf32x3::Roles<TM, TA, false>::kThreads, C::kSmemBytes, stream>>>(g, s, ctl, vec_a, tma_c, map_a,
-                                                                                    map_a, map_c);
+    kern<<<grid, tf32x3::Roles<TM, true, false>::kThreads, C::kSmemBytes, stream>>>(g, s, ctl, 1, tma_c, map_a,
+                                                                                      map_a, map_c);
     return cudaGetLastError();
 }
 
 template <int TM>
-cudaError_t launch_conv_rows(const GemmArgs &g, const Schedule &s, const DeviceCtl &ctl, int vec_a, int vec_c,
+cudaError_t launch_conv_rows(const GemmArgs &g, const Schedule &s, const DeviceCtl &ctl, int order, int vec_c,
                              int grid, int batch, cudaStream_t stream) {
     CUtensorMap ma, mc;
     std::memset(&ma, 0, sizeof(ma));
     std::memset(&mc, 0, sizeof(mc));
-    const bool ta = vec_a && make_tmap_a(g, TM, batch, &ma);
+    if (!make_tmap_a(g, TM, batch, &ma)) return cudaErrorNotSupported;
     const int tc = (vec_c && make_tmap_c(g, batch, &mc)) ? 1 : 0;
-    if (ta) return launch_conv_tm<TM, true>(g, s, ctl, vec_a, tc, grid, ma, mc, stream);
-    return launch_conv_tm<TM, false>(g, s, ctl, vec_a, tc, grid, ma, mc, stream);
+    if (order == kConvChannels) return launch_conv_tm<TM, kConvChannels>(g, s, ctl, tc, grid, ma, mc, stream);
+    return launch_conv_tm<TM, kConvTaps>(g, s, ctl, tc, grid, ma, mc, stream);
+}
+
+// dst[f][(kh * KW + kw) * C + c] = w[f][c][kh][kw]: OIHW rows to OHWI rows of
+// leading dimension ld.  Grid-stride over the destination, which is written
+// in order; the filter is small, so its strided reads stay in cache.
+__global__ void filter_ohwi_kernel(const float *__restrict__ w, int F, int C, int KHW, float *__restrict__ dst,
+                                   long long ld) {
+    const long long row = static_cast<long long>(C) * KHW;
+    const long long total = static_cast<long long>(F) * row;
+    for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const long long f = i / row;
+        const int r = static_cast<int>(i - f * row);
+        const int tap = r / C, c = r - tap * C;
+        dst[f * ld + r] = w[(f * C + c) * KHW + tap];
+    }
 }
 
 }  // namespace
 
-cudaError_t tf32x3_conv_launch(int tm, const GemmArgs &g, const Schedule &s, const DeviceCtl &ctl, int vec_a,
+cudaError_t filter_ohwi_launch(const float *w, int F, int C, int KH, int KW, float *dst, long long ld,
+                               cudaStream_t stream) {
+    const long long total = static_cast<long long>(F) * C * KH * KW;
+    if (total <= 0) return cudaSuccess;
+    const long long blocks = (total + 255) / 256;
+    filter_ohwi_kernel<<<static_cast<unsigned>(blocks < 4096 ? blocks : 4096), 256, 0, stream>>>(w, F, C, KH * KW,
+                                                                                                 dst, ld);
+    return cudaGetLastError();
+}
+
+cudaError_t tf32x3_conv_launch(int tm, const GemmArgs &g, const Schedule &s, const DeviceCtl &ctl, int order,
                                int vec_c, int grid, cudaStream_t stream, int batch) {
     switch (tm) {
-        case 16: return launch_conv_rows<16>(g, s, ctl, vec_a, vec_c, grid, batch, stream);
-        case 32: return launch_conv_rows<32>(g, s, ctl, vec_a, vec_c, grid, batch, stream);
-        case 64: return launch_conv_rows<64>(g, s, ctl, vec_a, vec_c, grid, batch, stream);
-        case 128: return launch_conv_rows<128>(g, s, ctl, vec_a, vec_c, grid, batch, stream);
-        case 192: return launch_conv_rows<192>(g, s, ctl, vec_a, vec_c, grid, batch, stream);
-        case 256: return launch_conv_rows<256>(g, s, ctl, vec_a, vec_c, grid, batch, stream);
+        case 16: return launch_conv_rows<16>(g, s, ctl, order, vec_c, grid, batch, stream);
+        case 32: return launch_conv_rows<32>(g, s, ctl, order, vec_c, grid, batch, stream);
+        case 64: return launch_conv_rows<64>(g, s, ctl, order, vec_c, grid, batch, stream);
+        case 128: return launch_conv_rows<128>(g, s, ctl, order, vec_c, grid, batch, stream);
+        case 192: return launch_conv_rows<192>(g, s, ctl, order, vec_c, grid, batch, stream);
+        case 256: return launch_conv_rows<256>(g, s, ctl, order, vec_c, grid, batch, stream);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -16,9 +16,14 @@ constexpr int kFfmaBK = 16;        // K per FFMA pipeline stage
 bool tf32x3_supported_tm(int tm);
 int tf32x3_stages(int tm);
 int tf32x3_smem_bytes(int tm);
-// Implicit-GEMM convolution (g.cv; B = the NCHW input, batch = images).
-cudaError_t tf32x3_conv_launch(int tm, const GemmArgs &g, const Schedule &s, const DeviceCtl &ctl, int vec_a,
+// Implicit-GEMM convolution (g.cv; B = the NCHW input, batch = images;
+// order: kConvTaps or kConvChannels; g.A: the filter in that k order with
+// 16-byte aligned rows).
+cudaError_t tf32x3_conv_launch(int tm, const GemmArgs &g, const Schedule &s, const DeviceCtl &ctl, int order,
                                int vec_c, int grid, cudaStream_t stream, int batch);
+// OIHW filter w (F x C x KH x KW) to OHWI rows of leading dimension ld.
+cudaError_t filter_ohwi_launch(const float *w, int F, int C, int KH, int KW, float *dst, long long ld,
+                               cudaStream_t stream);
 
 // batch: matrices of a strided batch (g.sA / sB / sC; s.tpb tiles each).
 cudaError_t tf32x3_launch(int tm, const GemmArgs &g, const Schedule &s, const DeviceCtl &ctl,

@@ -196,12 +196,30 @@ struct Raw<0, 0> {};
 // j = gt + GT * r: row j >> 2, k chunk j & 3 (GT threads per group).
 // CONV: B is gathered from the input image (implicit im2col); a warp's 32
 // columns are 32 neighbouring output pixels, so each k reads one stretch of
-// an input row.  The filter tap (c, kh, kw) of k is the same for the whole
-// warp and advances with k.
-template <int TM, int BtK, int GT, int AJ, bool CONV = false>
+// an input row.  kConvTaps: k = (c * KH + kh) * KW + kw, the filter's own
+// (OIHW) order; the tap of k is the same for the whole warp and advances
+// with k.  kConvChannels: k = (kh * KW + kw) * C + c (filter staged OHWI,
+// C a multiple of 16), so the 16 k of a call are 16 channels at one tap:
+// one bounds check, then loads H * W apart, like a plain B column.
+template <int TM, int BtK, int GT, int AJ, int CONV = kConvNone>
 __device__ __forceinline__ void load_raw(const GemmArgs &g, bool vec_a, int bi, int m0, int n0, int k0,
                                          int ptid, Raw<BtK, AJ> &raw) {
-    if constexpr (BtK > 0 && CONV) {
+    if constexpr (BtK > 0 && CONV == kConvChannels) {
+        const ConvGeom &cv = g.cv;
+        const int n = n0 + (ptid & (kTileN - 1));
+        const int kb = k0 + (ptid >> 7) * BtK;
+        const int tap = kb / cv.C, c0 = kb - tap * cv.C;
+        const int kh = tap / cv.KW, kw = tap - kh * cv.KW;
+        const int oh = n / cv.OW;
+        const int ih = oh * cv.sh - cv.ph + kh * cv.dh;
+        const int iw = (n - oh * cv.OW) * cv.sw - cv.pw + kw * cv.dw;
+        const bool ok = n < g.N && kb < g.K && static_cast<unsigned>(ih) < static_cast<unsigned>(cv.H) &&
+                        static_cast<unsigned>(iw) < static_cast<unsigned>(cv.W);
+        const long long plane = static_cast<long long>(cv.H) * cv.W;
+        const float *src = g.B + bi * g.sB + c0 * plane + static_cast<long long>(ih) * cv.W + iw;
+#pragma unroll
+        for (int e = 0; e < BtK; ++e) raw.b[e] = ok ? __ldg(src + e * plane) : 0.f;
+    } else if constexpr (BtK > 0 && CONV == kConvTaps) {
         const ConvGeom &cv = g.cv;
         const int n = n0 + (ptid & (kTileN - 1));
         const int kb = k0 + (ptid >> 7) * BtK;
@@ -343,11 +361,29 @@ __device__ __forceinline__ void store_split(uint32_t stage, uint32_t ring_taddr,
 // 3xTF32 split an infinite operand meeting a partner whose lo part is zero
 // gives Inf * 0 = NaN where fp32 arithmetic gives +-Inf, so NaN results are
 // recomputed on the CUDA cores.  Stops early once the sum itself is NaN.
-template <bool CONV>
+template <int CONV>
 __device__ __noinline__ float recompute_dot(const GemmArgs &g, int bi, int m, int n) {
     const float *a = g.A + bi * g.sA + static_cast<long long>(m) * g.lda;
     float s = 0.f;
-    if constexpr (CONV) {  // k walks the filter taps (c, kh, kw) in order
+    if constexpr (CONV == kConvChannels) {  // k walks (kh, kw, c) in order
+        const ConvGeom &cv = g.cv;
+        const int oh = n / cv.OW;
+        const int ih0 = oh * cv.sh - cv.ph, iw0 = (n - oh * cv.OW) * cv.sw - cv.pw;
+        const long long plane = static_cast<long long>(cv.H) * cv.W;
+        const float *x = g.B + bi * g.sB;
+        int k = 0;
+        for (int kh = 0; kh < cv.KH; ++kh) {
+            const int ih = ih0 + kh * cv.dh;
+            for (int kw = 0; kw < cv.KW; ++kw) {
+                const int iw = iw0 + kw * cv.dw;
+                const bool in = static_cast<unsigned>(ih) < static_cast<unsigned>(cv.H) &&
+                                static_cast<unsigned>(iw) < static_cast<unsigned>(cv.W);
+                const float *px = x + static_cast<long long>(ih) * cv.W + iw;
+                for (int c = 0; c < cv.C; ++c, ++k) s = fmaf(__ldg(a + k), in ? __ldg(px + c * plane) : 0.f, s);
+            }
+            if (s != s) break;
+        }
+    } else if constexpr (CONV == kConvTaps) {  // k walks the filter taps (c, kh, kw) in order
         const ConvGeom &cv = g.cv;
         const int oh = n / cv.OW;
         const int ih0 = oh * cv.sh - cv.ph, iw0 = (n - oh * cv.OW) * cv.sw - cv.pw;
@@ -459,7 +495,7 @@ __device__ __forceinline__ float fix_lane(const float4 &v, int q) {
     return q == 0 ? v.x : q == 1 ? v.y : q == 2 ? v.z : v.w;
 }
 
-template <int TM, bool CONV>
+template <int TM, int CONV>
 __device__ __forceinline__ void fixup_tile(const GemmArgs &g, int bi, const float *wb, int nseg, int m0, int n0,
                                         int wid, int nw, int lane) {
     float *const cmat = g.C + bi * g.sC;  // matrix bi of a batch
@@ -564,9 +600,9 @@ __device__ __forceinline__ void prefetch_c_tile(const GemmArgs &g, int bi, int m
 // swizzle, box 16 x TM); otherwise the producers load A themselves.
 // TMA_B: B rows are 16-byte aligned and tmap_b describes B (N x K, box
 // 128 x 16, no swizzle); otherwise the producers load B^T themselves.
-// CONV: implicit-GEMM convolution (B gathered from the input image by the
-// producers; TMA_B is false).
-template <int TM, bool TMA_A, bool TMA_B, bool CONV = false>
+// CONV: implicit-GEMM convolution (kConvTaps or kConvChannels; B gathered
+// from the input image by the producers, TMA_B false).
+template <int TM, bool TMA_A, bool TMA_B, int CONV = kConvNone>
 __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
     tf32x3_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ Schedule sch,
                        const __grid_constant__ DeviceCtl ctl, int vec_a, int tma_c,
@@ -574,7 +610,7 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
                        const __grid_constant__ CUtensorMap tmap_c) {
     using C = Cfg<TM, TMA_B>;
     using R = Roles<TM, TMA_A, TMA_B>;
-    static_assert(!(CONV && TMA_B), "a convolution gathers B in the producers");
+    static_assert(CONV == kConvNone || !TMA_B, "a convolution gathers B in the producers");
     constexpr int S = C::kStages;
     constexpr int CH = C::kChunk;
     static_assert(R::kGroups <= S, "a group's next stage must not wrap the ring twice");
