@@ -635,7 +635,7 @@ int run_conv(int nb, int C, int H, int W, int F, int KH, int KW, int sh, int sw,
     if (pw < 0) return -11;
     if (dh < 1) return -12;
     if (dw < 1) return -13;
-    if (algo != SGEMM_ALGO_AUTO && algo != SGEMM_ALGO_TF32X3) return -20;
+    if (algo != SGEMM_ALGO_AUTO && algo != SGEMM_ALGO_TF32X3 && algo != SGEMM_ALGO_FFMA) return -20;
     const long long span_h = static_cast<long long>(H) + 2LL * ph, span_w = static_cast<long long>(W) + 2LL * pw;
     const long long reach_h = static_cast<long long>(dh) * (KH - 1) + 1, reach_w = static_cast<long long>(dw) * (KW - 1) + 1;
     if (span_h < reach_h) return -6;  // the filter is taller than the padded image
@@ -652,6 +652,11 @@ int run_conv(int nb, int C, int H, int W, int F, int KH, int KW, int sh, int sw,
     if (use_ab && Wt == nullptr) return -16;
     if (Y == nullptr) return -18;
     const int K = static_cast<int>(Kl), N = static_cast<int>(Nl);
+    // the wide-N FFMA kernel's convolution form: up to 32 filters of up to 64
+    // taps; AUTO takes it where its GEMM form beats the tensor path (K <= 48)
+    const bool wide = sg::ffma_wide_fits(F, K) && (algo == SGEMM_ALGO_FFMA || (algo == SGEMM_ALGO_AUTO &&
+                                                                               K <= kWideAutoMaxK));
+    if (algo == SGEMM_ALGO_FFMA && !wide) return -20;
     const long long img_in = static_cast<long long>(C) * H * W, img_out = static_cast<long long>(F) * N;
     const size_t y_bytes = static_cast<size_t>(nb) * img_out * sizeof(float);
     if (use_ab && (overlaps(Y, y_bytes, X, static_cast<size_t>(nb) * img_in * sizeof(float)) ||
@@ -666,7 +671,7 @@ int run_conv(int nb, int C, int H, int W, int F, int KH, int KW, int sh, int sw,
         std::lock_guard<std::mutex> lk(g_mu);
         int rc = device_state(&d);
         if (rc != 0) return rc;
-        if (use_ab && (order == sg::kConvChannels || !aligned16(Wt, K))) {
+        if (use_ab && !wide && (order == sg::kConvChannels || !aligned16(Wt, K))) {
             rc = get_transpose_ws(*d, stream, static_cast<size_t>(F) * lda * sizeof(float), &wpad);
             if (rc != 0) return rc;
         }
@@ -690,6 +695,20 @@ int run_conv(int nb, int C, int H, int W, int F, int KH, int KW, int sh, int sw,
     }
     const float *A = wpad ? wpad : Wt;
     const int ldA = wpad ? lda : K;
+    if (wide) {
+        // columns = the pixels of all images of a launch (fewer than 2^31)
+        const int imgs = static_cast<int>(std::max(1LL, std::min<long long>(nb, INT32_MAX / Nl)));
+        for (int b0 = 0; b0 < nb; b0 += imgs) {
+            const int nbc = std::min(imgs, nb - b0);
+            const int Nt = nbc * N;
+            GemmArgs g{F, Nt, K, alpha, beta, Wt, K, X + b0 * img_in, 1, Y + b0 * img_out, N, 0, img_in, img_out};
+            g.cv = sg::ConvGeom{C, H, W, static_cast<int>(OW), KH, KW, sh, sw, ph, pw, dh, dw};
+            const int grid = std::min(sg::ffma_wide_blocks(Nt), 2 * d->sms);
+            cudaError_t e = sg::ffma_wide_launch(g, 0, grid, stream, true);
+            if (e != cudaSuccess) return from_cuda(e);
+        }
+        return 0;
+    }
     // images per launch: the schedule's unit index is 32-bit (at most 16 K
     // slices of tiles 16 rows high)
     const long long per_img = static_cast<long long>(ceil_div(F, 16)) * ceil_div(N, sg::kTf32x3TileN) * 16;

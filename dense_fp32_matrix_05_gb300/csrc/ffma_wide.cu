@@ -18,6 +18,13 @@
 // Work decomposition follows the 2-D thread tiles of "NVIDIA_SGEMM_PRACTICE"
 // (sections "kernel 4" and "kernel 5", here 32 x 2 per thread) and the
 // prefetching of its "kernel 7", reorganised around a resident A.
+//
+// Convolution form (CONV): the implicit GEMM of a layer with at most 32
+// filters and 64 taps (ConvGeom, k = (c * KH + kh) * KW + kw, the OIHW filter
+// rows as A).  The columns run over the output pixels of all images
+// (n = image * ldc + pixel, ldc = OH * OW); the slab copies gather B from the
+// input image, 4 bytes each, zero-filled outside it, and C goes to the
+// image's NCHW output (sC floats per image).
 #include <cstdint>
 
 #include "common.cuh"
@@ -37,9 +44,51 @@ constexpr int kAFloats = kMaxK * kMaxM;  // A^T: row k holds A[0..31][k]
 constexpr int kSmemBytes = (kStages * kStageFloats + kAFloats) * 4;
 
 // Slab q of this CTA: k rows [kc * 16, +16) of column block cb.
+template <bool CONV>
 __device__ __forceinline__ void load_slab(const GemmArgs &g, bool vec_b, int cb, int kc, uint32_t dst, int tid) {
     const int n0 = cb * kCols;
-    if (vec_b) {
+    if constexpr (CONV) {
+        // this thread copies columns tid and tid + 256 of every slab row
+        const ConvGeom &cv = g.cv;
+        const float *col[2];
+        int ih0[2], iw0[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int n = n0 + tid + h * kThreads;
+            const bool n_ok = n < g.N;
+            const int img = n_ok ? n / static_cast<int>(g.ldc) : 0;
+            const int pix = n_ok ? n - img * static_cast<int>(g.ldc) : 0;
+            const int oh = pix / cv.OW;
+            ih0[h] = n_ok ? oh * cv.sh - cv.ph : -(1 << 20);  // a column past N reads nothing
+            iw0[h] = (pix - oh * cv.OW) * cv.sw - cv.pw;
+            col[h] = g.B + img * g.sB;
+        }
+        const int khw = cv.KH * cv.KW;
+        const int kb = kc * kKc;
+        int c = kb / khw;
+        int kh = (kb - c * khw) / cv.KW;
+        int kw = kb - c * khw - kh * cv.KW;
+#pragma unroll 4
+        for (int r = 0; r < kKc; ++r) {
+            const bool k_ok = kb + r < g.K;
+            const int dy = kh * cv.dh, dx = kw * cv.dw;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int ih = ih0[h] + dy, iw = iw0[h] + dx;
+                const bool ok = k_ok && static_cast<unsigned>(ih) < static_cast<unsigned>(cv.H) &&
+                                static_cast<unsigned>(iw) < static_cast<unsigned>(cv.W);
+                const float *src = ok ? col[h] + (static_cast<long long>(c) * cv.H + ih) * cv.W + iw : g.B;
+                cp_async4(dst + static_cast<uint32_t>((r * kCols + tid + h * kThreads) * 4), src, ok ? 4u : 0u);
+            }
+            if (++kw == cv.KW) {
+                kw = 0;
+                if (++kh == cv.KH) {
+                    kh = 0;
+                    ++c;
+                }
+            }
+        }
+    } else if (vec_b) {
 #pragma unroll
         for (int i = 0; i < kKc * kCols / 4 / kThreads; ++i) {
             const int c = tid + i * kThreads;
@@ -67,9 +116,40 @@ __device__ __forceinline__ void load_slab(const GemmArgs &g, bool vec_b, int cb,
 }
 
 // C[m][n], C[m][n + 1] for the rows m < M of this thread's two columns.
+// CONV: column n is pixel n % ldc of image n / ldc, whose output starts
+// sC floats after the previous image's.
+template <bool CONV>
 __device__ __forceinline__ void store_block(const GemmArgs &g, int n, const uint64_t (&acc0)[16],
                                             const uint64_t (&acc1)[16]) {
     if (n >= g.N) return;
+    if constexpr (CONV) {
+        const int ld = static_cast<int>(g.ldc);
+        float *cp[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int nn = min(n + h, g.N - 1);
+            const int img = nn / ld;
+            cp[h] = g.C + img * g.sC + (nn - img * ld);
+        }
+        const bool two = n + 1 < g.N;
+        const bool read_c = g.beta != 0.f;
+#pragma unroll
+        for (int mp = 0; mp < kMaxM / 2; ++mp) {
+            float c0[2], c1[2];
+            pair_split(acc0[mp], c0[0], c0[1]);
+            pair_split(acc1[mp], c1[0], c1[1]);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int m = 2 * mp + h;
+                if (m >= g.M) break;
+                float *p0 = cp[0] + static_cast<long long>(m) * ld;
+                float *p1 = cp[1] + static_cast<long long>(m) * ld;
+                p0[0] = read_c ? fmaf(g.beta, p0[0], g.alpha * c0[h]) : g.alpha * c0[h];
+                if (two) p1[0] = read_c ? fmaf(g.beta, p1[0], g.alpha * c1[h]) : g.alpha * c1[h];
+            }
+        }
+        return;
+    }
     const bool pair = ((reinterpret_cast<uintptr_t>(g.C) & 7u) == 0) && ((g.ldc & 1) == 0) && n + 1 < g.N;
     const bool read_c = g.beta != 0.f;
 #pragma unroll
@@ -98,6 +178,7 @@ __device__ __forceinline__ void store_block(const GemmArgs &g, int n, const uint
     }
 }
 
+template <bool CONV>
 __global__ void __launch_bounds__(kThreads, 2) ffma_wide_kernel(const __grid_constant__ GemmArgs g, int vec_b) {
     extern __shared__ __align__(16) float smem_w[];
     const int tid = threadIdx.x;
@@ -114,7 +195,7 @@ __global__ void __launch_bounds__(kThreads, 2) ffma_wide_kernel(const __grid_con
     const int jobs = mine * KC;  // slabs of this CTA, block-major
     auto issue = [&](int q) {
         if (q < jobs)
-            load_slab(g, vec_b != 0, static_cast<int>(blockIdx.x) + (q / KC) * static_cast<int>(gridDim.x), q % KC,
+            load_slab<CONV>(g, vec_b != 0, static_cast<int>(blockIdx.x) + (q / KC) * static_cast<int>(gridDim.x), q % KC,
                       s0 + static_cast<uint32_t>((q % kStages) * kStageFloats * 4), tid);
         cp_async_commit();
     };
@@ -161,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, 2) ffma_wide_kernel(const __grid_con
             }
         }
         const int cb = static_cast<int>(blockIdx.x) + bi * static_cast<int>(gridDim.x);
-        store_block(g, cb * kCols + 2 * tid, acc0, acc1);
+        store_block<CONV>(g, cb * kCols + 2 * tid, acc0, acc1);
 #pragma unroll
         for (int mp = 0; mp < kMaxM / 2; ++mp) acc0[mp] = acc1[mp] = 0ull;
     }
@@ -176,11 +257,11 @@ int ffma_wide_blocks(int N) { return (N + wide::kCols - 1) / wide::kCols; }
 
 int ffma_wide_smem_bytes() { return wide::kSmemBytes; }
 
-cudaError_t ffma_wide_launch(const GemmArgs &g, int vec_b, int grid, cudaStream_t stream) {
-    cudaError_t e =
-        cudaFuncSetAttribute(wide::ffma_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, wide::kSmemBytes);
+cudaError_t ffma_wide_launch(const GemmArgs &g, int vec_b, int grid, cudaStream_t stream, bool conv) {
+    auto kern = conv ? wide::ffma_wide_kernel<true> : wide::ffma_wide_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, wide::kSmemBytes);
     if (e != cudaSuccess) return e;
-    wide::ffma_wide_kernel<<<grid, wide::kThreads, wide::kSmemBytes, stream>>>(g, vec_b);
+    kern<<<grid, wide::kThreads, wide::kSmemBytes, stream>>>(g, vec_b);
     return cudaGetLastError();
 }
 

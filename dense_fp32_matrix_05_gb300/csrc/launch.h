@@ -58,7 +58,8 @@ int plan_tensor_call(int M, int N, int K, const float *A, int lda, const float *
 bool ffma_wide_fits(int M, int K);
 int ffma_wide_blocks(int N);
 int ffma_wide_smem_bytes();
-cudaError_t ffma_wide_launch(const GemmArgs &g, int vec_b, int grid, cudaStream_t stream);
+// conv: the implicit-GEMM convolution form (g.cv; N = images * ldc pixels).
+cudaError_t ffma_wide_launch(const GemmArgs &g, int vec_b, int grid, cudaStream_t stream, bool conv = false);
 
 // dst (cols x rows, leading dimension ldd) = transpose of src (rows x cols,
 // leading dimension lds); row-major fp32.  count matrices, src_stride /

@@ -313,8 +313,12 @@ int sgemm_strided_batched(int transa, int transb, int M, int N, int K, float alp
  *                 OW likewise; must not overlap X or Wt.  beta == 0: Y is
  *                 not read.
  *   stream (19):  as in sgemm.
- *   algo (20):    SGEMM_ALGO_AUTO or SGEMM_ALGO_TF32X3 (3xTF32 tensor path;
- *                 the FFMA path has no convolution form: -20).
+ *   algo (20):    SGEMM_ALGO_TF32X3: the 3xTF32 tensor kernel, producers
+ *                 gathering B.  SGEMM_ALGO_FFMA: the wide-N FFMA kernel's
+ *                 convolution form (resident filter, slabs of the im2col
+ *                 matrix gathered by cp.async), only for F <= 32 and
+ *                 C * KH * KW <= 64 (else -20).  SGEMM_ALGO_AUTO: FFMA for
+ *                 F <= 32 and C * KH * KW <= 48, else TF32X3.
  * Limits: a padded image with its filter reach, times C + 1, below 2^31
  * elements (32-bit offsets in the gather; else -2), OH * OW < 2^31 (else -3).
  * The filter's rows (C * KH * KW floats) are first copied to 16-byte aligned

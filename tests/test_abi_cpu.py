@@ -263,7 +263,8 @@ def test_conv2d_argument_checks(lib):
     assert conv(dw=0) == -13
     assert conv(KH=11, ph=1) == -6                     # dilated filter taller than the padded image
     assert conv(KW=3, dw=5, pw=0) == -7
-    assert conv(algo=pkg.SGEMM_ALGO_FFMA) == -20
+    assert conv(F=33, algo=pkg.SGEMM_ALGO_FFMA) == -20     # the FFMA form takes at most 32 filters
+    assert conv(C=8, algo=pkg.SGEMM_ALGO_FFMA) == -20      # ... and at most 64 taps (8 x 3 x 3 = 72)
     assert conv(algo=7) == -20
     assert conv(x=None) == -15
     assert conv(w=None) == -16

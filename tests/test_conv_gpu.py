@@ -37,7 +37,7 @@ def _inputs(nb, C, H, W, F, KH, KW, seed, relu=False):
     return X, Wt
 
 
-def _run(X, Wt, Y0, alpha, beta, stride, pad, dil, images=None):
+def _run(X, Wt, Y0, alpha, beta, stride, pad, dil, images=None, algo=0):
     """sgemm_conv2d on the device; returns the selected images of Y."""
     import torch
     nb, F, OH, OW = Y0.shape
@@ -47,7 +47,7 @@ def _run(X, Wt, Y0, alpha, beta, stride, pad, dil, images=None):
     buf[GUARD:GUARD + Y0.size] = torch.from_numpy(Y0.reshape(-1)).cuda()
     st = torch.cuda.current_stream()
     rc = pkg.sgemm_conv2d(dX, dW, buf.data_ptr() + GUARD * 4, alpha=alpha, beta=beta, stride=stride, pad=pad,
-                          dil=dil, stream=st, shape=X.shape + Wt.shape[:1] + Wt.shape[2:])
+                          dil=dil, stream=st, shape=X.shape + Wt.shape[:1] + Wt.shape[2:], algo=algo)
     assert rc == 0, rc
     assert pkg.sgemm_check_status(st) == 0
     out = buf.cpu().numpy()
@@ -56,12 +56,12 @@ def _run(X, Wt, Y0, alpha, beta, stride, pad, dil, images=None):
     return Y if images is None else Y[images]
 
 
-def _check(X, Wt, alpha, beta, stride, pad, dil, seed, images=None):
+def _check(X, Wt, alpha, beta, stride, pad, dil, seed, images=None, algo=0):
     nb, C, H, W = X.shape
     F = Wt.shape[0]
     OH, OW = oracle.conv2d_out_size(H, W, Wt.shape[2], Wt.shape[3], stride, pad, dil)
     Y0 = uniform(np.random.default_rng(seed + 1), nb * F * OH * OW).reshape(nb, F, OH, OW)
-    got = _run(X, Wt, Y0, alpha, beta, stride, pad, dil, images)
+    got = _run(X, Wt, Y0, alpha, beta, stride, pad, dil, images, algo)
     sel = slice(None) if images is None else images
     ref, scale = oracle.conv2d_ref(alpha, X[sel], Wt, beta, Y0[sel] if beta != 0 else None, stride, pad, dil)
     msg = oracle.first_failures(got, ref, scale)
@@ -79,38 +79,50 @@ CASES = [
     (1, 64, 31, 31, 200, 4, 4, (1, 1), (0, 0), (1, 1), 1.0, 0.0),    # K = 1024
     (5, 4, 6, 5, 3, 5, 5, (1, 1), (2, 2), (1, 1), 2.0, 0.0),         # image smaller than one tile, 3 filters
     (40, 3, 14, 14, 16, 3, 3, (1, 1), (1, 1), (1, 1), 1.0, 0.5),     # many small images: one launch
+    (3, 7, 9, 10, 32, 3, 3, (2, 1), (0, 2), (1, 2), 1.0, 0.0),       # K = 63, 32 filters: FFMA form fits
+    (2, 2, 37, 41, 5, 5, 3, (1, 3), (2, 1), (2, 1), -1.0, 0.75),     # K = 30, 5 filters, pixels not even
 ]
+# small enough for the FFMA form (F <= 32, K <= 64): run on both paths
+FFMA_FITS = [c for c in CASES if c[4] <= 32 and c[1] * c[5] * c[6] <= 64]
+ALGOS = [("auto", pkg.SGEMM_ALGO_AUTO), ("tf32x3", pkg.SGEMM_ALGO_TF32X3), ("ffma", pkg.SGEMM_ALGO_FFMA)]
 
 
 @pytest.mark.parametrize("case", CASES, ids=[f"b{c[0]}c{c[1]}h{c[2]}w{c[3]}f{c[4]}k{c[5]}x{c[6]}s{c[7][0]}{c[7][1]}"
                                              f"p{c[8][0]}{c[8][1]}d{c[9][0]}{c[9][1]}" for c in CASES])
-def test_conv2d_parity(case):
+@pytest.mark.parametrize("algo", [a for _, a in ALGOS], ids=[n for n, _ in ALGOS])
+def test_conv2d_parity(case, algo):
+    if algo == pkg.SGEMM_ALGO_FFMA and case not in FFMA_FITS:
+        pytest.skip("the FFMA form takes at most 32 filters of 64 taps")
     nb, C, H, W, F, KH, KW, stride, pad, dil, alpha, beta = case
     X, Wt = _inputs(nb, C, H, W, F, KH, KW, seed=sum(case[:7]))
-    _check(X, Wt, alpha, beta, stride, pad, dil, seed=nb * 1000 + F)
+    _check(X, Wt, alpha, beta, stride, pad, dil, seed=nb * 1000 + F, algo=algo)
 
 
 @pytest.mark.parametrize("layer", [(32, 3, 224, 224, 32, 3, 3, 1, 1), (32, 3, 224, 224, 64, 7, 7, 1, 3),
                                    (1, 128, 121, 121, 384, 3, 3, 1, 0)],
                          ids=["32x3x224x224-f32k3", "32x3x224x224-f64k7", "1x128x121x121-f384k3"])
-def test_conv2d_full_size_layers(layer):
+@pytest.mark.parametrize("algo", [pkg.SGEMM_ALGO_AUTO, pkg.SGEMM_ALGO_TF32X3], ids=["auto", "tf32x3"])
+def test_conv2d_full_size_layers(layer, algo):
     """The layers whose im2col GEMMs are the skinny benchmark shapes
     (32 x 1605632 x 27, 64 x 1605632 x 147, 384 x 14161 x 1152), with ReLU'd
     normal inputs; the oracle checks the first and last image."""
     nb, C, H, W, F, KH, KW, s, p = layer
     X, Wt = _inputs(nb, C, H, W, F, KH, KW, seed=F + KH, relu=True)
     images = [0, nb - 1] if nb > 1 else [0]
-    _check(X, Wt, 1.0, 0.0, (s, s), (p, p), (1, 1), seed=7, images=images)
+    _check(X, Wt, 1.0, 0.0, (s, s), (p, p), (1, 1), seed=7, images=images, algo=algo)
 
 
-def test_conv2d_special_values():
+@pytest.mark.parametrize("C,algo", [(4, pkg.SGEMM_ALGO_TF32X3), (16, pkg.SGEMM_ALGO_TF32X3),
+                                    (4, pkg.SGEMM_ALGO_FFMA)], ids=["taps-tf32x3", "channels-tf32x3", "ffma"])
+def test_conv2d_special_values(C, algo):
     """An infinite input pixel gives +-Inf (or NaN where the taps' signs
-    clash) in the outputs that see it, as fp64 arithmetic does; the NaN
-    recompute on the CUDA cores walks the taps of the window."""
-    X, Wt = _inputs(2, 4, 10, 11, 20, 3, 3, seed=91)
+    clash) in the outputs that see it, as fp64 arithmetic does; the tensor
+    path's NaN recompute on the CUDA cores walks the taps of the window in
+    its k order."""
+    X, Wt = _inputs(2, C, 10, 11, 20, 3, 3, seed=91)
     X[0, 1, 4, 5] = np.inf
     X[1, 2, 0, 0] = -np.inf
-    _check(X, Wt, 1.0, 0.0, (1, 1), (1, 1), (1, 1), seed=92)
+    _check(X, Wt, 1.0, 0.0, (1, 1), (1, 1), (1, 1), seed=92, algo=algo)
 
 
 def test_conv2d_alpha_zero_and_no_channels():
