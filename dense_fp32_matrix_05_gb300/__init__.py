@@ -22,7 +22,7 @@ __all__ = [
     "SGEMM_ERR_DEVICE_TIMEOUT",
     "SgemmError", "library", "lib_path", "declared_functions",
     "sgemm", "sgemm_ex", "sgemm_host", "sgemm_plan_info", "sgemm_check_status",
-    "sgemm_status_string", "sgemm_release", "sgemm_version", "sgemm_noalloc", "sgemm_tf32_mma_rate", "sgemm_t", "sgemm_strided_batched", "sgemm_conv2d", "conv2d_out_size", "matmul",
+    "sgemm_status_string", "sgemm_release", "sgemm_version", "sgemm_noalloc", "sgemm_tf32_mma_rate", "sgemm_t", "sgemm_strided_batched", "sgemm_conv2d", "sgemm_conv2d_ex", "SGEMM_CONV_NO_PAD_COPY", "conv2d_out_size", "matmul",
     "SGEMM_ERR_SCRATCH_LIMIT",
 ]
 
@@ -69,6 +69,7 @@ _SIGS = {
                                    _f, _p, _i, ctypes.c_longlong, _i, _p, _i]),
     "sgemm_noalloc": (_i, [_i, _i, _i, _f, _p, _i, _p, _i, _f, _p, _i, _p, _i]),
     "sgemm_conv2d": (_i, [_i] * 13 + [_f, _p, _p, _f, _p, _p, _i]),
+    "sgemm_conv2d_ex": (_i, [_i] * 13 + [_f, _p, _p, _f, _p, _p, _i, _i]),
 }
 
 
@@ -155,17 +156,23 @@ def conv2d_out_size(H, W, KH, KW, stride=(1, 1), pad=(0, 0), dil=(1, 1)):
             (W + 2 * pad[1] - dil[1] * (KW - 1) - 1) // stride[1] + 1)
 
 
+SGEMM_CONV_NO_PAD_COPY = 1
+
+
 def sgemm_conv2d(X, Wt, Y, alpha=1.0, beta=0.0, stride=(1, 1), pad=(0, 0), dil=(1, 1), stream=None,
-                 algo=0, shape=None) -> int:
+                 algo=0, shape=None, flags=None) -> int:
     """Y = alpha * conv2d(X, Wt) + beta * Y; X NCHW, Wt OIHW, Y NCHW, fp32 device tensors
-    (or addresses, with ``shape`` = (nb, C, H, W, F, KH, KW))."""
+    (or addresses, with ``shape`` = (nb, C, H, W, F, KH, KW)).  ``flags`` given: sgemm_conv2d_ex."""
     if shape is None:
         nb, C, H, W = X.shape
         F, _, KH, KW = Wt.shape
     else:
         nb, C, H, W, F, KH, KW = shape
-    return library().sgemm_conv2d(nb, C, H, W, F, KH, KW, stride[0], stride[1], pad[0], pad[1], dil[0], dil[1],
-                                  alpha, _ptr(X), _ptr(Wt), beta, _ptr(Y), _stream(stream), algo)
+    args = (nb, C, H, W, F, KH, KW, stride[0], stride[1], pad[0], pad[1], dil[0], dil[1],
+            alpha, _ptr(X), _ptr(Wt), beta, _ptr(Y), _stream(stream), algo)
+    if flags is None:
+        return library().sgemm_conv2d(*args)
+    return library().sgemm_conv2d_ex(*args, flags)
 
 
 def sgemm_host(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, algo=0) -> int:

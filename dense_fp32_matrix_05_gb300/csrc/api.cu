@@ -620,8 +620,11 @@ int run_batched(int transa, int transb, int M, int N, int K, float alpha, const 
 //    order); a filter whose rows are not 16-byte aligned is copied into rows
 //    padded to 4 floats there.
 // Returns 0, -i for the i-th argument of sgemm_conv2d, or a positive error.
+constexpr long long kPadCopyMaxBytes = 1LL << 30;  // largest zero-bordered input copy a call makes
+
 int run_conv(int nb, int C, int H, int W, int F, int KH, int KW, int sh, int sw, int ph, int pw, int dh, int dw,
-             float alpha, const float *X, const float *Wt, float beta, float *Y, cudaStream_t stream, int algo) {
+             float alpha, const float *X, const float *Wt, float beta, float *Y, cudaStream_t stream, int algo,
+             int flags) {
     if (nb < 0) return -1;
     if (C < 0) return -2;
     if (H < 1) return -3;
@@ -636,6 +639,7 @@ int run_conv(int nb, int C, int H, int W, int F, int KH, int KW, int sh, int sw,
     if (dh < 1) return -12;
     if (dw < 1) return -13;
     if (algo != SGEMM_ALGO_AUTO && algo != SGEMM_ALGO_TF32X3 && algo != SGEMM_ALGO_FFMA) return -20;
+    if (flags & ~SGEMM_CONV_NO_PAD_COPY) return -21;
     const long long span_h = static_cast<long long>(H) + 2LL * ph, span_w = static_cast<long long>(W) + 2LL * pw;
     const long long reach_h = static_cast<long long>(dh) * (KH - 1) + 1, reach_w = static_cast<long long>(dw) * (KW - 1) + 1;
     if (span_h < reach_h) return -6;  // the filter is taller than the padded image
@@ -664,17 +668,35 @@ int run_conv(int nb, int C, int H, int W, int F, int KH, int KW, int sh, int sw,
         return -18;
 
     DevState *d = nullptr;
-    float *wpad = nullptr;
+    float *wpad = nullptr, *xpad = nullptr;
     const int lda = (K + 3) / 4 * 4;
-    const int order = C % 16 == 0 ? sg::kConvChannels : sg::kConvTaps;
-    {
+    // k order: channels at each tap when C % 16 == 0 (tensor path), else the
+    // filter's taps; those gather without bounds checks (a tap table) when
+    // every tap lies in the image: no padding, or a zero-bordered copy
+    int order = (!wide && C % 16 == 0) ? sg::kConvChannels : sg::kConvTaps;
+    const long long pad_elems = (ph || pw) ? static_cast<long long>(nb) * C * span_h * span_w : 0;
+    bool copy_pad = false;
+    if (order == sg::kConvTaps && K <= sg::kConvTabMax &&
+        (pad_elems == 0 ||
+         (!(flags & SGEMM_CONV_NO_PAD_COPY) && pad_elems * static_cast<long long>(sizeof(float)) <= kPadCopyMaxBytes))) {
+        order = sg::kConvTapsDense;
+        copy_pad = pad_elems > 0;
+    }
+    const bool stage_filter = !wide && (order == sg::kConvChannels || !aligned16(Wt, K));
+    const size_t filter_bytes = stage_filter ? (static_cast<size_t>(F) * lda * sizeof(float) + 255) / 256 * 256 : 0;
+    if (use_ab && (filter_bytes > 0 || copy_pad)) {
         std::lock_guard<std::mutex> lk(g_mu);
         int rc = device_state(&d);
         if (rc != 0) return rc;
-        if (use_ab && !wide && (order == sg::kConvChannels || !aligned16(Wt, K))) {
-            rc = get_transpose_ws(*d, stream, static_cast<size_t>(F) * lda * sizeof(float), &wpad);
-            if (rc != 0) return rc;
-        }
+        float *ws = nullptr;
+        rc = get_transpose_ws(*d, stream, filter_bytes + (copy_pad ? pad_elems * sizeof(float) : 0), &ws);
+        if (rc != 0) return rc;
+        if (stage_filter) wpad = ws;
+        if (copy_pad) xpad = ws + filter_bytes / sizeof(float);
+    } else {
+        std::lock_guard<std::mutex> lk(g_mu);
+        const int rc = device_state(&d);
+        if (rc != 0) return rc;
     }
     if (!use_ab) {  // Y = beta * Y, image by image (F x N each)
         if (beta == 1.f) return 0;
@@ -695,16 +717,30 @@ int run_conv(int nb, int C, int H, int W, int F, int KH, int KW, int sh, int sw,
     }
     const float *A = wpad ? wpad : Wt;
     const int ldA = wpad ? lda : K;
+    // the gather's view of the input: the zero-bordered copy, with no padding left
+    const float *Xg = X;
+    long long g_img = img_in;
+    int gH = H, gW = W, gph = ph, gpw = pw;
+    if (copy_pad) {
+        cudaError_t e = sg::pad_planes_launch(X, static_cast<long long>(nb) * C, H, W, ph, pw, xpad, stream);
+        if (e != cudaSuccess) return from_cuda(e);
+        Xg = xpad;
+        gH = static_cast<int>(span_h);
+        gW = static_cast<int>(span_w);
+        gph = gpw = 0;
+        g_img = static_cast<long long>(C) * gH * gW;
+    }
+    const sg::ConvGeom geom{C, gH, gW, static_cast<int>(OW), KH, KW, sh, sw, gph, gpw, dh, dw};
     if (wide) {
         // columns = the pixels of all images of a launch (fewer than 2^31)
         const int imgs = static_cast<int>(std::max(1LL, std::min<long long>(nb, INT32_MAX / Nl)));
         for (int b0 = 0; b0 < nb; b0 += imgs) {
             const int nbc = std::min(imgs, nb - b0);
             const int Nt = nbc * N;
-            GemmArgs g{F, Nt, K, alpha, beta, Wt, K, X + b0 * img_in, 1, Y + b0 * img_out, N, 0, img_in, img_out};
-            g.cv = sg::ConvGeom{C, H, W, static_cast<int>(OW), KH, KW, sh, sw, ph, pw, dh, dw};
+            GemmArgs g{F, Nt, K, alpha, beta, Wt, K, Xg + b0 * g_img, 1, Y + b0 * img_out, N, 0, g_img, img_out};
+            g.cv = geom;
             const int grid = std::min(sg::ffma_wide_blocks(Nt), 2 * d->sms);
-            cudaError_t e = sg::ffma_wide_launch(g, 0, grid, stream, true);
+            cudaError_t e = sg::ffma_wide_launch(g, 0, grid, stream, order);
             if (e != cudaSuccess) return from_cuda(e);
         }
         return 0;
@@ -734,8 +770,8 @@ int run_conv(int nb, int C, int H, int W, int F, int KH, int KW, int sh, int sw,
         }
         float *Yb = Y + b0 * img_out;
         const int vec_c = aligned16(Yb, N) && img_out % 4 == 0;
-        GemmArgs g{F, N, K, alpha, beta, A, ldA, X + b0 * img_in, N, Yb, N, 0, img_in, img_out};
-        g.cv = sg::ConvGeom{C, H, W, static_cast<int>(OW), KH, KW, sh, sw, ph, pw, dh, dw};
+        GemmArgs g{F, N, K, alpha, beta, A, ldA, Xg + b0 * g_img, N, Yb, N, 0, g_img, img_out};
+        g.cv = geom;
         cudaError_t e = sg::tf32x3_conv_launch(p.tile_m, g, p.sch, ctl, order, vec_c, p.grid, stream, nbc);
         if (e != cudaSuccess) return from_cuda(e);
     }
@@ -964,7 +1000,14 @@ int sgemm_conv2d(int nb, int C, int H, int W, int F, int KH, int KW, int stride_
                  int pad_w, int dil_h, int dil_w, float alpha, const float *X, const float *Wt, float beta, float *Y,
                  sgemm_stream_t stream, int algo) {
     return run_conv(nb, C, H, W, F, KH, KW, stride_h, stride_w, pad_h, pad_w, dil_h, dil_w, alpha, X, Wt, beta, Y,
-                    reinterpret_cast<cudaStream_t>(stream), algo);
+                    reinterpret_cast<cudaStream_t>(stream), algo, 0);
+}
+
+int sgemm_conv2d_ex(int nb, int C, int H, int W, int F, int KH, int KW, int stride_h, int stride_w, int pad_h,
+                    int pad_w, int dil_h, int dil_w, float alpha, const float *X, const float *Wt, float beta,
+                    float *Y, sgemm_stream_t stream, int algo, int flags) {
+    return run_conv(nb, C, H, W, F, KH, KW, stride_h, stride_w, pad_h, pad_w, dil_h, dil_w, alpha, X, Wt, beta, Y,
+                    reinterpret_cast<cudaStream_t>(stream), algo, flags);
 }
 
 int sgemm_version(void) { return kVersion; }

@@ -33,7 +33,10 @@ enum : int {
     kConvNone = 0,      // a plain GEMM
     kConvTaps = 1,      // k = (c * KH + kh) * KW + kw (OIHW filter rows)
     kConvChannels = 2,  // k = (kh * KW + kw) * C + c (OHWI filter rows, C % 16 == 0)
+    kConvTapsDense = 3, // kConvTaps with every tap inside the image (no padding, or an input
+                        // copied with zero borders): no bounds checks, tap offsets from a table
 };
+constexpr int kConvTabMax = 2048;  // taps of a kConvTapsDense table (ints in shared memory)
 
 struct ConvGeom {
     int C;       // input channels

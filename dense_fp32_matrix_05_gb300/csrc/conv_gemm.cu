@@ -21,11 +21,12 @@ cudaError_t launch_conv_tm(const GemmArgs &g, const Schedule &s, const DeviceCtl
                            const CUtensorMap &map_a, const CUtensorMap &map_c, cudaStream_t stream) {
     using C = tf32x3::Cfg<TM, false>;
     auto kern = tf32x3::tf32x3_gemm_kernel<TM, true, false, ORDER>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    const int smem = C::kSmemBytes + (ORDER == kConvTapsDense ? C::kConvTabBytes : 0);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     // no B map: the kernel does not read it when TMA_B is false
-    kern<<<grid, tf32x3::Roles<TM, true, false>::kThreads, C::kSmemBytes, stream>>>(g, s, ctl, 1, tma_c, map_a,
-                                                                                      map_a, map_c);
+    kern<<<grid, tf32x3::Roles<TM, true, false>::kThreads, smem, stream>>>(g, s, ctl, 1, tma_c, map_a, map_a,
+                                                                           map_c);
     return cudaGetLastError();
 }
 
@@ -38,6 +39,10 @@ cudaError_t launch_conv_rows(const GemmArgs &g, const Schedule &s, const DeviceC
     if (!make_tmap_a(g, TM, batch, &ma)) return cudaErrorNotSupported;
     const int tc = (vec_c && make_tmap_c(g, batch, &mc)) ? 1 : 0;
     if (order == kConvChannels) return launch_conv_tm<TM, kConvChannels>(g, s, ctl, tc, grid, ma, mc, stream);
+    if (order == kConvTapsDense) {
+        if (g.K > kConvTabMax) return cudaErrorInvalidValue;
+        return launch_conv_tm<TM, kConvTapsDense>(g, s, ctl, tc, grid, ma, mc, stream);
+    }
     return launch_conv_tm<TM, kConvTaps>(g, s, ctl, tc, grid, ma, mc, stream);
 }
 
@@ -57,7 +62,35 @@ __global__ void filter_ohwi_kernel(const float *__restrict__ w, int F, int C, in
     }
 }
 
+// xp = x with zero borders: planes of H x W become (H + 2 ph) x (W + 2 pw),
+// the image at (ph, pw).  One block per destination row at a time, threads
+// along the row, so both sides are coalesced.
+__global__ void pad_planes_kernel(const float *__restrict__ x, long long rows, int H, int W, int ph, int pw,
+                                  float *__restrict__ xp) {
+    const int Hp = H + 2 * ph, Wp = W + 2 * pw;
+    for (long long row = blockIdx.x; row < rows; row += gridDim.x) {
+        const long long plane = row / Hp;
+        const int y = static_cast<int>(row - plane * Hp) - ph;
+        const bool y_in = static_cast<unsigned>(y) < static_cast<unsigned>(H);
+        const float *src = x + (plane * H + (y_in ? y : 0)) * W;
+        float *dst = xp + row * Wp;
+        for (int c = threadIdx.x; c < Wp; c += blockDim.x) {
+            const int sx = c - pw;
+            dst[c] = (y_in && static_cast<unsigned>(sx) < static_cast<unsigned>(W)) ? src[sx] : 0.f;
+        }
+    }
+}
+
 }  // namespace
+
+cudaError_t pad_planes_launch(const float *x, long long planes, int H, int W, int ph, int pw, float *xp,
+                              cudaStream_t stream) {
+    const long long rows = planes * (H + 2LL * ph);
+    if (rows <= 0) return cudaSuccess;
+    pad_planes_kernel<<<static_cast<unsigned>(rows < 16384 ? rows : 16384), 256, 0, stream>>>(x, rows, H, W, ph, pw,
+                                                                                              xp);
+    return cudaGetLastError();
+}
 
 cudaError_t filter_ohwi_launch(const float *w, int F, int C, int KH, int KW, float *dst, long long ld,
                                cudaStream_t stream) {

@@ -24,7 +24,10 @@
 // rows as A).  The columns run over the output pixels of all images
 // (n = image * ldc + pixel, ldc = OH * OW); the slab copies gather B from the
 // input image, 4 bytes each, zero-filled outside it, and C goes to the
-// image's NCHW output (sC floats per image).
+// image's NCHW output (sC floats per image).  kConvTapsDense: every tap lies
+// in the image (no padding, or an input copied with zero borders), so a copy
+// is the column's window origin plus the tap's offset from a table in shared
+// memory, without bounds checks.
 #include <cstdint>
 
 #include "common.cuh"
@@ -41,13 +44,39 @@ constexpr int kKc = 16;              // k rows per slab
 constexpr int kStages = 3;
 constexpr int kStageFloats = kKc * kCols;
 constexpr int kAFloats = kMaxK * kMaxM;  // A^T: row k holds A[0..31][k]
-constexpr int kSmemBytes = (kStages * kStageFloats + kAFloats) * 4;
+constexpr int kSmemBytes = (kStages * kStageFloats + kAFloats + kMaxK) * 4;  // + tap table (kMaxK ints)
 
 // Slab q of this CTA: k rows [kc * 16, +16) of column block cb.
-template <bool CONV>
-__device__ __forceinline__ void load_slab(const GemmArgs &g, bool vec_b, int cb, int kc, uint32_t dst, int tid) {
+template <int CONV>
+__device__ __forceinline__ void load_slab(const GemmArgs &g, bool vec_b, int cb, int kc, uint32_t dst, int tid,
+                                          const int *tab) {
     const int n0 = cb * kCols;
-    if constexpr (CONV) {
+    if constexpr (CONV == kConvTapsDense) {
+        const ConvGeom &cv = g.cv;
+        const float *col[2];
+        bool n_ok[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int n = n0 + tid + h * kThreads;
+            n_ok[h] = n < g.N;
+            const int img = n_ok[h] ? n / static_cast<int>(g.ldc) : 0;
+            const int pix = n_ok[h] ? n - img * static_cast<int>(g.ldc) : 0;
+            const int oh = pix / cv.OW;
+            col[h] = g.B + img * g.sB + (oh * cv.sh * cv.W + (pix - oh * cv.OW) * cv.sw);
+        }
+        const int kb = kc * kKc;
+#pragma unroll 4
+        for (int r = 0; r < kKc; ++r) {
+            const bool k_ok = kb + r < g.K;
+            const int off = tab[kb + r];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const bool ok = k_ok && n_ok[h];
+                cp_async4(dst + static_cast<uint32_t>((r * kCols + tid + h * kThreads) * 4), ok ? col[h] + off : g.B,
+                          ok ? 4u : 0u);
+            }
+        }
+    } else if constexpr (CONV == kConvTaps) {
         // this thread copies columns tid and tid + 256 of every slab row
         const ConvGeom &cv = g.cv;
         const float *col[2];
@@ -118,11 +147,11 @@ __device__ __forceinline__ void load_slab(const GemmArgs &g, bool vec_b, int cb,
 // C[m][n], C[m][n + 1] for the rows m < M of this thread's two columns.
 // CONV: column n is pixel n % ldc of image n / ldc, whose output starts
 // sC floats after the previous image's.
-template <bool CONV>
+template <int CONV>
 __device__ __forceinline__ void store_block(const GemmArgs &g, int n, const uint64_t (&acc0)[16],
                                             const uint64_t (&acc1)[16]) {
     if (n >= g.N) return;
-    if constexpr (CONV) {
+    if constexpr (CONV != kConvNone) {
         const int ld = static_cast<int>(g.ldc);
         float *cp[2];
 #pragma unroll
@@ -178,13 +207,14 @@ __device__ __forceinline__ void store_block(const GemmArgs &g, int n, const uint
     }
 }
 
-template <bool CONV>
+template <int CONV>
 __global__ void __launch_bounds__(kThreads, 2) ffma_wide_kernel(const __grid_constant__ GemmArgs g, int vec_b) {
     extern __shared__ __align__(16) float smem_w[];
     const int tid = threadIdx.x;
     const uint32_t s0 = smem_u32(smem_w);
     const uint32_t sA = s0 + static_cast<uint32_t>(kStages * kStageFloats * 4);
     float *a_t = smem_w + kStages * kStageFloats;
+    int *tab = reinterpret_cast<int *>(a_t + kAFloats);  // tap offsets (kConvTapsDense)
 
     const int KC = (g.K + kKc - 1) / kKc;
     const int nblk = (g.N + kCols - 1) / kCols;
@@ -196,9 +226,18 @@ __global__ void __launch_bounds__(kThreads, 2) ffma_wide_kernel(const __grid_con
     auto issue = [&](int q) {
         if (q < jobs)
             load_slab<CONV>(g, vec_b != 0, static_cast<int>(blockIdx.x) + (q / KC) * static_cast<int>(gridDim.x), q % KC,
-                      s0 + static_cast<uint32_t>((q % kStages) * kStageFloats * 4), tid);
+                      s0 + static_cast<uint32_t>((q % kStages) * kStageFloats * 4), tid, tab);
         cp_async_commit();
     };
+    if constexpr (CONV == kConvTapsDense) {  // tap offsets, needed by the first slab copies
+        const ConvGeom &cv = g.cv;
+        const int khw = cv.KH * cv.KW;
+        for (int k = tid; k < kMaxK; k += kThreads) {
+            const int c = k / khw, r = k - c * khw, kh = r / cv.KW, kw = r - kh * cv.KW;
+            tab[k] = k < g.K ? (c * cv.H + kh * cv.dh) * cv.W + kw * cv.dw : 0;
+        }
+        __syncthreads();
+    }
 #pragma unroll
     for (int q = 0; q < kStages - 1; ++q) issue(q);
 
@@ -257,8 +296,10 @@ int ffma_wide_blocks(int N) { return (N + wide::kCols - 1) / wide::kCols; }
 
 int ffma_wide_smem_bytes() { return wide::kSmemBytes; }
 
-cudaError_t ffma_wide_launch(const GemmArgs &g, int vec_b, int grid, cudaStream_t stream, bool conv) {
-    auto kern = conv ? wide::ffma_wide_kernel<true> : wide::ffma_wide_kernel<false>;
+cudaError_t ffma_wide_launch(const GemmArgs &g, int vec_b, int grid, cudaStream_t stream, int conv) {
+    auto kern = conv == kConvTapsDense ? wide::ffma_wide_kernel<kConvTapsDense>
+                : conv == kConvTaps    ? wide::ffma_wide_kernel<kConvTaps>
+                                       : wide::ffma_wide_kernel<kConvNone>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, wide::kSmemBytes);
     if (e != cudaSuccess) return e;
     kern<<<grid, wide::kThreads, wide::kSmemBytes, stream>>>(g, vec_b);

@@ -21,6 +21,9 @@ int tf32x3_smem_bytes(int tm);
 // 16-byte aligned rows).
 cudaError_t tf32x3_conv_launch(int tm, const GemmArgs &g, const Schedule &s, const DeviceCtl &ctl, int order,
                                int vec_c, int grid, cudaStream_t stream, int batch);
+// planes H x W of x copied into (H + 2 ph) x (W + 2 pw) planes with zero borders.
+cudaError_t pad_planes_launch(const float *x, long long planes, int H, int W, int ph, int pw, float *xp,
+                              cudaStream_t stream);
 // OIHW filter w (F x C x KH x KW) to OHWI rows of leading dimension ld.
 cudaError_t filter_ohwi_launch(const float *w, int F, int C, int KH, int KW, float *dst, long long ld,
                                cudaStream_t stream);
@@ -58,8 +61,9 @@ int plan_tensor_call(int M, int N, int K, const float *A, int lda, const float *
 bool ffma_wide_fits(int M, int K);
 int ffma_wide_blocks(int N);
 int ffma_wide_smem_bytes();
-// conv: the implicit-GEMM convolution form (g.cv; N = images * ldc pixels).
-cudaError_t ffma_wide_launch(const GemmArgs &g, int vec_b, int grid, cudaStream_t stream, bool conv = false);
+// conv: kConvNone, or the implicit-GEMM convolution form kConvTaps /
+// kConvTapsDense (g.cv; N = images * ldc pixels).
+cudaError_t ffma_wide_launch(const GemmArgs &g, int vec_b, int grid, cudaStream_t stream, int conv = kConvNone);
 
 // dst (cols x rows, leading dimension ldd) = transpose of src (rows x cols,
 // leading dimension lds); row-major fp32.  count matrices, src_stride /

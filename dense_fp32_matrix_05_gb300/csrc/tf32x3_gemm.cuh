@@ -147,6 +147,9 @@ struct Cfg {
     static constexpr int kBarBytes = 8 * (3 * kStages + 5 + kEpiBufs) + 4 * (4 + 5 * kMaxDefer);
     static constexpr int kSmemBytes = 1024 + kOffEpi + kEpiBufBytes + kBarBytes;
     static_assert(kSmemBytes <= kSmemLimit, "shared memory per CTA");
+    // a dense convolution's tap table (kConvTabMax ints, 16-byte aligned)
+    static constexpr int kConvTabBytes = kConvTabMax * 4 + 16;
+    static_assert(TMA_B || kSmemBytes + kConvTabBytes <= kSmemLimit, "shared memory with a tap table");
     static_assert(kStages >= 4, "pipeline depth");
 };
 
@@ -201,10 +204,23 @@ struct Raw<0, 0> {};
 // with k.  kConvChannels: k = (kh * KW + kw) * C + c (filter staged OHWI,
 // C a multiple of 16), so the 16 k of a call are 16 channels at one tap:
 // one bounds check, then loads H * W apart, like a plain B column.
+// kConvTapsDense: the kConvTaps order on an input where every tap lies in
+// the image; element (k, n) is the pixel at the column's window origin plus
+// ctab[k] (the tap's offset, a per-CTA table in shared memory).
 template <int TM, int BtK, int GT, int AJ, int CONV = kConvNone>
 __device__ __forceinline__ void load_raw(const GemmArgs &g, bool vec_a, int bi, int m0, int n0, int k0,
-                                         int ptid, Raw<BtK, AJ> &raw) {
-    if constexpr (BtK > 0 && CONV == kConvChannels) {
+                                         int ptid, Raw<BtK, AJ> &raw, const int *ctab = nullptr) {
+    if constexpr (BtK > 0 && CONV == kConvTapsDense) {
+        const ConvGeom &cv = g.cv;
+        const int n = n0 + (ptid & (kTileN - 1));
+        const int kb = k0 + (ptid >> 7) * BtK;
+        const bool n_ok = n < g.N;
+        const int oh = n_ok ? n / cv.OW : 0;
+        const int pix0 = oh * cv.sh * cv.W + (n_ok ? n - oh * cv.OW : 0) * cv.sw;
+        const float *xp = g.B + bi * g.sB + pix0;
+#pragma unroll
+        for (int e = 0; e < BtK; ++e) raw.b[e] = (n_ok && kb + e < g.K) ? __ldg(xp + ctab[kb + e]) : 0.f;
+    } else if constexpr (BtK > 0 && CONV == kConvChannels) {
         const ConvGeom &cv = g.cv;
         const int n = n0 + (ptid & (kTileN - 1));
         const int kb = k0 + (ptid >> 7) * BtK;
@@ -383,7 +399,7 @@ __device__ __noinline__ float recompute_dot(const GemmArgs &g, int bi, int m, in
             }
             if (s != s) break;
         }
-    } else if constexpr (CONV == kConvTaps) {  // k walks the filter taps (c, kh, kw) in order
+    } else if constexpr (CONV == kConvTaps || CONV == kConvTapsDense) {  // k walks the taps (c, kh, kw) in order
         const ConvGeom &cv = g.cv;
         const int oh = n / cv.OW;
         const int ih0 = oh * cv.sh - cv.ph, iw0 = (n - oh * cv.OW) * cv.sw - cv.pw;
@@ -600,8 +616,10 @@ __device__ __forceinline__ void prefetch_c_tile(const GemmArgs &g, int bi, int m
 // swizzle, box 16 x TM); otherwise the producers load A themselves.
 // TMA_B: B rows are 16-byte aligned and tmap_b describes B (N x K, box
 // 128 x 16, no swizzle); otherwise the producers load B^T themselves.
-// CONV: implicit-GEMM convolution (kConvTaps or kConvChannels; B gathered
-// from the input image by the producers, TMA_B false).
+// CONV: implicit-GEMM convolution (kConvTaps, kConvChannels or
+// kConvTapsDense; B gathered from the input image by the producers, TMA_B
+// false).  kConvTapsDense launches with kConvTabBytes more shared memory for
+// the tap table.
 template <int TM, bool TMA_A, bool TMA_B, int CONV = kConvNone>
 __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
     tf32x3_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ Schedule sch,
@@ -631,6 +649,16 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     volatile int *s_ndefer = reinterpret_cast<volatile int *>(tmem_slot + 3);
     volatile int *s_defer = reinterpret_cast<volatile int *>(tmem_slot + 4);  // [kMaxDefer][mt, nt, nseg, slot0, b]
+    // tap offsets of a dense convolution, after the barriers (16-byte aligned)
+    int *ctab = reinterpret_cast<int *>(base_ptr + ((C::kOffEpi + C::kEpiBufBytes + C::kBarBytes + 15) & ~15));
+    if constexpr (CONV == kConvTapsDense) {
+        const ConvGeom &cv = g.cv;
+        const int khw = cv.KH * cv.KW;
+        for (int k = threadIdx.x; k < g.K; k += blockDim.x) {
+            const int c = k / khw, r = k - c * khw, kh = r / cv.KW, kw = r - kh * cv.KW;
+            ctab[k] = (c * cv.H + kh * cv.dh) * cv.W + kw * cv.dw;
+        }
+    }
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -884,7 +912,7 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
         for (int i = 0; i < NB; ++i) {
             if (next.valid(sch)) {
                 load_raw<TM, BtK, GT, AJ, CONV>(g, vec_a != 0, next.b, next.mt * TM, next.nt * kTileN, next.kt * kBK, gt,
-                                          buf[i]);
+                                          buf[i], ctab);
                 for (int t = 0; t < G && next.valid(sch); ++t) next.advance(sch);
                 ++loaded;
             }
@@ -925,7 +953,7 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
                     }
                     if (next.valid(sch)) {
                         load_raw<TM, BtK, GT, AJ, CONV>(g, vec_a != 0, next.b, next.mt * TM, next.nt * kTileN, next.kt * kBK,
-                                                  gt, buf[i]);
+                                                  gt, buf[i], ctab);
                         for (int t = 0; t < G && next.valid(sch); ++t) next.advance(sch);
                         ++loaded;
                     }

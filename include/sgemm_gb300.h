@@ -321,9 +321,12 @@ int sgemm_strided_batched(int transa, int transb, int M, int N, int K, float alp
  *                 F <= 32 and C * KH * KW <= 48, else TF32X3.
  * Limits: a padded image with its filter reach, times C + 1, below 2^31
  * elements (32-bit offsets in the gather; else -2), OH * OW < 2^31 (else -3).
- * The filter's rows (C * KH * KW floats) are first copied to 16-byte aligned
- * rows in a library buffer of this stream (as in sgemm_t) when they are not
- * aligned.  Accuracy and status reporting are those of sgemm_ex with the
+ * The tensor path reads the filter through a tensor map: its rows (C * KH *
+ * KW floats) are first copied to 16-byte aligned rows in a library buffer of
+ * this stream (as in sgemm_t) when they are not aligned, and reordered to
+ * OHWI (k over the channels at each tap) when C is a multiple of 16.  Layers
+ * with padding may also get a zero-bordered copy of the input there (see
+ * sgemm_conv2d_ex).  Accuracy and status reporting are those of sgemm_ex with the
  * TF32X3 path: the same bound per output element, with the sum over the
  * filter taps that fall inside the image.  Returns 0, -i for the i-th
  * argument, a positive cudaError_t, or SGEMM_ERR_WORKSPACE.
@@ -332,6 +335,23 @@ int sgemm_conv2d(int nb, int C, int H, int W, int F, int KH, int KW,
                  int stride_h, int stride_w, int pad_h, int pad_w, int dil_h, int dil_w,
                  float alpha, const float *X, const float *Wt, float beta, float *Y,
                  sgemm_stream_t stream, int algo);
+
+/*
+ * sgemm_conv2d_ex - sgemm_conv2d with flags (21):
+ *   SGEMM_CONV_NO_PAD_COPY: never make the zero-bordered copy of the input.
+ *     For a layer with padding, fewer than 16-multiple channels and at most
+ *     kConvTabMax (2048) taps, the library otherwise copies the input once
+ *     into this stream's transpose buffer, at most 1 GiB, with zero borders,
+ *     so that the gather needs no bounds checks.  With the flag, or above that
+ *     size, the gather checks every tap against the image instead (slower,
+ *     no extra memory).
+ *   Other bits: -21.  Everything else as sgemm_conv2d.
+ */
+#define SGEMM_CONV_NO_PAD_COPY 1
+int sgemm_conv2d_ex(int nb, int C, int H, int W, int F, int KH, int KW,
+                    int stride_h, int stride_w, int pad_h, int pad_w, int dil_h, int dil_w,
+                    float alpha, const float *X, const float *Wt, float beta, float *Y,
+                    sgemm_stream_t stream, int algo, int flags);
 
 /* sgemm_version - library version as 10000*major + 100*minor + patch. */
 int sgemm_version(void);

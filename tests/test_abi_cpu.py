@@ -272,5 +272,6 @@ def test_conv2d_argument_checks(lib):
     assert conv(y=X + 64) == -18                       # Y overlaps X
     assert conv(C=70000, H=200, W_=200) == -2         # 32-bit offsets inside one image
     assert conv(nb=0) == 0 and conv(F=0) == 0
+    assert pkg.sgemm_conv2d(X, W, Y, shape=(2, 3, 8, 8, 4, 3, 3), flags=2) == -21   # unknown flag bit
     assert pkg.conv2d_out_size(224, 224, 7, 7, (2, 2), (3, 3)) == (112, 112)
     assert pkg.conv2d_out_size(10, 9, 3, 2, (1, 2), (0, 1), (2, 3)) == (6, 4)

@@ -37,7 +37,7 @@ def _inputs(nb, C, H, W, F, KH, KW, seed, relu=False):
     return X, Wt
 
 
-def _run(X, Wt, Y0, alpha, beta, stride, pad, dil, images=None, algo=0):
+def _run(X, Wt, Y0, alpha, beta, stride, pad, dil, images=None, algo=0, flags=None):
     """sgemm_conv2d on the device; returns the selected images of Y."""
     import torch
     nb, F, OH, OW = Y0.shape
@@ -47,7 +47,8 @@ def _run(X, Wt, Y0, alpha, beta, stride, pad, dil, images=None, algo=0):
     buf[GUARD:GUARD + Y0.size] = torch.from_numpy(Y0.reshape(-1)).cuda()
     st = torch.cuda.current_stream()
     rc = pkg.sgemm_conv2d(dX, dW, buf.data_ptr() + GUARD * 4, alpha=alpha, beta=beta, stride=stride, pad=pad,
-                          dil=dil, stream=st, shape=X.shape + Wt.shape[:1] + Wt.shape[2:], algo=algo)
+                          dil=dil, stream=st, shape=X.shape + Wt.shape[:1] + Wt.shape[2:], algo=algo,
+                          flags=flags)
     assert rc == 0, rc
     assert pkg.sgemm_check_status(st) == 0
     out = buf.cpu().numpy()
@@ -56,12 +57,12 @@ def _run(X, Wt, Y0, alpha, beta, stride, pad, dil, images=None, algo=0):
     return Y if images is None else Y[images]
 
 
-def _check(X, Wt, alpha, beta, stride, pad, dil, seed, images=None, algo=0):
+def _check(X, Wt, alpha, beta, stride, pad, dil, seed, images=None, algo=0, flags=None):
     nb, C, H, W = X.shape
     F = Wt.shape[0]
     OH, OW = oracle.conv2d_out_size(H, W, Wt.shape[2], Wt.shape[3], stride, pad, dil)
     Y0 = uniform(np.random.default_rng(seed + 1), nb * F * OH * OW).reshape(nb, F, OH, OW)
-    got = _run(X, Wt, Y0, alpha, beta, stride, pad, dil, images, algo)
+    got = _run(X, Wt, Y0, alpha, beta, stride, pad, dil, images, algo, flags)
     sel = slice(None) if images is None else images
     ref, scale = oracle.conv2d_ref(alpha, X[sel], Wt, beta, Y0[sel] if beta != 0 else None, stride, pad, dil)
     msg = oracle.first_failures(got, ref, scale)
@@ -96,6 +97,23 @@ def test_conv2d_parity(case, algo):
     nb, C, H, W, F, KH, KW, stride, pad, dil, alpha, beta = case
     X, Wt = _inputs(nb, C, H, W, F, KH, KW, seed=sum(case[:7]))
     _check(X, Wt, alpha, beta, stride, pad, dil, seed=nb * 1000 + F, algo=algo)
+
+
+PADDED_TAPS = [c for c in CASES if c[1] % 16 != 0 and (c[8][0] or c[8][1])]
+
+
+@pytest.mark.parametrize("case", PADDED_TAPS, ids=[f"b{c[0]}c{c[1]}f{c[4]}k{c[5]}x{c[6]}p{c[8][0]}{c[8][1]}"
+                                                   for c in PADDED_TAPS])
+@pytest.mark.parametrize("algo", [pkg.SGEMM_ALGO_TF32X3, pkg.SGEMM_ALGO_FFMA], ids=["tf32x3", "ffma"])
+def test_conv2d_bounds_checked_gather(case, algo):
+    """Padded layers without the zero-bordered input copy: the gather checks
+    every tap against the image (the path a copy over 1 GiB also takes)."""
+    if algo == pkg.SGEMM_ALGO_FFMA and case not in FFMA_FITS:
+        pytest.skip("the FFMA form takes at most 32 filters of 64 taps")
+    nb, C, H, W, F, KH, KW, stride, pad, dil, alpha, beta = case
+    X, Wt = _inputs(nb, C, H, W, F, KH, KW, seed=sum(case[:7]) + 5)
+    _check(X, Wt, alpha, beta, stride, pad, dil, seed=nb * 1000 + F + 5, algo=algo,
+           flags=pkg.SGEMM_CONV_NO_PAD_COPY)
 
 
 @pytest.mark.parametrize("layer", [(32, 3, 224, 224, 32, 3, 3, 1, 1), (32, 3, 224, 224, 64, 7, 7, 1, 3),
