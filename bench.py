@@ -3,6 +3,9 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload NAME] [--algo auto|ffma|tf32x3] [--shapes-out FILE]
 
+--workload conv...: one implicit-GEMM convolution layer per step
+(sgemm_conv2d; the layers whose im2col GEMMs are the skinny workloads).
+
 One step is one C = alpha*A*B + beta*C call on the workload (default
 square5120: M=N=K=5120, alpha=1, beta=0.5, the size of the overview table of
 "NVIDIA_SGEMM_PRACTICE"), inputs resident in HBM.  Inputs (315 MB) exceed the
@@ -49,7 +52,9 @@ KERNEL_SOURCES = ["dense_fp32_matrix_05_gb300/csrc/tf32x3_gemm.cuh",
                   "dense_fp32_matrix_05_gb300/csrc/ffma_gemm.cuh",
                   "dense_fp32_matrix_05_gb300/csrc/common.cuh",
                   "dense_fp32_matrix_05_gb300/csrc/ptx.cuh",
-                  "dense_fp32_matrix_05_gb300/csrc/ffma_wide.cu"]
+                  "dense_fp32_matrix_05_gb300/csrc/ffma_wide.cu",
+                  "dense_fp32_matrix_05_gb300/csrc/conv_gemm.cu"]
+L2_FLUSH_BYTES = 512 << 20  # written between timed steps of workloads that fit in the 129 MB L2
 
 
 def log(*a):
@@ -425,6 +430,214 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     return result, p
 
 
+def conv_path(layer, algo: str) -> str:
+    """Kernel sgemm_conv2d runs for a layer: the wide FFMA form for at most 32
+    filters of at most 48 taps under AUTO (64 when FFMA is asked for)."""
+    m, _, k = layer.gemm_mnk
+    if algo == "ffma" or (algo == "auto" and m <= 32 and k <= 48):
+        return "ffma_wide"
+    return "tf32x3"
+
+
+def run_conv_ours(args, rank: int, world: int, local_rank: int):
+    """One step = one sgemm_conv2d call over the whole layer (implicit GEMM)."""
+    import torch
+
+    import dense_fp32_matrix_05_gb300 as pkg
+    from dense_fp32_matrix_05_gb300.workloads import CONV_LAYERS, make_conv_inputs
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    from dense_fp32_matrix_05_gb300 import _build_ext
+    _build_ext.build()
+    pkg.library()
+    layer = CONV_LAYERS[args.workload]
+    algo = {"auto": 0, "ffma": 1, "tf32x3": 2}[args.algo]
+    Xh, Wh = make_conv_inputs(layer)
+    X = torch.from_numpy(Xh).to(dev)
+    Wt = torch.from_numpy(Wh).to(dev)
+    oh, ow = layer.out_hw
+    Y = torch.zeros((layer.nb, layer.F, oh, ow), device=dev)
+    stream = torch.cuda.current_stream(dev)
+    M, N, K = layer.gemm_mnk
+    flops = layer.flops
+    st_pad = (layer.stride, layer.stride), (layer.pad, layer.pad)
+    path_name = conv_path(layer, args.algo)
+    # kernels per call: the conv kernel, plus the zero-bordered input copy
+    # (padded layers whose channels are not a multiple of 16) or the OHWI
+    # filter reorder (channels a multiple of 16, tensor path)
+    launches = 1 + int(layer.pad > 0 and layer.C % 16 != 0) + int(path_name == "tf32x3" and layer.C % 16 == 0)
+
+    def step():
+        rc = pkg.sgemm_conv2d(X, Wt, Y, stride=st_pad[0], pad=st_pad[1], stream=stream, algo=algo)
+        if rc != 0:
+            raise pkg.SgemmError("sgemm_conv2d", rc)
+
+    for _ in range(args.warmup):
+        step()
+    st = pkg.sgemm_check_status(stream)
+    if st != 0:
+        raise pkg.SgemmError("warmup", st)
+    flush = layer.compulsory_bytes < 2 * 129e6
+    fbuf = torch.empty(L2_FLUSH_BYTES // 4, device=dev) if flush else None
+    dist = world > 1
+    if dist:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    with ClockSampler(local_rank) as clk:
+        for i in range(args.steps):
+            if flush:
+                fbuf.zero_()
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+    if dist:
+        torch.distributed.barrier()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    total_ms = max_over_ranks(float(np.sum(step_ms)), dev if dist else None)
+    launch_ms = float(np.mean(step_ms))
+    st = pkg.sgemm_check_status(stream)
+    if st != 0:
+        raise pkg.SgemmError("timed region", st)
+    clocks = clk.summary()
+
+    # e2e: pinned host input and filter in, the layer, the output back, every step
+    e2e_steps = max(1, min(args.steps, args.e2e_steps))
+    hX = torch.from_numpy(Xh).pin_memory()
+    hW = torch.from_numpy(Wh).pin_memory()
+    hY = torch.empty(tuple(Y.shape), dtype=torch.float32).pin_memory()
+
+    def host_step():
+        X.copy_(hX, non_blocking=True)
+        Wt.copy_(hW, non_blocking=True)
+        step()
+        hY.copy_(Y, non_blocking=True)
+        torch.cuda.synchronize()
+
+    for _ in range(min(3, args.warmup)):
+        host_step()
+    if dist:
+        torch.distributed.barrier()
+    h0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        host_step()
+    e2e_s = time.perf_counter() - h0
+    if dist:
+        t = torch.tensor([e2e_s], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_s = float(t.item())
+
+    props = torch.cuda.get_device_properties(dev)
+    peaks, peak_src = load_peaks()
+    bound, peak, basis = roofline_peak(1 if path_name == "ffma_wide" else 2, peaks, peak_src,
+                                       props.multi_processor_count)
+    t_compute = flops / (peak * 1e12)
+    t_memory = layer.compulsory_bytes / (peaks["hbm_gbs"] * 1e9)
+    if t_memory > t_compute:
+        bound, peak, unit_r = "hbm", peaks["hbm_gbs"], "GB/s"
+        achieved = layer.compulsory_bytes / (launch_ms * 1e-3) / 1e9
+        basis = f"{peak_src} HBM copy bandwidth {peaks['hbm_gbs']} GB/s (compulsory bytes / call time)"
+    else:
+        unit_r = "TFLOP/s"
+        achieved = flops / (launch_ms * 1e-3) / 1e12
+    value = job_throughput(world, flops, args.steps, total_ms)
+    kernel_name = "ffma_wide_kernel<conv>" if path_name == "ffma_wide" else "tf32x3_gemm_kernel<conv>"
+    result = {
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {
+            "workload": f"{layer.name}: {layer.note()}",
+            "algo": f"{args.algo} -> {path_name} (implicit GEMM, sgemm_conv2d)",
+            "l2": (f"flushed between steps ({L2_FLUSH_BYTES >> 20} MB written, untimed)" if flush else
+                   f"no flush: compulsory bytes {layer.compulsory_bytes / 1e6:.0f} MB vs 129 MB L2"),
+            "parallelism": f"replicas x{world}",
+        },
+        "roofline": {"bound": bound, "achieved": round(achieved, 3), "peak": round(peak, 3), "unit": unit_r,
+                     "frac": round(achieved / peak, 4), "traffic": recorded_traffic(args.workload, path_name),
+                     "peak_basis": basis, "kernel": kernel_name, "launch_ms": round(launch_ms, 5),
+                     "launch_note": "whole sgemm_conv2d call: conv kernel plus any input/filter staging kernel",
+                     "compulsory_bytes": layer.compulsory_bytes,
+                     "hbm_frac_of_measured": round(layer.compulsory_bytes / (launch_ms * 1e-3) /
+                                                   (peaks["hbm_gbs"] * 1e9), 4)},
+        "e2e": {"value": round(world * flops * e2e_steps / e2e_s / 1e12, 3), "unit": UNIT,
+                "h2d_bytes_per_step": int(Xh.nbytes + Wh.nbytes), "d2h_bytes_per_step": int(4 * Y.numel()),
+                "steps": e2e_steps, "api": "sgemm_conv2d with pinned host copies in and out"},
+        "gpu_launches": args.steps * launches,
+        "clocks": clocks,
+    }
+    return result, layer
+
+
+def conv_oracle_sample(layer, target_s: float, threads: int = 0):
+    """Time the conv oracle on the first image and the first f filters,
+    growing f until the call takes target_s; returns (TFLOP/s, f, seconds)."""
+    import oracle
+
+    from dense_fp32_matrix_05_gb300.workloads import make_conv_inputs
+    oracle.build()
+    X, Wt = make_conv_inputs(layer)
+    x0 = np.ascontiguousarray(X[:1])
+    oh, ow = layer.out_hw
+    f = 1
+    while True:
+        t = time.perf_counter()
+        oracle.conv2d_ref(1.0, x0, np.ascontiguousarray(Wt[:f]), stride=(layer.stride,) * 2,
+                          pad=(layer.pad,) * 2, threads=threads)
+        dt = time.perf_counter() - t
+        if dt >= target_s or f >= layer.F:
+            return 2.0 * f * oh * ow * layer.C * layer.KH * layer.KW / dt / 1e12, f, dt
+        f = min(layer.F, max(f + 1, int(f * min(8.0, 1.3 * target_s / max(dt, 1e-3)))))
+
+
+def conv_cpu_baseline(layer, target_s: float):
+    import oracle
+    v, f, dt = conv_oracle_sample(layer, target_s)
+    return {"value": v, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": f"image 0 of {layer.nb}, filters 0..{f - 1} of {layer.F}, all output pixels, "
+                      f"float64 direct convolution (oracle as committed), {dt:.1f} s"}
+
+
+def run_conv_reference(args, world: int):
+    """The reference arm for a convolution layer: the float64 direct
+    convolution oracle on a bounded sample (first image, first f filters)."""
+    import oracle
+
+    from dense_fp32_matrix_05_gb300.workloads import CONV_LAYERS, make_conv_inputs
+    layer = CONV_LAYERS[args.workload]
+    per_step = max(0.02, args.reference_budget_s / max(1, args.warmup + args.steps))
+    _, f, _ = conv_oracle_sample(layer, per_step)
+    X, Wt = make_conv_inputs(layer)
+    x0, w0 = np.ascontiguousarray(X[:1]), np.ascontiguousarray(Wt[:f])
+    oh, ow = layer.out_hw
+
+    def step():
+        oracle.conv2d_ref(1.0, x0, w0, stride=(layer.stride,) * 2, pad=(layer.pad,) * 2)
+
+    for _ in range(args.warmup):
+        step()
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t
+    value = 2.0 * f * oh * ow * layer.C * layer.KH * layer.KW * args.steps / dt / 1e12
+    sample = f"image 0 of {layer.nb}, filters 0..{f - 1} of {layer.F} per step, float64 direct convolution"
+    return {
+        "impl": "reference",
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{layer.name}: {layer.note()}",
+                   "algo": "float64 CPU oracle (the pages publish no GPU code to run here)"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
 def oracle_sample_rate(p, target_s: float, threads: int = 0):
     """Time the oracle on a bounded row sample; returns (TFLOP/s, rows, seconds)."""
     import oracle
@@ -514,19 +727,23 @@ def main():
     if "WORLD_SIZE" not in os.environ:
         world = 1
 
+    from dense_fp32_matrix_05_gb300.workloads import CONV_LAYERS
+    conv = args.workload in CONV_LAYERS
+    if conv and args.trans != "NN":
+        ap.error("--trans applies to GEMM workloads")
     if args.impl == "reference":
         if rank != 0:
             return 0
-        print(json.dumps(run_reference(args, world)), flush=True)
+        print(json.dumps(run_conv_reference(args, world) if conv else run_reference(args, world)), flush=True)
         return 0
 
     if world > 1:
         import torch
         torch.cuda.set_device(local_rank)
         torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
-    result, p = run_ours(args, rank, world, local_rank)
+    result, p = (run_conv_ours if conv else run_ours)(args, rank, world, local_rank)
     if rank == 0 and world == 1:
-        result["cpu_baseline"] = cpu_baseline(p, args.cpu_baseline_s)
+        result["cpu_baseline"] = (conv_cpu_baseline if conv else cpu_baseline)(p, args.cpu_baseline_s)
     elif rank == 0:
         result["cpu_baseline"] = None
     if rank == 0 and args.shapes_out:
@@ -561,6 +778,19 @@ def measure_all(args, local_rank):
             out.write(json.dumps(r) + "\n")
             out.flush()
             log(f"{name} {algo}: {r.get('value')} TFLOP/s, roofline {r.get('roofline', {}).get('frac')}")
+    from dense_fp32_matrix_05_gb300.workloads import CONV_LAYERS
+    for name, layer in CONV_LAYERS.items():
+        a = argparse.Namespace(**vars(args))
+        a.workload, a.algo = name, "auto"
+        a.steps = max(5, min(200, int(2e12 / layer.flops)))
+        a.warmup, a.e2e_steps = 3, 3
+        try:
+            r, _ = run_conv_ours(a, 0, 1, local_rank)
+        except Exception as e:  # keep measuring the rest
+            r = {"workload": name, "algo": "auto", "error": str(e)}
+        out.write(json.dumps(r) + "\n")
+        out.flush()
+        log(f"{name}: {r.get('value')} TFLOP/s, roofline {r.get('roofline', {}).get('frac')}")
     out.close()
 
 

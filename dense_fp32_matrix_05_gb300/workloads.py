@@ -148,3 +148,75 @@ def random_problem(M: int, N: int, K: int, alpha: float = 1.0, beta: float = 0.0
     """Ad-hoc U[-1,1) problem of any shape (used by the shape sweeps of the tests)."""
     w = Workload(f"adhoc{M}x{N}x{K}", M, N, K, alpha, beta, seed)
     return make_problem(w, lda, ldb, ldc, pad_value)
+
+
+# ------------------------------------------------------------ convolutions
+# The layers whose im2col lowering gives the skinny shapes above (M = filters,
+# K = channels * KH * KW, N = images * output pixels).  The pages list only the
+# lowered shapes; these geometries reproduce them exactly (the 64 x 559104 x 147
+# shape has no square-image layer and stays a GEMM workload).  Inputs: X =
+# ReLU(N(0, 1)) (the activations the B operand stands for), the filter
+# U[-1, 1); seeds 20265000 + layer index; X then the filter from one generator.
+
+@dataclass(frozen=True)
+class ConvLayer:
+    name: str
+    nb: int
+    C: int
+    H: int
+    W: int
+    F: int
+    KH: int
+    KW: int
+    stride: int
+    pad: int
+    seed: int
+    gemm: str  # the skinny workload its im2col lowering is
+
+    @property
+    def out_hw(self) -> tuple[int, int]:
+        return ((self.H + 2 * self.pad - self.KH) // self.stride + 1,
+                (self.W + 2 * self.pad - self.KW) // self.stride + 1)
+
+    @property
+    def gemm_mnk(self) -> tuple[int, int, int]:
+        oh, ow = self.out_hw
+        return self.F, self.nb * oh * ow, self.C * self.KH * self.KW
+
+    @property
+    def flops(self) -> float:
+        m, n, k = self.gemm_mnk
+        return 2.0 * m * n * k
+
+    @property
+    def compulsory_bytes(self) -> float:
+        """Input, filter and output once (beta = 0: the output is only written)."""
+        oh, ow = self.out_hw
+        return 4.0 * (self.nb * self.C * self.H * self.W + self.F * self.C * self.KH * self.KW +
+                      self.nb * self.F * oh * ow)
+
+    def note(self) -> str:
+        m, n, k = self.gemm_mnk
+        return (f"conv2d NCHW {self.nb}x{self.C}x{self.H}x{self.W}, {self.F} filters {self.KH}x{self.KW}, "
+                f"stride {self.stride}, pad {self.pad}, alpha=1, beta=0; im2col GEMM {m}x{n}x{k} ({self.gemm})")
+
+
+CONV_LAYERS: dict[str, ConvLayer] = {}
+for _i, (_nb, _c, _h, _w, _f, _k, _s, _p, _g) in enumerate([
+        (32, 3, 224, 224, 32, 3, 1, 1, "skinny32x1605632x27"),
+        (1, 128, 121, 121, 384, 3, 1, 0, "skinny384x14161x1152"),
+        (1, 128, 210, 210, 256, 3, 1, 0, "skinny256x43264x1152"),
+        (32, 3, 224, 224, 64, 7, 1, 3, "skinny64x1605632x147"),
+        (1, 64, 227, 227, 256, 4, 1, 0, "skinny256x50176x1024")]):
+    _name = f"conv{_nb}x{_c}x{_h}x{_w}f{_f}k{_k}p{_p}"
+    CONV_LAYERS[_name] = ConvLayer(_name, _nb, _c, _h, _w, _f, _k, _k, _s, _p, SEED_BASE + 5000 + _i, _g)
+
+
+def make_conv_inputs(layer: ConvLayer | str) -> tuple[np.ndarray, np.ndarray]:
+    """(X, filter) of a convolution layer, float32 NCHW and OIHW."""
+    if isinstance(layer, str):
+        layer = CONV_LAYERS[layer]
+    rng = np.random.default_rng(layer.seed)
+    X = relu_normal(rng, layer.nb * layer.C * layer.H * layer.W).reshape(layer.nb, layer.C, layer.H, layer.W)
+    Wt = uniform(rng, layer.F * layer.C * layer.KH * layer.KW).reshape(layer.F, layer.C, layer.KH, layer.KW)
+    return X, Wt
