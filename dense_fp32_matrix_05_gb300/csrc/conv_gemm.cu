@@ -63,20 +63,29 @@ __global__ void filter_ohwi_kernel(const float *__restrict__ w, int F, int C, in
 }
 
 // xp = x with zero borders: planes of H x W become (H + 2 ph) x (W + 2 pw),
-// the image at (ph, pw).  One block per destination row at a time, threads
-// along the row, so both sides are coalesced.
-__global__ void pad_planes_kernel(const float *__restrict__ x, long long rows, int H, int W, int ph, int pw,
-                                  float *__restrict__ xp) {
+// the image at (ph, pw).  A warp copies one destination row (lanes along it,
+// both sides coalesced), 8 rows per block; a grid-stride loop covers the rest.
+// Four independent loads per lane are in flight before the stores.
+__global__ void __launch_bounds__(256) pad_planes_kernel(const float *__restrict__ x, long long rows, int H, int W,
+                                                         int ph, int pw, float *__restrict__ xp) {
     const int Hp = H + 2 * ph, Wp = W + 2 * pw;
-    for (long long row = blockIdx.x; row < rows; row += gridDim.x) {
+    const int lane = threadIdx.x & 31;
+    for (long long row = blockIdx.x * 8LL + (threadIdx.x >> 5); row < rows; row += gridDim.x * 8LL) {
         const long long plane = row / Hp;
         const int y = static_cast<int>(row - plane * Hp) - ph;
         const bool y_in = static_cast<unsigned>(y) < static_cast<unsigned>(H);
         const float *src = x + (plane * H + (y_in ? y : 0)) * W;
         float *dst = xp + row * Wp;
-        for (int c = threadIdx.x; c < Wp; c += blockDim.x) {
-            const int sx = c - pw;
-            dst[c] = (y_in && static_cast<unsigned>(sx) < static_cast<unsigned>(W)) ? src[sx] : 0.f;
+        for (int c0 = lane; c0 < Wp; c0 += 128) {
+            float v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int sx = c0 + 32 * u - pw;
+                v[u] = (y_in && static_cast<unsigned>(sx) < static_cast<unsigned>(W)) ? __ldg(src + sx) : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (c0 + 32 * u < Wp) dst[c0 + 32 * u] = v[u];
         }
     }
 }
@@ -87,8 +96,9 @@ cudaError_t pad_planes_launch(const float *x, long long planes, int H, int W, in
                               cudaStream_t stream) {
     const long long rows = planes * (H + 2LL * ph);
     if (rows <= 0) return cudaSuccess;
-    pad_planes_kernel<<<static_cast<unsigned>(rows < 16384 ? rows : 16384), 256, 0, stream>>>(x, rows, H, W, ph, pw,
-                                                                                              xp);
+    const long long blocks = (rows + 7) / 8;
+    pad_planes_kernel<<<static_cast<unsigned>(blocks < 8192 ? blocks : 8192), 256, 0, stream>>>(x, rows, H, W, ph,
+                                                                                                pw, xp);
     return cudaGetLastError();
 }
 
