@@ -433,10 +433,13 @@ int get_transpose_ws(DevState &d, cudaStream_t stream, size_t bytes, float **out
 
 // batch > 1: a strided batch in one launch of the 3xTF32 kernel (the caller
 // has checked the strides and that the path is the tensor path).
+// trans_b: B is stored N x K (ldb >= K) and read in place by the 3xTF32
+// kernel's transposed-B form; the caller has checked the arguments, chosen
+// the tensor path, and made sure A and B are 16-byte aligned.
 int run(int M, int N, int K, float alpha, const float *A, int lda, const float *B, int ldb, float beta,
         float *C, int ldc, cudaStream_t stream, int algo, int splits, int flags, int batch = 1, long long sA = 0,
-        long long sB = 0, long long sC = 0) {
-    int rc = check_args(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, algo, splits, flags);
+        long long sB = 0, long long sC = 0, bool trans_b = false) {
+    int rc = trans_b ? 0 : check_args(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, algo, splits, flags);
     if (rc != 0) return rc;
     if (M == 0 || N == 0) return 0;
 
@@ -468,7 +471,11 @@ int run(int M, int N, int K, float alpha, const float *A, int lda, const float *
     }
     GemmArgs g{M, N, K, alpha, beta, A, lda, B, ldb, C, ldc, sA, sB, sC};
     cudaError_t e;
-    if (p.path == SGEMM_ALGO_TF32X3)
+    if (trans_b && (p.path != SGEMM_ALGO_TF32X3 || !p.vec_a || !p.vec_b))
+        return SGEMM_ERR_INTERNAL;
+    if (trans_b)
+        e = sg::tf32x3_launch_tb(p.tile_m, g, p.sch, ctl, p.vec_a, p.vec_c, p.grid, stream, batch);
+    else if (p.path == SGEMM_ALGO_TF32X3)
         e = sg::tf32x3_launch(p.tile_m, g, p.sch, ctl, p.vec_a, p.vec_b, p.vec_c, p.grid, stream, batch);
     else if (p.wide)
         e = sg::ffma_wide_launch(g, p.vec_b, p.grid, stream);
@@ -513,10 +520,19 @@ int run_t(int transa, int transb, int M, int N, int K, float alpha, const float 
     if (!use_ab)  // C = beta * C; A and B are not read
         return run(M, N, K, alpha, nullptr, std::max(1, K), nullptr, std::max(1, N), beta, C, ldc, stream, algo, 0, 0);
     if (!transa && !transb) return run(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream, algo, 0, 0);
-    // A^T copy at offset 0, B^T copy after it on a 256-byte boundary
-    const size_t a_floats = transa ? static_cast<size_t>(M) * K : 0;
+    // A transposed B is read in place (the kernel's transposed-B form) on the
+    // tensor path when B and A (or A's transposed copy) are 16-byte aligned;
+    // otherwise it is copied.  Copies: A^T at offset 0 in rows of K rounded
+    // up to 4 floats (16-byte aligned rows), B^T after it on a 256-byte
+    // boundary in rows of N rounded up to 4.
+    const int K4 = (K + 3) / 4 * 4, N4 = (N + 3) / 4 * 4;
+    const bool fuse_b = transb && resolve_path(M, K, algo, 0) == SGEMM_ALGO_TF32X3 && aligned16(B, ldb) &&
+                        (transa || aligned16(A, lda));
+    if (fuse_b && !transa)
+        return run(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream, algo, 0, 0, 1, 0, 0, 0, true);
+    const size_t a_floats = transa ? static_cast<size_t>(M) * K4 : 0;
     const size_t b_off = (a_floats + 63) / 64 * 64;
-    const size_t floats = b_off + (transb ? static_cast<size_t>(K) * N : 0);
+    const size_t floats = b_off + ((transb && !fuse_b) ? static_cast<size_t>(K) * N4 : 0);
     float *ws = nullptr;
     {
         std::lock_guard<std::mutex> lk(g_mu);
@@ -527,11 +543,14 @@ int run_t(int transa, int transb, int M, int N, int K, float alpha, const float 
         if (rc != 0) return rc;
     }
     cudaError_t e = cudaSuccess;
-    if (transa) e = sg::transpose_launch(A, lda, K, M, ws, K, stream);  // K x M -> M x K
-    if (e == cudaSuccess && transb) e = sg::transpose_launch(B, ldb, N, K, ws + b_off, N, stream);  // N x K -> K x N
+    if (transa) e = sg::transpose_launch(A, lda, K, M, ws, K4, stream);  // K x M -> M x K
+    if (e == cudaSuccess && transb && !fuse_b)
+        e = sg::transpose_launch(B, ldb, N, K, ws + b_off, N4, stream);  // N x K -> K x N
     if (e != cudaSuccess) return from_cuda(e);
-    return run(M, N, K, alpha, transa ? ws : A, transa ? K : lda, transb ? ws + b_off : B, transb ? N : ldb, beta,
-               C, ldc, stream, algo, 0, 0);
+    if (fuse_b)
+        return run(M, N, K, alpha, ws, K4, B, ldb, beta, C, ldc, stream, algo, 0, 0, 1, 0, 0, 0, true);
+    return run(M, N, K, alpha, transa ? ws : A, transa ? K4 : lda, transb ? ws + b_off : B, transb ? N4 : ldb,
+               beta, C, ldc, stream, algo, 0, 0);
 }
 
 // One launch for a whole strided batch on the 3xTF32 path: transposed
@@ -553,26 +572,36 @@ int run_batched_one_launch(int transa, int transb, int M, int N, int K, float al
     if (overlaps(C, c_span, A, a_span) || overlaps(C, c_span, B, b_span)) return 1;
     if (!transa && !transb)
         return run(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream, algo, 0, 0, batch, sA, sB, sC);
-    // transposed copies, each matrix on a 256-byte boundary: A^T (M x K) first, then B^T (K x N)
-    const long long a_str = transa ? (static_cast<long long>(M) * K + 63) / 64 * 64 : 0;
-    const long long b_str = transb ? (static_cast<long long>(K) * N + 63) / 64 * 64 : 0;
+    // a transposed B is read in place when B and A (or A's copy) are 16-byte
+    // aligned, batch strides included (as in run_t)
+    const bool fuse_b = transb && aligned16(B, ldb) && sB % 4 == 0 && (transa || (aligned16(A, lda) && sA % 4 == 0));
+    // transposed copies, each matrix on a 256-byte boundary, rows rounded up
+    // to 4 floats: A^T (M x K) first, then B^T (K x N)
+    const int K4 = (K + 3) / 4 * 4, N4 = (N + 3) / 4 * 4;
+    const long long a_str = transa ? (static_cast<long long>(M) * K4 + 63) / 64 * 64 : 0;
+    const long long b_str = (transb && !fuse_b) ? (static_cast<long long>(K) * N4 + 63) / 64 * 64 : 0;
     const long long b_off = a_str * (transa ? nA : 0);
+    if (fuse_b && !transa)
+        return run(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream, algo, 0, 0, batch, sA, sB, sC, true);
     float *ws = nullptr;
     {
         std::lock_guard<std::mutex> lk(g_mu);
         DevState *d = nullptr;
         int rc = device_state(&d);
         if (rc != 0) return rc;
-        rc = get_transpose_ws(*d, stream, static_cast<size_t>(b_off + b_str * (transb ? nB : 0)) * sizeof(float),
+        rc = get_transpose_ws(*d, stream, static_cast<size_t>(b_off + b_str * (b_str ? nB : 0)) * sizeof(float),
                               &ws);
         if (rc != 0) return rc;
     }
     cudaError_t e = cudaSuccess;
-    if (transa) e = sg::transpose_launch(A, lda, K, M, ws, K, stream, static_cast<int>(nA), sA, a_str);
-    if (e == cudaSuccess && transb)
-        e = sg::transpose_launch(B, ldb, N, K, ws + b_off, N, stream, static_cast<int>(nB), sB, b_str);
+    if (transa) e = sg::transpose_launch(A, lda, K, M, ws, K4, stream, static_cast<int>(nA), sA, a_str);
+    if (e == cudaSuccess && transb && !fuse_b)
+        e = sg::transpose_launch(B, ldb, N, K, ws + b_off, N4, stream, static_cast<int>(nB), sB, b_str);
     if (e != cudaSuccess) return from_cuda(e);
-    return run(M, N, K, alpha, transa ? ws : A, transa ? K : lda, transb ? ws + b_off : B, transb ? N : ldb, beta,
+    if (fuse_b)
+        return run(M, N, K, alpha, ws, K4, B, ldb, beta, C, ldc, stream, algo, 0, 0, batch, sA ? a_str : 0, sB, sC,
+                   true);
+    return run(M, N, K, alpha, transa ? ws : A, transa ? K4 : lda, transb ? ws + b_off : B, transb ? N4 : ldb, beta,
                C, ldc, stream, algo, 0, 0, batch, transa ? (sA ? a_str : 0) : sA, transb ? (sB ? b_str : 0) : sB,
                sC);
 }

@@ -16,6 +16,13 @@ constexpr int kFfmaBK = 16;        // K per FFMA pipeline stage
 bool tf32x3_supported_tm(int tm);
 int tf32x3_stages(int tm);
 int tf32x3_smem_bytes(int tm);
+// B stored transposed (N x K, row stride g.ldb; BLAS transb): the 3xTF32
+// kernel copies B^T slabs by TMA and reads them column by column, with no
+// transpose pass.  A's and B's rows (and batch strides) must be 16-byte
+// aligned; cudaErrorNotSupported if a tensor map cannot be made.
+cudaError_t tf32x3_launch_tb(int tm, const GemmArgs &g, const Schedule &s, const DeviceCtl &ctl, int vec_a,
+                             int vec_c, int grid, cudaStream_t stream, int batch);
+
 // Implicit-GEMM convolution (g.cv; B = the NCHW input, batch = images;
 // order: kConvTaps or kConvChannels; g.A: the filter in that k order with
 // 16-byte aligned rows).

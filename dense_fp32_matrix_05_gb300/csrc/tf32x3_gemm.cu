@@ -95,6 +95,24 @@ bool make_tmap_b(const GemmArgs &g, int batch, CUtensorMap *map) {
 // with row stride ldc * 4 bytes, copied in and out in boxes of 128 (n) x 16
 // (rows) without swizzle; loads fill out-of-range elements with zeros and
 // stores skip them.
+// Tensor map of a transposed B (stored N x K, k innermost, row stride ldb):
+// a K x N tensor copied in boxes of 16 (k) x 128 (n) with the 64-byte
+// swizzle, so that each n row of the slab is one swizzled 64-byte row.
+bool make_tmap_bt(const GemmArgs &g, int batch, CUtensorMap *map) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t nb, sb;
+    if (!batch_dim(g.sB, batch, g.ldb * g.N, nb, sb)) return false;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(g.K), static_cast<cuuint64_t>(g.N), nb};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(g.ldb) * sizeof(float), sb};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(tf32x3::kBK), static_cast<cuuint32_t>(tf32x3::kTileN), 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(g.B), dims, strides,
+                           box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 bool make_tmap_c(const GemmArgs &g, int batch, CUtensorMap *map) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
     if (!enc) return false;

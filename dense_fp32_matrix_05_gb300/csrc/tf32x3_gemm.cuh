@@ -319,7 +319,11 @@ __device__ __forceinline__ void split_store4(uint32_t hi_addr, uint32_t lo_addr,
 // lanes; A hi/lo into the shared-memory stage at `stage`, from registers
 // (AJ > 0) or, after a TMA copy into the hi buffer, lo alone (the raw tile
 // is already a valid hi operand).
-template <int TM, bool TMA_B, int KB, int BtK, int GT, int AJ, int AJ_TMA>
+// TRANS_B: B is stored transposed (N x K, k innermost) and TMA copied the
+// slab as 128 n rows of 16 k (64 bytes, 64-byte swizzle): a thread's column
+// is one row, read as KB / 4 16-byte chunks (the swizzle spreads the 8
+// lanes of each 128-bit load phase over all 32 banks).
+template <int TM, bool TMA_B, int KB, int BtK, int GT, int AJ, int AJ_TMA, bool TRANS_B = false>
 __device__ __forceinline__ void store_split(uint32_t stage, uint32_t ring_taddr, int ptid,
                                             const Raw<BtK, AJ> &raw) {
     using C = Cfg<TM, TMA_B>;
@@ -327,7 +331,22 @@ __device__ __forceinline__ void store_split(uint32_t stage, uint32_t ring_taddr,
         // KB k values of this thread's B^T column: from registers, or from the
         // raw B tile (k rows of 128 floats) that TMA copied into the stage
         uint32_t hi[KB], lo[KB];
-        if constexpr (TMA_B) {
+        if constexpr (TMA_B && TRANS_B) {
+            static_assert(KB % 4 == 0, "whole 16-byte chunks");
+            const uint32_t slab = stage + C::kOffBRaw;
+            const int n = ptid & (kTileN - 1);
+            const int q0 = ((ptid >> 7) * KB) >> 2;  // first 16-byte chunk (4 k) of this thread
+#pragma unroll
+            for (int q = 0; q < KB / 4; ++q) {
+                const float4 v = lds128(slab + sw64_off(n, q0 + q));
+                const float x[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    split_tf32(x[u], hi[4 * q + u], lo[4 * q + u]);
+                    hi[4 * q + u] = __float_as_uint(x[u]);  // raw word: the tensor core drops the low bits
+                }
+            }
+        } else if constexpr (TMA_B) {
             const uint32_t col = stage + C::kOffBRaw + static_cast<uint32_t>((ptid & (kTileN - 1)) * 4);
             const int kb = (ptid >> 7) * KB;
 #pragma unroll
@@ -377,7 +396,8 @@ __device__ __forceinline__ void store_split(uint32_t stage, uint32_t ring_taddr,
 // 3xTF32 split an infinite operand meeting a partner whose lo part is zero
 // gives Inf * 0 = NaN where fp32 arithmetic gives +-Inf, so NaN results are
 // recomputed on the CUDA cores.  Stops early once the sum itself is NaN.
-template <int CONV>
+// TRANS_B: B is stored N x K (element (k, n) at B[n * ldb + k]).
+template <int CONV, bool TRANS_B = false>
 __device__ __noinline__ float recompute_dot(const GemmArgs &g, int bi, int m, int n) {
     const float *a = g.A + bi * g.sA + static_cast<long long>(m) * g.lda;
     float s = 0.f;
@@ -415,6 +435,12 @@ __device__ __noinline__ float recompute_dot(const GemmArgs &g, int bi, int m, in
                     s = fmaf(__ldg(a + k), in ? __ldg(x + static_cast<long long>(ih) * cv.W + iw) : 0.f, s);
                 }
             }
+            if (s != s) break;
+        }
+    } else if constexpr (TRANS_B) {
+        const float *b = g.B + bi * g.sB + static_cast<long long>(n) * g.ldb;
+        for (int k = 0; k < g.K; ++k) {
+            s = fmaf(__ldg(a + k), __ldg(b + k), s);
             if (s != s) break;
         }
     } else {
@@ -511,7 +537,7 @@ __device__ __forceinline__ float fix_lane(const float4 &v, int q) {
     return q == 0 ? v.x : q == 1 ? v.y : q == 2 ? v.z : v.w;
 }
 
-template <int TM, int CONV>
+template <int TM, int CONV, bool TRANS_B>
 __device__ __forceinline__ void fixup_tile(const GemmArgs &g, int bi, const float *wb, int nseg, int m0, int n0,
                                         int wid, int nw, int lane) {
     float *const cmat = g.C + bi * g.sC;  // matrix bi of a batch
@@ -576,7 +602,7 @@ __device__ __forceinline__ void fixup_tile(const GemmArgs &g, int bi, const floa
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 float s = fix_lane(sum[j], q);
-                if (s != s && nc + q < g.N) s = recompute_dot<CONV>(g, bi, m, nc + q);
+                if (s != s && nc + q < g.N) s = recompute_dot<CONV, TRANS_B>(g, bi, m, nc + q);
                 const float a = g.alpha * s;
                 res[q] = read_c ? fmaf(g.beta, fix_lane(old[j], q), a) : a;
             }
@@ -620,7 +646,9 @@ __device__ __forceinline__ void prefetch_c_tile(const GemmArgs &g, int bi, int m
 // kConvTapsDense; B gathered from the input image by the producers, TMA_B
 // false).  kConvTapsDense launches with kConvTabBytes more shared memory for
 // the tap table.
-template <int TM, bool TMA_A, bool TMA_B, int CONV = kConvNone>
+// TRANS_B: B is stored N x K (BLAS transb) and tmap_b describes it as K x N
+// (box 16 x 128, 64-byte swizzle); needs TMA_B.
+template <int TM, bool TMA_A, bool TMA_B, int CONV = kConvNone, bool TRANS_B = false>
 __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
     tf32x3_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ Schedule sch,
                        const __grid_constant__ DeviceCtl ctl, int vec_a, int tma_c,
@@ -629,6 +657,7 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
     using C = Cfg<TM, TMA_B>;
     using R = Roles<TM, TMA_A, TMA_B>;
     static_assert(CONV == kConvNone || !TMA_B, "a convolution gathers B in the producers");
+    static_assert(!TRANS_B || (TMA_B && CONV == kConvNone), "a transposed B comes by TMA");
     constexpr int S = C::kStages;
     constexpr int CH = C::kChunk;
     static_assert(R::kGroups <= S, "a group's next stage must not wrap the ring twice");
@@ -761,7 +790,7 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
                     if (nan && n_ok) {
 #pragma unroll 1
                         for (int j = 0; j < CH; ++j)
-                            if (v[j] != v[j] && mb + j < g.M) v[j] = recompute_dot<CONV>(g, c.b, mb + j, n);
+                            if (v[j] != v[j] && mb + j < g.M) v[j] = recompute_dot<CONV, TRANS_B>(g, c.b, mb + j, n);
                     }
 #pragma unroll
                     for (int j = 0; j < CH; ++j) {
@@ -819,7 +848,7 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
                         // a non-finite input reached this chunk: exact dot products
 #pragma unroll 1
                         for (int j = 0; j < CH; ++j)
-                            if (v[j] != v[j] && mb + j < g.M) v[j] = recompute_dot<CONV>(g, c.b, mb + j, n);
+                            if (v[j] != v[j] && mb + j < g.M) v[j] = recompute_dot<CONV, TRANS_B>(g, c.b, mb + j, n);
                     }
                     if (n_ok) {
                         if (read_c) {
@@ -936,7 +965,7 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    store_split<TM, TMA_B, KB, BtK, GT, AJ, AJ_ALL>(base + s * C::kStageBytes,
+                    store_split<TM, TMA_B, KB, BtK, GT, AJ, AJ_ALL, TRANS_B>(base + s * C::kStageBytes,
                                                          ring_lane + static_cast<uint32_t>(s * kRingColsPerStage),
                                                          gt, buf[i]);
                     fence_proxy_async_smem();
@@ -979,7 +1008,10 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
                     tma_load_3d(base + s * C::kStageBytes + C::kOffAHi, &tmap_a, it.kt * kBK, it.mt * TM,
                                 g.sA != 0 ? it.b : 0,
                                 afull0 + 8u * s);
-                if (TMA_B)
+                if (TMA_B && TRANS_B)
+                    tma_load_3d(base + s * C::kStageBytes + C::kOffBRaw, &tmap_b, it.kt * kBK, it.nt * kTileN,
+                                g.sB != 0 ? it.b : 0, afull0 + 8u * s);
+                else if (TMA_B)
                     tma_load_3d(base + s * C::kStageBytes + C::kOffBRaw, &tmap_b, it.nt * kTileN, it.kt * kBK,
                                 g.sB != 0 ? it.b : 0,
                                 afull0 + 8u * s);
@@ -1065,7 +1097,7 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
         __threadfence();
 #pragma unroll 1
         for (int e = 0; e < nd; ++e)
-            fixup_tile<TM, CONV>(g, s_defer[5 * e + 4], ctl.ws + static_cast<long long>(s_defer[5 * e + 3]) * (kTileN * TM),
+            fixup_tile<TM, CONV, TRANS_B>(g, s_defer[5 * e + 4], ctl.ws + static_cast<long long>(s_defer[5 * e + 3]) * (kTileN * TM),
                            s_defer[5 * e + 2], s_defer[5 * e] * TM, s_defer[5 * e + 1] * kTileN, warp,
                            R::kThreads / 32, lane);
     }

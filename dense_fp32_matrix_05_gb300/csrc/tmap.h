@@ -15,6 +15,9 @@ namespace sg {
 bool make_tmap_a(const GemmArgs &g, int tm, int batch, CUtensorMap *map);
 // B: N x K fp32 (N innermost), box 128 x 16.
 bool make_tmap_b(const GemmArgs &g, int batch, CUtensorMap *map);
+// A transposed B (stored N x K, K innermost) as K x N, box 16 x 128,
+// 64-byte swizzle.
+bool make_tmap_bt(const GemmArgs &g, int batch, CUtensorMap *map);
 // C: N x M fp32 (N innermost), box 128 x 16 (one epilogue chunk).
 bool make_tmap_c(const GemmArgs &g, int batch, CUtensorMap *map);
 

@@ -418,6 +418,42 @@ def test_transposed_operands(shape, trans, algo):
     check_against_oracle(p, dC.cpu().numpy(), what=f"{shape} trans={trans} algo={algo}")
 
 
+FUSED_TB_SHAPES = [(130, 260, 129), (257, 130, 160), (300, 1000, 64), (64, 2000, 147), (1024, 1024, 1024),
+                   (17, 333, 21)]
+
+
+@pytest.mark.parametrize("ta", [0, 1], ids=["NT", "TT"])
+@pytest.mark.parametrize("shape", FUSED_TB_SHAPES, ids=[f"{m}x{n}x{k}" for m, n, k in FUSED_TB_SHAPES])
+def test_transposed_b_read_in_place(shape, ta):
+    """A transposed B with 16-byte rows is read in place by the tensor
+    kernel's transposed-B form (no transpose pass): every element against
+    the oracle, ragged K and N included, and bit for bit the same as the
+    row-major kernel on an explicitly transposed copy of B."""
+    import torch
+
+    M, N, K = shape
+    p = _with_c(random_problem(M, N, K, alpha=1.25, beta=0.5, seed=M * 7 + N + K + ta))
+    pad_a = 4 - (M if ta else K) % 4
+    pad_b = 4 - K % 4  # ldb = K + pad_b: a multiple of 4
+    As, lda = _stored(p.A[:, :K], ta, pad_a)
+    Bs, ldb = _stored(p.B[:, :N], 1, pad_b)
+    assert ldb % 4 == 0
+    dA, dB = torch.from_numpy(As).cuda(), torch.from_numpy(Bs).cuda()
+    dC = torch.from_numpy(p.C.copy()).cuda()
+    st = torch.cuda.current_stream()
+    assert pkg.sgemm_t(ta, 1, M, N, K, p.alpha, dA, lda, dB, ldb, p.beta, dC, p.ldc, st, pkg.SGEMM_ALGO_TF32X3) == 0
+    assert pkg.sgemm_check_status(st) == 0
+    got = dC.cpu().numpy()
+    check_against_oracle(p, got, what=f"{shape} ta={ta} transposed B in place")
+    # the same product with B materialised row-major (K x N, ldb a multiple of 4)
+    Bn, ldn = _stored(p.B[:, :N], 0, 4 - N % 4)
+    dC2 = torch.from_numpy(p.C.copy()).cuda()
+    assert pkg.sgemm_t(ta, 0, M, N, K, p.alpha, dA, lda, torch.from_numpy(Bn).cuda(), ldn, p.beta, dC2, p.ldc, st,
+                       pkg.SGEMM_ALGO_TF32X3) == 0
+    torch.cuda.synchronize()
+    assert np.array_equal(got.view(np.uint32), dC2.cpu().numpy().view(np.uint32)), "transposed-B form differs in bits"
+
+
 @pytest.mark.parametrize("tb", [0, 1], ids=["B", "Bt"])
 def test_strided_batched(tb):
     """A batch of 3 sharing one A (stride 0), with B and C strided past
@@ -459,6 +495,8 @@ BATCH_CASES = [
     (130, 260, 129, 4, 1, 1, False, 1, 0.5),    # both operands transposed
     (130, 260, 129, 4, 1, 0, True, 0, 0.5),     # one transposed A shared by the batch
     (24, 3000, 27, 3, 0, 0, False, 0, 0.5),     # FFMA wide-N shape: matrix by matrix
+    (130, 260, 128, 4, 0, 1, False, 0, 0.5),    # transposed B read in place over the batch
+    (130, 260, 129, 3, 1, 1, True, 0, -1.0),    # transposed shared A copied, transposed B in place
 ]
 
 
