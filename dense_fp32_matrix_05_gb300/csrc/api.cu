@@ -35,10 +35,14 @@ struct Workspace {
     size_t tr_bytes = 0;
 };
 
+constexpr int kHostMaxBlocks = 8;  // row blocks of a pipelined sgemm_host
+
 struct HostBuffers {
     float *A = nullptr, *B = nullptr, *C = nullptr;
     size_t a_bytes = 0, b_bytes = 0, c_bytes = 0;
-    cudaStream_t stream = nullptr;
+    cudaStream_t stream = nullptr;           // GEMMs
+    cudaStream_t up = nullptr, down = nullptr;  // host->device and device->host copies
+    cudaEvent_t b_in = nullptr, in[kHostMaxBlocks] = {}, out[kHostMaxBlocks] = {};
 };
 
 struct DevState {
@@ -837,6 +841,14 @@ int sgemm_host(int M, int N, int K, float alpha, const float *A, int lda, const 
     if (!h.stream) {
         e = cudaStreamCreateWithFlags(&h.stream, cudaStreamNonBlocking);
         if (e != cudaSuccess) return from_cuda(e);
+        if ((e = cudaStreamCreateWithFlags(&h.up, cudaStreamNonBlocking)) != cudaSuccess ||
+            (e = cudaStreamCreateWithFlags(&h.down, cudaStreamNonBlocking)) != cudaSuccess ||
+            (e = cudaEventCreateWithFlags(&h.b_in, cudaEventDisableTiming)) != cudaSuccess)
+            return from_cuda(e);
+        for (int i = 0; i < kHostMaxBlocks; ++i)
+            if ((e = cudaEventCreateWithFlags(&h.in[i], cudaEventDisableTiming)) != cudaSuccess ||
+                (e = cudaEventCreateWithFlags(&h.out[i], cudaEventDisableTiming)) != cudaSuccess)
+                return from_cuda(e);
     }
     const bool use_ab = alpha != 0.f && K > 0;
     const size_t a_bytes = use_ab ? span_bytes(M, K, lda) : 0;
@@ -860,6 +872,112 @@ int sgemm_host(int M, int N, int K, float alpha, const float *A, int lda, const 
     if ((rc = grow(h.A, h.a_bytes, std::max<size_t>(a_bytes, 16))) != 0) return rc;
     if ((rc = grow(h.B, h.b_bytes, std::max<size_t>(b_bytes, 16))) != 0) return rc;
     if ((rc = grow(h.C, h.c_bytes, c_bytes)) != 0) return rc;
+    // Large calls run as row blocks of C, so that copies overlap the GEMMs:
+    // B goes up first, then each block's rows of A (and C when beta != 0) on
+    // the upload stream; a block's GEMM runs once its rows have landed, and
+    // its rows of C come back on the download stream while the next blocks
+    // compute.  Each block is a planned GEMM of its own (the same arithmetic
+    // per element; a block's schedule may differ from the whole call's).
+    const size_t in_bytes = a_bytes + b_bytes + (beta != 0.f ? c_bytes : 0);
+    int nblk = 1;
+    if (in_bytes + c_bytes >= (64u << 20) && M >= 512)
+        nblk = std::min(kHostMaxBlocks, std::max(2, M / 1024));
+    // short and wide (the im2col shapes): column blocks instead; A goes up
+    // first and each block's columns of B (and C) move as pitched copies
+    int ncb = 1;
+    if (nblk == 1 && in_bytes + c_bytes >= (64u << 20) && N >= 8192)
+        ncb = std::min(kHostMaxBlocks, std::max(2, N / 8192));
+    if (ncb > 1) {
+        const int cols = (ceil_div(N, ncb) + 127) / 128 * 128;
+        ncb = ceil_div(N, cols);
+        float *dA = h.A, *dB = h.B, *dC = h.C;
+        cudaStream_t st = h.stream, up = h.up, down = h.down;
+        cudaEvent_t a_in = h.b_in, ev_in[kHostMaxBlocks], ev_out[kHostMaxBlocks];
+        for (int i = 0; i < ncb; ++i) {
+            ev_in[i] = h.in[i];
+            ev_out[i] = h.out[i];
+        }
+        lk.unlock();
+        if (a_bytes && (e = cudaMemcpyAsync(dA, A, a_bytes, cudaMemcpyHostToDevice, up)) != cudaSuccess)
+            return from_cuda(e);
+        if ((e = cudaEventRecord(a_in, up)) != cudaSuccess || (e = cudaStreamWaitEvent(st, a_in, 0)) != cudaSuccess)
+            return from_cuda(e);
+        int first_rc = 0;
+        for (int i = 0; i < ncb; ++i) {
+            const int c0 = i * cols, nc = std::min(cols, N - c0);
+            const size_t w = static_cast<size_t>(nc) * sizeof(float);
+            if (use_ab && (e = cudaMemcpy2DAsync(dB + c0, static_cast<size_t>(ldb) * sizeof(float), B + c0,
+                                                 static_cast<size_t>(ldb) * sizeof(float), w, static_cast<size_t>(K),
+                                                 cudaMemcpyHostToDevice, up)) != cudaSuccess)
+                return from_cuda(e);
+            if (beta != 0.f && (e = cudaMemcpy2DAsync(dC + c0, static_cast<size_t>(ldc) * sizeof(float), C + c0,
+                                                      static_cast<size_t>(ldc) * sizeof(float), w,
+                                                      static_cast<size_t>(M), cudaMemcpyHostToDevice, up)) !=
+                                    cudaSuccess)
+                return from_cuda(e);
+            if ((e = cudaEventRecord(ev_in[i], up)) != cudaSuccess ||
+                (e = cudaStreamWaitEvent(st, ev_in[i], 0)) != cudaSuccess)
+                return from_cuda(e);
+            rc = run(M, nc, K, alpha, use_ab ? dA : nullptr, lda, use_ab ? dB + c0 : nullptr, ldb, beta, dC + c0, ldc,
+                     st, algo, 0, 0);
+            if (rc != 0 && first_rc == 0) first_rc = rc;
+            if ((e = cudaEventRecord(ev_out[i], st)) != cudaSuccess ||
+                (e = cudaStreamWaitEvent(down, ev_out[i], 0)) != cudaSuccess)
+                return from_cuda(e);
+            if ((e = cudaMemcpy2DAsync(C + c0, static_cast<size_t>(ldc) * sizeof(float), dC + c0,
+                                       static_cast<size_t>(ldc) * sizeof(float), w, static_cast<size_t>(M),
+                                       cudaMemcpyDeviceToHost, down)) != cudaSuccess)
+                return from_cuda(e);
+        }
+        e = cudaStreamSynchronize(down);
+        const cudaError_t e2 = cudaStreamSynchronize(st);
+        if (first_rc != 0) return first_rc;
+        return from_cuda(e != cudaSuccess ? e : e2);
+    }
+    if (nblk > 1) {
+        const int rows = (ceil_div(M, nblk) + 255) / 256 * 256;
+        nblk = ceil_div(M, rows);
+        float *dA = h.A, *dB = h.B, *dC = h.C;
+        cudaStream_t st = h.stream, up = h.up, down = h.down;
+        cudaEvent_t b_in = h.b_in, ev_in[kHostMaxBlocks], ev_out[kHostMaxBlocks];
+        for (int i = 0; i < nblk; ++i) {
+            ev_in[i] = h.in[i];
+            ev_out[i] = h.out[i];
+        }
+        lk.unlock();
+        // the previous call's copies and GEMMs on these streams are finished
+        // (it synchronised), so the buffers are free
+        if (b_bytes && (e = cudaMemcpyAsync(dB, B, b_bytes, cudaMemcpyHostToDevice, up)) != cudaSuccess)
+            return from_cuda(e);
+        if ((e = cudaEventRecord(b_in, up)) != cudaSuccess || (e = cudaStreamWaitEvent(st, b_in, 0)) != cudaSuccess)
+            return from_cuda(e);
+        int first_rc = 0;
+        for (int i = 0; i < nblk; ++i) {
+            const int r0 = i * rows, mr = std::min(rows, M - r0);
+            const size_t ao = static_cast<size_t>(r0) * lda, co = static_cast<size_t>(r0) * ldc;
+            const size_t cb = span_bytes(mr, N, ldc);
+            if (use_ab && (e = cudaMemcpyAsync(dA + ao, A + ao, span_bytes(mr, K, lda), cudaMemcpyHostToDevice,
+                                               up)) != cudaSuccess)
+                return from_cuda(e);
+            if (beta != 0.f && (e = cudaMemcpyAsync(dC + co, C + co, cb, cudaMemcpyHostToDevice, up)) != cudaSuccess)
+                return from_cuda(e);
+            if ((e = cudaEventRecord(ev_in[i], up)) != cudaSuccess ||
+                (e = cudaStreamWaitEvent(st, ev_in[i], 0)) != cudaSuccess)
+                return from_cuda(e);
+            rc = run(mr, N, K, alpha, use_ab ? dA + ao : nullptr, lda, use_ab ? dB : nullptr, ldb, beta, dC + co, ldc,
+                     st, algo, 0, 0);
+            if (rc != 0 && first_rc == 0) first_rc = rc;
+            if ((e = cudaEventRecord(ev_out[i], st)) != cudaSuccess ||
+                (e = cudaStreamWaitEvent(down, ev_out[i], 0)) != cudaSuccess)
+                return from_cuda(e);
+            if ((e = cudaMemcpyAsync(C + co, dC + co, cb, cudaMemcpyDeviceToHost, down)) != cudaSuccess)
+                return from_cuda(e);
+        }
+        e = cudaStreamSynchronize(down);
+        const cudaError_t e2 = cudaStreamSynchronize(st);
+        if (first_rc != 0) return first_rc;
+        return from_cuda(e != cudaSuccess ? e : e2);
+    }
     if (a_bytes && (e = cudaMemcpyAsync(h.A, A, a_bytes, cudaMemcpyHostToDevice, h.stream)) != cudaSuccess)
         return from_cuda(e);
     if (b_bytes && (e = cudaMemcpyAsync(h.B, B, b_bytes, cudaMemcpyHostToDevice, h.stream)) != cudaSuccess)

@@ -139,11 +139,23 @@ int sgemm_ex(int M, int N, int K, float alpha,
 /*
  * sgemm_host - C = alpha * A * B + beta * C on HOST buffers, synchronous.
  *
- * A, B, C are host pointers (pinned memory gives full copy bandwidth).  The
- * call copies A, B (and C when beta != 0) to library-owned device buffers on
- * the current device, runs the GEMM, copies C back and waits for completion.
+ * A, B, C are host pointers (pinned memory gives full copy bandwidth and
+ * lets the copies overlap the GEMMs).  The call copies A, B (and C when
+ * beta != 0) to library-owned device buffers on the current device, runs
+ * the GEMM, copies C back and waits for completion.  From 64 MB of traffic
+ * and 512 rows up it runs as 2..8 row blocks of C (256-row multiples): B goes up
+ * first, each block's rows of A (and C) follow on an upload stream, a
+ * block's GEMM starts once its rows have landed, and its rows of C return
+ * on a download stream while later blocks compute.  A call with fewer rows
+ * and at least 8192 columns runs as 2..8 column blocks (128-column
+ * multiples) the same way, with A first and pitched copies of the blocks'
+ * columns of B and C.  Each block is a planned
+ * GEMM of its own, so the schedule, and with it the rounding of each
+ * element's sum, may differ from one sgemm_ex call over the whole matrix
+ * (the accuracy bound is the same).
  * Same argument rules and return codes as sgemm_ex; algo as in sgemm_ex.
  * The device buffers are kept for reuse and freed by sgemm_release().
+ * Calls from several host threads at once race on those buffers.
  */
 int sgemm_host(int M, int N, int K, float alpha,
                const float *A, int lda,

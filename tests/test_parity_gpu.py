@@ -305,6 +305,45 @@ def test_host_entry_point(algo):
     check_against_oracle(p, Cn, what="sgemm_host pageable")
 
 
+@pytest.mark.parametrize("algo", [pkg.SGEMM_ALGO_AUTO, pkg.SGEMM_ALGO_FFMA], ids=["auto", "ffma"])
+def test_host_entry_point_pipelined(algo):
+    """A call over 64 MB runs as row blocks whose copies overlap the GEMMs
+    (here 2 blocks of 1024 and 976 rows, padded leading dimensions): rows
+    on both sides of the block boundary against the oracle, pinned and
+    pageable host buffers."""
+    import torch
+    M, N, K = 2000, 3000, 2500
+    p = _with_c(random_problem(M, N, K, alpha=0.5, beta=-0.75, seed=19, lda=K + 4, ldb=N + 8, ldc=N + 4,
+                               pad_value=0.0))
+    rows = sorted(set(sample_rows(M, 48, seed=3)) | {1022, 1023, 1024, 1025, M - 1})
+    A = torch.from_numpy(p.A).pin_memory()
+    B = torch.from_numpy(p.B).pin_memory()
+    C = torch.from_numpy(p.C.copy()).pin_memory()
+    assert pkg.sgemm_host(M, N, K, p.alpha, A.data_ptr(), p.lda, B.data_ptr(), p.ldb, p.beta, C.data_ptr(),
+                          p.ldc, algo) == 0
+    check_against_oracle(p, C.numpy(), rows=rows, what=f"pipelined sgemm_host algo={algo}")
+    assert np.array_equal(C.numpy()[:, N:].view(np.uint32), p.C[:, N:].view(np.uint32)), "ldc padding written"
+    Cn = p.C.copy()
+    assert pkg.sgemm_host(M, N, K, p.alpha, p.A, p.lda, p.B, p.ldb, p.beta, Cn, p.ldc, algo) == 0
+    assert np.array_equal(Cn.view(np.uint32), C.numpy().view(np.uint32)), "pageable and pinned calls differ"
+
+
+def test_host_entry_point_column_blocks():
+    """A short, wide call over 64 MB runs as column blocks with pitched
+    copies (M = 200, N = 40000, padded ldb / ldc): columns on both sides of
+    the block boundaries against the oracle, padding untouched."""
+    import torch
+    M, N, K = 200, 40000, 700
+    p = _with_c(random_problem(M, N, K, alpha=1.25, beta=0.5, seed=23, ldb=N + 8, ldc=N + 12, pad_value=0.0))
+    A = torch.from_numpy(p.A).pin_memory()
+    B = torch.from_numpy(p.B).pin_memory()
+    C = torch.from_numpy(p.C.copy()).pin_memory()
+    assert pkg.sgemm_host(M, N, K, p.alpha, A.data_ptr(), p.lda, B.data_ptr(), p.ldb, p.beta, C.data_ptr(),
+                          p.ldc, pkg.SGEMM_ALGO_AUTO) == 0
+    check_against_oracle(p, C.numpy(), rows=sample_rows(M, 40, seed=5), what="column-block sgemm_host")
+    assert np.array_equal(C.numpy()[:, N:].view(np.uint32), p.C[:, N:].view(np.uint32)), "ldc padding written"
+
+
 def test_torch_matmul_and_streams():
     import torch
     a = torch.rand(513, 257, device="cuda") - 0.5
