@@ -74,6 +74,13 @@ typedef struct CUstream_st *sgemm_stream_t;
  * planner's run-time estimate prefers whole tiles (for tuning and tests).
  * Ignored with an explicit split count; WHOLE_TILES wins over it. */
 #define SGEMM_FLAG_SPLIT_TAIL 4
+/* SGEMM_FLAG_NO_A_COPY: 3xTF32 path only.  An A whose rows are not 16-byte
+ * aligned (lda % 4 != 0 or a misaligned pointer) and that is far smaller
+ * than B (M * 32 <= N, the im2col shapes) is otherwise copied first,
+ * on the call's stream, into a library buffer with rows padded to 4 floats
+ * (2 * M * K * 4 bytes of traffic), so that its tiles come by TMA.  With the
+ * flag the kernel loads such an A itself.  Both give the same bits. */
+#define SGEMM_FLAG_NO_A_COPY (1 << 16)
 #define SGEMM_FLAG_DEBUG_WITHHOLD_ARRIVE 1 /* test only: one pipeline arrive
                                               is withheld and the on-device
                                               wait budget is cut to ~1 ms, so

@@ -90,13 +90,32 @@ def test_tma_and_load_paths_agree_bitwise(rows):
     p = _with_c(random_problem(M, N, K, alpha=1.0, beta=0.5, seed=rows, pad_value=0.0))
     flags = pkg.SGEMM_FLAG_TILE_ROWS(rows) | pkg.SGEMM_FLAG_WHOLE_TILES
     outs = {}
+    # NO_A_COPY: a misaligned A is loaded by the producers, not staged
     for off in [(0, 0, 0), (1, 0, 0), (0, 1, 0), (1, 1, 0)]:
-        C, st = run_sgemm(p, pkg.SGEMM_ALGO_TF32X3, offsets=off, flags=flags)
+        C, st = run_sgemm(p, pkg.SGEMM_ALGO_TF32X3, offsets=off, flags=flags | pkg.SGEMM_FLAG_NO_A_COPY)
         assert st == 0
         outs[off] = C.view(np.uint32)
     check_against_oracle(p, outs[(0, 0, 0)].view(np.float32), what=f"rows={rows} aligned")
     for off, c in outs.items():
         assert np.array_equal(c, outs[(0, 0, 0)]), f"offsets {off} differ from the TMA path"
+
+
+@pytest.mark.parametrize("shape", [(40, 2000, 147), (64, 4096, 27), (17, 3000, 333)],
+                         ids=["40x2000x147", "64x4096x27", "17x3000x333"])
+def test_unaligned_a_is_staged(shape):
+    """An A with unaligned rows that is far smaller than B is copied to
+    aligned rows and comes by TMA: against the oracle, and bit for bit the
+    same as the producers loading it themselves (SGEMM_FLAG_NO_A_COPY)."""
+    M, N, K = shape
+    p = _with_c(random_problem(M, N, K, alpha=0.75, beta=0.5, seed=M + N, lda=K + (2 if (K + 1) % 4 == 0 else 1),
+                               pad_value=np.nan))
+    assert p.lda % 4 != 0
+    staged, st = run_sgemm(p, pkg.SGEMM_ALGO_TF32X3)
+    assert st == 0
+    check_against_oracle(p, staged, what=f"{shape} staged A")
+    loaded, st = run_sgemm(p, pkg.SGEMM_ALGO_TF32X3, flags=pkg.SGEMM_FLAG_NO_A_COPY)
+    assert st == 0
+    assert np.array_equal(staged.view(np.uint32), loaded.view(np.uint32)), "staged and loaded A differ"
 
 
 TILE_ROWS = [16, 32, 64, 128, 192, 256]
