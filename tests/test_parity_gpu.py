@@ -609,8 +609,10 @@ def test_strided_batched_one_launch(case):
 @pytest.mark.parametrize("shape,algo", [((1024, 1024, 1024), pkg.SGEMM_ALGO_AUTO),
                                         ((300, 5000, 200), pkg.SGEMM_ALGO_TF32X3),
                                         ((24, 3000, 27), pkg.SGEMM_ALGO_AUTO),
-                                        ((257, 130, 160), pkg.SGEMM_ALGO_FFMA)],
-                         ids=["1024-auto", "300x5000x200-tf32x3", "24x3000x27-wide", "257x130x160-ffma"])
+                                        ((257, 130, 160), pkg.SGEMM_ALGO_FFMA),
+                                        ((40, 2000, 147), pkg.SGEMM_ALGO_TF32X3)],
+                         ids=["1024-auto", "300x5000x200-tf32x3", "24x3000x27-wide", "257x130x160-ffma",
+                              "40x2000x147-staged-A"])
 def test_cuda_graph_capture_and_replay(shape, algo):
     """After one call has sized the library's buffers, calls can be captured
     into a CUDA graph on a side stream and replayed (beta = 0, so replays are
@@ -637,4 +639,37 @@ def test_cuda_graph_capture_and_replay(shape, algo):
     torch.cuda.synchronize()
     assert pkg.sgemm_check_status(side) == 0
     check_against_oracle(p, C.cpu().numpy(), what=f"graph {shape} algo={algo}")
+
+
+@pytest.mark.parametrize("layer", [(2, 3, 20, 22, 16, 3, 3, 1), (1, 32, 12, 12, 48, 3, 3, 0),
+                                   (2, 3, 17, 19, 64, 7, 7, 3)],
+                         ids=["wide-ffma-padded", "channels-order", "tap-table-padded"])
+def test_cuda_graph_capture_conv(layer):
+    """sgemm_conv2d calls (filter staging and zero-bordered copies included)
+    captured into a CUDA graph after one sizing call, then replayed."""
+    import torch
+
+    nb, C, H, W, F, KH, KW, pad = layer
+    rng = np.random.default_rng(F + KH)
+    X = (rng.random((nb, C, H, W), dtype=np.float32) * 2 - 1)
+    Wt = (rng.random((F, C, KH, KW), dtype=np.float32) * 2 - 1)
+    OH, OW = oracle.conv2d_out_size(H, W, KH, KW, (1, 1), (pad, pad))
+    dX, dW = torch.from_numpy(X).cuda(), torch.from_numpy(Wt).cuda()
+    Y = torch.full((nb, F, OH, OW), float("nan"), device="cuda")
+    side = torch.cuda.Stream()
+    with torch.cuda.stream(side):
+        assert pkg.sgemm_conv2d(dX, dW, Y, pad=(pad, pad), stream=side) == 0
+    side.synchronize()
+    Y.fill_(float("nan"))
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        for _ in range(2):
+            assert pkg.sgemm_conv2d(dX, dW, Y, pad=(pad, pad), stream=side) == 0
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    assert pkg.sgemm_check_status(side) == 0
+    ref, scale = oracle.conv2d_ref(1.0, X, Wt, pad=(pad, pad))
+    msg = oracle.first_failures(Y.cpu().numpy(), ref, scale)
+    assert not msg, msg
 
