@@ -384,6 +384,79 @@ def test_torch_matmul_and_streams():
     assert not oracle.first_failures(cs.cpu().numpy(), ref, scale)
 
 
+def test_concurrent_calls_from_host_threads():
+    """Four host threads call the library at the same time, each on its own
+    stream, with plans that need the split-K workspace (forced slices, a
+    split tail) or the aligned copy of an unaligned A.  Those buffers belong
+    to a (device, stream) pair, so every thread's result must equal, bit for
+    bit, the same call made alone, which in turn matches the oracle."""
+    import threading
+    import torch
+
+    cases = [  # M, N, K, alpha, beta, algo, forced K slices
+        (300, 700, 2048, 1.0, 0.5, pkg.SGEMM_ALGO_TF32X3, 4),
+        (129, 513, 4096, 1.5, 0.0, pkg.SGEMM_ALGO_TF32X3, 8),
+        (1023, 1021, 1025, 1.0, 1.0, pkg.SGEMM_ALGO_AUTO, 0),
+        (64, 20000, 147, 1.0, 0.0, pkg.SGEMM_ALGO_AUTO, 0),
+        (200, 300, 1000, 2.0, 0.5, pkg.SGEMM_ALGO_FFMA, 3),
+    ]
+    dev = []
+    for i, (M, N, K, alpha, beta, algo, splits) in enumerate(cases):
+        p = random_problem(M, N, K, alpha=alpha, beta=beta, seed=70 + i, pad_value=0.0)
+        A = torch.from_numpy(p.A).cuda()
+        B = torch.from_numpy(p.B).cuda()
+        C0 = torch.from_numpy(p.C).cuda()
+        dev.append((p, A, B, C0, algo, splits))
+
+    def call(i, C, stream):
+        p, A, B, _, algo, splits = dev[i]
+        return pkg.sgemm_ex(p.M, p.N, p.K, p.alpha, A, p.lda, B, p.ldb, p.beta, C, p.ldc, stream, algo,
+                            splits, 0)
+
+    solo = []
+    for i, (p, _, _, C0, _, _) in enumerate(dev):
+        C = C0.clone()
+        st = torch.cuda.current_stream()
+        assert call(i, C, st) == 0
+        assert pkg.sgemm_check_status(st) == 0
+        solo.append(C.cpu().numpy())
+        check_against_oracle(p, solo[-1], what=f"solo {i}")
+
+    reps, errors, outs = 6, [], {}
+
+    def worker(t):
+        try:
+            s = torch.cuda.Stream()
+            mine = []
+            for r in range(reps):
+                i = (t + r) % len(dev)
+                C = dev[i][3].clone()  # the clone is ordered on the current stream, not s
+                s.wait_stream(torch.cuda.current_stream())
+                rc = call(i, C, s)
+                if rc != 0:
+                    errors.append((t, r, rc))
+                    return
+                mine.append((i, C))
+            st = pkg.sgemm_check_status(s)
+            if st != 0:
+                errors.append((t, "status", st))
+            s.synchronize()
+            outs[t] = [(i, C.cpu().numpy()) for i, C in mine]
+        except Exception as e:  # surfaced below
+            errors.append((t, repr(e)))
+
+    threads = [threading.Thread(target=worker, args=(t,)) for t in range(4)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    assert not errors, errors
+    assert sorted(outs) == [0, 1, 2, 3]
+    for t, res in outs.items():
+        for i, C in res:
+            assert np.array_equal(C.view(np.uint32), solo[i].view(np.uint32)), f"thread {t}, case {i}"
+
+
 def test_plan_info_on_device_matches_sm_count():
     import torch
     props = torch.cuda.get_device_properties(0)
