@@ -25,9 +25,8 @@ cudaError_t launch_conv_tm(const GemmArgs &g, const Schedule &s, const DeviceCtl
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     // no B map: the kernel does not read it when TMA_B is false
-    kern<<<grid, tf32x3::Roles<TM, true, false>::kThreads, smem, stream>>>(g, s, ctl, 1, tma_c, map_a, map_a,
-                                                                           map_c);
-    return cudaGetLastError();
+    return launch_pdl(kern, grid, tf32x3::Roles<TM, true, false>::kThreads, smem, stream, g, s, ctl, 1, tma_c, map_a,
+                      map_a, map_c);
 }
 
 template <int TM>

@@ -24,9 +24,8 @@ cudaError_t launch_tb_tm(const GemmArgs &g, const Schedule &s, const DeviceCtl &
     auto kern = tf32x3::tf32x3_gemm_kernel<TM, true, true, kConvNone, true>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    kern<<<grid, tf32x3::Roles<TM, true, true>::kThreads, C::kSmemBytes, stream>>>(g, s, ctl, 1, tma_c, map_a,
-                                                                                     map_b, map_c);
-    return cudaGetLastError();
+    return launch_pdl(kern, grid, tf32x3::Roles<TM, true, true>::kThreads, C::kSmemBytes, stream, g, s, ctl, 1, tma_c,
+                      map_a, map_b, map_c);
 }
 
 template <int TM>

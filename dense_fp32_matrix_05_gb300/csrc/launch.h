@@ -6,6 +6,26 @@
 
 namespace sg {
 
+// Launch with programmatic stream serialization: the kernel may begin while
+// the kernel ahead of it in the stream is finishing, so its on-chip set-up
+// overlaps that kernel's tail.  Only for kernels that call grid_dep_wait()
+// before their first global-memory access (the 3xTF32 kernel).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), int grid, int threads, int smem, cudaStream_t stream,
+                       Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(static_cast<unsigned>(threads));
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<Args &&>(args)...);
+}
+
 // Tile constants the planner needs (checked against the kernels' own).
 constexpr int kTf32x3TileN = 128;  // C columns per 3xTF32 tile
 constexpr int kTf32x3BK = 16;      // K per 3xTF32 pipeline stage

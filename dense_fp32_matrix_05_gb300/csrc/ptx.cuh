@@ -28,6 +28,15 @@ __device__ __forceinline__ void fence_mbar_init() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
 
+// Programmatic dependent launch.  A kernel launched with programmatic
+// stream serialization may start before the kernel ahead of it in the stream
+// has finished; grid_dep_wait() blocks until that kernel has completed and
+// its memory is visible, so it must come before this kernel's first access
+// to global memory.  grid_dep_trigger() lets the next such kernel begin its
+// own launch (it too waits for this one to complete before touching memory).
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile(
         "{\n\t.reg .b64 st;\n\t"

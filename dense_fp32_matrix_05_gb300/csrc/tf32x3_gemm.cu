@@ -138,9 +138,8 @@ cudaError_t launch_tm(const GemmArgs &g, const Schedule &s, const DeviceCtl &ctl
     auto kern = tf32x3::tf32x3_gemm_kernel<TM, TA, TB>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    kern<<<grid, tf32x3::Roles<TM, TA, TB>::kThreads, C::kSmemBytes, stream>>>(g, s, ctl, vec_a, tma_c, map_a,
-                                                                                 map_b, map_c);
-    return cudaGetLastError();
+    return launch_pdl(kern, grid, tf32x3::Roles<TM, TA, TB>::kThreads, C::kSmemBytes, stream, g, s, ctl, vec_a, tma_c,
+                      map_a, map_b, map_c);
 }
 
 // Operands go through TMA whenever their rows are 16-byte aligned: the deep

@@ -716,6 +716,11 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // Everything above is on chip.  Launched after another kernel of this
+    // library, that kernel may still be running: wait for it here, before
+    // any global memory is read or written, then let the next one start.
+    grid_dep_wait();
+    grid_dep_trigger();
 
     if (warp < kEpiWarps) {
         // ------------------------------------------------------ epilogue
