@@ -32,6 +32,10 @@
  *     1e-4 * (|alpha| * sum_k |A[m][k] * B[k][n]| + |beta * C[m][n]|)
  *     of the exact result, on every path.
  *   - Calls from several host threads on different streams are safe.
+ *   - The tensor-core kernels are launched with programmatic stream
+ *     serialization: one may begin its on-chip set-up while the kernel ahead
+ *     of it on the stream finishes, but it reads and writes no global memory
+ *     before that kernel has completed, so stream order is unchanged.
  */
 #ifndef SGEMM_GB300_H
 #define SGEMM_GB300_H
