@@ -457,6 +457,38 @@ def test_concurrent_calls_from_host_threads():
             assert np.array_equal(C.view(np.uint32), solo[i].view(np.uint32)), f"thread {t}, case {i}"
 
 
+@pytest.mark.parametrize("n,splits", [(256, 4), (512, 0), (1024, 2)])
+def test_back_to_back_dependent_calls(n, splits):
+    """A chain of calls enqueued on one stream with no host synchronisation,
+    each reading the previous call's output as its A: Y_{i+1} = Y_i W.  The
+    tensor-core kernels may start while the kernel ahead of them finishes
+    (programmatic dependent launch) and share the stream's split-K
+    workspace, so any access before the predecessor completed would read a
+    stale Y_i or a busy workspace.  An FFMA call in the middle of the chain
+    puts a kernel without that launch mode between two with it.  Every link
+    is checked against the oracle applied to the previous link's result."""
+    import torch
+
+    rng = np.random.default_rng(n + splits)
+    W = (uniform(rng, n * n).reshape(n, n) / np.sqrt(n)).astype(np.float32)
+    X = uniform(rng, n * n).reshape(n, n).astype(np.float32)
+    dW = torch.from_numpy(W).cuda()
+    ys = [torch.from_numpy(X).cuda()] + [torch.empty(n, n, device="cuda") for _ in range(8)]
+    st = torch.cuda.current_stream()
+    torch.cuda.synchronize()
+    for i in range(8):
+        algo = pkg.SGEMM_ALGO_FFMA if i == 4 else pkg.SGEMM_ALGO_TF32X3
+        rc = pkg.sgemm_ex(n, n, n, 1.0, ys[i], n, dW, n, 0.0, ys[i + 1], n, st, algo,
+                          splits if algo == pkg.SGEMM_ALGO_TF32X3 else 0, 0)
+        assert rc == 0
+    assert pkg.sgemm_check_status(st) == 0
+    host = [y.cpu().numpy() for y in ys]
+    for i in range(8):
+        ref, scale = oracle.sgemm_ref(n, n, n, 1.0, host[i], n, W, n, 0.0, None, n)
+        msg = oracle.first_failures(host[i + 1], ref, scale)
+        assert not msg, f"link {i}: {msg}"
+
+
 def test_plan_info_on_device_matches_sm_count():
     import torch
     props = torch.cuda.get_device_properties(0)
