@@ -376,7 +376,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     kernel_name = "ffma_wide_kernel" if plan.get("wide") else f"{path_name}_gemm_kernel"
     if plan.get("wide"):
         path_name = "ffma_wide"
-    traffic = recorded_traffic(args.workload, path_name)
+    # a transposed form runs another kernel instantiation: its own summary, if any
+    traffic = recorded_traffic(args.workload, path_name if args.trans == "NN" else f"{path_name}_{args.trans}")
     value = job_throughput(world, flops, args.steps, total_ms)
 
     result = {
