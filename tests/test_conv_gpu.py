@@ -88,12 +88,19 @@ FFMA_FITS = [c for c in CASES if c[4] <= 32 and c[1] * c[5] * c[6] <= 64]
 ALGOS = [("auto", pkg.SGEMM_ALGO_AUTO), ("tf32x3", pkg.SGEMM_ALGO_TF32X3), ("ffma", pkg.SGEMM_ALGO_FFMA)]
 
 
-@pytest.mark.parametrize("case", CASES, ids=[f"b{c[0]}c{c[1]}h{c[2]}w{c[3]}f{c[4]}k{c[5]}x{c[6]}s{c[7][0]}{c[7][1]}"
-                                             f"p{c[8][0]}{c[8][1]}d{c[9][0]}{c[9][1]}" for c in CASES])
-@pytest.mark.parametrize("algo", [a for _, a in ALGOS], ids=[n for n, _ in ALGOS])
+def _case_id(c):
+    return (f"b{c[0]}c{c[1]}h{c[2]}w{c[3]}f{c[4]}k{c[5]}x{c[6]}s{c[7][0]}{c[7][1]}"
+            f"p{c[8][0]}{c[8][1]}d{c[9][0]}{c[9][1]}")
+
+
+# every case on AUTO and 3xTF32; on FFMA only where its form applies (the
+# library rejects the rest with -20, which test_abi_cpu checks)
+PARITY = [pytest.param(c, a, id=f"{n}-{_case_id(c)}") for n, a in ALGOS for c in CASES
+          if a != pkg.SGEMM_ALGO_FFMA or c in FFMA_FITS]
+
+
+@pytest.mark.parametrize("case,algo", PARITY)
 def test_conv2d_parity(case, algo):
-    if algo == pkg.SGEMM_ALGO_FFMA and case not in FFMA_FITS:
-        pytest.skip("the FFMA form takes at most 32 filters of 64 taps")
     nb, C, H, W, F, KH, KW, stride, pad, dil, alpha, beta = case
     X, Wt = _inputs(nb, C, H, W, F, KH, KW, seed=sum(case[:7]))
     _check(X, Wt, alpha, beta, stride, pad, dil, seed=nb * 1000 + F, algo=algo)
@@ -102,14 +109,15 @@ def test_conv2d_parity(case, algo):
 PADDED_TAPS = [c for c in CASES if c[1] % 16 != 0 and (c[8][0] or c[8][1])]
 
 
-@pytest.mark.parametrize("case", PADDED_TAPS, ids=[f"b{c[0]}c{c[1]}f{c[4]}k{c[5]}x{c[6]}p{c[8][0]}{c[8][1]}"
-                                                   for c in PADDED_TAPS])
-@pytest.mark.parametrize("algo", [pkg.SGEMM_ALGO_TF32X3, pkg.SGEMM_ALGO_FFMA], ids=["tf32x3", "ffma"])
+GATHER = [pytest.param(c, a, id=f"{n}-b{c[0]}c{c[1]}f{c[4]}k{c[5]}x{c[6]}p{c[8][0]}{c[8][1]}")
+          for n, a in (("tf32x3", pkg.SGEMM_ALGO_TF32X3), ("ffma", pkg.SGEMM_ALGO_FFMA)) for c in PADDED_TAPS
+          if a != pkg.SGEMM_ALGO_FFMA or c in FFMA_FITS]
+
+
+@pytest.mark.parametrize("case,algo", GATHER)
 def test_conv2d_bounds_checked_gather(case, algo):
     """Padded layers without the zero-bordered input copy: the gather checks
     every tap against the image (the path a copy over 1 GiB also takes)."""
-    if algo == pkg.SGEMM_ALGO_FFMA and case not in FFMA_FITS:
-        pytest.skip("the FFMA form takes at most 32 filters of 64 taps")
     nb, C, H, W, F, KH, KW, stride, pad, dil, alpha, beta = case
     X, Wt = _inputs(nb, C, H, W, F, KH, KW, seed=sum(case[:7]) + 5)
     _check(X, Wt, alpha, beta, stride, pad, dil, seed=nb * 1000 + F + 5, algo=algo,
