@@ -275,3 +275,75 @@ def test_conv2d_argument_checks(lib):
     assert pkg.sgemm_conv2d(X, W, Y, shape=(2, 3, 8, 8, 4, 3, 3), flags=2) == -21   # unknown flag bit
     assert pkg.conv2d_out_size(224, 224, 7, 7, (2, 2), (3, 3)) == (112, 112)
     assert pkg.conv2d_out_size(10, 9, 3, 2, (1, 2), (0, 1), (2, 3)) == (6, 4)
+
+
+def _walk_units(p, M, N, K, sms):
+    """The 3xTF32 kernel's unit sequence as its schedule documents it, per
+    CTA: split-K units u = cta + i * grid (tile u / S, slice u % S, slice s
+    covering K tiles [s*KT/S, (s+1)*KT/S)); or, with a split tail, whole
+    tiles t = cta + i * grid below the whole waves, then one K slice of a
+    tail tile for each of the first tail * slices CTAs.  Returns the
+    (tile, k tile) pairs of every CTA."""
+    tm, tn = p["tile_m"], p["tile_n"]
+    tiles = -(-M // tm) * -(-N // tn)
+    kt = -(-K // 16)
+    grid = p["grid"]
+    per_cta = [[] for _ in range(grid)]
+    if p["tail_tiles"] == 0:
+        s = p["splits"]
+        for cta in range(grid):
+            for u in range(cta, p["units"], grid):
+                t, sl = divmod(u, s)
+                per_cta[cta].append([(t, k) for k in range(sl * kt // s, (sl + 1) * kt // s)])
+    else:
+        tail = p["tail_tiles"]
+        ts = p["ws_bytes"] // (tail * tm * tn * 4)
+        dp = tiles - tail
+        for cta in range(grid):
+            for t in range(cta, dp, grid):
+                per_cta[cta].append([(t, k) for k in range(kt)])
+            if cta < tail * ts:
+                t, sl = divmod(cta, ts)
+                per_cta[cta].append([(dp + t, k) for k in range(sl * kt // ts, (sl + 1) * kt // ts)])
+    return tiles, kt, per_cta
+
+
+@pytest.mark.parametrize("sms", [152, 148, 132])
+def test_plan_schedules_cover_every_k_tile_once(sms):
+    """Over a spread of shapes, forced split counts and both last-wave
+    treatments, the planner's schedule covers every (tile, k tile) of C
+    exactly once, hands no CTA more than 8 shared tiles (the sums a CTA can
+    defer to its exit), and sizes the workspace to one slot per partial
+    tile; whole-wave schedules run one CTA per SM."""
+    import itertools
+    shapes = [(1, 1, 1), (5, 7, 3), (64, 64, 16), (100, 300, 17), (256, 256, 256), (1023, 1021, 1025),
+              (1024, 1024, 1024), (384, 14161, 1152), (256, 50176, 1024), (64, 559104, 147),
+              (5120, 5120, 5120), (2048, 8192, 64), (130, 4000, 4096), (16, 100000, 512)]
+    variants = [{}, {"splits": 2}, {"splits": 7}, {"splits": 16}, {"flags": pkg.SGEMM_FLAG_WHOLE_TILES},
+                {"flags": pkg.SGEMM_FLAG_SPLIT_TAIL}]
+    checked = 0
+    for (M, N, K), kw in itertools.product(shapes, variants):
+        p = plan(M, N, K, algo=pkg.SGEMM_ALGO_TF32X3, num_sms=sms, **kw)
+        tiles, kt, per_cta = _walk_units(p, M, N, K, sms)
+        seen = {}
+        for units in per_cta:
+            for unit in units:
+                for tk in unit:
+                    seen[tk] = seen.get(tk, 0) + 1
+        assert len(seen) == tiles * kt and set(seen.values()) == {1}, (M, N, K, kw, p)
+        if p["splits"] > 1:  # every unit is a partial tile
+            assert max(len(u) for u in per_cta) <= 8, (M, N, K, kw, p)
+        if p["tail_tiles"] == 0:
+            assert p["units"] == tiles * p["splits"]
+            assert p["ws_bytes"] == (p["units"] * p["tile_m"] * p["tile_n"] * 4 if p["splits"] > 1 else 0)
+            assert 1 <= p["grid"] <= max(p["units"], 1)
+            if p["splits"] == 1:
+                assert p["grid"] == min(p["units"], sms)
+        else:
+            tail = p["tail_tiles"]
+            ts = p["ws_bytes"] // (tail * p["tile_m"] * p["tile_n"] * 4)
+            assert p["grid"] == sms and 0 < tail < sms and (tiles - tail) % sms == 0
+            assert ts >= 2 and tail * ts <= sms and ts <= kt
+            assert p["ws_bytes"] == tail * ts * p["tile_m"] * p["tile_n"] * 4
+        checked += 1
+    assert checked == len(shapes) * len(variants)
