@@ -85,6 +85,12 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
+def profile_name(path_name: str, trans: str = "NN") -> str:
+    """Name of the ncu summary for a path: a transposed form (sgemm_t with
+    NT, TN or TT) runs another kernel instantiation and has its own."""
+    return path_name if trans == "NN" else f"{path_name}_{trans}"
+
+
 def recorded_traffic(workload: str, path_name: str):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on
     the current kernel sources (the summary records their hash)."""
@@ -376,8 +382,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     kernel_name = "ffma_wide_kernel" if plan.get("wide") else f"{path_name}_gemm_kernel"
     if plan.get("wide"):
         path_name = "ffma_wide"
-    # a transposed form runs another kernel instantiation: its own summary, if any
-    traffic = recorded_traffic(args.workload, path_name if args.trans == "NN" else f"{path_name}_{args.trans}")
+    traffic = recorded_traffic(args.workload, profile_name(path_name, args.trans))
     value = job_throughput(world, flops, args.steps, total_ms)
 
     result = {

@@ -1,0 +1,49 @@
+"""Host logic of bench.py that needs no GPU: which committed ncu summary a
+bench line takes its DRAM traffic from, and when it takes none."""
+import os
+
+import pytest
+
+import bench
+
+
+@pytest.fixture
+def fake_root(tmp_path, monkeypatch):
+    (tmp_path / "profiles").mkdir()
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda: "feedc0de12345678")
+    return tmp_path
+
+
+def _summary(root, name, hash_, nbytes):
+    (root / "profiles" / f"{name}.md").write_text(
+        f"# summary\n\nkernel_source_hash: {hash_}\ndram_bytes_per_launch: {nbytes}\n\ntext\n")
+
+
+def test_traffic_comes_from_a_summary_of_the_current_sources(fake_root):
+    _summary(fake_root, "tf32x3_square5120", "feedc0de12345678", 886701824)
+    assert bench.recorded_traffic("square5120", "tf32x3") == 886701824.0
+    assert bench.recorded_traffic("square1024", "tf32x3") is None          # no summary
+    _summary(fake_root, "ffma_square5120", "0123456789abcdef", 1000789504)
+    assert bench.recorded_traffic("square5120", "ffma") is None            # taken on other sources
+
+
+def test_transposed_forms_use_their_own_summary(fake_root):
+    _summary(fake_root, "tf32x3_square5120", "feedc0de12345678", 886701824)
+    assert bench.profile_name("tf32x3") == "tf32x3"
+    assert bench.profile_name("tf32x3", "NT") == "tf32x3_NT"
+    assert bench.recorded_traffic("square5120", bench.profile_name("tf32x3", "TN")) is None
+    _summary(fake_root, "tf32x3_NT_square5120", "feedc0de12345678", 887937024)
+    assert bench.recorded_traffic("square5120", bench.profile_name("tf32x3", "NT")) == 887937024.0
+
+
+def test_committed_summaries_name_their_sources_and_traffic():
+    """Every committed summary records the source hash and the DRAM bytes
+    per launch it was taken with, in the form the lookup reads."""
+    root = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "profiles")
+    names = [n for n in os.listdir(root) if n.endswith(".md")]
+    assert names
+    for n in names:
+        text = open(os.path.join(root, n)).read()
+        assert "kernel_source_hash:" in text and "dram_bytes_per_launch:" in text, n
+        assert "--clock-control none" in text, n
