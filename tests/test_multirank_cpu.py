@@ -1,5 +1,5 @@
 """The N > 1 host path of bench.py on CPU: two gloo ranks (one process per
-GPU on the GPU machine; replicas, no data-path collective)."""
+GPU when run on GPUs; replicas, no data-path collective)."""
 import json
 import os
 import socket
