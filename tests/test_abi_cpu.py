@@ -347,3 +347,19 @@ def test_plan_schedules_cover_every_k_tile_once(sms):
             assert p["ws_bytes"] == tail * ts * p["tile_m"] * p["tile_n"] * 4
         checked += 1
     assert checked == len(shapes) * len(variants)
+
+
+def test_binding_constants_match_the_header():
+    """Every integer constant the header #defines (algorithms, flags, status
+    codes) has the same value in the Python binding."""
+    import re
+    text = open(pkg.HEADER).read()
+    defs = {}
+    for name, expr in re.findall(r"^#define\s+(SGEMM_\w+)\s+(\(?[0-9][0-9 <()]*\)?)", text, re.M):
+        shift = re.fullmatch(r"\(\s*(\d+)\s*<<\s*(\d+)\s*\)", expr.strip())
+        defs[name] = int(shift.group(1)) << int(shift.group(2)) if shift else int(expr)
+    assert len(defs) >= 12
+    for name, value in defs.items():
+        assert hasattr(pkg, name), f"{name} is in the header but not in the binding"
+        assert getattr(pkg, name) == value, f"{name}: header {value}, binding {getattr(pkg, name)}"
+    assert pkg.SGEMM_FLAG_TILE_ROWS(192) == (192 // 16) << 8
