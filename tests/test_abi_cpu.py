@@ -363,3 +363,33 @@ def test_binding_constants_match_the_header():
         assert hasattr(pkg, name), f"{name} is in the header but not in the binding"
         assert getattr(pkg, name) == value, f"{name}: header {value}, binding {getattr(pkg, name)}"
     assert pkg.SGEMM_FLAG_TILE_ROWS(192) == (192 // 16) << 8
+
+
+def test_binding_signatures_match_the_header():
+    """The ctypes argument lists of the binding have one entry per parameter
+    of each prototype in the header, with the matching C type class (int,
+    float, 64-bit integer, pointer or stream), so no argument is marshalled
+    into the wrong slot."""
+    import re
+    text = re.sub(r"/\*.*?\*/", "", open(pkg.HEADER).read(), flags=re.S)
+    protos = dict(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(sgemm\w*)\s*\(([^)]*)\)\s*;", text, flags=re.M))
+    assert set(protos) == set(pkg.declared_functions())
+
+    def kind(param: str) -> str:
+        p = " ".join(param.split())
+        if "*" in p or p.startswith("sgemm_stream_t"):
+            return "ptr"
+        if p.startswith("long long"):
+            return "i64"
+        if p.startswith("float"):
+            return "f32"
+        if p.startswith("int"):
+            return "i32"
+        raise AssertionError(f"unexpected parameter type: {param!r}")
+
+    ct_kind = {ctypes.c_int: "i32", ctypes.c_float: "f32", ctypes.c_longlong: "i64", ctypes.c_void_p: "ptr"}
+    for name, params in protos.items():
+        assert name in pkg._SIGS, f"{name} has no ctypes signature"
+        want = [] if params.strip() in ("", "void") else [kind(p) for p in params.split(",")]
+        got = [ct_kind.get(a, "ptr") for a in pkg._SIGS[name][1]]
+        assert got == want, f"{name}: binding {got}, header {want}"
