@@ -32,6 +32,9 @@
 // a stage through tcgen05.commit) and one or two accumulators in tensor
 // memory (acc_full/acc_empty; with two, a tile's epilogue overlaps the next
 // tile's main loop).  Every wait is bounded (see mbar_wait_bounded).
+// Launched with programmatic stream serialization: barrier set-up and the
+// tensor-memory allocation may run while the previous kernel on the stream
+// finishes; griddepcontrol.wait comes before the first global access.
 //
 // Operand staging follows the shared-memory tiling, vector-load and
 // prefetch ideas of "NVIDIA_SGEMM_PRACTICE" (sections "kernel 2", "kernel 6",
