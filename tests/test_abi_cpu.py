@@ -393,3 +393,29 @@ def test_binding_signatures_match_the_header():
         want = [] if params.strip() in ("", "void") else [kind(p) for p in params.split(",")]
         got = [ct_kind.get(a, "ptr") for a in pkg._SIGS[name][1]]
         assert got == want, f"{name}: binding {got}, header {want}"
+
+
+@pytest.mark.parametrize("sms", [152, 132])
+def test_ffma_plans_cover_every_k_tile_once(sms):
+    """The FFMA path's plans under the same walk: the tiled kernel runs one
+    unit per CTA (split-K slices included), the wide-N kernel strides its
+    CTAs over 512-column blocks with the whole K; every (tile, k tile) is
+    covered once and the split workspace holds one slot per partial tile."""
+    import itertools
+    shapes = [(1, 1, 1), (5, 7, 3), (32, 4096, 27), (32, 1605632, 64), (64, 559104, 147), (100, 300, 17),
+              (1023, 1021, 1025), (1024, 1024, 1024), (5120, 5120, 5120), (129, 257, 4096)]
+    for (M, N, K), splits in itertools.product(shapes, (0, 2, 5)):
+        p = plan(M, N, K, algo=pkg.SGEMM_ALGO_FFMA, splits=splits, num_sms=sms)
+        assert p["path"] == pkg.SGEMM_ALGO_FFMA and p["tail_tiles"] == 0
+        tiles, kt, per_cta = _walk_units(p, M, N, K, sms)
+        seen = {}
+        for units in per_cta:
+            for unit in units:
+                for tk in unit:
+                    seen[tk] = seen.get(tk, 0) + 1
+        assert len(seen) == tiles * kt and set(seen.values()) == {1}, (M, N, K, splits, p)
+        if p["wide"]:
+            assert p["splits"] == 1 and p["grid"] == min(p["units"], 2 * sms) and p["ws_bytes"] == 0
+        else:
+            assert p["grid"] == p["units"] == tiles * p["splits"]
+            assert p["ws_bytes"] == (p["units"] * p["tile_m"] * p["tile_n"] * 4 if p["splits"] > 1 else 0)
