@@ -161,6 +161,18 @@ class ClockSampler:
 
 
 _MMA_RATE = {}
+_FFMA_RATE = {}
+
+
+def ffma_rate(pkg):
+    """fp32 TFLOP/s of packed fma.rn.f32x2 on this GPU (measured once)."""
+    if "v" not in _FFMA_RATE:
+        try:
+            _FFMA_RATE["v"] = pkg.sgemm_ffma_rate(True, 20000)
+        except Exception as exc:  # reported, not fatal: the formula peak stands
+            log(f"FFMA rate probe failed: {exc}")
+            _FFMA_RATE["v"] = None
+    return _FFMA_RATE["v"]
 
 
 def tf32_mma_rate(pkg) -> float:
@@ -214,6 +226,54 @@ def graph_rate(pkg, p, A, B, C, algo: int, flops: float, per_graph: int = 20, re
             "gemms_per_graph": per_graph, "replays": replays}
 
 
+def copy_bound(hA, hB, hC, A, B, C, read_c: bool, stream, reps: int = 5) -> dict:
+    """The host-link floor of one end-to-end step: the same bytes sgemm_host
+    moves (A, B and, when beta != 0, C up; C down), as plain pinned copies
+    timed with CUDA events.  Up and down are timed alone and together on
+    two streams; the floor is the slower direction alone (the step's
+    copies can at best overlap each other and the GEMM)."""
+    import torch
+    down = torch.cuda.Stream()
+
+    def up_copies():
+        A.copy_(hA, non_blocking=True)
+        B.copy_(hB, non_blocking=True)
+        if read_c:
+            C.copy_(hC, non_blocking=True)
+
+    def timed(fn):
+        fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    def down_copy():
+        hC.copy_(C, non_blocking=True)
+
+    def both():
+        down.wait_stream(stream)
+        with torch.cuda.stream(down):
+            hC.copy_(C, non_blocking=True)
+        up_copies()
+        stream.wait_stream(down)
+
+    with torch.cuda.stream(stream):
+        up_ms = timed(up_copies)
+        down_ms = timed(down_copy)
+        both_ms = timed(both)
+    up_b = 4 * (hA.numel() + hB.numel() + (hC.numel() if read_c else 0))
+    down_b = 4 * hC.numel()
+    return {"h2d_ms": round(up_ms, 4), "d2h_ms": round(down_ms, 4), "both_ms": round(both_ms, 4),
+            "h2d_gbs": round(up_b / (up_ms * 1e-3) / 1e9, 1), "d2h_gbs": round(down_b / (down_ms * 1e-3) / 1e9, 1),
+            "copy_bound_ms": round(max(up_ms, down_ms), 4),
+            "note": "pinned cudaMemcpyAsync of the step's bytes; floor = slower direction alone"}
+
+
 def max_over_ranks(local_ms: float, device=None) -> float:
     """The job's time: the largest of the ranks' timed regions (every rank
     calls this; device None means a single process).  The tensor lives on
@@ -242,8 +302,13 @@ def roofline_peak(path: int, peaks: dict, source: str, sms: int):
                 f"x (tf32 1.1 / bf16 2.25 nominal) / 3 MMAs per fp32 product "
                 f"(raw tf32 peak {tf32:.1f} TF/s)")
     mhz = peaks.get("sm_max_mhz", 2070.0)
-    peak = sms * 128 * 2 * mhz * 1e6 / 1e12
-    return ("alu", peak, f"FFMA peak = {sms} SMs x 128 fp32 lanes x 2 flop x {mhz} MHz ({source} max clock)")
+    formula = sms * 128 * 2 * mhz * 1e6 / 1e12
+    measured = ffma_rate(pkg)
+    if measured:
+        return ("alu", measured,
+                f"FFMA peak measured by sgemm_ffma_rate (packed fma.rn.f32x2, 2048 threads x 16 chains per SM): "
+                f"{measured:.1f} TF/s; formula {sms} SMs x 128 fp32 lanes x 2 flop x {mhz} MHz = {formula:.1f}")
+    return ("alu", formula, f"FFMA peak = {sms} SMs x 128 fp32 lanes x 2 flop x {mhz} MHz ({source} max clock)")
 
 
 def run_ours(args, rank: int, world: int, local_rank: int):
@@ -345,6 +410,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         e2e_s = float(t.item())
     h2d = 4 * (p.A.size + p.B.size + (p.C.size if p.beta != 0 else 0))
     d2h = 4 * p.C.size
+    copy = copy_bound(hA, hB, hC, A, B, C, p.beta != 0, stream)
 
     # ---------------------------------------------------------- context: cuBLAS SGEMM
     cublas = None
@@ -419,7 +485,11 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                                                    (peaks["hbm_gbs"] * 1e9), 4)},
         "e2e": {"value": round(world * flops * e2e_steps / e2e_s / 1e12, 3), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-                "api": "sgemm_host (pinned host buffers)"},
+                "api": "sgemm_host (pinned host buffers)",
+                "ms_per_step": round(e2e_s * 1e3 / e2e_steps, 4),
+                "copy_bound_ms": copy["copy_bound_ms"],
+                "frac_of_copy_bound": round(copy["copy_bound_ms"] / (e2e_s * 1e3 / e2e_steps), 4),
+                "copies": copy},
         "gpu_launches": args.steps * (1 + int(ta) + int(tb)),
         "clocks": clocks,
     }

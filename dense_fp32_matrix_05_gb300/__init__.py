@@ -22,7 +22,7 @@ __all__ = [
     "SGEMM_ERR_DEVICE_TIMEOUT",
     "SgemmError", "library", "lib_path", "declared_functions",
     "sgemm", "sgemm_ex", "sgemm_host", "sgemm_plan_info", "sgemm_check_status",
-    "sgemm_status_string", "sgemm_release", "sgemm_version", "sgemm_noalloc", "sgemm_tf32_mma_rate", "sgemm_t", "sgemm_strided_batched", "sgemm_conv2d", "sgemm_conv2d_ex", "SGEMM_CONV_NO_PAD_COPY", "conv2d_out_size", "matmul",
+    "sgemm_status_string", "sgemm_release", "sgemm_version", "sgemm_noalloc", "sgemm_noalloc_debug_flags", "sgemm_tf32_mma_rate", "sgemm_ffma_rate", "sgemm_t", "sgemm_strided_batched", "sgemm_conv2d", "sgemm_conv2d_ex", "SGEMM_CONV_NO_PAD_COPY", "conv2d_out_size", "matmul",
     "SGEMM_ERR_SCRATCH_LIMIT",
 ]
 
@@ -64,10 +64,12 @@ _SIGS = {
     "sgemm_release": (_i, []),
     "sgemm_version": (_i, []),
     "sgemm_tf32_mma_rate": (_i, [_i, _i, _p, ctypes.POINTER(ctypes.c_double)]),
+    "sgemm_ffma_rate": (_i, [_i, _i, _p, ctypes.POINTER(ctypes.c_double)]),
     "sgemm_t": (_i, [_i, _i, _i, _i, _i, _f, _p, _i, _p, _i, _f, _p, _i, _p, _i]),
     "sgemm_strided_batched": (_i, [_i, _i, _i, _i, _i, _f, _p, _i, ctypes.c_longlong, _p, _i, ctypes.c_longlong,
                                    _f, _p, _i, ctypes.c_longlong, _i, _p, _i]),
     "sgemm_noalloc": (_i, [_i, _i, _i, _f, _p, _i, _p, _i, _f, _p, _i, _p, _i]),
+    "sgemm_noalloc_debug_flags": (_i, [_i]),
     "sgemm_conv2d": (_i, [_i] * 13 + [_f, _p, _p, _f, _p, _p, _i]),
     "sgemm_conv2d_ex": (_i, [_i] * 13 + [_f, _p, _p, _f, _p, _p, _i, _i]),
 }
@@ -224,6 +226,15 @@ def sgemm_tf32_mma_rate(n: int = 256, iters: int = 20000, stream=None) -> float:
     return out.value
 
 
+def sgemm_ffma_rate(packed: bool = True, iters: int = 20000, stream=None) -> float:
+    """fp32 FMA TFLOP/s of the CUDA cores (packed fma.rn.f32x2 or scalar)."""
+    out = ctypes.c_double(0.0)
+    rc = library().sgemm_ffma_rate(1 if packed else 0, iters, _stream(stream), ctypes.byref(out))
+    if rc != 0:
+        raise SgemmError("sgemm_ffma_rate", rc)
+    return out.value
+
+
 def sgemm_release() -> int:
     return library().sgemm_release()
 
@@ -236,6 +247,11 @@ def sgemm_noalloc(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None, spl
     """Allocation-free 3xTF32 entry point (split-K scratch in a fixed library array)."""
     return library().sgemm_noalloc(M, N, K, alpha, _ptr(A), lda, _ptr(B), ldb, beta, _ptr(C), ldc,
                                    _stream(stream), splits)
+
+
+def sgemm_noalloc_debug_flags(flags: int) -> int:
+    """Test hook: debug flags consumed by the next sgemm_noalloc GEMM call."""
+    return library().sgemm_noalloc_debug_flags(flags)
 
 
 # ------------------------------------------------------- torch convenience

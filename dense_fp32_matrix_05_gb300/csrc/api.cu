@@ -59,6 +59,13 @@ struct DevState {
 std::mutex g_mu;  // guards g_dev (setup, workspace growth, host buffers)
 DevState g_dev[kMaxDevices];
 
+// The device status word of sgemm / sgemm_ex / sgemm_t / the batched and
+// convolution calls: a __device__ variable (one per GPU, zero when the
+// library's device code is loaded), so that reading and clearing it in
+// sgemm_check_status allocates nothing.  Host code reaches it only through
+// the address cudaGetSymbolAddress gives for the current device.
+__device__ int g_status_word;
+
 int from_cuda(cudaError_t e) { return e == cudaSuccess ? 0 : static_cast<int>(e); }
 
 // Initialise per-device state; caller holds g_mu.
@@ -77,10 +84,10 @@ int device_state(DevState **out) {
         d.minor = prop.minor;
         d.sms = prop.multiProcessorCount;
         if (!(d.major == 10 && d.minor == 3)) return SGEMM_ERR_UNSUPPORTED_DEVICE;
-        e = cudaMalloc(reinterpret_cast<void **>(&d.status), sizeof(int));
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_status_word);
         if (e != cudaSuccess) return from_cuda(e);
-        e = cudaMemset(d.status, 0, sizeof(int));
-        if (e != cudaSuccess) return from_cuda(e);
+        d.status = static_cast<int *>(p);
         d.ready = true;
     }
     *out = &d;
@@ -1107,9 +1114,12 @@ int sgemm_check_status(sgemm_stream_t stream) {
             if (kv.second.counters) cudaMemset(kv.second.counters, 0, kv.second.n_counters * sizeof(int));
         e = cudaMemset(d->status, 0, sizeof(int));
         if (e != cudaSuccess) return from_cuda(e);
-        return SGEMM_ERR_DEVICE_TIMEOUT;
     }
-    return 0;
+    // the status word of sgemm_noalloc on this device (it clears its own
+    // arrival counters when the word is set)
+    const int na = sg::noalloc_take_status();
+    if (na < 0) return -na;  // a CUDA error, as a positive code
+    return (word != 0 || na > 0) ? SGEMM_ERR_DEVICE_TIMEOUT : 0;
 }
 
 const char *sgemm_status_string(int status) {

@@ -40,6 +40,11 @@ cudaError_t ffma_launch(int bm, int bn, const GemmArgs &g, const Schedule &s, co
     return cudaErrorInvalidValue;
 }
 
+cudaError_t scale_c_preload() {
+    cudaFuncAttributes attr;
+    return cudaFuncGetAttributes(&attr, ffma::scale_c_kernel);
+}
+
 cudaError_t scale_c_launch(float *C, long long ldc, int M, int N, float beta, int num_sms,
                            cudaStream_t stream) {
     const long long total = static_cast<long long>(M) * N;

@@ -82,6 +82,17 @@ int check_tensor_call(int M, int N, int K, float alpha, const float *A, int lda,
                       float beta, const float *C, int ldc, int splits);
 int plan_tensor_call(int M, int N, int K, const float *A, int lda, const float *B, int ldb, float beta,
                      const float *C, int ldc, int splits, int sms, size_t max_ws_floats, TensorPlan *out);
+// Read and clear sgemm_noalloc's status word on the current device (after
+// the caller has waited for its stream).  Returns 0 when the word is clear
+// or sgemm_noalloc has not been set up on this device, 1 when it was set
+// (the word and sgemm_noalloc's arrival counters are then cleared, after a
+// device-wide wait), or -e for a failed CUDA call returning e.
+int noalloc_take_status();
+// Load the device code of every kernel sgemm_noalloc can launch (with lazy
+// module loading, a kernel's code is otherwise loaded, and device memory
+// taken for it, at its first launch).
+cudaError_t tf32x3_preload();
+cudaError_t scale_c_preload();
 
 // Wide-N FFMA kernel for M <= 32, K <= 64 (A resident, B streamed):
 // persistent CTAs over blocks of 512 columns.

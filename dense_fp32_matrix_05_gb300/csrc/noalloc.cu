@@ -14,9 +14,14 @@
 // until the process exits (about 16 MiB + 16 KiB per GPU).  In host code
 // their names are only host-side stand-ins; the device addresses are fetched
 // once per device with cudaGetSymbolAddress, with that device current, on
-// the first call made on it.
+// the first call made on it.  With lazy module loading (the CUDA default)
+// that first call is also when the arrays and the kernels' code are loaded
+// onto the device, so the set-up loads every kernel this entry point can
+// launch there and then: after it, later calls leave the device's free
+// memory unchanged.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstddef>
 #include <mutex>
 
@@ -29,6 +34,7 @@ constexpr size_t kScratchFloats = size_t(4) << 20;  // 16 MiB of split-K partial
 constexpr int kScratchCounters = 4096;              // one arrival counter per output tile
 constexpr int kMaxDevices = 64;
 constexpr long long kWaitBudget = 20000000000LL;    // same bounded-wait budget as sgemm_ex
+constexpr long long kDebugWaitBudget = 2000000LL;   // ~1 ms, test-only withheld-arrive mode
 
 __device__ __align__(256) float g_scratch[kScratchFloats];
 __device__ __align__(256) int g_scratch_counters[kScratchCounters];
@@ -44,8 +50,11 @@ struct DeviceScratch {
 
 std::mutex g_setup_mu;
 DeviceScratch g_scratch_ptrs[kMaxDevices];
+// test hook: debug flags for the next call (sgemm_noalloc_debug_flags)
+std::atomic<int> g_next_debug_flags{0};
 
-// Resolve the device addresses of the arrays on the current device (once).
+// Resolve the device addresses of the arrays on the current device and load
+// the kernels (once per device).
 int device_scratch(DeviceScratch **out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -67,6 +76,8 @@ int device_scratch(DeviceScratch **out) {
         d.counters = static_cast<int *>(p);
         if ((e = cudaGetSymbolAddress(&p, g_scratch_status)) != cudaSuccess) return static_cast<int>(e);
         d.status = static_cast<int *>(p);
+        if ((e = sg::tf32x3_preload()) != cudaSuccess || (e = sg::scale_c_preload()) != cudaSuccess)
+            return static_cast<int>(e);
         d.sms = sms;
         d.ready = true;
     }
@@ -75,6 +86,37 @@ int device_scratch(DeviceScratch **out) {
 }
 
 }  // namespace
+
+namespace sg {
+
+int noalloc_take_status() {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return -static_cast<int>(e);
+    if (dev < 0 || dev >= kMaxDevices) return 0;
+    std::lock_guard<std::mutex> lk(g_setup_mu);
+    DeviceScratch &d = g_scratch_ptrs[dev];
+    if (!d.ready) return 0;  // no call has run on this device
+    int word = 0;
+    if ((e = cudaMemcpy(&word, d.status, sizeof(int), cudaMemcpyDeviceToHost)) != cudaSuccess)
+        return -static_cast<int>(e);
+    if (word == 0) return 0;
+    // a kernel that gave up may have left arrival counters non-zero: wait for
+    // every stream of the device, then clear them and the word
+    if ((e = cudaDeviceSynchronize()) != cudaSuccess ||
+        (e = cudaMemset(d.counters, 0, sizeof(int) * kScratchCounters)) != cudaSuccess ||
+        (e = cudaMemset(d.status, 0, sizeof(int))) != cudaSuccess)
+        return -static_cast<int>(e);
+    return 1;
+}
+
+}  // namespace sg
+
+extern "C" int sgemm_noalloc_debug_flags(int flags) {
+    if (flags & ~SGEMM_FLAG_DEBUG_WITHHOLD_ARRIVE) return -1;
+    g_next_debug_flags.store(flags);
+    return 0;
+}
 
 extern "C" int sgemm_noalloc(int M, int N, int K, float alpha, const float *A, int lda, const float *B, int ldb,
                              float beta, float *C, int ldc, sgemm_stream_t stream, int splits) {
@@ -92,16 +134,17 @@ extern "C" int sgemm_noalloc(int M, int N, int K, float alpha, const float *A, i
     }
     if ((rc = sg::plan_tensor_call(M, N, K, A, lda, B, ldb, beta, C, ldc, splits, d->sms, kScratchFloats, &plan)) != 0)
         return rc;
+    const int debug = g_next_debug_flags.exchange(0);
     sg::DeviceCtl ctl{};
     ctl.status = d->status;
-    ctl.wait_budget = kWaitBudget;
-    ctl.debug_flags = 0;
+    ctl.wait_budget = (debug & SGEMM_FLAG_DEBUG_WITHHOLD_ARRIVE) ? kDebugWaitBudget : kWaitBudget;
+    ctl.debug_flags = (debug & SGEMM_FLAG_DEBUG_WITHHOLD_ARRIVE) ? sg::kDebugWithholdArrive : 0;
     if (plan.ws_floats > 0) {  // split-K or split tail: tiles shared by several units
         if (plan.ws_floats > kScratchFloats || plan.tiles > kScratchCounters) return SGEMM_ERR_SCRATCH_LIMIT;
-        // the array keeps the previous call's contents; the counters must
-        // start at zero (a call that gave up a bounded wait can leave some set)
-        cudaError_t e = cudaMemsetAsync(d->counters, 0, sizeof(int) * static_cast<size_t>(plan.tiles), st);
-        if (e != cudaSuccess) return static_cast<int>(e);
+        // The counters are zero here: they start at zero when the library's
+        // device code is loaded, the kernel puts each one back to zero when
+        // its tile is finished, and a call that gave up a bounded wait sets
+        // the status word, whose check (sgemm_check_status) clears them.
         ctl.ws = d->partials;
         ctl.counters = d->counters;
     }

@@ -166,6 +166,35 @@ cudaError_t launch_rows(const GemmArgs &g, const Schedule &s, const DeviceCtl &c
 
 }  // namespace
 
+namespace {
+
+template <int TM, bool TA, bool TB>
+cudaError_t preload_one() {
+    cudaFuncAttributes attr;
+    return cudaFuncGetAttributes(&attr, tf32x3::tf32x3_gemm_kernel<TM, TA, TB>);
+}
+
+template <int TM>
+cudaError_t preload_tm() {
+    cudaError_t e;
+    if ((e = preload_one<TM, false, false>()) != cudaSuccess) return e;
+    if ((e = preload_one<TM, false, true>()) != cudaSuccess) return e;
+    if ((e = preload_one<TM, true, false>()) != cudaSuccess) return e;
+    return preload_one<TM, true, true>();
+}
+
+}  // namespace
+
+cudaError_t tf32x3_preload() {
+    cudaError_t e;
+    if ((e = preload_tm<16>()) != cudaSuccess) return e;
+    if ((e = preload_tm<32>()) != cudaSuccess) return e;
+    if ((e = preload_tm<64>()) != cudaSuccess) return e;
+    if ((e = preload_tm<128>()) != cudaSuccess) return e;
+    if ((e = preload_tm<192>()) != cudaSuccess) return e;
+    return preload_tm<256>();
+}
+
 bool tf32x3_supported_tm(int tm) {
     return tm == 16 || tm == 32 || tm == 64 || tm == 128 || tm == 192 || tm == 256;
 }

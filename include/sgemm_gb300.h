@@ -199,10 +199,13 @@ int sgemm_plan_info(int M, int N, int K, const void *A, int lda,
 
 /*
  * sgemm_check_status - wait for `stream`, then read and clear the device
- * status word of the current device.  Returns 0, SGEMM_ERR_DEVICE_TIMEOUT if
- * a kernel launched since the last check gave up a bounded wait (or met a
- * work split it cannot finish, which the planner never produces), or a
- * positive cudaError_t.
+ * status words of the current device: the one of every allocating entry
+ * point and the one of sgemm_noalloc.  Returns 0, SGEMM_ERR_DEVICE_TIMEOUT
+ * if a kernel launched since the last check gave up a bounded wait (or met
+ * a work split it cannot finish, which the planner never produces), or a
+ * positive cudaError_t.  When a word was set, it also waits for the whole
+ * device and clears the split-K arrival counters that word's kernels use.
+ * Allocates no device memory.
  */
 int sgemm_check_status(sgemm_stream_t stream);
 
@@ -236,23 +239,41 @@ int sgemm_release(void);
  * more returns SGEMM_ERR_SCRATCH_LIMIT before anything runs.  The call never
  * calls cudaMalloc, cudaFree or any allocating routine.
  *
- * Set-up: the first call on a device (with that device current) resolves
- * the arrays' device addresses with cudaGetSymbolAddress; make that first
- * call before any stream capture.
+ * Set-up: the first call on a device with M > 0 and N > 0 (with that device
+ * current) resolves the arrays' device addresses with cudaGetSymbolAddress.
+ * Under CUDA's lazy module loading (the default) that is also when the
+ * arrays and the device code of every kernel this entry point can launch
+ * are loaded onto the device, which takes device memory (16 MiB for the
+ * arrays, plus the code): make that first call before reserving the
+ * device's memory for a pool, and before any stream capture.  A call with
+ * alpha == 0 and beta == 1 does the set-up and nothing else (C, which must
+ * be a non-NULL device pointer, is neither read nor written); after it,
+ * later calls leave the device's free memory unchanged.
  * Sharing: every call uses the same arrays, which keep the previous call's
- * contents (the counters are cleared at the start of each call with
- * cudaMemsetAsync).  Calls whose work overlaps on the GPU - on different
- * streams, or from several host threads at once - race on the arrays and
- * give wrong results: serialise them.
- * Status: a bounded on-device wait that gives up (only a broken GPU does)
- * leaves C unspecified and is recorded in a status word of this entry point
- * that sgemm_check_status does not read.
+ * contents.  The arrival counters start at zero and each call leaves them
+ * at zero.  Calls whose work overlaps on the GPU - on different streams, or
+ * from several host threads at once - race on the arrays and give wrong
+ * results: serialise them.
+ * Status: a bounded on-device wait that gives up (only a broken GPU does,
+ * or the test hook below) leaves C unspecified and sets this entry point's
+ * device status word.  sgemm_check_status reads and clears it, and then
+ * clears the arrival counters; until that check, later split-K calls of
+ * this entry point may give wrong results.
  */
 int sgemm_noalloc(int M, int N, int K, float alpha,
                   const float *A, int lda,
                   const float *B, int ldb,
                   float beta, float *C, int ldc,
                   sgemm_stream_t stream, int splits);
+
+/*
+ * sgemm_noalloc_debug_flags - test hook: debug flags for the next
+ * sgemm_noalloc call that launches a GEMM (it consumes them; later calls run
+ * normally).  flags (1): 0 or SGEMM_FLAG_DEBUG_WITHHOLD_ARRIVE, which makes
+ * that call's bounded wait run out after about 1 ms, so that its failure is
+ * reported by sgemm_check_status.  Returns 0, or -1 for other bits.
+ */
+int sgemm_noalloc_debug_flags(int flags);
 
 /*
  * sgemm_t - C = alpha * op(A) * op(B) + beta * C, with op(X) = X or X^T
@@ -398,6 +419,25 @@ int sgemm_version(void);
  * wait for the MMAs gave up.  Allocates nothing on the device.
  */
 int sgemm_tf32_mma_rate(int n, int iters, sgemm_stream_t stream, double *tflops);
+
+/*
+ * sgemm_ffma_rate - measure the CUDA cores' fp32 FMA rate on the current
+ * device: the peak of the FFMA path (the pages estimate theirs from core
+ * counts and clocks, "matmul_opt.cu", its theoretical-peak paragraph; this
+ * call measures it).  Every SM runs 2048 threads, each with 16 independent
+ * FMA chains.  Measurement, not GEMM.
+ *
+ *   packed (1): 0 = scalar fma.rn.f32; 1 = packed fma.rn.f32x2 (two FMAs per
+ *               instruction, the form the FFMA kernels issue).
+ *   iters  (2): steps per thread, >= 1 (16 FMAs each).
+ *   stream (3): stream the two launches (warm-up, timed) are ordered on;
+ *               the call waits for them.
+ *   tflops (4): out, fp32 TFLOP/s = 2 x FMAs / time.
+ *
+ * Returns 0, -i for a bad argument, a positive cudaError_t or
+ * SGEMM_ERR_UNSUPPORTED_DEVICE.  Allocates nothing on the device.
+ */
+int sgemm_ffma_rate(int packed, int iters, sgemm_stream_t stream, double *tflops);
 
 #ifdef __cplusplus
 }

@@ -5,11 +5,15 @@ synchronisation).  Its split-K scratch lives in a fixed array compiled into
 the library.
 
 Checked through the C ABI against the existing entry point (sgemm_ex with the
-same path and split count) with the parity tolerance of the other tests, on
-two calls in a row, so that leftovers of the first call in the shared array
-cannot leak into the second.  Collected last (file name) so that a run
-stopping at the first failure has already run everything else; it also
-passes alone in a fresh process.
+same path and split count) on two calls in a row, so that leftovers of the
+first call in the shared array cannot leak into the second: both calls run
+the same kernel on the same plan, so the results must be the same bits, and
+both must pass the oracle's tolerance.  Also checked: after the documented
+set-up call the device's free memory does not change across calls, and a
+call whose bounded wait runs out (test hook) is reported by
+sgemm_check_status, after which the next call is correct.  Collected last
+(file name) so that a run stopping at the first failure has already run
+everything else; it also passes alone in a fresh process.
 """
 from __future__ import annotations
 
@@ -38,6 +42,12 @@ def _device(p):
             torch.from_numpy(p.C).cuda())
 
 
+def _setup_call(C, st):
+    """The documented set-up call: alpha = 0, beta = 1 (C untouched)."""
+    rc = pkg.sgemm_noalloc(1, 1, 0, 0.0, None, 1, None, 1, 1.0, C, 1, st, 0)
+    assert rc == 0, pkg.sgemm_status_string(rc)
+
+
 @pytest.mark.parametrize("name,splits", [("square1024", 4), ("ragged1023x1021x1025", 3)])
 def test_noalloc_matches_sgemm_ex_twice(name, splits):
     import torch
@@ -57,10 +67,61 @@ def test_noalloc_matches_sgemm_ex_twice(name, splits):
                           pkg.SGEMM_ALGO_TF32X3, splits, 0)
         assert rc == 0, pkg.sgemm_status_string(rc)
         assert pkg.sgemm_check_status(st) == 0
+        assert torch.equal(C_noalloc, C_ex), f"call {call}: differs from sgemm_ex"
         got = C_noalloc.cpu().numpy()[:, :p.N].astype(np.float64)
-        want = C_ex.cpu().numpy()[:, :p.N].astype(np.float64)
-        assert np.all(np.abs(got - want) <= oracle.REL_TOL * scale), f"call {call}: differs from sgemm_ex"
         assert not oracle.first_failures(got, ref, scale), f"call {call}: differs from the oracle"
+
+
+def test_noalloc_leaves_free_memory_unchanged():
+    """After the set-up call, GEMMs of several plans (split-K, whole tiles,
+    tensor-map and element-load operands) take no device memory."""
+    import torch
+    st = torch.cuda.current_stream()
+    cases = []
+    for (M, N, K, off, splits) in [(1024, 1024, 1024, 0, 4), (333, 517, 301, 1, 2), (64, 4096, 147, 0, 1),
+                                   (512, 384, 2048, 0, 0)]:
+        p = random_problem(M, N, K, alpha=1.0, beta=0.5, seed=M + N + K, pad_value=0.0)
+        A = torch.zeros(p.A.size + 4, device="cuda")
+        B = torch.zeros(p.B.size + 4, device="cuda")
+        C = torch.zeros(p.C.size + 4, device="cuda")
+        A[off:off + p.A.size] = torch.from_numpy(p.A.reshape(-1)).cuda()
+        B[off:off + p.B.size] = torch.from_numpy(p.B.reshape(-1)).cuda()
+        cases.append((p, A[off:], B[off:], C[off:], splits))
+    _setup_call(cases[0][3], st)
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    for _ in range(2):
+        for p, A, B, C, splits in cases:
+            rc = pkg.sgemm_noalloc(p.M, p.N, p.K, p.alpha, A, p.lda, B, p.ldb, p.beta, C, p.ldc, st, splits)
+            assert rc == 0, pkg.sgemm_status_string(rc)
+    assert pkg.sgemm_check_status(st) == 0
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0, f"device free memory changed by {free0 - free1} bytes across sgemm_noalloc calls"
+
+
+def test_noalloc_timeout_is_reported_and_cleared():
+    """A call whose bounded wait runs out (the test hook withholds one
+    pipeline arrive and cuts the budget to ~1 ms) sets sgemm_noalloc's status
+    word; sgemm_check_status reports it and clears the word and the arrival
+    counters, and the next split-K call is correct again."""
+    import torch
+    p = make_problem("square1024", pad_value=0.0)
+    A, B, C0 = _device(p)
+    st = torch.cuda.current_stream()
+    assert pkg.sgemm_noalloc_debug_flags(pkg.SGEMM_FLAG_DEBUG_WITHHOLD_ARRIVE) == 0
+    C = C0.clone()
+    assert pkg.sgemm_noalloc(p.M, p.N, p.K, p.alpha, A, p.lda, B, p.ldb, p.beta, C, p.ldc, st, 4) == 0
+    assert pkg.sgemm_check_status(st) == pkg.SGEMM_ERR_DEVICE_TIMEOUT
+    assert pkg.sgemm_check_status(st) == 0  # read and cleared
+    C = C0.clone()
+    C_ex = C0.clone()
+    assert pkg.sgemm_noalloc(p.M, p.N, p.K, p.alpha, A, p.lda, B, p.ldb, p.beta, C, p.ldc, st, 4) == 0
+    assert pkg.sgemm_ex(p.M, p.N, p.K, p.alpha, A, p.lda, B, p.ldb, p.beta, C_ex, p.ldc, st,
+                        pkg.SGEMM_ALGO_TF32X3, 4, 0) == 0
+    assert pkg.sgemm_check_status(st) == 0
+    assert torch.equal(C, C_ex)
+    assert pkg.sgemm_noalloc_debug_flags(2) == -1
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch():
