@@ -24,9 +24,9 @@ cudaError_t launch_conv_tm(const GemmArgs &g, const Schedule &s, const DeviceCtl
     const int smem = C::kSmemBytes + (ORDER == kConvTapsDense ? C::kConvTabBytes : 0);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    // no B map: the kernel does not read it when TMA_B is false
-    return launch_pdl(kern, grid, tf32x3::Roles<TM, true, false>::kThreads, smem, stream, g, s, ctl, 1, tma_c, map_a,
-                      map_a, map_c);
+    // no B maps: the kernel does not read them when TMA_B is false
+    return launch_pdl(kern, grid, tf32x3::Roles<TM, true, false>::kThreads, smem, stream, g, s, ctl, 1, tma_c, 0u,
+                      map_a, map_a, map_c, map_a, map_a, map_a);
 }
 
 template <int TM>

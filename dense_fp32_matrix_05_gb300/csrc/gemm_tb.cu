@@ -24,8 +24,9 @@ cudaError_t launch_tb_tm(const GemmArgs &g, const Schedule &s, const DeviceCtl &
     auto kern = tf32x3::tf32x3_gemm_kernel<TM, true, true, kConvNone, true>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
+    // the residue-class maps are unused by the transposed-B form
     return launch_pdl(kern, grid, tf32x3::Roles<TM, true, true>::kThreads, C::kSmemBytes, stream, g, s, ctl, 1, tma_c,
-                      map_a, map_b, map_c);
+                      0u, map_a, map_b, map_c, map_b, map_b, map_b);
 }
 
 template <int TM>

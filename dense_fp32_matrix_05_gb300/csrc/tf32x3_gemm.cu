@@ -113,6 +113,39 @@ bool make_tmap_bt(const GemmArgs &g, int batch, CUtensorMap *map) {
     return r == CUDA_SUCCESS;
 }
 
+// Tensor maps of a B whose rows are not 16-byte aligned (ldb % 4 != 0),
+// one per residue class r = k % 4: rows r, r + 4, r + 8, ... are 4 * ldb
+// floats apart (a multiple of 16 bytes).  Class r starts at B + r * ldb -
+// o_r, rounded down to a 16-byte boundary (o_r = (r * ldb) % 4), and is
+// N + o_r floats wide, so its rows' columns 0..N-1 sit o_r floats into the
+// box of 132 x 4 (columns x rows of the class) copied without swizzle;
+// out-of-range elements read as zero.  Needs a 16-byte aligned B (so the
+// leading floats of a row are the tail of the row before it, inside B),
+// K >= 4 (every class has a row) and a batch stride that is a multiple of 4
+// floats.  *offs packs o_r in bits 2r..2r+1.
+bool make_tmap_b4(const GemmArgs &g, int batch, CUtensorMap maps[4], uint32_t *offs) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    if (!enc) return false;
+    if ((reinterpret_cast<uintptr_t>(g.B) & 15u) != 0 || g.K < 4 || (g.sB & 3) != 0) return false;
+    cuuint64_t nb, sb;
+    if (!batch_dim(g.sB, batch, g.ldb * g.K, nb, sb)) return false;
+    *offs = 0;
+    for (int r = 0; r < 4; ++r) {
+        const long long o = (static_cast<long long>(r) * g.ldb) & 3;
+        const float *base = g.B + static_cast<long long>(r) * g.ldb - o;
+        const cuuint64_t dims[3] = {static_cast<cuuint64_t>(g.N + o), static_cast<cuuint64_t>((g.K - r + 3) / 4), nb};
+        const cuuint64_t strides[2] = {static_cast<cuuint64_t>(4 * g.ldb) * sizeof(float), sb};
+        const cuuint32_t box[3] = {static_cast<cuuint32_t>(tf32x3::kB4Row), 4, 1};
+        const cuuint32_t estr[3] = {1, 1, 1};
+        const CUresult res = enc(&maps[r], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(base), dims,
+                                 strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (res != CUDA_SUCCESS) return false;
+        *offs |= static_cast<uint32_t>(o) << (2 * r);
+    }
+    return true;
+}
+
 bool make_tmap_c(const GemmArgs &g, int batch, CUtensorMap *map) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
     if (!enc) return false;
@@ -130,48 +163,57 @@ bool make_tmap_c(const GemmArgs &g, int batch, CUtensorMap *map) {
 
 namespace {
 
-template <int TM, bool TA, bool TB>
+template <int TM, bool TA, bool TB, bool B4 = false>
 cudaError_t launch_tm(const GemmArgs &g, const Schedule &s, const DeviceCtl &ctl, int vec_a, int tma_c, int grid,
-                      const CUtensorMap &map_a, const CUtensorMap &map_b, const CUtensorMap &map_c,
-                      cudaStream_t stream) {
-    using C = tf32x3::Cfg<TM, TB>;
-    auto kern = tf32x3::tf32x3_gemm_kernel<TM, TA, TB>;
+                      const CUtensorMap &map_a, const CUtensorMap (&map_b)[4], uint32_t b_offs,
+                      const CUtensorMap &map_c, cudaStream_t stream) {
+    using C = tf32x3::Cfg<TM, TB, B4>;
+    auto kern = tf32x3::tf32x3_gemm_kernel<TM, TA, TB, kConvNone, false, B4>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     return launch_pdl(kern, grid, tf32x3::Roles<TM, TA, TB>::kThreads, C::kSmemBytes, stream, g, s, ctl, vec_a, tma_c,
-                      map_a, map_b, map_c);
+                      b_offs, map_a, map_b[0], map_c, map_b[1], map_b[2], map_b[3]);
 }
 
 // Operands go through TMA whenever their rows are 16-byte aligned: the deep
 // asynchronous ring hides memory latency and the producers then hold almost
 // nothing in registers (the extra shared-memory pass for B^T is cheaper than
-// the register spills and load stalls it removes).
+// the register spills and load stalls it removes).  A B whose rows are not
+// aligned (but whose start is) comes by TMA too, as four residue classes of
+// rows.  SGEMM_FLAG_B_ROWS_LOADED (b_rows) keeps such a B on the producers'
+// own loads.
 template <int TM>
 cudaError_t launch_rows(const GemmArgs &g, const Schedule &s, const DeviceCtl &ctl, int vec_a, int vec_b,
-                        int vec_c, int grid, int batch, cudaStream_t stream) {
-    CUtensorMap ma, mb, mc;
+                        int vec_c, int grid, int batch, bool b_rows, cudaStream_t stream) {
+    CUtensorMap ma, mb[4], mc;
     std::memset(&ma, 0, sizeof(ma));
-    std::memset(&mb, 0, sizeof(mb));
+    std::memset(mb, 0, sizeof(mb));
     std::memset(&mc, 0, sizeof(mc));
+    uint32_t offs = 0;
     const bool ta = vec_a && make_tmap_a(g, TM, batch, &ma);
-    const bool tb = vec_b && make_tmap_b(g, batch, &mb);
+    const bool tb = vec_b && make_tmap_b(g, batch, &mb[0]);
+    const bool tb4 = !vec_b && !b_rows && make_tmap_b4(g, batch, mb, &offs);
     const int tc = (vec_c && make_tmap_c(g, batch, &mc)) ? 1 : 0;
     if (tb) {
-        if (ta) return launch_tm<TM, true, true>(g, s, ctl, vec_a, tc, grid, ma, mb, mc, stream);
-        return launch_tm<TM, false, true>(g, s, ctl, vec_a, tc, grid, ma, mb, mc, stream);
+        if (ta) return launch_tm<TM, true, true>(g, s, ctl, vec_a, tc, grid, ma, mb, 0, mc, stream);
+        return launch_tm<TM, false, true>(g, s, ctl, vec_a, tc, grid, ma, mb, 0, mc, stream);
     }
-    if (ta) return launch_tm<TM, true, false>(g, s, ctl, vec_a, tc, grid, ma, mb, mc, stream);
-    return launch_tm<TM, false, false>(g, s, ctl, vec_a, tc, grid, ma, mb, mc, stream);
+    if (tb4) {
+        if (ta) return launch_tm<TM, true, true, true>(g, s, ctl, vec_a, tc, grid, ma, mb, offs, mc, stream);
+        return launch_tm<TM, false, true, true>(g, s, ctl, vec_a, tc, grid, ma, mb, offs, mc, stream);
+    }
+    if (ta) return launch_tm<TM, true, false>(g, s, ctl, vec_a, tc, grid, ma, mb, 0, mc, stream);
+    return launch_tm<TM, false, false>(g, s, ctl, vec_a, tc, grid, ma, mb, 0, mc, stream);
 }
 
 }  // namespace
 
 namespace {
 
-template <int TM, bool TA, bool TB>
+template <int TM, bool TA, bool TB, bool B4 = false>
 cudaError_t preload_one() {
     cudaFuncAttributes attr;
-    return cudaFuncGetAttributes(&attr, tf32x3::tf32x3_gemm_kernel<TM, TA, TB>);
+    return cudaFuncGetAttributes(&attr, tf32x3::tf32x3_gemm_kernel<TM, TA, TB, kConvNone, false, B4>);
 }
 
 template <int TM>
@@ -180,6 +222,8 @@ cudaError_t preload_tm() {
     if ((e = preload_one<TM, false, false>()) != cudaSuccess) return e;
     if ((e = preload_one<TM, false, true>()) != cudaSuccess) return e;
     if ((e = preload_one<TM, true, false>()) != cudaSuccess) return e;
+    if ((e = preload_one<TM, false, true, true>()) != cudaSuccess) return e;
+    if ((e = preload_one<TM, true, true, true>()) != cudaSuccess) return e;
     return preload_one<TM, true, true>();
 }
 
@@ -224,14 +268,14 @@ int tf32x3_smem_bytes(int tm) {
 }
 
 cudaError_t tf32x3_launch(int tm, const GemmArgs &g, const Schedule &s, const DeviceCtl &ctl, int vec_a,
-                          int vec_b, int vec_c, int grid, cudaStream_t stream, int batch) {
+                          int vec_b, int vec_c, int grid, cudaStream_t stream, int batch, bool b_rows) {
     switch (tm) {
-        case 16: return launch_rows<16>(g, s, ctl, vec_a, vec_b, vec_c, grid, batch, stream);
-        case 32: return launch_rows<32>(g, s, ctl, vec_a, vec_b, vec_c, grid, batch, stream);
-        case 64: return launch_rows<64>(g, s, ctl, vec_a, vec_b, vec_c, grid, batch, stream);
-        case 128: return launch_rows<128>(g, s, ctl, vec_a, vec_b, vec_c, grid, batch, stream);
-        case 192: return launch_rows<192>(g, s, ctl, vec_a, vec_b, vec_c, grid, batch, stream);
-        case 256: return launch_rows<256>(g, s, ctl, vec_a, vec_b, vec_c, grid, batch, stream);
+        case 16: return launch_rows<16>(g, s, ctl, vec_a, vec_b, vec_c, grid, batch, b_rows, stream);
+        case 32: return launch_rows<32>(g, s, ctl, vec_a, vec_b, vec_c, grid, batch, b_rows, stream);
+        case 64: return launch_rows<64>(g, s, ctl, vec_a, vec_b, vec_c, grid, batch, b_rows, stream);
+        case 128: return launch_rows<128>(g, s, ctl, vec_a, vec_b, vec_c, grid, batch, b_rows, stream);
+        case 192: return launch_rows<192>(g, s, ctl, vec_a, vec_b, vec_c, grid, batch, b_rows, stream);
+        case 256: return launch_rows<256>(g, s, ctl, vec_a, vec_b, vec_c, grid, batch, b_rows, stream);
         default: return cudaErrorInvalidValue;
     }
 }

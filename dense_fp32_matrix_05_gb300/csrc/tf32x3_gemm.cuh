@@ -116,25 +116,47 @@ constexpr int kEpiChunkBytes = kEpiRows * 128 * 4;
 // planner gives no CTA more split-K units than this.
 constexpr int kMaxDefer = 8;
 
-// TM = C rows per tile (MMA N).  TMA_B: the stage also holds the raw B tile
-// (16 k rows x 128 n, copied by TMA) that the producers read and split.
-template <int TM, bool TMA_B = false>
+// B rows that are not 16-byte aligned (ldb % 4 != 0, e.g. N = 14161) still
+// come by TMA: rows k with the same k % 4 (a residue class r) lie 4 * ldb
+// floats apart, a multiple of 16 bytes, so each class is a tensor of its own
+// whose start is rounded down to 16 bytes; its rows then begin o_r = (r *
+// ldb) % 4 floats into the copied box.  A stage's slab holds, per class,
+// the 4 rows of the class among its 16 k, each kB4Row floats wide (128
+// columns plus up to 3 leading floats), in blocks of kB4ClassBytes (a
+// multiple of 128 bytes, the TMA destination alignment).
+constexpr int kB4Row = kTileN + 4;                     // 132 floats = 528 bytes, a multiple of 16
+constexpr int kB4RowBytes = kB4Row * 4;
+constexpr int kB4ClassBytes = (4 * kB4RowBytes + 127) / 128 * 128;  // 2176
+constexpr int kB4SlabBytes = 4 * kB4ClassBytes;
+
+// TM = C rows per tile (MMA N).  TMA_B: each stage also has a slab for the
+// raw B tile (16 k rows x 128 n, copied by TMA) that the producers read and
+// split; B4: that slab holds the four residue classes of an unaligned B.
+// Shared memory: the stages' A tiles (hi, lo), then the stages' B slabs,
+// then the epilogue's C buffers and the barriers.
+template <int TM, bool TMA_B = false, bool B4 = false>
 struct Cfg {
     static_assert(TM % 16 == 0 && TM >= 16 && TM <= 256, "MMA N for M=128 must be 16..256, step 16");
+    static_assert(TMA_B || !B4, "the residue-class form is a TMA form");
     static constexpr int kNacc = nacc_for(TM);
     static constexpr int kABytes = TM * kBK * 4;  // A tile (MMA B operand), one of hi / lo
     static constexpr int kOffAHi = 0;             // also where TMA lands the raw A tile
     static constexpr int kOffALo = kABytes;
-    static constexpr int kBRawBytes = TMA_B ? kBK * kTileN * 4 : 0;
-    static constexpr int kOffBRaw = 2 * kABytes;
-    static constexpr int kStageBytes = 2 * kABytes + kBRawBytes;
+    static constexpr int kAStageBytes = 2 * kABytes;
+    static constexpr int kBRawBytes = TMA_B ? (B4 ? kB4SlabBytes : kBK * kTileN * 4) : 0;
+    static constexpr int kStageBytes = kAStageBytes + kBRawBytes;  // shared memory per stage, A and B
     // epilogue staging for TMA copies of C: kEpiBufs chunks of 16 rows x 128
     static constexpr int kEpiBufBytes = kEpiBufs * kEpiChunkBytes;
     // as many stages as tensor memory and the 227 KB of shared memory allow
-    static constexpr int kStages = stages_for(TM) < (kSmemLimit - 2048 - kEpiBufBytes) / kStageBytes
-                                       ? stages_for(TM) : (kSmemLimit - 2048 - kEpiBufBytes) / kStageBytes;
+    // (1 KB of alignment slack and up to 528 bytes of barriers and words)
+    static constexpr int kStageRoom = kSmemLimit - 1024 - 528 - kEpiBufBytes;
+    static constexpr int kStages = stages_for(TM) < kStageRoom / kStageBytes ? stages_for(TM)
+                                                                             : kStageRoom / kStageBytes;
+    static constexpr int kOffBRegion = kStages * kAStageBytes;  // slab of stage s at + s * kBRawBytes
     static constexpr int kOffEpi = kStages * kStageBytes;
-    static_assert(kStageBytes % 1024 == 0, "stages must keep 1 KB alignment");
+    static_assert(kAStageBytes % 1024 == 0, "A tiles must keep 1 KB alignment (64-byte swizzle atoms)");
+    static_assert(kBRawBytes % 512 == 0 || B4, "B slabs keep the 64-byte swizzle's 512-byte alignment");
+    static_assert(kBRawBytes % 128 == 0 && kOffEpi % 128 == 0, "TMA destinations 128-byte aligned");
     static constexpr bool kPaired = paired_for(TM);
     static constexpr int kAccCols = acc_cols_for(TM);  // one accumulator (two TM halves when paired)
     static constexpr int kRingCol = kNacc * kAccCols;
@@ -149,6 +171,7 @@ struct Cfg {
     // tile column, segment count, first workspace slot)
     static constexpr int kBarBytes = 8 * (3 * kStages + 5 + kEpiBufs) + 4 * (4 + 5 * kMaxDefer);
     static constexpr int kSmemBytes = 1024 + kOffEpi + kEpiBufBytes + kBarBytes;
+    static_assert(kBarBytes <= 528, "room kept for the barriers");
     static_assert(kSmemBytes <= kSmemLimit, "shared memory per CTA");
     // a dense convolution's tap table (kConvTabMax ints, 16-byte aligned)
     static constexpr int kConvTabBytes = kConvTabMax * 4 + 16;
@@ -326,17 +349,32 @@ __device__ __forceinline__ void split_store4(uint32_t hi_addr, uint32_t lo_addr,
 // slab as 128 n rows of 16 k (64 bytes, 64-byte swizzle): a thread's column
 // is one row, read as KB / 4 16-byte chunks (the swizzle spreads the 8
 // lanes of each 128-bit load phase over all 32 banks).
-template <int TM, bool TMA_B, int KB, int BtK, int GT, int AJ, int AJ_TMA, bool TRANS_B = false>
-__device__ __forceinline__ void store_split(uint32_t stage, uint32_t ring_taddr, int ptid,
-                                            const Raw<BtK, AJ> &raw) {
-    using C = Cfg<TM, TMA_B>;
+// B4: the slab holds the residue classes of an unaligned B (kB4Row floats
+// per row); b_offs packs o_r, the leading floats of class r's rows, in bits
+// 2r..2r+1.
+template <int TM, bool TMA_B, int KB, int BtK, int GT, int AJ, int AJ_TMA, bool TRANS_B = false, bool B4 = false>
+__device__ __forceinline__ void store_split(uint32_t stage, uint32_t slab, uint32_t ring_taddr, int ptid,
+                                            const Raw<BtK, AJ> &raw, uint32_t b_offs = 0) {
+    using C = Cfg<TM, TMA_B, B4>;
     {
         // KB k values of this thread's B^T column: from registers, or from the
-        // raw B tile (k rows of 128 floats) that TMA copied into the stage
+        // raw B tile (k rows of 128 floats) that TMA copied into the slab
         uint32_t hi[KB], lo[KB];
-        if constexpr (TMA_B && TRANS_B) {
+        if constexpr (TMA_B && B4) {
+            static_assert(KB % 4 == 0, "whole residue classes");
+            const int n = ptid & (kTileN - 1);
+            const int kb = (ptid >> 7) * KB;  // a multiple of 4: k % 4 == e % 4
+#pragma unroll
+            for (int e = 0; e < KB; ++e) {
+                const int r = e & 3;
+                const uint32_t o = (b_offs >> (2 * r)) & 3u;
+                const float x = lds32f(slab + static_cast<uint32_t>(r * kB4ClassBytes + ((kb + e) >> 2) * kB4RowBytes) +
+                                       (static_cast<uint32_t>(n) + o) * 4u);
+                split_tf32(x, hi[e], lo[e]);
+                hi[e] = __float_as_uint(x);  // raw word: the tensor core drops the low bits
+            }
+        } else if constexpr (TMA_B && TRANS_B) {
             static_assert(KB % 4 == 0, "whole 16-byte chunks");
-            const uint32_t slab = stage + C::kOffBRaw;
             const int n = ptid & (kTileN - 1);
             const int q0 = ((ptid >> 7) * KB) >> 2;  // first 16-byte chunk (4 k) of this thread
 #pragma unroll
@@ -350,7 +388,7 @@ __device__ __forceinline__ void store_split(uint32_t stage, uint32_t ring_taddr,
                 }
             }
         } else if constexpr (TMA_B) {
-            const uint32_t col = stage + C::kOffBRaw + static_cast<uint32_t>((ptid & (kTileN - 1)) * 4);
+            const uint32_t col = slab + static_cast<uint32_t>((ptid & (kTileN - 1)) * 4);
             const int kb = (ptid >> 7) * KB;
 #pragma unroll
             for (int e = 0; e < KB; ++e) {
@@ -651,16 +689,21 @@ __device__ __forceinline__ void prefetch_c_tile(const GemmArgs &g, int bi, int m
 // the tap table.
 // TRANS_B: B is stored N x K (BLAS transb) and tmap_b describes it as K x N
 // (box 16 x 128, 64-byte swizzle); needs TMA_B.
-template <int TM, bool TMA_A, bool TMA_B, int CONV = kConvNone, bool TRANS_B = false>
+// B4: B's rows are not 16-byte aligned; tmap_b, tmap_b1, tmap_b2, tmap_b3
+// describe its residue classes k % 4 = 0..3 (each N + o_r floats wide, box
+// 132 x 4, no swizzle) and b_offs packs the o_r; needs TMA_B.
+template <int TM, bool TMA_A, bool TMA_B, int CONV = kConvNone, bool TRANS_B = false, bool B4 = false>
 __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
     tf32x3_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ Schedule sch,
-                       const __grid_constant__ DeviceCtl ctl, int vec_a, int tma_c,
+                       const __grid_constant__ DeviceCtl ctl, int vec_a, int tma_c, uint32_t b_offs,
                        const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-                       const __grid_constant__ CUtensorMap tmap_c) {
-    using C = Cfg<TM, TMA_B>;
+                       const __grid_constant__ CUtensorMap tmap_c, const __grid_constant__ CUtensorMap tmap_b1,
+                       const __grid_constant__ CUtensorMap tmap_b2, const __grid_constant__ CUtensorMap tmap_b3) {
+    using C = Cfg<TM, TMA_B, B4>;
     using R = Roles<TM, TMA_A, TMA_B>;
     static_assert(CONV == kConvNone || !TMA_B, "a convolution gathers B in the producers");
     static_assert(!TRANS_B || (TMA_B && CONV == kConvNone), "a transposed B comes by TMA");
+    static_assert(!B4 || (TMA_B && !TRANS_B && CONV == kConvNone), "residue classes of a row-major B");
     constexpr int S = C::kStages;
     constexpr int CH = C::kChunk;
     static_assert(R::kGroups <= S, "a group's next stage must not wrap the ring twice");
@@ -973,9 +1016,9 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    store_split<TM, TMA_B, KB, BtK, GT, AJ, AJ_ALL, TRANS_B>(base + s * C::kStageBytes,
-                                                         ring_lane + static_cast<uint32_t>(s * kRingColsPerStage),
-                                                         gt, buf[i]);
+                    store_split<TM, TMA_B, KB, BtK, GT, AJ, AJ_ALL, TRANS_B, B4>(
+                        base + s * C::kAStageBytes, base + C::kOffBRegion + s * C::kBRawBytes,
+                        ring_lane + static_cast<uint32_t>(s * kRingColsPerStage), gt, buf[i], b_offs);
                     fence_proxy_async_smem();
                     tmem_st_wait();
                     tc_fence_before();
@@ -1002,7 +1045,13 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
         if (lane == 0) {
             if (TMA_A) prefetch_tmap(&tmap_a);
             if (TMA_B) prefetch_tmap(&tmap_b);
-            constexpr uint32_t kTx = (TMA_A ? TM * kBK * 4 : 0) + (TMA_B ? kBK * kTileN * 4 : 0);
+            if (B4) {
+                prefetch_tmap(&tmap_b1);
+                prefetch_tmap(&tmap_b2);
+                prefetch_tmap(&tmap_b3);
+            }
+            constexpr uint32_t kTx =
+                (TMA_A ? TM * kBK * 4 : 0) + (TMA_B ? (B4 ? kBK * kB4RowBytes : kBK * kTileN * 4) : 0);
             int s = 0;
             uint32_t ph = 0;
             uint32_t used = 0, last_ph = 0;  // per stage: copy issued / its phase parity
@@ -1012,17 +1061,23 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
                 if (!mbar_wait_bounded(bars + 8u * (S + s), ph ^ 1u, abort_flag, ctl, kStatusTimeoutProducer))
                     break;
                 mbar_arrive_expect_tx(afull0 + 8u * s, kTx);
+                const uint32_t slab = base + C::kOffBRegion + s * C::kBRawBytes;
                 if (TMA_A)
-                    tma_load_3d(base + s * C::kStageBytes + C::kOffAHi, &tmap_a, it.kt * kBK, it.mt * TM,
+                    tma_load_3d(base + s * C::kAStageBytes + C::kOffAHi, &tmap_a, it.kt * kBK, it.mt * TM,
                                 g.sA != 0 ? it.b : 0,
                                 afull0 + 8u * s);
-                if (TMA_B && TRANS_B)
-                    tma_load_3d(base + s * C::kStageBytes + C::kOffBRaw, &tmap_b, it.kt * kBK, it.nt * kTileN,
-                                g.sB != 0 ? it.b : 0, afull0 + 8u * s);
-                else if (TMA_B)
-                    tma_load_3d(base + s * C::kStageBytes + C::kOffBRaw, &tmap_b, it.nt * kTileN, it.kt * kBK,
-                                g.sB != 0 ? it.b : 0,
-                                afull0 + 8u * s);
+                if (TMA_B && TRANS_B) {
+                    tma_load_3d(slab, &tmap_b, it.kt * kBK, it.nt * kTileN, g.sB != 0 ? it.b : 0, afull0 + 8u * s);
+                } else if (TMA_B && B4) {
+                    // rows k0 + 4i + r of the stage (i < 4) are rows 4 kt + i of class r
+                    const CUtensorMap *maps[4] = {&tmap_b, &tmap_b1, &tmap_b2, &tmap_b3};
+#pragma unroll
+                    for (int r = 0; r < 4; ++r)
+                        tma_load_3d(slab + r * kB4ClassBytes, maps[r], it.nt * kTileN, it.kt * (kBK / 4),
+                                    g.sB != 0 ? it.b : 0, afull0 + 8u * s);
+                } else if (TMA_B) {
+                    tma_load_3d(slab, &tmap_b, it.nt * kTileN, it.kt * kBK, g.sB != 0 ? it.b : 0, afull0 + 8u * s);
+                }
                 used |= 1u << s;
                 last_ph = (last_ph & ~(1u << s)) | (ph << s);
                 it.advance(sch);
@@ -1060,7 +1115,7 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t st = base + s * C::kStageBytes;
+                const uint32_t st = base + s * C::kAStageBytes;
                 const uint32_t ring = tmem_base + static_cast<uint32_t>(C::kRingCol + s * kRingColsPerStage);
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {

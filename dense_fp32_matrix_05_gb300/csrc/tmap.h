@@ -18,6 +18,9 @@ bool make_tmap_b(const GemmArgs &g, int batch, CUtensorMap *map);
 // A transposed B (stored N x K, K innermost) as K x N, box 16 x 128,
 // 64-byte swizzle.
 bool make_tmap_bt(const GemmArgs &g, int batch, CUtensorMap *map);
+// B with rows that are not 16-byte aligned: one map per residue class of
+// rows k % 4 (box 132 x 4); offs packs each class's leading floats.
+bool make_tmap_b4(const GemmArgs &g, int batch, CUtensorMap maps[4], uint32_t *offs);
 // C: N x M fp32 (N innermost), box 128 x 16 (one epilogue chunk).
 bool make_tmap_c(const GemmArgs &g, int batch, CUtensorMap *map);
 

@@ -85,6 +85,13 @@ typedef struct CUstream_st *sgemm_stream_t;
  * (2 * M * K * 4 bytes of traffic), so that its tiles come by TMA.  With the
  * flag the kernel loads such an A itself.  Both give the same bits. */
 #define SGEMM_FLAG_NO_A_COPY (1 << 16)
+/* SGEMM_FLAG_B_ROWS_LOADED: 3xTF32 path only.  A B whose rows are not
+ * 16-byte aligned (ldb % 4 != 0) but whose start is, with K >= 4, is
+ * otherwise copied by TMA as four tensors, one per residue class of rows
+ * k % 4 (the rows of a class lie 4 * ldb floats apart, a multiple of 16
+ * bytes).  With the flag the kernel loads such a B itself.  Both give the
+ * same bits. */
+#define SGEMM_FLAG_B_ROWS_LOADED (1 << 17)
 #define SGEMM_FLAG_DEBUG_WITHHOLD_ARRIVE 1 /* test only: one pipeline arrive
                                               is withheld and the on-device
                                               wait budget is cut to ~1 ms, so

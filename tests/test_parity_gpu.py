@@ -100,6 +100,64 @@ def test_tma_and_load_paths_agree_bitwise(rows):
         assert np.array_equal(c, outs[(0, 0, 0)]), f"offsets {off} differ from the TMA path"
 
 
+B4_CASES = [  # (M, N, K, ldb - N, tile rows): B rows not 16-byte aligned, several K tails
+    (300, 1021, 700, 0, 128), (384, 1413, 1152, 0, 192), (130, 517, 37, 0, 256), (65, 263, 5, 2, 64),
+    (200, 333, 4, 2, 32), (97, 130, 129, 0, 16), (257, 901, 300, 2, 256), (33, 14161, 64, 0, 64)]
+
+
+@pytest.mark.parametrize("case", B4_CASES, ids=[f"{c[0]}x{c[1]}x{c[2]}+{c[3]}-tm{c[4]}" for c in B4_CASES])
+def test_unaligned_b_rows_by_tma(case):
+    """A B whose rows are not 16-byte aligned comes by TMA as four residue
+    classes of rows (k % 4), each class's rows read from a few floats into
+    the copied box.  Against the oracle, and bit for bit the same as the
+    producers loading B themselves (SGEMM_FLAG_B_ROWS_LOADED), on whole-tile
+    and split-K schedules."""
+    M, N, K, pad, rows = case
+    p = _with_c(random_problem(M, N, K, alpha=1.25, beta=0.5, seed=M + 7 * N + K, ldb=N + pad, pad_value=np.nan))
+    assert p.ldb % 4 != 0
+    for sched in (pkg.SGEMM_FLAG_WHOLE_TILES, 0):
+        flags = pkg.SGEMM_FLAG_TILE_ROWS(rows) | sched
+        splits = 0 if sched else 3
+        tma, st = run_sgemm(p, pkg.SGEMM_ALGO_TF32X3, splits=splits, flags=flags)
+        assert st == 0
+        check_against_oracle(p, tma, what=f"{case} residue-class TMA, splits {splits}")
+        loaded, st = run_sgemm(p, pkg.SGEMM_ALGO_TF32X3, splits=splits, flags=flags | pkg.SGEMM_FLAG_B_ROWS_LOADED)
+        assert st == 0
+        assert np.array_equal(tma.view(np.uint32), loaded.view(np.uint32)), f"{case}: TMA and loaded B differ"
+
+
+def test_unaligned_b_rows_batched_and_misaligned_start():
+    """The residue-class maps with a batch dimension (a B stride that is a
+    multiple of 4 floats), and a B whose start is not 16-byte aligned (the
+    producers load it): both against the oracle."""
+    import torch
+    M, N, K, batch = 150, 389, 203, 3
+    ps = [_with_c(random_problem(M, N, K, alpha=0.5, beta=0.25, seed=60 + b, pad_value=0.0), seed=70 + b)
+          for b in range(batch)]
+    for p in ps[1:]:
+        p.A = ps[0].A
+    sB = (K * N + 3) // 4 * 4 + 8
+    sC = M * N + 5
+    hB = np.full(sB * batch, np.nan, np.float32)
+    hC = np.zeros(sC * batch, np.float32)
+    for b, p in enumerate(ps):
+        hB[b * sB:b * sB + K * N] = p.B.reshape(-1)
+        hC[b * sC:b * sC + M * N] = p.C.reshape(-1)
+    dA = torch.from_numpy(ps[0].A).cuda()
+    dB, dC = torch.from_numpy(hB).cuda(), torch.from_numpy(hC).cuda()
+    st = torch.cuda.current_stream()
+    rc = pkg.sgemm_strided_batched(0, 0, M, N, K, 0.5, dA, K, 0, dB, N, sB, 0.25, dC, N, sC, batch, st,
+                                   pkg.SGEMM_ALGO_TF32X3)
+    assert rc == 0 and pkg.sgemm_check_status(st) == 0
+    out = dC.cpu().numpy()
+    for b, p in enumerate(ps):
+        check_against_oracle(p, out[b * sC:b * sC + M * N].reshape(M, N), what=f"batched residue classes, {b}")
+    p = _with_c(random_problem(M, N, K, alpha=1.0, beta=0.5, seed=5, pad_value=np.nan))
+    C, st = run_sgemm(p, pkg.SGEMM_ALGO_TF32X3, offsets=(0, 1, 0))
+    assert st == 0
+    check_against_oracle(p, C, what="B start not 16-byte aligned")
+
+
 @pytest.mark.parametrize("shape", [(40, 2000, 147), (64, 4096, 27), (17, 3000, 333)],
                          ids=["40x2000x147", "64x4096x27", "17x3000x333"])
 def test_unaligned_a_is_staged(shape):
