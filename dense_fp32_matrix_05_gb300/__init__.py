@@ -161,6 +161,7 @@ def conv2d_out_size(H, W, KH, KW, stride=(1, 1), pad=(0, 0), dil=(1, 1)):
 SGEMM_CONV_NO_PAD_COPY = 1
 SGEMM_FLAG_NO_A_COPY = 1 << 16
 SGEMM_FLAG_B_ROWS_LOADED = 1 << 17
+SGEMM_FLAG_TWO_CTAS_PER_SM = 1 << 18
 
 
 def sgemm_conv2d(X, Wt, Y, alpha=1.0, beta=0.0, stride=(1, 1), pad=(0, 0), dil=(1, 1), stream=None,

@@ -37,7 +37,31 @@ struct Workspace {
     size_t ap_bytes = 0;
 };
 
-constexpr int kHostMaxBlocks = 8;  // row blocks of a pipelined sgemm_host
+constexpr int kHostMaxBlocks = 12;  // row (or column) blocks of a pipelined sgemm_host
+
+// Sizes of the blocks a pipelined sgemm_host cuts `total` rows (or columns)
+// into, in multiples of `quantum`: blocks of about total / 5 while more than
+// two of them remain, then halving blocks down to two quanta.  The call's
+// time is the upload of every block plus the last block's GEMM and its
+// download, so the last blocks are made small; the first ones stay large
+// enough for the GEMMs to keep up with the uploads.  Returns the count.
+int host_blocks(int total, int quantum, int sizes[kHostMaxBlocks]) {
+    const int big = std::max(quantum, (total / 5 + quantum - 1) / quantum * quantum);
+    int n = 0, left = total;
+    while (left > 0 && n < kHostMaxBlocks - 1) {
+        int take;
+        if (left > 2 * big) {
+            take = big;
+        } else {
+            take = std::max(2 * quantum, (left / 2 + quantum - 1) / quantum * quantum);
+            if (take >= left) take = left;
+        }
+        sizes[n++] = take;
+        left -= take;
+    }
+    if (left > 0) sizes[n++] = left;
+    return n;
+}
 
 struct HostBuffers {
     float *A = nullptr, *B = nullptr, *C = nullptr;
@@ -355,7 +379,7 @@ size_t span_bytes(int rows, int cols, long long ld) {
 
 bool flags_valid(int flags) {
     if (flags & ~(SGEMM_FLAG_DEBUG_WITHHOLD_ARRIVE | SGEMM_FLAG_WHOLE_TILES | SGEMM_FLAG_SPLIT_TAIL | 0xFF00 |
-                  SGEMM_FLAG_NO_A_COPY))
+                  SGEMM_FLAG_NO_A_COPY | SGEMM_FLAG_B_ROWS_LOADED | SGEMM_FLAG_TWO_CTAS_PER_SM))
         return false;
     const int tm = forced_tile_rows(flags);
     return tm == 0 || sg::tf32x3_supported_tm(tm);
@@ -527,13 +551,27 @@ int run(int M, int N, int K, float alpha, const float *A, int lda, const float *
         }
     }
     GemmArgs g{M, N, K, alpha, beta, A, lda, B, ldb, C, ldc, sA, sB, sC};
+    // two CTAs per SM for short tiles whose A comes by TMA: the split-K
+    // schedule strides its units over twice the SMs
+    const bool dual = (flags & SGEMM_FLAG_TWO_CTAS_PER_SM) && p.path == SGEMM_ALGO_TF32X3 && p.tile_m <= 64 &&
+                      p.vec_a && !trans_b && p.sch.tail_tiles == 0;
+    if (dual) {
+        int sms = 0;
+        {
+            std::lock_guard<std::mutex> lk(g_mu);
+            sms = d->sms;
+        }
+        p.grid = std::min(p.sch.units, 2 * sms);
+        if (p.sch.splits > 1) p.grid = std::max(p.grid, ceil_div(p.sch.units, sg::kTf32x3MaxDefer));
+    }
     cudaError_t e;
     if (trans_b && (p.path != SGEMM_ALGO_TF32X3 || !p.vec_a || !p.vec_b))
         return SGEMM_ERR_INTERNAL;
     if (trans_b)
         e = sg::tf32x3_launch_tb(p.tile_m, g, p.sch, ctl, p.vec_a, p.vec_c, p.grid, stream, batch);
     else if (p.path == SGEMM_ALGO_TF32X3)
-        e = sg::tf32x3_launch(p.tile_m, g, p.sch, ctl, p.vec_a, p.vec_b, p.vec_c, p.grid, stream, batch);
+        e = sg::tf32x3_launch(p.tile_m, g, p.sch, ctl, p.vec_a, p.vec_b, p.vec_c, p.grid, stream, batch,
+                              (flags & SGEMM_FLAG_B_ROWS_LOADED) != 0, dual);
     else if (p.wide)
         e = sg::ffma_wide_launch(g, p.vec_b, p.grid, stream);
     else
@@ -932,17 +970,14 @@ int sgemm_host(int M, int N, int K, float alpha, const float *A, int lda, const 
     // compute.  Each block is a planned GEMM of its own (the same arithmetic
     // per element; a block's schedule may differ from the whole call's).
     const size_t in_bytes = a_bytes + b_bytes + (beta != 0.f ? c_bytes : 0);
-    int nblk = 1;
-    if (in_bytes + c_bytes >= (64u << 20) && M >= 512)
-        nblk = std::min(kHostMaxBlocks, std::max(2, M / 1024));
-    // short and wide (the im2col shapes): column blocks instead; A goes up
-    // first and each block's columns of B (and C) move as pitched copies
-    int ncb = 1;
-    if (nblk == 1 && in_bytes + c_bytes >= (64u << 20) && N >= 8192)
-        ncb = std::min(kHostMaxBlocks, std::max(2, N / 8192));
+    const bool large = in_bytes + c_bytes >= (64u << 20);
+    int sizes[kHostMaxBlocks];
+    // row blocks; short and wide (the im2col shapes): column blocks instead,
+    // A goes up first and each block's columns of B (and C) move as pitched
+    // copies
+    const int nblk = (large && M >= 512) ? host_blocks(M, 128, sizes) : 1;
+    const int ncb = (nblk == 1 && large && N >= 8192) ? host_blocks(N, 1024, sizes) : 1;
     if (ncb > 1) {
-        const int cols = (ceil_div(N, ncb) + 127) / 128 * 128;
-        ncb = ceil_div(N, cols);
         float *dA = h.A, *dB = h.B, *dC = h.C;
         cudaStream_t st = h.stream, up = h.up, down = h.down;
         cudaEvent_t a_in = h.b_in, ev_in[kHostMaxBlocks], ev_out[kHostMaxBlocks];
@@ -956,8 +991,8 @@ int sgemm_host(int M, int N, int K, float alpha, const float *A, int lda, const 
         if ((e = cudaEventRecord(a_in, up)) != cudaSuccess || (e = cudaStreamWaitEvent(st, a_in, 0)) != cudaSuccess)
             return from_cuda(e);
         int first_rc = 0;
-        for (int i = 0; i < ncb; ++i) {
-            const int c0 = i * cols, nc = std::min(cols, N - c0);
+        for (int i = 0, c0 = 0; i < ncb; c0 += sizes[i], ++i) {
+            const int nc = sizes[i];
             const size_t w = static_cast<size_t>(nc) * sizeof(float);
             if (use_ab && (e = cudaMemcpy2DAsync(dB + c0, static_cast<size_t>(ldb) * sizeof(float), B + c0,
                                                  static_cast<size_t>(ldb) * sizeof(float), w, static_cast<size_t>(K),
@@ -988,8 +1023,6 @@ int sgemm_host(int M, int N, int K, float alpha, const float *A, int lda, const 
         return from_cuda(e != cudaSuccess ? e : e2);
     }
     if (nblk > 1) {
-        const int rows = (ceil_div(M, nblk) + 255) / 256 * 256;
-        nblk = ceil_div(M, rows);
         float *dA = h.A, *dB = h.B, *dC = h.C;
         cudaStream_t st = h.stream, up = h.up, down = h.down;
         cudaEvent_t b_in = h.b_in, ev_in[kHostMaxBlocks], ev_out[kHostMaxBlocks];
@@ -1005,8 +1038,8 @@ int sgemm_host(int M, int N, int K, float alpha, const float *A, int lda, const 
         if ((e = cudaEventRecord(b_in, up)) != cudaSuccess || (e = cudaStreamWaitEvent(st, b_in, 0)) != cudaSuccess)
             return from_cuda(e);
         int first_rc = 0;
-        for (int i = 0; i < nblk; ++i) {
-            const int r0 = i * rows, mr = std::min(rows, M - r0);
+        for (int i = 0, r0 = 0; i < nblk; r0 += sizes[i], ++i) {
+            const int mr = sizes[i];
             const size_t ao = static_cast<size_t>(r0) * lda, co = static_cast<size_t>(r0) * ldc;
             const size_t cb = span_bytes(mr, N, ldc);
             if (use_ab && (e = cudaMemcpyAsync(dA + ao, A + ao, span_bytes(mr, K, lda), cudaMemcpyHostToDevice,

@@ -14,10 +14,12 @@
 //     its 16-byte chunks XOR-swizzled by (row / 4) % 4, so the four distinct
 //     rows a warp reads per instruction fall in four different bank groups;
 //     B is kept N-major, read as 8 consecutive 16-byte chunks per warp;
-//   - per 4-k step a thread loads its 8 rows x 4 k of A and, per k, 8 values
-//     of B (16 LDS.128 per 256 FMAs) and updates 64 accumulators, held as
-//     32 column pairs so that each k takes 32 packed fma.rn.f32x2 (same
-//     per-element rounding and order as fmaf, half the issue slots);
+//   - per 2-k step a thread loads its 8 rows x 2 k of A (8-byte loads: with
+//     4 k at a time the A fragment pushed the 128 x 128 tile past the 128
+//     registers two CTAs per SM allow, and it spilled) and, per k, 8 values
+//     of B, and updates 64 accumulators, held as 32 column pairs so that
+//     each k takes 32 packed fma.rn.f32x2 (same per-element rounding and
+//     order as fmaf, half the issue slots);
 //   - epilogue alpha*acc + beta*C (C not read when beta == 0), 128-bit
 //     accesses when C rows are aligned, predicated edges; split-K partials
 //     go to a workspace and the last slice to arrive sums them in order.
@@ -148,21 +150,18 @@ __global__ void __launch_bounds__(kThreads, 2)
         const uint32_t sA = s0 + static_cast<uint32_t>((t % STAGES) * Cf::kStageFloats * 4);
         const uint32_t sB = sA + Cf::kAFloats * 4;
 #pragma unroll
-        for (int kq = 0; kq < 4; ++kq) {
-            float a[8][4];
-            const uint32_t chunk = static_cast<uint32_t>((kq ^ lm) << 2);
+        for (int kh = 0; kh < 8; ++kh) {
+            const int kq = kh >> 1;
+            float a[8][2];
+            const uint32_t chunk = static_cast<uint32_t>(((kq ^ lm) << 2) + 2 * (kh & 1));
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const float4 v0 = lds128(sA + ((row_base + i) * kBK + chunk) * 4);
-                const float4 v1 = lds128(sA + ((row_base + 16 + i) * kBK + chunk) * 4);
-                a[i][0] = v0.x; a[i][1] = v0.y; a[i][2] = v0.z; a[i][3] = v0.w;
-                a[4 + i][0] = v1.x; a[4 + i][1] = v1.y; a[4 + i][2] = v1.z; a[4 + i][3] = v1.w;
+                lds2f(sA + ((row_base + i) * kBK + chunk) * 4, a[i][0], a[i][1]);
+                lds2f(sA + ((row_base + 16 + i) * kBK + chunk) * 4, a[4 + i][0], a[4 + i][1]);
             }
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                // 8 values of B as 4 column pairs; a[i] broadcast into a pair:
-                // 32 paired FMAs per k instead of 64 single ones
-                const int k = kq * 4 + kk;
+            for (int kk = 0; kk < 2; ++kk) {
+                const int k = kh * 2 + kk;
                 uint64_t b[4];
                 lds_pairs(sB + (k * BN + col_base) * 4, b[0], b[1]);
                 lds_pairs(sB + (k * BN + col_base + 32) * 4, b[2], b[3]);

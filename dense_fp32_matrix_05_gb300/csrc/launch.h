@@ -58,9 +58,10 @@ cudaError_t filter_ohwi_launch(const float *w, int F, int C, int KH, int KW, flo
 // batch: matrices of a strided batch (g.sA / sB / sC; s.tpb tiles each).
 // b_rows: a B whose rows are not 16-byte aligned is loaded by the producers
 // instead of being copied by TMA as four residue classes of rows.
+// dual (tm <= 64, A by TMA): two CTAs per SM, the grid counting both.
 cudaError_t tf32x3_launch(int tm, const GemmArgs &g, const Schedule &s, const DeviceCtl &ctl,
                           int vec_a, int vec_b, int vec_c, int grid, cudaStream_t stream, int batch = 1,
-                          bool b_rows = false);
+                          bool b_rows = false, bool dual = false);
 
 // FFMA path.  (bm, bn) in {(128,128), (64,256), (32,512)}.
 bool ffma_supported_tile(int bm, int bn);

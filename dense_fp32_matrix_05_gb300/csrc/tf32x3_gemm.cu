@@ -163,16 +163,16 @@ bool make_tmap_c(const GemmArgs &g, int batch, CUtensorMap *map) {
 
 namespace {
 
-template <int TM, bool TA, bool TB, bool B4 = false>
+template <int TM, bool TA, bool TB, bool B4 = false, bool DUAL = false>
 cudaError_t launch_tm(const GemmArgs &g, const Schedule &s, const DeviceCtl &ctl, int vec_a, int tma_c, int grid,
                       const CUtensorMap &map_a, const CUtensorMap (&map_b)[4], uint32_t b_offs,
                       const CUtensorMap &map_c, cudaStream_t stream) {
-    using C = tf32x3::Cfg<TM, TB, B4>;
-    auto kern = tf32x3::tf32x3_gemm_kernel<TM, TA, TB, kConvNone, false, B4>;
+    using C = tf32x3::Cfg<TM, TB, B4, DUAL>;
+    auto kern = tf32x3::tf32x3_gemm_kernel<TM, TA, TB, kConvNone, false, B4, DUAL>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    return launch_pdl(kern, grid, tf32x3::Roles<TM, TA, TB>::kThreads, C::kSmemBytes, stream, g, s, ctl, vec_a, tma_c,
-                      b_offs, map_a, map_b[0], map_c, map_b[1], map_b[2], map_b[3]);
+    return launch_pdl(kern, grid, tf32x3::Roles<TM, TA, TB, DUAL>::kThreads, C::kSmemBytes, stream, g, s, ctl, vec_a,
+                      tma_c, b_offs, map_a, map_b[0], map_c, map_b[1], map_b[2], map_b[3]);
 }
 
 // Operands go through TMA whenever their rows are 16-byte aligned: the deep
@@ -184,7 +184,7 @@ cudaError_t launch_tm(const GemmArgs &g, const Schedule &s, const DeviceCtl &ctl
 // own loads.
 template <int TM>
 cudaError_t launch_rows(const GemmArgs &g, const Schedule &s, const DeviceCtl &ctl, int vec_a, int vec_b,
-                        int vec_c, int grid, int batch, bool b_rows, cudaStream_t stream) {
+                        int vec_c, int grid, int batch, bool b_rows, bool dual, cudaStream_t stream) {
     CUtensorMap ma, mb[4], mc;
     std::memset(&ma, 0, sizeof(ma));
     std::memset(mb, 0, sizeof(mb));
@@ -194,6 +194,14 @@ cudaError_t launch_rows(const GemmArgs &g, const Schedule &s, const DeviceCtl &c
     const bool tb = vec_b && make_tmap_b(g, batch, &mb[0]);
     const bool tb4 = !vec_b && !b_rows && make_tmap_b4(g, batch, mb, &offs);
     const int tc = (vec_c && make_tmap_c(g, batch, &mc)) ? 1 : 0;
+    if constexpr (TM <= 64) {
+        // two CTAs per SM (A by TMA): the grid already counts two per SM
+        if (dual && ta) {
+            if (tb) return launch_tm<TM, true, true, false, true>(g, s, ctl, vec_a, tc, grid, ma, mb, 0, mc, stream);
+            if (tb4) return launch_tm<TM, true, true, true, true>(g, s, ctl, vec_a, tc, grid, ma, mb, offs, mc, stream);
+            return launch_tm<TM, true, false, false, true>(g, s, ctl, vec_a, tc, grid, ma, mb, 0, mc, stream);
+        }
+    }
     if (tb) {
         if (ta) return launch_tm<TM, true, true>(g, s, ctl, vec_a, tc, grid, ma, mb, 0, mc, stream);
         return launch_tm<TM, false, true>(g, s, ctl, vec_a, tc, grid, ma, mb, 0, mc, stream);
@@ -268,14 +276,14 @@ int tf32x3_smem_bytes(int tm) {
 }
 
 cudaError_t tf32x3_launch(int tm, const GemmArgs &g, const Schedule &s, const DeviceCtl &ctl, int vec_a,
-                          int vec_b, int vec_c, int grid, cudaStream_t stream, int batch, bool b_rows) {
+                          int vec_b, int vec_c, int grid, cudaStream_t stream, int batch, bool b_rows, bool dual) {
     switch (tm) {
-        case 16: return launch_rows<16>(g, s, ctl, vec_a, vec_b, vec_c, grid, batch, b_rows, stream);
-        case 32: return launch_rows<32>(g, s, ctl, vec_a, vec_b, vec_c, grid, batch, b_rows, stream);
-        case 64: return launch_rows<64>(g, s, ctl, vec_a, vec_b, vec_c, grid, batch, b_rows, stream);
-        case 128: return launch_rows<128>(g, s, ctl, vec_a, vec_b, vec_c, grid, batch, b_rows, stream);
-        case 192: return launch_rows<192>(g, s, ctl, vec_a, vec_b, vec_c, grid, batch, b_rows, stream);
-        case 256: return launch_rows<256>(g, s, ctl, vec_a, vec_b, vec_c, grid, batch, b_rows, stream);
+        case 16: return launch_rows<16>(g, s, ctl, vec_a, vec_b, vec_c, grid, batch, b_rows, dual, stream);
+        case 32: return launch_rows<32>(g, s, ctl, vec_a, vec_b, vec_c, grid, batch, b_rows, dual, stream);
+        case 64: return launch_rows<64>(g, s, ctl, vec_a, vec_b, vec_c, grid, batch, b_rows, dual, stream);
+        case 128: return launch_rows<128>(g, s, ctl, vec_a, vec_b, vec_c, grid, batch, b_rows, false, stream);
+        case 192: return launch_rows<192>(g, s, ctl, vec_a, vec_b, vec_c, grid, batch, b_rows, false, stream);
+        case 256: return launch_rows<256>(g, s, ctl, vec_a, vec_b, vec_c, grid, batch, b_rows, false, stream);
         default: return cudaErrorInvalidValue;
     }
 }

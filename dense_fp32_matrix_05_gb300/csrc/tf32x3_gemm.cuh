@@ -66,13 +66,16 @@ constexpr int kEpiBarrierId = 1;
 // flight while it splits one.  With A arriving by TMA the registers only
 // hold B^T; without it they also hold A chunks, so wide tiles use fewer,
 // larger groups to stay within the register budget.
-template <int TM, bool TMA_A, bool TMA_B>
+// DUAL: two CTAs share an SM (each with half the tensor memory and shared
+// memory); one group of 4 producer warps each keeps the pair within the
+// SM's registers (2 x 320 threads x 96).
+template <int TM, bool TMA_A, bool TMA_B, bool DUAL = false>
 struct Roles {
     static constexpr bool kTma = TMA_A || TMA_B;  // the TMA thread fills stages
     // With A copied by TMA the producers hold few registers: 12 warps in 3
     // groups leave 96 registers per thread; otherwise 16 warps.
-    static constexpr int kProdWarps = TMA_A ? 12 : 16;
-    static constexpr int kGroups = TMA_A ? 3 : (TM <= 64 ? 4 : 2);
+    static constexpr int kProdWarps = DUAL ? 4 : (TMA_A ? 12 : 16);
+    static constexpr int kGroups = DUAL ? 1 : (TMA_A ? 3 : (TM <= 64 ? 4 : 2));
     static constexpr int kWarpsPerGroup = kProdWarps / kGroups;
     static_assert(kWarpsPerGroup % 4 == 0, "each group covers the four lane quadrants");
     static constexpr int kGroupThreads = kWarpsPerGroup * 32;
@@ -81,15 +84,16 @@ struct Roles {
     static constexpr int kMmaWarp = kEpiWarps + kProdWarps;
     static constexpr int kTmaWarp = kMmaWarp + 1;
     static constexpr int kThreads = (kEpiWarps + kProdWarps + 2) * 32;
+    static constexpr int kCtasPerSm = DUAL ? 2 : 1;
 };
 
-// Tensor memory (512 columns of 128 lanes x 32 bit): accumulators of TM
-// columns each, then a ring of STAGES B^T stages of 32 columns (16 hi + 16 lo
-// k values per lane = per C column).
+// Tensor memory (512 columns of 128 lanes x 32 bit per SM; 256 per CTA when
+// two CTAs share the SM): accumulators of TM columns each, then a ring of
+// STAGES B^T stages of 32 columns (16 hi + 16 lo k values per lane = per C
+// column).
 constexpr uint32_t kTmemCols = 512;
 constexpr int kRingColsPerStage = 2 * kBK;
 constexpr int kMaxStages = 12;
-__host__ __device__ constexpr int nacc_for(int tm) { return tm >= 192 ? 1 : 2; }
 // Short tiles (TM <= 64) pair the products: a tf32 MMA costs at least ~40 ns
 // whatever its N up to 128, and in a stage the lo half of the A tile follows
 // the hi half with the same row pitch, so [A_hi; A_lo] is one 2TM-row
@@ -99,14 +103,20 @@ __host__ __device__ constexpr int nacc_for(int tm) { return tm >= 192 ? 1 : 2; }
 // the epilogue adds its halves.
 __host__ __device__ constexpr bool paired_for(int tm) { return tm <= 64; }
 __host__ __device__ constexpr int acc_cols_for(int tm) { return (paired_for(tm) ? 2 : 1) * tm; }
+// Accumulators: two (a tile's epilogue overlaps the next tile's MMAs) where
+// they leave room for 4 ring stages; in 512 columns, one from TM = 192 up.
+__host__ __device__ constexpr int nacc_for(int tm, int cols = 512) {
+    return cols == 512 ? (tm >= 192 ? 1 : 2) : (2 * acc_cols_for(tm) + 4 * kRingColsPerStage <= cols ? 2 : 1);
+}
 // every tensor-memory column the accumulators leave, up to kMaxStages (short
 // tiles stream long B panels and want many copies in flight)
-__host__ __device__ constexpr int stages_for(int tm) {
-    return (static_cast<int>(kTmemCols) - nacc_for(tm) * acc_cols_for(tm)) / kRingColsPerStage < kMaxStages
-               ? (static_cast<int>(kTmemCols) - nacc_for(tm) * acc_cols_for(tm)) / kRingColsPerStage
+__host__ __device__ constexpr int stages_for(int tm, int cols = 512) {
+    return (cols - nacc_for(tm, cols) * acc_cols_for(tm)) / kRingColsPerStage < kMaxStages
+               ? (cols - nacc_for(tm, cols) * acc_cols_for(tm)) / kRingColsPerStage
                : kMaxStages;
 }
-constexpr int kSmemLimit = 232448;  // dynamic shared memory one CTA may use on sm_103a
+constexpr int kSmemLimit = 232448;      // dynamic shared memory one CTA may use on sm_103a
+constexpr int kSmemLimitDual = 115712;  // per CTA when two share an SM (228 KB less 1 KB each)
 // C chunks the epilogue stages in shared memory for TMA copies (16 rows of
 // the 128 tile columns each); loads run two chunks ahead of the arithmetic.
 constexpr int kEpiBufs = 3;
@@ -134,11 +144,13 @@ constexpr int kB4SlabBytes = 4 * kB4ClassBytes;
 // split; B4: that slab holds the four residue classes of an unaligned B.
 // Shared memory: the stages' A tiles (hi, lo), then the stages' B slabs,
 // then the epilogue's C buffers and the barriers.
-template <int TM, bool TMA_B = false, bool B4 = false>
+template <int TM, bool TMA_B = false, bool B4 = false, bool DUAL = false>
 struct Cfg {
     static_assert(TM % 16 == 0 && TM >= 16 && TM <= 256, "MMA N for M=128 must be 16..256, step 16");
     static_assert(TMA_B || !B4, "the residue-class form is a TMA form");
-    static constexpr int kNacc = nacc_for(TM);
+    static constexpr uint32_t kCols = DUAL ? kTmemCols / 2 : kTmemCols;  // tensor-memory columns of the CTA
+    static constexpr int kSmemMax = DUAL ? kSmemLimitDual : kSmemLimit;
+    static constexpr int kNacc = nacc_for(TM, kCols);
     static constexpr int kABytes = TM * kBK * 4;  // A tile (MMA B operand), one of hi / lo
     static constexpr int kOffAHi = 0;             // also where TMA lands the raw A tile
     static constexpr int kOffALo = kABytes;
@@ -149,9 +161,9 @@ struct Cfg {
     static constexpr int kEpiBufBytes = kEpiBufs * kEpiChunkBytes;
     // as many stages as tensor memory and the 227 KB of shared memory allow
     // (1 KB of alignment slack and up to 528 bytes of barriers and words)
-    static constexpr int kStageRoom = kSmemLimit - 1024 - 528 - kEpiBufBytes;
-    static constexpr int kStages = stages_for(TM) < kStageRoom / kStageBytes ? stages_for(TM)
-                                                                             : kStageRoom / kStageBytes;
+    static constexpr int kStageRoom = kSmemMax - 1024 - 528 - kEpiBufBytes;
+    static constexpr int kStages = stages_for(TM, kCols) < kStageRoom / kStageBytes ? stages_for(TM, kCols)
+                                                                                    : kStageRoom / kStageBytes;
     static constexpr int kOffBRegion = kStages * kAStageBytes;  // slab of stage s at + s * kBRawBytes
     static constexpr int kOffEpi = kStages * kStageBytes;
     static_assert(kAStageBytes % 1024 == 0, "A tiles must keep 1 KB alignment (64-byte swizzle atoms)");
@@ -160,7 +172,7 @@ struct Cfg {
     static constexpr bool kPaired = paired_for(TM);
     static constexpr int kAccCols = acc_cols_for(TM);  // one accumulator (two TM halves when paired)
     static constexpr int kRingCol = kNacc * kAccCols;
-    static_assert(kRingCol + kStages * kRingColsPerStage <= static_cast<int>(kTmemCols), "tensor memory");
+    static_assert(kRingCol + kStages * kRingColsPerStage <= static_cast<int>(kCols), "tensor memory");
     static constexpr int kChunk = 16;  // accumulator columns per tensor-memory load in the epilogue
     static constexpr uint32_t kIdesc = umma_idesc_tf32(kTileN, TM);
     static constexpr uint32_t kIdescPair = umma_idesc_tf32(kTileN, 2 * TM);  // N = 2TM: [A_hi; A_lo]
@@ -172,10 +184,10 @@ struct Cfg {
     static constexpr int kBarBytes = 8 * (3 * kStages + 5 + kEpiBufs) + 4 * (4 + 5 * kMaxDefer);
     static constexpr int kSmemBytes = 1024 + kOffEpi + kEpiBufBytes + kBarBytes;
     static_assert(kBarBytes <= 528, "room kept for the barriers");
-    static_assert(kSmemBytes <= kSmemLimit, "shared memory per CTA");
+    static_assert(kSmemBytes <= kSmemMax, "shared memory per CTA");
     // a dense convolution's tap table (kConvTabMax ints, 16-byte aligned)
     static constexpr int kConvTabBytes = kConvTabMax * 4 + 16;
-    static_assert(TMA_B || kSmemBytes + kConvTabBytes <= kSmemLimit, "shared memory with a tap table");
+    static_assert(TMA_B || DUAL || kSmemBytes + kConvTabBytes <= kSmemLimit, "shared memory with a tap table");
     static_assert(kStages >= 4, "pipeline depth");
 };
 
@@ -541,24 +553,38 @@ __device__ __forceinline__ bool epi_all(bool v) {
 
 // One 16-column chunk of an accumulator: 16 C rows of this thread's column.
 // A paired accumulator holds hi*hi + lo*hi in its first TM columns and hi*lo
-// in the next TM; the chunk is their sum.
-template <int TM>
-__device__ __forceinline__ void acc_chunk(uint32_t taddr, float (&v)[16]) {
+// in the next TM; the chunk is their sum.  The epilogue issues the load of
+// chunk c + 1 (issue) before it stores chunk c, and collects it (finish)
+// at the start of the next iteration, so the tensor-memory latency overlaps
+// the stores, the proxy fence and the barrier of chunk c.
+// The look-ahead costs 16 registers per epilogue thread (32 for a paired
+// accumulator): kernels whose register budget has no room for them (paired
+// tiles, and the 16-producer-warp forms when A is not copied by TMA) load
+// each chunk where it is used (AHEAD false), which keeps them clear of
+// spills.
+template <int TM, bool AHEAD>
+struct AccChunk {
+    static constexpr bool kPaired = paired_for(TM);
+    static constexpr bool kAhead = AHEAD && !kPaired;
     uint32_t r[16];
-    tmem_ld32x16_issue(taddr, r);
-    if constexpr (paired_for(TM)) {
-        uint32_t q[16];
-        tmem_ld32x16_issue(taddr + static_cast<uint32_t>(TM), q);
-        tmem_ld_wait16(r);
-        tmem_ld_wait16(q);
-#pragma unroll
-        for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]) + __uint_as_float(q[j]);
-    } else {
-        tmem_ld_wait16(r);
-#pragma unroll
-        for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
+    uint32_t q[kPaired ? 16 : 1];
+    __device__ __forceinline__ void issue(uint32_t taddr) {
+        tmem_ld32x16_issue(taddr, r);
+        if constexpr (kPaired) tmem_ld32x16_issue(taddr + static_cast<uint32_t>(TM), *reinterpret_cast<uint32_t(*)[16]>(q));
     }
-}
+    // wait for the loads issued last (every tcgen05.ld of this thread) and sum
+    __device__ __forceinline__ void finish(float (&v)[16]) {
+        tmem_ld_wait16(r);
+        if constexpr (kPaired) {
+            tmem_ld_wait16(*reinterpret_cast<uint32_t(*)[16]>(q));
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]) + __uint_as_float(q[j]);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
+        }
+    }
+};
 
 // Last-arriver sum of a shared tile, by a team of nw warps (wid = this
 // warp's index in the team).  The nseg partial tiles (TM x 128, row-major,
@@ -692,16 +718,19 @@ __device__ __forceinline__ void prefetch_c_tile(const GemmArgs &g, int bi, int m
 // B4: B's rows are not 16-byte aligned; tmap_b, tmap_b1, tmap_b2, tmap_b3
 // describe its residue classes k % 4 = 0..3 (each N + o_r floats wide, box
 // 132 x 4, no swizzle) and b_offs packs the o_r; needs TMA_B.
-template <int TM, bool TMA_A, bool TMA_B, int CONV = kConvNone, bool TRANS_B = false, bool B4 = false>
-__global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
+// DUAL: two CTAs per SM (Roles, Cfg).
+template <int TM, bool TMA_A, bool TMA_B, int CONV = kConvNone, bool TRANS_B = false, bool B4 = false,
+          bool DUAL = false>
+__global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B, DUAL>::kThreads, (DUAL ? 2 : 1))
     tf32x3_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ Schedule sch,
                        const __grid_constant__ DeviceCtl ctl, int vec_a, int tma_c, uint32_t b_offs,
                        const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                        const __grid_constant__ CUtensorMap tmap_c, const __grid_constant__ CUtensorMap tmap_b1,
                        const __grid_constant__ CUtensorMap tmap_b2, const __grid_constant__ CUtensorMap tmap_b3) {
-    using C = Cfg<TM, TMA_B, B4>;
-    using R = Roles<TM, TMA_A, TMA_B>;
+    using C = Cfg<TM, TMA_B, B4, DUAL>;
+    using R = Roles<TM, TMA_A, TMA_B, DUAL>;
     static_assert(CONV == kConvNone || !TMA_B, "a convolution gathers B in the producers");
+    static_assert(!DUAL || (TMA_A && CONV == kConvNone), "two CTAs per SM: A by TMA (producer registers)");
     static_assert(!TRANS_B || (TMA_B && CONV == kConvNone), "a transposed B comes by TMA");
     static_assert(!B4 || (TMA_B && !TRANS_B && CONV == kConvNone), "residue classes of a row-major B");
     constexpr int S = C::kStages;
@@ -755,7 +784,7 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
         fence_mbar_init();
     }
     if (warp == R::kMmaWarp) {
-        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+        tmem_alloc(smem_u32(tmem_slot), C::kCols);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -770,6 +799,7 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
 
     if (warp < kEpiWarps) {
         // ------------------------------------------------------ epilogue
+        using Acc = AccChunk<TM, TMA_A>;
         const int nl = warp * 32 + lane;  // tensor-memory lane = column within the tile
         int it = 0;
         uint32_t cpar = 0;      // per C buffer: parity of its next c_full phase
@@ -818,6 +848,8 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
                 const int n0 = c.nt * kTileN;
                 const int nch = min(TM / CH, (g.M - m0 + CH - 1) / CH);  // chunks with rows below M
                 bool ok = true;
+                Acc ld;
+                if (Acc::kAhead && nch > 0) ld.issue(t0);
 #pragma unroll 1
                 for (int ch = 0; ch < nch; ++ch) {
                     const int b = ch % kEpiBufs;
@@ -826,6 +858,7 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
                         const bool wc = mbar_wait_bounded(cfull0 + 8u * b, (cpar >> b) & 1u, abort_flag, ctl,
                                                           kStatusTimeoutEpilogue);
                         if (!epi_all(wc)) {
+                            tmem_ld_wait();  // the chunk load in flight lands before the CTA goes on
                             ok = false;
                             break;
                         }
@@ -834,7 +867,9 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
                     }
                     const int mb = m0 + ch * CH;
                     float v[CH];
-                    acc_chunk<TM>(t0 + ch * CH, v);
+                    if (!Acc::kAhead) ld.issue(t0 + ch * CH);
+                    ld.finish(v);
+                    if (Acc::kAhead && ch + 1 < nch) ld.issue(t0 + (ch + 1) * CH);
                     bool nan = false;
 #pragma unroll
                     for (int j = 0; j < CH; ++j) nan |= v[j] != v[j];
@@ -880,6 +915,8 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
                 const bool read_c = g.beta != 0.f;
                 const bool n_ok = n < g.N;
                 float *cbase = g.C + c.b * g.sC + static_cast<long long>(m0) * g.ldc + n;
+                Acc ld;
+                if (Acc::kAhead) ld.issue(t0);
 #pragma unroll 1
                 for (int ch = 0; ch < TM / CH; ++ch) {
                     const int mb = m0 + ch * CH;
@@ -891,7 +928,9 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
                             old[j] = (n_ok && mb + j < g.M) ? cp[j * g.ldc] : 0.f;
                     }
                     float v[CH];
-                    acc_chunk<TM>(t0 + ch * CH, v);
+                    if (!Acc::kAhead) ld.issue(t0 + ch * CH);
+                    ld.finish(v);
+                    if (Acc::kAhead && ch + 1 < TM / CH) ld.issue(t0 + (ch + 1) * CH);
                     bool nan = false;
 #pragma unroll
                     for (int j = 0; j < CH; ++j) nan |= v[j] != v[j];
@@ -925,10 +964,14 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
                 // unit to arrive adds all partials in segment order
                 constexpr int kTileElems = kTileN * TM;
                 float *wt = ctl.ws + (c.slot0 + c.seg) * kTileElems;
+                Acc ld;
+                if (Acc::kAhead) ld.issue(t0);
 #pragma unroll 1
                 for (int ch = 0; ch < TM / CH; ++ch) {
                     float v[CH];
-                    acc_chunk<TM>(t0 + ch * CH, v);
+                    if (!Acc::kAhead) ld.issue(t0 + ch * CH);
+                    ld.finish(v);
+                    if (Acc::kAhead && ch + 1 < TM / CH) ld.issue(t0 + (ch + 1) * CH);
 #pragma unroll
                     for (int j = 0; j < CH; ++j) __stcg(wt + (ch * CH + j) * kTileN + nl, v[j]);
                 }
@@ -1152,7 +1195,7 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
     __syncthreads();
     if (warp == R::kMmaWarp) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, kTmemCols);
+        tmem_dealloc(tmem_base, C::kCols);
     }
     // deferred sums of shared tiles, by every warp of the CTA
     const int nd = *s_ndefer;

@@ -92,6 +92,11 @@ typedef struct CUstream_st *sgemm_stream_t;
  * bytes).  With the flag the kernel loads such a B itself.  Both give the
  * same bits. */
 #define SGEMM_FLAG_B_ROWS_LOADED (1 << 17)
+/* SGEMM_FLAG_TWO_CTAS_PER_SM: 3xTF32 path, tiles of at most 64 rows whose A
+ * comes by TMA, split-K schedules: run two CTAs per SM, each with half the
+ * tensor memory and shared memory and one group of producer warps, so that
+ * two independent pipelines share each SM.  Same bits. */
+#define SGEMM_FLAG_TWO_CTAS_PER_SM (1 << 18)
 #define SGEMM_FLAG_DEBUG_WITHHOLD_ARRIVE 1 /* test only: one pipeline arrive
                                               is withheld and the on-device
                                               wait budget is cut to ~1 ms, so

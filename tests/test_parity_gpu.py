@@ -126,6 +126,26 @@ def test_unaligned_b_rows_by_tma(case):
         assert np.array_equal(tma.view(np.uint32), loaded.view(np.uint32)), f"{case}: TMA and loaded B differ"
 
 
+DUAL_CASES = [(64, 5000, 147, 64, 1), (50, 3000, 300, 64, 3), (32, 4100, 27, 32, 1), (20, 2000, 40, 16, 2),
+              (64, 1021, 128, 64, 1)]
+
+
+@pytest.mark.parametrize("case", DUAL_CASES, ids=[f"{c[0]}x{c[1]}x{c[2]}-tm{c[3]}-s{c[4]}" for c in DUAL_CASES])
+def test_two_ctas_per_sm_same_bits(case):
+    """Short tiles run as two CTAs per SM (each with half the tensor and
+    shared memory): against the oracle, and bit for bit the same as one CTA
+    per SM, with whole tiles and split-K, aligned and unaligned B rows."""
+    M, N, K, rows, splits = case
+    p = _with_c(random_problem(M, N, K, alpha=0.75, beta=0.5, seed=M * 31 + N + K, pad_value=0.0))
+    flags = pkg.SGEMM_FLAG_TILE_ROWS(rows)
+    two, st = run_sgemm(p, pkg.SGEMM_ALGO_TF32X3, splits=splits, flags=flags | pkg.SGEMM_FLAG_TWO_CTAS_PER_SM)
+    assert st == 0
+    check_against_oracle(p, two, what=f"{case} two CTAs per SM")
+    one, st = run_sgemm(p, pkg.SGEMM_ALGO_TF32X3, splits=splits, flags=flags)
+    assert st == 0
+    assert np.array_equal(two.view(np.uint32), one.view(np.uint32)), f"{case}: one and two CTAs per SM differ"
+
+
 def test_unaligned_b_rows_batched_and_misaligned_start():
     """The residue-class maps with a batch dimension (a B stride that is a
     multiple of 4 floats), and a B whose start is not 16-byte aligned (the
