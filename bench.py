@@ -48,12 +48,18 @@ PAGES_5120_TFLOPS = 13.63498
 TF32_OVER_BF16 = 1.1 / 2.25
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
                   "sm_max_mhz": 2070.0}
-KERNEL_SOURCES = ["dense_fp32_matrix_05_gb300/csrc/tf32x3_gemm.cuh",
-                  "dense_fp32_matrix_05_gb300/csrc/ffma_gemm.cuh",
-                  "dense_fp32_matrix_05_gb300/csrc/common.cuh",
-                  "dense_fp32_matrix_05_gb300/csrc/ptx.cuh",
-                  "dense_fp32_matrix_05_gb300/csrc/ffma_wide.cu",
-                  "dense_fp32_matrix_05_gb300/csrc/conv_gemm.cu"]
+# The sources each kernel family's code comes from: a committed ncu summary
+# records the hash of its family's sources, so work on one family does not
+# retire the others' summaries.
+_COMMON_SOURCES = ["dense_fp32_matrix_05_gb300/csrc/common.cuh", "dense_fp32_matrix_05_gb300/csrc/ptx.cuh"]
+KERNEL_SOURCES = {
+    "tf32x3": ["dense_fp32_matrix_05_gb300/csrc/tf32x3_gemm.cuh", "dense_fp32_matrix_05_gb300/csrc/tf32x3_gemm.cu",
+               "dense_fp32_matrix_05_gb300/csrc/gemm_tb.cu", "dense_fp32_matrix_05_gb300/csrc/conv_gemm.cu"]
+              + _COMMON_SOURCES,
+    "ffma": ["dense_fp32_matrix_05_gb300/csrc/ffma_gemm.cuh", "dense_fp32_matrix_05_gb300/csrc/ffma_gemm.cu"]
+            + _COMMON_SOURCES,
+    "ffma_wide": ["dense_fp32_matrix_05_gb300/csrc/ffma_wide.cu"] + _COMMON_SOURCES,
+}
 L2_FLUSH_BYTES = 512 << 20  # written between timed steps of workloads that fit in the 129 MB L2
 
 
@@ -70,11 +76,16 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_hash() -> str:
-    """Hash of the kernel sources' code: comments and blank lines are left
-    out, so editing a comment does not retire a recorded ncu summary."""
+def kernel_family(path_name: str) -> str:
+    """The kernel family of a summary name (tf32x3, tf32x3_NT, ffma_wide ...)."""
+    return "ffma_wide" if path_name.startswith("ffma_wide") else ("ffma" if path_name.startswith("ffma") else "tf32x3")
+
+
+def kernel_source_hash(family: str = "tf32x3") -> str:
+    """Hash of one kernel family's source code: comments and blank lines are
+    left out, so editing a comment does not retire a recorded ncu summary."""
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in KERNEL_SOURCES[family]:
         with open(os.path.join(ROOT, rel)) as f:
             text = f.read()
         text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
@@ -100,7 +111,7 @@ def recorded_traffic(workload: str, path_name: str):
     text = open(fn).read()
     m_hash = re.search(r"kernel_source_hash:\s*([0-9a-f]+)", text)
     m_bytes = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    if not m_hash or not m_bytes or m_hash.group(1) != kernel_source_hash():
+    if not m_hash or not m_bytes or m_hash.group(1) != kernel_source_hash(kernel_family(path_name)):
         return None
     return float(m_bytes.group(1))
 

@@ -23,7 +23,7 @@ __all__ = [
     "SgemmError", "library", "lib_path", "declared_functions",
     "sgemm", "sgemm_ex", "sgemm_host", "sgemm_plan_info", "sgemm_check_status",
     "sgemm_status_string", "sgemm_release", "sgemm_version", "sgemm_noalloc", "sgemm_noalloc_debug_flags", "sgemm_tf32_mma_rate", "sgemm_ffma_rate", "sgemm_t", "sgemm_strided_batched", "sgemm_conv2d", "sgemm_conv2d_ex", "SGEMM_CONV_NO_PAD_COPY", "conv2d_out_size", "matmul",
-    "SGEMM_ERR_SCRATCH_LIMIT",
+    "SGEMM_ERR_SCRATCH_LIMIT", "SGEMM_ERR_OUT_OF_BOUNDS",
 ]
 
 SGEMM_ALGO_AUTO = 0
@@ -45,6 +45,7 @@ SGEMM_ERR_UNSUPPORTED_DEVICE = 10003
 SGEMM_ERR_WORKSPACE = 10004
 SGEMM_ERR_INTERNAL = 10005
 SGEMM_ERR_SCRATCH_LIMIT = 10006
+SGEMM_ERR_OUT_OF_BOUNDS = 10007
 
 HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
                       "include", "sgemm_gb300.h")
@@ -161,7 +162,6 @@ def conv2d_out_size(H, W, KH, KW, stride=(1, 1), pad=(0, 0), dil=(1, 1)):
 SGEMM_CONV_NO_PAD_COPY = 1
 SGEMM_FLAG_NO_A_COPY = 1 << 16
 SGEMM_FLAG_B_ROWS_LOADED = 1 << 17
-SGEMM_FLAG_TWO_CTAS_PER_SM = 1 << 18
 
 
 def sgemm_conv2d(X, Wt, Y, alpha=1.0, beta=0.0, stride=(1, 1), pad=(0, 0), dil=(1, 1), stream=None,

@@ -23,12 +23,15 @@ CUDA_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompil
               "--expt-relaxed-constexpr", "-I", INCLUDE]
 
 
-def build_dir() -> str:
-    return os.path.join(HERE, "_build", platform.machine())
+def build_dir(debug: bool = False) -> str:
+    return os.path.join(HERE, "_build", platform.machine() + ("-debug" if debug else ""))
 
 
-def lib_path() -> str:
-    return os.path.join(build_dir(), LIB_NAME)
+def lib_path(debug: bool = False) -> str:
+    """The library; debug=True: the SGEMM_DEBUG build (device-side bounds
+    checks on every computed global address, reported through the status
+    word), built on request only."""
+    return os.path.join(build_dir(debug), LIB_NAME)
 
 
 def nvcc() -> str:
@@ -50,23 +53,24 @@ def _deps():
             + glob.glob(os.path.join(INCLUDE, "*.h")) + [os.path.abspath(__file__)])
 
 
-def up_to_date() -> bool:
-    out = lib_path()
+def up_to_date(debug: bool = False) -> bool:
+    out = lib_path(debug)
     if not os.path.exists(out):
         return False
     t = os.path.getmtime(out)
     return all(os.path.getmtime(d) <= t for d in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    """Compile (if needed) and return the path of the shared library."""
-    out = lib_path()
-    if not force and up_to_date():
+def build(force: bool = False, verbose: bool = False, extra_flags=(), debug: bool = False) -> str:
+    """Compile (if needed) and return the path of the shared library
+    (debug=True: the SGEMM_DEBUG build, in a directory of its own)."""
+    out = lib_path(debug)
+    if not force and up_to_date(debug):
         return out
-    bdir = build_dir()
+    bdir = build_dir(debug)
     os.makedirs(bdir, exist_ok=True)
     cc = nvcc()
-    flags = ARCH_FLAGS + CUDA_FLAGS + list(extra_flags)
+    flags = ARCH_FLAGS + CUDA_FLAGS + list(extra_flags) + (["-DSGEMM_DEBUG"] if debug else [])
 
     def compile_one(src):
         obj = os.path.join(bdir, os.path.basename(src)[:-3] + ".o")

@@ -325,15 +325,19 @@ void plan_ffma(int M, int N, int K, int sms, int splits_req, Plan &p) {
         p.ws_bytes = 0;
         return;
     }
+    // 128 x 256 tiles, one CTA per SM, when they fill at least 80 % of a
+    // wave; else 128 x 128 (two CTAs per SM), or wide tiles for short A
+    const bool big = M > 64 && static_cast<long long>(ceil_div(M, 128)) * ceil_div(N, 256) * 5 >= 4LL * sms;
     if (M <= 32) { p.tile_m = 32; p.tile_n = 512; }
     else if (M <= 64) { p.tile_m = 64; p.tile_n = 256; }
+    else if (big) { p.tile_m = 128; p.tile_n = 256; }
     else { p.tile_m = 128; p.tile_n = 128; }
     Schedule &s = p.sch;
     s.m_tiles = ceil_div(M, p.tile_m);
     s.n_tiles = ceil_div(N, p.tile_n);
     s.k_tiles = ceil_div(K, sg::kFfmaBK);
     const int tiles = s.m_tiles * s.n_tiles;
-    s.splits = choose_splits(tiles, s.k_tiles, 2 * sms, splits_req, 4);
+    s.splits = choose_splits(tiles, s.k_tiles, big ? sms : 2 * sms, splits_req, 4);
     s.units = tiles * s.splits;
     s.group_m = std::min(8, s.m_tiles);
     p.grid = s.units;
@@ -379,7 +383,7 @@ size_t span_bytes(int rows, int cols, long long ld) {
 
 bool flags_valid(int flags) {
     if (flags & ~(SGEMM_FLAG_DEBUG_WITHHOLD_ARRIVE | SGEMM_FLAG_WHOLE_TILES | SGEMM_FLAG_SPLIT_TAIL | 0xFF00 |
-                  SGEMM_FLAG_NO_A_COPY | SGEMM_FLAG_B_ROWS_LOADED | SGEMM_FLAG_TWO_CTAS_PER_SM))
+                  SGEMM_FLAG_NO_A_COPY | SGEMM_FLAG_B_ROWS_LOADED))
         return false;
     const int tm = forced_tile_rows(flags);
     return tm == 0 || sg::tf32x3_supported_tm(tm);
@@ -526,6 +530,8 @@ int run(int M, int N, int K, float alpha, const float *A, int lda, const float *
             if (rc != 0) return rc;
             ctl.ws = w->ws;
             ctl.counters = w->counters;
+            ctl.ws_end = w->ws + p.ws_bytes / sizeof(float);
+            ctl.n_counters = static_cast<long long>(w->n_counters);
         }
         // A whose rows are not 16-byte aligned (one matrix, or one shared by
         // the batch) and that is far smaller than B (M * 32 <= N, the im2col
@@ -551,19 +557,7 @@ int run(int M, int N, int K, float alpha, const float *A, int lda, const float *
         }
     }
     GemmArgs g{M, N, K, alpha, beta, A, lda, B, ldb, C, ldc, sA, sB, sC};
-    // two CTAs per SM for short tiles whose A comes by TMA: the split-K
-    // schedule strides its units over twice the SMs
-    const bool dual = (flags & SGEMM_FLAG_TWO_CTAS_PER_SM) && p.path == SGEMM_ALGO_TF32X3 && p.tile_m <= 64 &&
-                      p.vec_a && !trans_b && p.sch.tail_tiles == 0;
-    if (dual) {
-        int sms = 0;
-        {
-            std::lock_guard<std::mutex> lk(g_mu);
-            sms = d->sms;
-        }
-        p.grid = std::min(p.sch.units, 2 * sms);
-        if (p.sch.splits > 1) p.grid = std::max(p.grid, ceil_div(p.sch.units, sg::kTf32x3MaxDefer));
-    }
+    sg::set_extents(g, batch, trans_b, ctl.status);
     cudaError_t e;
     if (trans_b && (p.path != SGEMM_ALGO_TF32X3 || !p.vec_a || !p.vec_b))
         return SGEMM_ERR_INTERNAL;
@@ -571,7 +565,7 @@ int run(int M, int N, int K, float alpha, const float *A, int lda, const float *
         e = sg::tf32x3_launch_tb(p.tile_m, g, p.sch, ctl, p.vec_a, p.vec_c, p.grid, stream, batch);
     else if (p.path == SGEMM_ALGO_TF32X3)
         e = sg::tf32x3_launch(p.tile_m, g, p.sch, ctl, p.vec_a, p.vec_b, p.vec_c, p.grid, stream, batch,
-                              (flags & SGEMM_FLAG_B_ROWS_LOADED) != 0, dual);
+                              (flags & SGEMM_FLAG_B_ROWS_LOADED) != 0);
     else if (p.wide)
         e = sg::ffma_wide_launch(g, p.vec_b, p.grid, stream);
     else
@@ -863,6 +857,10 @@ int run_conv(int nb, int C, int H, int W, int F, int KH, int KW, int sh, int sw,
             const int Nt = nbc * N;
             GemmArgs g{F, Nt, K, alpha, beta, Wt, K, Xg + b0 * g_img, 1, Y + b0 * img_out, N, 0, g_img, img_out};
             g.cv = geom;
+            g.a_end = Wt + static_cast<long long>(F) * K;
+            g.b_end = Xg + (b0 + nbc) * g_img;
+            g.c_end = Y + (b0 + nbc) * img_out;
+            g.dbg_status = d->status;
             const int grid = std::min(sg::ffma_wide_blocks(Nt), 2 * d->sms);
             cudaError_t e = sg::ffma_wide_launch(g, 0, grid, stream, order);
             if (e != cudaSuccess) return from_cuda(e);
@@ -890,12 +888,18 @@ int run_conv(int nb, int C, int H, int W, int F, int KH, int KW, int sh, int sw,
                 if (rc != 0) return rc;
                 ctl.ws = w->ws;
                 ctl.counters = w->counters;
+                ctl.ws_end = w->ws + p.ws_bytes / sizeof(float);
+                ctl.n_counters = static_cast<long long>(w->n_counters);
             }
         }
         float *Yb = Y + b0 * img_out;
         const int vec_c = aligned16(Yb, N) && img_out % 4 == 0;
         GemmArgs g{F, N, K, alpha, beta, A, ldA, Xg + b0 * g_img, N, Yb, N, 0, g_img, img_out};
         g.cv = geom;
+        g.a_end = A + static_cast<long long>(F - 1) * ldA + K;
+        g.b_end = Xg + (b0 + nbc) * g_img;
+        g.c_end = Yb + nbc * img_out;
+        g.dbg_status = ctl.status;
         cudaError_t e = sg::tf32x3_conv_launch(p.tile_m, g, p.sch, ctl, order, vec_c, p.grid, stream, nbc);
         if (e != cudaSuccess) return from_cuda(e);
     }
@@ -1152,6 +1156,7 @@ int sgemm_check_status(sgemm_stream_t stream) {
     // arrival counters when the word is set)
     const int na = sg::noalloc_take_status();
     if (na < 0) return -na;  // a CUDA error, as a positive code
+    if (word & sg::kStatusOutOfBounds) return SGEMM_ERR_OUT_OF_BOUNDS;
     return (word != 0 || na > 0) ? SGEMM_ERR_DEVICE_TIMEOUT : 0;
 }
 
@@ -1180,6 +1185,8 @@ const char *sgemm_status_string(int status) {
         case SGEMM_ERR_UNSUPPORTED_DEVICE: return "device is not compute capability 10.3 (sm_103a)";
         case SGEMM_ERR_WORKSPACE: return "could not allocate library-owned device memory";
         case SGEMM_ERR_INTERNAL: return "internal planner error";
+        case SGEMM_ERR_OUT_OF_BOUNDS:
+            return "SGEMM_DEBUG build: a kernel address outside its matrix was found and skipped (result unspecified)";
         case SGEMM_ERR_SCRATCH_LIMIT:
             return "the problem needs more split-K scratch than sgemm_noalloc's fixed array "
                    "(16 MiB of partial tiles, 4096 tiles): use sgemm_ex or fewer splits";

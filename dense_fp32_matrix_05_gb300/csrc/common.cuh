@@ -16,7 +16,19 @@ enum : int {
     kStatusTimeoutDrain = 8,
     kStatusNoWorkspace = 16,  // a shared tile met a missing workspace (a planner bug)
     kStatusDeferOverflow = 32,  // a CTA got more shared tiles than it can defer (a planner bug)
+    kStatusOutOfBounds = 64,    // SGEMM_DEBUG builds: an access outside its matrix was skipped
 };
+
+// SGEMM_DEBUG builds check every computed global-memory address of the
+// kernels against the byte range of the matrix it belongs to (GemmArgs'
+// extents, DeviceCtl's workspace); an address outside is not accessed, and
+// the status bit kStatusOutOfBounds is set (never a trap).  The release
+// build compiles the checks away.
+#ifdef SGEMM_DEBUG
+constexpr bool kDebugBounds = true;
+#else
+constexpr bool kDebugBounds = false;
+#endif
 
 // Test-only flag: withhold the first producer arrive (see the header).
 enum : int { kDebugWithholdArrive = 1 };
@@ -61,7 +73,30 @@ struct GemmArgs {
     long long ldc;
     long long sA = 0, sB = 0, sC = 0;
     ConvGeom cv{};  // implicit-GEMM convolution kernels only
+    // One past the last float any access to A, B, C may touch (every matrix
+    // of a batch, a convolution's whole input); checked in SGEMM_DEBUG
+    // builds, which report into dbg_status.
+    const float *a_end = nullptr, *b_end = nullptr;
+    const float *c_end = nullptr;
+    int *dbg_status = nullptr;
 };
+
+// SGEMM_DEBUG: is [p, p + n) inside [lo, hi)?  Reports when it is not.
+template <typename T>
+__device__ __forceinline__ bool in_bounds(const T *p, int n, const void *lo, const void *hi, int *status) {
+    if constexpr (!kDebugBounds) {
+        return true;
+    } else {
+        const char *b = reinterpret_cast<const char *>(p);
+        const bool ok = lo != nullptr && b >= static_cast<const char *>(lo) &&
+                        b + static_cast<long long>(n) * sizeof(T) <= static_cast<const char *>(hi);
+        if (!ok && status) atomicOr(status, kStatusOutOfBounds);
+        return ok;
+    }
+}
+#define SG_IN_A(g, p, n) ::sg::in_bounds((p), (n), (g).A, (g).a_end, (g).dbg_status)
+#define SG_IN_B(g, p, n) ::sg::in_bounds((p), (n), (g).B, (g).b_end, (g).dbg_status)
+#define SG_IN_C(g, p, n) ::sg::in_bounds((p), (n), (g).C, (g).c_end, (g).dbg_status)
 
 // Work decomposition.  A work unit is one (tile, K range) pair; a tile whose
 // K range is spread over nseg > 1 units is finished by the last of its units
@@ -91,7 +126,10 @@ struct DeviceCtl {
     int *status;         // device status word
     long long wait_budget;  // clock64 cycles a bounded wait may spin
     int debug_flags;
+    const float *ws_end = nullptr;  // one past the workspace (SGEMM_DEBUG checks)
+    long long n_counters = 0;       // arrival counters available (SGEMM_DEBUG checks)
 };
+#define SG_IN_WS(ctl, p, n) ::sg::in_bounds((p), (n), (ctl).ws, (ctl).ws_end, (ctl).status)
 
 struct UnitCoord {
     int b;            // matrix of the batch

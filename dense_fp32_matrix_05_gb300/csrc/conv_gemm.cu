@@ -37,6 +37,7 @@ cudaError_t launch_conv_rows(const GemmArgs &g, const Schedule &s, const DeviceC
     std::memset(&mc, 0, sizeof(mc));
     if (!make_tmap_a(g, TM, batch, &ma)) return cudaErrorNotSupported;
     const int tc = (vec_c && make_tmap_c(g, batch, &mc)) ? 1 : 0;
+    if (map_range_error()) return cudaErrorInvalidValue;  // SGEMM_DEBUG only
     if (order == kConvChannels) return launch_conv_tm<TM, kConvChannels>(g, s, ctl, tc, grid, ma, mc, stream);
     if (order == kConvTapsDense) {
         if (g.K > kConvTabMax) return cudaErrorInvalidValue;

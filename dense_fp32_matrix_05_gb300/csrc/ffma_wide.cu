@@ -71,7 +71,7 @@ __device__ __forceinline__ void load_slab(const GemmArgs &g, bool vec_b, int cb,
             const int off = tab[kb + r];
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-                const bool ok = k_ok && n_ok[h];
+                const bool ok = k_ok && n_ok[h] && SG_IN_B(g, col[h] + off, 1);
                 cp_async4(dst + static_cast<uint32_t>((r * kCols + tid + h * kThreads) * 4), ok ? col[h] + off : g.B,
                           ok ? 4u : 0u);
             }
@@ -107,7 +107,9 @@ __device__ __forceinline__ void load_slab(const GemmArgs &g, bool vec_b, int cb,
                 const bool ok = k_ok && static_cast<unsigned>(ih) < static_cast<unsigned>(cv.H) &&
                                 static_cast<unsigned>(iw) < static_cast<unsigned>(cv.W);
                 const float *src = ok ? col[h] + (static_cast<long long>(c) * cv.H + ih) * cv.W + iw : g.B;
-                cp_async4(dst + static_cast<uint32_t>((r * kCols + tid + h * kThreads) * 4), src, ok ? 4u : 0u);
+                const bool in = ok && SG_IN_B(g, src, 1);
+                cp_async4(dst + static_cast<uint32_t>((r * kCols + tid + h * kThreads) * 4), in ? src : g.B,
+                          in ? 4u : 0u);
             }
             if (++kw == cv.KW) {
                 kw = 0;
@@ -128,6 +130,10 @@ __device__ __forceinline__ void load_slab(const GemmArgs &g, bool vec_b, int cb,
             if (k < g.K && n < g.N) {
                 src = g.B + static_cast<long long>(k) * g.ldb + n;
                 bytes = static_cast<uint32_t>(min(4, g.N - n) * 4);
+                if (!SG_IN_B(g, src, static_cast<int>(bytes / 4))) {
+                    src = g.B;
+                    bytes = 0;
+                }
             }
             cp_async16(dst + static_cast<uint32_t>((r * kCols + cc * 4) * 4), src, bytes);
         }
@@ -137,7 +143,7 @@ __device__ __forceinline__ void load_slab(const GemmArgs &g, bool vec_b, int cb,
             const int c = tid + i * kThreads;
             const int r = c / kCols, cc = c % kCols;
             const int k = kc * kKc + r, n = n0 + cc;
-            const bool ok = k < g.K && n < g.N;
+            const bool ok = k < g.K && n < g.N && SG_IN_B(g, g.B + static_cast<long long>(k) * g.ldb + n, 1);
             const float *src = ok ? g.B + static_cast<long long>(k) * g.ldb + n : g.B;
             cp_async4(dst + static_cast<uint32_t>((r * kCols + cc) * 4), src, ok ? 4u : 0u);
         }
@@ -173,8 +179,8 @@ __device__ __forceinline__ void store_block(const GemmArgs &g, int n, const uint
                 if (m >= g.M) break;
                 float *p0 = cp[0] + static_cast<long long>(m) * ld;
                 float *p1 = cp[1] + static_cast<long long>(m) * ld;
-                p0[0] = read_c ? fmaf(g.beta, p0[0], g.alpha * c0[h]) : g.alpha * c0[h];
-                if (two) p1[0] = read_c ? fmaf(g.beta, p1[0], g.alpha * c1[h]) : g.alpha * c1[h];
+                if (SG_IN_C(g, p0, 1)) p0[0] = read_c ? fmaf(g.beta, p0[0], g.alpha * c0[h]) : g.alpha * c0[h];
+                if (two && SG_IN_C(g, p1, 1)) p1[0] = read_c ? fmaf(g.beta, p1[0], g.alpha * c1[h]) : g.alpha * c1[h];
             }
         }
         return;
@@ -192,6 +198,7 @@ __device__ __forceinline__ void store_block(const GemmArgs &g, int n, const uint
             if (m >= g.M) break;
             float *p = g.C + static_cast<long long>(m) * g.ldc + n;
             float r0 = g.alpha * c0[h], r1 = g.alpha * c1[h];
+            if (!SG_IN_C(g, p, (pair || n + 1 < g.N) ? 2 : 1)) continue;
             if (pair) {
                 if (read_c) {
                     const float2 o = *reinterpret_cast<const float2 *>(p);
@@ -244,7 +251,8 @@ __global__ void __launch_bounds__(kThreads, 2) ffma_wide_kernel(const __grid_con
     // A^T, zero outside M x K (its loads overlap the first slab copies)
     for (int i = tid; i < kAFloats; i += kThreads) {
         const int k = i / kMaxM, m = i % kMaxM;
-        a_t[i] = (m < g.M && k < g.K) ? g.A[static_cast<long long>(m) * g.lda + k] : 0.f;
+        const float *pa = g.A + static_cast<long long>(m) * g.lda + k;
+        a_t[i] = (m < g.M && k < g.K && SG_IN_A(g, pa, 1)) ? *pa : 0.f;
     }
 
     uint64_t acc0[kMaxM / 2], acc1[kMaxM / 2];  // row pairs of columns 2t and 2t + 1

@@ -38,6 +38,7 @@ cudaError_t launch_tb_rows(const GemmArgs &g, const Schedule &s, const DeviceCtl
     std::memset(&mc, 0, sizeof(mc));
     if (!vec_a || !make_tmap_a(g, TM, batch, &ma) || !make_tmap_bt(g, batch, &mb)) return cudaErrorNotSupported;
     const int tc = (vec_c && make_tmap_c(g, batch, &mc)) ? 1 : 0;
+    if (map_range_error()) return cudaErrorInvalidValue;  // SGEMM_DEBUG only
     return launch_tb_tm<TM>(g, s, ctl, tc, grid, ma, mb, mc, stream);
 }
 

@@ -26,6 +26,20 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), int grid, int threads, int smem, 
     return cudaLaunchKernelEx(&cfg, kern, static_cast<Args &&>(args)...);
 }
 
+// Extents of a GEMM's operands for the SGEMM_DEBUG bounds checks: one past
+// the last float of A (M x K), B (K x N, or N x K when transposed) and C
+// (M x N) over `batch` matrices with the strides in g; dbg_status is where
+// violations are reported.
+inline void set_extents(GemmArgs &g, int batch, bool trans_b, int *status) {
+    const long long nb = batch > 1 ? batch - 1 : 0;
+    g.a_end = (g.A && g.M > 0 && g.K > 0) ? g.A + nb * g.sA + (g.M - 1) * g.lda + g.K : nullptr;
+    g.b_end = (g.B && g.N > 0 && g.K > 0)
+                  ? g.B + nb * g.sB + (trans_b ? (g.N - 1) * g.ldb + g.K : (g.K - 1) * g.ldb + g.N)
+                  : nullptr;
+    g.c_end = (g.C && g.M > 0 && g.N > 0) ? g.C + nb * g.sC + (g.M - 1) * g.ldc + g.N : nullptr;
+    g.dbg_status = status;
+}
+
 // Tile constants the planner needs (checked against the kernels' own).
 constexpr int kTf32x3TileN = 128;  // C columns per 3xTF32 tile
 constexpr int kTf32x3BK = 16;      // K per 3xTF32 pipeline stage
@@ -58,10 +72,9 @@ cudaError_t filter_ohwi_launch(const float *w, int F, int C, int KH, int KW, flo
 // batch: matrices of a strided batch (g.sA / sB / sC; s.tpb tiles each).
 // b_rows: a B whose rows are not 16-byte aligned is loaded by the producers
 // instead of being copied by TMA as four residue classes of rows.
-// dual (tm <= 64, A by TMA): two CTAs per SM, the grid counting both.
 cudaError_t tf32x3_launch(int tm, const GemmArgs &g, const Schedule &s, const DeviceCtl &ctl,
                           int vec_a, int vec_b, int vec_c, int grid, cudaStream_t stream, int batch = 1,
-                          bool b_rows = false, bool dual = false);
+                          bool b_rows = false);
 
 // FFMA path.  (bm, bn) in {(128,128), (64,256), (32,512)}.
 bool ffma_supported_tile(int bm, int bn);

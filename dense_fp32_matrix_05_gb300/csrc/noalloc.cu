@@ -147,8 +147,11 @@ extern "C" int sgemm_noalloc(int M, int N, int K, float alpha, const float *A, i
         // the status word, whose check (sgemm_check_status) clears them.
         ctl.ws = d->partials;
         ctl.counters = d->counters;
+        ctl.ws_end = d->partials + kScratchFloats;
+        ctl.n_counters = kScratchCounters;
     }
     sg::GemmArgs g{M, N, K, alpha, beta, A, lda, B, ldb, C, ldc};
+    sg::set_extents(g, 1, false, ctl.status);
     return static_cast<int>(
         sg::tf32x3_launch(plan.tile_m, g, plan.sch, ctl, plan.vec_a, plan.vec_b, plan.vec_c, plan.grid, st));
 }

@@ -369,9 +369,6 @@ __device__ __forceinline__ void tmem_ld32x16_issue(uint32_t taddr, uint32_t (&r)
         : "memory");
 }
 
-// Wait for every tensor-memory load this thread issued (registers not needed).
-__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-
 // Wait for every tensor-memory load this thread issued.
 __device__ __forceinline__ void tmem_ld_wait16(uint32_t (&r)[16]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;"

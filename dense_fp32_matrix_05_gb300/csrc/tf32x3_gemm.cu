@@ -39,6 +39,29 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 }  // namespace
 
+// SGEMM_DEBUG: a tensor map that could address bytes outside its operand
+// ([lo, hi)) is not made, and the launch fails with cudaErrorInvalidValue
+// (map_range_error tells the launchers).
+thread_local bool t_map_range_error = false;
+
+bool map_in(const void *base, int rank, const cuuint64_t *dims, const cuuint64_t *strides, const void *lo,
+            const void *hi) {
+    if (!kDebugBounds) return true;
+    unsigned long long last = (dims[0] - 1) * sizeof(float);
+    for (int i = 1; i < rank; ++i) last += (dims[i] - 1) * strides[i - 1];
+    const char *b = static_cast<const char *>(base);
+    const bool ok = lo != nullptr && hi != nullptr && b >= static_cast<const char *>(lo) &&
+                    b + last + sizeof(float) <= static_cast<const char *>(hi);
+    if (!ok) t_map_range_error = true;
+    return ok;
+}
+
+bool map_range_error() {
+    const bool e = t_map_range_error;
+    t_map_range_error = false;
+    return e;
+}
+
 // Third (batch) dimension of a tensor map: `batch` matrices `stride`
 // elements apart, or one matrix when the stride is 0 (an operand shared by
 // the batch, or no batch).  The stride must be a multiple of 16 bytes.
@@ -67,6 +90,7 @@ bool make_tmap_a(const GemmArgs &g, int tm, int batch, CUtensorMap *map) {
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(g.lda) * sizeof(float), sb};
     const cuuint32_t box[3] = {static_cast<cuuint32_t>(tf32x3::kBK), static_cast<cuuint32_t>(tm), 1};
     const cuuint32_t estr[3] = {1, 1, 1};
+    if (!map_in(g.A, 3, dims, strides, g.A, g.a_end)) return false;
     const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(g.A), dims, strides,
                            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -85,6 +109,7 @@ bool make_tmap_b(const GemmArgs &g, int batch, CUtensorMap *map) {
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(g.ldb) * sizeof(float), sb};
     const cuuint32_t box[3] = {static_cast<cuuint32_t>(tf32x3::kTileN), static_cast<cuuint32_t>(tf32x3::kBK), 1};
     const cuuint32_t estr[3] = {1, 1, 1};
+    if (!map_in(g.B, 3, dims, strides, g.B, g.b_end)) return false;
     const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(g.B), dims, strides,
                            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -107,6 +132,7 @@ bool make_tmap_bt(const GemmArgs &g, int batch, CUtensorMap *map) {
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(g.ldb) * sizeof(float), sb};
     const cuuint32_t box[3] = {static_cast<cuuint32_t>(tf32x3::kBK), static_cast<cuuint32_t>(tf32x3::kTileN), 1};
     const cuuint32_t estr[3] = {1, 1, 1};
+    if (!map_in(g.B, 3, dims, strides, g.B, g.b_end)) return false;
     const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(g.B), dims, strides,
                            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -137,6 +163,7 @@ bool make_tmap_b4(const GemmArgs &g, int batch, CUtensorMap maps[4], uint32_t *o
         const cuuint64_t strides[2] = {static_cast<cuuint64_t>(4 * g.ldb) * sizeof(float), sb};
         const cuuint32_t box[3] = {static_cast<cuuint32_t>(tf32x3::kB4Row), 4, 1};
         const cuuint32_t estr[3] = {1, 1, 1};
+        if (!map_in(base, 3, dims, strides, g.B, g.b_end)) return false;
         const CUresult res = enc(&maps[r], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(base), dims,
                                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -149,12 +176,18 @@ bool make_tmap_b4(const GemmArgs &g, int batch, CUtensorMap maps[4], uint32_t *o
 bool make_tmap_c(const GemmArgs &g, int batch, CUtensorMap *map) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
     if (!enc) return false;
+    // A TMA store writes whole 16-byte units at the end of a row: with N not
+    // a multiple of 4 it would write the first floats of the ld padding
+    // (measured on GB300: N = 15, ldc = 20).  Such a C takes the epilogue's
+    // own stores.
+    if (g.N % 4 != 0) return false;
     cuuint64_t nb, sb;
     if (!batch_dim(g.sC, batch, g.ldc * g.M, nb, sb)) return false;
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(g.N), static_cast<cuuint64_t>(g.M), nb};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(g.ldc) * sizeof(float), sb};
     const cuuint32_t box[3] = {static_cast<cuuint32_t>(tf32x3::kTileN), static_cast<cuuint32_t>(tf32x3::kEpiRows), 1};
     const cuuint32_t estr[3] = {1, 1, 1};
+    if (!map_in(g.C, 3, dims, strides, g.C, g.c_end)) return false;
     const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, g.C, dims, strides, box, estr,
                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -163,15 +196,15 @@ bool make_tmap_c(const GemmArgs &g, int batch, CUtensorMap *map) {
 
 namespace {
 
-template <int TM, bool TA, bool TB, bool B4 = false, bool DUAL = false>
+template <int TM, bool TA, bool TB, bool B4 = false>
 cudaError_t launch_tm(const GemmArgs &g, const Schedule &s, const DeviceCtl &ctl, int vec_a, int tma_c, int grid,
                       const CUtensorMap &map_a, const CUtensorMap (&map_b)[4], uint32_t b_offs,
                       const CUtensorMap &map_c, cudaStream_t stream) {
-    using C = tf32x3::Cfg<TM, TB, B4, DUAL>;
-    auto kern = tf32x3::tf32x3_gemm_kernel<TM, TA, TB, kConvNone, false, B4, DUAL>;
+    using C = tf32x3::Cfg<TM, TB, B4>;
+    auto kern = tf32x3::tf32x3_gemm_kernel<TM, TA, TB, kConvNone, false, B4>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    return launch_pdl(kern, grid, tf32x3::Roles<TM, TA, TB, DUAL>::kThreads, C::kSmemBytes, stream, g, s, ctl, vec_a,
+    return launch_pdl(kern, grid, tf32x3::Roles<TM, TA, TB>::kThreads, C::kSmemBytes, stream, g, s, ctl, vec_a,
                       tma_c, b_offs, map_a, map_b[0], map_c, map_b[1], map_b[2], map_b[3]);
 }
 
@@ -184,7 +217,7 @@ cudaError_t launch_tm(const GemmArgs &g, const Schedule &s, const DeviceCtl &ctl
 // own loads.
 template <int TM>
 cudaError_t launch_rows(const GemmArgs &g, const Schedule &s, const DeviceCtl &ctl, int vec_a, int vec_b,
-                        int vec_c, int grid, int batch, bool b_rows, bool dual, cudaStream_t stream) {
+                        int vec_c, int grid, int batch, bool b_rows, cudaStream_t stream) {
     CUtensorMap ma, mb[4], mc;
     std::memset(&ma, 0, sizeof(ma));
     std::memset(mb, 0, sizeof(mb));
@@ -194,14 +227,7 @@ cudaError_t launch_rows(const GemmArgs &g, const Schedule &s, const DeviceCtl &c
     const bool tb = vec_b && make_tmap_b(g, batch, &mb[0]);
     const bool tb4 = !vec_b && !b_rows && make_tmap_b4(g, batch, mb, &offs);
     const int tc = (vec_c && make_tmap_c(g, batch, &mc)) ? 1 : 0;
-    if constexpr (TM <= 64) {
-        // two CTAs per SM (A by TMA): the grid already counts two per SM
-        if (dual && ta) {
-            if (tb) return launch_tm<TM, true, true, false, true>(g, s, ctl, vec_a, tc, grid, ma, mb, 0, mc, stream);
-            if (tb4) return launch_tm<TM, true, true, true, true>(g, s, ctl, vec_a, tc, grid, ma, mb, offs, mc, stream);
-            return launch_tm<TM, true, false, false, true>(g, s, ctl, vec_a, tc, grid, ma, mb, 0, mc, stream);
-        }
-    }
+    if (map_range_error()) return cudaErrorInvalidValue;  // SGEMM_DEBUG only
     if (tb) {
         if (ta) return launch_tm<TM, true, true>(g, s, ctl, vec_a, tc, grid, ma, mb, 0, mc, stream);
         return launch_tm<TM, false, true>(g, s, ctl, vec_a, tc, grid, ma, mb, 0, mc, stream);
@@ -276,14 +302,14 @@ int tf32x3_smem_bytes(int tm) {
 }
 
 cudaError_t tf32x3_launch(int tm, const GemmArgs &g, const Schedule &s, const DeviceCtl &ctl, int vec_a,
-                          int vec_b, int vec_c, int grid, cudaStream_t stream, int batch, bool b_rows, bool dual) {
+                          int vec_b, int vec_c, int grid, cudaStream_t stream, int batch, bool b_rows) {
     switch (tm) {
-        case 16: return launch_rows<16>(g, s, ctl, vec_a, vec_b, vec_c, grid, batch, b_rows, dual, stream);
-        case 32: return launch_rows<32>(g, s, ctl, vec_a, vec_b, vec_c, grid, batch, b_rows, dual, stream);
-        case 64: return launch_rows<64>(g, s, ctl, vec_a, vec_b, vec_c, grid, batch, b_rows, dual, stream);
-        case 128: return launch_rows<128>(g, s, ctl, vec_a, vec_b, vec_c, grid, batch, b_rows, false, stream);
-        case 192: return launch_rows<192>(g, s, ctl, vec_a, vec_b, vec_c, grid, batch, b_rows, false, stream);
-        case 256: return launch_rows<256>(g, s, ctl, vec_a, vec_b, vec_c, grid, batch, b_rows, false, stream);
+        case 16: return launch_rows<16>(g, s, ctl, vec_a, vec_b, vec_c, grid, batch, b_rows, stream);
+        case 32: return launch_rows<32>(g, s, ctl, vec_a, vec_b, vec_c, grid, batch, b_rows, stream);
+        case 64: return launch_rows<64>(g, s, ctl, vec_a, vec_b, vec_c, grid, batch, b_rows, stream);
+        case 128: return launch_rows<128>(g, s, ctl, vec_a, vec_b, vec_c, grid, batch, b_rows, stream);
+        case 192: return launch_rows<192>(g, s, ctl, vec_a, vec_b, vec_c, grid, batch, b_rows, stream);
+        case 256: return launch_rows<256>(g, s, ctl, vec_a, vec_b, vec_c, grid, batch, b_rows, stream);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -66,16 +66,13 @@ constexpr int kEpiBarrierId = 1;
 // flight while it splits one.  With A arriving by TMA the registers only
 // hold B^T; without it they also hold A chunks, so wide tiles use fewer,
 // larger groups to stay within the register budget.
-// DUAL: two CTAs share an SM (each with half the tensor memory and shared
-// memory); one group of 4 producer warps each keeps the pair within the
-// SM's registers (2 x 320 threads x 96).
-template <int TM, bool TMA_A, bool TMA_B, bool DUAL = false>
+template <int TM, bool TMA_A, bool TMA_B>
 struct Roles {
     static constexpr bool kTma = TMA_A || TMA_B;  // the TMA thread fills stages
     // With A copied by TMA the producers hold few registers: 12 warps in 3
     // groups leave 96 registers per thread; otherwise 16 warps.
-    static constexpr int kProdWarps = DUAL ? 4 : (TMA_A ? 12 : 16);
-    static constexpr int kGroups = DUAL ? 1 : (TMA_A ? 3 : (TM <= 64 ? 4 : 2));
+    static constexpr int kProdWarps = TMA_A ? 12 : 16;
+    static constexpr int kGroups = TMA_A ? 3 : (TM <= 64 ? 4 : 2);
     static constexpr int kWarpsPerGroup = kProdWarps / kGroups;
     static_assert(kWarpsPerGroup % 4 == 0, "each group covers the four lane quadrants");
     static constexpr int kGroupThreads = kWarpsPerGroup * 32;
@@ -84,13 +81,11 @@ struct Roles {
     static constexpr int kMmaWarp = kEpiWarps + kProdWarps;
     static constexpr int kTmaWarp = kMmaWarp + 1;
     static constexpr int kThreads = (kEpiWarps + kProdWarps + 2) * 32;
-    static constexpr int kCtasPerSm = DUAL ? 2 : 1;
 };
 
-// Tensor memory (512 columns of 128 lanes x 32 bit per SM; 256 per CTA when
-// two CTAs share the SM): accumulators of TM columns each, then a ring of
-// STAGES B^T stages of 32 columns (16 hi + 16 lo k values per lane = per C
-// column).
+// Tensor memory (512 columns of 128 lanes x 32 bit): accumulators of TM
+// columns each, then a ring of STAGES B^T stages of 32 columns (16 hi + 16 lo
+// k values per lane = per C column).
 constexpr uint32_t kTmemCols = 512;
 constexpr int kRingColsPerStage = 2 * kBK;
 constexpr int kMaxStages = 12;
@@ -103,20 +98,17 @@ constexpr int kMaxStages = 12;
 // the epilogue adds its halves.
 __host__ __device__ constexpr bool paired_for(int tm) { return tm <= 64; }
 __host__ __device__ constexpr int acc_cols_for(int tm) { return (paired_for(tm) ? 2 : 1) * tm; }
-// Accumulators: two (a tile's epilogue overlaps the next tile's MMAs) where
-// they leave room for 4 ring stages; in 512 columns, one from TM = 192 up.
-__host__ __device__ constexpr int nacc_for(int tm, int cols = 512) {
-    return cols == 512 ? (tm >= 192 ? 1 : 2) : (2 * acc_cols_for(tm) + 4 * kRingColsPerStage <= cols ? 2 : 1);
-}
+// Accumulators: two (a tile's epilogue overlaps the next tile's MMAs), one
+// from TM = 192 up.
+__host__ __device__ constexpr int nacc_for(int tm) { return tm >= 192 ? 1 : 2; }
 // every tensor-memory column the accumulators leave, up to kMaxStages (short
 // tiles stream long B panels and want many copies in flight)
-__host__ __device__ constexpr int stages_for(int tm, int cols = 512) {
-    return (cols - nacc_for(tm, cols) * acc_cols_for(tm)) / kRingColsPerStage < kMaxStages
-               ? (cols - nacc_for(tm, cols) * acc_cols_for(tm)) / kRingColsPerStage
+__host__ __device__ constexpr int stages_for(int tm) {
+    return (static_cast<int>(kTmemCols) - nacc_for(tm) * acc_cols_for(tm)) / kRingColsPerStage < kMaxStages
+               ? (static_cast<int>(kTmemCols) - nacc_for(tm) * acc_cols_for(tm)) / kRingColsPerStage
                : kMaxStages;
 }
-constexpr int kSmemLimit = 232448;      // dynamic shared memory one CTA may use on sm_103a
-constexpr int kSmemLimitDual = 115712;  // per CTA when two share an SM (228 KB less 1 KB each)
+constexpr int kSmemLimit = 232448;  // dynamic shared memory one CTA may use on sm_103a
 // C chunks the epilogue stages in shared memory for TMA copies (16 rows of
 // the 128 tile columns each); loads run two chunks ahead of the arithmetic.
 constexpr int kEpiBufs = 3;
@@ -144,13 +136,11 @@ constexpr int kB4SlabBytes = 4 * kB4ClassBytes;
 // split; B4: that slab holds the four residue classes of an unaligned B.
 // Shared memory: the stages' A tiles (hi, lo), then the stages' B slabs,
 // then the epilogue's C buffers and the barriers.
-template <int TM, bool TMA_B = false, bool B4 = false, bool DUAL = false>
+template <int TM, bool TMA_B = false, bool B4 = false>
 struct Cfg {
     static_assert(TM % 16 == 0 && TM >= 16 && TM <= 256, "MMA N for M=128 must be 16..256, step 16");
     static_assert(TMA_B || !B4, "the residue-class form is a TMA form");
-    static constexpr uint32_t kCols = DUAL ? kTmemCols / 2 : kTmemCols;  // tensor-memory columns of the CTA
-    static constexpr int kSmemMax = DUAL ? kSmemLimitDual : kSmemLimit;
-    static constexpr int kNacc = nacc_for(TM, kCols);
+    static constexpr int kNacc = nacc_for(TM);
     static constexpr int kABytes = TM * kBK * 4;  // A tile (MMA B operand), one of hi / lo
     static constexpr int kOffAHi = 0;             // also where TMA lands the raw A tile
     static constexpr int kOffALo = kABytes;
@@ -161,9 +151,9 @@ struct Cfg {
     static constexpr int kEpiBufBytes = kEpiBufs * kEpiChunkBytes;
     // as many stages as tensor memory and the 227 KB of shared memory allow
     // (1 KB of alignment slack and up to 528 bytes of barriers and words)
-    static constexpr int kStageRoom = kSmemMax - 1024 - 528 - kEpiBufBytes;
-    static constexpr int kStages = stages_for(TM, kCols) < kStageRoom / kStageBytes ? stages_for(TM, kCols)
-                                                                                    : kStageRoom / kStageBytes;
+    static constexpr int kStageRoom = kSmemLimit - 1024 - 528 - kEpiBufBytes;
+    static constexpr int kStages = stages_for(TM) < kStageRoom / kStageBytes ? stages_for(TM)
+                                                                             : kStageRoom / kStageBytes;
     static constexpr int kOffBRegion = kStages * kAStageBytes;  // slab of stage s at + s * kBRawBytes
     static constexpr int kOffEpi = kStages * kStageBytes;
     static_assert(kAStageBytes % 1024 == 0, "A tiles must keep 1 KB alignment (64-byte swizzle atoms)");
@@ -172,7 +162,7 @@ struct Cfg {
     static constexpr bool kPaired = paired_for(TM);
     static constexpr int kAccCols = acc_cols_for(TM);  // one accumulator (two TM halves when paired)
     static constexpr int kRingCol = kNacc * kAccCols;
-    static_assert(kRingCol + kStages * kRingColsPerStage <= static_cast<int>(kCols), "tensor memory");
+    static_assert(kRingCol + kStages * kRingColsPerStage <= static_cast<int>(kTmemCols), "tensor memory");
     static constexpr int kChunk = 16;  // accumulator columns per tensor-memory load in the epilogue
     static constexpr uint32_t kIdesc = umma_idesc_tf32(kTileN, TM);
     static constexpr uint32_t kIdescPair = umma_idesc_tf32(kTileN, 2 * TM);  // N = 2TM: [A_hi; A_lo]
@@ -184,10 +174,10 @@ struct Cfg {
     static constexpr int kBarBytes = 8 * (3 * kStages + 5 + kEpiBufs) + 4 * (4 + 5 * kMaxDefer);
     static constexpr int kSmemBytes = 1024 + kOffEpi + kEpiBufBytes + kBarBytes;
     static_assert(kBarBytes <= 528, "room kept for the barriers");
-    static_assert(kSmemBytes <= kSmemMax, "shared memory per CTA");
+    static_assert(kSmemBytes <= kSmemLimit, "shared memory per CTA");
     // a dense convolution's tap table (kConvTabMax ints, 16-byte aligned)
     static constexpr int kConvTabBytes = kConvTabMax * 4 + 16;
-    static_assert(TMA_B || DUAL || kSmemBytes + kConvTabBytes <= kSmemLimit, "shared memory with a tap table");
+    static_assert(TMA_B || kSmemBytes + kConvTabBytes <= kSmemLimit, "shared memory with a tap table");
     static_assert(kStages >= 4, "pipeline depth");
 };
 
@@ -257,7 +247,8 @@ __device__ __forceinline__ void load_raw(const GemmArgs &g, bool vec_a, int bi, 
         const int pix0 = oh * cv.sh * cv.W + (n_ok ? n - oh * cv.OW : 0) * cv.sw;
         const float *xp = g.B + bi * g.sB + pix0;
 #pragma unroll
-        for (int e = 0; e < BtK; ++e) raw.b[e] = (n_ok && kb + e < g.K) ? __ldg(xp + ctab[kb + e]) : 0.f;
+        for (int e = 0; e < BtK; ++e)
+            raw.b[e] = (n_ok && kb + e < g.K && SG_IN_B(g, xp + ctab[kb + e], 1)) ? __ldg(xp + ctab[kb + e]) : 0.f;
     } else if constexpr (BtK > 0 && CONV == kConvChannels) {
         const ConvGeom &cv = g.cv;
         const int n = n0 + (ptid & (kTileN - 1));
@@ -272,7 +263,7 @@ __device__ __forceinline__ void load_raw(const GemmArgs &g, bool vec_a, int bi, 
         const long long plane = static_cast<long long>(cv.H) * cv.W;
         const float *src = g.B + bi * g.sB + c0 * plane + static_cast<long long>(ih) * cv.W + iw;
 #pragma unroll
-        for (int e = 0; e < BtK; ++e) raw.b[e] = ok ? __ldg(src + e * plane) : 0.f;
+        for (int e = 0; e < BtK; ++e) raw.b[e] = (ok && SG_IN_B(g, src + e * plane, 1)) ? __ldg(src + e * plane) : 0.f;
     } else if constexpr (BtK > 0 && CONV == kConvTaps) {
         const ConvGeom &cv = g.cv;
         const int n = n0 + (ptid & (kTileN - 1));
@@ -296,7 +287,8 @@ __device__ __forceinline__ void load_raw(const GemmArgs &g, bool vec_a, int bi, 
             const int dy = kh * cv.dh, dx = kw * cv.dw;
             const bool ok = n_ok && kb + e < g.K && static_cast<unsigned>(ih0 + dy) < static_cast<unsigned>(cv.H) &&
                             static_cast<unsigned>(iw0 + dx) < static_cast<unsigned>(cv.W);
-            raw.b[e] = ok ? __ldg(xb + (coff + dy * cv.W + dx + pix0)) : 0.f;
+            const float *px = xb + (coff + dy * cv.W + dx + pix0);
+            raw.b[e] = (ok && SG_IN_B(g, px, 1)) ? __ldg(px) : 0.f;
             if (++kw == cv.KW) {
                 kw = 0;
                 if (++kh == cv.KH) {
@@ -312,7 +304,7 @@ __device__ __forceinline__ void load_raw(const GemmArgs &g, bool vec_a, int bi, 
         const float *src = g.B + bi * g.sB + static_cast<long long>(kb) * g.ldb + n;
 #pragma unroll
         for (int e = 0; e < BtK; ++e)
-            raw.b[e] = (n_ok && kb + e < g.K) ? __ldg(src + e * g.ldb) : 0.f;
+            raw.b[e] = (n_ok && kb + e < g.K && SG_IN_B(g, src + e * g.ldb, 1)) ? __ldg(src + e * g.ldb) : 0.f;
     }
     if constexpr (AJ > 0) {
 #pragma unroll
@@ -325,12 +317,12 @@ __device__ __forceinline__ void load_raw(const GemmArgs &g, bool vec_a, int bi, 
                 if (m < g.M) {
                     const float *src = g.A + bi * g.sA + static_cast<long long>(m) * g.lda + k;
                     if (vec_a && k + 3 < g.K) {
-                        v = __ldg(reinterpret_cast<const float4 *>(src));
+                        if (SG_IN_A(g, src, 4)) v = __ldg(reinterpret_cast<const float4 *>(src));
                     } else {
-                        v.x = (k + 0 < g.K) ? __ldg(src + 0) : 0.f;
-                        v.y = (k + 1 < g.K) ? __ldg(src + 1) : 0.f;
-                        v.z = (k + 2 < g.K) ? __ldg(src + 2) : 0.f;
-                        v.w = (k + 3 < g.K) ? __ldg(src + 3) : 0.f;
+                        v.x = (k + 0 < g.K && SG_IN_A(g, src + 0, 1)) ? __ldg(src + 0) : 0.f;
+                        v.y = (k + 1 < g.K && SG_IN_A(g, src + 1, 1)) ? __ldg(src + 1) : 0.f;
+                        v.z = (k + 2 < g.K && SG_IN_A(g, src + 2, 1)) ? __ldg(src + 2) : 0.f;
+                        v.w = (k + 3 < g.K && SG_IN_A(g, src + 3, 1)) ? __ldg(src + 3) : 0.f;
                     }
                 }
             }
@@ -468,7 +460,9 @@ __device__ __noinline__ float recompute_dot(const GemmArgs &g, int bi, int m, in
                 const bool in = static_cast<unsigned>(ih) < static_cast<unsigned>(cv.H) &&
                                 static_cast<unsigned>(iw) < static_cast<unsigned>(cv.W);
                 const float *px = x + static_cast<long long>(ih) * cv.W + iw;
-                for (int c = 0; c < cv.C; ++c, ++k) s = fmaf(__ldg(a + k), in ? __ldg(px + c * plane) : 0.f, s);
+                for (int c = 0; c < cv.C; ++c, ++k)
+                    s = fmaf(SG_IN_A(g, a + k, 1) ? __ldg(a + k) : 0.f,
+                             (in && SG_IN_B(g, px + c * plane, 1)) ? __ldg(px + c * plane) : 0.f, s);
             }
             if (s != s) break;
         }
@@ -485,7 +479,8 @@ __device__ __noinline__ float recompute_dot(const GemmArgs &g, int bi, int m, in
                     const int iw = iw0 + kw * cv.dw;
                     const bool in = static_cast<unsigned>(ih) < static_cast<unsigned>(cv.H) &&
                                     static_cast<unsigned>(iw) < static_cast<unsigned>(cv.W);
-                    s = fmaf(__ldg(a + k), in ? __ldg(x + static_cast<long long>(ih) * cv.W + iw) : 0.f, s);
+                    const float *px = x + static_cast<long long>(ih) * cv.W + iw;
+                    s = fmaf(SG_IN_A(g, a + k, 1) ? __ldg(a + k) : 0.f, (in && SG_IN_B(g, px, 1)) ? __ldg(px) : 0.f, s);
                 }
             }
             if (s != s) break;
@@ -493,13 +488,14 @@ __device__ __noinline__ float recompute_dot(const GemmArgs &g, int bi, int m, in
     } else if constexpr (TRANS_B) {
         const float *b = g.B + bi * g.sB + static_cast<long long>(n) * g.ldb;
         for (int k = 0; k < g.K; ++k) {
-            s = fmaf(__ldg(a + k), __ldg(b + k), s);
+            s = fmaf(SG_IN_A(g, a + k, 1) ? __ldg(a + k) : 0.f, SG_IN_B(g, b + k, 1) ? __ldg(b + k) : 0.f, s);
             if (s != s) break;
         }
     } else {
         const float *b = g.B + bi * g.sB + n;
         for (int k = 0; k < g.K; ++k) {
-            s = fmaf(__ldg(a + k), __ldg(b + static_cast<long long>(k) * g.ldb), s);
+            const float *pb = b + static_cast<long long>(k) * g.ldb;
+            s = fmaf(SG_IN_A(g, a + k, 1) ? __ldg(a + k) : 0.f, SG_IN_B(g, pb, 1) ? __ldg(pb) : 0.f, s);
             if (s != s) break;
         }
     }
@@ -553,38 +549,24 @@ __device__ __forceinline__ bool epi_all(bool v) {
 
 // One 16-column chunk of an accumulator: 16 C rows of this thread's column.
 // A paired accumulator holds hi*hi + lo*hi in its first TM columns and hi*lo
-// in the next TM; the chunk is their sum.  The epilogue issues the load of
-// chunk c + 1 (issue) before it stores chunk c, and collects it (finish)
-// at the start of the next iteration, so the tensor-memory latency overlaps
-// the stores, the proxy fence and the barrier of chunk c.
-// The look-ahead costs 16 registers per epilogue thread (32 for a paired
-// accumulator): kernels whose register budget has no room for them (paired
-// tiles, and the 16-producer-warp forms when A is not copied by TMA) load
-// each chunk where it is used (AHEAD false), which keeps them clear of
-// spills.
-template <int TM, bool AHEAD>
-struct AccChunk {
-    static constexpr bool kPaired = paired_for(TM);
-    static constexpr bool kAhead = AHEAD && !kPaired;
+// in the next TM; the chunk is their sum.
+template <int TM>
+__device__ __forceinline__ void acc_chunk(uint32_t taddr, float (&v)[16]) {
     uint32_t r[16];
-    uint32_t q[kPaired ? 16 : 1];
-    __device__ __forceinline__ void issue(uint32_t taddr) {
-        tmem_ld32x16_issue(taddr, r);
-        if constexpr (kPaired) tmem_ld32x16_issue(taddr + static_cast<uint32_t>(TM), *reinterpret_cast<uint32_t(*)[16]>(q));
-    }
-    // wait for the loads issued last (every tcgen05.ld of this thread) and sum
-    __device__ __forceinline__ void finish(float (&v)[16]) {
+    tmem_ld32x16_issue(taddr, r);
+    if constexpr (paired_for(TM)) {
+        uint32_t q[16];
+        tmem_ld32x16_issue(taddr + static_cast<uint32_t>(TM), q);
         tmem_ld_wait16(r);
-        if constexpr (kPaired) {
-            tmem_ld_wait16(*reinterpret_cast<uint32_t(*)[16]>(q));
+        tmem_ld_wait16(q);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]) + __uint_as_float(q[j]);
-        } else {
+        for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]) + __uint_as_float(q[j]);
+    } else {
+        tmem_ld_wait16(r);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
-        }
+        for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
     }
-};
+}
 
 // Last-arriver sum of a shared tile, by a team of nw warps (wid = this
 // warp's index in the team).  The nseg partial tiles (TM x 128, row-major,
@@ -605,8 +587,8 @@ __device__ __forceinline__ float fix_lane(const float4 &v, int q) {
 }
 
 template <int TM, int CONV, bool TRANS_B>
-__device__ __forceinline__ void fixup_tile(const GemmArgs &g, int bi, const float *wb, int nseg, int m0, int n0,
-                                        int wid, int nw, int lane) {
+__device__ __forceinline__ void fixup_tile(const GemmArgs &g, const DeviceCtl &ctl, int bi, const float *wb, int nseg,
+                                           int m0, int n0, int wid, int nw, int lane) {
     float *const cmat = g.C + bi * g.sC;  // matrix bi of a batch
     constexpr long long kTileElems = static_cast<long long>(kTileN) * TM;
     const int pass = kFixRows * nw;  // rows per pass
@@ -627,12 +609,12 @@ __device__ __forceinline__ void fixup_tile(const GemmArgs &g, int bi, const floa
             if (read_c && r < rows) {
                 const float *cp = cmat + static_cast<long long>(m0 + r) * g.ldc + nc;
                 if (full4) {
-                    old[j] = *reinterpret_cast<const float4 *>(cp);
+                    if (SG_IN_C(g, cp, 4)) old[j] = *reinterpret_cast<const float4 *>(cp);
                 } else {
-                    old[j].x = cp[0];
-                    if (nc + 1 < g.N) old[j].y = cp[1];
-                    if (nc + 2 < g.N) old[j].z = cp[2];
-                    if (nc + 3 < g.N) old[j].w = cp[3];
+                    if (SG_IN_C(g, cp, 1)) old[j].x = cp[0];
+                    if (nc + 1 < g.N && SG_IN_C(g, cp + 1, 1)) old[j].y = cp[1];
+                    if (nc + 2 < g.N && SG_IN_C(g, cp + 2, 1)) old[j].z = cp[2];
+                    if (nc + 3 < g.N && SG_IN_C(g, cp + 3, 1)) old[j].w = cp[3];
                 }
             }
         }
@@ -646,9 +628,11 @@ __device__ __forceinline__ void fixup_tile(const GemmArgs &g, int bi, const floa
             for (int q = 0; q < kFixSegs; ++q)
 #pragma unroll
                 for (int j = 0; j < kFixRows; ++j)
-                    if (s0 + q < nseg && r0 + nw * j < rows)
-                        v[q][j] = ld4cg(wb + (s0 + q) * kTileElems +
-                                        static_cast<long long>(r0 + nw * j) * kTileN + 4 * lane);
+                    if (s0 + q < nseg && r0 + nw * j < rows) {
+                        const float *pw = wb + (s0 + q) * kTileElems + static_cast<long long>(r0 + nw * j) * kTileN +
+                                          4 * lane;
+                        v[q][j] = SG_IN_WS(ctl, pw, 4) ? ld4cg(pw) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
 #pragma unroll
             for (int q = 0; q < kFixSegs; ++q)
                 if (s0 + q < nseg)
@@ -675,11 +659,11 @@ __device__ __forceinline__ void fixup_tile(const GemmArgs &g, int bi, const floa
             }
             float *cp = cmat + static_cast<long long>(m) * g.ldc + nc;
             if (full4) {
-                *reinterpret_cast<float4 *>(cp) = make_float4(res[0], res[1], res[2], res[3]);
+                if (SG_IN_C(g, cp, 4)) *reinterpret_cast<float4 *>(cp) = make_float4(res[0], res[1], res[2], res[3]);
             } else {
 #pragma unroll
                 for (int q = 0; q < 4; ++q)
-                    if (nc + q < g.N) cp[q] = res[q];
+                    if (nc + q < g.N && SG_IN_C(g, cp + q, 1)) cp[q] = res[q];
             }
         }
     }
@@ -698,9 +682,10 @@ __device__ __forceinline__ void prefetch_c_tile(const GemmArgs &g, int bi, int m
         const float *row = cmat + static_cast<long long>(m0 + r) * g.ldc + n0;
         if (vec) {
             const uint32_t bytes = static_cast<uint32_t>(cols * 4) & ~15u;
-            if (bytes) prefetch_l2_bulk(row, bytes);
+            if (bytes && SG_IN_C(g, row, static_cast<int>(bytes / 4))) prefetch_l2_bulk(row, bytes);
         } else {
-            for (int q = 0; q < cols; q += 32) prefetch_l2(row + q);
+            for (int q = 0; q < cols; q += 32)
+                if (SG_IN_C(g, row + q, 1)) prefetch_l2(row + q);
         }
     }
 }
@@ -718,19 +703,16 @@ __device__ __forceinline__ void prefetch_c_tile(const GemmArgs &g, int bi, int m
 // B4: B's rows are not 16-byte aligned; tmap_b, tmap_b1, tmap_b2, tmap_b3
 // describe its residue classes k % 4 = 0..3 (each N + o_r floats wide, box
 // 132 x 4, no swizzle) and b_offs packs the o_r; needs TMA_B.
-// DUAL: two CTAs per SM (Roles, Cfg).
-template <int TM, bool TMA_A, bool TMA_B, int CONV = kConvNone, bool TRANS_B = false, bool B4 = false,
-          bool DUAL = false>
-__global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B, DUAL>::kThreads, (DUAL ? 2 : 1))
+template <int TM, bool TMA_A, bool TMA_B, int CONV = kConvNone, bool TRANS_B = false, bool B4 = false>
+__global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
     tf32x3_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ Schedule sch,
                        const __grid_constant__ DeviceCtl ctl, int vec_a, int tma_c, uint32_t b_offs,
                        const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                        const __grid_constant__ CUtensorMap tmap_c, const __grid_constant__ CUtensorMap tmap_b1,
                        const __grid_constant__ CUtensorMap tmap_b2, const __grid_constant__ CUtensorMap tmap_b3) {
-    using C = Cfg<TM, TMA_B, B4, DUAL>;
-    using R = Roles<TM, TMA_A, TMA_B, DUAL>;
+    using C = Cfg<TM, TMA_B, B4>;
+    using R = Roles<TM, TMA_A, TMA_B>;
     static_assert(CONV == kConvNone || !TMA_B, "a convolution gathers B in the producers");
-    static_assert(!DUAL || (TMA_A && CONV == kConvNone), "two CTAs per SM: A by TMA (producer registers)");
     static_assert(!TRANS_B || (TMA_B && CONV == kConvNone), "a transposed B comes by TMA");
     static_assert(!B4 || (TMA_B && !TRANS_B && CONV == kConvNone), "residue classes of a row-major B");
     constexpr int S = C::kStages;
@@ -784,7 +766,7 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B, DUAL>::kThreads, (DUAL
         fence_mbar_init();
     }
     if (warp == R::kMmaWarp) {
-        tmem_alloc(smem_u32(tmem_slot), C::kCols);
+        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -799,7 +781,6 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B, DUAL>::kThreads, (DUAL
 
     if (warp < kEpiWarps) {
         // ------------------------------------------------------ epilogue
-        using Acc = AccChunk<TM, TMA_A>;
         const int nl = warp * 32 + lane;  // tensor-memory lane = column within the tile
         int it = 0;
         uint32_t cpar = 0;      // per C buffer: parity of its next c_full phase
@@ -848,8 +829,6 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B, DUAL>::kThreads, (DUAL
                 const int n0 = c.nt * kTileN;
                 const int nch = min(TM / CH, (g.M - m0 + CH - 1) / CH);  // chunks with rows below M
                 bool ok = true;
-                Acc ld;
-                if (Acc::kAhead && nch > 0) ld.issue(t0);
 #pragma unroll 1
                 for (int ch = 0; ch < nch; ++ch) {
                     const int b = ch % kEpiBufs;
@@ -858,7 +837,6 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B, DUAL>::kThreads, (DUAL
                         const bool wc = mbar_wait_bounded(cfull0 + 8u * b, (cpar >> b) & 1u, abort_flag, ctl,
                                                           kStatusTimeoutEpilogue);
                         if (!epi_all(wc)) {
-                            tmem_ld_wait();  // the chunk load in flight lands before the CTA goes on
                             ok = false;
                             break;
                         }
@@ -867,9 +845,7 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B, DUAL>::kThreads, (DUAL
                     }
                     const int mb = m0 + ch * CH;
                     float v[CH];
-                    if (!Acc::kAhead) ld.issue(t0 + ch * CH);
-                    ld.finish(v);
-                    if (Acc::kAhead && ch + 1 < nch) ld.issue(t0 + (ch + 1) * CH);
+                    acc_chunk<TM>(t0 + ch * CH, v);
                     bool nan = false;
 #pragma unroll
                     for (int j = 0; j < CH; ++j) nan |= v[j] != v[j];
@@ -915,8 +891,6 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B, DUAL>::kThreads, (DUAL
                 const bool read_c = g.beta != 0.f;
                 const bool n_ok = n < g.N;
                 float *cbase = g.C + c.b * g.sC + static_cast<long long>(m0) * g.ldc + n;
-                Acc ld;
-                if (Acc::kAhead) ld.issue(t0);
 #pragma unroll 1
                 for (int ch = 0; ch < TM / CH; ++ch) {
                     const int mb = m0 + ch * CH;
@@ -925,12 +899,10 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B, DUAL>::kThreads, (DUAL
                     if (read_c) {
 #pragma unroll
                         for (int j = 0; j < CH; ++j)
-                            old[j] = (n_ok && mb + j < g.M) ? cp[j * g.ldc] : 0.f;
+                            old[j] = (n_ok && mb + j < g.M && SG_IN_C(g, cp + j * g.ldc, 1)) ? cp[j * g.ldc] : 0.f;
                     }
                     float v[CH];
-                    if (!Acc::kAhead) ld.issue(t0 + ch * CH);
-                    ld.finish(v);
-                    if (Acc::kAhead && ch + 1 < TM / CH) ld.issue(t0 + (ch + 1) * CH);
+                    acc_chunk<TM>(t0 + ch * CH, v);
                     bool nan = false;
 #pragma unroll
                     for (int j = 0; j < CH; ++j) nan |= v[j] != v[j];
@@ -944,11 +916,12 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B, DUAL>::kThreads, (DUAL
                         if (read_c) {
 #pragma unroll
                             for (int j = 0; j < CH; ++j)
-                                if (mb + j < g.M) cp[j * g.ldc] = fmaf(g.beta, old[j], g.alpha * v[j]);
+                                if (mb + j < g.M && SG_IN_C(g, cp + j * g.ldc, 1))
+                                    cp[j * g.ldc] = fmaf(g.beta, old[j], g.alpha * v[j]);
                         } else {
 #pragma unroll
                             for (int j = 0; j < CH; ++j)
-                                if (mb + j < g.M) cp[j * g.ldc] = g.alpha * v[j];
+                                if (mb + j < g.M && SG_IN_C(g, cp + j * g.ldc, 1)) cp[j * g.ldc] = g.alpha * v[j];
                         }
                     }
                 }
@@ -964,16 +937,13 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B, DUAL>::kThreads, (DUAL
                 // unit to arrive adds all partials in segment order
                 constexpr int kTileElems = kTileN * TM;
                 float *wt = ctl.ws + (c.slot0 + c.seg) * kTileElems;
-                Acc ld;
-                if (Acc::kAhead) ld.issue(t0);
 #pragma unroll 1
                 for (int ch = 0; ch < TM / CH; ++ch) {
                     float v[CH];
-                    if (!Acc::kAhead) ld.issue(t0 + ch * CH);
-                    ld.finish(v);
-                    if (Acc::kAhead && ch + 1 < TM / CH) ld.issue(t0 + (ch + 1) * CH);
+                    acc_chunk<TM>(t0 + ch * CH, v);
 #pragma unroll
-                    for (int j = 0; j < CH; ++j) __stcg(wt + (ch * CH + j) * kTileN + nl, v[j]);
+                    for (int j = 0; j < CH; ++j)
+                        if (SG_IN_WS(ctl, wt + (ch * CH + j) * kTileN + nl, 1)) __stcg(wt + (ch * CH + j) * kTileN + nl, v[j]);
                 }
                 tc_fence_before();
                 mbar_arrive(acc_empty0 + 8u * acc);
@@ -982,7 +952,9 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B, DUAL>::kThreads, (DUAL
                 if (threadIdx.x == 0) {
                     // the last unit to arrive queues the tile's sum for the
                     // CTA's exit, where every warp of the CTA is free for it
-                    const int prev = atomicAdd(ctl.counters + c.tile, 1);
+                    const bool cnt_ok = !kDebugBounds || (c.tile >= 0 && c.tile < ctl.n_counters);
+                    if (!cnt_ok) atomicOr(ctl.status, kStatusOutOfBounds);
+                    const int prev = cnt_ok ? atomicAdd(ctl.counters + c.tile, 1) : -1;
                     if (prev == c.nseg - 1) {
                         ctl.counters[c.tile] = 0;
                         const int nd = *s_ndefer;
@@ -1195,7 +1167,7 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B, DUAL>::kThreads, (DUAL
     __syncthreads();
     if (warp == R::kMmaWarp) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, C::kCols);
+        tmem_dealloc(tmem_base, kTmemCols);
     }
     // deferred sums of shared tiles, by every warp of the CTA
     const int nd = *s_ndefer;
@@ -1203,7 +1175,7 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B, DUAL>::kThreads, (DUAL
         __threadfence();
 #pragma unroll 1
         for (int e = 0; e < nd; ++e)
-            fixup_tile<TM, CONV, TRANS_B>(g, s_defer[5 * e + 4], ctl.ws + static_cast<long long>(s_defer[5 * e + 3]) * (kTileN * TM),
+            fixup_tile<TM, CONV, TRANS_B>(g, ctl, s_defer[5 * e + 4], ctl.ws + static_cast<long long>(s_defer[5 * e + 3]) * (kTileN * TM),
                            s_defer[5 * e + 2], s_defer[5 * e] * TM, s_defer[5 * e + 1] * kTileN, warp,
                            R::kThreads / 32, lane);
     }

@@ -23,5 +23,8 @@ bool make_tmap_bt(const GemmArgs &g, int batch, CUtensorMap *map);
 bool make_tmap_b4(const GemmArgs &g, int batch, CUtensorMap maps[4], uint32_t *offs);
 // C: N x M fp32 (N innermost), box 128 x 16 (one epilogue chunk).
 bool make_tmap_c(const GemmArgs &g, int batch, CUtensorMap *map);
+// SGEMM_DEBUG builds: whether a map since the last call was refused because
+// it could address bytes outside its operand (clears the flag; this thread).
+bool map_range_error();
 
 }  // namespace sg

@@ -58,6 +58,10 @@ typedef struct CUstream_st *sgemm_stream_t;
 #define SGEMM_ERR_SCRATCH_LIMIT      10006 /* sgemm_noalloc: problem needs more
                                               split-K scratch than its fixed
                                               array holds                      */
+#define SGEMM_ERR_OUT_OF_BOUNDS      10007 /* a library built with SGEMM_DEBUG
+                                              found a kernel address outside
+                                              its matrix (the access was
+                                              skipped; C is unspecified)      */
 
 /* Algorithm selector for sgemm_ex / sgemm_host. */
 #define SGEMM_ALGO_AUTO   0 /* planner picks the faster path                  */
@@ -92,11 +96,6 @@ typedef struct CUstream_st *sgemm_stream_t;
  * bytes).  With the flag the kernel loads such a B itself.  Both give the
  * same bits. */
 #define SGEMM_FLAG_B_ROWS_LOADED (1 << 17)
-/* SGEMM_FLAG_TWO_CTAS_PER_SM: 3xTF32 path, tiles of at most 64 rows whose A
- * comes by TMA, split-K schedules: run two CTAs per SM, each with half the
- * tensor memory and shared memory and one group of producer warps, so that
- * two independent pipelines share each SM.  Same bits. */
-#define SGEMM_FLAG_TWO_CTAS_PER_SM (1 << 18)
 #define SGEMM_FLAG_DEBUG_WITHHOLD_ARRIVE 1 /* test only: one pipeline arrive
                                               is withheld and the on-device
                                               wait budget is cut to ~1 ms, so
@@ -214,8 +213,9 @@ int sgemm_plan_info(int M, int N, int K, const void *A, int lda,
  * status words of the current device: the one of every allocating entry
  * point and the one of sgemm_noalloc.  Returns 0, SGEMM_ERR_DEVICE_TIMEOUT
  * if a kernel launched since the last check gave up a bounded wait (or met
- * a work split it cannot finish, which the planner never produces), or a
- * positive cudaError_t.  When a word was set, it also waits for the whole
+ * a work split it cannot finish, which the planner never produces),
+ * SGEMM_ERR_OUT_OF_BOUNDS (SGEMM_DEBUG builds only) if a kernel computed an
+ * address outside its matrix, or a positive cudaError_t.  When a word was set, it also waits for the whole
  * device and clears the split-K arrival counters that word's kernels use.
  * Allocates no device memory.
  */

@@ -144,7 +144,12 @@ def test_plan_forced_splits_bound_units_per_cta():
 def test_plan_ffma_tiles():
     assert (plan(32, 4096, 64, algo=1)["tile_m"], plan(32, 4096, 64, algo=1)["tile_n"]) == (32, 512)
     assert plan(64, 4096, 64, algo=1)["tile_n"] == 256
-    assert plan(4096, 4096, 4096, algo=1)["tile_n"] == 128
+    # 128 x 256 tiles (one CTA per SM) once they fill 80 % of a wave, else 128 x 128
+    big = plan(4096, 4096, 4096, algo=1)
+    assert (big["tile_m"], big["tile_n"], big["grid"]) == (128, 256, 32 * 16)
+    assert plan(1024, 1024, 1024, algo=1)["tile_n"] == 128
+    assert plan(2048, 2048, 2048, algo=1, num_sms=152)["tile_n"] == 256  # 16 x 8 = 128 tiles >= 0.8 x 152
+    assert plan(2048, 1536, 2048, algo=1, num_sms=152)["tile_n"] == 128  # 16 x 6 = 96 tiles
 
 
 def test_plan_split_tail():

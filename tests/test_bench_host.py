@@ -11,7 +11,7 @@ import bench
 def fake_root(tmp_path, monkeypatch):
     (tmp_path / "profiles").mkdir()
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
-    monkeypatch.setattr(bench, "kernel_source_hash", lambda: "feedc0de12345678")
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda family="tf32x3": "feedc0de12345678")
     return tmp_path
 
 
@@ -47,3 +47,13 @@ def test_committed_summaries_name_their_sources_and_traffic():
         text = open(os.path.join(root, n)).read()
         assert "kernel_source_hash:" in text and "dram_bytes_per_launch:" in text, n
         assert "--clock-control none" in text, n
+
+
+def test_each_kernel_family_has_its_own_hash():
+    """A summary is retired only by changes to its own kernel family's
+    sources: the families hash different files."""
+    assert bench.kernel_family("tf32x3_NT") == "tf32x3"
+    assert bench.kernel_family("ffma_wide") == "ffma_wide"
+    assert bench.kernel_family("ffma") == "ffma"
+    hashes = {f: bench.kernel_source_hash(f) for f in bench.KERNEL_SOURCES}
+    assert len(set(hashes.values())) == len(hashes)

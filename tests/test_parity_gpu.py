@@ -79,6 +79,46 @@ def test_leading_dimensions_and_alignment(algo, layout, shape):
     check_against_oracle(p, C, what=f"{shape} {layout} algo={algo}")
 
 
+BIG_FFMA_CASES = [  # (M, N, K, ld pads, offsets, splits, beta): >= 0.8 of a wave of 128 x 256 tiles
+    (1100, 3900, 333, (0, 0, 0), (0, 0, 0), 0, 0.5), (1100, 3900, 333, (1, 3, 5), (0, 0, 0), 0, 1.25),
+    (1030, 4000, 200, (0, 0, 0), (1, 3, 2), 0, 0.5), (1100, 3900, 160, (0, 0, 0), (0, 0, 0), 3, 0.5),
+    (1024, 4096, 64, (0, 0, 0), (0, 0, 0), 0, 0.0)]
+
+
+@pytest.mark.parametrize("case", BIG_FFMA_CASES, ids=[f"{c[0]}x{c[1]}x{c[2]}-ld{c[3]}-off{c[4]}-s{c[5]}"
+                                                      for c in BIG_FFMA_CASES])
+def test_ffma_large_tiles(case):
+    """The FFMA path's 128 x 256 tiles (one CTA per SM, A transposed into
+    shared memory): every element against the oracle over ragged edges in
+    M, N and K, odd leading dimensions, misaligned pointers (4-byte copies),
+    forced split-K and beta = 0 with NaN in the old C."""
+    M, N, K, ld, off, splits, beta = case
+    p = _with_c(random_problem(M, N, K, alpha=0.5, beta=beta, seed=M + N + K + splits, lda=K + ld[0],
+                               ldb=N + ld[1], ldc=N + ld[2]))
+    plan = pkg.sgemm_plan_info(M, N, K, algo=pkg.SGEMM_ALGO_FFMA, splits=splits, num_sms=0)
+    assert (plan["tile_m"], plan["tile_n"]) == (128, 256), plan
+    C, st = run_sgemm(p, pkg.SGEMM_ALGO_FFMA, splits=splits, offsets=off)
+    assert st == 0
+    check_against_oracle(p, C, what=f"{case} FFMA 128 x 256")
+
+
+C_PAD_CASES = [(17, 15, 33, 20), (200, 301, 77, 304), (130, 1021, 64, 1024), (65, 255, 129, 260), (300, 14161, 40, 14164)]
+
+
+@pytest.mark.parametrize("algo", ALGOS, ids=ALGO_IDS)
+@pytest.mark.parametrize("case", C_PAD_CASES, ids=[f"{c[0]}x{c[1]}x{c[2]}-ldc{c[3]}" for c in C_PAD_CASES])
+def test_c_rows_aligned_but_n_ragged(algo, case):
+    """C rows 16-byte aligned (ldc % 4 == 0) while N is not a multiple of 4:
+    the padding floats right after each row's last column must stay as they
+    were (a TMA store would write the whole last 16-byte unit of a row)."""
+    M, N, K, ldc = case
+    for beta in (0.0, 0.5):
+        p = _with_c(random_problem(M, N, K, alpha=1.25, beta=beta, seed=M + N + ldc, ldc=ldc))
+        C, st = run_sgemm(p, algo)
+        assert st == 0
+        check_against_oracle(p, C, what=f"{case} beta={beta}")
+
+
 @pytest.mark.parametrize("rows", [64, 256])
 def test_tma_and_load_paths_agree_bitwise(rows):
     """Operands copied by TMA keep their raw fp32 words as the hi part (the
@@ -124,26 +164,6 @@ def test_unaligned_b_rows_by_tma(case):
         loaded, st = run_sgemm(p, pkg.SGEMM_ALGO_TF32X3, splits=splits, flags=flags | pkg.SGEMM_FLAG_B_ROWS_LOADED)
         assert st == 0
         assert np.array_equal(tma.view(np.uint32), loaded.view(np.uint32)), f"{case}: TMA and loaded B differ"
-
-
-DUAL_CASES = [(64, 5000, 147, 64, 1), (50, 3000, 300, 64, 3), (32, 4100, 27, 32, 1), (20, 2000, 40, 16, 2),
-              (64, 1021, 128, 64, 1)]
-
-
-@pytest.mark.parametrize("case", DUAL_CASES, ids=[f"{c[0]}x{c[1]}x{c[2]}-tm{c[3]}-s{c[4]}" for c in DUAL_CASES])
-def test_two_ctas_per_sm_same_bits(case):
-    """Short tiles run as two CTAs per SM (each with half the tensor and
-    shared memory): against the oracle, and bit for bit the same as one CTA
-    per SM, with whole tiles and split-K, aligned and unaligned B rows."""
-    M, N, K, rows, splits = case
-    p = _with_c(random_problem(M, N, K, alpha=0.75, beta=0.5, seed=M * 31 + N + K, pad_value=0.0))
-    flags = pkg.SGEMM_FLAG_TILE_ROWS(rows)
-    two, st = run_sgemm(p, pkg.SGEMM_ALGO_TF32X3, splits=splits, flags=flags | pkg.SGEMM_FLAG_TWO_CTAS_PER_SM)
-    assert st == 0
-    check_against_oracle(p, two, what=f"{case} two CTAs per SM")
-    one, st = run_sgemm(p, pkg.SGEMM_ALGO_TF32X3, splits=splits, flags=flags)
-    assert st == 0
-    assert np.array_equal(two.view(np.uint32), one.view(np.uint32)), f"{case}: one and two CTAs per SM differ"
 
 
 def test_unaligned_b_rows_batched_and_misaligned_start():
