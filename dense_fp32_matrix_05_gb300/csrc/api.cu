@@ -344,6 +344,20 @@ void plan_ffma(int M, int N, int K, int sms, int splits_req, Plan &p) {
     p.stages = sg::ffma_stages(p.tile_m, p.tile_n);
     p.ws_bytes = s.splits > 1
                      ? static_cast<size_t>(s.units) * p.tile_m * p.tile_n * sizeof(float) : 0;
+    // 128 x 256 tiles beyond whole waves: the leftover tiles of the partly
+    // empty last wave are cut into K slices (each at least 8 K tiles), so
+    // that the last wave is short instead of mostly idle
+    const int ts = big && splits_req == 0 ? tail_splits_for(tiles, s.k_tiles, sms) : 0;
+    if (ts > 0) {
+        const int rem = tiles % sms;
+        s.splits = 1;
+        s.dp_tiles = tiles - rem;
+        s.tail_tiles = rem;
+        s.tail_splits = ts;
+        s.units = s.dp_tiles + rem * ts;
+        p.grid = s.units;
+        p.ws_bytes = static_cast<size_t>(rem) * ts * p.tile_m * p.tile_n * sizeof(float);
+    }
 }
 
 // The path AUTO takes: the tensor path, except for the shapes the wide-N
@@ -364,6 +378,8 @@ int make_plan(int M, int N, int K, const void *A, int lda, const void *B, int ld
     p.vec_a = aligned16(A, lda) && sA % 4 == 0;
     p.vec_b = aligned16(B, ldb) && sB % 4 == 0;
     p.vec_c = aligned16(C, ldc) && sC % 4 == 0;
+    // the wide kernel's bulk-copy form runs one CTA per SM
+    if (p.wide && p.vec_b && N % 4 == 0) p.grid = std::min(p.sch.units, sms);
     if (p.sch.units <= 0 || p.grid <= 0) return SGEMM_ERR_INTERNAL;
     return 0;
 }
@@ -567,7 +583,7 @@ int run(int M, int N, int K, float alpha, const float *A, int lda, const float *
         e = sg::tf32x3_launch(p.tile_m, g, p.sch, ctl, p.vec_a, p.vec_b, p.vec_c, p.grid, stream, batch,
                               (flags & SGEMM_FLAG_B_ROWS_LOADED) != 0);
     else if (p.wide)
-        e = sg::ffma_wide_launch(g, p.vec_b, p.grid, stream);
+        e = sg::ffma_wide_launch(g, p.vec_b, p.grid, stream, sg::kConvNone, &ctl);
     else
         e = sg::ffma_launch(p.tile_m, p.tile_n, g, p.sch, ctl, p.vec_a, p.vec_b, p.vec_c, stream);
     return from_cuda(e);

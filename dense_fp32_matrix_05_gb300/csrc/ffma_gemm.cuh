@@ -273,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
 }
 
-// Large-tile form: CTA tile 128 x 256 x 16, one CTA of 256 threads per SM,
+// Large-tile form: CTA tile 128 x 256 x 32, one CTA of 256 threads per SM,
 // warps 2 (M) x 4 (N) of 64 x 64, each thread 8 rows x 16 columns (64 packed
 // column pairs).  A is stored transposed in shared memory (k rows of the
 // tile's 128 m, pitch 132 floats, filled by 4-byte cp.async copies that
@@ -285,43 +285,48 @@ __global__ void __launch_bounds__(kThreads, 2)
 // two groups of 4 (lm * 4 and 32 + lm * 4 in its warp's 64) and its columns
 // four groups of 4 (ln * 4 + 16 q), so each 128-bit shared load of a warp
 // touches every bank once.  Same per-element arithmetic and order as the
-// other FFMA kernels (an in-order fma.rn chain over k).
+// other FFMA kernels (an in-order fma.rn chain over k).  Stages of 32 k
+// (two of the schedule's 16-k tiles; one barrier per 32 k) measured 2 %
+// faster than 16 k on GB300 at 2048-8192 cubed.
 constexpr int kBigBM = 128;
 constexpr int kBigBN = 256;
+constexpr int kBigBK = 32;              // k per stage (a whole number of the schedule's 16-k tiles)
 constexpr int kBigPitchA = kBigBM + 4;  // A^T row pitch: stores of a warp hit 2 banks at most
 constexpr int kBigStages = 4;
+static_assert(kBigBK % kBK == 0, "stages hold whole schedule k tiles");
 
 struct BigCfg {
-    static constexpr int kAFloats = kBK * kBigPitchA;
-    static constexpr int kBFloats = kBK * kBigBN;
+    static constexpr int kAFloats = kBigBK * kBigPitchA;
+    static constexpr int kBFloats = kBigBK * kBigBN;
     static constexpr int kStageFloats = kAFloats + kBFloats;
     static constexpr int kSmemBytes = kBigStages * kStageFloats * 4 + 16;
 };
 
-// One stage: A^T (16 k x 128 m) and B (16 k x 256 n); out-of-range elements
+// One stage: A^T (kBigBK k x 128 m) and B (kBigBK k x 256 n); elements at
+// or beyond kend (the end of K, or of this unit's K slice) or outside M, N
 // are zero-filled by the copies.
-__device__ __forceinline__ void big_load_stage(const GemmArgs &g, bool vec_b, int m0, int n0, int k0, uint32_t sA,
-                                               uint32_t sB, int tid) {
-    // element e = tid + 256 i: row m = e / 16, k = e % 16 (a warp reads two
-    // 64-byte pieces of A's rows)
+__device__ __forceinline__ void big_load_stage(const GemmArgs &g, bool vec_b, int m0, int n0, int k0, int kend,
+                                               uint32_t sA, uint32_t sB, int tid) {
+    // element e = tid + 256 i: row m = e / kBigBK, k = e % kBigBK (a warp
+    // reads pieces of A's rows kBigBK floats long)
 #pragma unroll
-    for (int i = 0; i < kBigBM * kBK / kThreads; ++i) {
+    for (int i = 0; i < kBigBM * kBigBK / kThreads; ++i) {
         const int e = tid + i * kThreads;
-        const int r = e >> 4, kk = e & 15;
+        const int r = e / kBigBK, kk = e % kBigBK;
         const int m = m0 + r, k = k0 + kk;
-        const bool ok = m < g.M && k < g.K && SG_IN_A(g, g.A + static_cast<long long>(m) * g.lda + k, 1);
+        const bool ok = m < g.M && k < kend && SG_IN_A(g, g.A + static_cast<long long>(m) * g.lda + k, 1);
         const float *src = ok ? g.A + static_cast<long long>(m) * g.lda + k : g.A;
         cp_async4(sA + static_cast<uint32_t>((kk * kBigPitchA + r) * 4), src, ok ? 4u : 0u);
     }
     if (vec_b) {
 #pragma unroll
-        for (int i = 0; i < kBK * kBigBN / 4 / kThreads; ++i) {
+        for (int i = 0; i < kBigBK * kBigBN / 4 / kThreads; ++i) {
             const int j = tid + i * kThreads;
             const int r = j / (kBigBN / 4), nc = j % (kBigBN / 4);
             const int k = k0 + r, n = n0 + nc * 4;
             const float *src = g.B;
             uint32_t bytes = 0;
-            if (k < g.K && n < g.N) {
+            if (k < kend && n < g.N) {
                 src = g.B + static_cast<long long>(k) * g.ldb + n;
                 bytes = static_cast<uint32_t>(min(4, g.N - n) * 4);
                 if (!SG_IN_B(g, src, static_cast<int>(bytes / 4))) {
@@ -333,10 +338,10 @@ __device__ __forceinline__ void big_load_stage(const GemmArgs &g, bool vec_b, in
         }
     } else {
 #pragma unroll 4
-        for (int j = tid; j < kBK * kBigBN; j += kThreads) {
+        for (int j = tid; j < kBigBK * kBigBN; j += kThreads) {
             const int r = j / kBigBN, c = j % kBigBN;
             const int k = k0 + r, n = n0 + c;
-            const bool ok = k < g.K && n < g.N && SG_IN_B(g, g.B + static_cast<long long>(k) * g.ldb + n, 1);
+            const bool ok = k < kend && n < g.N && SG_IN_B(g, g.B + static_cast<long long>(k) * g.ldb + n, 1);
             const float *src = ok ? g.B + static_cast<long long>(k) * g.ldb + n : g.B;
             cp_async4(sB + static_cast<uint32_t>((r * kBigBN + c) * 4), src, ok ? 4u : 0u);
         }
@@ -356,9 +361,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int rowa = wm * 64 + lm * 4;  // rows rowa + i and rowa + 32 + i, i < 4
     const int colb = wn * 64 + ln * 4;  // columns colb + 16 q + j, q < 4, j < 4
 
-    const UnitCoord c = decode_unit(sch, blockIdx.x);
+    // one unit per CTA: split-K units, or whole tiles followed by the K
+    // slices of a split tail (the leftover tiles of a partly empty last wave)
+    const int u = static_cast<int>(blockIdx.x);
+    UnitCoord c;
+    if (sch.tail_tiles > 0 && u >= sch.dp_tiles) {
+        c = slice_unit(sch, sch.dp_tiles, u - sch.dp_tiles, sch.tail_splits, 0);
+    } else if (sch.tail_tiles > 0) {
+        tile_coords(sch, u, c);
+        c.kb = 0;
+        c.ke = sch.k_tiles;
+        c.seg = 0;
+        c.nseg = 1;
+        c.slot0 = 0;
+    } else {
+        c = decode_unit(sch, u);
+    }
     const int m0 = c.mt * kBigBM, n0 = c.nt * kBigBN;
-    const int KT = c.ke - c.kb;
+    const int kend = min(g.K, c.ke * kBK);             // end of this unit's K range
+    constexpr int kTilesPerStage = kBigBK / kBK;
+    const int KT = (c.ke - c.kb + kTilesPerStage - 1) / kTilesPerStage;  // stages of this unit
     const uint32_t s0 = smem_u32(smem_f);
 
     // acc[i][p]: row i of the thread (rowa + i, then rowa + 32 + i - 4),
@@ -373,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < kBigStages - 1; ++s) {
         if (s < KT) {
             const uint32_t st = s0 + static_cast<uint32_t>(s * BigCfg::kStageFloats * 4);
-            big_load_stage(g, vec_b != 0, m0, n0, (c.kb + s) * kBK, st, st + BigCfg::kAFloats * 4, tid);
+            big_load_stage(g, vec_b != 0, m0, n0, c.kb * kBK + s * kBigBK, kend, st, st + BigCfg::kAFloats * 4, tid);
         }
         cp_async_commit();
     }
@@ -386,14 +408,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int nt = t + kBigStages - 1;
             if (nt < KT) {
                 const uint32_t st = s0 + static_cast<uint32_t>((nt % kBigStages) * BigCfg::kStageFloats * 4);
-                big_load_stage(g, vec_b != 0, m0, n0, (c.kb + nt) * kBK, st, st + BigCfg::kAFloats * 4, tid);
+                big_load_stage(g, vec_b != 0, m0, n0, c.kb * kBK + nt * kBigBK, kend, st, st + BigCfg::kAFloats * 4,
+                               tid);
             }
             cp_async_commit();
         }
         const float *sA = smem_f + (t % kBigStages) * BigCfg::kStageFloats;
         const float *sB = sA + BigCfg::kAFloats;
 #pragma unroll
-        for (int k = 0; k < kBK; ++k) {
+        for (int k = 0; k < kBigBK; ++k) {
             const float4 a0 = *reinterpret_cast<const float4 *>(sA + k * kBigPitchA + rowa);
             const float4 a1 = *reinterpret_cast<const float4 *>(sA + k * kBigPitchA + rowa + 32);
             uint64_t b[8];

@@ -296,7 +296,148 @@ __global__ void __launch_bounds__(kThreads, 2) ffma_wide_kernel(const __grid_con
     cp_async_wait<0>();
 }
 
+// Bulk-copy form (B's rows and N 16-byte aligned, no convolution): one CTA
+// per SM with 8 compute warps and one loader warp.  The loader copies each
+// slab row (up to 2 KB of one B row) with a 1-D cp.async.bulk into a ring
+// of kBulkStages slabs with full/empty mbarriers, up to three blocks ahead
+// of the compute warps, which only wait, multiply and store C.  In the
+// cp.async form every thread issues its own copies between its FMAs and
+// the CTA's loads, FMAs and C stores took turns (measured on GB300 at
+// 32 x 1605632 x 27: loads and stores alone 74 us, with the FMAs 103 us).
+// The arithmetic is the cp.async form's, in the same order.
+constexpr int kBulkStages = 6;
+constexpr int kBulkThreads = kThreads + 32;  // + the loader warp
+constexpr int kBulkBarBytes = 16 * kBulkStages + 16;
+constexpr int kBulkSmemBytes = (kBulkStages * kStageFloats + kAFloats) * 4 + kBulkBarBytes;
+
+__global__ void __launch_bounds__(kBulkThreads, 1)
+    ffma_wide_bulk_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ DeviceCtl ctl) {
+    extern __shared__ __align__(16) float smem_w[];
+    const int tid = threadIdx.x;
+    const uint32_t s0 = smem_u32(smem_w);
+    float *a_t = smem_w + kBulkStages * kStageFloats;
+    const uint32_t sA = smem_u32(a_t);
+    const uint32_t bars = sA + kAFloats * 4;  // full[s] at bars + 8 s, empty[s] at bars + 8 (S + s)
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(a_t + kAFloats + 4 * kBulkStages);
+    constexpr int S = kBulkStages;
+
+    const int KC = (g.K + kKc - 1) / kKc;
+    const int nblk = (g.N + kCols - 1) / kCols;
+    const int mine = nblk > static_cast<int>(blockIdx.x)
+                         ? (nblk - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
+                               static_cast<int>(gridDim.x)
+                         : 0;
+    const int jobs = mine * KC;  // slabs of this CTA, block-major
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(bars + 8u * s, 1);                      // full: the loader's expect_tx arrive
+            mbar_init(bars + 8u * (S + s), kThreads / 32);    // empty: one arrive per compute warp
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    // A^T, zero outside M x K
+    for (int i = tid; i < kAFloats; i += kBulkThreads) {
+        const int k = i / kMaxM, m = i % kMaxM;
+        const float *pa = g.A + static_cast<long long>(m) * g.lda + k;
+        a_t[i] = (m < g.M && k < g.K && SG_IN_A(g, pa, 1)) ? *pa : 0.f;
+    }
+    __syncthreads();
+
+    if (tid >= kThreads) {
+        // ---------------------------------------------------- loader
+        if (tid == kThreads) {
+            int s = 0;
+            uint32_t ph = 0, used = 0, last_ph = 0;
+#pragma unroll 1
+            for (int q = 0; q < jobs; ++q) {
+                if (!mbar_wait_bounded(bars + 8u * (S + s), ph ^ 1u, abort_flag, ctl, kStatusTimeoutProducer)) break;
+                const int cb = static_cast<int>(blockIdx.x) + (q / KC) * static_cast<int>(gridDim.x);
+                const int kc = q % KC;
+                const int n0 = cb * kCols;
+                const uint32_t bytes = static_cast<uint32_t>(min(kCols, g.N - n0) * 4);
+                const int rows = min(kKc, g.K - kc * kKc);
+                mbar_arrive_expect_tx(bars + 8u * s, bytes * static_cast<uint32_t>(rows));
+                const uint32_t dst = s0 + static_cast<uint32_t>(s * kStageFloats * 4);
+#pragma unroll 1
+                for (int r = 0; r < rows; ++r) {
+                    const float *src = g.B + static_cast<long long>(kc * kKc + r) * g.ldb + n0;
+                    // SGEMM_DEBUG: a row outside B is not copied (the wait then runs out)
+                    if (SG_IN_B(g, src, static_cast<int>(bytes / 4)))
+                        bulk_load_1d(dst + static_cast<uint32_t>(r * kCols * 4), src, bytes, bars + 8u * s);
+                }
+                used |= 1u << s;
+                last_ph = (last_ph & ~(1u << s)) | (ph << s);
+                if (++s == S) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+            // every copy issued has landed before the CTA can exit
+            volatile int no_abort = 0;
+            for (int t = 0; t < S; ++t)
+                if (used & (1u << t))
+                    mbar_wait_bounded(bars + 8u * t, (last_ph >> t) & 1u, &no_abort, ctl, kStatusTimeoutDrain);
+        }
+        return;
+    }
+
+    // -------------------------------------------------------- compute
+    uint64_t acc0[kMaxM / 2], acc1[kMaxM / 2];  // row pairs of columns 2t and 2t + 1
+#pragma unroll
+    for (int mp = 0; mp < kMaxM / 2; ++mp) acc0[mp] = acc1[mp] = 0ull;
+    int s = 0;
+    uint32_t ph = 0;
+    const int lane = tid & 31;
+#pragma unroll 1
+    for (int bi = 0; bi < mine; ++bi) {
+        bool ok = true;
+#pragma unroll 1
+        for (int kc = 0; kc < KC; ++kc) {
+            if (!mbar_wait_bounded(bars + 8u * s, ph, abort_flag, ctl, kStatusTimeoutMma)) {
+                ok = false;
+                break;
+            }
+            const uint32_t st = s0 + static_cast<uint32_t>(s * kStageFloats * 4);
+            const int kn = min(kKc, g.K - kc * kKc);  // rows of this slab inside K
+#pragma unroll 2
+            for (int kk = 0; kk < kn; ++kk) {
+                float bx, by;
+                lds2f(st + static_cast<uint32_t>((kk * kCols + 2 * tid) * 4), bx, by);
+                const uint32_t arow = sA + static_cast<uint32_t>((kc * kKc + kk) * kMaxM * 4);
+                const uint64_t b0 = pair_bcast(bx), b1 = pair_bcast(by);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    uint64_t a[kMaxM / 4];
+#pragma unroll
+                    for (int p = 0; p < kMaxM / 8; ++p) lds_pairs(arow + h * 64 + p * 16, a[2 * p], a[2 * p + 1]);
+#pragma unroll
+                    for (int i = 0; i < kMaxM / 4; ++i) {
+                        ffma2(acc0[h * 8 + i], a[i], b0);
+                        ffma2(acc1[h * 8 + i], a[i], b1);
+                    }
+                }
+            }
+            // this warp is done with the slab: the loader may refill it
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bars + 8u * (S + s));
+            if (++s == S) {
+                s = 0;
+                ph ^= 1u;
+            }
+        }
+        if (!ok) break;
+        const int cb = static_cast<int>(blockIdx.x) + bi * static_cast<int>(gridDim.x);
+        store_block<kConvNone>(g, cb * kCols + 2 * tid, acc0, acc1);
+#pragma unroll
+        for (int mp = 0; mp < kMaxM / 2; ++mp) acc0[mp] = acc1[mp] = 0ull;
+    }
+}
+
 }  // namespace wide
+
+bool ffma_wide_bulk(const GemmArgs &g, int vec_b) { return vec_b && g.N % 4 == 0; }
 
 bool ffma_wide_fits(int M, int K) { return M >= 1 && M <= wide::kMaxM && K >= 1 && K <= wide::kMaxK; }
 
@@ -304,7 +445,16 @@ int ffma_wide_blocks(int N) { return (N + wide::kCols - 1) / wide::kCols; }
 
 int ffma_wide_smem_bytes() { return wide::kSmemBytes; }
 
-cudaError_t ffma_wide_launch(const GemmArgs &g, int vec_b, int grid, cudaStream_t stream, int conv) {
+cudaError_t ffma_wide_launch(const GemmArgs &g, int vec_b, int grid, cudaStream_t stream, int conv,
+                             const DeviceCtl *ctl) {
+    if (conv == kConvNone && ctl != nullptr && ffma_wide_bulk(g, vec_b)) {
+        // one CTA per SM (the caller's grid counts two per SM for the cp.async form)
+        cudaError_t e = cudaFuncSetAttribute(wide::ffma_wide_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             wide::kBulkSmemBytes);
+        if (e != cudaSuccess) return e;
+        wide::ffma_wide_bulk_kernel<<<grid, wide::kBulkThreads, wide::kBulkSmemBytes, stream>>>(g, *ctl);
+        return cudaGetLastError();
+    }
     auto kern = conv == kConvTapsDense ? wide::ffma_wide_kernel<kConvTapsDense>
                 : conv == kConvTaps    ? wide::ffma_wide_kernel<kConvTaps>
                                        : wide::ffma_wide_kernel<kConvNone>;

@@ -118,7 +118,11 @@ int ffma_wide_blocks(int N);
 int ffma_wide_smem_bytes();
 // conv: kConvNone, or the implicit-GEMM convolution form kConvTaps /
 // kConvTapsDense (g.cv; N = images * ldc pixels).
-cudaError_t ffma_wide_launch(const GemmArgs &g, int vec_b, int grid, cudaStream_t stream, int conv = kConvNone);
+// With ctl given, a plain GEMM whose B rows and N are 16-byte aligned runs
+// the bulk-copy form (ffma_wide_bulk; one CTA per SM: grid <= SMs).
+cudaError_t ffma_wide_launch(const GemmArgs &g, int vec_b, int grid, cudaStream_t stream, int conv = kConvNone,
+                             const DeviceCtl *ctl = nullptr);
+bool ffma_wide_bulk(const GemmArgs &g, int vec_b);
 
 // dst (cols x rows, leading dimension ldd) = transpose of src (rows x cols,
 // leading dimension lds); row-major fp32.  count matrices, src_stride /

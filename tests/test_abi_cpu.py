@@ -145,8 +145,8 @@ def test_plan_ffma_tiles():
     assert (plan(32, 4096, 64, algo=1)["tile_m"], plan(32, 4096, 64, algo=1)["tile_n"]) == (32, 512)
     assert plan(64, 4096, 64, algo=1)["tile_n"] == 256
     # 128 x 256 tiles (one CTA per SM) once they fill 80 % of a wave, else 128 x 128
-    big = plan(4096, 4096, 4096, algo=1)
-    assert (big["tile_m"], big["tile_n"], big["grid"]) == (128, 256, 32 * 16)
+    big = plan(4096, 4096, 4096, algo=1)  # 512 tiles: 3 waves, then 56 tiles in 2 K slices each
+    assert (big["tile_m"], big["tile_n"], big["tail_tiles"], big["grid"]) == (128, 256, 56, 3 * SMS + 56 * 2)
     assert plan(1024, 1024, 1024, algo=1)["tile_n"] == 128
     assert plan(2048, 2048, 2048, algo=1, num_sms=152)["tile_n"] == 256  # 16 x 8 = 128 tiles >= 0.8 x 152
     assert plan(2048, 1536, 2048, algo=1, num_sms=152)["tile_n"] == 128  # 16 x 6 = 96 tiles
@@ -205,7 +205,10 @@ def test_plan_wide_kernel_for_short_shallow_a():
     """M <= 32 and K <= 64 go to the FFMA path's wide-N kernel under AUTO."""
     p = plan(32, 1605632, 27)
     assert p["path"] == pkg.SGEMM_ALGO_FFMA and p["wide"] == 1
-    assert p["units"] == -(-1605632 // 512) and p["grid"] == min(p["units"], 2 * SMS)
+    # aligned B rows and N: the bulk-copy form, one CTA per SM; else two
+    assert p["units"] == -(-1605632 // 512) and p["grid"] == min(p["units"], SMS)
+    q = plan(32, 1605630, 27)
+    assert q["wide"] == 1 and q["grid"] == min(q["units"], 2 * SMS)
     assert plan(1, 7, 1)["wide"] == 1
     assert plan(32, 4096, 48)["wide"] == 1
     assert plan(32, 4096, 64)["path"] == pkg.SGEMM_ALGO_TF32X3      # AUTO: the tensor path wins at K = 64
@@ -408,10 +411,31 @@ def test_ffma_plans_cover_every_k_tile_once(sms):
     covered once and the split workspace holds one slot per partial tile."""
     import itertools
     shapes = [(1, 1, 1), (5, 7, 3), (32, 4096, 27), (32, 1605632, 64), (64, 559104, 147), (100, 300, 17),
-              (1023, 1021, 1025), (1024, 1024, 1024), (5120, 5120, 5120), (129, 257, 4096)]
+              (1023, 1021, 1025), (1024, 1024, 1024), (5120, 5120, 5120), (129, 257, 4096), (4096, 4096, 4096),
+              (2048, 2048, 2048), (3000, 5000, 700)]
     for (M, N, K), splits in itertools.product(shapes, (0, 2, 5)):
         p = plan(M, N, K, algo=pkg.SGEMM_ALGO_FFMA, splits=splits, num_sms=sms)
-        assert p["path"] == pkg.SGEMM_ALGO_FFMA and p["tail_tiles"] == 0
+        assert p["path"] == pkg.SGEMM_ALGO_FFMA
+        if p["tail_tiles"]:
+            # 128 x 256 tiles with a split tail: one unit per CTA, whole
+            # tiles first, then the K slices of the leftover tiles
+            assert (p["tile_m"], p["tile_n"]) == (128, 256) and splits == 0
+            tiles = -(-M // 128) * -(-N // 256)
+            kt = -(-K // 16)
+            tail = p["tail_tiles"]
+            ts = p["ws_bytes"] // (tail * 128 * 256 * 4)
+            dp = tiles - tail
+            assert dp % sms == 0 and 0 < tail < sms and ts >= 2 and p["grid"] == p["units"] == dp + tail * ts
+            per_cta = [[[(t, k) for k in range(kt)]] for t in range(dp)]
+            per_cta += [[[(dp + u // ts, k) for k in range((u % ts) * kt // ts, (u % ts + 1) * kt // ts)]]
+                        for u in range(tail * ts)]
+            seen = {}
+            for units in per_cta:
+                for unit in units:
+                    for tk in unit:
+                        seen[tk] = seen.get(tk, 0) + 1
+            assert len(seen) == tiles * kt and set(seen.values()) == {1}, (M, N, K, p)
+            continue
         tiles, kt, per_cta = _walk_units(p, M, N, K, sms)
         seen = {}
         for units in per_cta:
@@ -420,7 +444,9 @@ def test_ffma_plans_cover_every_k_tile_once(sms):
                     seen[tk] = seen.get(tk, 0) + 1
         assert len(seen) == tiles * kt and set(seen.values()) == {1}, (M, N, K, splits, p)
         if p["wide"]:
-            assert p["splits"] == 1 and p["grid"] == min(p["units"], 2 * sms) and p["ws_bytes"] == 0
+            # the bulk-copy form (aligned B rows and N) runs one CTA per SM
+            per_sm = 1 if N % 4 == 0 else 2
+            assert p["splits"] == 1 and p["grid"] == min(p["units"], per_sm * sms) and p["ws_bytes"] == 0
         else:
             assert p["grid"] == p["units"] == tiles * p["splits"]
             assert p["ws_bytes"] == (p["units"] * p["tile_m"] * p["tile_n"] * 4 if p["splits"] > 1 else 0)

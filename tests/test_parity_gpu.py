@@ -102,6 +102,29 @@ def test_ffma_large_tiles(case):
     check_against_oracle(p, C, what=f"{case} FFMA 128 x 256")
 
 
+WIDE_CASES = [(32, 1605632 // 64, 27), (24, 1500 * 4, 27), (17, 5000, 64), (32, 4096 + 512 + 4, 48), (5, 20, 3)]
+
+
+@pytest.mark.parametrize("case", WIDE_CASES, ids=[f"{c[0]}x{c[1]}x{c[2]}" for c in WIDE_CASES])
+def test_wide_bulk_form_matches_cp_async_form(case):
+    """The wide-N FFMA kernel's bulk-copy form (B rows and N 16-byte aligned:
+    one loader warp, a 6-slab ring) against the oracle, and bit for bit the
+    same as its cp.async form, which a B start 4 bytes off a 16-byte
+    boundary selects (same arithmetic, same order); N tails that are and
+    are not whole 512-column blocks, K tails."""
+    M, N, K = case
+    p = random_problem(M, N, K, alpha=-0.75, beta=0.5, seed=M + N + K, pad_value=0.0)
+    p.C[:, :N] = uniform(np.random.default_rng(N), M * N).reshape(M, N)
+    plan = pkg.sgemm_plan_info(M, N, K, algo=pkg.SGEMM_ALGO_FFMA, num_sms=0)
+    assert plan["wide"] == 1
+    bulk, st = run_sgemm(p, pkg.SGEMM_ALGO_FFMA)
+    assert st == 0
+    check_against_oracle(p, bulk, what=f"{case} bulk-copy wide form")
+    cp, st = run_sgemm(p, pkg.SGEMM_ALGO_FFMA, offsets=(0, 1, 0))
+    assert st == 0
+    assert np.array_equal(bulk.view(np.uint32), cp.view(np.uint32)), f"{case}: bulk and cp.async forms differ"
+
+
 C_PAD_CASES = [(17, 15, 33, 20), (200, 301, 77, 304), (130, 1021, 64, 1024), (65, 255, 129, 260), (300, 14161, 40, 14164)]
 
 
