@@ -19,6 +19,7 @@ from . import _build_ext
 __all__ = [
     "SGEMM_ALGO_AUTO", "SGEMM_ALGO_FFMA", "SGEMM_ALGO_TF32X3",
     "SGEMM_FLAG_DEBUG_WITHHOLD_ARRIVE", "SGEMM_FLAG_TILE_ROWS", "SGEMM_FLAG_WHOLE_TILES", "SGEMM_FLAG_SPLIT_TAIL",
+    "SGEMM_FLAG_PAIRS", "SGEMM_FLAG_NO_PAIRS",
     "SGEMM_ERR_DEVICE_TIMEOUT",
     "SgemmError", "library", "lib_path", "declared_functions",
     "sgemm", "sgemm_ex", "sgemm_host", "sgemm_plan_info", "sgemm_check_status",
@@ -162,6 +163,8 @@ def conv2d_out_size(H, W, KH, KW, stride=(1, 1), pad=(0, 0), dil=(1, 1)):
 SGEMM_CONV_NO_PAD_COPY = 1
 SGEMM_FLAG_NO_A_COPY = 1 << 16
 SGEMM_FLAG_B_ROWS_LOADED = 1 << 17
+SGEMM_FLAG_PAIRS = 1 << 18
+SGEMM_FLAG_NO_PAIRS = 1 << 19
 
 
 def sgemm_conv2d(X, Wt, Y, alpha=1.0, beta=0.0, stride=(1, 1), pad=(0, 0), dil=(1, 1), stream=None,
@@ -192,7 +195,7 @@ def sgemm_host(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, algo=0) -> int:
 
 
 _PLAN_KEYS = ["path", "tile_m", "tile_n", "splits", "units", "grid", "stages", "vec_a", "vec_b",
-              "ws_bytes", "tail_tiles", "wide"]
+              "ws_bytes", "tail_tiles", "wide", "pairs"]
 
 
 def sgemm_plan_info(M, N, K, A=0, lda=None, B=0, ldb=None, C=0, ldc=None, algo=0, splits=0,

@@ -74,6 +74,7 @@ struct HostBuffers {
 struct DevState {
     bool ready = false;
     int sms = 0;
+    int pair_slots = 0;  // CTA pairs of the 3xTF32 pair form resident at once
     int major = 0, minor = 0;
     int *status = nullptr;
     std::map<cudaStream_t, Workspace> ws;
@@ -112,6 +113,7 @@ int device_state(DevState **out) {
         e = cudaGetSymbolAddress(&p, g_status_word);
         if (e != cudaSuccess) return from_cuda(e);
         d.status = static_cast<int *>(p);
+        d.pair_slots = sg::tf32x3_pair_slots();
         d.ready = true;
     }
     *out = &d;
@@ -264,11 +266,64 @@ Tf32x3Choice choose_tf32x3(int M, int N, int K, int sms, int forced_tm, int spli
     return best;
 }
 
+// A tile of 192 or 256 rows on CTA pairs (SGEMM_FLAG_PAIRS): tiles of 256
+// columns walked by `slots` pairs (the pairs resident at once), each pair
+// two CTAs of the grid.  Whole waves of tiles plus a split tail, or split-K
+// when a split count is forced.  Counters: two per tile (one per CTA half).
+void plan_pairs(int M, int N, int K, int tm, int slots, int splits_req, int flags, Plan &p, int batch) {
+    constexpr int kPairN = 2 * sg::kTf32x3TileN;
+    p.tile_m = tm;
+    p.tile_n = kPairN;
+    Schedule &s = p.sch;
+    s = Schedule{};
+    s.pair_shift = 1;
+    s.m_tiles = ceil_div(M, tm);
+    s.n_tiles = ceil_div(N, kPairN);
+    s.k_tiles = ceil_div(K, sg::kTf32x3BK);
+    s.tpb = batch > 1 ? s.m_tiles * s.n_tiles : 0;
+    const int tiles = s.m_tiles * s.n_tiles * batch;
+    s.splits = splits_req > 0 ? std::max(1, std::min(splits_req, s.k_tiles)) : 1;
+    s.units = tiles * s.splits;
+    s.group_m = std::min(8, s.m_tiles);
+    int walkers = std::min(s.units, slots);
+    // a CTA finishes at most kTf32x3MaxDefer shared tiles (one half each)
+    if (s.splits > 1) walkers = std::max(walkers, ceil_div(s.units, sg::kTf32x3MaxDefer));
+    p.grid = 2 * walkers;
+    p.stages = sg::tf32x3_stages(tm, true);
+    const size_t tile_bytes = static_cast<size_t>(kPairN) * tm * sizeof(float);
+    p.ws_bytes = s.splits > 1 ? static_cast<size_t>(s.units) * tile_bytes : 0;
+    const int ts = (s.splits == 1 && !(flags & SGEMM_FLAG_WHOLE_TILES)) ? tail_splits_for(tiles, s.k_tiles, slots) : 0;
+    if (ts > 0) {
+        const int rem = tiles % slots;
+        s.dp_tiles = tiles - rem;
+        s.tail_tiles = rem;
+        s.tail_splits = ts;
+        p.grid = 2 * slots;
+        p.ws_bytes = static_cast<size_t>(rem) * ts * tile_bytes;
+    }
+}
+
+// Whether a tile of tm rows runs on CTA pairs.  Measured on GB300 (TF/s,
+// single CTAs -> pairs): 5120^3 322 -> 342, 8192^3 whole tiles 340 -> 362,
+// 2048^3 237 -> 244, 256 x 43264 x 1152 208 -> 218; tiles of 192 rows
+// gained nothing (384 x 14161 x 1152: 178 both).
+bool use_pairs(int tm, int flags, int pair_slots) {
+    if (pair_slots <= 0 || (flags & SGEMM_FLAG_NO_PAIRS) || !sg::tf32x3_pair_tm(tm)) return false;
+    return (flags & SGEMM_FLAG_PAIRS) || tm == 256;
+}
+
 // batch > 1: one launch over the tiles of every matrix (Schedule::tpb).
-void plan_tf32x3(int M, int N, int K, int sms, int splits_req, int flags, bool read_c, Plan &p, int batch = 1) {
+// pair_slots > 0: CTA pairs are possible for this call (operands copied by
+// TMA) and that many fit on the device (use_pairs decides).
+void plan_tf32x3(int M, int N, int K, int sms, int splits_req, int flags, bool read_c, Plan &p, int batch = 1,
+                 int pair_slots = 0) {
     p.path = SGEMM_ALGO_TF32X3;
     const Tf32x3Choice ch = choose_tf32x3(M, N, K, sms, forced_tile_rows(flags), splits_req, flags, read_c, batch);
     const int tm = ch.tm;
+    if (use_pairs(tm, flags, pair_slots)) {
+        plan_pairs(M, N, K, tm, pair_slots, splits_req, flags, p, batch);
+        return;
+    }
     p.tile_m = tm;
     p.tile_n = sg::kTf32x3TileN;
     Schedule &s = p.sch;
@@ -368,15 +423,23 @@ int resolve_path(int M, int K, int algo, int splits) {
 
 // batch > 1 (3xTF32 path only): matrix b of each operand starts b * stride
 // elements after the first; 16-byte copies need 16-byte strides too.
+// pair_slots: CTA pairs the device holds at once (0: no pair form).
 int make_plan(int M, int N, int K, const void *A, int lda, const void *B, int ldb, const void *C, int ldc,
               int algo, int splits, int flags, int sms, bool read_c, Plan &p, int batch = 1, long long sA = 0,
-              long long sB = 0, long long sC = 0) {
+              long long sB = 0, long long sC = 0, int pair_slots = 0) {
     const int path = resolve_path(M, K, algo, splits);
     if (batch > 1 && path != SGEMM_ALGO_TF32X3) return SGEMM_ERR_INTERNAL;
-    if (path == SGEMM_ALGO_TF32X3) plan_tf32x3(M, N, K, sms, splits, flags, read_c, p, batch);
+    const bool va = aligned16(A, lda) && sA % 4 == 0;
+    const bool vb = aligned16(B, ldb) && sB % 4 == 0;
+    // the pair form copies A and B by TMA: B's rows aligned, or an aligned
+    // start with whole residue classes (K >= 4, batch stride of 4 floats)
+    const bool b_tma = vb || ((reinterpret_cast<uintptr_t>(B) & 15u) == 0 && K >= 4 && sB % 4 == 0 &&
+                              !(flags & SGEMM_FLAG_B_ROWS_LOADED));
+    const int slots = (va && b_tma) ? pair_slots : 0;
+    if (path == SGEMM_ALGO_TF32X3) plan_tf32x3(M, N, K, sms, splits, flags, read_c, p, batch, slots);
     else plan_ffma(M, N, K, sms, splits, p);
-    p.vec_a = aligned16(A, lda) && sA % 4 == 0;
-    p.vec_b = aligned16(B, ldb) && sB % 4 == 0;
+    p.vec_a = va;
+    p.vec_b = vb;
     p.vec_c = aligned16(C, ldc) && sC % 4 == 0;
     // the wide kernel's bulk-copy form runs one CTA per SM
     if (p.wide && p.vec_b && N % 4 == 0) p.grid = std::min(p.sch.units, sms);
@@ -399,7 +462,7 @@ size_t span_bytes(int rows, int cols, long long ld) {
 
 bool flags_valid(int flags) {
     if (flags & ~(SGEMM_FLAG_DEBUG_WITHHOLD_ARRIVE | SGEMM_FLAG_WHOLE_TILES | SGEMM_FLAG_SPLIT_TAIL | 0xFF00 |
-                  SGEMM_FLAG_NO_A_COPY | SGEMM_FLAG_B_ROWS_LOADED))
+                  SGEMM_FLAG_NO_A_COPY | SGEMM_FLAG_B_ROWS_LOADED | SGEMM_FLAG_PAIRS | SGEMM_FLAG_NO_PAIRS))
         return false;
     const int tm = forced_tile_rows(flags);
     return tm == 0 || sg::tf32x3_supported_tm(tm);
@@ -534,7 +597,7 @@ int run(int M, int N, int K, float alpha, const float *A, int lda, const float *
             return from_cuda(sg::scale_c_launch(C, ldc, M, N, beta, d->sms, stream));
         }
         rc = make_plan(M, N, K, A, lda, B, ldb, C, ldc, algo, splits, flags, d->sms, beta != 0.f, p, batch, sA, sB,
-                       sC);
+                       sC, trans_b ? 0 : d->pair_slots);
         if (rc != 0) return rc;
         ctl.status = d->status;
         ctl.wait_budget = (flags & SGEMM_FLAG_DEBUG_WITHHOLD_ARRIVE) ? kDebugWaitBudget : kWaitBudget;
@@ -542,7 +605,8 @@ int run(int M, int N, int K, float alpha, const float *A, int lda, const float *
         if (p.ws_bytes > 0) {  // split-K or split tail: tiles shared by several units
             Workspace *w = nullptr;
             rc = get_workspace(*d, stream, p.ws_bytes,
-                               static_cast<size_t>(p.sch.m_tiles) * p.sch.n_tiles * std::max(batch, 1), &w);
+                               static_cast<size_t>(p.sch.m_tiles) * p.sch.n_tiles * std::max(batch, 1)
+                                   << p.sch.pair_shift, &w);
             if (rc != 0) return rc;
             ctl.ws = w->ws;
             ctl.counters = w->counters;
@@ -1118,18 +1182,20 @@ int sgemm_plan_info(int M, int N, int K, const void *A, int lda, const void *B, 
     if (ninfo < 0) return -17;
     (void)alpha;
     (void)beta;
-    int sms = num_sms;
+    int sms = num_sms, pair_slots = num_sms / 2;
     if (sms == 0) {
         std::lock_guard<std::mutex> lk(g_mu);
         DevState *d = nullptr;
         int rc = device_state(&d);
         if (rc != 0) return rc;
         sms = d->sms;
+        pair_slots = d->pair_slots;
     }
-    int vals[12] = {0};
+    int vals[13] = {0};
     if (M > 0 && N > 0 && K > 0) {
         Plan p;
-        int rc = make_plan(M, N, K, A, lda, B, ldb, C, ldc, algo, splits, flags, sms, beta != 0.f, p);
+        int rc = make_plan(M, N, K, A, lda, B, ldb, C, ldc, algo, splits, flags, sms, beta != 0.f, p, 1, 0, 0, 0,
+                           pair_slots);
         if (rc != 0) return rc;
         vals[0] = p.path;
         vals[1] = p.tile_m;
@@ -1143,8 +1209,9 @@ int sgemm_plan_info(int M, int N, int K, const void *A, int lda, const void *B, 
         vals[9] = static_cast<int>(std::min<size_t>(p.ws_bytes, 0x7fffffff));
         vals[10] = p.sch.tail_tiles;
         vals[11] = p.wide ? 1 : 0;
+        vals[12] = p.sch.pair_shift;
     }
-    for (int i = 0; i < ninfo && i < 12; ++i) info[i] = vals[i];
+    for (int i = 0; i < ninfo && i < 13; ++i) info[i] = vals[i];
     return 0;
 }
 
@@ -1287,15 +1354,17 @@ int check_tensor_call(int M, int N, int K, float alpha, const float *A, int lda,
 }
 
 int plan_tensor_call(int M, int N, int K, const float *A, int lda, const float *B, int ldb, float beta,
-                     const float *C, int ldc, int splits, int sms, size_t max_ws_floats, TensorPlan *out) {
+                     const float *C, int ldc, int splits, int sms, int pair_slots, size_t max_ws_floats,
+                     TensorPlan *out) {
     Plan p;
-    int rc = make_plan(M, N, K, A, lda, B, ldb, C, ldc, SGEMM_ALGO_TF32X3, splits, 0, sms, beta != 0.f, p);
+    int rc = make_plan(M, N, K, A, lda, B, ldb, C, ldc, SGEMM_ALGO_TF32X3, splits, 0, sms, beta != 0.f, p, 1, 0, 0,
+                       0, pair_slots);
     if (rc != 0) return rc;
     if (p.sch.tail_tiles > 0 && p.ws_bytes / sizeof(float) > max_ws_floats) {
         // the split tail is an optimisation: drop it rather than exceed the scratch
         p = Plan();
         rc = make_plan(M, N, K, A, lda, B, ldb, C, ldc, SGEMM_ALGO_TF32X3, splits, SGEMM_FLAG_WHOLE_TILES, sms,
-                       beta != 0.f, p);
+                       beta != 0.f, p, 1, 0, 0, 0, pair_slots);
         if (rc != 0) return rc;
     }
     out->tile_m = p.tile_m;
@@ -1305,7 +1374,7 @@ int plan_tensor_call(int M, int N, int K, const float *A, int lda, const float *
     out->vec_b = p.vec_b;
     out->vec_c = p.vec_c;
     out->ws_floats = p.ws_bytes / sizeof(float);
-    out->tiles = p.sch.m_tiles * p.sch.n_tiles;
+    out->tiles = (p.sch.m_tiles * p.sch.n_tiles) << p.sch.pair_shift;
     return 0;
 }
 

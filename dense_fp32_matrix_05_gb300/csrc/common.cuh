@@ -118,6 +118,8 @@ struct Schedule {
     int tail_tiles;   // tiles after them, split along K (0 = split-K schedule)
     int tail_splits;  // K slices per tail tile
     int tpb;          // tiles per matrix of a batch (0: one matrix); tile t is tile t % tpb of matrix t / tpb
+    int pair_shift;   // 1: the units are walked by CTA pairs (clusters of two CTAs, one walker each;
+                      //    a tile is then 256 columns, 128 per CTA); 0: by single CTAs
 };
 
 struct DeviceCtl {
@@ -176,18 +178,20 @@ __device__ __forceinline__ UnitCoord decode_unit(const Schedule &s, int u) {
     return slice_unit(s, 0, u, s.splits, 0);
 }
 
-// The work units of one CTA, in order: next_unit() advances the position
-// (i: index of the next strided unit; tail: the tail slice was handed out)
-// and returns the unit there.  Every role of the CTA walks the same sequence.
+// The work units of one walker (a CTA, or a CTA pair: cta = its index), in
+// order: next_unit() advances the position (i: index of the next strided
+// unit; tail: the tail slice was handed out) and returns the unit there.
+// Every role of the CTA (of both CTAs of a pair) walks the same sequence.
 __device__ __forceinline__ bool next_unit(const Schedule &s, int cta, int &i, bool &tail, UnitCoord &c) {
+    const int walkers = static_cast<int>(gridDim.x) >> s.pair_shift;
     if (s.tail_tiles == 0) {
-        const int u = cta + i * static_cast<int>(gridDim.x);
+        const int u = cta + i * walkers;
         ++i;
         if (u >= s.units) return false;
         c = decode_unit(s, u);
         return true;
     }
-    const int t = cta + i * static_cast<int>(gridDim.x);
+    const int t = cta + i * walkers;
     if (t < s.dp_tiles) {
         ++i;
         tile_coords(s, t, c);
@@ -222,16 +226,24 @@ struct UnitIter {
 
 // Spin on an mbarrier phase with a cycle budget.  Returns false when the
 // budget runs out (the status word and the CTA's abort flag are then set) or
-// when another role of the CTA has already aborted.
+// when another role of the CTA has already aborted.  CLUSTER: the phase is
+// completed by threads of the other CTA of a pair (acquire at cluster scope).
+template <bool CLUSTER = false>
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+    if constexpr (CLUSTER) return mbar_try_wait_cluster(bar, parity);
+    else return mbar_try_wait(bar, parity);
+}
+
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
                                                   volatile int *abort_flag,
                                                   const DeviceCtl &ctl, int status_bit) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try<CLUSTER>(bar, parity)) return true;
     const long long t0 = clock64();
     while (true) {
 #pragma unroll 1
         for (int i = 0; i < 16; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
+            if (mbar_try<CLUSTER>(bar, parity)) return true;
         if (*abort_flag) return false;
         if (clock64() - t0 > ctl.wait_budget) {
             *abort_flag = 1;

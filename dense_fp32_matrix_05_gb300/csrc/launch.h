@@ -26,6 +26,28 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), int grid, int threads, int smem, 
     return cudaLaunchKernelEx(&cfg, kern, static_cast<Args &&>(args)...);
 }
 
+// Same, in clusters of two CTAs along x (grid even): the CTA pairs of the
+// 3xTF32 kernel's cta_group::2 form.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl_pairs(void (*kern)(KArgs...), int grid, int threads, int smem, cudaStream_t stream,
+                             Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(static_cast<unsigned>(threads));
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 2;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<Args &&>(args)...);
+}
+
 // Extents of a GEMM's operands for the SGEMM_DEBUG bounds checks: one past
 // the last float of A (M x K), B (K x N, or N x K when transposed) and C
 // (M x N) over `batch` matrices with the strides in g; dbg_status is where
@@ -48,8 +70,13 @@ constexpr int kFfmaBK = 16;        // K per FFMA pipeline stage
 
 // 3xTF32 tensor-core path.  tm = C rows per tile: 16, 32, 64, 128, 192, 256.
 bool tf32x3_supported_tm(int tm);
-int tf32x3_stages(int tm);
+int tf32x3_stages(int tm, bool pair = false);
 int tf32x3_smem_bytes(int tm);
+// CTA pairs (clusters of two sharing a cta_group::2 MMA; tiles of 192 or 256
+// rows x 256 columns, s.pair_shift = 1, grid = 2 x pairs): whether tm has the
+// form, and how many pairs the device holds at once (0 if none, or on error).
+bool tf32x3_pair_tm(int tm);
+int tf32x3_pair_slots();
 // B stored transposed (N x K, row stride g.ldb; BLAS transb): the 3xTF32
 // kernel copies B^T slabs by TMA and reads them column by column, with no
 // transpose pass.  A's and B's rows (and batch strides) must be 16-byte
@@ -93,12 +120,14 @@ struct TensorPlan {
     int vec_b = 0;
     int vec_c = 0;
     size_t ws_floats = 0;  // split-K partial-tile floats needed (0 without split-K)
-    int tiles = 0;         // output tiles (= arrival counters needed)
+    int tiles = 0;         // arrival counters needed (one per tile; two per tile of a CTA pair)
 };
 int check_tensor_call(int M, int N, int K, float alpha, const float *A, int lda, const float *B, int ldb,
                       float beta, const float *C, int ldc, int splits);
+// pair_slots: CTA pairs the device holds at once (tf32x3_pair_slots; 0: none).
 int plan_tensor_call(int M, int N, int K, const float *A, int lda, const float *B, int ldb, float beta,
-                     const float *C, int ldc, int splits, int sms, size_t max_ws_floats, TensorPlan *out);
+                     const float *C, int ldc, int splits, int sms, int pair_slots, size_t max_ws_floats,
+                     TensorPlan *out);
 // Read and clear sgemm_noalloc's status word on the current device (after
 // the caller has waited for its stream).  Returns 0 when the word is clear
 // or sgemm_noalloc has not been set up on this device, 1 when it was set

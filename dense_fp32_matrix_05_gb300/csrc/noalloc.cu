@@ -46,6 +46,7 @@ struct DeviceScratch {
     int *counters = nullptr;
     int *status = nullptr;
     int sms = 0;
+    int pair_slots = 0;  // CTA pairs of the 3xTF32 kernel resident at once
 };
 
 std::mutex g_setup_mu;
@@ -79,6 +80,7 @@ int device_scratch(DeviceScratch **out) {
         if ((e = sg::tf32x3_preload()) != cudaSuccess || (e = sg::scale_c_preload()) != cudaSuccess)
             return static_cast<int>(e);
         d.sms = sms;
+        d.pair_slots = sg::tf32x3_pair_slots();
         d.ready = true;
     }
     *out = &d;
@@ -132,7 +134,8 @@ extern "C" int sgemm_noalloc(int M, int N, int K, float alpha, const float *A, i
         if (beta == 1.f) return 0;
         return static_cast<int>(sg::scale_c_launch(C, ldc, M, N, beta, d->sms, st));
     }
-    if ((rc = sg::plan_tensor_call(M, N, K, A, lda, B, ldb, beta, C, ldc, splits, d->sms, kScratchFloats, &plan)) != 0)
+    if ((rc = sg::plan_tensor_call(M, N, K, A, lda, B, ldb, beta, C, ldc, splits, d->sms, d->pair_slots,
+                                   kScratchFloats, &plan)) != 0)
         return rc;
     const int debug = g_next_debug_flags.exchange(0);
     sg::DeviceCtl ctl{};

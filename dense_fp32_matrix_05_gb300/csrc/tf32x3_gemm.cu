@@ -196,16 +196,44 @@ bool make_tmap_c(const GemmArgs &g, int batch, CUtensorMap *map) {
 
 namespace {
 
-template <int TM, bool TA, bool TB, bool B4 = false>
+template <int TM, bool TA, bool TB, bool B4 = false, bool PAIR = false>
 cudaError_t launch_tm(const GemmArgs &g, const Schedule &s, const DeviceCtl &ctl, int vec_a, int tma_c, int grid,
                       const CUtensorMap &map_a, const CUtensorMap (&map_b)[4], uint32_t b_offs,
                       const CUtensorMap &map_c, cudaStream_t stream) {
-    using C = tf32x3::Cfg<TM, TB, B4>;
-    auto kern = tf32x3::tf32x3_gemm_kernel<TM, TA, TB, kConvNone, false, B4>;
+    using C = tf32x3::Cfg<TM, TB, B4, PAIR>;
+    auto kern = tf32x3::tf32x3_gemm_kernel<TM, TA, TB, kConvNone, false, B4, PAIR>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    return launch_pdl(kern, grid, tf32x3::Roles<TM, TA, TB>::kThreads, C::kSmemBytes, stream, g, s, ctl, vec_a,
-                      tma_c, b_offs, map_a, map_b[0], map_c, map_b[1], map_b[2], map_b[3]);
+    if constexpr (PAIR)
+        return launch_pdl_pairs(kern, grid, tf32x3::Roles<TM, TA, TB>::kThreads, C::kSmemBytes, stream, g, s, ctl,
+                                vec_a, tma_c, b_offs, map_a, map_b[0], map_c, map_b[1], map_b[2], map_b[3]);
+    else
+        return launch_pdl(kern, grid, tf32x3::Roles<TM, TA, TB>::kThreads, C::kSmemBytes, stream, g, s, ctl, vec_a,
+                          tma_c, b_offs, map_a, map_b[0], map_c, map_b[1], map_b[2], map_b[3]);
+}
+
+// The CTA-pair form (s.pair_shift = 1): A and B copied by TMA (B's rows
+// aligned, or as residue classes), A in boxes of TM / 2 rows, one per CTA.
+template <int TM>
+cudaError_t launch_pairs(const GemmArgs &g, const Schedule &s, const DeviceCtl &ctl, int vec_a, int vec_b,
+                         int vec_c, int grid, int batch, bool b_rows, cudaStream_t stream) {
+    if constexpr (TM != 192 && TM != 256) {
+        return cudaErrorInvalidValue;
+    } else {
+        CUtensorMap ma, mb[4], mc;
+        std::memset(&ma, 0, sizeof(ma));
+        std::memset(mb, 0, sizeof(mb));
+        std::memset(&mc, 0, sizeof(mc));
+        uint32_t offs = 0;
+        if (grid % 2 != 0 || !vec_a || !make_tmap_a(g, TM / 2, batch, &ma)) return cudaErrorInvalidValue;
+        const bool tb = vec_b && make_tmap_b(g, batch, &mb[0]);
+        const bool tb4 = !tb && !vec_b && !b_rows && make_tmap_b4(g, batch, mb, &offs);
+        const int tc = (vec_c && make_tmap_c(g, batch, &mc)) ? 1 : 0;
+        if (map_range_error()) return cudaErrorInvalidValue;  // SGEMM_DEBUG only
+        if (tb) return launch_tm<TM, true, true, false, true>(g, s, ctl, vec_a, tc, grid, ma, mb, 0, mc, stream);
+        if (tb4) return launch_tm<TM, true, true, true, true>(g, s, ctl, vec_a, tc, grid, ma, mb, offs, mc, stream);
+        return cudaErrorInvalidValue;
+    }
 }
 
 // Operands go through TMA whenever their rows are 16-byte aligned: the deep
@@ -218,6 +246,7 @@ cudaError_t launch_tm(const GemmArgs &g, const Schedule &s, const DeviceCtl &ctl
 template <int TM>
 cudaError_t launch_rows(const GemmArgs &g, const Schedule &s, const DeviceCtl &ctl, int vec_a, int vec_b,
                         int vec_c, int grid, int batch, bool b_rows, cudaStream_t stream) {
+    if (s.pair_shift) return launch_pairs<TM>(g, s, ctl, vec_a, vec_b, vec_c, grid, batch, b_rows, stream);
     CUtensorMap ma, mb[4], mc;
     std::memset(&ma, 0, sizeof(ma));
     std::memset(mb, 0, sizeof(mb));
@@ -244,10 +273,10 @@ cudaError_t launch_rows(const GemmArgs &g, const Schedule &s, const DeviceCtl &c
 
 namespace {
 
-template <int TM, bool TA, bool TB, bool B4 = false>
+template <int TM, bool TA, bool TB, bool B4 = false, bool PAIR = false>
 cudaError_t preload_one() {
     cudaFuncAttributes attr;
-    return cudaFuncGetAttributes(&attr, tf32x3::tf32x3_gemm_kernel<TM, TA, TB, kConvNone, false, B4>);
+    return cudaFuncGetAttributes(&attr, tf32x3::tf32x3_gemm_kernel<TM, TA, TB, kConvNone, false, B4, PAIR>);
 }
 
 template <int TM>
@@ -270,14 +299,55 @@ cudaError_t tf32x3_preload() {
     if ((e = preload_tm<64>()) != cudaSuccess) return e;
     if ((e = preload_tm<128>()) != cudaSuccess) return e;
     if ((e = preload_tm<192>()) != cudaSuccess) return e;
+    if ((e = preload_one<192, true, true, false, true>()) != cudaSuccess) return e;
+    if ((e = preload_one<192, true, true, true, true>()) != cudaSuccess) return e;
+    if ((e = preload_one<256, true, true, false, true>()) != cudaSuccess) return e;
+    if ((e = preload_one<256, true, true, true, true>()) != cudaSuccess) return e;
     return preload_tm<256>();
+}
+
+bool tf32x3_pair_tm(int tm) { return tm == 192 || tm == 256; }
+
+int tf32x3_pair_slots() {
+    // both pair kernels hold one CTA per SM; the larger shared-memory
+    // footprint bounds how many clusters of two can be resident
+    using C = tf32x3::Cfg<256, true, false, true>;
+    auto kern = tf32x3::tf32x3_gemm_kernel<256, true, true, kConvNone, false, false, true>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2);
+    cfg.blockDim = dim3(tf32x3::Roles<256, true, true>::kThreads);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return n;
 }
 
 bool tf32x3_supported_tm(int tm) {
     return tm == 16 || tm == 32 || tm == 64 || tm == 128 || tm == 192 || tm == 256;
 }
 
-int tf32x3_stages(int tm) {
+int tf32x3_stages(int tm, bool pair) {
+    if (pair) {
+        switch (tm) {
+            case 192: return tf32x3::Cfg<192, true, false, true>::kStages;
+            case 256: return tf32x3::Cfg<256, true, false, true>::kStages;
+            default: return 0;
+        }
+    }
     switch (tm) {  // with B copied by TMA (the usual case)
         case 16: return tf32x3::Cfg<16, true>::kStages;
         case 32: return tf32x3::Cfg<32, true>::kStages;

@@ -134,14 +134,19 @@ constexpr int kB4SlabBytes = 4 * kB4ClassBytes;
 // TM = C rows per tile (MMA N).  TMA_B: each stage also has a slab for the
 // raw B tile (16 k rows x 128 n, copied by TMA) that the producers read and
 // split; B4: that slab holds the four residue classes of an unaligned B.
+// PAIR: the tile is shared by the two CTAs of a cluster (one cta_group::2
+// MMA of M = 256: 128 C columns per CTA); each CTA holds TM / 2 of the A
+// tile's rows (the MMA's N rows are split between the pair).
 // Shared memory: the stages' A tiles (hi, lo), then the stages' B slabs,
 // then the epilogue's C buffers and the barriers.
-template <int TM, bool TMA_B = false, bool B4 = false>
+template <int TM, bool TMA_B = false, bool B4 = false, bool PAIR = false>
 struct Cfg {
     static_assert(TM % 16 == 0 && TM >= 16 && TM <= 256, "MMA N for M=128 must be 16..256, step 16");
     static_assert(TMA_B || !B4, "the residue-class form is a TMA form");
+    static_assert(!PAIR || TM == 192 || TM == 256, "CTA pairs for tiles of 192 or 256 rows");
     static constexpr int kNacc = nacc_for(TM);
-    static constexpr int kABytes = TM * kBK * 4;  // A tile (MMA B operand), one of hi / lo
+    static constexpr int kAR = PAIR ? TM / 2 : TM;  // A rows held by this CTA
+    static constexpr int kABytes = kAR * kBK * 4;  // A tile (MMA B operand), one of hi / lo
     static constexpr int kOffAHi = 0;             // also where TMA lands the raw A tile
     static constexpr int kOffALo = kABytes;
     static constexpr int kAStageBytes = 2 * kABytes;
@@ -164,9 +169,10 @@ struct Cfg {
     static constexpr int kRingCol = kNacc * kAccCols;
     static_assert(kRingCol + kStages * kRingColsPerStage <= static_cast<int>(kTmemCols), "tensor memory");
     static constexpr int kChunk = 16;  // accumulator columns per tensor-memory load in the epilogue
-    static constexpr uint32_t kIdesc = umma_idesc_tf32(kTileN, TM);
+    static constexpr uint32_t kIdesc = umma_idesc_tf32(PAIR ? 2 * kTileN : kTileN, TM);
     static constexpr uint32_t kIdescPair = umma_idesc_tf32(kTileN, 2 * TM);  // N = 2TM: [A_hi; A_lo]
     static_assert(!kPaired || (kABytes % 512 == 0 && 2 * TM <= 256), "[A_hi; A_lo] as one swizzled operand");
+    static_assert(!(PAIR && kPaired), "paired products are a single-CTA form");
     // barriers: full[S], empty[S], a_full[S], acc_full[2], acc_empty[2],
     // drain, c_full[kEpiBufs]; then words: tensor-memory address, abort
     // flag, (unused), count of deferred sums, and kMaxDefer entries (tile row,
@@ -356,10 +362,12 @@ __device__ __forceinline__ void split_store4(uint32_t hi_addr, uint32_t lo_addr,
 // B4: the slab holds the residue classes of an unaligned B (kB4Row floats
 // per row); b_offs packs o_r, the leading floats of class r's rows, in bits
 // 2r..2r+1.
-template <int TM, bool TMA_B, int KB, int BtK, int GT, int AJ, int AJ_TMA, bool TRANS_B = false, bool B4 = false>
+template <int TM, bool TMA_B, int KB, int BtK, int GT, int AJ, int AJ_TMA, bool TRANS_B = false, bool B4 = false,
+          bool PAIR = false>
 __device__ __forceinline__ void store_split(uint32_t stage, uint32_t slab, uint32_t ring_taddr, int ptid,
                                             const Raw<BtK, AJ> &raw, uint32_t b_offs = 0) {
-    using C = Cfg<TM, TMA_B, B4>;
+    using C = Cfg<TM, TMA_B, B4, PAIR>;
+    static_assert(!PAIR || AJ == 0, "a CTA pair copies A by TMA");
     {
         // KB k values of this thread's B^T column: from registers, or from the
         // raw B tile (k rows of 128 floats) that TMA copied into the slab
@@ -421,7 +429,7 @@ __device__ __forceinline__ void store_split(uint32_t stage, uint32_t slab, uint3
 #pragma unroll
         for (int r = 0; r < AJ_TMA; ++r) {
             const int j = ptid + r * GT;
-            if (j < TM * 4) {
+            if (j < C::kAR * 4) {
                 const uint32_t off = sw64_off(j >> 2, j & 3);
                 // the raw tile stays in place as hi; only lo is written
                 const float4 v = lds128(stage + C::kOffAHi + off);
@@ -703,16 +711,23 @@ __device__ __forceinline__ void prefetch_c_tile(const GemmArgs &g, int bi, int m
 // B4: B's rows are not 16-byte aligned; tmap_b, tmap_b1, tmap_b2, tmap_b3
 // describe its residue classes k % 4 = 0..3 (each N + o_r floats wide, box
 // 132 x 4, no swizzle) and b_offs packs the o_r; needs TMA_B.
-template <int TM, bool TMA_A, bool TMA_B, int CONV = kConvNone, bool TRANS_B = false, bool B4 = false>
+// PAIR: launched in clusters of two CTAs that share each 256-column tile
+// (sch.pair_shift = 1): CTA r of the pair owns columns 128 r .. 128 r + 127
+// of the tile (its B^T slab, its tensor-memory lanes, its C stores) and
+// rows kAR r .. kAR r + kAR - 1 of the A tile (tmap_a's box is kAR rows);
+// the even CTA's MMA thread issues the pair's MMAs.  Needs TMA_A and TMA_B.
+template <int TM, bool TMA_A, bool TMA_B, int CONV = kConvNone, bool TRANS_B = false, bool B4 = false,
+          bool PAIR = false>
 __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
     tf32x3_gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ Schedule sch,
                        const __grid_constant__ DeviceCtl ctl, int vec_a, int tma_c, uint32_t b_offs,
                        const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                        const __grid_constant__ CUtensorMap tmap_c, const __grid_constant__ CUtensorMap tmap_b1,
                        const __grid_constant__ CUtensorMap tmap_b2, const __grid_constant__ CUtensorMap tmap_b3) {
-    using C = Cfg<TM, TMA_B, B4>;
+    using C = Cfg<TM, TMA_B, B4, PAIR>;
     using R = Roles<TM, TMA_A, TMA_B>;
     static_assert(CONV == kConvNone || !TMA_B, "a convolution gathers B in the producers");
+    static_assert(!PAIR || (TMA_A && TMA_B && CONV == kConvNone), "a CTA pair copies A and B by TMA");
     static_assert(!TRANS_B || (TMA_B && CONV == kConvNone), "a transposed B comes by TMA");
     static_assert(!B4 || (TMA_B && !TRANS_B && CONV == kConvNone), "residue classes of a row-major B");
     constexpr int S = C::kStages;
@@ -748,17 +763,26 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    // CTA pair: this CTA's rank, the pair's index among the walkers of the
+    // schedule, and the column tile (of 128) this CTA owns in a unit's tile
+    const int rank = PAIR ? static_cast<int>(cluster_ctarank()) : 0;
+    const int walker = PAIR ? static_cast<int>(blockIdx.x) >> 1 : static_cast<int>(blockIdx.x);
+    auto col_tile = [&](int nt) { return PAIR ? 2 * nt + rank : nt; };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            mbar_init(bars + 8u * s, R::kGroupThreads);  // full: every thread of the filling group
+            // full: every thread of the filling group; of a pair, one arrive
+            // per warp of each CTA's group (on the even CTA's barrier)
+            mbar_init(bars + 8u * s, PAIR ? 2 * R::kWarpsPerGroup : R::kGroupThreads);
             mbar_init(bars + 8u * (S + s), 1);       // empty: one tcgen05.commit
             mbar_init(afull0 + 8u * s, 1);           // a_full: the TMA thread's expect_tx arrive
         }
         mbar_init(acc_full0, 1);
         mbar_init(acc_full0 + 8u, 1);
-        mbar_init(acc_empty0, kEpiWarps * 32);
-        mbar_init(acc_empty0 + 8u, kEpiWarps * 32);
+        // acc_empty: every epilogue thread; of a pair, one arrive per
+        // epilogue warp of each CTA
+        mbar_init(acc_empty0, PAIR ? 2 * kEpiWarps : kEpiWarps * 32);
+        mbar_init(acc_empty0 + 8u, PAIR ? 2 * kEpiWarps : kEpiWarps * 32);
         mbar_init(drain_bar, 1);
         for (int b = 0; b < kEpiBufs; ++b) mbar_init(cfull0 + 8u * b, 1);
         *abort_flag = 0;
@@ -766,13 +790,33 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
         fence_mbar_init();
     }
     if (warp == R::kMmaWarp) {
-        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
-        tmem_relinquish();
+        if constexpr (PAIR) {
+            tmem_alloc2(smem_u32(tmem_slot), kTmemCols);  // collective over the pair
+            tmem_relinquish2();
+        } else {
+            tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+            tmem_relinquish();
+        }
     }
     tc_fence_before();
     __syncthreads();
+    // a pair: the other CTA's barriers are initialised before any arrive on them
+    if constexpr (PAIR) cluster_sync();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // of a pair, the even CTA's barriers that both CTAs arrive on
+    const uint32_t lead_full0 = PAIR ? mapa_shared(bars, 0) : bars;
+    const uint32_t lead_acc_empty0 = PAIR ? mapa_shared(acc_empty0, 0) : acc_empty0;
+    // this warp has read the accumulator `acc` out: free it for the MMA
+    auto release_acc = [&](int acc) {
+        tc_fence_before();
+        if constexpr (PAIR) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(lead_acc_empty0 + 8u * acc);
+        } else {
+            mbar_arrive(acc_empty0 + 8u * acc);
+        }
+    };
     // Everything above is on chip.  Launched after another kernel of this
     // library, that kernel may still be running: wait for it here, before
     // any global memory is read or written, then let the next one start.
@@ -786,11 +830,12 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
         uint32_t cpar = 0;      // per C buffer: parity of its next c_full phase
         uint32_t inflight = 0;  // per C buffer: a TMA copy into it not yet waited for
         UnitIter ui;
-        for (ui.start(sch, blockIdx.x); ui.ok; ui.next(sch), ++it) {
+        for (ui.start(sch, walker); ui.ok; ui.next(sch), ++it) {
             const UnitCoord &c = ui.c;
             const int acc = it % C::kNacc;
             const uint32_t aph = (it / C::kNacc) & 1;
-            if (c.nseg == 1 && g.beta != 0.f) prefetch_c_tile<TM>(g, c.b, c.mt * TM, c.nt * kTileN, threadIdx.x);
+            const int ct = col_tile(c.nt);  // this CTA's column tile
+            if (c.nseg == 1 && g.beta != 0.f) prefetch_c_tile<TM>(g, c.b, c.mt * TM, ct * kTileN, threadIdx.x);
             if (c.nseg == 1 && tma_c) {
                 // the previous tile's stores have read their buffers; copy the
                 // first C chunks of this tile while the accumulator is computed
@@ -802,7 +847,7 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
                     for (int ch = 0; ch < kEpiBufs - 1 && ch < nch; ++ch) {
                         if (threadIdx.x == 0) {
                             mbar_arrive_expect_tx(cfull0 + 8u * ch, kEpiChunkBytes);
-                            tma_load_3d(epi_buf0 + ch * kEpiChunkBytes, &tmap_c, c.nt * kTileN, c.mt * TM + ch * CH,
+                            tma_load_3d(epi_buf0 + ch * kEpiChunkBytes, &tmap_c, ct * kTileN, c.mt * TM + ch * CH,
                                         c.b, cfull0 + 8u * ch);
                         }
                         inflight |= 1u << ch;
@@ -813,7 +858,7 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
                                              kStatusTimeoutEpilogue);
             if (!epi_all(w)) break;
             tc_fence_after();
-            const int n = c.nt * kTileN + nl;
+            const int n = ct * kTileN + nl;
             const int m0 = c.mt * TM;
             const uint32_t t0 = tmem_base + (static_cast<uint32_t>(warp * 32) << 16) +
                                 static_cast<uint32_t>(acc * C::kAccCols);
@@ -826,7 +871,7 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
                 static_assert(CH == kEpiRows, "one C chunk per tensor-memory load");
                 const bool read_c = g.beta != 0.f;
                 const bool n_ok = n < g.N;
-                const int n0 = c.nt * kTileN;
+                const int n0 = ct * kTileN;
                 const int nch = min(TM / CH, (g.M - m0 + CH - 1) / CH);  // chunks with rows below M
                 bool ok = true;
 #pragma unroll 1
@@ -880,8 +925,7 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
                     }
                 }
                 if (!ok) break;
-                tc_fence_before();
-                mbar_arrive(acc_empty0 + 8u * acc);
+                release_acc(acc);
             } else if (c.nseg == 1) {
                 // Chunks of CH accumulator columns (C rows): each chunk's C
                 // loads are issued before its tensor-memory load and are in
@@ -925,18 +969,21 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
                         }
                     }
                 }
-                tc_fence_before();
-                mbar_arrive(acc_empty0 + 8u * acc);
+                release_acc(acc);
             } else if (ctl.ws == nullptr || ctl.counters == nullptr) {
                 // a shared tile without a workspace: report, never dereference
-                tc_fence_before();
-                mbar_arrive(acc_empty0 + 8u * acc);
+                release_acc(acc);
                 if (threadIdx.x == 0) atomicOr(ctl.status, kStatusNoWorkspace);
             } else {
                 // shared tile: write this unit's partial tile, then the last
-                // unit to arrive adds all partials in segment order
+                // unit to arrive adds all partials in segment order.  Of a
+                // pair, each CTA's half of the tile counts and sums on its
+                // own: the tile's 2 nseg slots from 2 slot0 hold half r's
+                // segments at 2 slot0 + r nseg, its counter is 2 tile + r.
                 constexpr int kTileElems = kTileN * TM;
-                float *wt = ctl.ws + (c.slot0 + c.seg) * kTileElems;
+                const long long slot_first = PAIR ? 2 * c.slot0 + rank * c.nseg : c.slot0;
+                const int counter = PAIR ? 2 * c.tile + rank : c.tile;
+                float *wt = ctl.ws + (slot_first + c.seg) * kTileElems;
 #pragma unroll 1
                 for (int ch = 0; ch < TM / CH; ++ch) {
                     float v[CH];
@@ -945,24 +992,23 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
                     for (int j = 0; j < CH; ++j)
                         if (SG_IN_WS(ctl, wt + (ch * CH + j) * kTileN + nl, 1)) __stcg(wt + (ch * CH + j) * kTileN + nl, v[j]);
                 }
-                tc_fence_before();
-                mbar_arrive(acc_empty0 + 8u * acc);
+                release_acc(acc);
                 __threadfence();
                 named_bar_sync(kEpiBarrierId, kEpiWarps * 32);
                 if (threadIdx.x == 0) {
                     // the last unit to arrive queues the tile's sum for the
                     // CTA's exit, where every warp of the CTA is free for it
-                    const bool cnt_ok = !kDebugBounds || (c.tile >= 0 && c.tile < ctl.n_counters);
+                    const bool cnt_ok = !kDebugBounds || (counter >= 0 && counter < ctl.n_counters);
                     if (!cnt_ok) atomicOr(ctl.status, kStatusOutOfBounds);
-                    const int prev = cnt_ok ? atomicAdd(ctl.counters + c.tile, 1) : -1;
+                    const int prev = cnt_ok ? atomicAdd(ctl.counters + counter, 1) : -1;
                     if (prev == c.nseg - 1) {
-                        ctl.counters[c.tile] = 0;
+                        ctl.counters[counter] = 0;
                         const int nd = *s_ndefer;
                         if (nd < kMaxDefer) {
                             s_defer[5 * nd + 0] = c.mt;
-                            s_defer[5 * nd + 1] = c.nt;
+                            s_defer[5 * nd + 1] = ct;
                             s_defer[5 * nd + 2] = c.nseg;
-                            s_defer[5 * nd + 3] = static_cast<int>(c.slot0);
+                            s_defer[5 * nd + 3] = static_cast<int>(slot_first);
                             s_defer[5 * nd + 4] = c.b;
                             *s_ndefer = nd + 1;
                         } else {
@@ -991,7 +1037,7 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
         constexpr int GT = R::kGroupThreads;
         constexpr int KB = R::kBtK;                  // B^T k values per thread and job
         constexpr int BtK = TMA_B ? 0 : KB;          // ... held in registers
-        constexpr int AJ_ALL = (TM * 4 + GT - 1) / GT;
+        constexpr int AJ_ALL = (C::kAR * 4 + GT - 1) / GT;
         constexpr int AJ = TMA_A ? 0 : AJ_ALL;
         constexpr int NB = R::kPrefetch;
         const int group = (warp - kEpiWarps) / R::kWarpsPerGroup;
@@ -999,7 +1045,7 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
         int s = group;  // stage of the group's current job (q % S, with G <= S)
         uint32_t ph = 0;
         JobIter next;
-        next.start(sch, blockIdx.x);
+        next.start(sch, walker);
         for (int i = 0; i < group && next.valid(sch); ++i) next.advance(sch);
         Raw<BtK, AJ> buf[NB];
         int loaded = 0, done = 0;
@@ -1031,15 +1077,24 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    store_split<TM, TMA_B, KB, BtK, GT, AJ, AJ_ALL, TRANS_B, B4>(
+                    store_split<TM, TMA_B, KB, BtK, GT, AJ, AJ_ALL, TRANS_B, B4, PAIR>(
                         base + s * C::kAStageBytes, base + C::kOffBRegion + s * C::kBRawBytes,
                         ring_lane + static_cast<uint32_t>(s * kRingColsPerStage), gt, buf[i], b_offs);
+                    // the lo tile was written to this CTA's own shared memory:
+                    // the proxy fence orders it for the tensor core (of a pair,
+                    // also for the even CTA's MMA, which reads it here)
                     fence_proxy_async_smem();
                     tmem_st_wait();
                     tc_fence_before();
                     const bool withhold =
                         done == 0 && group == 0 && gt == 0 && (ctl.debug_flags & kDebugWithholdArrive);
-                    if (!withhold) mbar_arrive(bars + 8u * s);
+                    if constexpr (PAIR) {
+                        // one arrive per warp, on the even CTA's barrier
+                        __syncwarp();
+                        if (lane == 0 && !withhold) mbar_arrive_cluster(lead_full0 + 8u * s);
+                    } else {
+                        if (!withhold) mbar_arrive(bars + 8u * s);
+                    }
                     ++done;
                     s += G;
                     if (s >= S) {
@@ -1066,32 +1121,32 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
                 prefetch_tmap(&tmap_b3);
             }
             constexpr uint32_t kTx =
-                (TMA_A ? TM * kBK * 4 : 0) + (TMA_B ? (B4 ? kBK * kB4RowBytes : kBK * kTileN * 4) : 0);
+                (TMA_A ? C::kAR * kBK * 4 : 0) + (TMA_B ? (B4 ? kBK * kB4RowBytes : kBK * kTileN * 4) : 0);
             int s = 0;
             uint32_t ph = 0;
             uint32_t used = 0, last_ph = 0;  // per stage: copy issued / its phase parity
             JobIter it;
-            it.start(sch, blockIdx.x);
+            it.start(sch, walker);
             while (it.valid(sch)) {
                 if (!mbar_wait_bounded(bars + 8u * (S + s), ph ^ 1u, abort_flag, ctl, kStatusTimeoutProducer))
                     break;
                 mbar_arrive_expect_tx(afull0 + 8u * s, kTx);
                 const uint32_t slab = base + C::kOffBRegion + s * C::kBRawBytes;
+                const int bn = col_tile(it.nt) * kTileN;  // this CTA's first B column
                 if (TMA_A)
-                    tma_load_3d(base + s * C::kAStageBytes + C::kOffAHi, &tmap_a, it.kt * kBK, it.mt * TM,
-                                g.sA != 0 ? it.b : 0,
-                                afull0 + 8u * s);
+                    tma_load_3d(base + s * C::kAStageBytes + C::kOffAHi, &tmap_a, it.kt * kBK,
+                                it.mt * TM + rank * C::kAR, g.sA != 0 ? it.b : 0, afull0 + 8u * s);
                 if (TMA_B && TRANS_B) {
-                    tma_load_3d(slab, &tmap_b, it.kt * kBK, it.nt * kTileN, g.sB != 0 ? it.b : 0, afull0 + 8u * s);
+                    tma_load_3d(slab, &tmap_b, it.kt * kBK, bn, g.sB != 0 ? it.b : 0, afull0 + 8u * s);
                 } else if (TMA_B && B4) {
                     // rows k0 + 4i + r of the stage (i < 4) are rows 4 kt + i of class r
                     const CUtensorMap *maps[4] = {&tmap_b, &tmap_b1, &tmap_b2, &tmap_b3};
 #pragma unroll
                     for (int r = 0; r < 4; ++r)
-                        tma_load_3d(slab + r * kB4ClassBytes, maps[r], it.nt * kTileN, it.kt * (kBK / 4),
+                        tma_load_3d(slab + r * kB4ClassBytes, maps[r], bn, it.kt * (kBK / 4),
                                     g.sB != 0 ? it.b : 0, afull0 + 8u * s);
                 } else if (TMA_B) {
-                    tma_load_3d(slab, &tmap_b, it.nt * kTileN, it.kt * kBK, g.sB != 0 ? it.b : 0, afull0 + 8u * s);
+                    tma_load_3d(slab, &tmap_b, bn, it.kt * kBK, g.sB != 0 ? it.b : 0, afull0 + 8u * s);
                 }
                 used |= 1u << s;
                 last_ph = (last_ph & ~(1u << s)) | (ph << s);
@@ -1109,65 +1164,89 @@ __global__ void __launch_bounds__(Roles<TM, TMA_A, TMA_B>::kThreads, 1)
         }
     } else if (warp == R::kMmaWarp && lane == 0) {
         // ------------------------------------------------------ MMA issuer
-        int s = 0;
-        uint32_t ph = 0;
-        int it = 0;
-        bool ok = true;
-        UnitIter ui;
-        for (ui.start(sch, blockIdx.x); ui.ok && ok; ui.next(sch), ++it) {
-            const UnitCoord &c = ui.c;
-            const int acc = it % C::kNacc;
-            const uint32_t aph = (it / C::kNacc) & 1;
-            if (!mbar_wait_bounded(acc_empty0 + 8u * acc, aph ^ 1u, abort_flag, ctl, kStatusTimeoutMma)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            const uint32_t d = tmem_base + static_cast<uint32_t>(acc * C::kAccCols);
-            for (int kt = c.kb; kt < c.ke; ++kt) {
-                if (!mbar_wait_bounded(bars + 8u * s, ph, abort_flag, ctl, kStatusTimeoutMma)) {
+        // Of a pair, the even CTA's thread issues the pair's MMAs and its
+        // commits arrive on the barriers of both CTAs; the odd CTA's thread
+        // only waits for the drain.
+        if (!PAIR || rank == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            int it = 0;
+            bool ok = true;
+            auto commit = [&](uint32_t bar) {
+                if constexpr (PAIR) mma_commit2(bar, 3);
+                else mma_commit(bar);
+            };
+            auto mma = [&](uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t accumulate) {
+                if constexpr (PAIR) mma_tf32_ts2(d, a, b, idesc, accumulate);
+                else mma_tf32_ts(d, a, b, idesc, accumulate);
+            };
+            UnitIter ui;
+            for (ui.start(sch, walker); ui.ok && ok; ui.next(sch), ++it) {
+                const UnitCoord &c = ui.c;
+                const int acc = it % C::kNacc;
+                const uint32_t aph = (it / C::kNacc) & 1;
+                if (!mbar_wait_bounded<PAIR>(acc_empty0 + 8u * acc, aph ^ 1u, abort_flag, ctl, kStatusTimeoutMma)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t st = base + s * C::kAStageBytes;
-                const uint32_t ring = tmem_base + static_cast<uint32_t>(C::kRingCol + s * kRingColsPerStage);
+                const uint32_t d = tmem_base + static_cast<uint32_t>(acc * C::kAccCols);
+                for (int kt = c.kb; kt < c.ke; ++kt) {
+                    if (!mbar_wait_bounded<PAIR>(bars + 8u * s, ph, abort_flag, ctl, kStatusTimeoutMma)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t st = base + s * C::kAStageBytes;
+                    const uint32_t ring = tmem_base + static_cast<uint32_t>(C::kRingCol + s * kRingColsPerStage);
 #pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    const uint32_t a_hi = ring + static_cast<uint32_t>(j * 8);
-                    const uint32_t a_lo = a_hi + static_cast<uint32_t>(kBK);
-                    const uint64_t b_hi = umma_desc_kmajor_sw64(st + C::kOffAHi + j * 32);
-                    if constexpr (C::kPaired) {
-                        // b_hi spans A_hi then A_lo: 2TM rows at the same pitch
-                        mma_tf32_ts(d, a_hi, b_hi, C::kIdescPair, (kt != c.kb || j != 0) ? 1u : 0u);
-                        mma_tf32_ts(d, a_lo, b_hi, C::kIdesc, 1u);
-                    } else {
-                        const uint64_t b_lo = umma_desc_kmajor_sw64(st + C::kOffALo + j * 32);
-                        mma_tf32_ts(d, a_lo, b_hi, C::kIdesc, (kt != c.kb || j != 0) ? 1u : 0u);
-                        mma_tf32_ts(d, a_hi, b_lo, C::kIdesc, 1u);
-                        mma_tf32_ts(d, a_hi, b_hi, C::kIdesc, 1u);
+                    for (int j = 0; j < 2; ++j) {
+                        const uint32_t a_hi = ring + static_cast<uint32_t>(j * 8);
+                        const uint32_t a_lo = a_hi + static_cast<uint32_t>(kBK);
+                        const uint64_t b_hi = umma_desc_kmajor_sw64(st + C::kOffAHi + j * 32);
+                        if constexpr (C::kPaired) {
+                            // b_hi spans A_hi then A_lo: 2TM rows at the same pitch
+                            mma(d, a_hi, b_hi, C::kIdescPair, (kt != c.kb || j != 0) ? 1u : 0u);
+                            mma(d, a_lo, b_hi, C::kIdesc, 1u);
+                        } else {
+                            const uint64_t b_lo = umma_desc_kmajor_sw64(st + C::kOffALo + j * 32);
+                            mma(d, a_lo, b_hi, C::kIdesc, (kt != c.kb || j != 0) ? 1u : 0u);
+                            mma(d, a_hi, b_lo, C::kIdesc, 1u);
+                            mma(d, a_hi, b_hi, C::kIdesc, 1u);
+                        }
+                    }
+                    commit(bars + 8u * (S + s));
+                    if (++s == S) {
+                        s = 0;
+                        ph ^= 1u;
                     }
                 }
-                mma_commit(bars + 8u * (S + s));
-                if (++s == S) {
-                    s = 0;
-                    ph ^= 1u;
-                }
+                if (!ok) break;
+                commit(acc_full0 + 8u * acc);
             }
-            if (!ok) break;
-            mma_commit(acc_full0 + 8u * acc);
+            // every MMA this thread issued has finished once the drain arrives
+            commit(drain_bar);
         }
-        // every MMA this thread issued has finished once the drain arrives
-        mma_commit(drain_bar);
         volatile int no_abort = 0;
         mbar_wait_bounded(drain_bar, 0u, &no_abort, ctl, kStatusTimeoutDrain);
     }
 
     tc_fence_before();
     __syncthreads();
-    if (warp == R::kMmaWarp) {
-        tc_fence_after();
-        tmem_dealloc(tmem_base, kTmemCols);
+    if constexpr (PAIR) {
+        // both CTAs are done with the pair's tensor memory, shared memory and
+        // barriers; the allocation is released by the pair together
+        cluster_sync();
+        if (warp == R::kMmaWarp) {
+            tc_fence_after();
+            tmem_dealloc2(tmem_base, kTmemCols);
+        }
+        cluster_sync();
+    } else {
+        if (warp == R::kMmaWarp) {
+            tc_fence_after();
+            tmem_dealloc(tmem_base, kTmemCols);
+        }
     }
     // deferred sums of shared tiles, by every warp of the CTA
     const int nd = *s_ndefer;

@@ -96,6 +96,18 @@ typedef struct CUstream_st *sgemm_stream_t;
  * bytes).  With the flag the kernel loads such a B itself.  Both give the
  * same bits. */
 #define SGEMM_FLAG_B_ROWS_LOADED (1 << 17)
+/* CTA pairs (3xTF32 path): clusters of two CTAs on neighbouring SMs share
+ * one tensor-core MMA (tcgen05 cta_group::2) over a tile of 256 columns,
+ * each CTA holding half of the tile's A rows (half the shared-memory traffic
+ * and producer work per MMA, deeper pipelines).  They need A's rows 16-byte
+ * aligned and B copied by TMA (its rows aligned, or as residue classes).
+ * The planner runs tiles of 256 rows on pairs; tiles of 192 rows only with
+ * SGEMM_FLAG_PAIRS.  Whole tiles give the same bits either way; tiles split
+ * along K may differ in rounding (their K slices can differ).
+ * SGEMM_FLAG_PAIRS: pairs for tiles of 192 or 256 rows whenever possible.
+ * SGEMM_FLAG_NO_PAIRS: never pairs (wins over SGEMM_FLAG_PAIRS). */
+#define SGEMM_FLAG_PAIRS (1 << 18)
+#define SGEMM_FLAG_NO_PAIRS (1 << 19)
 #define SGEMM_FLAG_DEBUG_WITHHOLD_ARRIVE 1 /* test only: one pipeline arrive
                                               is withheld and the on-device
                                               wait budget is cut to ~1 ms, so
@@ -200,6 +212,8 @@ int sgemm_host(int M, int N, int K, float alpha,
  *   [10] leftover tiles split along K after the whole waves (0 = none)
  *   [11] 1 for the FFMA path's wide-N kernel (M <= 32, K <= 64: A resident
  *        in shared memory, B streamed, persistent CTAs), else 0
+ *   [12] 1 when the tiles run on CTA pairs (SGEMM_FLAG_PAIRS; tile columns
+ *        then 256, grid = 2 x pairs), else 0
  * Returns 0, or -i for an invalid argument (the i-th argument of this
  * function, 1-based).
  */

@@ -96,9 +96,37 @@ def plan(M, N, K, **kw):
 def test_plan_large_square_uses_tensor_path_without_split():
     p = plan(5120, 5120, 5120)
     assert p["path"] == pkg.SGEMM_ALGO_TF32X3
-    assert (p["tile_m"], p["tile_n"]) == (256, 128)
-    assert p["splits"] == 1 and p["units"] == 20 * 40 and p["grid"] == SMS
+    # 256-row tiles run on CTA pairs: 256 x 256 tiles, two CTAs each
+    assert (p["tile_m"], p["tile_n"], p["pairs"]) == (256, 256, 1)
+    assert p["splits"] == 1 and p["units"] == 20 * 20 and p["grid"] == SMS
     assert p["vec_a"] == 1 and p["vec_b"] == 1
+    q = plan(5120, 5120, 5120, flags=pkg.SGEMM_FLAG_NO_PAIRS)
+    assert (q["tile_m"], q["tile_n"], q["pairs"]) == (256, 128, 0)
+    assert q["units"] == 20 * 40 and q["grid"] == SMS
+
+
+def test_plan_cta_pairs():
+    """When the planner runs tiles on CTA pairs: 256-row tiles by default,
+    192-row tiles only with SGEMM_FLAG_PAIRS, never with SGEMM_FLAG_NO_PAIRS
+    or when an operand cannot come by TMA (A rows not 16-byte aligned; a B
+    whose start is misaligned or whose residue classes are turned off)."""
+    P, NP = pkg.SGEMM_FLAG_PAIRS, pkg.SGEMM_FLAG_NO_PAIRS
+    assert plan(256, 43264, 1152)["pairs"] == 1
+    assert plan(384, 14161, 1152)["pairs"] == 0  # 192-row tiles
+    p = plan(384, 14161, 1152, flags=P)
+    assert (p["pairs"], p["tile_m"], p["tile_n"]) == (1, 192, 256)
+    assert plan(384, 14161, 1152, flags=P | NP)["pairs"] == 0
+    assert plan(1024, 1024, 1024, flags=P)["pairs"] == 0  # 128-row tiles have no pair form
+    # unaligned A rows: no TMA for A, no pairs
+    assert pkg.sgemm_plan_info(5120, 5120, 5121, A=0x100000, B=0x200000, C=0x300000, num_sms=SMS)["pairs"] == 0
+    # unaligned B rows with an aligned start come by TMA as residue classes
+    q = pkg.sgemm_plan_info(5120, 5121, 5120, A=0x100000, B=0x200000, C=0x300000, num_sms=SMS)
+    assert q["pairs"] == 1 and q["vec_b"] == 0
+    assert pkg.sgemm_plan_info(5120, 5121, 5120, A=0x100000, B=0x200004, C=0x300000, num_sms=SMS)["pairs"] == 0
+    assert pkg.sgemm_plan_info(5120, 5121, 5120, A=0x100000, B=0x200000, C=0x300000, num_sms=SMS,
+                               flags=pkg.SGEMM_FLAG_B_ROWS_LOADED)["pairs"] == 0
+    # the FFMA path never pairs
+    assert plan(5120, 5120, 5120, algo=pkg.SGEMM_ALGO_FFMA)["pairs"] == 0
 
 
 def test_plan_small_square_splits_k():
@@ -154,28 +182,29 @@ def test_plan_ffma_tiles():
 
 def test_plan_split_tail():
     """Tiles beyond many whole waves: the whole waves keep whole tiles, the
-    leftover tiles are cut into K slices over the otherwise idle SMs."""
-    p = plan(8192, 8192, 8192)          # 2048 tiles = 13 waves of 152 + 72
+    leftover tiles are cut into K slices over the otherwise idle SMs (single
+    CTAs here; CTA pairs: test_plan_cta_pairs)."""
+    p = plan(8192, 8192, 8192, flags=pkg.SGEMM_FLAG_NO_PAIRS)  # 2048 tiles = 13 waves of 152 + 72
     assert p["tail_tiles"] == 72 and p["grid"] == SMS
     assert p["ws_bytes"] == 72 * (SMS // 72) * 256 * 128 * 4
-    q = plan(8192, 8192, 8192, flags=pkg.SGEMM_FLAG_WHOLE_TILES)
+    q = plan(8192, 8192, 8192, flags=pkg.SGEMM_FLAG_WHOLE_TILES | pkg.SGEMM_FLAG_NO_PAIRS)
     assert q["tail_tiles"] == 0 and q["ws_bytes"] == 0
-    p5 = plan(5120, 5120, 5120)                          # 800 tiles = 5 waves + 40
+    p5 = plan(5120, 5120, 5120, flags=pkg.SGEMM_FLAG_NO_PAIRS)  # 800 tiles = 5 waves + 40
     assert p5["tail_tiles"] == 40 and p5["tile_m"] == 256
     assert p5["ws_bytes"] == 40 * (SMS // 40) * 256 * 128 * 4
-    assert plan(4864, 4096, 4096)["tail_tiles"] == 0    # 19 x 32 = 608 tiles: 4 whole waves
+    assert plan(4864, 4096, 4096, flags=pkg.SGEMM_FLAG_NO_PAIRS)["tail_tiles"] == 0  # 19 x 32 = 608 tiles: 4 whole waves
     assert plan(1024, 1024, 1024)["tail_tiles"] == 0    # fewer tiles than SMs: split-K instead
-    assert plan(8192, 8192, 8192, splits=1)["tail_tiles"] == 0  # explicit split count wins
+    assert plan(8192, 8192, 8192, splits=1, flags=pkg.SGEMM_FLAG_NO_PAIRS)["tail_tiles"] == 0  # explicit split count wins
     # a forced split tail where the estimate prefers whole tiles
-    f = plan(4096, 24576, 256, flags=pkg.SGEMM_FLAG_SPLIT_TAIL)
+    f = plan(4096, 24576, 256, flags=pkg.SGEMM_FLAG_SPLIT_TAIL | pkg.SGEMM_FLAG_NO_PAIRS)
     assert f["tail_tiles"] > 0 and f["grid"] == SMS
     assert f["tail_tiles"] == (-(-4096 // f["tile_m"]) * 192) % SMS
-    assert plan(3072, 3072, 3072, flags=pkg.SGEMM_FLAG_SPLIT_TAIL)["tail_tiles"] == 0  # none possible
+    assert plan(3072, 3072, 3072, flags=pkg.SGEMM_FLAG_SPLIT_TAIL | pkg.SGEMM_FLAG_NO_PAIRS)["tail_tiles"] == 0  # none possible
 
 
 @pytest.mark.parametrize("rows", [16, 32, 64, 128, 192, 256])
 def test_plan_forced_tile_rows(rows):
-    p = plan(5120, 5120, 5120, flags=pkg.SGEMM_FLAG_TILE_ROWS(rows))
+    p = plan(5120, 5120, 5120, flags=pkg.SGEMM_FLAG_TILE_ROWS(rows) | pkg.SGEMM_FLAG_NO_PAIRS)
     assert p["tile_m"] == rows
     assert p["units"] == -(-5120 // rows) * 40
 
@@ -295,7 +324,7 @@ def _walk_units(p, M, N, K, sms):
     tm, tn = p["tile_m"], p["tile_n"]
     tiles = -(-M // tm) * -(-N // tn)
     kt = -(-K // 16)
-    grid = p["grid"]
+    grid = p["grid"] // 2 if p.get("pairs") else p["grid"]  # CTA pairs walk the units together
     per_cta = [[] for _ in range(grid)]
     if p["tail_tiles"] == 0:
         s = p["splits"]
@@ -341,17 +370,22 @@ def test_plan_schedules_cover_every_k_tile_once(sms):
         assert len(seen) == tiles * kt and set(seen.values()) == {1}, (M, N, K, kw, p)
         if p["splits"] > 1:  # every unit is a partial tile
             assert max(len(u) for u in per_cta) <= 8, (M, N, K, kw, p)
+        # walkers: CTAs, or CTA pairs (two CTAs of the grid each, sms / 2 of them)
+        pw = 2 if p["pairs"] else 1
+        walkers, slots = p["grid"] // pw, sms // pw
+        if p["pairs"]:
+            assert p["tile_m"] == 256 and p["tile_n"] == 256 and p["grid"] % 2 == 0
         if p["tail_tiles"] == 0:
             assert p["units"] == tiles * p["splits"]
             assert p["ws_bytes"] == (p["units"] * p["tile_m"] * p["tile_n"] * 4 if p["splits"] > 1 else 0)
-            assert 1 <= p["grid"] <= max(p["units"], 1)
+            assert 1 <= walkers <= max(p["units"], 1)
             if p["splits"] == 1:
-                assert p["grid"] == min(p["units"], sms)
+                assert walkers == min(p["units"], slots)
         else:
             tail = p["tail_tiles"]
             ts = p["ws_bytes"] // (tail * p["tile_m"] * p["tile_n"] * 4)
-            assert p["grid"] == sms and 0 < tail < sms and (tiles - tail) % sms == 0
-            assert ts >= 2 and tail * ts <= sms and ts <= kt
+            assert walkers == slots and 0 < tail < slots and (tiles - tail) % slots == 0
+            assert ts >= 2 and tail * ts <= slots and ts <= kt
             assert p["ws_bytes"] == tail * ts * p["tile_m"] * p["tile_n"] * 4
         checked += 1
     assert checked == len(shapes) * len(variants)

@@ -148,10 +148,11 @@ def test_tma_and_load_paths_agree_bitwise(rows):
     tensor core reads only the top 19 bits of a tf32 operand); operands the
     producers load themselves get hi with the low 13 bits cleared.  Both must
     give the same bits: aligned and misaligned copies of the same problem
-    take the two paths with the same schedule and summation order."""
+    take the two paths with the same schedule and summation order (single
+    CTAs: a CTA pair copies both operands by TMA)."""
     M, N, K = 300, 392, 700  # lda and ldb multiples of 4: offset 0 is 16-byte aligned
     p = _with_c(random_problem(M, N, K, alpha=1.0, beta=0.5, seed=rows, pad_value=0.0))
-    flags = pkg.SGEMM_FLAG_TILE_ROWS(rows) | pkg.SGEMM_FLAG_WHOLE_TILES
+    flags = pkg.SGEMM_FLAG_TILE_ROWS(rows) | pkg.SGEMM_FLAG_WHOLE_TILES | pkg.SGEMM_FLAG_NO_PAIRS
     outs = {}
     # NO_A_COPY: a misaligned A is loaded by the producers, not staged
     for off in [(0, 0, 0), (1, 0, 0), (0, 1, 0), (1, 1, 0)]:
@@ -179,7 +180,8 @@ def test_unaligned_b_rows_by_tma(case):
     p = _with_c(random_problem(M, N, K, alpha=1.25, beta=0.5, seed=M + 7 * N + K, ldb=N + pad, pad_value=np.nan))
     assert p.ldb % 4 != 0
     for sched in (pkg.SGEMM_FLAG_WHOLE_TILES, 0):
-        flags = pkg.SGEMM_FLAG_TILE_ROWS(rows) | sched
+        # single CTAs on both sides (residue classes on CTA pairs: test_cta_pairs)
+        flags = pkg.SGEMM_FLAG_TILE_ROWS(rows) | sched | pkg.SGEMM_FLAG_NO_PAIRS
         splits = 0 if sched else 3
         tma, st = run_sgemm(p, pkg.SGEMM_ALGO_TF32X3, splits=splits, flags=flags)
         assert st == 0
@@ -187,6 +189,80 @@ def test_unaligned_b_rows_by_tma(case):
         loaded, st = run_sgemm(p, pkg.SGEMM_ALGO_TF32X3, splits=splits, flags=flags | pkg.SGEMM_FLAG_B_ROWS_LOADED)
         assert st == 0
         assert np.array_equal(tma.view(np.uint32), loaded.view(np.uint32)), f"{case}: TMA and loaded B differ"
+
+
+# CTA pairs (SGEMM_FLAG_PAIRS): (M, N, K, ldb padding, tile rows).  Ragged
+# edges where one CTA of a pair has no rows of A (M below TM / 2 in the last
+# tile row) or no columns of B (N % 256 <= 128), residue-class B, a plan with
+# more tiles than pairs (whole waves plus a split tail).
+PAIR_CASES = [(256, 256, 64, 0, 256), (300, 700, 200, 0, 256), (257, 129, 33, 0, 256), (100, 120, 48, 0, 256),
+              (512, 1000, 1000, 3, 256), (400, 900, 301, 0, 192), (192, 300, 129, 1, 192), (90, 383, 70, 0, 192),
+              (1280, 4352, 256, 0, 256)]
+
+
+@pytest.mark.parametrize("case", PAIR_CASES, ids=[f"{c[0]}x{c[1]}x{c[2]}p{c[3]}t{c[4]}" for c in PAIR_CASES])
+def test_cta_pairs(case):
+    """Tiles on CTA pairs (one cta_group::2 MMA per pair, half of the A tile
+    in each CTA) against the oracle on whole tiles, the planner's split tail
+    and a forced split-K; whole tiles bit for bit the same as the single-CTA
+    kernel with the same tile height."""
+    M, N, K, pad, tm = case
+    lda = (K + 3) // 4 * 4 + 4  # the pair form copies A by TMA: 16-byte rows
+    p = _with_c(random_problem(M, N, K, alpha=0.75, beta=-0.5, seed=3 * M + N + K, lda=lda, ldb=N + pad,
+                               pad_value=np.nan))
+    base = pkg.SGEMM_FLAG_TILE_ROWS(tm) | pkg.SGEMM_FLAG_PAIRS
+    # whole tiles (splits = 1: no split-K either), the planner's schedule
+    # (split tail when there are more tiles than pairs), forced split-K
+    for sched, splits in ((pkg.SGEMM_FLAG_WHOLE_TILES, 1), (pkg.SGEMM_FLAG_SPLIT_TAIL, 0), (0, 3)):
+        flags = base | sched
+        plan = pkg.sgemm_plan_info(M, N, K, A=0, B=0, C=0, lda=p.lda, ldb=p.ldb, algo=pkg.SGEMM_ALGO_TF32X3,
+                                   splits=splits, flags=flags, beta=p.beta)
+        assert plan["pairs"] == 1 and plan["tile_n"] == 256, plan
+        got, st = run_sgemm(p, pkg.SGEMM_ALGO_TF32X3, splits=splits, flags=flags)
+        assert st == 0
+        check_against_oracle(p, got, what=f"{case} pairs, flags {flags:#x} splits {splits}")
+        if sched == pkg.SGEMM_FLAG_WHOLE_TILES:
+            single, st = run_sgemm(p, pkg.SGEMM_ALGO_TF32X3, splits=1, flags=flags & ~pkg.SGEMM_FLAG_PAIRS)
+            assert st == 0
+            diff = got.view(np.uint32) != single.view(np.uint32)
+            assert not diff.any(), (f"{case}: pair and single differ in {int(diff.sum())} elements, max "
+                                    f"{float(np.nanmax(np.abs(got - single)))}, first at "
+                                    f"{np.argwhere(diff)[:4].tolist()}")
+
+
+def test_cta_pairs_repeatable():
+    """The pair form under load, run after run: whole 256 x 256 tiles over
+    more tiles than pairs (several per pair), eight launches back to back,
+    each bit for bit the single-CTA result; then the planner's schedule
+    (split tail) twice, identical to itself and within the oracle's bound on
+    sampled rows."""
+    import torch
+    M, N, K = 2304, 4608, 1536
+    p = _with_c(random_problem(M, N, K, alpha=1.0, beta=0.5, seed=1234, pad_value=0.0))
+    A, B = torch.from_numpy(p.A).cuda(), torch.from_numpy(p.B).cuda()
+    C0 = torch.from_numpy(p.C).cuda()
+    st = torch.cuda.current_stream()
+
+    def call(flags, splits):
+        C = C0.clone()
+        assert pkg.sgemm_ex(M, N, K, p.alpha, A, p.lda, B, p.ldb, p.beta, C, p.ldc, st,
+                            pkg.SGEMM_ALGO_TF32X3, splits, flags) == 0
+        return C
+
+    whole = pkg.SGEMM_FLAG_TILE_ROWS(256) | pkg.SGEMM_FLAG_WHOLE_TILES
+    single = call(whole | pkg.SGEMM_FLAG_NO_PAIRS, 1)
+    outs = [call(whole | pkg.SGEMM_FLAG_PAIRS, 1) for _ in range(8)]
+    assert pkg.sgemm_check_status(st) == 0
+    for i, o in enumerate(outs):
+        assert torch.equal(o, single), f"launch {i}: pair result differs from the single-CTA result"
+    plan = pkg.sgemm_plan_info(M, N, K, A=A.data_ptr(), B=B.data_ptr(), C=C0.data_ptr(), algo=pkg.SGEMM_ALGO_TF32X3,
+                               beta=p.beta)
+    assert plan["pairs"] == 1
+    a, b = call(0, 0), call(0, 0)
+    assert pkg.sgemm_check_status(st) == 0
+    assert torch.equal(a, b)
+    rows = sample_rows(M, 24, seed=5)
+    check_against_oracle(p, a.cpu().numpy(), rows=rows, what="pairs, planner schedule")
 
 
 def test_unaligned_b_rows_batched_and_misaligned_start():
