@@ -303,13 +303,17 @@ void plan_pairs(int M, int N, int K, int tm, int slots, int splits_req, int flag
     }
 }
 
-// Whether a tile of tm rows runs on CTA pairs.  Measured on GB300 (TF/s,
-// single CTAs -> pairs): 5120^3 322 -> 342, 8192^3 whole tiles 340 -> 362,
-// 2048^3 237 -> 244, 256 x 43264 x 1152 208 -> 218; tiles of 192 rows
-// gained nothing (384 x 14161 x 1152: 178 both).
-bool use_pairs(int tm, int flags, int pair_slots) {
+// Whether a tile of tm rows runs on CTA pairs (splits: the single-CTA
+// plan's split-K count).  Measured on GB300 (TF/s, single CTAs -> pairs):
+// 4096^3 311 -> 330, 5120^3 321 -> 342, 8192^3 349 -> 374, 12288^3
+// 343 -> 380, 2048^3 237 -> 244, 256 x 50176 x 1024 206 -> 223.  Where the
+// single-CTA plan splits K to fill the SMs, pairs (half as many tiles) lose:
+// 1536^3 174 -> 130 (166 with the same split), 1024^3 with 256-row pair
+// tiles and 2-4 slices 57-61 against 73.  Tiles of 192 rows gained nothing
+// (384 x 14161 x 1152: 178 both).
+bool use_pairs(int tm, int splits, int flags, int pair_slots) {
     if (pair_slots <= 0 || (flags & SGEMM_FLAG_NO_PAIRS) || !sg::tf32x3_pair_tm(tm)) return false;
-    return (flags & SGEMM_FLAG_PAIRS) || tm == 256;
+    return (flags & SGEMM_FLAG_PAIRS) || (tm == 256 && splits == 1);
 }
 
 // batch > 1: one launch over the tiles of every matrix (Schedule::tpb).
@@ -320,7 +324,7 @@ void plan_tf32x3(int M, int N, int K, int sms, int splits_req, int flags, bool r
     p.path = SGEMM_ALGO_TF32X3;
     const Tf32x3Choice ch = choose_tf32x3(M, N, K, sms, forced_tile_rows(flags), splits_req, flags, read_c, batch);
     const int tm = ch.tm;
-    if (use_pairs(tm, flags, pair_slots)) {
+    if (use_pairs(tm, ch.splits, flags, pair_slots)) {
         plan_pairs(M, N, K, tm, pair_slots, splits_req, flags, p, batch);
         return;
     }

@@ -117,6 +117,10 @@ def test_plan_cta_pairs():
     assert (p["pairs"], p["tile_m"], p["tile_n"]) == (1, 192, 256)
     assert plan(384, 14161, 1152, flags=P | NP)["pairs"] == 0
     assert plan(1024, 1024, 1024, flags=P)["pairs"] == 0  # 128-row tiles have no pair form
+    # where the single-CTA plan splits K to fill the SMs, pairs (half the tiles) stay off
+    q = plan(1536, 1536, 1536)
+    assert q["pairs"] == 0 and q["splits"] > 1 and q["tile_m"] == 256
+    assert plan(1536, 1536, 1536, flags=P)["pairs"] == 1
     # unaligned A rows: no TMA for A, no pairs
     assert pkg.sgemm_plan_info(5120, 5120, 5121, A=0x100000, B=0x200000, C=0x300000, num_sms=SMS)["pairs"] == 0
     # unaligned B rows with an aligned start come by TMA as residue classes
