@@ -3,7 +3,7 @@ SGEMM_DEBUG build of the library (every computed global address of the
 kernels checked against its matrix, violations reported as
 SGEMM_ERR_OUT_OF_BOUNDS; tensor maps that could reach outside their operand
 refused) and runs parity cases that cross every tile edge, odd leading
-dimensions, misaligned pointers, the residue-class and two-CTA forms, split-K
+dimensions, misaligned pointers, the residue-class form, CTA pairs, split-K
 and split tails, the wide-N kernel, transposed operands, a strided batch,
 convolutions and sgemm_noalloc.  Each must report status 0 and match the
 float64 oracle.  Prints one line per case group; exits non-zero on failure."""
@@ -56,6 +56,13 @@ def gemm_cases():
              (64, 5000, 147, 1, 0), (32, 4100, 27, 2, pkg.SGEMM_FLAG_TILE_ROWS(32)),
              (300, 1021, 700, 0, pkg.SGEMM_FLAG_B_ROWS_LOADED), (40, 2000, 147, 0, pkg.SGEMM_FLAG_NO_A_COPY),
              (1000, 1000, 600, 0, pkg.SGEMM_FLAG_SPLIT_TAIL), (1000, 1000, 600, 0, pkg.SGEMM_FLAG_WHOLE_TILES)]
+    # CTA pairs (A rows 16-byte aligned: K a multiple of 4): whole tiles with
+    # ragged edges, residue-class B, 192-row tiles, forced split-K, and a
+    # split tail over more tiles than pairs
+    P = pkg.SGEMM_FLAG_PAIRS
+    forms += [(300, 1021, 700, 0, pkg.SGEMM_FLAG_TILE_ROWS(256) | P | pkg.SGEMM_FLAG_WHOLE_TILES),
+              (384, 1413, 300, 0, pkg.SGEMM_FLAG_TILE_ROWS(192) | P), (257, 129, 36, 3, pkg.SGEMM_FLAG_TILE_ROWS(256) | P),
+              (1280, 4352, 256, 0, pkg.SGEMM_FLAG_TILE_ROWS(256) | P | pkg.SGEMM_FLAG_SPLIT_TAIL)]
     for M, N, K, splits, flags in forms:
         p = with_c(random_problem(M, N, K, alpha=0.75, beta=0.5, seed=M * 3 + K, pad_value=0.0), 6)
         C, st = run_sgemm(p, pkg.SGEMM_ALGO_TF32X3, splits=splits, flags=flags)
