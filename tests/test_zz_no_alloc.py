@@ -74,12 +74,13 @@ def test_noalloc_matches_sgemm_ex_twice(name, splits):
 
 def test_noalloc_leaves_free_memory_unchanged():
     """After the set-up call, GEMMs of several plans (split-K, whole tiles,
-    tensor-map and element-load operands) take no device memory."""
+    tensor-map and element-load operands, CTA pairs) take no device
+    memory."""
     import torch
     st = torch.cuda.current_stream()
     cases = []
     for (M, N, K, off, splits) in [(1024, 1024, 1024, 0, 4), (333, 517, 301, 1, 2), (64, 4096, 147, 0, 1),
-                                   (512, 384, 2048, 0, 0)]:
+                                   (512, 384, 2048, 0, 0), (2560, 5120, 768, 0, 0)]:
         p = random_problem(M, N, K, alpha=1.0, beta=0.5, seed=M + N + K, pad_value=0.0)
         A = torch.zeros(p.A.size + 4, device="cuda")
         B = torch.zeros(p.B.size + 4, device="cuda")
@@ -98,6 +99,31 @@ def test_noalloc_leaves_free_memory_unchanged():
     torch.cuda.synchronize()
     free1, _ = torch.cuda.mem_get_info()
     assert free1 == free0, f"device free memory changed by {free0 - free1} bytes across sgemm_noalloc calls"
+
+
+def test_noalloc_cta_pairs():
+    """A plan on CTA pairs (256-row tiles): sgemm_noalloc matches the oracle
+    on sampled rows and gives the same bits as sgemm_ex with the same
+    schedule (whole tiles when the split tail's partial tiles would not fit
+    sgemm_noalloc's 16 MiB of scratch, which then drops the tail)."""
+    import torch
+    M, N, K = 2560, 5120, 768
+    p = random_problem(M, N, K, alpha=1.25, beta=0.5, seed=77, pad_value=0.0)
+    p.C[:, :p.N] = uniform(np.random.default_rng(78), p.M * p.N).reshape(p.M, p.N)
+    plan = pkg.sgemm_plan_info(M, N, K, algo=pkg.SGEMM_ALGO_TF32X3, beta=p.beta, num_sms=0)
+    assert plan["pairs"] == 1, plan
+    same_schedule = pkg.SGEMM_FLAG_WHOLE_TILES if plan["ws_bytes"] > (16 << 20) else 0
+    st = torch.cuda.current_stream()
+    A, B = torch.from_numpy(p.A).cuda(), torch.from_numpy(p.B).cuda()
+    C1, C2 = torch.from_numpy(p.C).cuda(), torch.from_numpy(p.C).cuda()
+    assert pkg.sgemm_noalloc(M, N, K, p.alpha, A, p.lda, B, p.ldb, p.beta, C1, p.ldc, st, 0) == 0
+    assert pkg.sgemm_ex(M, N, K, p.alpha, A, p.lda, B, p.ldb, p.beta, C2, p.ldc, st, pkg.SGEMM_ALGO_TF32X3, 0,
+                        same_schedule) == 0
+    assert pkg.sgemm_check_status(st) == 0
+    assert torch.equal(C1, C2)
+    rows = [0, 255, 256, 1000, 2047, 2559]
+    ref, scale = oracle.sgemm_ref(M, N, K, p.alpha, p.A, p.lda, p.B, p.ldb, p.beta, p.C, p.ldc, rows=rows)
+    assert not oracle.first_failures(C1.cpu().numpy()[rows, :N], ref, scale)
 
 
 def test_noalloc_timeout_is_reported_and_cleared():
