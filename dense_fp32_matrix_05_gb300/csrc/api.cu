@@ -266,11 +266,41 @@ Tf32x3Choice choose_tf32x3(int M, int N, int K, int sms, int forced_tm, int spli
     return best;
 }
 
+// Run-time model of the CTA-pair form: a 256 x 256 tile over two SMs costs
+// kPairKTile times the single-CTA 256-row tile per K tile and kPairUnitUs
+// more per unit; tiles of 256 columns are walked by `slots` pairs.  Least-
+// squares fit to GB300 kernel times of 21 shapes from 2560 x 2560 x 1024
+// to 12288^3 (each within 6 %, most within 2 %).  *tail: the split-tail
+// schedule is the faster one (K slices per leftover tile from
+// tail_splits_for).
+constexpr double kPairKTile = 0.94;
+constexpr double kPairUnitUs = 0.5;
+
+double model_pairs(int M, int N, int K, int tm, int slots, bool read_c, long long batch, int flags, bool *tail) {
+    const TileCost c = tile_cost(tm);
+    const double unit = c.per_unit + (read_c ? c.per_unit_c : 0.0) + kPairUnitUs;
+    const double per_k = c.per_k_tile * kPairKTile;
+    const long long tiles = static_cast<long long>(ceil_div(M, tm)) * ceil_div(N, 2 * sg::kTf32x3TileN) * batch;
+    const int kt = ceil_div(std::max(K, 1), sg::kTf32x3BK);
+    const double whole = kLaunchUs + static_cast<double>((tiles + slots - 1) / slots) * (kt * per_k + unit);
+    *tail = false;
+    if (flags & SGEMM_FLAG_WHOLE_TILES) return whole;
+    const int ts = tail_splits_for(tiles, kt, slots);
+    if (ts == 0) return whole;
+    const double split = kLaunchUs + static_cast<double>(tiles / slots) * (kt * per_k + unit) +
+                         ceil_div(kt, ts) * per_k + unit + kSumUsPer256Rows * (ts + 1) * tm / 256.0;
+    if (split < whole || (flags & SGEMM_FLAG_SPLIT_TAIL)) {
+        *tail = true;
+        return split;
+    }
+    return whole;
+}
+
 // A tile of 192 or 256 rows on CTA pairs (SGEMM_FLAG_PAIRS): tiles of 256
 // columns walked by `slots` pairs (the pairs resident at once), each pair
 // two CTAs of the grid.  Whole waves of tiles plus a split tail, or split-K
 // when a split count is forced.  Counters: two per tile (one per CTA half).
-void plan_pairs(int M, int N, int K, int tm, int slots, int splits_req, int flags, Plan &p, int batch) {
+void plan_pairs(int M, int N, int K, int tm, int slots, int splits_req, int flags, bool read_c, Plan &p, int batch) {
     constexpr int kPairN = 2 * sg::kTf32x3TileN;
     p.tile_m = tm;
     p.tile_n = kPairN;
@@ -292,7 +322,9 @@ void plan_pairs(int M, int N, int K, int tm, int slots, int splits_req, int flag
     p.stages = sg::tf32x3_stages(tm, true);
     const size_t tile_bytes = static_cast<size_t>(kPairN) * tm * sizeof(float);
     p.ws_bytes = s.splits > 1 ? static_cast<size_t>(s.units) * tile_bytes : 0;
-    const int ts = (s.splits == 1 && !(flags & SGEMM_FLAG_WHOLE_TILES)) ? tail_splits_for(tiles, s.k_tiles, slots) : 0;
+    bool tail = false;
+    if (s.splits == 1) model_pairs(M, N, K, tm, slots, read_c, batch, flags, &tail);
+    const int ts = tail ? tail_splits_for(tiles, s.k_tiles, slots) : 0;
     if (ts > 0) {
         const int rem = tiles % slots;
         s.dp_tiles = tiles - rem;
@@ -303,17 +335,26 @@ void plan_pairs(int M, int N, int K, int tm, int slots, int splits_req, int flag
     }
 }
 
-// Whether a tile of tm rows runs on CTA pairs (splits: the single-CTA
-// plan's split-K count).  Measured on GB300 (TF/s, single CTAs -> pairs):
-// 4096^3 311 -> 330, 5120^3 321 -> 342, 8192^3 349 -> 374, 12288^3
-// 343 -> 380, 2048^3 237 -> 244, 256 x 50176 x 1024 206 -> 223.  Where the
-// single-CTA plan splits K to fill the SMs, pairs (half as many tiles) lose:
-// 1536^3 174 -> 130 (166 with the same split), 1024^3 with 256-row pair
-// tiles and 2-4 slices 57-61 against 73.  Tiles of 192 rows gained nothing
-// (384 x 14161 x 1152: 178 both).
-bool use_pairs(int tm, int splits, int flags, int pair_slots) {
-    if (pair_slots <= 0 || (flags & SGEMM_FLAG_NO_PAIRS) || !sg::tf32x3_pair_tm(tm)) return false;
-    return (flags & SGEMM_FLAG_PAIRS) || (tm == 256 && splits == 1);
+// Whether a tile of tm rows runs on CTA pairs, given the single-CTA plan
+// (split count and estimated time).  SGEMM_FLAG_PAIRS forces them for tiles
+// of 192 or 256 rows; otherwise 256-row plans without split-K take them when
+// the model above estimates them faster.  Measured on GB300 (TF/s, single
+// CTAs -> pairs): 4096^3 311 -> 330, 5120^3 321 -> 342, 8192^3 349 -> 374,
+// 12288^3 343 -> 380, 3000^3 283 -> 302, 2304 x 2304 x 8192 297 -> 314,
+// 256 x 50176 x 1024 206 -> 223; the model keeps single CTAs where they win
+// clearly: 10000 x 600 x 3000 254 against 204 (N padded to 256-column tiles,
+// 1.6 waves).  It misjudges near-ties: 2560 x 2560 x 1024 runs on pairs at
+// 197 against 203, 512 x 20000 x 1024 at 198 against 200.
+// Where the single-CTA plan splits K to fill the SMs, pairs (half as many
+// tiles) lose: 1536^3 174 -> 130, 1024^3 57-61 against 73.  Tiles of 192
+// rows gained nothing (384 x 14161 x 1152: 178 both).
+bool use_pairs(int M, int N, int K, const Tf32x3Choice &ch, int flags, int pair_slots, bool read_c,
+               long long batch) {
+    if (pair_slots <= 0 || (flags & SGEMM_FLAG_NO_PAIRS) || !sg::tf32x3_pair_tm(ch.tm)) return false;
+    if (flags & SGEMM_FLAG_PAIRS) return true;
+    if (ch.tm != 256 || ch.splits != 1) return false;
+    bool tail = false;
+    return model_pairs(M, N, K, ch.tm, pair_slots, read_c, batch, flags, &tail) < ch.us;
 }
 
 // batch > 1: one launch over the tiles of every matrix (Schedule::tpb).
@@ -324,8 +365,8 @@ void plan_tf32x3(int M, int N, int K, int sms, int splits_req, int flags, bool r
     p.path = SGEMM_ALGO_TF32X3;
     const Tf32x3Choice ch = choose_tf32x3(M, N, K, sms, forced_tile_rows(flags), splits_req, flags, read_c, batch);
     const int tm = ch.tm;
-    if (use_pairs(tm, ch.splits, flags, pair_slots)) {
-        plan_pairs(M, N, K, tm, pair_slots, splits_req, flags, p, batch);
+    if (use_pairs(M, N, K, ch, flags, pair_slots, read_c, batch)) {
+        plan_pairs(M, N, K, tm, pair_slots, splits_req, flags, read_c, p, batch);
         return;
     }
     p.tile_m = tm;

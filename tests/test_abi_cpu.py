@@ -121,14 +121,20 @@ def test_plan_cta_pairs():
     q = plan(1536, 1536, 1536)
     assert q["pairs"] == 0 and q["splits"] > 1 and q["tile_m"] == 256
     assert plan(1536, 1536, 1536, flags=P)["pairs"] == 1
-    # unaligned A rows: no TMA for A, no pairs
-    assert pkg.sgemm_plan_info(5120, 5120, 5121, A=0x100000, B=0x200000, C=0x300000, num_sms=SMS)["pairs"] == 0
+    # the pair model keeps single CTAs where 256-column tiles waste a wave:
+    # N = 600 pads to 768 columns and 120 pair tiles fill 1.6 waves
+    assert plan(10000, 600, 3000)["pairs"] == 0
+    assert plan(10000, 600, 3000, flags=P)["pairs"] == 1
+    # unaligned A rows: no TMA for A, no pairs (not even when asked for)
+    assert pkg.sgemm_plan_info(5120, 5120, 5121, A=0x100000, B=0x200000, C=0x300000, num_sms=SMS,
+                               flags=P)["pairs"] == 0
     # unaligned B rows with an aligned start come by TMA as residue classes
-    q = pkg.sgemm_plan_info(5120, 5121, 5120, A=0x100000, B=0x200000, C=0x300000, num_sms=SMS)
+    q = pkg.sgemm_plan_info(5120, 5121, 5120, A=0x100000, B=0x200000, C=0x300000, num_sms=SMS, flags=P)
     assert q["pairs"] == 1 and q["vec_b"] == 0
-    assert pkg.sgemm_plan_info(5120, 5121, 5120, A=0x100000, B=0x200004, C=0x300000, num_sms=SMS)["pairs"] == 0
+    assert pkg.sgemm_plan_info(5120, 5121, 5120, A=0x100000, B=0x200004, C=0x300000, num_sms=SMS,
+                               flags=P)["pairs"] == 0
     assert pkg.sgemm_plan_info(5120, 5121, 5120, A=0x100000, B=0x200000, C=0x300000, num_sms=SMS,
-                               flags=pkg.SGEMM_FLAG_B_ROWS_LOADED)["pairs"] == 0
+                               flags=P | pkg.SGEMM_FLAG_B_ROWS_LOADED)["pairs"] == 0
     # the FFMA path never pairs
     assert plan(5120, 5120, 5120, algo=pkg.SGEMM_ALGO_FFMA)["pairs"] == 0
 
