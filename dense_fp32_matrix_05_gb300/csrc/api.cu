@@ -468,6 +468,14 @@ int resolve_path(int M, int K, int algo, int splits) {
 
 // batch > 1 (3xTF32 path only): matrix b of each operand starts b * stride
 // elements after the first; 16-byte copies need 16-byte strides too.
+// Whether run() copies an A whose rows are not 16-byte aligned into aligned
+// rows before the 3xTF32 kernel (then its tiles come by TMA): A far smaller
+// than B (M * 32 <= N, the im2col shapes), one matrix or one shared by the
+// batch, unless SGEMM_FLAG_NO_A_COPY.
+bool a_gets_staged(int M, int N, int flags, int batch, long long sA) {
+    return !(flags & SGEMM_FLAG_NO_A_COPY) && (batch <= 1 || sA == 0) && static_cast<long long>(M) * 32 <= N;
+}
+
 // pair_slots: CTA pairs the device holds at once (0: no pair form).
 int make_plan(int M, int N, int K, const void *A, int lda, const void *B, int ldb, const void *C, int ldc,
               int algo, int splits, int flags, int sms, bool read_c, Plan &p, int batch = 1, long long sA = 0,
@@ -480,7 +488,9 @@ int make_plan(int M, int N, int K, const void *A, int lda, const void *B, int ld
     // start with whole residue classes (K >= 4, batch stride of 4 floats)
     const bool b_tma = vb || ((reinterpret_cast<uintptr_t>(B) & 15u) == 0 && K >= 4 && sB % 4 == 0 &&
                               !(flags & SGEMM_FLAG_B_ROWS_LOADED));
-    const int slots = (va && b_tma) ? pair_slots : 0;
+    // an unaligned A that run() stages into aligned rows comes by TMA too
+    const bool a_staged = !va && a_gets_staged(M, N, flags, batch, sA);
+    const int slots = ((va || a_staged) && b_tma) ? pair_slots : 0;
     if (path == SGEMM_ALGO_TF32X3) plan_tf32x3(M, N, K, sms, splits, flags, read_c, p, batch, slots);
     else plan_ffma(M, N, K, sms, splits, p);
     p.vec_a = va;
@@ -666,8 +676,7 @@ int run(int M, int N, int K, float alpha, const float *A, int lda, const float *
         // themselves with 80.  Measured: 64 x 1605632 x 147 from 74.7 to
         // 90.0 TF/s; at 1023 x 1021 x 1025 the copy cost more than it saved.
         // The two forms give the same bits.
-        if (p.path == SGEMM_ALGO_TF32X3 && !p.vec_a && !(flags & SGEMM_FLAG_NO_A_COPY) && (batch <= 1 || sA == 0) &&
-            static_cast<long long>(M) * 32 <= N) {
+        if (p.path == SGEMM_ALGO_TF32X3 && !p.vec_a && a_gets_staged(M, N, flags, batch, sA)) {
             const int K4 = (K + 3) / 4 * 4;
             float *apad = nullptr;
             rc = get_apad_ws(*d, stream, static_cast<size_t>(M) * K4 * sizeof(float), &apad);

@@ -230,6 +230,28 @@ def test_cta_pairs(case):
                                     f"{np.argwhere(diff)[:4].tolist()}")
 
 
+def test_cta_pairs_with_staged_a():
+    """An A whose rows are not 16-byte aligned but that is far smaller than
+    B is copied to aligned rows before the kernel; the planner counts it as
+    copied by TMA, so 256-row tiles can still run on CTA pairs."""
+    M, N, K = 256, 9000, 147
+    p = _with_c(random_problem(M, N, K, alpha=1.0, beta=0.5, seed=4242, pad_value=np.nan))
+    assert p.lda % 4 != 0
+    flags = pkg.SGEMM_FLAG_TILE_ROWS(256) | pkg.SGEMM_FLAG_PAIRS
+    plan = pkg.sgemm_plan_info(M, N, K, A=0, B=0, C=0, lda=p.lda, ldb=p.ldb, algo=pkg.SGEMM_ALGO_TF32X3,
+                               flags=flags, beta=p.beta)
+    assert plan["pairs"] == 1 and plan["vec_a"] == 0, plan
+    got, st = run_sgemm(p, pkg.SGEMM_ALGO_TF32X3, flags=flags)
+    assert st == 0
+    check_against_oracle(p, got, what="pairs with a staged A")
+    single, st = run_sgemm(p, pkg.SGEMM_ALGO_TF32X3, splits=1,
+                           flags=pkg.SGEMM_FLAG_TILE_ROWS(256) | pkg.SGEMM_FLAG_NO_PAIRS | pkg.SGEMM_FLAG_WHOLE_TILES)
+    assert st == 0
+    whole, st = run_sgemm(p, pkg.SGEMM_ALGO_TF32X3, splits=1, flags=flags | pkg.SGEMM_FLAG_WHOLE_TILES)
+    assert st == 0
+    assert np.array_equal(whole.view(np.uint32), single.view(np.uint32))
+
+
 def test_cta_pairs_repeatable():
     """The pair form under load, run after run: whole 256 x 256 tiles over
     more tiles than pairs (several per pair), eight launches back to back,
