@@ -35,6 +35,10 @@
 // Launched with programmatic stream serialization: barrier set-up and the
 // tensor-memory allocation may run while the previous kernel on the stream
 // finishes; griddepcontrol.wait comes before the first global access.
+// CTA pairs (PAIR): tiles of 256 columns are shared by the two CTAs of a
+// cluster through one cta_group::2 MMA per product and k slice (each CTA
+// keeps its 128 columns of B^T and of the accumulator and half the A rows);
+// the roles are the same, and the even CTA's MMA thread issues for both.
 //
 // Operand staging follows the shared-memory tiling, vector-load and
 // prefetch ideas of "NVIDIA_SGEMM_PRACTICE" (sections "kernel 2", "kernel 6",
