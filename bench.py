@@ -21,6 +21,10 @@ square5120: M=N=K=5120, alpha=1, beta=0.5, the size of the overview table of
   roofline  the GEMM kernel's 2MNK per launch / mean launch time (timed
             region over its steps) against the path's peak
   cpu_baseline  the float64 oracle on a bounded row sample, host cores
+  per_shape every benchmark workload on both paths and every convolution
+            layer, measured after the headline (value, roofline fraction,
+            L2 mode, clocks); on by default for the square5120 run on one
+            GPU, --no-per-shape leaves it out
 --impl reference times the oracle alone (the pages publish no GPU code to
 run here), same workload and metric.
 Multi-GPU (torchrun): independent replicas, one per GPU ("scaling": "weak").
@@ -851,6 +855,10 @@ def main():
     ap.add_argument("--no-cublas", dest="cublas", action="store_false")
     ap.add_argument("--shapes-out", default=None,
                     help="also measure every benchmark workload and write JSON lines here")
+    ap.add_argument("--per-shape", dest="per_shape", action="store_true", default=None,
+                    help="add a per_shape summary of every workload to the line (default: on for the "
+                         "default square5120 run on one GPU)")
+    ap.add_argument("--no-per-shape", dest="per_shape", action="store_false")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -880,8 +888,13 @@ def main():
         result["cpu_baseline"] = (conv_cpu_baseline if conv else cpu_baseline)(p, args.cpu_baseline_s)
     elif rank == 0:
         result["cpu_baseline"] = None
-    if rank == 0 and args.shapes_out:
-        measure_all(args, local_rank)
+    per_shape = args.per_shape
+    if per_shape is None:
+        per_shape = args.workload == "square5120" and args.trans == "NN" and args.algo == "auto"
+    if rank == 0 and world == 1 and (per_shape or args.shapes_out):
+        lines = measure_all(args, local_rank)
+        if per_shape:
+            result["per_shape"] = [shape_summary(r) for r in lines]
     if rank == 0:
         print(json.dumps(result), flush=True)
     if world > 1:
@@ -890,10 +903,31 @@ def main():
     return 0
 
 
-def measure_all(args, local_rank):
-    """Every benchmark workload on both paths, one JSON line each (to a file)."""
+def shape_summary(r: dict) -> dict:
+    """The figures of one per-shape line that the per_shape list carries."""
+    if "error" in r:
+        return r
+    rf = r["roofline"]
+    s = {"workload": r["config"]["workload"].split(":")[0], "algo": r["config"]["algo"],
+         "value": r["value"], "unit": r["unit"], "bound": rf["bound"], "frac": rf["frac"],
+         "launch_ms": rf["launch_ms"], "steps": r["steps"],
+         "l2": "flushed" if r["config"]["l2"].startswith("flushed") else "larger than L2",
+         "sm_mhz": (r.get("clocks") or {}).get("sm_mhz"), "reasons": (r.get("clocks") or {}).get("reasons")}
+    if "frac_of_mma_rate" in rf:
+        s["frac_of_mma_rate"] = rf["frac_of_mma_rate"]
+    if "context_cublas_sgemm_tflops" in r:
+        s["context_cublas_sgemm_tflops"] = r["context_cublas_sgemm_tflops"]
+    if "context_back_to_back_l2_resident" in r:
+        s["context_back_to_back_l2_resident"] = r["context_back_to_back_l2_resident"]["value"]
+    return s
+
+
+def measure_all(args, local_rank) -> list:
+    """Every benchmark workload on both paths and every convolution layer, one
+    result each; written as JSON lines to --shapes-out when given."""
     from dense_fp32_matrix_05_gb300.workloads import WORKLOADS
-    out = open(args.shapes_out, "w")
+    out = open(args.shapes_out, "w") if args.shapes_out else None
+    lines = []
     names = ["square256", "square1024", "ragged1023x1021x1025", "square5120"] + \
         [n for n in WORKLOADS if n.startswith("skinny")] + [n for n in WORKLOADS if n.startswith("sweep")]
     for name in names:
@@ -909,8 +943,10 @@ def measure_all(args, local_rank):
                 r, _ = run_ours(a, 0, 1, local_rank)
             except Exception as e:  # keep measuring the rest
                 r = {"workload": name, "algo": algo, "error": str(e)}
-            out.write(json.dumps(r) + "\n")
-            out.flush()
+            lines.append(r)
+            if out:
+                out.write(json.dumps(r) + "\n")
+                out.flush()
             log(f"{name} {algo}: {r.get('value')} TFLOP/s, roofline {r.get('roofline', {}).get('frac')}")
     from dense_fp32_matrix_05_gb300.workloads import CONV_LAYERS
     for name, layer in CONV_LAYERS.items():
@@ -922,10 +958,14 @@ def measure_all(args, local_rank):
             r, _ = run_conv_ours(a, 0, 1, local_rank)
         except Exception as e:  # keep measuring the rest
             r = {"workload": name, "algo": "auto", "error": str(e)}
-        out.write(json.dumps(r) + "\n")
-        out.flush()
+        lines.append(r)
+        if out:
+            out.write(json.dumps(r) + "\n")
+            out.flush()
         log(f"{name}: {r.get('value')} TFLOP/s, roofline {r.get('roofline', {}).get('frac')}")
-    out.close()
+    if out:
+        out.close()
+    return lines
 
 
 if __name__ == "__main__":

@@ -57,3 +57,21 @@ def test_each_kernel_family_has_its_own_hash():
     assert bench.kernel_family("ffma") == "ffma"
     hashes = {f: bench.kernel_source_hash(f) for f in bench.KERNEL_SOURCES}
     assert len(set(hashes.values())) == len(hashes)
+
+
+def test_per_shape_summary_keeps_the_figures_and_the_l2_mode():
+    gemm = {"config": {"workload": "square1024: M=1024 N=1024 K=1024 ...", "algo": "auto -> tf32x3",
+                       "l2": "flushed between steps (512 MB written, untimed; ...)"},
+            "value": 73.4, "unit": "TFLOP/s", "steps": 200,
+            "roofline": {"bound": "tensor", "frac": 0.23, "launch_ms": 0.0293, "frac_of_mma_rate": 0.18},
+            "clocks": {"sm_mhz": 2070.0, "reasons": []},
+            "context_cublas_sgemm_tflops": 49.3,
+            "context_back_to_back_l2_resident": {"value": 91.4}}
+    s = bench.shape_summary(gemm)
+    assert s["workload"] == "square1024" and s["l2"] == "flushed"
+    assert (s["value"], s["frac"], s["frac_of_mma_rate"]) == (73.4, 0.23, 0.18)
+    assert s["context_back_to_back_l2_resident"] == 91.4
+    big = dict(gemm, config=dict(gemm["config"], l2="no flush: inputs larger than L2 (419 MB vs 129 MB)"))
+    assert bench.shape_summary(big)["l2"] == "larger than L2"
+    err = {"workload": "square256", "algo": "auto", "error": "boom"}
+    assert bench.shape_summary(err) == err
