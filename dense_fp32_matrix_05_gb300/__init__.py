@@ -22,7 +22,7 @@ __all__ = [
     "SGEMM_FLAG_PAIRS", "SGEMM_FLAG_NO_PAIRS",
     "SGEMM_ERR_DEVICE_TIMEOUT",
     "SgemmError", "library", "lib_path", "declared_functions",
-    "sgemm", "sgemm_ex", "sgemm_host", "sgemm_plan_info", "sgemm_check_status",
+    "sgemm", "sgemm_ex", "sgemm_host", "sgemm_host_blocks", "sgemm_plan_info", "sgemm_check_status",
     "sgemm_status_string", "sgemm_release", "sgemm_version", "sgemm_noalloc", "sgemm_noalloc_debug_flags", "sgemm_tf32_mma_rate", "sgemm_ffma_rate", "sgemm_t", "sgemm_strided_batched", "sgemm_conv2d", "sgemm_conv2d_ex", "SGEMM_CONV_NO_PAD_COPY", "conv2d_out_size", "matmul",
     "SGEMM_ERR_SCRATCH_LIMIT", "SGEMM_ERR_OUT_OF_BOUNDS",
 ]
@@ -61,6 +61,8 @@ _SIGS = {
     "sgemm_host": (_i, [_i, _i, _i, _f, _p, _i, _p, _i, _f, _p, _i, _i]),
     "sgemm_plan_info": (_i, [_i, _i, _i, _p, _i, _p, _i, _p, _i, _i, _i, _i, _f, _f, _i,
                              ctypes.POINTER(ctypes.c_int), _i]),
+    "sgemm_host_blocks": (_i, [_i, _i, _i, _i, _i, _i, _f, _f, _i, _i, ctypes.POINTER(ctypes.c_int),
+                               ctypes.POINTER(ctypes.c_int), _i]),
     "sgemm_check_status": (_i, [_p]),
     "sgemm_status_string": (ctypes.c_char_p, [_i]),
     "sgemm_release": (_i, []),
@@ -196,6 +198,20 @@ def sgemm_host(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, algo=0) -> int:
 
 _PLAN_KEYS = ["path", "tile_m", "tile_n", "splits", "units", "grid", "stages", "vec_a", "vec_b",
               "ws_bytes", "tail_tiles", "wide", "pairs"]
+
+
+def sgemm_host_blocks(M, N, K, lda=None, ldb=None, ldc=None, alpha=1.0, beta=0.0, algo=0, num_sms=0):
+    """(axis, sizes): how sgemm_host cuts the call (axis 0: row blocks of C,
+    1: column blocks; one size = one GEMM)."""
+    lda = max(1, K) if lda is None else lda
+    ldb = max(1, N) if ldb is None else ldb
+    ldc = max(1, N) if ldc is None else ldc
+    axis = ctypes.c_int(0)
+    buf = (ctypes.c_int * 16)()
+    n = library().sgemm_host_blocks(M, N, K, lda, ldb, ldc, alpha, beta, algo, num_sms, ctypes.byref(axis), buf, 16)
+    if n < 0:
+        raise SgemmError("sgemm_host_blocks", n)
+    return axis.value, list(buf)[:n]
 
 
 def sgemm_plan_info(M, N, K, A=0, lda=None, B=0, ldb=None, C=0, ldc=None, algo=0, splits=0,

@@ -1040,6 +1040,123 @@ int run_conv(int nb, int C, int H, int W, int F, int KH, int KW, int sh, int sw,
     return 0;
 }
 
+// ------------------------------------------------- host-buffer pipeline
+
+// Assumed host <-> device copy rate of pinned memory, each direction, and
+// the gap between a block's rows landing and its GEMM starting.  They only
+// shape the choice of block sizes below; every block is an ordinary planned
+// GEMM, so the result does not depend on them.
+constexpr double kHostLinkGBs = 200.0;
+constexpr double kHostGemmGapUs = 8.0;
+constexpr int kHostRowQuantum = 128;
+
+// The planner's run-time estimate (us) of a 3xTF32 call: the single-CTA
+// choice, or the CTA-pair form where the planner would take it.
+double model_tf32x3_us(int M, int N, int K, int sms, int pair_slots, bool read_c) {
+    const Tf32x3Choice ch = choose_tf32x3(M, N, K, sms, 0, 0, 0, read_c);
+    if (use_pairs(M, N, K, ch, 0, pair_slots, read_c, 1)) {
+        bool tail = false;
+        return model_pairs(M, N, K, ch.tm, pair_slots, read_c, 1, 0, &tail);
+    }
+    return ch.us;
+}
+
+// Row blocks of a pipelined 3xTF32 call, chosen by simulating its timeline:
+// B goes up first, then each block's rows of A (and of C when beta != 0);
+// a block's GEMM starts once its rows have landed and the previous GEMM is
+// done (its time from the planner's model); its rows of C go down after
+// it, one block after another.  The call ends with the last download.
+// Candidates: a first block of 1..8 quanta (the GEMMs start early), a last
+// block of 1..4 quanta (little work after the last upload), and 1..10
+// equal middle blocks, plus the fixed policy of host_blocks.  Returns the
+// count.
+int host_row_blocks_tf32x3(int M, int N, int K, int lda, int ldb, int ldc, bool use_ab, bool read_c, int sms,
+                           int pair_slots, int sizes[kHostMaxBlocks]) {
+    constexpr int q = kHostRowQuantum;
+    // the pair form needs operands that come by TMA (as make_plan decides
+    // for the library's own, 256-byte aligned device buffers)
+    const bool va = lda % 4 == 0, b_tma = ldb % 4 == 0 || K >= 4;
+    std::map<int, double> gemm_us;
+    auto gemm = [&](int rows) {
+        auto it = gemm_us.find(rows);
+        if (it != gemm_us.end()) return it->second;
+        const bool a_tma = va || a_gets_staged(rows, N, 0, 1, 0);
+        const double us = model_tf32x3_us(rows, N, K, sms, (a_tma && b_tma) ? pair_slots : 0, read_c);
+        gemm_us.emplace(rows, us);
+        return us;
+    };
+    const double bytes_per_us = kHostLinkGBs * 1e3;
+    auto simulate = [&](const int *sz, int n) {
+        double up = use_ab ? static_cast<double>(span_bytes(K, N, ldb)) / bytes_per_us : 0.0;
+        double g_end = 0.0, d_end = 0.0;
+        for (int i = 0; i < n; ++i) {
+            double in = use_ab ? static_cast<double>(span_bytes(sz[i], K, lda)) : 0.0;
+            const double c = static_cast<double>(span_bytes(sz[i], N, ldc));
+            if (read_c) in += c;
+            up += in / bytes_per_us;
+            g_end = std::max(up, g_end) + kHostGemmGapUs + gemm(sz[i]);
+            d_end = std::max(g_end, d_end) + c / bytes_per_us;
+        }
+        return d_end;
+    };
+    int n_best = host_blocks(M, q, sizes);
+    double t_best = simulate(sizes, n_best);
+    int cand[kHostMaxBlocks];
+    const int r = M % q;
+    for (int f = q; f <= 8 * q; f += q) {
+        for (int l = q; l <= 4 * q; l += q) {
+            const int mid = M - f - (l + r);
+            if (mid < 0 || f > M / 3) continue;
+            for (int nm = (mid > 0 ? 1 : 0); nm <= kHostMaxBlocks - 2 && nm <= mid / q; ++nm) {
+                int n = 0;
+                cand[n++] = f;
+                if (nm > 0) {
+                    const int base = mid / q / nm * q;
+                    int extra = (mid - base * nm) / q;
+                    for (int i = 0; i < nm; ++i, --extra) cand[n++] = base + (extra > 0 ? q : 0);
+                }
+                cand[n++] = l + r;
+                const double t = simulate(cand, n);
+                if (t < t_best) {
+                    t_best = t;
+                    n_best = n;
+                    std::copy(cand, cand + n, sizes);
+                }
+                if (mid == 0) break;
+            }
+        }
+    }
+    return n_best;
+}
+
+// How sgemm_host cuts a call: returns the block count (1: one GEMM) and
+// sets *axis (0: row blocks of C, 1: column blocks).  From 64 MB of traffic
+// up, calls of 512 rows or more run as row blocks (3xTF32: chosen by
+// host_row_blocks_tf32x3; FFMA: host_blocks), shorter ones of at least
+// 8192 columns as column blocks of 1024-column multiples.
+int host_split(int M, int N, int K, int lda, int ldb, int ldc, float alpha, float beta, int algo, int sms,
+               int pair_slots, int *axis, int sizes[kHostMaxBlocks]) {
+    *axis = 0;
+    sizes[0] = M;
+    const bool use_ab = alpha != 0.f && K > 0;
+    const bool read_c = beta != 0.f;
+    const size_t a_bytes = use_ab ? span_bytes(M, K, lda) : 0;
+    const size_t b_bytes = use_ab ? span_bytes(K, N, ldb) : 0;
+    const size_t c_bytes = span_bytes(M, N, ldc);
+    const size_t in_bytes = a_bytes + b_bytes + (read_c ? c_bytes : 0);
+    if (in_bytes + c_bytes < (64u << 20)) return 1;
+    if (M >= 512) {
+        if (resolve_path(kHostRowQuantum, K, algo, 0) == SGEMM_ALGO_TF32X3)
+            return host_row_blocks_tf32x3(M, N, K, lda, ldb, ldc, use_ab, read_c, sms, pair_slots, sizes);
+        return host_blocks(M, kHostRowQuantum, sizes);
+    }
+    if (N >= 8192) {
+        *axis = 1;
+        return host_blocks(N, 1024, sizes);
+    }
+    return 1;
+}
+
 }  // namespace
 
 extern "C" {
@@ -1107,14 +1224,14 @@ int sgemm_host(int M, int N, int K, float alpha, const float *A, int lda, const 
     // its rows of C come back on the download stream while the next blocks
     // compute.  Each block is a planned GEMM of its own (the same arithmetic
     // per element; a block's schedule may differ from the whole call's).
-    const size_t in_bytes = a_bytes + b_bytes + (beta != 0.f ? c_bytes : 0);
-    const bool large = in_bytes + c_bytes >= (64u << 20);
     int sizes[kHostMaxBlocks];
+    int axis = 0;
     // row blocks; short and wide (the im2col shapes): column blocks instead,
     // A goes up first and each block's columns of B (and C) move as pitched
     // copies
-    const int nblk = (large && M >= 512) ? host_blocks(M, 128, sizes) : 1;
-    const int ncb = (nblk == 1 && large && N >= 8192) ? host_blocks(N, 1024, sizes) : 1;
+    const int nb = host_split(M, N, K, lda, ldb, ldc, alpha, beta, algo, d->sms, d->pair_slots, &axis, sizes);
+    const int nblk = axis == 0 ? nb : 1;
+    const int ncb = axis == 1 ? nb : 1;
     if (ncb > 1) {
         float *dA = h.A, *dB = h.B, *dC = h.C;
         cudaStream_t st = h.stream, up = h.up, down = h.down;
@@ -1267,6 +1384,37 @@ int sgemm_plan_info(int M, int N, int K, const void *A, int lda, const void *B, 
     }
     for (int i = 0; i < ninfo && i < 13; ++i) info[i] = vals[i];
     return 0;
+}
+
+int sgemm_host_blocks(int M, int N, int K, int lda, int ldb, int ldc, float alpha, float beta, int algo,
+                      int num_sms, int *axis, int *sizes, int max_sizes) {
+    if (M < 0) return -1;
+    if (N < 0) return -2;
+    if (K < 0) return -3;
+    if (lda < std::max(1, K)) return -4;
+    if (ldb < std::max(1, N)) return -5;
+    if (ldc < std::max(1, N)) return -6;
+    if (algo < SGEMM_ALGO_AUTO || algo > SGEMM_ALGO_TF32X3) return -9;
+    if (num_sms < 0) return -10;
+    if (axis == nullptr) return -11;
+    if (sizes == nullptr && max_sizes > 0) return -12;
+    if (max_sizes < 0) return -13;
+    int sms = num_sms, pair_slots = num_sms / 2;
+    if (sms == 0) {
+        std::lock_guard<std::mutex> lk(g_mu);
+        DevState *d = nullptr;
+        int rc = device_state(&d);
+        if (rc != 0) return rc;
+        sms = d->sms;
+        pair_slots = d->pair_slots;
+    }
+    int sz[kHostMaxBlocks];
+    int n = 1;
+    *axis = 0;
+    if (M > 0 && N > 0) n = host_split(M, N, K, lda, ldb, ldc, alpha, beta, algo, sms, pair_slots, axis, sz);
+    else sz[0] = M;
+    for (int i = 0; i < n && i < max_sizes; ++i) sizes[i] = sz[i];
+    return n;
 }
 
 int sgemm_check_status(sgemm_stream_t stream) {

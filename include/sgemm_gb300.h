@@ -177,11 +177,15 @@ int sgemm_ex(int M, int N, int K, float alpha,
  * lets the copies overlap the GEMMs).  The call copies A, B (and C when
  * beta != 0) to library-owned device buffers on the current device, runs
  * the GEMM, copies C back and waits for completion.  From 64 MB of traffic
- * and 512 rows up it runs as 2..8 row blocks of C (256-row multiples): B goes up
- * first, each block's rows of A (and C) follow on an upload stream, a
- * block's GEMM starts once its rows have landed, and its rows of C return
- * on a download stream while later blocks compute.  A call with fewer rows
- * and at least 8192 columns runs as 2..8 column blocks (128-column
+ * and 512 rows up it runs as up to 12 row blocks of C (128-row multiples,
+ * the last one taking any remainder): B goes up first, each block's rows of
+ * A (and C) follow on an upload stream, a block's GEMM starts once its rows
+ * have landed, and its rows of C return on a download stream while later
+ * blocks compute.  On the 3xTF32 path the block sizes come from simulating
+ * that timeline with the planner's run-time model of each block's GEMM (a
+ * small first block so the GEMMs start early, a small last one, equal
+ * blocks between); sgemm_host_blocks reports them.  A call with fewer rows
+ * and at least 8192 columns runs as up to 12 column blocks (1024-column
  * multiples) the same way, with A first and pitched copies of the blocks'
  * columns of B and C.  Each block is a planned
  * GEMM of its own, so the schedule, and with it the rounding of each
@@ -195,6 +199,22 @@ int sgemm_host(int M, int N, int K, float alpha,
                const float *A, int lda,
                const float *B, int ldb,
                float beta, float *C, int ldc, int algo);
+
+/*
+ * sgemm_host_blocks - how sgemm_host would cut a call into blocks, without
+ * running it.
+ *
+ * Host-only: makes no CUDA call when num_sms > 0 (num_sms = 0 queries the
+ * current device; the pair form is then sized for num_sms / 2 CTA pairs).
+ * M, N, K, lda, ldb, ldc, alpha, beta, algo as in sgemm_host (no buffers).
+ * Sets *axis to 0 for row blocks of C or 1 for column blocks, writes up to
+ * max_sizes block sizes (rows, or columns) in call order to sizes, and
+ * returns the block count: 1 when the call runs as one GEMM (sizes[0] is
+ * then M).  Returns -i for an invalid argument (the i-th argument of this
+ * function, 1-based), or a negative sgemm error code from the device query.
+ */
+int sgemm_host_blocks(int M, int N, int K, int lda, int ldb, int ldc, float alpha, float beta, int algo,
+                      int num_sms, int *axis, int *sizes, int max_sizes);
 
 /*
  * sgemm_plan_info - what the planner would launch, without launching.

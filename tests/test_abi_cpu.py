@@ -494,3 +494,30 @@ def test_ffma_plans_cover_every_k_tile_once(sms):
         else:
             assert p["grid"] == p["units"] == tiles * p["splits"]
             assert p["ws_bytes"] == (p["units"] * p["tile_m"] * p["tile_n"] * 4 if p["splits"] > 1 else 0)
+
+
+def test_host_blocks_pipeline_policy():
+    """sgemm_host's blocks: one GEMM below 64 MB; row blocks of 128-row
+    multiples (the last one takes the remainder) that cover M, at most 12;
+    column blocks for short, wide calls.  On the 3xTF32 path the timeline
+    simulation with the planner's model picks, for 5120^3 with beta != 0 on
+    152 SMs, a 256-row first block, six of 768 rows (60 CTA-pair tiles: one
+    wave on 76 pairs) and a 256-row last block; the FFMA path keeps the
+    fixed policy."""
+    assert pkg.sgemm_host_blocks(1000, 1000, 1000, num_sms=152) == (0, [1000])
+    assert pkg.sgemm_host_blocks(5120, 5120, 5120, beta=0.5, num_sms=152) == (0, [256] + [768] * 6 + [256])
+    assert pkg.sgemm_host_blocks(5120, 5120, 5120, beta=0.5, algo=pkg.SGEMM_ALGO_FFMA, num_sms=152) == \
+        (0, [1024, 1024, 1024, 1024, 512, 256, 256])
+    for M, N, K, beta in [(2000, 3000, 2500, -0.75), (8192, 8192, 8192, 0.0), (4097, 5000, 3000, 1.0),
+                          (16384, 16384, 16384, 0.0), (100000, 1024, 1024, 0.0), (600, 20000, 512, 0.0),
+                          (513, 40000, 1024, 0.5)]:
+        for algo in (pkg.SGEMM_ALGO_AUTO, pkg.SGEMM_ALGO_FFMA):
+            axis, sizes = pkg.sgemm_host_blocks(M, N, K, beta=beta, algo=algo, num_sms=152)
+            assert axis == 0 and 1 < len(sizes) <= 12 and sum(sizes) == M, (M, N, K, algo, sizes)
+            assert all(s % 128 == 0 and s > 0 for s in sizes[:-1]) and sizes[-1] > 0, sizes
+    axis, sizes = pkg.sgemm_host_blocks(200, 40000, 700, ldb=40008, ldc=40012, beta=0.5, num_sms=152)
+    assert axis == 1 and sum(sizes) == 40000 and len(sizes) <= 12
+    assert all(s % 1024 == 0 for s in sizes[:-1])
+    assert pkg.library().sgemm_host_blocks(-1, 5, 5, 5, 5, 5, 1.0, 0.0, 0, 152, None, None, 0) == -1
+    with pytest.raises(pkg.SgemmError):
+        pkg.sgemm_host_blocks(10, 10, 10, lda=5, num_sms=152)

@@ -546,14 +546,17 @@ def test_host_entry_point(algo):
 @pytest.mark.parametrize("algo", [pkg.SGEMM_ALGO_AUTO, pkg.SGEMM_ALGO_FFMA], ids=["auto", "ffma"])
 def test_host_entry_point_pipelined(algo):
     """A call over 64 MB runs as row blocks whose copies overlap the GEMMs
-    (here 2 blocks of 1024 and 976 rows, padded leading dimensions): rows
-    on both sides of the block boundary against the oracle, pinned and
+    (padded leading dimensions; the blocks sgemm_host_blocks reports): rows
+    on both sides of every block boundary against the oracle, pinned and
     pageable host buffers."""
     import torch
     M, N, K = 2000, 3000, 2500
     p = _with_c(random_problem(M, N, K, alpha=0.5, beta=-0.75, seed=19, lda=K + 4, ldb=N + 8, ldc=N + 4,
                                pad_value=0.0))
-    rows = sorted(set(sample_rows(M, 48, seed=3)) | {1022, 1023, 1024, 1025, M - 1})
+    axis, sizes = pkg.sgemm_host_blocks(M, N, K, p.lda, p.ldb, p.ldc, p.alpha, p.beta, algo)
+    assert axis == 0 and len(sizes) > 1 and sum(sizes) == M
+    edges = np.cumsum(sizes)[:-1]
+    rows = sorted(set(sample_rows(M, 48, seed=3)) | {int(e) + d for e in edges for d in (-1, 0)} | {M - 1})
     A = torch.from_numpy(p.A).pin_memory()
     B = torch.from_numpy(p.B).pin_memory()
     C = torch.from_numpy(p.C.copy()).pin_memory()
