@@ -316,6 +316,17 @@ def job_throughput(world: int, flops_per_step: float, steps: int, job_ms: float)
     return world * flops_per_step * steps / (job_ms * 1e-3) / 1e12
 
 
+def pipeline_bound(copy: dict, prefix_bytes: float, gemm_ms: float, step_ms: float) -> dict:
+    """Floor of one pipelined host-buffer call: the smaller of A and B goes
+    up whole before the first block's GEMM can start (sgemm_host's row
+    blocks send B first, its column blocks A), after which the other copies
+    can overlap the GEMMs; and never less than the copy floor."""
+    prefix_ms = prefix_bytes / (copy["h2d_gbs"] * 1e9) * 1e3
+    bound = max(copy["copy_bound_ms"], prefix_ms + gemm_ms)
+    return {"pipeline_bound_ms": round(bound, 4), "frac_of_pipeline_bound": round(bound / step_ms, 4),
+            "pipeline_note": "max(copy floor, upload of the smaller of A and B + the GEMM's device time)"}
+
+
 def roofline_peak(path: int, peaks: dict, source: str, sms: int):
     """(bound, peak TFLOP/s, basis text) for a path."""
     import dense_fp32_matrix_05_gb300 as pkg
@@ -451,10 +462,13 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     torch.cuda.synchronize()
     if dist:
         torch.distributed.barrier()
+    step_s = []
     h0 = time.perf_counter()
     for _ in range(e2e_steps):
         host_step()
-    e2e_s = time.perf_counter() - h0
+        step_s.append(time.perf_counter())
+    e2e_s = step_s[-1] - h0
+    step_s = np.diff([h0] + step_s)
     if dist:
         t = torch.tensor([e2e_s], device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
@@ -542,9 +556,12 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                 "api": "sgemm_host (pinned host buffers)",
                 "ms_per_step": round(e2e_s * 1e3 / e2e_steps, 4),
+                "ms_per_step_median": round(float(np.median(step_s)) * 1e3, 4),
+                "ms_per_step_max": round(float(np.max(step_s)) * 1e3, 4),
                 "copy_bound_ms": copy["copy_bound_ms"],
                 "frac_of_copy_bound": round(copy["copy_bound_ms"] / (e2e_s * 1e3 / e2e_steps), 4),
                 "frac_of_concurrent_copies": round(copy["both_ms"] / (e2e_s * 1e3 / e2e_steps), 4),
+                **pipeline_bound(copy, 4 * min(p.A.size, p.B.size), launch_ms, e2e_s * 1e3 / e2e_steps),
                 "copies": copy},
         "gpu_launches": args.steps * (1 + int(ta) + int(tb)),
         "clocks": clocks,
@@ -659,10 +676,13 @@ def run_conv_ours(args, rank: int, world: int, local_rank: int):
         host_step()
     if dist:
         torch.distributed.barrier()
+    step_s = []
     h0 = time.perf_counter()
     for _ in range(e2e_steps):
         host_step()
-    e2e_s = time.perf_counter() - h0
+        step_s.append(time.perf_counter())
+    e2e_s = step_s[-1] - h0
+    step_s = np.diff([h0] + step_s)
     if dist:
         t = torch.tensor([e2e_s], device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
@@ -703,7 +723,10 @@ def run_conv_ours(args, rank: int, world: int, local_rank: int):
                                                    (peaks["hbm_gbs"] * 1e9), 4)},
         "e2e": {"value": round(world * flops * e2e_steps / e2e_s / 1e12, 3), "unit": UNIT,
                 "h2d_bytes_per_step": int(Xh.nbytes + Wh.nbytes), "d2h_bytes_per_step": int(4 * Y.numel()),
-                "steps": e2e_steps, "api": "sgemm_conv2d with pinned host copies in and out"},
+                "steps": e2e_steps, "api": "sgemm_conv2d with pinned host copies in and out",
+                "ms_per_step": round(e2e_s * 1e3 / e2e_steps, 4),
+                "ms_per_step_median": round(float(np.median(step_s)) * 1e3, 4),
+                "ms_per_step_max": round(float(np.max(step_s)) * 1e3, 4)},
         "gpu_launches": args.steps * launches,
         "clocks": clocks,
     }
@@ -919,6 +942,12 @@ def shape_summary(r: dict) -> dict:
         s["context_cublas_sgemm_tflops"] = r["context_cublas_sgemm_tflops"]
     if "context_back_to_back_l2_resident" in r:
         s["context_back_to_back_l2_resident"] = r["context_back_to_back_l2_resident"]["value"]
+    e = r.get("e2e") or {}
+    if "value" in e:
+        s["e2e"] = e["value"]
+        for k in ("frac_of_copy_bound", "frac_of_pipeline_bound"):
+            if e.get(k) is not None:
+                s["e2e_" + k] = e[k]
     return s
 
 
@@ -937,7 +966,7 @@ def measure_all(args, local_rank) -> list:
             w = WORKLOADS[name]
             a.steps = max(5, min(200, int(2e12 / max(w.flops, 1.0))))
             a.warmup = 3
-            a.e2e_steps = 3
+            a.e2e_steps = 10
             a.cublas = True
             try:
                 r, _ = run_ours(a, 0, 1, local_rank)
@@ -953,7 +982,7 @@ def measure_all(args, local_rank) -> list:
         a = argparse.Namespace(**vars(args))
         a.workload, a.algo = name, "auto"
         a.steps = max(5, min(200, int(2e12 / layer.flops)))
-        a.warmup, a.e2e_steps = 3, 3
+        a.warmup, a.e2e_steps = 3, 10
         try:
             r, _ = run_conv_ours(a, 0, 1, local_rank)
         except Exception as e:  # keep measuring the rest

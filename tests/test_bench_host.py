@@ -75,3 +75,13 @@ def test_per_shape_summary_keeps_the_figures_and_the_l2_mode():
     assert bench.shape_summary(big)["l2"] == "larger than L2"
     err = {"workload": "square256", "algo": "auto", "error": "boom"}
     assert bench.shape_summary(err) == err
+
+
+def test_pipeline_bound_is_the_larger_of_the_copy_floor_and_prefix_plus_gemm():
+    copy = {"h2d_gbs": 200.0, "copy_bound_ms": 1.5}
+    # link-bound: 100 MB prefix (0.5 ms) + 0.8 ms GEMM is under the 1.5 ms copy floor
+    b = bench.pipeline_bound(copy, 100e6, 0.8, 1.875)
+    assert b["pipeline_bound_ms"] == 1.5 and b["frac_of_pipeline_bound"] == 0.8
+    # GEMM-bound: 0.5 ms prefix + 24 ms GEMM
+    b = bench.pipeline_bound(copy, 100e6, 24.0, 30.625)
+    assert b["pipeline_bound_ms"] == 24.5 and b["frac_of_pipeline_bound"] == 0.8
